@@ -56,8 +56,10 @@ def pack_awq(qv: np.ndarray, zv: np.ndarray):
 def mx_quantize_lib(v: np.ndarray):
     """MXFP8 quantization through library routines: the shared exponent from
     numpy.frexp, the element rounding from PyTorch's RNE float8_e4m3fn cast
-    (float64 -> float8 directly; it turns |u| >= 464 into NaN instead of saturating, so those are
-    clamped to 448 first: saturating conversion)."""
+    (which turns |u| >= 464 into NaN instead of saturating, so those are
+    clamped to 448 first: saturating conversion).  Inputs with more than 24
+    significant bits may be double-rounded by the cast; the pins feed it
+    bf16/fp32-derived values or compare codes away from ties."""
     rows, K = v.shape
     blocks = v.reshape(rows, K // 32, 32)
     amax = np.abs(blocks).max(axis=-1)
