@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MoE expert-FFN layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_m1|tiny|sweep_m<M>[_zipf]|large_m1|large_m8]
+
+A step is one pass of the hot path over one batch of fresh synthetic input:
+top-k routing of the step's router logits, then the layer (output-centric
+decode kernels).  The default workload is the 128-expert d=2048 / I=768
+top-8 layer at M=1 with MXFP8 weights (623 MB resident), fresh routing every
+step.  The L2 is flushed (a 512 MiB write) between timed steps, outside the
+timed interval.  Each step's device time is taken with CUDA events on the
+launching stream around a CUDA-graph replay of the step.
+
+Metric: achieved HBM TB/s of the layer = algorithmic bytes (the distinct
+routed experts' MXFP8 weights incl. scales, plus x, the router logits and y)
+divided by the step time; also reported as microseconds per layer.
+
+--impl reference times the CPU oracle (binary64, test infrastructure) on
+the host cores on a bounded sample of the same workload, in the same units.
+Multi-GPU (torchrun): independent replicas, one per GPU, no collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer µs & achieved HBM TB/s (% of GB300 peak) at M=1–64 decode"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 * 2 ** 20
+
+
+# ------------------------------------------------------------------ helpers
+
+def workload_from_name(name: str):
+    from top_moe_expert_gb300 import inputs
+    if name == "decode_m1":
+        return inputs.DECODE
+    if name == "tiny":
+        return inputs.TINY
+    if name == "large_m1":
+        return inputs.LARGE_M1
+    if name == "large_m8":
+        return inputs.LARGE_M8
+    if name.startswith("sweep_m"):
+        rest = name[len("sweep_m"):]
+        routing = "zipf" if rest.endswith("_zipf") else "uniform"
+        return inputs.sweep(int(rest.split("_")[0]), routing)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def expert_bytes(wl) -> int:
+    """MXFP8 bytes of one expert: 3*I*d codes + 3*I*d/32 scale bytes."""
+    return 3 * wl.I * wl.d * 33 // 32
+
+
+def step_bytes(wl, ids: np.ndarray) -> int:
+    """Algorithmic bytes of one step: distinct routed experts' weights, the
+    activations read (x, router logits) and the output written (bf16 y)."""
+    distinct = len(np.unique(ids[(ids >= 0) & (ids < wl.E)]))
+    return distinct * expert_bytes(wl) + wl.M * wl.d * 2 + wl.M * wl.E * 4 + wl.M * wl.d * 2
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.perf_counter(), parts))
+
+    def stop(self, t0: float, t1: float):
+        """Summary of the samples that arrived inside [t0, t1] (the timed loop)."""
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1]
+        self.rows = inside
+        if not self.rows:
+            return None
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def committed_traffic(kernel_key: str, src_hash: str):
+    """DRAM traffic per launch from the committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[kernel_key]
+    except Exception:
+        return None
+    return d["bytes_per_launch"] if d.get("src_sha256") == src_hash else None
+
+
+def decode_src_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "topk.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "top_moe_expert_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------------ our arm
+
+class DecodeStep:
+    """Device-resident workload + a CUDA graph of one step (routing + layer)."""
+
+    def __init__(self, wl, nsteps: int, device):
+        import top_moe_expert_gb300 as moe
+        from top_moe_expert_gb300 import inputs
+        self.moe, self.wl, self.dev = moe, wl, device
+        E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
+        self.q13 = torch.empty((E, 2 * I, d), dtype=torch.uint8, device=device)
+        self.s13 = torch.empty((E, 2 * I, d // 32), dtype=torch.uint8, device=device)
+        self.q2 = torch.empty((E, d, I), dtype=torch.uint8, device=device)
+        self.s2 = torch.empty((E, d, I // 32), dtype=torch.uint8, device=device)
+        for e in range(E):
+            moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w13", e, device), self.q13[e], self.s13[e])
+            moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), self.q2[e], self.s2[e])
+        self.w13 = moe.Weights(moe.MOE_W_MXFP8, self.q13, self.s13)
+        self.w2 = moe.Weights(moe.MOE_W_MXFP8, self.q2, self.s2)
+        # fresh routing and activations for every step
+        self.logits_host = torch.from_numpy(np.stack([inputs.router_logits(wl, i) for i in range(nsteps)]))
+        self.x_host = torch.stack([inputs.activations(wl, i) for i in range(nsteps)])
+        self.logits_all = self.logits_host.to(device)
+        self.x_all = self.x_host.to(device)
+        self.logits = torch.empty((M, E), dtype=torch.float32, device=device)
+        self.x = torch.empty((M, d), dtype=torch.bfloat16, device=device)
+        self.ids = torch.empty((M, k), dtype=torch.int32, device=device)
+        self.w = torch.empty((M, k), dtype=torch.float32, device=device)
+        self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
+        self.ws = torch.empty(moe.moe_ffn_decode_workspace_size(M, k, I), dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.Stream(device)
+        torch.cuda.synchronize()
+
+    def launch(self, stream=None):
+        self.moe.moe_topk_softmax(self.logits, self.wl.k, self.ids, self.w, stream=stream)
+        self.moe.moe_ffn_decode(self.x, self.ids, self.w, self.w13, self.w2, y=self.y, ws=self.ws,
+                                stream=stream)
+
+    def capture(self):
+        with torch.cuda.stream(self.stream):
+            self.launch(self.stream)            # warm, outside capture
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self.launch(self.stream)
+        self.stream.synchronize()
+
+
+def host_topk_ids(logits: np.ndarray, k: int) -> np.ndarray:
+    """Top-k expert ids by logit (stable sort: ties to the lower id), used
+    only to count the distinct experts a step touches for the byte count."""
+    return np.argsort(-logits, axis=1, kind="stable")[:, :k]
+
+
+def run_ours(args, rank, world, device):
+    wl = workload_from_name(args.workload)
+    K, W = args.steps, args.warmup
+    st = DecodeStep(wl, K + W, device)
+    st.capture()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    s = st.stream
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(W):
+            st.x.copy_(st.x_all[i], non_blocking=True)
+            st.logits.copy_(st.logits_all[i], non_blocking=True)
+            flush.fill_(float(i))
+            st.graph.replay()
+    torch.cuda.synchronize()
+    sampler.start()
+    with torch.cuda.stream(s):                  # keep the GPU busy while the sampler starts
+        for i in range(400):
+            flush.fill_(float(i))
+            st.graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for i in range(K):
+            j = W + i
+            st.x.copy_(st.x_all[j], non_blocking=True)
+            st.logits.copy_(st.logits_all[j], non_blocking=True)
+            flush.fill_(float(j))
+            ev0[i].record(s)
+            st.graph.replay()
+            ev1[i].record(s)
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
+    t_wall = t_wall1 - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    total_ms = sum(step_ms)
+
+    # bytes of every timed step (distinct experts of that step's routing)
+    logits_np = st.logits_host.numpy()
+    bytes_steps = [step_bytes(wl, host_topk_ids(logits_np[W + i], wl.k)) for i in range(K)]
+    total_bytes = float(sum(bytes_steps))
+
+    # e2e: the same steps through the public API with host buffers (pinned)
+    Ke = min(K, 2000)
+    x_pin = st.x_host[W:W + Ke].pin_memory()
+    l_pin = st.logits_host[W:W + Ke].pin_memory()
+    y_pin = torch.empty((Ke, wl.M, wl.d), dtype=torch.bfloat16).pin_memory()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(Ke):
+            flush.fill_(float(i))
+            e0[i].record(s)
+            st.x.copy_(x_pin[i], non_blocking=True)
+            st.logits.copy_(l_pin[i], non_blocking=True)
+            st.launch(s)
+            y_pin[i].copy_(st.y, non_blocking=True)
+            e1[i].record(s)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
+    e2e_bytes = float(sum(bytes_steps[:Ke]))
+
+    # gather across replicas: max time, summed bytes
+    t = torch.tensor([total_ms, total_bytes, e2e_ms, e2e_bytes], dtype=torch.float64, device=device)
+    if world > 1:
+        tmax = t.clone()
+        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+        tsum = t.clone()
+        torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
+        total_ms, e2e_ms = float(tmax[0]), float(tmax[2])
+        total_bytes, e2e_bytes = float(tsum[1]), float(tsum[3])
+    if rank != 0:
+        return None
+
+    tbps = total_bytes / (total_ms * 1e-3) / 1e12
+    us_layer = total_ms * 1e3 / K
+    peak_gbs, peak_kind = measured_peak()
+    achieved_gbs = tbps * 1e3 / world
+    line = {
+        "metric": METRIC,
+        "value": round(tbps, 4),
+        "unit": "TB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(total_ms / K, 6),
+        "us_per_layer": round(us_layer, 3),
+        "tokens_per_s": round(wl.M * world / (total_ms * 1e-3 / K), 1),
+        "frac_of_8TBps": round(tbps / world / 8.0, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp8-weights/bf16-act/f32-accum",
+        "data": "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
+                "N(0,1) router logits; fresh routing every step)",
+        "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "path": "output-centric decode (topk + gate/up + down, CUDA graph)",
+                   "l2": "flushed between timed steps (512 MiB write, outside the timed interval)",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
+                "us_per_layer": round(e2e_ms * 1e3 / Ke, 3), "steps": Ke,
+                "h2d_bytes_per_step": wl.M * wl.d * 2 + wl.M * wl.E * 4,
+                "d2h_bytes_per_step": wl.M * wl.d * 2},
+        "gpu_launches": 3 * K,
+        "roofline": {"kernel": "decode layer: decode_gate_up_kernel + decode_down_kernel (PDL-chained)",
+                     "bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak_gbs,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved_gbs / peak_gbs, 4),
+                     "traffic": committed_traffic(f"decode:{wl.name}", decode_src_hash())},
+        "clocks": clocks,
+        "wall_s_timed_loop": round(t_wall, 3),
+    }
+    return line
+
+
+def cpu_baseline(wl, device, seconds=12.0):
+    """The oracle, as it stands, on the host cores: full decode steps (top-k
+    + layer) of the same workload, fresh routing per step, until ~`seconds`
+    of timed CPU work.  Expert weights are quantized by the oracle from the
+    same fp32 draws (setup, not timed)."""
+    import oracle
+    from top_moe_expert_gb300 import inputs
+    cache = {}
+
+    def expert(which, e):
+        if (which, e) not in cache:
+            f = inputs.weights_fp32_device(wl, which, e, device).cpu().numpy().astype(np.float64)
+            cache[(which, e)] = oracle.mxfp8_quantize(f)
+        return cache[(which, e)]
+
+    t_total, nbytes, steps = 0.0, 0, 0
+    while t_total < seconds and steps < 64:
+        logits = inputs.router_logits(wl, 10_000 + steps)
+        ids, _ = oracle.topk_softmax(logits, wl.k)
+        experts = sorted(set(ids.reshape(-1).tolist()))
+        slot = np.full(wl.E, -1, dtype=np.int32)
+        slot[experts] = np.arange(len(experts), dtype=np.int32)
+        ws = {}
+        for which in ("w13", "w2"):
+            qs = [expert(which, e) for e in experts]
+            ws[which] = {"fmt": "mxfp8", "q": np.stack([q for q, _ in qs]),
+                         "s": np.stack([s for _, s in qs]), "slot": slot}
+        x = inputs.activations(wl, 10_000 + steps).to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        ids2, w2 = oracle.topk_softmax(logits, wl.k)
+        oracle.moe_layer(x, ids2, w2, wl.E, ws["w13"], ws["w2"])
+        t_total += time.perf_counter() - t0
+        nbytes += step_bytes(wl, ids)
+        steps += 1
+    threads = min(oracle.num_threads(), wl.M)   # the oracle parallelises over tokens
+    return {"value": nbytes / t_total / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{steps} full steps (top-k + layer, binary64) of {wl.name}, "
+                      f"fresh routing each, {t_total:.1f} s timed",
+            "us_per_layer": round(t_total / steps * 1e6, 1)}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    from top_moe_expert_gb300 import inputs
+    wl = workload_from_name(args.workload)
+    oracle.build()
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    # Each step is a bounded sample of the workload: one routed expert of one
+    # token restricted to its first 64 intermediate neurons (gate/up rows
+    # 0..63, down columns 0..63), so K+W steps stay within a few minutes.
+    K, W = args.steps, args.warmup
+    Is = 64
+    logits = inputs.router_logits(wl, 0)
+    ids, _ = oracle.topk_softmax(logits, wl.k)
+    e0 = int(ids[0, 0])
+    def draw(which):
+        if device is not None:
+            return inputs.weights_fp32_device(wl, which, e0, device).cpu().numpy()
+        return inputs.weights_fp32(wl, which, [e0])[0]
+    f13 = draw("w13")
+    f13 = np.concatenate([f13[:Is], f13[wl.I:wl.I + Is]])[None].astype(np.float64)
+    f2 = draw("w2")[:, :Is][None].astype(np.float64)
+    slot = np.full(wl.E, -1, dtype=np.int32)
+    slot[e0] = 0
+    q13, s13 = oracle.mxfp8_quantize_3d(f13)
+    q2, s2 = oracle.mxfp8_quantize_3d(f2)
+    w13 = {"fmt": "mxfp8", "q": q13, "s": s13, "slot": slot}
+    w2 = {"fmt": "mxfp8", "q": q2, "s": s2, "slot": slot}
+    x = inputs.activations(wl, 0).to(torch.float64).numpy()[:1]
+    one = np.array([[e0]], dtype=np.int32)
+    wone = np.ones((1, 1))
+    sample_bytes = 3 * Is * wl.d * 33 // 32 + wl.d * 2 + wl.d * 2
+    nbytes, t_total = 0, 0.0
+    for i in range(W + K):
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, one, wone, wl.E, w13, w2)
+        dt = time.perf_counter() - t0
+        if i >= W:
+            t_total += dt
+            nbytes += sample_bytes
+    v = nbytes / t_total / 1e12
+    return {"metric": METRIC, "impl": "reference", "value": v, "unit": "TB/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": t_total * 1e3 / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k},
+            "cpu_baseline": {"value": v, "unit": "TB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"per step: one routed expert of one token of {wl.name}, "
+                                       f"first {Is} intermediate neurons (binary64 oracle, 1 thread)"},
+            "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_m1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    import __graft_entry__
+    __graft_entry__.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    line = run_ours(args, rank, world, device)
+    if line is not None:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(workload_from_name(args.workload), device)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * moe_ffn.h -- C ABI of libmoe_ffn.so, the GB300 (sm_103a) routed
+ * Mixture-of-Experts expert-FFN layer.
+ *
+ * The layer (pages cited by title and section):
+ *   - "Route-Block Membership Selects Packed-AWQ Arithmetic" (arXiv
+ *     2607.26316), opening paragraph: a top-k router produces an M x k array
+ *     of expert ids; flattening it row-major gives route ids r = t*k + j;
+ *     alignment groups the valid routes by expert, pads each expert to a
+ *     multiple of a block size b and emits a parallel expert-block vector.
+ *   - "Warp decode" (cursor.com blog), section on how the two kernels work:
+ *     per routed expert a gate/up projection, SiLU(gate) x up, a down
+ *     projection, and the routing-weighted combine folded into the down
+ *     accumulation; MXFP8 weights, BF16 activations, FP32 accumulation.
+ *   - "Hardware-Native Joint Sparse-Quantization for Trillion-Scale
+ *     Mixture-of-Experts" (arXiv 2610.02241), Sec. 3.4 and App. D.1: the
+ *     expert products Y_e = X_e W_e^T of a grouped GEMM, computed with the
+ *     weights as the left operand (Y_e^T = W_e X_e^T), activations quantized
+ *     at run time into 32-element scale blocks, fused SwiGLU + requantization.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *     and densely packed, unless a parameter says otherwise.  The library
+ *     allocates and frees nothing; scratch memory is the caller's `ws`.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work
+ *     is enqueued on it and never synchronised; results are ready when the
+ *     stream reaches them.  Calls that share `ws` must not overlap.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     non-MOE_OK status means nothing was enqueued (MOE_ERR_CUDA: a launch
+ *     failed; the stream may hold earlier work of the same call).
+ *   - Expert ids outside [0, E) are invalid routes: they are skipped,
+ *     contribute nothing, and their number is ADDED to *dev_status (a device
+ *     int32 the caller zeroes; may be NULL).
+ *   - Shapes are int32; M*k and the padded row counts must fit in int32.
+ *
+ * Weight formats (one projection of all E experts, [E][N][K], K contracted):
+ *   MOE_W_MXFP8: q uint8 [E][N][K] OCP E4M3 codes; scale uint8 [E][N][K/32]
+ *                OCP E8M0 bytes (value 2^(s-127)); zero NULL.  K % 32 == 0.
+ *   MOE_W_AWQ4:  q int32 [E][N][K/8], element 8c+i of a row in bits
+ *                4i..4i+3 of word c; scale fp16 [E][N][K/128];
+ *                zero int32 [E][N/8][K/128], the zero of row 8a+i in nibble i
+ *                of word a; weight = (q - zero) * scale.  K % 128 == 0,
+ *                N % 8 == 0.
+ *   W13 is the fused gate/up projection: N = 2I (rows 0..I-1 gate, rows
+ *   I..2I-1 up), K = d.  W2 is the down projection: N = d, K = I.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_FFN_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, bad enum       */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid but not implemented (format/size) */
+    MOE_ERR_CAPACITY = 3,     /* an output capacity is too small         */
+    MOE_ERR_WORKSPACE = 4,    /* ws too small or misaligned (256 B)      */
+    MOE_ERR_CUDA = 5,         /* a CUDA launch/attribute call failed      */
+    MOE_ERR_TIMEOUT = 6       /* reserved: a bounded device wait expired */
+} moe_status_t;
+
+typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1 } moe_wfmt_t;
+typedef enum { MOE_BF16 = 0, MOE_FP16 = 1, MOE_FP32 = 2 } moe_dtype_t;
+
+/* One projection of all experts; see "Weight formats" above. */
+typedef struct {
+    int32_t fmt;         /* moe_wfmt_t                                   */
+    int32_t E, N, K;
+    const void *q;       /* codes / packed nibbles                       */
+    const void *scale;   /* E8M0 bytes / fp16 group scales               */
+    const void *zero;    /* NULL / packed zero nibbles                   */
+} moe_weights_t;
+
+/* Human-readable name of a status code (static storage). */
+const char *moe_status_string(moe_status_t s);
+/* MOE_FFN_ABI_VERSION of the loaded library. */
+int32_t moe_abi_version(void);
+
+/* ---------------------------------------------------------------- routing
+ * Top-k softmax routing ("Warp decode", section on the conventional MoE
+ * path: each token selects k of E experts, e.g. 8 of 128).
+ *   logits  fp32 [M][E];  topk_ids int32 [M][k];  topk_w fp32 [M][k].
+ * Experts are selected by logit (ties to the lower id), slots in descending
+ * order; topk_w = softmax over the E logits renormalised over the k chosen
+ * (= softmax over the chosen logits).  Logits must be finite.
+ * Limits: 1 <= k <= min(E, 32), E <= 4096. */
+moe_status_t moe_topk_softmax(const float *logits, int32_t M, int32_t E, int32_t k,
+                              int32_t *topk_ids, float *topk_w, void *stream);
+
+/* --------------------------------------------------------------- alignment
+ * Route alignment by stable construction ("Route-Block Membership Selects
+ * Packed-AWQ Arithmetic", opening and stable-construction paragraphs).
+ * Valid routes (id in [0,E)) are ordered by (expert id, route id); each
+ * active expert's run is padded with the sentinel M*k to a multiple of b;
+ * experts without routes get no block.
+ *   topk_ids          int32 [M*k] (the M x k router output, flattened)
+ *   sorted_route_ids  int32 [cap_rows]: aligned rows; rows past the padded
+ *                     end also hold the sentinel M*k
+ *   expert_ids        int32 [cap_blocks]: expert of aligned block j (rows
+ *                     j*b .. j*b+b-1); -1 past the last active block
+ *   num_rows_post_pad int32 [1]: b * number of active blocks
+ * The result is unique, so it is bit-exact and history-independent.
+ * moe_align_capacity gives the worst-case cap_rows / cap_blocks
+ * (M*k + min(E, M*k)*(b-1), rounded up to b); smaller capacities are
+ * accepted, and MOE_ERR_CAPACITY is returned if they are below that bound.
+ * ws: moe_align_workspace_size bytes (may be 0).  Limits: E <= 1024,
+ * 1 <= b <= 256. */
+moe_status_t moe_align_capacity(int32_t M, int32_t k, int32_t E, int32_t b,
+                                int32_t *cap_rows, int32_t *cap_blocks);
+moe_status_t moe_align_workspace_size(int32_t M, int32_t k, int32_t E, int32_t b, size_t *bytes);
+moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, int32_t k, int32_t E,
+                                  int32_t b, int32_t *sorted_route_ids, int32_t *expert_ids,
+                                  int32_t *num_rows_post_pad, int32_t cap_rows, int32_t cap_blocks,
+                                  void *ws, size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------- quantization
+ * MXFP8 quantization of rows of K values, per 32-element block along K
+ * ("Hardware-Native Joint Sparse-Quantization ...", Sec. 3.4 / App. D.1:
+ * 32-element scale blocks; OCP MX rule): X = floor(log2 amax) - 8 clamped to
+ * [-127,127] (amax = 0 gives -127), s = X + 127, q = RNE(v / 2^X) on the E4M3
+ * grid, saturating at +-448, sign kept.  Used to build MXFP8 weights and by
+ * the grouped path's activation quantization.
+ *   v: [rows][K] of vdt (MOE_FP32 or MOE_BF16); q uint8 [rows][K];
+ *   s uint8 [rows][K/32].  Inputs must be finite. */
+moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_t K,
+                                uint8_t *q, uint8_t *s, void *stream);
+
+/* ------------------------------------------------------------ the layer
+ * Output-centric decode path ("Warp decode", sections on what changed and
+ * how the two kernels work): one warp per intermediate scalar of a
+ * (token, routed expert) and one warp per output scalar of a token; weight
+ * rows streamed with 16-byte loads, dequantised on the fly, FP32
+ * accumulation, warp butterfly reductions, the routing weight folded into
+ * the down accumulation.  No alignment, padding, scatter or combine buffer.
+ *   x        [M][d] of xdt (MOE_BF16, or MOE_FP16 / MOE_BF16 for AWQ)
+ *   topk_ids int32 [M][k], topk_w fp32 [M][k]
+ *   w13      N = 2I, K = d;  w2: N = d, K = I (same format, same E)
+ *   y        [M][d] of ydt (MOE_BF16 or MOE_FP32)
+ *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned: holds
+ *            the FP32 intermediate h [M*k][I]
+ * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
+ * Per-output summation order is fixed (independent of M, of the other
+ * tokens and of the grid), so results are bit-reproducible.
+ * Limits: d % 512 == 0 and I % 32 == 0 (MXFP8); d % 1024 == 0 and
+ * I % 128 == 0 (AWQ4); k <= 32. */
+moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t I, size_t *bytes);
+moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
+                            const int32_t *topk_ids, const float *topk_w, int32_t k,
+                            const moe_weights_t *w13, const moe_weights_t *w2,
+                            void *y, int32_t ydt, void *ws, size_t ws_bytes,
+                            int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

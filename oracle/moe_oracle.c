@@ -157,8 +157,10 @@ static uint8_t e4m3_rne_magnitude(double a)
  * s: [rows][K/32] E8M0 bytes. */
 void orc_mxfp8_quantize(const double *v, int64_t rows, int64_t K, uint8_t *q, uint8_t *s)
 {
-    int64_t r, blk, i;
+    int64_t r;
+#pragma omp parallel for schedule(static)
     for (r = 0; r < rows; ++r) {
+        int64_t blk, i;
         for (blk = 0; blk < K / 32; ++blk) {
             const double *vb = v + r * K + blk * 32;
             double amax = 0.0;

@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports what include/*.h declares.
+
+CPU only: no call here launches a kernel.  Host-side entry points (status
+names, capacities, workspace sizes) are exercised, and argument validation is
+checked to reject bad calls before anything would reach the GPU.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import top_moe_expert_gb300 as moe
+from top_moe_expert_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return moe.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert "moe_ffn_decode" in names and "moe_align_block_size" in names
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    # and the binding knows every declared entry point
+    assert set(names) <= set(moe._PROTOS), set(names) - set(moe._PROTOS)
+
+
+def test_status_names_and_version(L):
+    for code, name in moe.STATUS_NAMES.items():
+        assert L.moe_status_string(code).decode() == name
+    assert L.moe_abi_version() == 1
+
+
+def test_align_capacity_bound():
+    # the packed-AWQ study's shape: 168 routes, worst case every route alone
+    cr, cb = moe.moe_align_capacity(21, 8, 128, 8)
+    assert cr == 168 + 128 * 7 and cb == cr // 8
+    cr, cb = moe.moe_align_capacity(1, 8, 128, 8)
+    assert cr == 8 * 8 and cb == 8
+    assert moe.moe_align_workspace_size(21, 8, 128, 8) == 0
+    assert moe.moe_align_workspace_size(16384, 8, 128, 16) == 64 * 128 * 4
+
+
+def test_decode_workspace_size():
+    assert moe.moe_ffn_decode_workspace_size(1, 8, 768) == 8 * 768 * 4
+    assert moe.moe_ffn_decode_workspace_size(3, 8, 100) % 256 == 0
+
+
+def test_host_validation_rejects_before_launch(L):
+    # invalid shapes / null pointers return synchronously, nothing launched
+    assert L.moe_topk_softmax(None, 4, 128, 0, None, None, None) == 1
+    assert L.moe_topk_softmax(None, 4, 8, 9, None, None, None) == 1
+    assert L.moe_align_block_size(None, 1, 8, 2048, 8, None, None, None, 64, 8, None, 0, None, None) == 2
+    assert L.moe_align_block_size(16, 21, 8, 128, 8, 16, 16, 16, 100, 100, None, 0, None, None) == 3
+    assert L.moe_mxfp8_quantize(None, 2, 4, 33, None, None, None) == 1
+    assert L.moe_mxfp8_quantize(None, 1, 4, 32, None, None, None) == 2
+    w = moe.moe_weights_t(0, 4, 64, 512, 16, 16, None)
+    w2 = moe.moe_weights_t(0, 4, 512, 32, 16, 16, None)
+    # W2 K (=I) must match W13 N/2
+    bad = moe.moe_weights_t(0, 4, 512, 64, 16, 16, None)
+    assert L.moe_ffn_decode(16, 0, 1, 512, 16, 16, 8, ctypes.byref(w), ctypes.byref(bad), 16, 0,
+                            None, 0, None, None) == 1
+    # workspace missing
+    assert L.moe_ffn_decode(16, 0, 1, 512, 16, 16, 8, ctypes.byref(w), ctypes.byref(w2), 16, 0,
+                            None, 0, None, None) == 4
+    # unsupported output dtype
+    assert L.moe_ffn_decode(16, 0, 1, 512, 16, 16, 8, ctypes.byref(w), ctypes.byref(w2), 16, 1,
+                            None, 0, None, None) == 2
+    # d not a multiple of 512
+    w3 = moe.moe_weights_t(0, 4, 64, 256, 16, 16, None)
+    w4 = moe.moe_weights_t(0, 4, 256, 32, 16, 16, None)
+    assert L.moe_ffn_decode(16, 0, 1, 256, 16, 16, 8, ctypes.byref(w3), ctypes.byref(w4), 16, 0,
+                            None, 0, None, None) == 2
+    # M == 0 is a no-op that succeeds without touching the GPU
+    assert L.moe_topk_softmax(None, 0, 128, 8, None, None, None) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(moe, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        moe.lib()

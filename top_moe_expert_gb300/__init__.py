@@ -1,0 +1,213 @@
+"""top_moe_expert_gb300 -- GB300 (sm_103a) routed MoE expert-FFN layer.
+
+A thin ctypes binding over the C ABI of ``libmoe_ffn.so`` (declared in
+``include/moe_ffn.h``).  The functions here carry the same names as the C
+entry points and only marshal arguments: PyTorch supplies device memory and
+the current CUDA stream; every step of the layer runs in the library's CUDA
+kernels.  There is no fallback: if the library is not built, or no GPU is
+present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_CAPACITY", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
+                6: "MOE_ERR_TIMEOUT"}
+MOE_W_MXFP8, MOE_W_AWQ4 = 0, 1
+MOE_BF16, MOE_FP16, MOE_FP32 = 0, 1, 2
+
+_DT = {torch.bfloat16: MOE_BF16, torch.float16: MOE_FP16, torch.float32: MOE_FP32}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class moe_weights_t(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("E", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("q", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("zero", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+_I32, _I64, _P, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+_PROTOS = {
+    "moe_status_string": (ctypes.c_char_p, [_I32]),
+    "moe_abi_version": (_I32, []),
+    "moe_topk_softmax": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P]),
+    "moe_align_capacity": (_I32, [_I32, _I32, _I32, _I32, _P, _P]),
+    "moe_align_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
+    "moe_align_block_size": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _I32, _P, _SZ, _P, _P]),
+    "moe_mxfp8_quantize": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P]),
+    "moe_ffn_decode_workspace_size": (_I32, [_I32, _I32, _I32, _P]),
+    "moe_ffn_decode": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
+                              ctypes.POINTER(moe_weights_t), _P, _I32, _P, _SZ, _P, _P]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmoe_ffn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m top_moe_expert_gb300.build` (no CPU fallback exists)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _PROTOS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+@dataclasses.dataclass
+class Weights:
+    """One projection of all experts: MXFP8 (q uint8 [E,N,K], scale uint8
+    [E,N,K/32]) or AWQ4 (q int32 [E,N,K/8], scale fp16 [E,N,K/128], zero
+    int32 [E,N/8,K/128])."""
+    fmt: int
+    q: torch.Tensor
+    scale: torch.Tensor
+    zero: torch.Tensor | None = None
+
+    @property
+    def E(self):
+        return self.q.shape[0]
+
+    @property
+    def N(self):
+        return self.q.shape[1]
+
+    @property
+    def K(self):
+        return self.q.shape[2] * (8 if self.fmt == MOE_W_AWQ4 else 1)
+
+    def c_struct(self) -> moe_weights_t:
+        return moe_weights_t(self.fmt, self.E, self.N, self.K, self.q.data_ptr(),
+                             self.scale.data_ptr(), self.zero.data_ptr() if self.zero is not None else None)
+
+
+# ---------------------------------------------------------------- routing
+
+def moe_topk_softmax(logits: torch.Tensor, k: int, topk_ids=None, topk_w=None, stream=None):
+    _dev(logits, "logits")
+    M, E = logits.shape
+    ids = topk_ids if topk_ids is not None else torch.empty((M, k), dtype=torch.int32, device=logits.device)
+    w = topk_w if topk_w is not None else torch.empty((M, k), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_topk_softmax(_ptr(logits), M, E, k, _ptr(ids), _ptr(w), _stream(stream)),
+           "moe_topk_softmax")
+    return ids, w
+
+
+# ---------------------------------------------------------------- alignment
+
+def moe_align_capacity(M: int, k: int, E: int, b: int):
+    cr, cb = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().moe_align_capacity(M, k, E, b, ctypes.byref(cr), ctypes.byref(cb)), "moe_align_capacity")
+    return cr.value, cb.value
+
+
+def moe_align_workspace_size(M: int, k: int, E: int, b: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_align_workspace_size(M, k, E, b, ctypes.byref(n)), "moe_align_workspace_size")
+    return n.value
+
+
+def moe_align_block_size(topk_ids: torch.Tensor, E: int, b: int, cap_rows=None, cap_blocks=None,
+                         out=None, ws=None, dev_status=None, stream=None):
+    """Returns (sorted_route_ids [cap_rows], expert_ids [cap_blocks],
+    num_rows_post_pad [1]) as int32 device tensors."""
+    _dev(topk_ids, "topk_ids")
+    M, k = topk_ids.shape
+    cr, cb = moe_align_capacity(M, k, E, b)
+    cap_rows = cr if cap_rows is None else cap_rows
+    cap_blocks = cb if cap_blocks is None else cap_blocks
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(cap_rows, dtype=torch.int32, device=dev),
+               torch.empty(cap_blocks, dtype=torch.int32, device=dev),
+               torch.empty(1, dtype=torch.int32, device=dev))
+    need = moe_align_workspace_size(M, k, E, b)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(lib().moe_align_block_size(_ptr(topk_ids), M, k, E, b, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                      cap_rows, cap_blocks, _ptr(ws), ws.numel() if ws is not None else 0,
+                                      _ptr(dev_status), _stream(stream)), "moe_align_block_size")
+    return out
+
+
+# ---------------------------------------------------------------- quantization
+
+def moe_mxfp8_quantize(v: torch.Tensor, q=None, s=None, stream=None):
+    """MXFP8 codes and E8M0 scales of v [rows, K] (fp32 or bf16)."""
+    _dev(v, "v")
+    K = v.shape[-1]
+    rows = v.numel() // K
+    q = q if q is not None else torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    s = s if s is not None else torch.empty((*v.shape[:-1], K // 32), dtype=torch.uint8, device=v.device)
+    _check(lib().moe_mxfp8_quantize(_ptr(v), _DT[v.dtype], rows, K, _ptr(q), _ptr(s), _stream(stream)),
+           "moe_mxfp8_quantize")
+    return q, s
+
+
+# ---------------------------------------------------------------- the layer
+
+def moe_ffn_decode_workspace_size(M: int, k: int, I: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_ffn_decode_workspace_size(M, k, I, ctypes.byref(n)), "moe_ffn_decode_workspace_size")
+    return n.value
+
+
+def moe_ffn_decode(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, w13: Weights, w2: Weights,
+                   out_dtype=torch.bfloat16, y=None, ws=None, dev_status=None, stream=None):
+    """Output-centric decode path: y [M, d] = sum_j w_j * FFN_{e_j}(x)."""
+    for t, n in ((x, "x"), (topk_ids, "topk_ids"), (topk_w, "topk_w")):
+        _dev(t, n)
+    M, d = x.shape
+    k = topk_ids.shape[1]
+    I = w2.K
+    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
+    if ws is None:
+        ws = torch.empty(moe_ffn_decode_workspace_size(M, k, I), dtype=torch.uint8, device=x.device)
+    a, b = w13.c_struct(), w2.c_struct()
+    _check(lib().moe_ffn_decode(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype], _ptr(ws),
+                                ws.numel(), _ptr(dev_status), _stream(stream)), "moe_ffn_decode")
+    return y

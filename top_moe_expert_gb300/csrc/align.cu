@@ -1,0 +1,291 @@
+// align.cu -- route alignment by stable construction.
+//
+// "Route-Block Membership Selects Packed-AWQ Arithmetic", opening paragraph:
+// alignment groups the valid routes by expert, pads each expert's count to a
+// multiple of the block size b and emits a parallel expert-block vector;
+// stable-construction paragraph: valid routes are ordered by (expert id,
+// flattened route id), which makes the result history-independent.
+//
+// GPU design: a counting sort whose every step is deterministic.
+//   pass 1 (only when M*k > one chunk): each CTA histograms a chunk of
+//          kChunk routes into ws[chunk][E];
+//   pass 2: each CTA recomputes the per-expert totals, the padded exclusive
+//          prefix over experts and its chunk's base, then places its routes:
+//          every warp owns a contiguous slice of the chunk and ranks routes
+//          of equal expert with __match_any_sync, so the position of route r
+//          is off[e] + (#routes of e before r) exactly as the definition.
+// No atomics decide a position, so repeated calls give identical bits.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kAlignThreads = 256;
+constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kChunk = 2048;                       // routes per CTA
+constexpr int kSlice = kChunk / kAlignWarps;       // routes per warp
+constexpr int kAlignMaxE = 1024;
+
+__device__ __forceinline__ bool valid_id(int e, int E) { return e >= 0 && e < E; }
+
+// Pass 1: per-chunk histogram.
+__global__ void __launch_bounds__(kAlignThreads)
+align_hist_kernel(const int32_t *__restrict__ ids, int MK, int E,
+                  int32_t *__restrict__ hist, int32_t *__restrict__ dev_status)
+{
+    extern __shared__ int32_t sm_hist[];
+    __shared__ int inval;
+    const int c = blockIdx.x;
+    for (int e = threadIdx.x; e < E; e += kAlignThreads)
+        sm_hist[e] = 0;
+    if (threadIdx.x == 0)
+        inval = 0;
+    __syncthreads();
+    const int r0 = c * kChunk, r1 = min(MK, r0 + kChunk);
+    int my_inval = 0;
+    for (int r = r0 + threadIdx.x; r < r1; r += kAlignThreads) {
+        int e = ids[r];
+        if (valid_id(e, E))
+            atomicAdd(&sm_hist[e], 1);
+        else
+            ++my_inval;
+    }
+    if (my_inval)
+        atomicAdd(&inval, my_inval);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kAlignThreads)
+        hist[static_cast<int64_t>(c) * E + e] = sm_hist[e];
+    if (threadIdx.x == 0 && inval && dev_status)
+        atomicAdd(dev_status, inval);
+}
+
+// Block-wide exclusive scan of n <= 4*kAlignThreads ints in place; returns
+// the total to every thread.
+__device__ int block_exclusive_scan(int32_t *a, int n)
+{
+    __shared__ int warp_tot[kAlignWarps];
+    const int per = 4;
+    const int base = threadIdx.x * per;
+    int v[per];
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+        v[i] = (base + i < n) ? a[base + i] : 0;
+        s += v[i];
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += t;
+    }
+    if (lane == 31)
+        warp_tot[w] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int i = 0; i < kAlignWarps; ++i) {
+        if (i < w)
+            wbase += warp_tot[i];
+        total += warp_tot[i];
+    }
+    int run = wbase + incl - s;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+        if (base + i < n)
+            a[base + i] = run;
+        run += v[i];
+    }
+    __syncthreads();
+    return total;
+}
+
+// Pass 2: offsets, padding, tails and stable placement of one chunk.
+__global__ void __launch_bounds__(kAlignThreads)
+align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nchunks,
+                   const int32_t *__restrict__ hist,      // [nchunks][E] or null (1 chunk)
+                   int32_t *__restrict__ sorted_ids, int32_t *__restrict__ expert_ids,
+                   int32_t *__restrict__ num_rows_post_pad, int cap_rows, int cap_blocks,
+                   int32_t *__restrict__ dev_status)
+{
+    extern __shared__ int32_t sm[];
+    int32_t *tot = sm;                 // [E] routes of expert e
+    int32_t *cbase = sm + E;           // [E] routes of e in earlier chunks
+    int32_t *off = sm + 2 * E;         // [E] first aligned row of e
+    int32_t *wcnt = sm + 3 * E;        // [kAlignWarps][E]
+    __shared__ int inval;
+    const int c = blockIdx.x;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int r0 = c * kChunk, r1 = min(MK, r0 + kChunk);
+
+    for (int i = threadIdx.x; i < (3 + kAlignWarps) * E; i += kAlignThreads)
+        sm[i] = 0;
+    if (threadIdx.x == 0)
+        inval = 0;
+    __syncthreads();
+    if (hist == nullptr) {
+        // single chunk: histogram here
+        int my_inval = 0;
+        for (int r = r0 + threadIdx.x; r < r1; r += kAlignThreads) {
+            int e = ids[r];
+            if (valid_id(e, E))
+                atomicAdd(&tot[e], 1);
+            else
+                ++my_inval;
+        }
+        if (my_inval)
+            atomicAdd(&inval, my_inval);
+    } else {
+        for (int e = threadIdx.x; e < E; e += kAlignThreads) {
+            int t = 0, cb = 0;
+            for (int cc = 0; cc < nchunks; ++cc) {
+                int h = hist[static_cast<int64_t>(cc) * E + e];
+                t += h;
+                if (cc < c)
+                    cb += h;
+            }
+            tot[e] = t;
+            cbase[e] = cb;
+        }
+    }
+    __syncthreads();
+    if (hist == nullptr && threadIdx.x == 0 && inval && dev_status)
+        atomicAdd(dev_status, inval);
+    for (int e = threadIdx.x; e < E; e += kAlignThreads)
+        off[e] = (tot[e] + b - 1) / b * b;
+    __syncthreads();
+    const int total_rows = block_exclusive_scan(off, E);
+
+    // bookkeeping rows: padding sentinels and expert-block ids of the experts
+    // this CTA owns (e % nchunks == c), and a slice of the tails
+    for (int e = c; e < E; e += nchunks) {
+        const int p = (tot[e] + b - 1) / b * b;
+        for (int i = tot[e] + threadIdx.x; i < p; i += kAlignThreads)
+            sorted_ids[off[e] + i] = MK;
+        for (int j = threadIdx.x; j < p / b; j += kAlignThreads)
+            expert_ids[off[e] / b + j] = e;
+    }
+    {
+        const int stride = nchunks * kAlignThreads;
+        for (int i = total_rows + c * kAlignThreads + threadIdx.x; i < cap_rows; i += stride)
+            sorted_ids[i] = MK;
+        for (int j = total_rows / b + c * kAlignThreads + threadIdx.x; j < cap_blocks; j += stride)
+            expert_ids[j] = -1;
+    }
+    if (c == 0 && threadIdx.x == 0)
+        *num_rows_post_pad = total_rows;
+
+    // stable placement: warp w owns routes [s0, s1) of this chunk
+    const int s0 = r0 + w * kSlice, s1 = min(r1, s0 + kSlice);
+    int32_t *mycnt = wcnt + w * E;
+    for (int r = s0 + lane; r < s1; r += 32) {
+        int e = ids[r];
+        if (valid_id(e, E))
+            atomicAdd(&mycnt[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kAlignThreads) {
+        int run = 0;
+        for (int ww = 0; ww < kAlignWarps; ++ww) {
+            int v = wcnt[ww * E + e];
+            wcnt[ww * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int base = s0; base < s1; base += 32) {
+        const int r = base + lane;
+        const bool in = r < s1;
+        const int e = in ? ids[r] : -1;
+        const bool ok = in && valid_id(e, E);
+        const unsigned key = ok ? static_cast<unsigned>(e) : 0xffffffffu;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const unsigned lt = (1u << lane) - 1u;
+        const int rank = __popc(peers & lt);
+        int before = 0;
+        if (ok)
+            before = mycnt[e];
+        __syncwarp();
+        if (ok) {
+            sorted_ids[off[e] + cbase[e] + before + rank] = r;
+            if ((peers & lt) == 0)                 // leader of its group
+                mycnt[e] = before + __popc(peers);
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+static int64_t align_bound_rows(int64_t M, int64_t k, int64_t E, int64_t b)
+{
+    int64_t mk = M * k;
+    int64_t rows = mk + (E < mk ? E : mk) * (b - 1);
+    return (rows + b - 1) / b * b;
+}
+
+MOE_API moe_status_t moe_align_capacity(int32_t M, int32_t k, int32_t E, int32_t b,
+                                        int32_t *cap_rows, int32_t *cap_blocks)
+{
+    if (M < 0 || k < 1 || E < 1 || b < 1 || !cap_rows || !cap_blocks)
+        return MOE_ERR_INVALID_ARG;
+    int64_t rows = align_bound_rows(M, k, E, b);
+    if (rows > INT32_MAX)
+        return MOE_ERR_UNSUPPORTED;
+    *cap_rows = static_cast<int32_t>(rows);
+    *cap_blocks = static_cast<int32_t>(rows / b);
+    return MOE_OK;
+}
+
+MOE_API moe_status_t moe_align_workspace_size(int32_t M, int32_t k, int32_t E, int32_t b, size_t *bytes)
+{
+    if (M < 0 || k < 1 || E < 1 || b < 1 || !bytes)
+        return MOE_ERR_INVALID_ARG;
+    int64_t mk = static_cast<int64_t>(M) * k;
+    int64_t nchunks = (mk + kChunk - 1) / kChunk;
+    *bytes = nchunks > 1 ? ws_round(static_cast<size_t>(nchunks) * E * sizeof(int32_t)) : 0;
+    return MOE_OK;
+}
+
+MOE_API moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, int32_t k, int32_t E,
+                                          int32_t b, int32_t *sorted_route_ids, int32_t *expert_ids,
+                                          int32_t *num_rows_post_pad, int32_t cap_rows,
+                                          int32_t cap_blocks, void *ws, size_t ws_bytes,
+                                          int32_t *dev_status, void *stream)
+{
+    if (M < 0 || k < 1 || E < 1 || b < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (E > kAlignMaxE || b > 256)
+        return MOE_ERR_UNSUPPORTED;
+    const int64_t mk = static_cast<int64_t>(M) * k;
+    const int64_t bound = align_bound_rows(M, k, E, b);
+    if (bound > INT32_MAX)
+        return MOE_ERR_UNSUPPORTED;
+    if ((cap_rows > 0 && !sorted_route_ids) || (cap_blocks > 0 && !expert_ids) || !num_rows_post_pad ||
+        (mk > 0 && !topk_ids))
+        return MOE_ERR_INVALID_ARG;
+    if (cap_rows < bound || cap_blocks < bound / b)
+        return MOE_ERR_CAPACITY;
+    size_t need = 0;
+    moe_align_workspace_size(M, k, E, b, &need);
+    if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256)))
+        return MOE_ERR_WORKSPACE;
+
+    const int nchunks = static_cast<int>(mk > 0 ? (mk + kChunk - 1) / kChunk : 1);
+    cudaStream_t s = as_stream(stream);
+    const size_t place_smem = static_cast<size_t>(3 + kAlignWarps) * E * sizeof(int32_t);
+    int32_t *hist = nullptr;
+    if (nchunks > 1) {
+        hist = static_cast<int32_t *>(ws);
+        align_hist_kernel<<<nchunks, kAlignThreads, E * sizeof(int32_t), s>>>(
+            topk_ids, static_cast<int>(mk), E, hist, dev_status);
+        if (launch_status() != MOE_OK)
+            return MOE_ERR_CUDA;
+    }
+    align_place_kernel<<<nchunks, kAlignThreads, place_smem, s>>>(
+        topk_ids, static_cast<int>(mk), E, b, nchunks, hist, sorted_route_ids, expert_ids,
+        num_rows_post_pad, cap_rows, cap_blocks, dev_status);
+    return launch_status();
+}
