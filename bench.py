@@ -150,7 +150,7 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 def decode_src_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cu", "topk.cu", "common.cuh"):
+    for f in ("decode.cu", "decode_fused.cu", "decode_stream.cu", "topk.cu", "common.cuh", "tc.cuh"):
         h.update(open(os.path.join(ROOT, "top_moe_expert_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
@@ -174,6 +174,13 @@ class DecodeStep:
             moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), self.q2[e], self.s2[e])
         self.w13 = moe.Weights(moe.MOE_W_MXFP8, self.q13, self.s13)
         self.w2 = moe.Weights(moe.MOE_W_MXFP8, self.q2, self.s2)
+        # small batches take the single-pass kernel, which reads the down
+        # projection neuron-major: pack it once (same bytes, K-outer order)
+        self.fused = M <= 4 and d % 1024 == 0
+        if self.fused:
+            self.w2 = moe.moe_mxfp8_transpose(self.w2)
+            del self.q2, self.s2
+            torch.cuda.empty_cache()
         # fresh routing and activations for every step
         self.logits_host = torch.from_numpy(np.stack([inputs.router_logits(wl, i) for i in range(nsteps)]))
         self.x_host = torch.stack([inputs.activations(wl, i) for i in range(nsteps)])
@@ -184,7 +191,7 @@ class DecodeStep:
         self.ids = torch.empty((M, k), dtype=torch.int32, device=device)
         self.w = torch.empty((M, k), dtype=torch.float32, device=device)
         self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
-        self.ws = torch.empty(moe.moe_ffn_decode_workspace_size(M, k, I), dtype=torch.uint8, device=device)
+        self.ws = torch.empty(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device)
         torch.cuda.synchronize()
 
@@ -317,15 +324,17 @@ def run_ours(args, rank, world, device):
         "data": "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
                 "N(0,1) router logits; fresh routing every step)",
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "path": "output-centric decode (topk + gate/up + down, CUDA graph)",
+                   "path": ("single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
+                            else "output-centric decode (topk + gate/up + down)") + ", CUDA graph",
                    "l2": "flushed between timed steps (512 MiB write, outside the timed interval)",
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
                 "us_per_layer": round(e2e_ms * 1e3 / Ke, 3), "steps": Ke,
                 "h2d_bytes_per_step": wl.M * wl.d * 2 + wl.M * wl.E * 4,
                 "d2h_bytes_per_step": wl.M * wl.d * 2},
-        "gpu_launches": 3 * K,
-        "roofline": {"kernel": "decode layer: decode_gate_up_kernel + decode_down_kernel (PDL-chained)",
+        "gpu_launches": 3 * K,      # top-k, layer kernel, reduction / down kernel
+        "roofline": {"kernel": ("decode layer: df::fused_kernel + df::reduce_kernel (PDL-chained)" if st.fused
+                               else "decode layer: ds::gate_up_kernel + ds::down_kernel (PDL-chained)"),
                      "bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak_gbs,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved_gbs / peak_gbs, 4),
                      "traffic": committed_traffic(f"decode:{wl.name}", decode_src_hash())},

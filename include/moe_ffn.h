@@ -28,9 +28,12 @@
  *   - Arguments are validated on the host before anything is launched; a
  *     non-MOE_OK status means nothing was enqueued (MOE_ERR_CUDA: a launch
  *     failed; the stream may hold earlier work of the same call).
- *   - Expert ids outside [0, E) are invalid routes: they are skipped,
- *     contribute nothing, and their number is ADDED to *dev_status (a device
- *     int32 the caller zeroes; may be NULL).
+ *   - Expert ids outside [0, E) are invalid routes: they are skipped and
+ *     contribute nothing.  dev_status is NULL or a device int32[2] that the
+ *     caller zeroes: dev_status[0] is INCREASED by the number of invalid
+ *     routes seen; dev_status[1] receives the first error a kernel detected
+ *     on the device (MOE_ERR_TIMEOUT when a bounded wait on an mbarrier
+ *     expired; the outputs of that call are then undefined).
  *   - Shapes are int32; M*k and the padded row counts must fit in int32.
  *
  * Weight formats (one projection of all E experts, [E][N][K], K contracted):
@@ -41,6 +44,12 @@
  *                zero int32 [E][N/8][K/128], the zero of row 8a+i in nibble i
  *                of word a; weight = (q - zero) * scale.  K % 128 == 0,
  *                N % 8 == 0.
+ *   MOE_W_MXFP8_T: the same MXFP8 values stored K-outer ("transposed"):
+ *                q uint8 [E][K][N], scale uint8 [E][K/32][N] (the E8M0 of
+ *                block (n, k/32) at [k/32][n]).  Same bytes, different order;
+ *                produced from MOE_W_MXFP8 by moe_mxfp8_transpose.  Accepted
+ *                for w2 by moe_ffn_decode (its single-pass small-batch path
+ *                streams each neuron's down-projection column contiguously).
  *   W13 is the fused gate/up projection: N = 2I (rows 0..I-1 gate, rows
  *   I..2I-1 up), K = d.  W2 is the down projection: N = d, K = I.
  */
@@ -63,10 +72,10 @@ typedef enum {
     MOE_ERR_CAPACITY = 3,     /* an output capacity is too small         */
     MOE_ERR_WORKSPACE = 4,    /* ws too small or misaligned (256 B)      */
     MOE_ERR_CUDA = 5,         /* a CUDA launch/attribute call failed      */
-    MOE_ERR_TIMEOUT = 6       /* reserved: a bounded device wait expired */
+    MOE_ERR_TIMEOUT = 6       /* a bounded device wait expired (dev_status[1]) */
 } moe_status_t;
 
-typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1 } moe_wfmt_t;
+typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1, MOE_W_MXFP8_T = 2 } moe_wfmt_t;
 typedef enum { MOE_BF16 = 0, MOE_FP16 = 1, MOE_FP32 = 2 } moe_dtype_t;
 
 /* One projection of all experts; see "Weight formats" above. */
@@ -132,25 +141,37 @@ moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, int32_t k,
 moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_t K,
                                 uint8_t *q, uint8_t *s, void *stream);
 
+/* Re-layout of MXFP8 weights into MOE_W_MXFP8_T (a one-time packing step,
+ * like the offline packing of expert weights on the sparse-quantization
+ * page, App. D.1).  w: MOE_W_MXFP8 [E][N][K]; q_t: uint8 [E][K][N];
+ * scale_t: uint8 [E][K/32][N] (caller-allocated device buffers). */
+moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_t, void *stream);
+
 /* ------------------------------------------------------------ the layer
  * Output-centric decode path ("Warp decode", sections on what changed and
- * how the two kernels work): one warp per intermediate scalar of a
- * (token, routed expert) and one warp per output scalar of a token; weight
- * rows streamed with 16-byte loads, dequantised on the fly, FP32
- * accumulation, warp butterfly reductions, the routing weight folded into
- * the down accumulation.  No alignment, padding, scatter or combine buffer.
- *   x        [M][d] of xdt (MOE_BF16, or MOE_FP16 / MOE_BF16 for AWQ)
+ * how the two kernels work): parallelism over outputs, weight rows streamed
+ * once with on-the-fly dequantisation, FP32 accumulation, warp butterfly
+ * reductions, the routing weight folded into the down accumulation; no
+ * alignment, padding, scatter or combine buffer.
+ *   x        [M][d] of xdt (MOE_BF16; MOE_FP16 or MOE_BF16 for AWQ)
  *   topk_ids int32 [M][k], topk_w fp32 [M][k]
- *   w13      N = 2I, K = d;  w2: N = d, K = I (same format, same E)
+ *   w13      N = 2I, K = d (MOE_W_MXFP8 or MOE_W_AWQ4)
+ *   w2       N = d, K = I, same format as w13, or MOE_W_MXFP8_T with
+ *            MXFP8 w13 (then M <= 4, M*k <= 64 and d % 1024 == 0)
  *   y        [M][d] of ydt (MOE_BF16 or MOE_FP32)
- *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned: holds
- *            the FP32 intermediate h [M*k][I]
+ *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
- * Per-output summation order is fixed (independent of M, of the other
- * tokens and of the grid), so results are bit-reproducible.
+ * Kernels by case: w2 in MOE_W_MXFP8_T -> one streaming pass (gate/up rows
+ * and down columns of each neuron together, per-SM partial outputs) plus a
+ * fixed-order reduction; MXFP8 with M*k <= 512 -> a gate/up kernel and a
+ * down kernel chained by programmatic dependent launch; otherwise one warp
+ * per intermediate / output scalar.  Every output's summation order is fixed
+ * by the shapes, the path and (single-pass path) the set of routed experts,
+ * so identical inputs give identical bits; the two-kernel and per-scalar
+ * paths are also independent of the other tokens in the batch.
  * Limits: d % 512 == 0 and I % 32 == 0 (MXFP8); d % 1024 == 0 and
- * I % 128 == 0 (AWQ4); k <= 32. */
-moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t I, size_t *bytes);
+ * I % 128 == 0 (AWQ4); k <= 32; M <= 65535. */
+moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t d, int32_t I, size_t *bytes);
 moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
                             const int32_t *topk_ids, const float *topk_w, int32_t k,
                             const moe_weights_t *w13, const moe_weights_t *w2,

@@ -57,8 +57,11 @@ def test_align_capacity_bound():
 
 
 def test_decode_workspace_size():
-    assert moe.moe_ffn_decode_workspace_size(1, 8, 768) == 8 * 768 * 4
-    assert moe.moe_ffn_decode_workspace_size(3, 8, 100) % 256 == 0
+    # h [M*k][I] f32 (the two-kernel paths); d % 1024 != 0 rules out the
+    # single-pass path and its per-SM partial outputs
+    assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 8 * 768 * 4
+    assert moe.moe_ffn_decode_workspace_size(3, 8, 512, 100) % 256 == 0
+    assert moe.moe_ffn_decode_workspace_size(64, 8, 2048, 768) == 64 * 8 * 768 * 4
 
 
 def test_host_validation_rejects_before_launch(L):

@@ -101,10 +101,10 @@ def test_decode_invalid_routes_counted_and_skipped():
     ids[3, 2] = -1
     ids[5, 0] = wl.E
     ids[5, 7] = 10 ** 6
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
     y = run_decode(layer, x, ids, w, torch.float32, dev_status=st)
     torch.cuda.synchronize()
-    assert int(st.item()) == 3
+    assert st.tolist() == [3, 0]
     gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
 
 
@@ -151,3 +151,81 @@ def test_large_expert_decode(wl):
     x = inputs.activations(wl)
     y = run_decode(layer, x, ids, w, torch.bfloat16)
     gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
+
+
+# ------------------------------------------------ single-pass path (W2 packed K-outer)
+
+def test_transpose_is_a_pure_relayout():
+    layer = mx_layer(inputs.TINY)
+    t = moe.moe_mxfp8_transpose(layer.w2)
+    assert torch.equal(t.q, layer.q2.transpose(1, 2).contiguous())
+    assert torch.equal(t.scale, layer.s2.transpose(1, 2).contiguous())
+
+
+def _fused_layer(seed):
+    layer = mx_layer(dataclasses.replace(inputs.DECODE, name=f"fused_layer_{seed}", seed=seed))
+    if not hasattr(layer, "w2t"):
+        layer.w2t = moe.moe_mxfp8_transpose(layer.w2)
+    return layer
+
+
+def run_fused(layer, x, ids, w, out_dtype, **kw):
+    return moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
+                              layer.w13, layer.w2t, out_dtype=out_dtype, **kw)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_fused_decode_matches_oracle(M):
+    layer = _fused_layer(5)
+    wl = dataclasses.replace(inputs.DECODE, name=f"fused_m{M}", M=M, seed=5)
+    for step in range(2):
+        x = inputs.activations(wl, step)
+        ids, w = gs.routing(wl, step)
+        y = run_fused(layer, x, ids, w, torch.float32)
+        gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
+
+
+def test_fused_decode_duplicates_invalid_bf16_and_repeatability():
+    layer = _fused_layer(5)
+    wl = dataclasses.replace(inputs.DECODE, name="fused_m3", M=3, seed=6)
+    x = inputs.activations(wl)
+    ids, w = gs.routing(wl)
+    ids = ids.copy()
+    ids[0, 1] = ids[0, 0]            # one expert twice for token 0 (more routes than kept in registers)
+    ids[1, :3] = ids[2, :3]          # tokens sharing experts
+    ids[2, 5] = -7                   # invalid route
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    y = run_fused(layer, x, ids, w, torch.bfloat16, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.tolist() == [1, 0]
+    gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
+    ys = {hashlib.sha256(run_fused(layer, x, ids, w, torch.float32).cpu().numpy().tobytes()).hexdigest()
+          for _ in range(4)}
+    assert len(ys) == 1
+    # M=1 with a duplicated expert exercises the per-batch flush
+    x1 = inputs.activations(wl, 3)[:1]
+    ids1 = np.array([[4, 4, 9, 100, 4, 17, 33, 90]], dtype=np.int32)
+    w1 = np.full((1, 8), 0.125, dtype=np.float32)
+    gs.assert_layer_close(run_fused(layer, x1, ids1, w1, torch.float32), oracle_decode(layer, x1, ids1, w1))
+
+
+def test_fused_decode_large_expert_m1():
+    wl = inputs.LARGE_M1
+    ids, w = gs.routing(wl)
+    layer = mx_layer(wl, experts=tuple(np.unique(ids).tolist()))
+    w2t = moe.moe_mxfp8_transpose(layer.w2)
+    x = inputs.activations(wl)
+    y = moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
+                           layer.w13, w2t, out_dtype=torch.bfloat16)
+    del w2t
+    gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
+
+
+def test_fused_path_rejects_large_batches():
+    layer = _fused_layer(5)
+    wl = dataclasses.replace(inputs.DECODE, name="fused_m16", M=16, seed=5)
+    x = inputs.activations(wl)
+    ids, w = gs.routing(wl)
+    with pytest.raises(moe.MoeError) as ei:
+        run_fused(layer, x, ids, w, torch.float32)
+    assert ei.value.status == 2

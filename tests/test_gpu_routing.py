@@ -81,13 +81,13 @@ def test_mxfp8_quantize_bf16_and_denormals_bit_exact():
 # ---------------------------------------------------------------- alignment
 
 def _align_both(ids, E, b, **kw):
-    dev_status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev_status = torch.zeros(2, dtype=torch.int32, device="cuda")
     s, ex, npp = moe.moe_align_block_size(torch.from_numpy(ids).cuda(), E, b, dev_status=dev_status, **kw)
     rs, rex, rnpp, rinv = oracle.align(ids, E, b, cap_rows=s.numel(), cap_blocks=ex.numel())
     assert int(npp.item()) == rnpp
     assert np.array_equal(s.cpu().numpy(), rs)
     assert np.array_equal(ex.cpu().numpy(), rex)
-    assert int(dev_status.item()) == rinv
+    assert dev_status.tolist() == [rinv, 0]
     return s, ex, npp
 
 

@@ -23,7 +23,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CAPACITY", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_TIMEOUT"}
-MOE_W_MXFP8, MOE_W_AWQ4 = 0, 1
+MOE_W_MXFP8, MOE_W_AWQ4, MOE_W_MXFP8_T = 0, 1, 2
 MOE_BF16, MOE_FP16, MOE_FP32 = 0, 1, 2
 
 _DT = {torch.bfloat16: MOE_BF16, torch.float16: MOE_FP16, torch.float32: MOE_FP32}
@@ -53,7 +53,8 @@ _PROTOS = {
     "moe_align_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
     "moe_align_block_size": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _I32, _P, _SZ, _P, _P]),
     "moe_mxfp8_quantize": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P]),
-    "moe_ffn_decode_workspace_size": (_I32, [_I32, _I32, _I32, _P]),
+    "moe_mxfp8_transpose": (_I32, [ctypes.POINTER(moe_weights_t), _P, _P, _P]),
+    "moe_ffn_decode_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
     "moe_ffn_decode": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                               ctypes.POINTER(moe_weights_t), _P, _I32, _P, _SZ, _P, _P]),
 }
@@ -100,8 +101,9 @@ def _dev(t: torch.Tensor, name: str):
 @dataclasses.dataclass
 class Weights:
     """One projection of all experts: MXFP8 (q uint8 [E,N,K], scale uint8
-    [E,N,K/32]) or AWQ4 (q int32 [E,N,K/8], scale fp16 [E,N,K/128], zero
-    int32 [E,N/8,K/128])."""
+    [E,N,K/32]), MXFP8_T (the same values K-outer: q uint8 [E,K,N], scale
+    uint8 [E,K/32,N]) or AWQ4 (q int32 [E,N,K/8], scale fp16 [E,N,K/128],
+    zero int32 [E,N/8,K/128])."""
     fmt: int
     q: torch.Tensor
     scale: torch.Tensor
@@ -113,10 +115,12 @@ class Weights:
 
     @property
     def N(self):
-        return self.q.shape[1]
+        return self.q.shape[2] if self.fmt == MOE_W_MXFP8_T else self.q.shape[1]
 
     @property
     def K(self):
+        if self.fmt == MOE_W_MXFP8_T:
+            return self.q.shape[1]
         return self.q.shape[2] * (8 if self.fmt == MOE_W_AWQ4 else 1)
 
     def c_struct(self) -> moe_weights_t:
@@ -187,11 +191,22 @@ def moe_mxfp8_quantize(v: torch.Tensor, q=None, s=None, stream=None):
     return q, s
 
 
+def moe_mxfp8_transpose(w: Weights, stream=None) -> Weights:
+    """The same MXFP8 weights re-laid K-outer (MOE_W_MXFP8_T)."""
+    assert w.fmt == MOE_W_MXFP8
+    q_t = torch.empty((w.E, w.K, w.N), dtype=torch.uint8, device=w.q.device)
+    s_t = torch.empty((w.E, w.K // 32, w.N), dtype=torch.uint8, device=w.q.device)
+    a = w.c_struct()
+    _check(lib().moe_mxfp8_transpose(ctypes.byref(a), _ptr(q_t), _ptr(s_t), _stream(stream)),
+           "moe_mxfp8_transpose")
+    return Weights(MOE_W_MXFP8_T, q_t, s_t)
+
+
 # ---------------------------------------------------------------- the layer
 
-def moe_ffn_decode_workspace_size(M: int, k: int, I: int) -> int:
+def moe_ffn_decode_workspace_size(M: int, k: int, d: int, I: int) -> int:
     n = ctypes.c_size_t()
-    _check(lib().moe_ffn_decode_workspace_size(M, k, I, ctypes.byref(n)), "moe_ffn_decode_workspace_size")
+    _check(lib().moe_ffn_decode_workspace_size(M, k, d, I, ctypes.byref(n)), "moe_ffn_decode_workspace_size")
     return n.value
 
 
@@ -205,7 +220,7 @@ def moe_ffn_decode(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor
     I = w2.K
     y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
     if ws is None:
-        ws = torch.empty(moe_ffn_decode_workspace_size(M, k, I), dtype=torch.uint8, device=x.device)
+        ws = torch.empty(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=x.device)
     a, b = w13.c_struct(), w2.c_struct()
     _check(lib().moe_ffn_decode(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
                                 ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype], _ptr(ws),

@@ -99,4 +99,23 @@ __device__ __forceinline__ float silu_mul(float g, float u)
     return g / (1.0f + expf(-g)) * u;
 }
 
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the previous kernel on the stream is still running; it must execute
+// griddepcontrol.wait before touching that kernel's outputs.
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace moe

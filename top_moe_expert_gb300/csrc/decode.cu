@@ -20,6 +20,7 @@
 // Per-output summation order depends only on (d, I, k) and the lane layout,
 // never on M, on other tokens or on the grid, so results are bit-stable.
 #include "common.cuh"
+#include "decode_internal.h"
 
 namespace moe {
 
@@ -282,22 +283,6 @@ decode_down_kernel(const float *__restrict__ h, int d, int I, const int32_t *__r
     }
 }
 
-template <typename K, typename... Args>
-cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 template <int FMT, typename XT, typename YT>
 moe_status_t decode_launch(const void *x, int M, int d, const int32_t *ids, const float *wts, int k,
                            const moe_weights_t *w13, const moe_weights_t *w2, void *y, float *h,
@@ -328,11 +313,13 @@ moe_status_t decode_launch(const void *x, int M, int d, const int32_t *ids, cons
 
 using namespace moe;
 
-MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t I, size_t *bytes)
+MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t d, int32_t I, size_t *bytes)
 {
-    if (M < 0 || k < 1 || I < 1 || !bytes)
+    if (M < 0 || k < 1 || d < 1 || I < 1 || !bytes)
         return MOE_ERR_INVALID_ARG;
-    *bytes = ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
+    size_t h = ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
+    size_t part = (M <= 4 && d % 1024 == 0) ? decode_fused_workspace(M, d) : 0;
+    *bytes = h > part ? h : part;
     return MOE_OK;
 }
 
@@ -340,7 +327,7 @@ static moe_status_t check_weights(const moe_weights_t *w, int N, int K)
 {
     if (!w || !w->q || !w->scale || w->N != N || w->K != K || w->E < 1)
         return MOE_ERR_INVALID_ARG;
-    if (w->fmt == MOE_W_MXFP8) {
+    if (w->fmt == MOE_W_MXFP8 || w->fmt == MOE_W_MXFP8_T) {
         if (K % 32 != 0)
             return MOE_ERR_INVALID_ARG;
     } else if (w->fmt == MOE_W_AWQ4) {
@@ -366,7 +353,28 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     moe_status_t st;
     if ((st = check_weights(w13, 2 * I, d)) != MOE_OK || (st = check_weights(w2, d, I)) != MOE_OK)
         return st;
-    if (w13->fmt != w2->fmt || w13->E != w2->E)
+    if (w13->fmt == MOE_W_MXFP8_T)
+        return MOE_ERR_INVALID_ARG;
+    if (w13->E != w2->E)
+        return MOE_ERR_INVALID_ARG;
+    if (w2->fmt == MOE_W_MXFP8_T) {
+        // single-pass small-batch path: W2 given neuron-major
+        if (w13->fmt != MOE_W_MXFP8 || xdt != MOE_BF16 || (ydt != MOE_BF16 && ydt != MOE_FP32))
+            return MOE_ERR_UNSUPPORTED;
+        if (!decode_fused_eligible(M, k, d, I, w13->E) || !aligned(w13->scale, 16) || !aligned(w2->scale, 16))
+            return M == 0 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+        if (!x || !topk_ids || !topk_w || !y || !aligned(x, 16))
+            return MOE_ERR_INVALID_ARG;
+        size_t need;
+        moe_ffn_decode_workspace_size(M, k, d, I, &need);
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return MOE_ERR_WORKSPACE;
+        return decode_fused_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
+                                   static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
+                                   static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y,
+                                   ydt == MOE_FP32, static_cast<float *>(ws), dev_status, as_stream(stream));
+    }
+    if (w13->fmt != w2->fmt)
         return MOE_ERR_INVALID_ARG;
     const int fmt = w13->fmt;
     if (fmt == MOE_W_MXFP8 && (d % 512 != 0 || I % 32 != 0))
@@ -386,11 +394,19 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     if (!x || !topk_ids || !topk_w || !y || !aligned(x, 16))
         return MOE_ERR_INVALID_ARG;
     size_t need;
-    moe_ffn_decode_workspace_size(M, k, I, &need);
+    moe_ffn_decode_workspace_size(M, k, d, I, &need);
     if (!ws || ws_bytes < need || !aligned(ws, 256))
         return MOE_ERR_WORKSPACE;
     float *h = static_cast<float *>(ws);
     cudaStream_t s = as_stream(stream);
+    if (fmt == MOE_W_MXFP8 && decode_stream_eligible(M, k, d, I, w13->E, w13->q, w13->scale, w2->q, w2->scale)) {
+        const moe_status_t st2 = decode_stream_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
+                                    static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
+                                    static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale),
+                                    y, ydt == MOE_FP32, h, dev_status, s);
+        if (st2 != MOE_ERR_UNSUPPORTED)      // shapes it cannot stage take the general kernels
+            return st2;
+    }
     if (fmt == MOE_W_MXFP8) {
         return ydt == MOE_FP32
                    ? decode_launch<MOE_W_MXFP8, __nv_bfloat16, float>(x, M, d, topk_ids, topk_w, k, w13, w2, y, h, dev_status, s)

@@ -1,0 +1,28 @@
+// decode_internal.h -- entry of the streaming MXFP8 decode kernels
+// (decode_stream.cu), called by moe_ffn_decode when the shape qualifies.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_ffn.h"
+
+namespace moe {
+
+bool decode_stream_eligible(int M, int k, int d, int I, int E, const void *q13, const void *s13,
+                            const void *q2, const void *s2);
+
+moe_status_t decode_stream_launch(const __nv_bfloat16 *x, int M, int d, int I, int E, const int32_t *ids,
+                                  const float *wts, int k, const uint8_t *q13, const uint8_t *s13,
+                                  const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32, float *h,
+                                  int32_t *dev_status, cudaStream_t stream);
+
+size_t decode_fused_workspace(int M, int d);
+bool decode_fused_eligible(int M, int k, int d, int I, int E);
+moe_status_t decode_fused_launch(const __nv_bfloat16 *x, int M, int d, int I, int E, const int32_t *ids,
+                                 const float *wts, int k, const uint8_t *q13, const uint8_t *s13,
+                                 const uint8_t *q2t, const uint8_t *s2t, void *y, bool y_f32, float *partial,
+                                 int32_t *dev_status, cudaStream_t stream);
+
+}  // namespace moe

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 topk_softmax_kernel(const float *__restrict__ logits, int M, int E, int k,
                     int32_t *__restrict__ ids, float *__restrict__ wts)
 {
+    // let the next kernel (the layer) get resident; it waits for us itself
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
     if (t >= M)
@@ -32,59 +34,54 @@ topk_softmax_kernel(const float *__restrict__ logits, int M, int E, int k,
     float v[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
-        int e = i * 32 + lane;
-        v[i] = e < E ? l[e] : -INFINITY;
+        const int e = i * 32 + lane;
+        v[i] = e < E ? __ldcg(l + e) : -INFINITY;
     }
-    // taken[] marks already selected entries of this lane (bit i).
     uint32_t taken[(PER_LANE + 31) / 32];
 #pragma unroll
     for (int i = 0; i < (PER_LANE + 31) / 32; ++i)
         taken[i] = 0;
-    float sel_l[32];
-    int sel_e[32];
+    float my_l = -INFINITY;     // slot j = lane keeps its (logit, id)
+    int my_e = -1;
     for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int be = 0x7fffffff;
-        int bi = -1;
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
-            int e = i * 32 + lane;
-            bool free_ = e < E && !((taken[i >> 5] >> (i & 31)) & 1u);
-            if (free_ && (bi < 0 || better(v[i], e, bv, be))) {
+            const int e = i * 32 + lane;
+            const bool free_ = e < E && !((taken[i >> 5] >> (i & 31)) & 1u);
+            if (free_ && (be == 0x7fffffff || better(v[i], e, bv, be))) {
                 bv = v[i];
                 be = e;
-                bi = i;
             }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
             if (oe != 0x7fffffff && (be == 0x7fffffff || better(ov, oe, bv, be))) {
                 bv = ov;
                 be = oe;
             }
         }
-        // the owner lane marks its entry as taken
-        if (be != 0x7fffffff && (be & 31) == lane) {
-            int i = be >> 5;
+        if ((be & 31) == lane) {           // the owner marks the entry as taken
+            const int i = be >> 5;
 #pragma unroll
             for (int ii = 0; ii < PER_LANE; ++ii)
                 if (ii == i)
                     taken[ii >> 5] |= 1u << (ii & 31);
         }
-        sel_l[j] = bv;
-        sel_e[j] = be;
-    }
-    if (lane == 0) {
-        float mx = sel_l[0];
-        float z = 0.f;
-        for (int j = 0; j < k; ++j)
-            z += expf(sel_l[j] - mx);
-        for (int j = 0; j < k; ++j) {
-            ids[static_cast<int64_t>(t) * k + j] = sel_e[j];
-            wts[static_cast<int64_t>(t) * k + j] = expf(sel_l[j] - mx) / z;
+        if (lane == j) {
+            my_l = bv;
+            my_e = be;
         }
+    }
+    const float mx = __shfl_sync(0xffffffffu, my_l, 0);
+    const float p = lane < k ? expf(my_l - mx) : 0.f;
+    const float z = warp_sum(p);
+    if (lane < k) {
+        ids[static_cast<int64_t>(t) * k + lane] = my_e;
+        wts[static_cast<int64_t>(t) * k + lane] = p / z;
     }
 }
 
