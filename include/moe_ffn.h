@@ -178,6 +178,30 @@ moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
                             void *y, int32_t ydt, void *ws, size_t ws_bytes,
                             int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------ allocation-free decode
+ * No counterpart on the pages: a convenience for callers that cannot hand
+ * the library any device memory of its own -- code running under a strict
+ * CUDA-graph capture, serving runtimes that plan all device memory up front
+ * and forbid later allocation, operator plugins that only see the tensors
+ * of the call.  Same arguments and result as moe_ffn_decode on its
+ * two-kernel MXFP8 path, but without ws: the FP32 intermediate h
+ * (M*k*I floats) lives in a fixed 4 MiB array inside the library.
+ *   - Only MOE_W_MXFP8 weights (standard layout), MOE_BF16 x, and the shapes
+ *     of the two-kernel path (M*k <= 512, d % 512 == 0, I % 256 == 0,
+ *     E <= 1024); MOE_ERR_UNSUPPORTED otherwise.
+ *   - M*k*I*4 bytes above 4 MiB return MOE_ERR_CAPACITY (nothing launched).
+ *   - Allocates and frees nothing.  Every GPU that loads the library holds
+ *     the array until the process exits.  The first call on each device
+ *     looks the array's device address up (with that device current); make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls that overlap
+ *     on the GPU race on it: order them on one stream. */
+moe_status_t moe_ffn_decode_noalloc(const void *x, int32_t xdt, int32_t M, int32_t d,
+                                    const int32_t *topk_ids, const float *topk_w, int32_t k,
+                                    const moe_weights_t *w13, const moe_weights_t *w2,
+                                    void *y, int32_t ydt, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -57,6 +57,8 @@ _PROTOS = {
     "moe_ffn_decode_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
     "moe_ffn_decode": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                               ctypes.POINTER(moe_weights_t), _P, _I32, _P, _SZ, _P, _P]),
+    "moe_ffn_decode_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
+                                      ctypes.POINTER(moe_weights_t), _P, _I32, _P, _P]),
 }
 
 
@@ -225,4 +227,22 @@ def moe_ffn_decode(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor
     _check(lib().moe_ffn_decode(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
                                 ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype], _ptr(ws),
                                 ws.numel(), _ptr(dev_status), _stream(stream)), "moe_ffn_decode")
+    return y
+
+
+def moe_ffn_decode_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, w13: Weights,
+                           w2: Weights, out_dtype=torch.bfloat16, y=None, dev_status=None, stream=None):
+    """moe_ffn_decode without a workspace, for callers that cannot give the
+    library device memory: the intermediate lives in a fixed 4 MiB array
+    inside the library (MXFP8 two-kernel path only; first call on a device
+    outside stream capture; calls must not overlap on the GPU)."""
+    for t, nm in ((x, "x"), (topk_ids, "topk_ids"), (topk_w, "topk_w")):
+        _dev(t, nm)
+    M, d = x.shape
+    k = topk_ids.shape[1]
+    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
+    a, b = w13.c_struct(), w2.c_struct()
+    _check(lib().moe_ffn_decode_noalloc(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                        ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype],
+                                        _ptr(dev_status), _stream(stream)), "moe_ffn_decode_noalloc")
     return y
