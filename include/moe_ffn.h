@@ -178,6 +178,54 @@ moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
                             void *y, int32_t ydt, void *ws, size_t ws_bytes,
                             int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------- expert-centric path
+ * Grouped path for larger batches ("Hardware-Native Joint Sparse-
+ * Quantization ...", Sec. 3.4 and App. D.1): the expert products
+ * Y_e = X_e W_e^T as a grouped GEMM on the tensor cores (tcgen05
+ * kind::mxf8f6f4 with E8M0 block scaling), weights on the left operand;
+ * activations quantized to MXFP8 at run time into 32-element blocks; fused
+ * SwiGLU + requantization after the first GEMM; the routing weight applied
+ * in the second GEMM's epilogue; a fixed-order combine over the k slots.
+ * Rows are the aligned routes of moe_align_block_size (same b); one MMA
+ * N-tile is one MoE block.  Each output element accumulates its K-tiles in
+ * ascending order in one accumulator (no split-K, no atomics), so a route's
+ * result does not depend on its block membership or on the grid size.
+ *
+ * moe_grouped_prepare packs the E8M0 scales of both projections once into
+ * the tensor-core scale layout (sizes from moe_grouped_prepare_size):
+ *   sfa13: [E][I/64][d/128][512] bytes, sfa2: [E][d/128][I/128][512] bytes.
+ * moe_ffn_grouped:
+ *   x bf16 [M][d]; topk_ids / topk_w [M][k]; w13, w2 MOE_W_MXFP8;
+ *   sorted_route_ids [cap_rows], expert_ids, num_rows_post_pad: the output
+ *   of moe_align_block_size for the same ids, E and b (8 <= b <= 256,
+ *   b % 8 == 0); y [M][d] bf16 or fp32;
+ *   ws: moe_ffn_grouped_workspace_size bytes, 256-aligned, laid out as
+ *   [Xq | Xs | Hq | Hs | Yr], each part rounded up to 256 bytes:
+ *     Xq uint8 [cap_rows][d]    MXFP8 codes of x per aligned row (rows of
+ *                               padding sentinels are zero)
+ *     Xs uint8 [cap_rows/b][d/128][nsf][512]  their E8M0 scales, in the
+ *                               scale layout: byte (m%32)*16 + (m/32)*4 + kb
+ *                               of atom m/128 holds block kb of row m
+ *     Hq uint8 [cap_rows][I]    MXFP8 codes of SiLU(g)*u per aligned row
+ *     Hs uint8 [cap_rows/b][I/128][nsf][512]  their scales (same layout)
+ *     Yr f32 [M*k][d]           w_route * (W2 h) per route
+ *   with nsf = ceil(roundup16(b) / 128).
+ * Limits: d % 128 == 0, I % 128 == 0. */
+moe_status_t moe_grouped_prepare_size(const moe_weights_t *w13, const moe_weights_t *w2,
+                                      size_t *sfa13_bytes, size_t *sfa2_bytes);
+moe_status_t moe_grouped_prepare(const moe_weights_t *w13, const moe_weights_t *w2,
+                                 void *sfa13, void *sfa2, void *stream);
+moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_t d, int32_t I, int32_t b,
+                                            int32_t cap_rows, size_t *bytes);
+moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d,
+                             const int32_t *topk_ids, const float *topk_w, int32_t k,
+                             const moe_weights_t *w13, const moe_weights_t *w2,
+                             const void *sfa13, const void *sfa2,
+                             const int32_t *sorted_route_ids, const int32_t *expert_ids,
+                             const int32_t *num_rows_post_pad, int32_t b, int32_t cap_rows,
+                             void *y, int32_t ydt, void *ws, size_t ws_bytes,
+                             int32_t *dev_status, void *stream);
+
 /* ------------------------------------------------ allocation-free decode
  * No counterpart on the pages: a convenience for callers that cannot hand
  * the library any device memory of its own -- code running under a strict

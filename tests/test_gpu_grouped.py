@@ -1,0 +1,202 @@
+"""GPU parity of the expert-centric grouped path (tcgen05 block-scaled MMA).
+
+The oracle runs in its block-scaled mode (x and h quantized to MXFP8, OCP
+rule).  Checked: the activation codes bit for bit (a unique result: the
+quantizer sees exact bf16 inputs), the h codes against the oracle's exact h
+(equal wherever the exact value is not within 1e-5 of a rounding boundary,
+else one of the two neighbours), the layer output within the layer
+tolerance, and bit-identical per-route rows across repeats and across a
+non-canonical but valid alignment.
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import top_moe_expert_gb300 as moe
+from tests import gpu_setup as gs
+from tests import refdecode as rd
+from top_moe_expert_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    gs.need_gpu()
+
+
+def _setup(wl, b):
+    layer = gs.MxLayer(wl)
+    sfa13, sfa2 = moe.moe_grouped_prepare(layer.w13, layer.w2)
+    x = inputs.activations(wl)
+    ids, w = gs.routing(wl)
+    return layer, sfa13, sfa2, x, ids, w
+
+
+def _run(layer, sfa13, sfa2, x, ids, w, b, aligned=None, out_dtype=torch.float32):
+    tid = torch.from_numpy(ids).cuda()
+    if aligned is None:
+        aligned = moe.moe_align_block_size(tid, layer.wl.E, b)
+    M, d, I, k = x.shape[0], layer.wl.d, layer.wl.I, ids.shape[1]
+    cap_rows = aligned[0].numel()
+    ws = torch.zeros(moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    y = moe.moe_ffn_grouped(x.cuda(), tid, torch.from_numpy(w).cuda(), layer.w13, layer.w2, sfa13, sfa2, aligned, b,
+                            out_dtype=out_dtype, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.tolist() == [0, 0]
+    return y, ws, aligned
+
+
+def _oracle_mx(layer, x, ids, w):
+    w13, w2 = layer.oracle_weights(np.unique(ids))
+    return oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), layer.wl.E, w13, w2, mode=oracle.MODE_MX,
+                            want_h=True, want_hq=True)
+
+
+@pytest.mark.parametrize("b", [8, 16, 64])
+def test_grouped_tiny_layer(b):
+    wl = inputs.TINY
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    y, ws, aligned = _run(layer, sfa13, sfa2, x, ids, w, b)
+    ref = _oracle_mx(layer, x, ids, w)
+    gs.assert_layer_close(y, ref["y"])
+
+
+def test_grouped_activation_codes_bit_exact():
+    wl, b = inputs.TINY, 16
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    y, ws, aligned = _run(layer, sfa13, sfa2, x, ids, w, b)
+    M, k, d, I = wl.M, wl.k, wl.d, wl.I
+    L = moe.grouped_workspace_layout(M, k, d, I, b, aligned[0].numel())
+    npp = int(aligned[2].item())
+    sorted_ids = aligned[0].cpu().numpy()
+    xq = ws[L["xq"]:L["xq"] + npp * d].cpu().numpy().reshape(npp, d)
+    xv = gs.x_exact(x)
+    want = np.zeros((npp, d), dtype=np.uint8)
+    valid = sorted_ids[:npp] < M * k
+    q, s = oracle.mxfp8_quantize(xv[sorted_ids[:npp][valid] // k])
+    want[valid] = q
+    assert np.array_equal(xq, want)
+
+
+def _unswizzle_hs(ws, L, aligned, b, I):
+    """Hs scale atoms -> [rows, I/32] bytes in aligned-row order."""
+    npp = int(aligned[2].item())
+    nsf = L["nsf"]
+    nblk = npp // b
+    atoms = ws[L["hs"]:L["hs"] + nblk * (I // 128) * nsf * 512].cpu().numpy().reshape(nblk, I // 128, nsf, 512)
+    out = np.zeros((npp, I // 32), dtype=np.uint8)
+    for rho in range(npp):
+        jb, m = divmod(rho, b)
+        for kblk in range(I // 32):
+            out[rho, kblk] = atoms[jb, kblk // 4, m // 128, (m % 32) * 16 + ((m % 128) // 32) * 4 + kblk % 4]
+    return out
+
+
+def test_grouped_h_codes_valid_against_exact_h():
+    wl, b = inputs.TINY, 16
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    y, ws, aligned = _run(layer, sfa13, sfa2, x, ids, w, b)
+    ref = _oracle_mx(layer, x, ids, w)
+    M, k, d, I = wl.M, wl.k, wl.d, wl.I
+    L = moe.grouped_workspace_layout(M, k, d, I, b, aligned[0].numel())
+    npp = int(aligned[2].item())
+    srt = aligned[0].cpu().numpy()[:npp]
+    hq = ws[L["hq"]:L["hq"] + npp * I].cpu().numpy().reshape(npp, I)
+    hs = _unswizzle_hs(ws, L, aligned, b, I)
+    valid = srt < M * k
+    routes = srt[valid]
+    g_q, g_s = hq[valid], hs[valid]
+    o_q, o_s = ref["hq"][routes], ref["hs"][routes]
+    h = ref["h"][routes]
+    # scales: equal unless the block's exact amax sits within 1e-5 of a power of two
+    amax = np.abs(h.reshape(len(routes), I // 32, 32)).max(-1)
+    near_pow2 = np.abs(np.log2(np.where(amax > 0, amax, 1.0)) % 1.0)
+    near_pow2 = np.minimum(near_pow2, 1 - near_pow2) < 2e-5
+    assert np.all((g_s == o_s) | near_pow2)
+    # codes: equal unless the exact scaled value is within 1e-5 of a rounding boundary
+    grid = rd.e4m3_table()
+    X = o_s.astype(np.int64) - 127
+    u = np.abs(h) / np.ldexp(1.0, np.repeat(X, 32, axis=1))
+    pos = grid[:127]
+    idx = np.clip(np.searchsorted(pos, u), 1, 126)
+    mid = (pos[idx - 1] + pos[idx]) / 2
+    near_tie = np.abs(u - mid) <= 1e-5 * np.maximum(u, 1e-30)
+    same_scale = np.repeat(g_s == o_s, 32, axis=1)
+    ok = (g_q == o_q) | near_tie | ~same_scale
+    assert ok.all(), f"{int((~ok).sum())} h codes differ away from rounding boundaries"
+
+
+@pytest.mark.parametrize("M,routing,b", [(64, "uniform", 16), (512, "uniform", 32), (512, "zipf", 64),
+                                         (128, "uniform", 128), (300, "uniform", 256)])
+def test_grouped_decode_shapes(M, routing, b):
+    wl = inputs.Workload(f"grouped_m{M}", M=M, d=2048, I=768, E=128, k=8, routing=routing, seed=11)
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    y, ws, aligned = _run(layer, sfa13, sfa2, x, ids, w, b, out_dtype=torch.bfloat16)
+    # the oracle on a sample of tokens (tokens are independent)
+    rng = np.random.default_rng(M)
+    tok = np.sort(rng.choice(M, size=min(M, 24), replace=False))
+    w13, w2 = layer.oracle_weights(np.unique(ids[tok]))
+    ref = oracle.moe_layer(gs.x_exact(x)[tok], ids[tok], w[tok].astype(np.float64), wl.E, w13, w2,
+                           mode=oracle.MODE_MX)["y"]
+    gs.assert_layer_close(y[torch.from_numpy(tok).cuda()], ref)
+
+
+def test_grouped_invalid_ids_and_repeat_bits():
+    wl, b = inputs.TINY, 16
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    ids = ids.copy()
+    ids[2, 3] = -5
+    ids[7, 0] = wl.E + 3
+    y1, ws1, al = _run(layer, sfa13, sfa2, x, ids, w, b)
+    ref = _oracle_mx(layer, x, ids, w)
+    gs.assert_layer_close(y1, ref["y"])
+    digests = {hashlib.sha256(_run(layer, sfa13, sfa2, x, ids, w, b)[0].cpu().numpy().tobytes()).hexdigest()
+               for _ in range(5)}
+    assert len(digests) == 1
+
+
+def test_grouped_rows_independent_of_block_membership():
+    """A valid but non-canonical alignment (two routes of one expert swapped
+    across a block boundary, as in the packed-AWQ study's cross-block
+    intervention) must give bit-identical per-route results: here the
+    reduction schedule never depends on membership."""
+    wl = inputs.Workload("grouped_membership", M=64, d=512, I=256, E=8, k=2, seed=13)
+    b = 8
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    tid = torch.from_numpy(ids).cuda()
+    aligned = moe.moe_align_block_size(tid, wl.E, b)
+    _, ws_a, _ = _run(layer, sfa13, sfa2, x, ids, w, b, aligned=aligned)
+    srt = aligned[0].cpu().numpy().copy()
+    ex = aligned[1].cpu().numpy()
+    npp = int(aligned[2].item())
+    # find an expert with >= 2 blocks and swap a route of its first block with one of its second
+    e = next(e for e in range(wl.E) if np.sum(ex == e) >= 2)
+    blocks = np.nonzero(ex == e)[0]
+    i0, i1 = blocks[0] * b, blocks[1] * b
+    assert srt[i0] < wl.M * wl.k and srt[i1] < wl.M * wl.k
+    srt[i0], srt[i1] = srt[i1], srt[i0]
+    swapped = (torch.from_numpy(srt).cuda(), aligned[1], aligned[2])
+    _, ws_b, _ = _run(layer, sfa13, sfa2, x, ids, w, b, aligned=swapped)
+    L = moe.grouped_workspace_layout(wl.M, wl.k, wl.d, wl.I, b, srt.size)
+    mk = wl.M * wl.k
+    yr_a = ws_a[L["yr"]:L["yr"] + mk * wl.d * 4].view(torch.float32).cpu().numpy()
+    yr_b = ws_b[L["yr"]:L["yr"] + mk * wl.d * 4].view(torch.float32).cpu().numpy()
+    assert np.array_equal(yr_a, yr_b)
+
+
+def test_grouped_compute_probe_sampled():
+    """16384 tokens (about 1024 rows per expert), checked on sampled tokens."""
+    wl = inputs.Workload("grouped_probe", M=16384, d=2048, I=768, E=128, k=8, seed=17)
+    b = 128
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    y, ws, aligned = _run(layer, sfa13, sfa2, x, ids, w, b, out_dtype=torch.bfloat16)
+    tok = np.sort(np.random.default_rng(5).choice(wl.M, size=16, replace=False))
+    w13, w2 = layer.oracle_weights(np.unique(ids[tok]))
+    ref = oracle.moe_layer(gs.x_exact(x)[tok], ids[tok], w[tok].astype(np.float64), wl.E, w13, w2,
+                           mode=oracle.MODE_MX)["y"]
+    gs.assert_layer_close(y[torch.from_numpy(tok).cuda()], ref)

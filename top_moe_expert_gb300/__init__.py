@@ -57,6 +57,12 @@ _PROTOS = {
     "moe_ffn_decode_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
     "moe_ffn_decode": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                               ctypes.POINTER(moe_weights_t), _P, _I32, _P, _SZ, _P, _P]),
+    "moe_grouped_prepare_size": (_I32, [ctypes.POINTER(moe_weights_t), ctypes.POINTER(moe_weights_t), _P, _P]),
+    "moe_grouped_prepare": (_I32, [ctypes.POINTER(moe_weights_t), ctypes.POINTER(moe_weights_t), _P, _P, _P]),
+    "moe_ffn_grouped_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P]),
+    "moe_ffn_grouped": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
+                               ctypes.POINTER(moe_weights_t), _P, _P, _P, _P, _P, _I32, _I32, _P, _I32,
+                               _P, _SZ, _P, _P]),
     "moe_ffn_decode_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                                       ctypes.POINTER(moe_weights_t), _P, _I32, _P, _P]),
 }
@@ -245,4 +251,71 @@ def moe_ffn_decode_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torc
     _check(lib().moe_ffn_decode_noalloc(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
                                         ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype],
                                         _ptr(dev_status), _stream(stream)), "moe_ffn_decode_noalloc")
+    return y
+
+
+# ---------------------------------------------------------------- grouped path
+
+def moe_grouped_prepare(w13: Weights, w2: Weights, stream=None):
+    """Scale atoms of both projections in the tensor-core layout."""
+    a, b = w13.c_struct(), w2.c_struct()
+    n13, n2 = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().moe_grouped_prepare_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(n13), ctypes.byref(n2)),
+           "moe_grouped_prepare_size")
+    sfa13 = torch.empty(n13.value, dtype=torch.uint8, device=w13.q.device)
+    sfa2 = torch.empty(n2.value, dtype=torch.uint8, device=w13.q.device)
+    _check(lib().moe_grouped_prepare(ctypes.byref(a), ctypes.byref(b), _ptr(sfa13), _ptr(sfa2), _stream(stream)),
+           "moe_grouped_prepare")
+    return sfa13, sfa2
+
+
+def _round256(n):
+    return (n + 255) // 256 * 256
+
+
+def grouped_workspace_layout(M, k, d, I, b, cap_rows):
+    """Byte offsets of Xq, Xs, Hq, Hs, Yr inside the grouped workspace (the
+    layout include/moe_ffn.h documents) and the total."""
+    n_mma = (b + 15) // 16 * 16
+    nsf = (n_mma + 127) // 128
+    cap_blocks = cap_rows // b
+    off, out = 0, {}
+    for name, size in (("xq", cap_rows * d), ("xs", cap_blocks * (d // 128) * nsf * 512),
+                       ("hq", cap_rows * I), ("hs", cap_blocks * (I // 128) * nsf * 512),
+                       ("yr", M * k * d * 4)):
+        out[name] = off
+        off += _round256(size)
+    out["total"] = off
+    out["nsf"] = nsf
+    return out
+
+
+def moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows, ctypes.byref(n)),
+           "moe_ffn_grouped_workspace_size")
+    return n.value
+
+
+def moe_ffn_grouped(x, topk_ids, topk_w, w13: Weights, w2: Weights, sfa13, sfa2, aligned, b: int,
+                    out_dtype=torch.bfloat16, y=None, ws=None, dev_status=None, stream=None):
+    """Expert-centric grouped path; `aligned` = (sorted_route_ids,
+    expert_ids, num_rows_post_pad) from moe_align_block_size with the same b."""
+    for t, nm in ((x, "x"), (topk_ids, "topk_ids"), (topk_w, "topk_w")):
+        _dev(t, nm)
+    M, d = x.shape
+    k = topk_ids.shape[1]
+    I = w2.K
+    sorted_ids, expert_ids, npp = aligned
+    cap_rows = sorted_ids.numel()
+    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
+    if ws is None:
+        ws = torch.empty(moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows), dtype=torch.uint8,
+                         device=x.device)
+    a, bb = w13.c_struct(), w2.c_struct()
+    _check(lib().moe_ffn_grouped(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                 ctypes.byref(a), ctypes.byref(bb), _ptr(sfa13), _ptr(sfa2),
+                                 _ptr(sorted_ids), _ptr(expert_ids), _ptr(npp), b, cap_rows,
+                                 _ptr(y), _DT[y.dtype], _ptr(ws), ws.numel(), _ptr(dev_status),
+                                 _stream(stream)), "moe_ffn_grouped")
     return y

@@ -1,0 +1,569 @@
+// grouped.cu -- expert-centric grouped path for larger batches (MXFP8).
+//
+// "Hardware-Native Joint Sparse-Quantization for Trillion-Scale MoE"
+// (arXiv 2610.02241), Sec. 3.4 and App. D.1: a routed MoE layer evaluates
+// the expert products Y_e = X_e W_e^T as one grouped GEMM; the weights go on
+// the MMA's left operand (Y_e^T = W_e X_e^T), which needs no copy because
+// row-major X_e is the column-major B operand; activations are quantized at
+// run time into 32-element scale blocks before the first GEMM, and the
+// SwiGLU output is requantized for the second.  Rows are the aligned routes
+// of "Route-Block Membership Selects Packed-AWQ Arithmetic" (stable
+// construction), one MMA N-tile per MoE block of b rows.
+//
+// Kernels (one CTA per SM for the GEMMs, persistent over tiles):
+//   act_quant_kernel : x[t] of every aligned row -> MXFP8 codes + E8M0 atoms
+//   gemm_kernel<1>   : [g;u] = W13_e Xq^T on tcgen05 kind::mxf8f6f4 with
+//                      block scaling; epilogue h = SiLU(g) * u -> MXFP8
+//   gemm_kernel<2>   : W2_e Hq^T; epilogue Yr[route] = w_route * acc
+//   combine_kernel   : y[t] = sum over slots j (in order) of Yr[t*k + j]
+// K-reduction order: every output element accumulates its K-tiles in
+// ascending order in one TMEM accumulator; no split-K, no atomics, so the
+// bits of a route's row do not depend on its block membership or the grid.
+//
+// GEMM roles: warp 0 issues TMA (operand tiles, 128-byte swizzled) and bulk
+// copies (scale atoms) into a 4-stage ring; warp 1 owns TMEM and issues
+// tcgen05.cp (scales -> TMEM) and tcgen05.mma from one thread; warps 2..5
+// drain the TMEM accumulator with tcgen05.ld.  Every mbarrier wait is
+// bounded; an expired wait records MOE_ERR_TIMEOUT in dev_status[1].
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;          // 6 warps
+constexpr uint32_t kTmemCols = 512;    // accumulator: columns 0..255; scales from 256
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct Args {
+    const uint8_t *sfa;       // A scale atoms  [E][n_mt][KT][512]
+    const uint8_t *sfb;       // B scale atoms  [cap_blocks][KT][nsf][512]
+    const int32_t *expert_ids;
+    const int32_t *npp;       // num_rows_post_pad
+    const int32_t *sorted;    // sorted_route_ids
+    const float *wts;         // topk_w flattened [MK]
+    uint8_t *hq;              // kind 1: [cap_rows][I] codes
+    uint8_t *hs;              // kind 1: [cap_blocks][I/128][nsf][512] atoms
+    float *yr;                // kind 2: [MK][d]
+    int32_t *dev_status;
+    int b, n_mma, nsf, n_mt, KT, I, d, MK;
+    int a_rows;               // rows of one expert in the A tensor (2I or d)
+};
+
+// Scale-atom byte offset of (row m of a 128-row group, k-block kb of 4):
+// 32 rows x 16 bytes; row m0 = m % 32 holds, for each 32-row group
+// m1 = m / 32, the four k-blocks' bytes.  tcgen05.cp .32x128b.warpx4 copies
+// it into TMEM (4 columns, every 32-lane quadrant).
+__host__ __device__ __forceinline__ int atom_off(int m, int kb) { return (m & 31) * 16 + (m >> 5) * 4 + kb; }
+
+__device__ __forceinline__ int mx_exp(uint32_t amax_bits)
+{
+    const int ef = static_cast<int>((amax_bits >> 23) & 0xFFu);
+    if (ef == 0)
+        return -127;
+    int X = ef - 127 - 8;
+    return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+__device__ __forceinline__ float mx_inv(int X)
+{
+    return X <= 126 ? __uint_as_float(static_cast<uint32_t>(127 - X) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t to_e4m3(float u)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(u));
+    return r & 0xFFu;
+}
+
+// ---------------------------------------------------------------- act quant
+// One warp per (aligned row, 32-element block): lane = element.
+__global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__restrict__ x, int d, int k, int MK,
+                                                        const int32_t *__restrict__ sorted,
+                                                        const int32_t *__restrict__ npp, int b, int nsf,
+                                                        uint8_t *__restrict__ xq, uint8_t *__restrict__ xs)
+{
+    const int lane = threadIdx.x & 31;
+    const int rows = *npp;
+    const int nblk = d / 32, KT = d / 128;
+    const int64_t total = static_cast<int64_t>(rows) * nblk;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += nw) {
+        const int rho = static_cast<int>(w / nblk), blk = static_cast<int>(w % nblk);
+        const int r = sorted[rho];
+        float v = 0.f;
+        if (r < MK)
+            v = __bfloat162float(x[static_cast<int64_t>(r / k) * d + blk * 32 + lane]);
+        const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+        const int X = mx_exp(amax);
+        xq[static_cast<int64_t>(rho) * d + blk * 32 + lane] = static_cast<uint8_t>(to_e4m3(v * mx_inv(X)));
+        if (lane == 0) {
+            const int jb = rho / b, m = rho % b;
+            xs[((static_cast<int64_t>(jb) * KT + blk / 4) * nsf + m / 128) * 512 + atom_off(m & 127, blk & 3)] =
+                static_cast<uint8_t>(X + 127);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- prepare
+// A-operand scale atoms of all experts.  kind 1 (W13, N = 2I): m-tile mt
+// holds gate rows 64mt..64mt+63 then up rows I+64mt..; kind 2 (W2, N = d):
+// rows 128mt..128mt+127.
+__global__ void prepare_sfa_kernel(const uint8_t *__restrict__ s, int E, int N, int K, int kind, int I,
+                                   uint8_t *__restrict__ atoms)
+{
+    const int KT = K / 128, n_mt = kind == 1 ? I / 64 : N / 128;
+    const int64_t total = static_cast<int64_t>(E) * n_mt * KT * 512;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int byte = static_cast<int>(i % 512);
+        const int64_t atom = i / 512;
+        const int kt = static_cast<int>(atom % KT);
+        const int mt = static_cast<int>((atom / KT) % n_mt);
+        const int e = static_cast<int>(atom / (static_cast<int64_t>(KT) * n_mt));
+        // invert atom_off: byte = m0*16 + m1*4 + kb
+        const int m0 = byte / 16, m1 = (byte % 16) / 4, kb = byte % 4;
+        const int m = m1 * 32 + m0;
+        int row;
+        if (kind == 1)
+            row = m < 64 ? 64 * mt + m : I + 64 * mt + (m - 64);
+        else
+            row = 128 * mt + m;
+        atoms[i] = s[(static_cast<int64_t>(e) * N + row) * (K / 32) + kt * 4 + kb];
+    }
+}
+
+// ---------------------------------------------------------------- the GEMM
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 1024-byte aligned base for the 128-byte swizzled tiles
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int NB = a.n_mma * 128;                                  // B tile bytes
+    const int stage_bytes = (16384 + NB + 512 + a.nsf * 512 + 1023) & ~1023;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * stage_bytes);
+    const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kStages;
+    const uint32_t accf = full0 + 16 * kStages, acce = accf + 8, fin = acce + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 3);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *ubuf = reinterpret_cast<float *>(tmem_slot + 4);        // [2][32][33]
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, 1);
+        }
+        tc::mbar_init(accf, 1);
+        tc::mbar_init(acce, 4);
+        tc::mbar_init(fin, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmA);
+        tc::prefetch_tmap(&tmB);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_blocks = *a.npp / a.b;
+    const int total = n_blocks * a.n_mt;
+    const int KT = a.KT;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0, issued = 0;
+            uint32_t ph = 0;
+            const uint32_t tx = 16384u + NB + 512u + a.nsf * 512u;
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                const int jb = t / a.n_mt, mt = t % a.n_mt;
+                const int e = a.expert_ids[jb];
+                for (int kt = 0; kt < KT; ++kt, ++issued) {
+                    if (!tc::mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, kWaitNs))
+                        break;
+                    uint8_t *st = smem + s * stage_bytes;
+                    const uint32_t fb = full0 + 8 * s;
+                    tc::mbar_arrive_expect_tx(fb, tx);
+                    const int x = kt * 128;
+                    if (KIND == 1) {
+                        tc::tma_load_2d(tc::smem_u32(st), &tmA, x, e * a.a_rows + 64 * mt, fb);
+                        tc::tma_load_2d(tc::smem_u32(st + 8192), &tmA, x, e * a.a_rows + a.I + 64 * mt, fb);
+                    } else {
+                        tc::tma_load_2d(tc::smem_u32(st), &tmA, x, e * a.a_rows + 128 * mt, fb);
+                    }
+                    tc::tma_load_2d(tc::smem_u32(st + 16384), &tmB, x, jb * a.b, fb);
+                    tc::bulk_load(tc::smem_u32(st + 16384 + NB),
+                                  a.sfa + ((static_cast<int64_t>(e) * a.n_mt + mt) * KT + kt) * 512, 512, fb);
+                    tc::bulk_load(tc::smem_u32(st + 16384 + NB + 512),
+                                  a.sfb + (static_cast<int64_t>(jb) * KT + kt) * a.nsf * 512, a.nsf * 512, fb);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // every issued copy must land before the CTA may finish
+            volatile int never = 0;
+            const int n = issued < kStages ? issued : kStages;
+            for (int i = 1; i <= n; ++i) {
+                int st = s - i;
+                uint32_t pp = ph;
+                if (st < 0) {
+                    st += kStages;
+                    pp ^= 1u;
+                }
+                tc::mbar_wait(full0 + 8 * st, pp, &never, kWaitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, aph = 0;
+            bool any = false;
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                if (!tc::mbar_wait(acce, aph ^ 1u, abort_flag, kWaitNs))
+                    break;
+                tc::tc_fence_after();
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!tc::mbar_wait(full0 + 8 * s, ph, abort_flag, kWaitNs))
+                        break;
+                    tc::tc_fence_after();
+                    const uint32_t sa = tc::smem_u32(smem + s * stage_bytes);
+                    const uint32_t sb = sa + 16384;
+                    const uint32_t ssfa = sb + NB, ssfb = ssfa + 512;
+                    const uint32_t tsfa = tmem + 256 + s * 16, tsfb = tsfa + 4;
+                    tc::tc_cp_32x128b_x4(tsfa, tc::smem_desc(ssfa, 0, 128, tc::kLayoutNone));
+                    for (int q = 0; q < a.nsf; ++q)
+                        tc::tc_cp_32x128b_x4(tsfb + 4 * q, tc::smem_desc(ssfb + 512 * q, 0, 128, tc::kLayoutNone));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = tc::smem_desc(sa + 32 * kk, 16, 1024, tc::kLayoutSw128);
+                        const uint64_t bd = tc::smem_desc(sb + 32 * kk, 16, 1024, tc::kLayoutSw128);
+                        tc::mma_mxf8(tmem, ad, bd, tc::idesc_mxf8(128, a.n_mma, kk, kk), tsfa, tsfb,
+                                     (kt | kk) != 0 ? 1u : 0u);
+                    }
+                    tc::tc_commit(empty0 + 8 * s);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                tc::tc_commit(accf);
+                aph ^= 1u;
+                any = true;
+            }
+            // all MMAs of this CTA complete before TMEM is released
+            tc::tc_commit(fin);
+            volatile int never = 0;
+            tc::mbar_wait(fin, 0, &never, kWaitNs);
+            (void)any;
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                       // TMEM lane quadrant
+        const int etid = threadIdx.x - 64;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const int jb = t / a.n_mt, mt = t % a.n_mt;
+            if (!tc::mbar_wait(accf, aph, abort_flag, kWaitNs) && a.dev_status)
+                atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+            tc::tc_fence_after();
+            const int rho0 = jb * a.b;
+            for (int c0 = 0; c0 < a.b; c0 += 32) {
+                uint32_t v[32];
+                tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+                tc::tmem_ld_wait();
+                const int ncol = min(32, a.b - c0);
+                if (KIND == 1) {
+                    // lanes 0..63 of the tile are gate rows, 64..127 up rows
+                    float *ub = ubuf + (q & 1) * 32 * 33;
+                    if (q >= 2)
+                        for (int c = 0; c < 32; ++c)
+                            ub[lane * 33 + c] = __uint_as_float(v[c]);
+                    tc::named_bar(1, 128);
+                    if (q < 2) {
+                        const int n = 64 * mt + 32 * q + lane;       // neuron of this lane
+                        for (int c = 0; c < ncol; ++c) {
+                            const float hval = silu_mul(__uint_as_float(v[c]), ub[lane * 33 + c]);
+                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hval)));
+                            const int X = mx_exp(amax);
+                            const int rho = rho0 + c0 + c;
+                            a.hq[static_cast<int64_t>(rho) * a.I + n] = static_cast<uint8_t>(to_e4m3(hval * mx_inv(X)));
+                            if (lane == 0) {
+                                const int kblk = (64 * mt + 32 * q) / 32;     // 32-neuron block
+                                const int m = c0 + c;
+                                a.hs[((static_cast<int64_t>(jb) * (a.I / 128) + kblk / 4) * a.nsf + m / 128) * 512 +
+                                     atom_off(m & 127, kblk & 3)] = static_cast<uint8_t>(X + 127);
+                            }
+                        }
+                    }
+                    tc::named_bar(1, 128);
+                } else {
+                    const int o = 128 * mt + 32 * q + lane;          // output row of this lane
+                    for (int c = 0; c < ncol; ++c) {
+                        const int r = a.sorted[rho0 + c0 + c];
+                        if (r < a.MK)
+                            a.yr[static_cast<int64_t>(r) * a.d + o] = a.wts[r] * __uint_as_float(v[c]);
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive(acce);
+            aph ^= 1u;
+        }
+        (void)etid;
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- combine
+template <typename YT>
+__global__ void combine_kernel(const float *__restrict__ yr, const int32_t *__restrict__ ids, int M, int k, int d,
+                               int E, YT *__restrict__ y)
+{
+    const int64_t total = static_cast<int64_t>(M) * d;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(i / d), o = static_cast<int>(i % d);
+        float s = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int e = ids[t * k + j];
+            if (e >= 0 && e < E)
+                s += yr[static_cast<int64_t>(t * k + j) * d + o];
+        }
+        if constexpr (sizeof(YT) == 4)
+            y[i] = s;
+        else
+            y[i] = __float2bfloat16_rn(s);
+    }
+}
+
+// ---------------------------------------------------------------- host helpers
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D uint8 tensor [rows][inner] (row stride = inner bytes), box
+// 128 bytes x box_rows, 128-byte swizzle.
+static bool tmap_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int sm_count()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+struct WsLayout {
+    size_t xq, xs, hq, hs, yr, total;
+};
+
+static WsLayout ws_layout(int M, int k, int d, int I, int b, int cap_rows)
+{
+    const int n_mma = (b + 15) / 16 * 16;
+    const int nsf = (n_mma + 127) / 128;
+    const int cap_blocks = cap_rows / b;
+    WsLayout L;
+    size_t off = 0;
+    L.xq = off;
+    off += ws_round(static_cast<size_t>(cap_rows) * d);
+    L.xs = off;
+    off += ws_round(static_cast<size_t>(cap_blocks) * (d / 128) * nsf * 512);
+    L.hq = off;
+    off += ws_round(static_cast<size_t>(cap_rows) * I);
+    L.hs = off;
+    off += ws_round(static_cast<size_t>(cap_blocks) * (I / 128) * nsf * 512);
+    L.yr = off;
+    off += ws_round(static_cast<size_t>(M) * k * d * sizeof(float));
+    L.total = off;
+    return L;
+}
+
+}  // namespace gg
+}  // namespace moe
+
+using namespace moe;
+using namespace moe::gg;
+
+MOE_API moe_status_t moe_grouped_prepare_size(const moe_weights_t *w13, const moe_weights_t *w2, size_t *sfa13_bytes,
+                                              size_t *sfa2_bytes)
+{
+    if (!w13 || !w2 || !sfa13_bytes || !sfa2_bytes || w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8)
+        return MOE_ERR_INVALID_ARG;
+    const int I = w2->K, d = w13->K, E = w13->E;
+    if (w13->N != 2 * I || w2->N != d || d % 128 || I % 128)
+        return MOE_ERR_UNSUPPORTED;
+    *sfa13_bytes = static_cast<size_t>(E) * (I / 64) * (d / 128) * 512;
+    *sfa2_bytes = static_cast<size_t>(E) * (d / 128) * (I / 128) * 512;
+    return MOE_OK;
+}
+
+MOE_API moe_status_t moe_grouped_prepare(const moe_weights_t *w13, const moe_weights_t *w2, void *sfa13, void *sfa2,
+                                         void *stream)
+{
+    size_t b13, b2;
+    moe_status_t st = moe_grouped_prepare_size(w13, w2, &b13, &b2);
+    if (st != MOE_OK)
+        return st;
+    if (!w13->scale || !w2->scale || !sfa13 || !sfa2)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    prepare_sfa_kernel<<<1024, 256, 0, s>>>(static_cast<const uint8_t *>(w13->scale), w13->E, w13->N, w13->K, 1,
+                                            w2->K, static_cast<uint8_t *>(sfa13));
+    if (launch_status() != MOE_OK)
+        return MOE_ERR_CUDA;
+    prepare_sfa_kernel<<<1024, 256, 0, s>>>(static_cast<const uint8_t *>(w2->scale), w2->E, w2->N, w2->K, 2, w2->K,
+                                            static_cast<uint8_t *>(sfa2));
+    return launch_status();
+}
+
+MOE_API moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_t d, int32_t I, int32_t b,
+                                                    int32_t cap_rows, size_t *bytes)
+{
+    if (M < 0 || k < 1 || d < 1 || I < 1 || b < 1 || cap_rows < 0 || !bytes)
+        return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(M, k, d, I, b, cap_rows).total;
+    return MOE_OK;
+}
+
+MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d, const int32_t *topk_ids,
+                                     const float *topk_w, int32_t k, const moe_weights_t *w13,
+                                     const moe_weights_t *w2, const void *sfa13, const void *sfa2,
+                                     const int32_t *sorted_route_ids, const int32_t *expert_ids,
+                                     const int32_t *num_rows_post_pad, int32_t b, int32_t cap_rows, void *y,
+                                     int32_t ydt, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream)
+{
+    if (M < 0 || d < 1 || k < 1 || !w13 || !w2)
+        return MOE_ERR_INVALID_ARG;
+    if (w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8 || xdt != MOE_BF16)
+        return MOE_ERR_UNSUPPORTED;
+    if (ydt != MOE_BF16 && ydt != MOE_FP32)
+        return MOE_ERR_UNSUPPORTED;
+    const int I = w2->K, E = w13->E;
+    if (w13->N != 2 * I || w13->K != d || w2->N != d || w2->E != E || E < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (d % 128 || I % 128 || b < 8 || b > 256 || b % 8)
+        return MOE_ERR_UNSUPPORTED;
+    const int64_t mk = static_cast<int64_t>(M) * k;
+    int32_t need_rows, need_blocks;
+    if (moe_align_capacity(M, k, E, b, &need_rows, &need_blocks) != MOE_OK)
+        return MOE_ERR_UNSUPPORTED;
+    if (cap_rows < need_rows || cap_rows % b)
+        return MOE_ERR_CAPACITY;
+    if (M == 0)
+        return MOE_OK;
+    if (!x || !topk_ids || !topk_w || !y || !sfa13 || !sfa2 || !sorted_route_ids || !expert_ids ||
+        !num_rows_post_pad || !w13->q || !w2->q)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(w13->q, 16) || !aligned(w2->q, 16) || !aligned(sfa13, 16) || !aligned(sfa2, 16))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(M, k, d, I, b, cap_rows);
+    if (!ws || ws_bytes < L.total || !aligned(ws, 256))
+        return MOE_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint8_t *xq = w + L.xq, *xs = w + L.xs, *hq = w + L.hq, *hs = w + L.hs;
+    float *yr = reinterpret_cast<float *>(w + L.yr);
+    const int n_mma = (b + 15) / 16 * 16;
+    const int nsf = (n_mma + 127) / 128;
+    cudaStream_t s = as_stream(stream);
+
+    // tensor maps: A = weights [E*N][K], B = activations [cap_rows][K]
+    CUtensorMap tA1, tB1, tA2, tB2;
+    if (!tmap_u8(&tA1, w13->q, d, static_cast<uint64_t>(E) * 2 * I, 64) ||
+        !tmap_u8(&tB1, xq, d, cap_rows, n_mma) ||
+        !tmap_u8(&tA2, w2->q, I, static_cast<uint64_t>(E) * d, 128) ||
+        !tmap_u8(&tB2, hq, I, cap_rows, n_mma))
+        return MOE_ERR_CUDA;
+
+    act_quant_kernel<<<sm_count() * 8, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk),
+                                                    sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs);
+    if (launch_status() != MOE_OK)
+        return MOE_ERR_CUDA;
+
+    const int stage_bytes = (16384 + n_mma * 128 + 512 + nsf * 512 + 1023) & ~1023;
+    const size_t smem = 1024 + kStages * stage_bytes + 128 + 2 * 32 * 33 * sizeof(float);
+    static std::once_flag attr_once;
+    static bool attr_ok = false;
+    std::call_once(attr_once, [] {
+        attr_ok = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+                      cudaSuccess &&
+                  cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+                      cudaSuccess;
+    });
+    if (!attr_ok || smem > 227 * 1024)
+        return MOE_ERR_CUDA;
+    const int grid = sm_count();
+
+    Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
+            hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I};
+    gemm_kernel<1><<<grid, kThreads, smem, s>>>(tA1, tB1, a1);
+    if (launch_status() != MOE_OK)
+        return MOE_ERR_CUDA;
+    Args a2{static_cast<const uint8_t *>(sfa2), hs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
+            nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d};
+    gemm_kernel<2><<<grid, kThreads, smem, s>>>(tA2, tB2, a2);
+    if (launch_status() != MOE_OK)
+        return MOE_ERR_CUDA;
+    const int64_t n = static_cast<int64_t>(M) * d;
+    const int cb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    if (ydt == MOE_FP32)
+        combine_kernel<float><<<cb, 256, 0, s>>>(yr, topk_ids, M, k, d, E, static_cast<float *>(y));
+    else
+        combine_kernel<__nv_bfloat16><<<cb, 256, 0, s>>>(yr, topk_ids, M, k, d, E, static_cast<__nv_bfloat16 *>(y));
+    return launch_status();
+}
