@@ -55,6 +55,9 @@ def workload_from_name(name: str):
         return inputs.LARGE_M1
     if name == "large_m8":
         return inputs.LARGE_M8
+    if name == "probe_m16384":
+        return inputs.Workload("grouped_probe_m16384_d2048_i768_e128_k8", M=16384, d=2048, I=768, E=128, k=8,
+                               seed=2)
     if name.startswith("sweep_m"):
         rest = name[len("sweep_m"):]
         routing = "zipf" if rest.endswith("_zipf") else "uniform"
@@ -72,6 +75,16 @@ def step_bytes(wl, ids: np.ndarray) -> int:
     activations read (x, router logits) and the output written (bf16 y)."""
     distinct = len(np.unique(ids[(ids >= 0) & (ids < wl.E)]))
     return distinct * expert_bytes(wl) + wl.M * wl.d * 2 + wl.M * wl.E * 4 + wl.M * wl.d * 2
+
+
+def measured_mxfp8_tflops():
+    """Dense MXFP8 tensor peak: the measured bf16 burst peak times the
+    nominal fp8:bf16 ratio of 2 (4.5 vs 2.25 PFLOP/s)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return 2.0 * float(json.load(open(p))["bf16_tflops"]), "measured bf16 x 2"
+    except Exception:
+        return 2.0 * 1900.0, "fallback bf16 x 2"
 
 
 def measured_peak():
@@ -150,20 +163,32 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 def decode_src_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cu", "decode_fused.cu", "decode_stream.cu", "topk.cu", "common.cuh", "tc.cuh"):
+    for f in ("decode.cu", "decode_fused.cu", "decode_stream.cu", "topk.cu", "common.cuh", "tc.cuh", "grouped.cu",
+              "align.cu"):
         h.update(open(os.path.join(ROOT, "top_moe_expert_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
 
 # ------------------------------------------------------------------ our arm
 
-class DecodeStep:
-    """Device-resident workload + a CUDA graph of one step (routing + layer)."""
+def grouped_block(wl) -> int:
+    """MoE block size b of the grouped path: the expected rows per expert,
+    rounded up to a power of two within [16, 128]."""
+    rows = max(1, wl.M * wl.k // wl.E)
+    b = 16
+    while b < rows and b < 128:
+        b *= 2
+    return b
 
-    def __init__(self, wl, nsteps: int, device):
+
+class DecodeStep:
+    """Device-resident workload + a CUDA graph of one step: top-k routing and
+    the layer (decode path), or top-k, alignment and the grouped layer."""
+
+    def __init__(self, wl, nsteps: int, device, path: str = "decode"):
         import top_moe_expert_gb300 as moe
         from top_moe_expert_gb300 import inputs
-        self.moe, self.wl, self.dev = moe, wl, device
+        self.moe, self.wl, self.dev, self.path = moe, wl, device, path
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
         self.q13 = torch.empty((E, 2 * I, d), dtype=torch.uint8, device=device)
         self.s13 = torch.empty((E, 2 * I, d // 32), dtype=torch.uint8, device=device)
@@ -174,16 +199,23 @@ class DecodeStep:
             moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), self.q2[e], self.s2[e])
         self.w13 = moe.Weights(moe.MOE_W_MXFP8, self.q13, self.s13)
         self.w2 = moe.Weights(moe.MOE_W_MXFP8, self.q2, self.s2)
-        # small batches take the single-pass kernel, which reads the down
-        # projection neuron-major: pack it once (same bytes, K-outer order)
-        self.fused = M <= 4 and d % 1024 == 0
-        if self.fused:
-            self.w2 = moe.moe_mxfp8_transpose(self.w2)
-            del self.q2, self.s2
-            torch.cuda.empty_cache()
-        # fresh routing and activations for every step
-        self.logits_host = torch.from_numpy(np.stack([inputs.router_logits(wl, i) for i in range(nsteps)]))
-        self.x_host = torch.stack([inputs.activations(wl, i) for i in range(nsteps)])
+        self.fused = False
+        if path == "grouped":
+            self.b = grouped_block(wl)
+            self.sfa13, self.sfa2 = moe.moe_grouped_prepare(self.w13, self.w2)
+        else:
+            # small batches take the single-pass kernel, which reads the down
+            # projection neuron-major: pack it once (same bytes, K-outer order)
+            self.fused = M <= 4 and d % 1024 == 0
+            if self.fused:
+                self.w2 = moe.moe_mxfp8_transpose(self.w2)
+                del self.q2, self.s2
+                torch.cuda.empty_cache()
+        # fresh routing and activations for every step (large batches cycle
+        # through a pool of distinct steps to bound host memory)
+        self.n_inputs = nsteps if M <= 64 else min(nsteps, 16)
+        self.logits_host = torch.from_numpy(np.stack([inputs.router_logits(wl, i) for i in range(self.n_inputs)]))
+        self.x_host = torch.stack([inputs.activations(wl, i) for i in range(self.n_inputs)])
         self.logits_all = self.logits_host.to(device)
         self.x_all = self.x_host.to(device)
         self.logits = torch.empty((M, E), dtype=torch.float32, device=device)
@@ -191,14 +223,35 @@ class DecodeStep:
         self.ids = torch.empty((M, k), dtype=torch.int32, device=device)
         self.w = torch.empty((M, k), dtype=torch.float32, device=device)
         self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
-        self.ws = torch.empty(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
+        if path == "grouped":
+            cr, cb = moe.moe_align_capacity(M, k, E, self.b)
+            self.aligned = (torch.empty(cr, dtype=torch.int32, device=device),
+                            torch.empty(cb, dtype=torch.int32, device=device),
+                            torch.empty(1, dtype=torch.int32, device=device))
+            na = moe.moe_align_workspace_size(M, k, E, self.b)
+            self.ws_align = torch.empty(max(na, 256), dtype=torch.uint8, device=device) if na else None
+            self.ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, k, d, I, self.b, cr), dtype=torch.uint8,
+                                  device=device)
+        else:
+            self.ws = torch.empty(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device)
         torch.cuda.synchronize()
 
     def launch(self, stream=None):
-        self.moe.moe_topk_softmax(self.logits, self.wl.k, self.ids, self.w, stream=stream)
-        self.moe.moe_ffn_decode(self.x, self.ids, self.w, self.w13, self.w2, y=self.y, ws=self.ws,
-                                stream=stream)
+        moe = self.moe
+        moe.moe_topk_softmax(self.logits, self.wl.k, self.ids, self.w, stream=stream)
+        if self.path == "grouped":
+            moe.moe_align_block_size(self.ids, self.wl.E, self.b, out=self.aligned, ws=self.ws_align, stream=stream)
+            moe.moe_ffn_grouped(self.x, self.ids, self.w, self.w13, self.w2, self.sfa13, self.sfa2, self.aligned,
+                                self.b, y=self.y, ws=self.ws, stream=stream)
+        else:
+            moe.moe_ffn_decode(self.x, self.ids, self.w, self.w13, self.w2, y=self.y, ws=self.ws, stream=stream)
+
+    def launches_per_step(self) -> int:
+        if self.path == "grouped":
+            na = 2 if self.ws_align is not None else 1
+            return 1 + na + 4
+        return 3
 
     def capture(self):
         with torch.cuda.stream(self.stream):
@@ -216,10 +269,38 @@ def host_topk_ids(logits: np.ndarray, k: int) -> np.ndarray:
     return np.argsort(-logits, axis=1, kind="stable")[:, :k]
 
 
+def roofline_obj(st, wl, total_ms, K, total_bytes, world):
+    """Roofline of the step's layer call.  HBM-bound unless the layer's FLOPs
+    at the MXFP8 tensor peak take longer than its bytes at the HBM peak."""
+    peak_gbs, peak_kind = measured_peak()
+    peak_tf, tf_kind = measured_mxfp8_tflops()
+    sec = total_ms * 1e-3
+    flops = 2.0 * wl.M * wl.k * 3 * wl.I * wl.d * K * world
+    t_hbm = total_bytes / (peak_gbs * 1e9)
+    t_mma = flops / (peak_tf * 1e12)
+    if st.path == "grouped":
+        kern = "grouped layer: act_quant + gemm_kernel<1> + gemm_kernel<2> + combine (+ topk, align)"
+    elif st.fused:
+        kern = "decode layer: df::fused_kernel + df::reduce_kernel, PDL-chained (+ topk)"
+    else:
+        kern = "decode layer: ds::gate_up_kernel + ds::down_kernel, PDL-chained (+ topk)"
+    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash())
+    if t_mma > t_hbm:
+        ach = flops / sec / 1e12 / world
+        return {"kernel": kern, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_tf,
+                "peak_kind": tf_kind, "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4), "traffic": traffic,
+                "hbm_frac": round(total_bytes / sec / 1e9 / world / peak_gbs, 4)}
+    ach = total_bytes / sec / 1e9 / world
+    return {"kernel": kern, "bound": "hbm", "achieved": round(ach, 1), "peak": peak_gbs, "peak_kind": peak_kind,
+            "unit": "GB/s", "frac": round(ach / peak_gbs, 4), "traffic": traffic,
+            "tensor_frac": round(flops / sec / 1e12 / world / peak_tf, 4)}
+
+
 def run_ours(args, rank, world, device):
     wl = workload_from_name(args.workload)
     K, W = args.steps, args.warmup
-    st = DecodeStep(wl, K + W, device)
+    path = args.path if args.path != "auto" else ("grouped" if wl.M >= 256 else "decode")
+    st = DecodeStep(wl, K + W, device, path)
     st.capture()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     s = st.stream
@@ -231,8 +312,8 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         for i in range(W):
-            st.x.copy_(st.x_all[i], non_blocking=True)
-            st.logits.copy_(st.logits_all[i], non_blocking=True)
+            st.x.copy_(st.x_all[i % st.n_inputs], non_blocking=True)
+            st.logits.copy_(st.logits_all[i % st.n_inputs], non_blocking=True)
             flush.fill_(float(i))
             st.graph.replay()
     torch.cuda.synchronize()
@@ -248,7 +329,7 @@ def run_ours(args, rank, world, device):
     t_wall0 = time.perf_counter()
     with torch.cuda.stream(s):
         for i in range(K):
-            j = W + i
+            j = (W + i) % st.n_inputs
             st.x.copy_(st.x_all[j], non_blocking=True)
             st.logits.copy_(st.logits_all[j], non_blocking=True)
             flush.fill_(float(j))
@@ -266,13 +347,14 @@ def run_ours(args, rank, world, device):
 
     # bytes of every timed step (distinct experts of that step's routing)
     logits_np = st.logits_host.numpy()
-    bytes_steps = [step_bytes(wl, host_topk_ids(logits_np[W + i], wl.k)) for i in range(K)]
+    bytes_steps = [step_bytes(wl, host_topk_ids(logits_np[(W + i) % st.n_inputs], wl.k)) for i in range(K)]
     total_bytes = float(sum(bytes_steps))
 
     # e2e: the same steps through the public API with host buffers (pinned)
     Ke = min(K, 2000)
-    x_pin = st.x_host[W:W + Ke].pin_memory()
-    l_pin = st.logits_host[W:W + Ke].pin_memory()
+    sel = [(W + i) % st.n_inputs for i in range(Ke)]
+    x_pin = st.x_host[sel].pin_memory() if wl.M <= 64 else st.x_host.pin_memory()
+    l_pin = st.logits_host[sel].pin_memory() if wl.M <= 64 else st.logits_host.pin_memory()
     y_pin = torch.empty((Ke, wl.M, wl.d), dtype=torch.bfloat16).pin_memory()
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
@@ -281,8 +363,9 @@ def run_ours(args, rank, world, device):
         for i in range(Ke):
             flush.fill_(float(i))
             e0[i].record(s)
-            st.x.copy_(x_pin[i], non_blocking=True)
-            st.logits.copy_(l_pin[i], non_blocking=True)
+            pi = i if wl.M <= 64 else sel[i]
+            st.x.copy_(x_pin[pi], non_blocking=True)
+            st.logits.copy_(l_pin[pi], non_blocking=True)
             st.launch(s)
             y_pin[i].copy_(st.y, non_blocking=True)
             e1[i].record(s)
@@ -324,7 +407,9 @@ def run_ours(args, rank, world, device):
         "data": "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
                 "N(0,1) router logits; fresh routing every step)",
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "path": ("single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
+                   "path": ("expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
+                            % st.b if st.path == "grouped" else
+                            "single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
                             else "output-centric decode (topk + gate/up + down)") + ", CUDA graph",
                    "l2": "flushed between timed steps (512 MiB write, outside the timed interval)",
                    "parallelism": f"replicas x{world}"},
@@ -332,23 +417,21 @@ def run_ours(args, rank, world, device):
                 "us_per_layer": round(e2e_ms * 1e3 / Ke, 3), "steps": Ke,
                 "h2d_bytes_per_step": wl.M * wl.d * 2 + wl.M * wl.E * 4,
                 "d2h_bytes_per_step": wl.M * wl.d * 2},
-        "gpu_launches": 3 * K,      # top-k, layer kernel, reduction / down kernel
-        "roofline": {"kernel": ("decode layer: df::fused_kernel + df::reduce_kernel (PDL-chained)" if st.fused
-                               else "decode layer: ds::gate_up_kernel + ds::down_kernel (PDL-chained)"),
-                     "bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak_gbs,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved_gbs / peak_gbs, 4),
-                     "traffic": committed_traffic(f"decode:{wl.name}", decode_src_hash())},
+        "gpu_launches": st.launches_per_step() * K,
+        "roofline": roofline_obj(st, wl, total_ms, K, total_bytes, world),
         "clocks": clocks,
         "wall_s_timed_loop": round(t_wall, 3),
+        "_path": st.path,
     }
     return line
 
 
-def cpu_baseline(wl, device, seconds=12.0):
-    """The oracle, as it stands, on the host cores: full decode steps (top-k
-    + layer) of the same workload, fresh routing per step, until ~`seconds`
-    of timed CPU work.  Expert weights are quantized by the oracle from the
-    same fp32 draws (setup, not timed)."""
+def cpu_baseline(wl, device, path="decode", seconds=12.0):
+    """The oracle, as it stands, on the host cores: steps (top-k + layer) of
+    the same workload with fresh routing, on at most 4 tokens per step,
+    until ~`seconds` of timed CPU work.  The oracle runs in the mode the path
+    computes (exact for decode, block-scaled for grouped).  Expert weights
+    are quantized by the oracle from the same fp32 draws (setup, not timed)."""
     import oracle
     from top_moe_expert_gb300 import inputs
     cache = {}
@@ -359,9 +442,11 @@ def cpu_baseline(wl, device, seconds=12.0):
             cache[(which, e)] = oracle.mxfp8_quantize(f)
         return cache[(which, e)]
 
+    mode = oracle.MODE_MX if path == "grouped" else oracle.MODE_EXACT
+    S = min(wl.M, 4)
     t_total, nbytes, steps = 0.0, 0, 0
     while t_total < seconds and steps < 64:
-        logits = inputs.router_logits(wl, 10_000 + steps)
+        logits = inputs.router_logits(wl, 10_000 + steps)[:S]
         ids, _ = oracle.topk_softmax(logits, wl.k)
         experts = sorted(set(ids.reshape(-1).tolist()))
         slot = np.full(wl.E, -1, dtype=np.int32)
@@ -371,18 +456,18 @@ def cpu_baseline(wl, device, seconds=12.0):
             qs = [expert(which, e) for e in experts]
             ws[which] = {"fmt": "mxfp8", "q": np.stack([q for q, _ in qs]),
                          "s": np.stack([s for _, s in qs]), "slot": slot}
-        x = inputs.activations(wl, 10_000 + steps).to(torch.float64).numpy()
+        x = inputs.activations(wl, 10_000 + steps)[:S].to(torch.float64).numpy()
         t0 = time.perf_counter()
         ids2, w2 = oracle.topk_softmax(logits, wl.k)
-        oracle.moe_layer(x, ids2, w2, wl.E, ws["w13"], ws["w2"])
+        oracle.moe_layer(x, ids2, w2, wl.E, ws["w13"], ws["w2"], mode=mode)
         t_total += time.perf_counter() - t0
-        nbytes += step_bytes(wl, ids)
+        nbytes += len(experts) * expert_bytes(wl) + S * (4 * wl.d + 4 * wl.E)
         steps += 1
-    threads = min(oracle.num_threads(), wl.M)   # the oracle parallelises over tokens
+    threads = min(oracle.num_threads(), S)     # the oracle parallelises over tokens
     return {"value": nbytes / t_total / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{steps} full steps (top-k + layer, binary64) of {wl.name}, "
-                      f"fresh routing each, {t_total:.1f} s timed",
-            "us_per_layer": round(t_total / steps * 1e6, 1)}
+            "sample": f"{steps} steps (top-k + layer, binary64, {'block-scaled' if mode else 'exact'} mode) "
+                      f"of {wl.name} on {S} token(s) each, fresh routing, {t_total:.1f} s timed",
+            "us_per_token": round(t_total / steps / S * 1e6, 1)}
 
 
 def run_reference(args, rank, world):
@@ -446,6 +531,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_m1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "decode", "grouped"])
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -474,7 +560,8 @@ def main():
     line = run_ours(args, rank, world, device)
     if line is not None:
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(workload_from_name(args.workload), device)
+            line["cpu_baseline"] = cpu_baseline(workload_from_name(args.workload), device, line["_path"])
+        line.pop("_path", None)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

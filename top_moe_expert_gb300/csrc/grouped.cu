@@ -84,7 +84,8 @@ __device__ __forceinline__ uint32_t to_e4m3(float u)
 }
 
 // ---------------------------------------------------------------- act quant
-// One warp per (aligned row, 32-element block): lane = element.
+// One warp per aligned row; lane l quantizes 32-element blocks l, l+32, ...
+// with 16-byte loads and stores (the block's amax stays in the lane).
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__restrict__ x, int d, int k, int MK,
                                                         const int32_t *__restrict__ sorted,
                                                         const int32_t *__restrict__ npp, int b, int nsf,
@@ -93,19 +94,43 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__r
     const int lane = threadIdx.x & 31;
     const int rows = *npp;
     const int nblk = d / 32, KT = d / 128;
-    const int64_t total = static_cast<int64_t>(rows) * nblk;
-    const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += nw) {
-        const int rho = static_cast<int>(w / nblk), blk = static_cast<int>(w % nblk);
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int rho = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rho < rows; rho += nw) {
         const int r = sorted[rho];
-        float v = 0.f;
-        if (r < MK)
-            v = __bfloat162float(x[static_cast<int64_t>(r / k) * d + blk * 32 + lane]);
-        const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-        const int X = mx_exp(amax);
-        xq[static_cast<int64_t>(rho) * d + blk * 32 + lane] = static_cast<uint8_t>(to_e4m3(v * mx_inv(X)));
-        if (lane == 0) {
-            const int jb = rho / b, m = rho % b;
+        const int jb = rho / b, m = rho % b;
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(r < MK ? r / k : 0) * d);
+        uint4 *qr = reinterpret_cast<uint4 *>(xq + static_cast<int64_t>(rho) * d);
+        for (int blk = lane; blk < nblk; blk += 32) {
+            float v[32];
+            if (r < MK) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 w = __ldg(xr + blk * 4 + i);
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        v[i * 8 + 2 * j] = __uint_as_float(ww[j] << 16);
+                        v[i * 8 + 2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[i] = 0.f;
+            }
+            uint32_t amax = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                amax = max(amax, __float_as_uint(fabsf(v[i])));
+            const int X = mx_exp(amax);
+            const float inv = mx_inv(X);
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                packed[i] = to_e4m3(v[4 * i] * inv) | (to_e4m3(v[4 * i + 1] * inv) << 8) |
+                            (to_e4m3(v[4 * i + 2] * inv) << 16) | (to_e4m3(v[4 * i + 3] * inv) << 24);
+            qr[blk * 2] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            qr[blk * 2 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
             xs[((static_cast<int64_t>(jb) * KT + blk / 4) * nsf + m / 128) * 512 + atom_off(m & 127, blk & 3)] =
                 static_cast<uint8_t>(X + 127);
         }
@@ -154,18 +179,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int stage_bytes = (16384 + NB + 512 + a.nsf * 512 + 1023) & ~1023;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * stage_bytes);
     const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kStages;
-    const uint32_t accf = full0 + 16 * kStages, acce = accf + 8, fin = acce + 8;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 3);
+    const uint32_t accf0 = full0 + 16 * kStages, acce0 = accf0 + 16, fin = acce0 + 16;   // accf[2], acce[2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *ubuf = reinterpret_cast<float *>(tmem_slot + 4);        // [2][32][33]
+    int *t_route = reinterpret_cast<int *>(ubuf + 2 * 32 * 33);    // [256] routes of the tile's rows
+    float *t_w = reinterpret_cast<float *>(t_route + 256);         // [256] their weights
+    // two accumulator buffers (columns 0 and 128) when a tile fits in 128
+    // columns, so the MMA of the next tile overlaps this tile's epilogue
+    const int nbuf = a.n_mma <= 128 ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(full0 + 8 * s, 1);
             tc::mbar_init(empty0 + 8 * s, 1);
         }
-        tc::mbar_init(accf, 1);
-        tc::mbar_init(acce, 4);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(accf0 + 8 * i, 1);
+            tc::mbar_init(acce0 + 8 * i, 4);
+        }
         tc::mbar_init(fin, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -236,13 +268,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0, aph = 0;
+            int s = 0, ti = 0;
+            uint32_t ph = 0;
             bool any = false;
-            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-                if (!tc::mbar_wait(acce, aph ^ 1u, abort_flag, kWaitNs))
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
+                const int buf = nbuf == 2 ? (ti & 1) : 0;
+                const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
+                if (!tc::mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag, kWaitNs))
                     break;
                 tc::tc_fence_after();
+                const uint32_t acc = tmem + 128 * buf;
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(full0 + 8 * s, ph, abort_flag, kWaitNs))
                         break;
@@ -258,7 +293,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = tc::smem_desc(sa + 32 * kk, 16, 1024, tc::kLayoutSw128);
                         const uint64_t bd = tc::smem_desc(sb + 32 * kk, 16, 1024, tc::kLayoutSw128);
-                        tc::mma_mxf8(tmem, ad, bd, tc::idesc_mxf8(128, a.n_mma, kk, kk), tsfa, tsfb,
+                        tc::mma_mxf8(acc, ad, bd, tc::idesc_mxf8(128, a.n_mma, kk, kk), tsfa, tsfb,
                                      (kt | kk) != 0 ? 1u : 0u);
                     }
                     tc::tc_commit(empty0 + 8 * s);
@@ -267,8 +302,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         ph ^= 1u;
                     }
                 }
-                tc::tc_commit(accf);
-                aph ^= 1u;
+                tc::tc_commit(accf0 + 8 * buf);
                 any = true;
             }
             // all MMAs of this CTA complete before TMEM is released
@@ -281,56 +315,74 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;                       // TMEM lane quadrant
         const int etid = threadIdx.x - 64;
-        uint32_t aph = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        int ti = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
             const int jb = t / a.n_mt, mt = t % a.n_mt;
-            if (!tc::mbar_wait(accf, aph, abort_flag, kWaitNs) && a.dev_status)
+            const int buf = nbuf == 2 ? (ti & 1) : 0;
+            const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
+            const int rho0 = jb * a.b;
+            if (KIND == 2) {
+                // routes and routing weights of the tile's rows, loaded once
+                for (int c = etid; c < a.b; c += 128) {
+                    const int r = a.sorted[rho0 + c];
+                    t_route[c] = r;
+                    t_w[c] = r < a.MK ? a.wts[r] : 0.f;
+                }
+            }
+            if (!tc::mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag, kWaitNs) && a.dev_status)
                 atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
             tc::tc_fence_after();
-            const int rho0 = jb * a.b;
+            tc::named_bar(1, 128);
             for (int c0 = 0; c0 < a.b; c0 += 32) {
                 uint32_t v[32];
-                tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+                tc::tmem_ld_32x32b_x32(tmem + 128 * buf + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
                 tc::tmem_ld_wait();
                 const int ncol = min(32, a.b - c0);
                 if (KIND == 1) {
                     // lanes 0..63 of the tile are gate rows, 64..127 up rows
                     float *ub = ubuf + (q & 1) * 32 * 33;
-                    if (q >= 2)
+                    if (q >= 2) {
+#pragma unroll
                         for (int c = 0; c < 32; ++c)
                             ub[lane * 33 + c] = __uint_as_float(v[c]);
+                    }
                     tc::named_bar(1, 128);
                     if (q < 2) {
                         const int n = 64 * mt + 32 * q + lane;       // neuron of this lane
-                        for (int c = 0; c < ncol; ++c) {
-                            const float hval = silu_mul(__uint_as_float(v[c]), ub[lane * 33 + c]);
-                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hval)));
-                            const int X = mx_exp(amax);
-                            const int rho = rho0 + c0 + c;
-                            a.hq[static_cast<int64_t>(rho) * a.I + n] = static_cast<uint8_t>(to_e4m3(hval * mx_inv(X)));
-                            if (lane == 0) {
-                                const int kblk = (64 * mt + 32 * q) / 32;     // 32-neuron block
-                                const int m = c0 + c;
-                                a.hs[((static_cast<int64_t>(jb) * (a.I / 128) + kblk / 4) * a.nsf + m / 128) * 512 +
-                                     atom_off(m & 127, kblk & 3)] = static_cast<uint8_t>(X + 127);
+                        const int kblk = 2 * mt + q;                  // its 32-neuron block
+                        uint8_t *hrow = a.hq + static_cast<int64_t>(rho0 + c0) * a.I + n;
+                        uint8_t *hsa = a.hs + ((static_cast<int64_t>(jb) * (a.I / 128) + kblk / 4) * a.nsf) * 512;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            if (c < ncol) {
+                                const float hval = silu_mul(__uint_as_float(v[c]), ub[lane * 33 + c]);
+                                const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hval)));
+                                const int X = mx_exp(amax);
+                                hrow[static_cast<int64_t>(c) * a.I] = static_cast<uint8_t>(to_e4m3(hval * mx_inv(X)));
+                                if (lane == 0) {
+                                    const int m = c0 + c;
+                                    hsa[(m / 128) * 512 + atom_off(m & 127, kblk & 3)] = static_cast<uint8_t>(X + 127);
+                                }
                             }
                         }
                     }
                     tc::named_bar(1, 128);
                 } else {
                     const int o = 128 * mt + 32 * q + lane;          // output row of this lane
-                    for (int c = 0; c < ncol; ++c) {
-                        const int r = a.sorted[rho0 + c0 + c];
-                        if (r < a.MK)
-                            a.yr[static_cast<int64_t>(r) * a.d + o] = a.wts[r] * __uint_as_float(v[c]);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        if (c < ncol) {
+                            const int r = t_route[c0 + c];
+                            if (r < a.MK)
+                                a.yr[static_cast<int64_t>(r) * a.d + o] = t_w[c0 + c] * __uint_as_float(v[c]);
+                        }
                     }
                 }
             }
             tc::tc_fence_before();
-            __syncwarp();
+            tc::named_bar(1, 128);                    // t_route / t_w reuse by the next tile
             if (lane == 0)
-                tc::mbar_arrive(acce);
-            aph ^= 1u;
+                tc::mbar_arrive(acce0 + 8 * buf);
         }
         (void)etid;
     }
@@ -530,13 +582,13 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         !tmap_u8(&tB2, hq, I, cap_rows, n_mma))
         return MOE_ERR_CUDA;
 
-    act_quant_kernel<<<sm_count() * 8, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk),
+    act_quant_kernel<<<sm_count() * 4, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk),
                                                     sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs);
     if (launch_status() != MOE_OK)
         return MOE_ERR_CUDA;
 
     const int stage_bytes = (16384 + n_mma * 128 + 512 + nsf * 512 + 1023) & ~1023;
-    const size_t smem = 1024 + kStages * stage_bytes + 128 + 2 * 32 * 33 * sizeof(float);
+    const size_t smem = 1024 + kStages * stage_bytes + 128 + 2 * 32 * 33 * sizeof(float) + 512 * 4;
     static std::once_flag attr_once;
     static bool attr_ok = false;
     std::call_once(attr_once, [] {
