@@ -185,7 +185,7 @@ class DecodeStep:
     """Device-resident workload + a CUDA graph of one step: top-k routing and
     the layer (decode path), or top-k, alignment and the grouped layer."""
 
-    def __init__(self, wl, nsteps: int, device, path: str = "decode"):
+    def __init__(self, wl, nsteps: int, device, path: str = "decode", block: int = 0):
         import top_moe_expert_gb300 as moe
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
@@ -201,7 +201,7 @@ class DecodeStep:
         self.w2 = moe.Weights(moe.MOE_W_MXFP8, self.q2, self.s2)
         self.fused = False
         if path == "grouped":
-            self.b = grouped_block(wl)
+            self.b = block or grouped_block(wl)
             self.sfa13, self.sfa2 = moe.moe_grouped_prepare(self.w13, self.w2)
         else:
             # small batches take the single-pass kernel, which reads the down
@@ -300,7 +300,7 @@ def run_ours(args, rank, world, device):
     wl = workload_from_name(args.workload)
     K, W = args.steps, args.warmup
     path = args.path if args.path != "auto" else ("grouped" if wl.M >= 256 else "decode")
-    st = DecodeStep(wl, K + W, device, path)
+    st = DecodeStep(wl, K + W, device, path, args.block)
     st.capture()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     s = st.stream
@@ -532,6 +532,7 @@ def main():
     ap.add_argument("--workload", default="decode_m1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "grouped"])
+    ap.add_argument("--block", type=int, default=0, help="MoE block size b of the grouped path (0: automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

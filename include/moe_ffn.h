@@ -210,7 +210,9 @@ moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
  *     Hs uint8 [cap_rows/b][I/128][nsf][512]  their scales (same layout)
  *     Yr f32 [M*k][d]           w_route * (W2 h) per route
  *   with nsf = ceil(roundup16(b) / 128).
- * Limits: d % 128 == 0, I % 128 == 0. */
+ * Limits: d % 128 == 0, I % 128 == 0, M * d / 4 <= INT32_MAX
+ * (MOE_ERR_UNSUPPORTED otherwise); x and y 16-byte aligned
+ * (MOE_ERR_INVALID_ARG otherwise). */
 moe_status_t moe_grouped_prepare_size(const moe_weights_t *w13, const moe_weights_t *w2,
                                       size_t *sfa13_bytes, size_t *sfa2_bytes);
 moe_status_t moe_grouped_prepare(const moe_weights_t *w13, const moe_weights_t *w2,

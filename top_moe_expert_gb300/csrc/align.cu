@@ -22,7 +22,6 @@ namespace moe {
 constexpr int kAlignThreads = 256;
 constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kChunk = 2048;                       // routes per CTA
-constexpr int kSlice = kChunk / kAlignWarps;       // routes per warp
 constexpr int kAlignMaxE = 1024;
 
 __device__ __forceinline__ bool valid_id(int e, int E) { return e >= 0 && e < E; }
@@ -100,6 +99,20 @@ __device__ int block_exclusive_scan(int32_t *a, int n)
     return total;
 }
 
+// Largest e in [0, n) with a[e] <= v, for ascending a with a[0] <= v.
+__device__ __forceinline__ int last_le(const int32_t *a, int n, int v)
+{
+    int lo = 0, hi = n;              // a[lo] <= v, answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] <= v)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
 // Pass 2: offsets, padding, tails and stable placement of one chunk.
 __global__ void __launch_bounds__(kAlignThreads)
 align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nchunks,
@@ -156,27 +169,33 @@ align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nc
     __syncthreads();
     const int total_rows = block_exclusive_scan(off, E);
 
-    // bookkeeping rows: padding sentinels and expert-block ids of the experts
-    // this CTA owns (e % nchunks == c), and a slice of the tails
-    for (int e = c; e < E; e += nchunks) {
-        const int p = (tot[e] + b - 1) / b * b;
-        for (int i = tot[e] + threadIdx.x; i < p; i += kAlignThreads)
-            sorted_ids[off[e] + i] = MK;
-        for (int j = threadIdx.x; j < p / b; j += kAlignThreads)
-            expert_ids[off[e] / b + j] = e;
-    }
+    // bookkeeping, spread over all CTAs' threads: every aligned row that is
+    // padding (its expert's rows end before it) and every row past the end
+    // gets the sentinel MK; every block gets its expert id, -1 past the end.
+    // The expert of row i is the last e with off[e] <= i (experts without
+    // rows share their offset with the next one and never match).
     {
         const int stride = nchunks * kAlignThreads;
-        for (int i = total_rows + c * kAlignThreads + threadIdx.x; i < cap_rows; i += stride)
-            sorted_ids[i] = MK;
-        for (int j = total_rows / b + c * kAlignThreads + threadIdx.x; j < cap_blocks; j += stride)
-            expert_ids[j] = -1;
+        for (int i = c * kAlignThreads + threadIdx.x; i < cap_rows; i += stride) {
+            if (i >= total_rows) {
+                sorted_ids[i] = MK;
+            } else {
+                const int e = last_le(off, E, i);
+                if (i - off[e] >= tot[e])
+                    sorted_ids[i] = MK;
+            }
+        }
+        const int nblk = total_rows / b;
+        for (int j = c * kAlignThreads + threadIdx.x; j < cap_blocks; j += stride)
+            expert_ids[j] = j < nblk ? last_le(off, E, j * b) : -1;
     }
     if (c == 0 && threadIdx.x == 0)
         *num_rows_post_pad = total_rows;
 
-    // stable placement: warp w owns routes [s0, s1) of this chunk
-    const int s0 = r0 + w * kSlice, s1 = min(r1, s0 + kSlice);
+    // stable placement: warp w owns routes [s0, s1) of this chunk (slices
+    // of whole 32-route groups, spread over all warps)
+    const int slice = ((r1 - r0 + kAlignWarps - 1) / kAlignWarps + 31) / 32 * 32;
+    const int s0 = min(r1, r0 + w * slice), s1 = min(r1, s0 + slice);
     int32_t *mycnt = wcnt + w * E;
     for (int r = s0 + lane; r < s1; r += 32) {
         int e = ids[r];

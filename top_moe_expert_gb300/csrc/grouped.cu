@@ -21,7 +21,8 @@
 // bits of a route's row do not depend on its block membership or the grid.
 //
 // GEMM roles: warp 0 issues TMA (operand tiles, 128-byte swizzled) and bulk
-// copies (scale atoms) into a 4-stage ring; warp 1 owns TMEM and issues
+// copies (scale atoms) into a ring of as many stages as shared memory holds
+// (up to 12); warp 1 owns TMEM and issues
 // tcgen05.cp (scales -> TMEM) and tcgen05.mma from one thread; warps 2..5
 // drain the TMEM accumulator with tcgen05.ld.  Every mbarrier wait is
 // bounded; an expired wait records MOE_ERR_TIMEOUT in dev_status[1].
@@ -36,7 +37,8 @@
 namespace moe {
 namespace gg {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 12;         // operand ring depth: as many stages as shared memory holds
+constexpr int kHeaderBytes = 256;      // mbarriers, TMEM address, abort flag
 constexpr int kThreads = 192;          // 6 warps
 constexpr uint32_t kTmemCols = 512;    // accumulator: columns 0..255; scales from 256
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -54,6 +56,7 @@ struct Args {
     int32_t *dev_status;
     int b, n_mma, nsf, n_mt, KT, I, d, MK;
     int a_rows;               // rows of one expert in the A tensor (2I or d)
+    int stages;               // ring depth (<= kMaxStages)
 };
 
 // Scale-atom byte offset of (row m of a 128-row group, k-block kb of 4):
@@ -74,6 +77,13 @@ __device__ __forceinline__ int mx_exp(uint32_t amax_bits)
 __device__ __forceinline__ float mx_inv(int X)
 {
     return X <= 126 ? __uint_as_float(static_cast<uint32_t>(127 - X) << 23) : __uint_as_float(0x00400000u);
+}
+
+// SiLU(g) * u with the fast exponential and division: no branches, so
+// independent columns pipeline (relative error a few ulp of fp32).
+__device__ __forceinline__ float silu_mul_fast(float g, float u)
+{
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 __device__ __forceinline__ uint32_t to_e4m3(float u)
@@ -177,13 +187,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const int NB = a.n_mma * 128;                                  // B tile bytes
     const int stage_bytes = (16384 + NB + 512 + a.nsf * 512 + 1023) & ~1023;
+    const int kStages = a.stages;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * stage_bytes);
     const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kStages;
     const uint32_t accf0 = full0 + 16 * kStages, acce0 = accf0 + 16, fin = acce0 + 16;   // accf[2], acce[2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *ubuf = reinterpret_cast<float *>(tmem_slot + 4);        // [2][32][33]
-    int *t_route = reinterpret_cast<int *>(ubuf + 2 * 32 * 33);    // [256] routes of the tile's rows
+    // 16-byte aligned after the 128-byte barrier header
+    float *ubuf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + kHeaderBytes);   // [2 bufs][2 pairs][32][33]
+    int *t_route = reinterpret_cast<int *>(ubuf + 4 * 32 * 33);    // [256] routes of the tile's rows
     float *t_w = reinterpret_cast<float *>(t_route + 256);         // [256] their weights
     // two accumulator buffers (columns 0 and 128) when a tile fits in 128
     // columns, so the MMA of the next tile overlaps this tile's epilogue
@@ -333,49 +345,78 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
             tc::tc_fence_after();
             tc::named_bar(1, 128);
-            for (int c0 = 0; c0 < a.b; c0 += 32) {
+            for (int c0 = 0, chunk = 0; c0 < a.b; c0 += 32, ++chunk) {
                 uint32_t v[32];
                 tc::tmem_ld_32x32b_x32(tmem + 128 * buf + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
                 tc::tmem_ld_wait();
                 const int ncol = min(32, a.b - c0);
                 if (KIND == 1) {
-                    // lanes 0..63 of the tile are gate rows, 64..127 up rows
-                    float *ub = ubuf + (q & 1) * 32 * 33;
-                    if (q >= 2) {
+                    // Lanes 0..63 of the tile are gate rows, 64..127 up rows:
+                    // quadrant q pairs with q ^ 2 (same 32 neurons).  The
+                    // gate quadrant finishes columns 0..15 of the chunk, the
+                    // up quadrant columns 16..31; each hands the other half
+                    // of its values over through a double-buffered exchange.
+                    const bool is_gate = q < 2;
+                    float *ub = ubuf + ((chunk & 1) * 2 + (q & 1)) * 32 * 33 + lane * 33;
+                    const int keep = is_gate ? 0 : 16;
+                    // register indices stay compile-time constants (a
+                    // runtime index would move v to local memory)
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            ub[lane * 33 + c] = __uint_as_float(v[c]);
-                    }
+                    for (int c = 0; c < 16; ++c)
+                        ub[16 - keep + c] = __uint_as_float(is_gate ? v[16 + c] : v[c]);
                     tc::named_bar(1, 128);
-                    if (q < 2) {
-                        const int n = 64 * mt + 32 * q + lane;       // neuron of this lane
-                        const int kblk = 2 * mt + q;                  // its 32-neuron block
-                        uint8_t *hrow = a.hq + static_cast<int64_t>(rho0 + c0) * a.I + n;
-                        uint8_t *hsa = a.hs + ((static_cast<int64_t>(jb) * (a.I / 128) + kblk / 4) * a.nsf) * 512;
+                    // the 16 columns are independent: SiLU, block amax and
+                    // code conversion each run as 16 parallel chains
+                    float hv[16];
+                    uint32_t am[16];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            if (c < ncol) {
-                                const float hval = silu_mul(__uint_as_float(v[c]), ub[lane * 33 + c]);
-                                const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hval)));
-                                const int X = mx_exp(amax);
-                                hrow[static_cast<int64_t>(c) * a.I] = static_cast<uint8_t>(to_e4m3(hval * mx_inv(X)));
-                                if (lane == 0) {
-                                    const int m = c0 + c;
-                                    hsa[(m / 128) * 512 + atom_off(m & 127, kblk & 3)] = static_cast<uint8_t>(X + 127);
-                                }
+                    for (int c = 0; c < 16; ++c) {
+                        const float mine = __uint_as_float(is_gate ? v[c] : v[16 + c]);
+                        const float other = ub[keep + c];
+                        hv[c] = is_gate ? silu_mul_fast(mine, other) : silu_mul_fast(other, mine);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        am[c] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[c])));
+                    const int n = 64 * mt + 32 * (q & 1) + lane;     // neuron of this lane
+                    const int kblk = 2 * mt + (q & 1);                // its 32-neuron block
+                    uint8_t *hrow = a.hq + static_cast<int64_t>(rho0 + c0 + keep) * a.I + n;
+                    uint8_t *hsa = a.hs + ((static_cast<int64_t>(jb) * (a.I / 128) + kblk / 4) * a.nsf) * 512;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int X = mx_exp(am[c]);
+                        if (keep + c < ncol) {
+                            hrow[static_cast<int64_t>(c) * a.I] = static_cast<uint8_t>(to_e4m3(hv[c] * mx_inv(X)));
+                            if (lane == 0) {
+                                const int m = c0 + keep + c;
+                                hsa[(m / 128) * 512 + atom_off(m & 127, kblk & 3)] = static_cast<uint8_t>(X + 127);
                             }
                         }
                     }
-                    tc::named_bar(1, 128);
                 } else {
                     const int o = 128 * mt + 32 * q + lane;          // output row of this lane
+                    // the chunk's routes and weights into registers first
+                    // (broadcast 16-byte loads), then 32 independent stores
+                    int rr[32];
+                    float ww[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int4 r4 = reinterpret_cast<const int4 *>(t_route + c0)[i];
+                        const float4 w4 = reinterpret_cast<const float4 *>(t_w + c0)[i];
+                        rr[4 * i] = r4.x;
+                        rr[4 * i + 1] = r4.y;
+                        rr[4 * i + 2] = r4.z;
+                        rr[4 * i + 3] = r4.w;
+                        ww[4 * i] = w4.x;
+                        ww[4 * i + 1] = w4.y;
+                        ww[4 * i + 2] = w4.z;
+                        ww[4 * i + 3] = w4.w;
+                    }
+                    float *yo = a.yr + o;
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        if (c < ncol) {
-                            const int r = t_route[c0 + c];
-                            if (r < a.MK)
-                                a.yr[static_cast<int64_t>(r) * a.d + o] = t_w[c0 + c] * __uint_as_float(v[c]);
-                        }
+                        if (c < ncol && rr[c] < a.MK)
+                            yo[static_cast<int64_t>(rr[c]) * a.d] = ww[c] * __uint_as_float(v[c]);
                     }
                 }
             }
@@ -395,24 +436,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 }
 
 // ---------------------------------------------------------------- combine
+// Four consecutive outputs per thread (d is a multiple of 128): 16-byte
+// loads of the k route rows, summed in slot order.
 template <typename YT>
 __global__ void combine_kernel(const float *__restrict__ yr, const int32_t *__restrict__ ids, int M, int k, int d,
                                int E, YT *__restrict__ y)
 {
-    const int64_t total = static_cast<int64_t>(M) * d;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / d), o = static_cast<int>(i % d);
-        float s = 0.f;
+    const int d4 = d >> 2;
+    const int total = M * d4;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int t = i / d4, o4 = i - t * d4;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
-            const int e = ids[t * k + j];
-            if (e >= 0 && e < E)
-                s += yr[static_cast<int64_t>(t * k + j) * d + o];
+            const int e = __ldg(ids + t * k + j);
+            if (e >= 0 && e < E) {
+                const float4 v = __ldcs(reinterpret_cast<const float4 *>(yr + static_cast<int64_t>(t * k + j) * d) + o4);
+                s.x += v.x;
+                s.y += v.y;
+                s.z += v.z;
+                s.w += v.w;
+            }
         }
-        if constexpr (sizeof(YT) == 4)
-            y[i] = s;
-        else
-            y[i] = __float2bfloat16_rn(s);
+        if constexpr (sizeof(YT) == 4) {
+            reinterpret_cast<float4 *>(y)[i] = s;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t *>(&lo);
+            pk.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(y)[i] = pk;
+        }
     }
 }
 
@@ -562,8 +615,11 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
     if (!x || !topk_ids || !topk_w || !y || !sfa13 || !sfa2 || !sorted_route_ids || !expert_ids ||
         !num_rows_post_pad || !w13->q || !w2->q)
         return MOE_ERR_INVALID_ARG;
-    if (!aligned(w13->q, 16) || !aligned(w2->q, 16) || !aligned(sfa13, 16) || !aligned(sfa2, 16))
+    if (!aligned(w13->q, 16) || !aligned(w2->q, 16) || !aligned(sfa13, 16) || !aligned(sfa2, 16) ||
+        !aligned(x, 16) || !aligned(y, 16))
         return MOE_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(M) * (d / 4) > INT32_MAX)
+        return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(M, k, d, I, b, cap_rows);
     if (!ws || ws_bytes < L.total || !aligned(ws, 256))
         return MOE_ERR_WORKSPACE;
@@ -588,7 +644,11 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         return MOE_ERR_CUDA;
 
     const int stage_bytes = (16384 + n_mma * 128 + 512 + nsf * 512 + 1023) & ~1023;
-    const size_t smem = 1024 + kStages * stage_bytes + 128 + 2 * 32 * 33 * sizeof(float) + 512 * 4;
+    const size_t fixed = 1024 + kHeaderBytes + 4 * 32 * 33 * sizeof(float) + 512 * 4;
+    const int stages = static_cast<int>((227 * 1024 - fixed) / stage_bytes) < kMaxStages
+                           ? static_cast<int>((227 * 1024 - fixed) / stage_bytes)
+                           : kMaxStages;
+    const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
     static std::once_flag attr_once;
     static bool attr_ok = false;
     std::call_once(attr_once, [] {
@@ -597,21 +657,21 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
                   cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
                       cudaSuccess;
     });
-    if (!attr_ok || smem > 227 * 1024)
+    if (!attr_ok || stages < 2 || smem > 227 * 1024)
         return MOE_ERR_CUDA;
     const int grid = sm_count();
 
     Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
-            hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I};
+            hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I, stages};
     gemm_kernel<1><<<grid, kThreads, smem, s>>>(tA1, tB1, a1);
     if (launch_status() != MOE_OK)
         return MOE_ERR_CUDA;
     Args a2{static_cast<const uint8_t *>(sfa2), hs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
-            nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d};
+            nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d, stages};
     gemm_kernel<2><<<grid, kThreads, smem, s>>>(tA2, tB2, a2);
     if (launch_status() != MOE_OK)
         return MOE_ERR_CUDA;
-    const int64_t n = static_cast<int64_t>(M) * d;
+    const int64_t n = static_cast<int64_t>(M) * (d / 4);
     const int cb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
     if (ydt == MOE_FP32)
         combine_kernel<float><<<cb, 256, 0, s>>>(yr, topk_ids, M, k, d, E, static_cast<float *>(y));
