@@ -70,6 +70,13 @@ def expert_bytes(wl) -> int:
     return 3 * wl.I * wl.d * 33 // 32
 
 
+def layer_bytes(wl, ids: np.ndarray) -> int:
+    """Algorithmic bytes of one layer call: distinct routed experts' weights,
+    x and the routing (ids, weights) read, y written (bf16)."""
+    distinct = len(np.unique(ids[(ids >= 0) & (ids < wl.E)]))
+    return distinct * expert_bytes(wl) + wl.M * wl.d * 2 + wl.M * wl.k * 8 + wl.M * wl.d * 2
+
+
 def step_bytes(wl, ids: np.ndarray) -> int:
     """Algorithmic bytes of one step: distinct routed experts' weights, the
     activations read (x, router logits) and the output written (bf16 y)."""
@@ -172,9 +179,10 @@ def decode_src_hash() -> str:
 # ------------------------------------------------------------------ our arm
 
 def grouped_block(wl) -> int:
-    """MoE block size b of the grouped path: the expected rows per expert,
-    rounded up to a power of two within [16, 128]."""
-    rows = max(1, wl.M * wl.k // wl.E)
+    """MoE block size b of the grouped path: twice the expected rows per
+    expert, rounded up to a power of two within [16, 128], so that most
+    experts fit in one block and their weights stream once."""
+    rows = max(1, 2 * wl.M * wl.k // wl.E)
     b = 16
     while b < rows and b < 128:
         b *= 2
@@ -189,6 +197,7 @@ class DecodeStep:
         import top_moe_expert_gb300 as moe
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
+        self.routed_in_layer = False
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
         self.q13 = torch.empty((E, 2 * I, d), dtype=torch.uint8, device=device)
         self.s13 = torch.empty((E, 2 * I, d // 32), dtype=torch.uint8, device=device)
@@ -207,6 +216,8 @@ class DecodeStep:
             # small batches take the single-pass kernel, which reads the down
             # projection neuron-major: pack it once (same bytes, K-outer order)
             self.fused = M <= 4 and d % 1024 == 0
+            # one token on that layout: routing runs inside the layer's kernel
+            self.routed_in_layer = self.fused and M == 1 and d in (1024, 2048) and E <= 512
             if self.fused:
                 self.w2 = moe.moe_mxfp8_transpose(self.w2)
                 del self.q2, self.s2
@@ -233,25 +244,50 @@ class DecodeStep:
             self.ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, k, d, I, self.b, cr), dtype=torch.uint8,
                                   device=device)
         else:
-            self.ws = torch.empty(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
+            self.ws = torch.zeros(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device)
         torch.cuda.synchronize()
 
-    def launch(self, stream=None):
+    def launch_pre(self, stream=None):
+        """Routing of the step: top-k (and, for the grouped path, alignment);
+        nothing when the layer call routes the token itself."""
         moe = self.moe
+        if self.routed_in_layer:
+            return
         moe.moe_topk_softmax(self.logits, self.wl.k, self.ids, self.w, stream=stream)
         if self.path == "grouped":
             moe.moe_align_block_size(self.ids, self.wl.E, self.b, out=self.aligned, ws=self.ws_align, stream=stream)
+
+    def launch_layer(self, stream=None):
+        """The layer call itself (one C-ABI call)."""
+        moe = self.moe
+        if self.path == "grouped":
             moe.moe_ffn_grouped(self.x, self.ids, self.w, self.w13, self.w2, self.sfa13, self.sfa2, self.aligned,
                                 self.b, y=self.y, ws=self.ws, stream=stream)
+        elif self.routed_in_layer:
+            moe.moe_ffn_decode_logits(self.logits, self.x, self.wl.k, self.w13, self.w2, y=self.y, topk_ids=self.ids,
+                                      topk_w=self.w, ws=self.ws, stream=stream)
         else:
             moe.moe_ffn_decode(self.x, self.ids, self.w, self.w13, self.w2, y=self.y, ws=self.ws, stream=stream)
+
+    def launch(self, stream=None):
+        self.launch_pre(stream)
+        self.launch_layer(stream)
+
+    def layer_kernels(self) -> str:
+        if self.path == "grouped":
+            return "moe_ffn_grouped: act_quant + gemm_kernel<1> + gemm_kernel<2> + combine"
+        if self.routed_in_layer:
+            return "moe_ffn_decode_logits: dm::m1_kernel (top-k routing + gate/up + SwiGLU + down + combine), one kernel"
+        if self.fused:
+            return "moe_ffn_decode: df::fused_kernel + df::reduce_kernel, PDL-chained"
+        return "moe_ffn_decode: ds::gate_up_kernel + ds::down_kernel, PDL-chained"
 
     def launches_per_step(self) -> int:
         if self.path == "grouped":
             na = 2 if self.ws_align is not None else 1
             return 1 + na + 4
-        return 3
+        return 1 if self.routed_in_layer else 3
 
     def capture(self):
         with torch.cuda.stream(self.stream):
@@ -260,6 +296,11 @@ class DecodeStep:
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, stream=self.stream):
             self.launch(self.stream)
+        self.stream.synchronize()
+        # the layer call alone, for the roofline of the dominant kernels
+        self.layer_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.layer_graph, stream=self.stream):
+            self.launch_layer(self.stream)
         self.stream.synchronize()
 
 
@@ -270,7 +311,9 @@ def host_topk_ids(logits: np.ndarray, k: int) -> np.ndarray:
 
 
 def roofline_obj(st, wl, total_ms, K, total_bytes, world):
-    """Roofline of the step's layer call.  HBM-bound unless the layer's FLOPs
+    """Roofline of the layer call (the dominant kernels of the step), timed
+    alone with CUDA events on its stream: total_ms over K calls moving
+    total_bytes of algorithmic traffic.  HBM-bound unless the layer's FLOPs
     at the MXFP8 tensor peak take longer than its bytes at the HBM peak."""
     peak_gbs, peak_kind = measured_peak()
     peak_tf, tf_kind = measured_mxfp8_tflops()
@@ -278,21 +321,20 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     flops = 2.0 * wl.M * wl.k * 3 * wl.I * wl.d * K * world
     t_hbm = total_bytes / (peak_gbs * 1e9)
     t_mma = flops / (peak_tf * 1e12)
-    if st.path == "grouped":
-        kern = "grouped layer: act_quant + gemm_kernel<1> + gemm_kernel<2> + combine (+ topk, align)"
-    elif st.fused:
-        kern = "decode layer: df::fused_kernel + df::reduce_kernel, PDL-chained (+ topk)"
-    else:
-        kern = "decode layer: ds::gate_up_kernel + ds::down_kernel, PDL-chained (+ topk)"
+    kern = st.layer_kernels()
     traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash())
     if t_mma > t_hbm:
         ach = flops / sec / 1e12 / world
         return {"kernel": kern, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_tf,
                 "peak_kind": tf_kind, "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4), "traffic": traffic,
+                "us_per_launch": round(total_ms * 1e3 / K, 3),
+                "algorithmic_flops_per_launch": round(flops / K / world),
                 "hbm_frac": round(total_bytes / sec / 1e9 / world / peak_gbs, 4)}
     ach = total_bytes / sec / 1e9 / world
     return {"kernel": kern, "bound": "hbm", "achieved": round(ach, 1), "peak": peak_gbs, "peak_kind": peak_kind,
             "unit": "GB/s", "frac": round(ach / peak_gbs, 4), "traffic": traffic,
+            "us_per_launch": round(total_ms * 1e3 / K, 3),
+            "algorithmic_bytes_per_launch": round(total_bytes / K / world),
             "tensor_frac": round(flops / sec / 1e12 / world / peak_tf, 4)}
 
 
@@ -373,15 +415,38 @@ def run_ours(args, rank, world, device):
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
     e2e_bytes = float(sum(bytes_steps[:Ke]))
 
+    # the layer call alone (roofline of the dominant kernels): routing of the
+    # step runs first, outside the events; L2 flushed before each call
+    Kl = min(K, 2000)
+    l0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kl)]
+    l1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kl)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(Kl):
+            j = (W + i) % st.n_inputs
+            st.x.copy_(st.x_all[j], non_blocking=True)
+            st.logits.copy_(st.logits_all[j], non_blocking=True)
+            st.launch_pre(s)
+            flush.fill_(float(j))
+            l0[i].record(s)
+            st.layer_graph.replay()
+            l1[i].record(s)
+    torch.cuda.synchronize()
+    layer_ms = sum(a.elapsed_time(b) for a, b in zip(l0, l1))
+    # (a layer call that routes the token itself also reads the logits)
+    lb = step_bytes if st.routed_in_layer else layer_bytes
+    layer_total_bytes = float(sum(lb(wl, host_topk_ids(logits_np[(W + i) % st.n_inputs], wl.k)) for i in range(Kl)))
+
     # gather across replicas: max time, summed bytes
-    t = torch.tensor([total_ms, total_bytes, e2e_ms, e2e_bytes], dtype=torch.float64, device=device)
+    t = torch.tensor([total_ms, total_bytes, e2e_ms, e2e_bytes, layer_ms, layer_total_bytes], dtype=torch.float64,
+                     device=device)
     if world > 1:
         tmax = t.clone()
         torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
         tsum = t.clone()
         torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
-        total_ms, e2e_ms = float(tmax[0]), float(tmax[2])
-        total_bytes, e2e_bytes = float(tsum[1]), float(tsum[3])
+        total_ms, e2e_ms, layer_ms = float(tmax[0]), float(tmax[2]), float(tmax[4])
+        total_bytes, e2e_bytes, layer_total_bytes = float(tsum[1]), float(tsum[3]), float(tsum[5])
     if rank != 0:
         return None
 
@@ -409,6 +474,8 @@ def run_ours(args, rank, world, device):
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
                    "path": ("expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
                             % st.b if st.path == "grouped" else
+                            "single-token decode: routing + gate/up + SwiGLU + down + combine in one kernel"
+                            if st.routed_in_layer else
                             "single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
                             else "output-centric decode (topk + gate/up + down)") + ", CUDA graph",
                    "l2": "flushed between timed steps (512 MiB write, outside the timed interval)",
@@ -418,7 +485,7 @@ def run_ours(args, rank, world, device):
                 "h2d_bytes_per_step": wl.M * wl.d * 2 + wl.M * wl.E * 4,
                 "d2h_bytes_per_step": wl.M * wl.d * 2},
         "gpu_launches": st.launches_per_step() * K,
-        "roofline": roofline_obj(st, wl, total_ms, K, total_bytes, world),
+        "roofline": roofline_obj(st, wl, layer_ms, Kl, layer_total_bytes, world),
         "clocks": clocks,
         "wall_s_timed_loop": round(t_wall, 3),
         "_path": st.path,

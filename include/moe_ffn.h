@@ -159,11 +159,19 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  *   w2       N = d, K = I, same format as w13, or MOE_W_MXFP8_T with
  *            MXFP8 w13 (then M <= 4, M*k <= 64 and d % 1024 == 0)
  *   y        [M][d] of ydt (MOE_BF16 or MOE_FP32)
- *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned
+ *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned; its
+ *            first 256 bytes must be zero before the first call that uses
+ *            it (e.g. cudaMemset once) -- every call leaves them zero again,
+ *            except one that reports MOE_ERR_TIMEOUT, after which they must
+ *            be zeroed again
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
- * Kernels by case: w2 in MOE_W_MXFP8_T -> one streaming pass (gate/up rows
- * and down columns of each neuron together, per-SM partial outputs) plus a
- * fixed-order reduction; MXFP8 with M*k <= 512 -> a gate/up kernel and a
+ * Kernels by case: w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
+ * streaming kernel (each warp owns whole neurons: gate/up dots and the
+ * down-column outer product; per-SM partial outputs reduced in a fixed order
+ * after a grid-wide barrier whose counters live in ws[0..8)); other
+ * MOE_W_MXFP8_T cases -> one streaming pass (gate/up rows and down columns of
+ * each neuron together, per-SM partial outputs) plus a fixed-order reduction
+ * kernel; MXFP8 with M*k <= 512 -> a gate/up kernel and a
  * down kernel chained by programmatic dependent launch; otherwise one warp
  * per intermediate / output scalar.  Every output's summation order is fixed
  * by the shapes, the path and (single-pass path) the set of routed experts,
@@ -177,6 +185,21 @@ moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
                             const moe_weights_t *w13, const moe_weights_t *w2,
                             void *y, int32_t ydt, void *ws, size_t ws_bytes,
                             int32_t *dev_status, void *stream);
+
+/* Routing and the decode layer in one call: the same result, bit for bit, as
+ * moe_topk_softmax(logits, M, w13->E, k, topk_ids, topk_w) followed by
+ * moe_ffn_decode(x, ..., topk_ids, topk_w, ...).  The whole decode step of
+ * "Warp decode" (section on the conventional MoE path: route, then the
+ * experts): for a single token (M == 1) on the single-pass layout
+ * (w2 MOE_W_MXFP8_T, d in {1024, 2048}, E <= 512) it is one kernel that
+ * routes the token itself in every CTA; otherwise it launches the two calls.
+ *   logits   fp32 [M][E] router logits, E = w13->E
+ *   topk_ids int32 [M][k], topk_w fp32 [M][k]: outputs (the routing used)
+ *   other arguments and the workspace contract as moe_ffn_decode. */
+moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t xdt, int32_t M, int32_t d,
+                                   int32_t k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                   int32_t *topk_ids, float *topk_w, void *y, int32_t ydt, void *ws,
+                                   size_t ws_bytes, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------- expert-centric path
  * Grouped path for larger batches ("Hardware-Native Joint Sparse-

@@ -229,3 +229,31 @@ def test_fused_path_rejects_large_batches():
     with pytest.raises(moe.MoeError) as ei:
         run_fused(layer, x, ids, w, torch.float32)
     assert ei.value.status == 2
+
+
+# ------------------------------------------------ routing fused into the layer call
+
+@pytest.mark.parametrize("M,transposed", [(1, True), (1, False), (3, True)])
+def test_decode_logits_equals_topk_then_decode(M, transposed):
+    """moe_ffn_decode_logits is, bit for bit, moe_topk_softmax followed by
+    moe_ffn_decode (one kernel at M = 1 on the single-pass layout, two calls
+    otherwise); its routing equals the oracle's top-k and its output the
+    oracle's layer."""
+    layer = _fused_layer(7)
+    w2 = layer.w2t if transposed else layer.w2
+    wl = dataclasses.replace(inputs.DECODE, name=f"logits_m{M}", M=M, seed=7)
+    for step in range(3):
+        logits_np = inputs.router_logits(wl, step)
+        logits = torch.from_numpy(logits_np).cuda()
+        x = inputs.activations(wl, step).cuda()
+        y1, ids1, w1 = moe.moe_ffn_decode_logits(logits, x, wl.k, layer.w13, w2, out_dtype=torch.float32)
+        ids2 = torch.empty((M, wl.k), dtype=torch.int32, device="cuda")
+        w2_ = torch.empty((M, wl.k), dtype=torch.float32, device="cuda")
+        moe.moe_topk_softmax(logits, wl.k, ids2, w2_)
+        y2 = moe.moe_ffn_decode(x, ids2, w2_, layer.w13, w2, out_dtype=torch.float32)
+        assert torch.equal(ids1, ids2) and torch.equal(w1, w2_)
+        assert torch.equal(y1, y2)
+        ids_ref, w_ref = oracle.topk_softmax(logits_np, wl.k)
+        assert np.array_equal(ids1.cpu().numpy(), ids_ref)
+        np.testing.assert_allclose(w1.cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
+        gs.assert_layer_close(y1, oracle_decode(layer, x.cpu(), ids_ref, w_ref.astype(np.float32)))

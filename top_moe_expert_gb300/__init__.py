@@ -57,6 +57,8 @@ _PROTOS = {
     "moe_ffn_decode_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
     "moe_ffn_decode": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                               ctypes.POINTER(moe_weights_t), _P, _I32, _P, _SZ, _P, _P]),
+    "moe_ffn_decode_logits": (_I32, [_P, _P, _I32, _I32, _I32, _I32, ctypes.POINTER(moe_weights_t),
+                                     ctypes.POINTER(moe_weights_t), _P, _P, _P, _I32, _P, _SZ, _P, _P]),
     "moe_grouped_prepare_size": (_I32, [ctypes.POINTER(moe_weights_t), ctypes.POINTER(moe_weights_t), _P, _P]),
     "moe_grouped_prepare": (_I32, [ctypes.POINTER(moe_weights_t), ctypes.POINTER(moe_weights_t), _P, _P, _P]),
     "moe_ffn_grouped_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P]),
@@ -228,12 +230,37 @@ def moe_ffn_decode(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor
     I = w2.K
     y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
     if ws is None:
-        ws = torch.empty(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=x.device)
+        # zeroed: the single-token path keeps its grid-barrier counters in the
+        # first 256 bytes and needs them zero before the first call
+        ws = torch.zeros(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=x.device)
     a, b = w13.c_struct(), w2.c_struct()
     _check(lib().moe_ffn_decode(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
                                 ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype], _ptr(ws),
                                 ws.numel(), _ptr(dev_status), _stream(stream)), "moe_ffn_decode")
     return y
+
+
+def moe_ffn_decode_logits(logits: torch.Tensor, x: torch.Tensor, k: int, w13: Weights, w2: Weights,
+                          out_dtype=torch.bfloat16, y=None, topk_ids=None, topk_w=None, ws=None, dev_status=None,
+                          stream=None):
+    """Routing + decode layer in one call (one kernel for a single token on the
+    single-pass layout): returns (y, topk_ids, topk_w), identical to
+    moe_topk_softmax followed by moe_ffn_decode."""
+    for t, n in ((logits, "logits"), (x, "x")):
+        _dev(t, n)
+    M, d = x.shape
+    I = w2.K
+    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
+    topk_ids = topk_ids if topk_ids is not None else torch.empty((M, k), dtype=torch.int32, device=x.device)
+    topk_w = topk_w if topk_w is not None else torch.empty((M, k), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = torch.zeros(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=x.device)
+    a, b = w13.c_struct(), w2.c_struct()
+    _check(lib().moe_ffn_decode_logits(_ptr(logits), _ptr(x), _DT[x.dtype], M, d, k, ctypes.byref(a),
+                                       ctypes.byref(b), _ptr(topk_ids), _ptr(topk_w), _ptr(y), _DT[y.dtype],
+                                       _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream)),
+           "moe_ffn_decode_logits")
+    return y, topk_ids, topk_w
 
 
 def moe_ffn_decode_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, w13: Weights,

@@ -319,6 +319,10 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
         return MOE_ERR_INVALID_ARG;
     size_t h = ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
     size_t part = (M <= 4 && d % 1024 == 0) ? decode_fused_workspace(M, d) : 0;
+    if (M == 1 && (d == 1024 || d == 2048)) {
+        const size_t m1 = decode_m1_workspace(d);
+        part = part > m1 ? part : m1;
+    }
     *bytes = h > part ? h : part;
     return MOE_OK;
 }
@@ -369,6 +373,12 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         moe_ffn_decode_workspace_size(M, k, d, I, &need);
         if (!ws || ws_bytes < need || !aligned(ws, 256))
             return MOE_ERR_WORKSPACE;
+        if (decode_m1_eligible(M, k, d, I, w13->E) && aligned(y, 16))
+            return decode_m1_launch(static_cast<const __nv_bfloat16 *>(x), d, I, w13->E, topk_ids, topk_w, nullptr,
+                                    nullptr, nullptr, k, static_cast<const uint8_t *>(w13->q),
+                                    static_cast<const uint8_t *>(w13->scale),
+                                    static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y,
+                                    ydt == MOE_FP32, ws, dev_status, as_stream(stream));
         return decode_fused_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
                                    static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
                                    static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y,
@@ -419,4 +429,39 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     return ydt == MOE_FP32
                ? decode_launch<MOE_W_AWQ4, __nv_bfloat16, float>(x, M, d, topk_ids, topk_w, k, w13, w2, y, h, dev_status, s)
                : decode_launch<MOE_W_AWQ4, __nv_bfloat16, __nv_bfloat16>(x, M, d, topk_ids, topk_w, k, w13, w2, y, h, dev_status, s);
+}
+
+MOE_API moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t xdt, int32_t M, int32_t d,
+                                           int32_t k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                           int32_t *topk_ids, float *topk_w, void *y, int32_t ydt, void *ws,
+                                           size_t ws_bytes, int32_t *dev_status, void *stream)
+{
+    if (M < 0 || d < 1 || k < 1 || k > 32 || !w13 || !w2)
+        return MOE_ERR_INVALID_ARG;
+    if (M == 0)
+        return MOE_OK;
+    if (!logits || !topk_ids || !topk_w)
+        return MOE_ERR_INVALID_ARG;
+    const int I = w2->K, E = w13->E;
+    // one kernel for a single token on the neuron-major single-pass layout
+    if (M == 1 && w2->fmt == MOE_W_MXFP8_T && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
+        (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
+        check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_m1_eligible(1, k, d, I, E) &&
+        decode_m1_route_eligible(E, k) && aligned(w13->scale, 16) && aligned(w2->scale, 16) && x && y &&
+        aligned(x, 16) && aligned(y, 16)) {
+        size_t need;
+        moe_ffn_decode_workspace_size(M, k, d, I, &need);
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return MOE_ERR_WORKSPACE;
+        return decode_m1_launch(static_cast<const __nv_bfloat16 *>(x), d, I, E, nullptr, nullptr, logits, topk_ids,
+                                topk_w, k, static_cast<const uint8_t *>(w13->q),
+                                static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
+                                static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status,
+                                as_stream(stream));
+    }
+    // otherwise: routing, then the layer
+    moe_status_t st = moe_topk_softmax(logits, M, E, k, topk_ids, topk_w, stream);
+    if (st != MOE_OK)
+        return st;
+    return moe_ffn_decode(x, xdt, M, d, topk_ids, topk_w, k, w13, w2, y, ydt, ws, ws_bytes, dev_status, stream);
 }

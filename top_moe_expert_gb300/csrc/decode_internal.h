@@ -25,4 +25,13 @@ moe_status_t decode_fused_launch(const __nv_bfloat16 *x, int M, int d, int I, in
                                  const uint8_t *q2t, const uint8_t *s2t, void *y, bool y_f32, float *partial,
                                  int32_t *dev_status, cudaStream_t stream);
 
+bool decode_m1_eligible(int M, int k, int d, int I, int E);
+size_t decode_m1_workspace(int d);
+bool decode_m1_route_eligible(int E, int k);
+// ids / wts given, or logits given (then ids_out / wts_out receive the routing)
+moe_status_t decode_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const int32_t *ids, const float *wts,
+                              const float *logits, int32_t *ids_out, float *wts_out, int k, const uint8_t *q13,
+                              const uint8_t *s13, const uint8_t *q2t, const uint8_t *s2t, void *y, bool y_f32,
+                              void *ws, int32_t *dev_status, cudaStream_t stream);
+
 }  // namespace moe

@@ -1,23 +1,12 @@
-// topk.cu -- top-k softmax routing (one warp per token).
-//
-// "Warp decode", section on the conventional MoE path: every token selects
-// k of E experts (8 of 128 in the page's layer).  Selection is by logit,
-// which orders experts exactly as the softmax probabilities do; ties go to
-// the lower expert id and slots come out in descending order.  The k weights
-// are the softmax probabilities renormalised over the chosen experts, i.e.
-// exp(l_j - l_max) / sum_{chosen} exp(l_i - l_max), computed in FP32.
+// topk.cu -- top-k softmax routing (one warp per token); the selection
+// itself is topk_warp (topk.cuh), shared with the fused single-token layer.
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
 constexpr int kTopkMaxPerLane = 128;   // E <= 4096
 constexpr int kTopkWarps = 4;
-
-// Order: larger logit first, then lower expert id.
-__device__ __forceinline__ bool better(float a, int ia, float b, int ib)
-{
-    return a > b || (a == b && ia < ib);
-}
 
 template <int PER_LANE>
 __global__ void __launch_bounds__(kTopkWarps * 32)
@@ -30,58 +19,12 @@ topk_softmax_kernel(const float *__restrict__ logits, int M, int E, int k,
     const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
     if (t >= M)
         return;
-    const float *l = logits + static_cast<int64_t>(t) * E;
-    float v[PER_LANE];
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-        const int e = i * 32 + lane;
-        v[i] = e < E ? __ldcg(l + e) : -INFINITY;
-    }
-    uint32_t taken[(PER_LANE + 31) / 32];
-#pragma unroll
-    for (int i = 0; i < (PER_LANE + 31) / 32; ++i)
-        taken[i] = 0;
-    float my_l = -INFINITY;     // slot j = lane keeps its (logit, id)
-    int my_e = -1;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < PER_LANE; ++i) {
-            const int e = i * 32 + lane;
-            const bool free_ = e < E && !((taken[i >> 5] >> (i & 31)) & 1u);
-            if (free_ && (be == 0x7fffffff || better(v[i], e, bv, be))) {
-                bv = v[i];
-                be = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (oe != 0x7fffffff && (be == 0x7fffffff || better(ov, oe, bv, be))) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane) {           // the owner marks the entry as taken
-            const int i = be >> 5;
-#pragma unroll
-            for (int ii = 0; ii < PER_LANE; ++ii)
-                if (ii == i)
-                    taken[ii >> 5] |= 1u << (ii & 31);
-        }
-        if (lane == j) {
-            my_l = bv;
-            my_e = be;
-        }
-    }
-    const float mx = __shfl_sync(0xffffffffu, my_l, 0);
-    const float p = lane < k ? expf(my_l - mx) : 0.f;
-    const float z = warp_sum(p);
+    int e;
+    float w;
+    topk_warp<PER_LANE>(logits + static_cast<int64_t>(t) * E, E, k, lane, e, w);
     if (lane < k) {
-        ids[static_cast<int64_t>(t) * k + lane] = my_e;
-        wts[static_cast<int64_t>(t) * k + lane] = p / z;
+        ids[static_cast<int64_t>(t) * k + lane] = e;
+        wts[static_cast<int64_t>(t) * k + lane] = w;
     }
 }
 
