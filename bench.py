@@ -170,8 +170,8 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 def decode_src_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cu", "decode_fused.cu", "decode_stream.cu", "topk.cu", "common.cuh", "tc.cuh", "grouped.cu",
-              "align.cu"):
+    for f in ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "topk.cu", "topk.cuh", "common.cuh",
+              "tc.cuh", "grouped.cu", "align.cu"):
         h.update(open(os.path.join(ROOT, "top_moe_expert_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
