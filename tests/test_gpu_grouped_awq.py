@@ -1,0 +1,88 @@
+"""GPU parity of the 4-bit AWQ grouped path (tcgen05 kind::f16 after
+in-shared-memory dequantization) on the packed-AWQ study's alignment shape.
+
+The oracle runs with h rounded to fp16 (the GEMM2 operand of this path).
+Checked: the alignment of fixture A (168 routes -> 400 aligned rows in 50
+blocks), the layer output within the layer tolerance, bit-identical outputs
+across five repeats, and bit-identical outputs under another block size (the
+result does not depend on block membership: every output accumulates its
+K-tiles in one fixed order, no split-K).
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import top_moe_expert_gb300 as moe
+from tests import gpu_setup as gs
+from top_moe_expert_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    gs.need_gpu()
+
+
+@pytest.fixture(scope="module")
+def fixture_a():
+    wl = inputs.AWQ_FIXTURE
+    layer = gs.AwqLayer(wl)
+    x = inputs.activations(wl, dtype=torch.float16)
+    ids, w = gs.routing(wl)
+    ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, layer.host13, layer.host2,
+                           mode=oracle.MODE_H16)["y"]
+    return wl, layer, x, ids, w, ref
+
+
+def _run(layer, x, ids, w, b, out_dtype=torch.float32):
+    wl = layer.wl
+    tid = torch.from_numpy(ids).cuda()
+    aligned = moe.moe_align_block_size(tid, wl.E, b)
+    M, k = ids.shape
+    ws = torch.zeros(moe.moe_ffn_grouped_workspace_size(M, k, wl.d, wl.I, b, aligned[0].numel()),
+                     dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    y = moe.moe_ffn_grouped(x.cuda(), tid, torch.from_numpy(w).cuda(), layer.w13, layer.w2, None, None, aligned, b,
+                            out_dtype=out_dtype, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.tolist() == [0, 0]
+    return y, aligned
+
+
+def test_awq_grouped_fixture_a(fixture_a):
+    wl, layer, x, ids, w, ref = fixture_a
+    y, aligned = _run(layer, x, ids, w, 8)
+    assert int(aligned[2].item()) == 400
+    ex = aligned[1].cpu().numpy()
+    assert int((ex >= 0).sum()) == 50
+    gs.assert_layer_close(y, ref)
+
+
+def test_awq_grouped_repeats_bit_identical(fixture_a):
+    wl, layer, x, ids, w, _ = fixture_a
+    digests = {hashlib.sha256(_run(layer, x, ids, w, 8)[0].cpu().numpy().tobytes()).hexdigest() for _ in range(5)}
+    assert len(digests) == 1
+
+
+def test_awq_grouped_independent_of_block_size(fixture_a):
+    wl, layer, x, ids, w, _ = fixture_a
+    y8, _ = _run(layer, x, ids, w, 8)
+    y16, _ = _run(layer, x, ids, w, 16)
+    y32, _ = _run(layer, x, ids, w, 32)
+    assert torch.equal(y8, y16) and torch.equal(y8, y32)
+
+
+@pytest.mark.parametrize("xdt,b", [(torch.float16, 16), (torch.bfloat16, 8), (torch.float16, 64)])
+def test_awq_grouped_small(xdt, b):
+    wl = inputs.Workload("awq_grouped_small", M=40, d=1024, I=256, E=16, k=4, fmt="awq4", seed=8)
+    layer = gs.AwqLayer(wl)
+    x = inputs.activations(wl, dtype=xdt)
+    ids, w = gs.routing(wl)
+    y, _ = _run(layer, x, ids, w, b, out_dtype=torch.bfloat16)
+    ref = oracle.moe_layer(gs.x_exact(x.to(torch.float16)), ids, w.astype(np.float64), wl.E, layer.host13,
+                           layer.host2, mode=oracle.MODE_H16)["y"]
+    gs.assert_layer_close(y, ref)

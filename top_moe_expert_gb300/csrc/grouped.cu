@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "grouped_internal.h"
 #include "tc.cuh"
 
 namespace moe {
@@ -540,6 +541,36 @@ static WsLayout ws_layout(int M, int k, int d, int I, int b, int cap_rows)
 }
 
 }  // namespace gg
+
+bool grouped_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, int elem_bytes, const void *base, uint64_t inner,
+                     uint64_t rows, uint32_t box_inner, uint32_t box_rows, bool sw128)
+{
+    auto fn = gg::encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * static_cast<cuuint64_t>(elem_bytes)};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int grouped_sm_count() { return gg::sm_count(); }
+
+moe_status_t grouped_combine_launch(const float *yr, const int32_t *ids, int M, int k, int d, int E, void *y,
+                                    bool y_f32, cudaStream_t s)
+{
+    const int64_t n = static_cast<int64_t>(M) * (d / 4);
+    const int cb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    if (y_f32)
+        gg::combine_kernel<float><<<cb, 256, 0, s>>>(yr, ids, M, k, d, E, static_cast<float *>(y));
+    else
+        gg::combine_kernel<__nv_bfloat16><<<cb, 256, 0, s>>>(yr, ids, M, k, d, E, static_cast<__nv_bfloat16 *>(y));
+    return launch_status();
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -582,7 +613,9 @@ MOE_API moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_
 {
     if (M < 0 || k < 1 || d < 1 || I < 1 || b < 1 || cap_rows < 0 || !bytes)
         return MOE_ERR_INVALID_ARG;
-    *bytes = ws_layout(M, k, d, I, b, cap_rows).total;
+    // one size for both weight formats: the MXFP8 layout or the AWQ one
+    const size_t mx = ws_layout(M, k, d, I, b, cap_rows).total, aw = grouped_awq_workspace(M, k, d, I, cap_rows);
+    *bytes = mx > aw ? mx : aw;
     return MOE_OK;
 }
 
@@ -595,7 +628,10 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
 {
     if (M < 0 || d < 1 || k < 1 || !w13 || !w2)
         return MOE_ERR_INVALID_ARG;
-    if (w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8 || xdt != MOE_BF16)
+    const bool awq = w13->fmt == MOE_W_AWQ4 && w2->fmt == MOE_W_AWQ4;
+    if (!awq && (w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8 || xdt != MOE_BF16))
+        return MOE_ERR_UNSUPPORTED;
+    if (awq && xdt != MOE_FP16 && xdt != MOE_BF16)
         return MOE_ERR_UNSUPPORTED;
     if (ydt != MOE_BF16 && ydt != MOE_FP32)
         return MOE_ERR_UNSUPPORTED;
@@ -612,6 +648,23 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         return MOE_ERR_CAPACITY;
     if (M == 0)
         return MOE_OK;
+    if (awq) {
+        if (!x || !topk_ids || !topk_w || !y || !sorted_route_ids || !expert_ids || !num_rows_post_pad ||
+            !w13->q || !w2->q || !w13->scale || !w2->scale || !w13->zero || !w2->zero)
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned(w13->q, 16) || !aligned(w2->q, 16) || !aligned(w13->scale, 16) || !aligned(w2->scale, 16) ||
+            !aligned(w13->zero, 16) || !aligned(w2->zero, 16) || !aligned(x, 16) || !aligned(y, 16))
+            return MOE_ERR_INVALID_ARG;
+        if (static_cast<int64_t>(M) * (d / 4) > INT32_MAX || d > 8192 || I > 8192)
+            return MOE_ERR_UNSUPPORTED;
+        size_t need = 0;
+        moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows, &need);
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return MOE_ERR_WORKSPACE;
+        return grouped_awq_launch(x, xdt == MOE_BF16, M, d, I, E, topk_ids, topk_w, k, w13, w2, sorted_route_ids,
+                                  expert_ids, num_rows_post_pad, b, cap_rows, y, ydt == MOE_FP32, ws, dev_status,
+                                  as_stream(stream));
+    }
     if (!x || !topk_ids || !topk_w || !y || !sfa13 || !sfa2 || !sorted_route_ids || !expert_ids ||
         !num_rows_post_pad || !w13->q || !w2->q)
         return MOE_ERR_INVALID_ARG;
@@ -671,11 +724,5 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
     gemm_kernel<2><<<grid, kThreads, smem, s>>>(tA2, tB2, a2);
     if (launch_status() != MOE_OK)
         return MOE_ERR_CUDA;
-    const int64_t n = static_cast<int64_t>(M) * (d / 4);
-    const int cb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    if (ydt == MOE_FP32)
-        combine_kernel<float><<<cb, 256, 0, s>>>(yr, topk_ids, M, k, d, E, static_cast<float *>(y));
-    else
-        combine_kernel<__nv_bfloat16><<<cb, 256, 0, s>>>(yr, topk_ids, M, k, d, E, static_cast<__nv_bfloat16 *>(y));
-    return launch_status();
+    return grouped_combine_launch(yr, topk_ids, M, k, d, E, y, ydt == MOE_FP32, s);
 }
