@@ -168,10 +168,19 @@ def committed_traffic(kernel_key: str, src_hash: str):
     return d["bytes_per_launch"] if d.get("src_sha256") == src_hash else None
 
 
-def decode_src_hash() -> str:
+SRC_FILES = {
+    "decode": ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "decode_internal.h", "topk.cu",
+               "topk.cuh", "common.cuh", "tc.cuh"),
+    "grouped": ("grouped.cu", "grouped_awq.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh",
+                "tc.cuh"),
+}
+
+
+def decode_src_hash(path: str = "decode") -> str:
+    """SHA-256 over the kernel sources of one path (the ncu counters in
+    profiles/traffic.json are valid only for these exact sources)."""
     h = hashlib.sha256()
-    for f in ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "topk.cu", "topk.cuh", "common.cuh",
-              "tc.cuh", "grouped.cu", "align.cu"):
+    for f in SRC_FILES[path]:
         h.update(open(os.path.join(ROOT, "top_moe_expert_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
@@ -322,7 +331,7 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     t_hbm = total_bytes / (peak_gbs * 1e9)
     t_mma = flops / (peak_tf * 1e12)
     kern = st.layer_kernels()
-    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash())
+    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash(st.path))
     if t_mma > t_hbm:
         ach = flops / sec / 1e12 / world
         return {"kernel": kern, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_tf,
@@ -341,7 +350,9 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
 def run_ours(args, rank, world, device):
     wl = workload_from_name(args.workload)
     K, W = args.steps, args.warmup
-    path = args.path if args.path != "auto" else ("grouped" if wl.M >= 256 else "decode")
+    # measured crossover at d=2048, I=768, E=128, k=8: the output-centric path
+    # wins for a single token, the grouped path from M = 4 on
+    path = args.path if args.path != "auto" else ("decode" if wl.M <= 2 else "grouped")
     st = DecodeStep(wl, K + W, device, path, args.block)
     st.capture()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
