@@ -161,14 +161,15 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  *   y        [M][d] of ydt (MOE_BF16 or MOE_FP32)
  *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned; its
  *            first 256 bytes must be zero before the first call that uses
- *            it (e.g. cudaMemset once) -- every call leaves them zero again,
- *            except one that reports MOE_ERR_TIMEOUT, after which they must
- *            be zeroed again
+ *            it (e.g. cudaMemset once) and then left alone: they hold a
+ *            grid-barrier arrival counter that every call advances by a
+ *            multiple of the grid size (after a call that reports
+ *            MOE_ERR_TIMEOUT they must be zeroed again)
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
  * Kernels by case: w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
  * streaming kernel (each warp owns whole neurons: gate/up dots and the
  * down-column outer product; per-SM partial outputs reduced in a fixed order
- * after a grid-wide barrier whose counters live in ws[0..8)); other
+ * after a grid-wide barrier whose counter lives in ws[0..8)); other
  * MOE_W_MXFP8_T cases -> one streaming pass (gate/up rows and down columns of
  * each neuron together, per-SM partial outputs) plus a fixed-order reduction
  * kernel; MXFP8 with M*k <= 512 -> a gate/up kernel and a

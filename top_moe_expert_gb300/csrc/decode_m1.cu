@@ -27,9 +27,11 @@
 //     accumulators of the current block; the block's E8M0 scales are applied
 //     once, when the block closes.
 //   * Each CTA writes its partial of y; a grid-wide barrier (bounded spin
-//     on a counter in the workspace) then lets each CTA reduce a slice of
-//     outputs over all CTAs in a fixed order and write y.  The last CTA to
-//     leave resets the counters, so they are zero between calls.
+//     on a 64-bit arrival counter in the workspace) then lets each CTA
+//     reduce a slice of outputs over all CTAs in a fixed order and write y.
+//     The counter is never reset: every launch adds exactly one arrival per
+//     CTA, so a CTA that draws arrival number a waits for the count to reach
+//     the next multiple of the grid size above a (the counter starts at 0).
 // The CTAs of the grid must be resident together: the grid is one CTA per SM
 // and the kernel lets dependent launches start only after the barrier.
 #include "common.cuh"
@@ -56,7 +58,7 @@ struct Args {
     float *wts_out;
     const uint8_t *q13, *s13;    // [E][2I][d], [E][2I][d/32]
     const uint8_t *q2t, *s2t;    // [E][I][d],  [E][I/32][d]
-    unsigned int *bar;           // [0] arrivals, [1] departures (zero between calls)
+    unsigned long long *bar;     // arrivals: every launch adds one per CTA (starts at 0)
     float *partial;              // [G][d]
     void *y;
     int32_t *dev_status;
@@ -198,18 +200,21 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
 
     if (warp == kWarps) {
         // ------------------------------------------------ producer warp
-        if (lane == 0) {
-            for (int s = 0; s < kStages; ++s) {
-                tc::mbar_init(full0 + 8 * s, 1);
-                tc::mbar_init(empty0 + 8 * s, kWarps);
-            }
-            *abort_flag = 0;
-            tc::fence_mbar_init();
-        }
         int e;
         float w;
         if constexpr (ROUTE_PL > 0) {
-            topk_warp<ROUTE_PL>(a.logits, a.E, a.k, lane, e, w);
+            // the logits are the first bytes the step needs: their loads go
+            // out first, the barriers are set up while they arrive
+            topk_warp<ROUTE_PL>(a.logits, a.E, a.k, lane, e, w, [&] {
+                if (lane == 0) {
+                    for (int s = 0; s < kStages; ++s) {
+                        tc::mbar_init(full0 + 8 * s, 1);
+                        tc::mbar_init(empty0 + 8 * s, kWarps);
+                    }
+                    *abort_flag = 0;
+                    tc::fence_mbar_init();
+                }
+            });
             if (blockIdx.x == 0 && lane < a.k) {
                 if (a.ids_out)
                     a.ids_out[lane] = e;
@@ -219,6 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
         } else {
             e = lane < a.k ? __ldcg(a.ids + lane) : -1;
             w = lane < a.k ? __ldcg(a.wts + lane) : 0.f;
+            if (lane == 0) {
+                for (int s = 0; s < kStages; ++s) {
+                    tc::mbar_init(full0 + 8 * s, 1);
+                    tc::mbar_init(empty0 + 8 * s, kWarps);
+                }
+                *abort_flag = 0;
+                tc::fence_mbar_init();
+            }
         }
         const bool ok = lane < a.k && e >= 0 && e < a.E;
         const unsigned vm = __ballot_sync(0xffffffffu, ok);
@@ -457,14 +470,16 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        atomicAdd(a.bar, 1u);
+        const unsigned long long G = gridDim.x;
+        const unsigned long long mine = atomicAdd(a.bar, 1ull);
+        const unsigned long long target = (mine / G + 1) * G;
         const long long t0 = clock64();
         const long long limit = static_cast<long long>(kWaitNs) * 5 / 2;
         int ok = 1;
-        unsigned int v;
+        unsigned long long v;
         for (;;) {
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.bar) : "memory");
-            if (v >= gridDim.x)
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.bar) : "memory");
+            if (v >= target)
                 break;
             if (clock64() - t0 > limit) {
                 ok = 0;
@@ -517,15 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
             }
         }
     }
-    // ---- departure: the last CTA out resets both counters for the next call
-    __syncthreads();
-    if (tid == 0 && passed) {
-        const unsigned int old = atomicAdd(a.bar + 1, 1u);
-        if (old == gridDim.x - 1) {
-            atomicExch(a.bar, 0u);
-            atomicExch(a.bar + 1, 0u);
-        }
-    }
 }
 
 }  // namespace dm
@@ -573,7 +579,7 @@ moe_status_t decode_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const
     if (smem > 220 * 1024 || !aligned(y, 16))
         return MOE_ERR_UNSUPPORTED;
     uint8_t *w = static_cast<uint8_t *>(ws);
-    Args a{x,  ids, wts, logits, ids_out, wts_out, q13, s13, q2t, s2t, reinterpret_cast<unsigned int *>(w),
+    Args a{x,  ids, wts, logits, ids_out, wts_out, q13, s13, q2t, s2t, reinterpret_cast<unsigned long long *>(w),
            reinterpret_cast<float *>(w + 256), y, dev_status, y_f32 ? 1 : 0, k, d, I, E};
     auto go = [&](auto kern) -> moe_status_t {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
