@@ -55,6 +55,8 @@ def workload_from_name(name: str):
         return inputs.LARGE_M1
     if name == "large_m8":
         return inputs.LARGE_M8
+    if name == "awq_fixture_a":
+        return inputs.AWQ_FIXTURE
     if name == "probe_m16384":
         return inputs.Workload("grouped_probe_m16384_d2048_i768_e128_k8", M=16384, d=2048, I=768, E=128, k=8,
                                seed=2)
@@ -66,7 +68,12 @@ def workload_from_name(name: str):
 
 
 def expert_bytes(wl) -> int:
-    """MXFP8 bytes of one expert: 3*I*d codes + 3*I*d/32 scale bytes."""
+    """Weight bytes of one expert.  MXFP8: 3*I*d codes + 3*I*d/32 scale
+    bytes.  AWQ-4bit: 3*I*d/2 packed values + an fp16 scale and a 4-bit zero
+    per 128 values."""
+    if wl.fmt == "awq4":
+        n = 3 * wl.I * wl.d
+        return n // 2 + n // 128 * 2 + n // 128 // 2
     return 3 * wl.I * wl.d * 33 // 32
 
 
@@ -81,7 +88,8 @@ def step_bytes(wl, ids: np.ndarray) -> int:
     """Algorithmic bytes of one step: distinct routed experts' weights, the
     activations read (x, router logits) and the output written (bf16 y)."""
     distinct = len(np.unique(ids[(ids >= 0) & (ids < wl.E)]))
-    return distinct * expert_bytes(wl) + wl.M * wl.d * 2 + wl.M * wl.E * 4 + wl.M * wl.d * 2
+    routing = wl.M * wl.k * 8 if wl.routing == "fixture_a" else wl.M * wl.E * 4   # fixed ids/w, or logits
+    return distinct * expert_bytes(wl) + wl.M * wl.d * 2 + routing + wl.M * wl.d * 2
 
 
 def measured_mxfp8_tflops():
@@ -207,7 +215,11 @@ class DecodeStep:
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
         self.routed_in_layer = False
+        self.awq = wl.fmt == "awq4"
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
+        if self.awq:
+            self._init_awq(wl, nsteps, device, block)
+            return
         self.q13 = torch.empty((E, 2 * I, d), dtype=torch.uint8, device=device)
         self.s13 = torch.empty((E, 2 * I, d // 32), dtype=torch.uint8, device=device)
         self.q2 = torch.empty((E, d, I), dtype=torch.uint8, device=device)
@@ -257,11 +269,58 @@ class DecodeStep:
         self.stream = torch.cuda.Stream(device)
         torch.cuda.synchronize()
 
+    def _init_awq(self, wl, nsteps, device, block):
+        """The 4-bit AWQ layer on its fixed closed-form routing (fixture A):
+        a step is alignment + the grouped layer; activations fp16."""
+        moe = self.moe
+        from top_moe_expert_gb300 import inputs
+        E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
+        assert self.path == "grouped", "the AWQ layer runs on the grouped path"
+        dev_t = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
+        q13, s13, z13 = inputs.awq_weights(wl, "w13")
+        q2, s2, z2 = inputs.awq_weights(wl, "w2")
+        self.w13 = moe.Weights(moe.MOE_W_AWQ4, dev_t(q13), dev_t(s13).view(torch.float16), dev_t(z13))
+        self.w2 = moe.Weights(moe.MOE_W_AWQ4, dev_t(q2), dev_t(s2).view(torch.float16), dev_t(z2))
+        del q13, s13, z13, q2, s2, z2
+        self.fused = False
+        self.b = block or wl.b
+        self.sfa13 = self.sfa2 = None
+        self.fixed_ids = inputs.fixture_a_ids(M, k, E)
+        self.n_inputs = min(nsteps, 64)
+        self.logits_host = torch.zeros((self.n_inputs, M, E), dtype=torch.float32)   # routing is fixed
+        self.x_host = torch.stack([inputs.activations(wl, i, dtype=torch.float16) for i in range(self.n_inputs)])
+        self.logits_all = self.logits_host.to(device)
+        self.x_all = self.x_host.to(device)
+        self.logits = torch.empty((M, E), dtype=torch.float32, device=device)
+        self.x = torch.empty((M, d), dtype=torch.float16, device=device)
+        self.ids = torch.from_numpy(self.fixed_ids).to(device)
+        self.w = torch.from_numpy(inputs.fixture_a_weights(M, k, wl.seed)).to(device)
+        self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
+        cr, cb = moe.moe_align_capacity(M, k, E, self.b)
+        self.aligned = (torch.empty(cr, dtype=torch.int32, device=device),
+                        torch.empty(cb, dtype=torch.int32, device=device),
+                        torch.empty(1, dtype=torch.int32, device=device))
+        na = moe.moe_align_workspace_size(M, k, E, self.b)
+        self.ws_align = torch.empty(max(na, 256), dtype=torch.uint8, device=device) if na else None
+        self.ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, k, d, I, self.b, cr), dtype=torch.uint8,
+                              device=device)
+        self.stream = torch.cuda.Stream(device)
+        torch.cuda.synchronize()
+
+    def step_ids(self, j: int) -> np.ndarray:
+        """Expert ids of input j (to count the distinct experts a step reads)."""
+        if self.awq:
+            return self.fixed_ids
+        return host_topk_ids(self.logits_host[j].numpy(), self.wl.k)
+
     def launch_pre(self, stream=None):
         """Routing of the step: top-k (and, for the grouped path, alignment);
         nothing when the layer call routes the token itself."""
         moe = self.moe
         if self.routed_in_layer:
+            return
+        if self.awq:
+            moe.moe_align_block_size(self.ids, self.wl.E, self.b, out=self.aligned, ws=self.ws_align, stream=stream)
             return
         moe.moe_topk_softmax(self.logits, self.wl.k, self.ids, self.w, stream=stream)
         if self.path == "grouped":
@@ -284,6 +343,8 @@ class DecodeStep:
         self.launch_layer(stream)
 
     def layer_kernels(self) -> str:
+        if self.awq:
+            return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel<1> + ga::gemm_kernel<2> + combine"
         if self.path == "grouped":
             return "moe_ffn_grouped: act_quant + gemm_kernel<1> + gemm_kernel<2> + combine"
         if self.routed_in_layer:
@@ -295,7 +356,7 @@ class DecodeStep:
     def launches_per_step(self) -> int:
         if self.path == "grouped":
             na = 2 if self.ws_align is not None else 1
-            return 1 + na + 4
+            return na + 4 if self.awq else 1 + na + 4
         return 1 if self.routed_in_layer else 3
 
     def capture(self):
@@ -399,8 +460,7 @@ def run_ours(args, rank, world, device):
     total_ms = sum(step_ms)
 
     # bytes of every timed step (distinct experts of that step's routing)
-    logits_np = st.logits_host.numpy()
-    bytes_steps = [step_bytes(wl, host_topk_ids(logits_np[(W + i) % st.n_inputs], wl.k)) for i in range(K)]
+    bytes_steps = [step_bytes(wl, st.step_ids((W + i) % st.n_inputs)) for i in range(K)]
     total_bytes = float(sum(bytes_steps))
 
     # e2e: the same steps through the public API with host buffers (pinned)
@@ -446,7 +506,7 @@ def run_ours(args, rank, world, device):
     layer_ms = sum(a.elapsed_time(b) for a, b in zip(l0, l1))
     # (a layer call that routes the token itself also reads the logits)
     lb = step_bytes if st.routed_in_layer else layer_bytes
-    layer_total_bytes = float(sum(lb(wl, host_topk_ids(logits_np[(W + i) % st.n_inputs], wl.k)) for i in range(Kl)))
+    layer_total_bytes = float(sum(lb(wl, st.step_ids((W + i) % st.n_inputs)) for i in range(Kl)))
 
     # gather across replicas: max time, summed bytes
     t = torch.tensor([total_ms, total_bytes, e2e_ms, e2e_bytes, layer_ms, layer_total_bytes], dtype=torch.float64,
@@ -479,7 +539,7 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp8-weights/bf16-act/f32-accum",
+        "dtype": "awq4-weights/fp16-act/f32-accum" if st.awq else "mxfp8-weights/bf16-act/f32-accum",
         "data": "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
                 "N(0,1) router logits; fresh routing every step)",
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
@@ -520,6 +580,8 @@ def cpu_baseline(wl, device, path="decode", seconds=12.0):
             cache[(which, e)] = oracle.mxfp8_quantize(f)
         return cache[(which, e)]
 
+    if wl.fmt == "awq4":
+        return _cpu_baseline_awq(wl, seconds)
     mode = oracle.MODE_MX if path == "grouped" else oracle.MODE_EXACT
     S = min(wl.M, 4)
     t_total, nbytes, steps = 0.0, 0, 0
@@ -548,6 +610,81 @@ def cpu_baseline(wl, device, path="decode", seconds=12.0):
             "us_per_token": round(t_total / steps / S * 1e6, 1)}
 
 
+def _cpu_baseline_awq(wl, seconds):
+    """The oracle on the AWQ layer (fp16 h, as the grouped path computes):
+    the fixed routing of the first 4 tokens per step."""
+    import oracle
+    from top_moe_expert_gb300 import inputs
+    S = min(wl.M, 4)
+    ids = inputs.fixture_a_ids(wl.M, wl.k, wl.E)[:S]
+    w = inputs.fixture_a_weights(wl.M, wl.k, wl.seed)[:S].astype(np.float64)
+    experts = sorted(set(ids.reshape(-1).tolist()))
+    slot = np.full(wl.E, -1, dtype=np.int32)
+    slot[experts] = np.arange(len(experts), dtype=np.int32)
+    ws = {}
+    for which in ("w13", "w2"):
+        q, sc, z = inputs.awq_weights(wl, which, experts)
+        ws[which] = {"fmt": "awq4", "q": q, "s": sc, "z": z, "slot": slot}
+    t_total, nbytes, steps = 0.0, 0, 0
+    while t_total < seconds and steps < 64:
+        x = inputs.activations(wl, 10_000 + steps, dtype=torch.float16)[:S].to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, ids, w, wl.E, ws["w13"], ws["w2"], mode=oracle.MODE_H16)
+        t_total += time.perf_counter() - t0
+        nbytes += len(experts) * expert_bytes(wl) + S * 4 * wl.d
+        steps += 1
+    threads = min(oracle.num_threads(), S)
+    return {"value": nbytes / t_total / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{steps} steps (layer, binary64, fp16-h mode) of {wl.name} on {S} token(s) each, "
+                      f"fixed routing, {t_total:.1f} s timed",
+            "us_per_token": round(t_total / steps / S * 1e6, 1)}
+
+
+def _reference_awq(args, wl, world):
+    """--impl reference on the AWQ layer: each step one routed expert of
+    token 0 restricted to its first 128 neurons (one AWQ group of the down
+    projection), binary64 with fp16 h."""
+    import oracle
+    from top_moe_expert_gb300 import inputs
+    K, W = args.steps, args.warmup
+    Is = 128
+    e0 = int(inputs.fixture_a_ids(wl.M, wl.k, wl.E)[0, 0])
+    q13, s13, z13 = inputs.awq_weights(wl, "w13", [e0])
+    q2, s2, z2 = inputs.awq_weights(wl, "w2", [e0])
+    I = wl.I
+    rows = np.r_[0:Is, I:I + Is]
+    zrows = np.r_[0:Is // 8, I // 8:I // 8 + Is // 8]
+    slot = np.full(wl.E, -1, dtype=np.int32)
+    slot[e0] = 0
+    w13 = {"fmt": "awq4", "q": q13[:, rows], "s": s13[:, rows], "z": z13[:, zrows], "slot": slot}
+    kq = Is // 8
+    w2 = {"fmt": "awq4", "q": np.ascontiguousarray(q2[:, :, :kq]), "s": np.ascontiguousarray(s2[:, :, :Is // 128]),
+          "z": np.ascontiguousarray(z2[:, :, :Is // 128]), "slot": slot}
+    x = inputs.activations(wl, 0, dtype=torch.float16).to(torch.float64).numpy()[:1]
+    one = np.array([[e0]], dtype=np.int32)
+    wone = np.ones((1, 1))
+    per = 3 * Is * wl.d
+    sample_bytes = per // 2 + per // 128 * 2 + per // 256 + wl.d * 2 + wl.d * 2
+    nbytes, t_total = 0, 0.0
+    for i in range(W + K):
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, one, wone, wl.E, w13, w2, mode=oracle.MODE_H16)
+        dt = time.perf_counter() - t0
+        if i >= W:
+            t_total += dt
+            nbytes += sample_bytes
+    v = nbytes / t_total / 1e12
+    sample = (f"one routed expert of one token, first {Is} intermediate neurons, binary64 with fp16 h, "
+              f"{oracle.num_threads()} OpenMP thread(s) available (one token: 1 used)")
+    return {"metric": METRIC, "impl": "reference", "value": v, "unit": "TB/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": t_total * 1e3 / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
+                       "path": "CPU oracle (sample)"},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": v, "unit": "TB/s"},
+            "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle timed on the host cores (rank 0 only)."""
     if rank != 0:
@@ -561,6 +698,8 @@ def run_reference(args, rank, world):
     # token restricted to its first 64 intermediate neurons (gate/up rows
     # 0..63, down columns 0..63), so K+W steps stay within a few minutes.
     K, W = args.steps, args.warmup
+    if wl.fmt == "awq4":
+        return _reference_awq(args, wl, world)
     Is = 64
     logits = inputs.router_logits(wl, 0)
     ids, _ = oracle.topk_softmax(logits, wl.k)

@@ -15,12 +15,14 @@
 //          of equal expert with __match_any_sync, so the position of route r
 //          is off[e] + (#routes of e before r) exactly as the definition.
 // No atomics decide a position, so repeated calls give identical bits.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kAlignThreads = 256;
-constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kAlignThreads = 256;                 // multi-chunk kernels
+constexpr int kAlignThreads1 = 1024;               // the single-chunk placement
 constexpr int kChunk = 2048;                       // routes per CTA
 constexpr int kAlignMaxE = 1024;
 
@@ -33,6 +35,8 @@ align_hist_kernel(const int32_t *__restrict__ ids, int MK, int E,
 {
     extern __shared__ int32_t sm_hist[];
     __shared__ int inval;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int c = blockIdx.x;
     for (int e = threadIdx.x; e < E; e += kAlignThreads)
         sm_hist[e] = 0;
@@ -57,13 +61,16 @@ align_hist_kernel(const int32_t *__restrict__ ids, int MK, int E,
         atomicAdd(dev_status, inval);
 }
 
-// Block-wide exclusive scan of n <= 4*kAlignThreads ints in place; returns
-// the total to every thread.
+// Block-wide exclusive scan of n <= 4*THREADS ints in place; returns the
+// total to every thread.
+template <int THREADS>
 __device__ int block_exclusive_scan(int32_t *a, int n)
 {
+    constexpr int kAlignWarps = THREADS / 32;
     __shared__ int warp_tot[kAlignWarps];
     const int per = 4;
     const int base = threadIdx.x * per;
+    static_assert(THREADS * per >= 1024, "E up to 1024");
     int v[per];
     int s = 0;
 #pragma unroll
@@ -114,23 +121,30 @@ __device__ __forceinline__ int last_le(const int32_t *a, int n, int v)
 }
 
 // Pass 2: offsets, padding, tails and stable placement of one chunk.
-__global__ void __launch_bounds__(kAlignThreads)
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
 align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nchunks,
                    const int32_t *__restrict__ hist,      // [nchunks][E] or null (1 chunk)
                    int32_t *__restrict__ sorted_ids, int32_t *__restrict__ expert_ids,
                    int32_t *__restrict__ num_rows_post_pad, int cap_rows, int cap_blocks,
                    int32_t *__restrict__ dev_status)
 {
+    constexpr int kAlignThreads = THREADS, kAlignWarps = THREADS / 32;
     extern __shared__ int32_t sm[];
     int32_t *tot = sm;                 // [E] routes of expert e
     int32_t *cbase = sm + E;           // [E] routes of e in earlier chunks
     int32_t *off = sm + 2 * E;         // [E] first aligned row of e
     int32_t *wcnt = sm + 3 * E;        // [kAlignWarps][E]
+    int32_t *s_ids = wcnt + kAlignWarps * E;   // [kChunk] this chunk's ids
     __shared__ int inval;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int c = blockIdx.x;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int r0 = c * kChunk, r1 = min(MK, r0 + kChunk);
 
+    for (int r = r0 + threadIdx.x; r < r1; r += kAlignThreads)
+        s_ids[r - r0] = __ldg(ids + r);
     for (int i = threadIdx.x; i < (3 + kAlignWarps) * E; i += kAlignThreads)
         sm[i] = 0;
     if (threadIdx.x == 0)
@@ -140,7 +154,7 @@ align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nc
         // single chunk: histogram here
         int my_inval = 0;
         for (int r = r0 + threadIdx.x; r < r1; r += kAlignThreads) {
-            int e = ids[r];
+            int e = s_ids[r - r0];
             if (valid_id(e, E))
                 atomicAdd(&tot[e], 1);
             else
@@ -167,7 +181,7 @@ align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nc
     for (int e = threadIdx.x; e < E; e += kAlignThreads)
         off[e] = (tot[e] + b - 1) / b * b;
     __syncthreads();
-    const int total_rows = block_exclusive_scan(off, E);
+    const int total_rows = block_exclusive_scan<THREADS>(off, E);
 
     // bookkeeping, spread over all CTAs' threads: every aligned row that is
     // padding (its expert's rows end before it) and every row past the end
@@ -198,7 +212,7 @@ align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nc
     const int s0 = min(r1, r0 + w * slice), s1 = min(r1, s0 + slice);
     int32_t *mycnt = wcnt + w * E;
     for (int r = s0 + lane; r < s1; r += 32) {
-        int e = ids[r];
+        int e = s_ids[r - r0];
         if (valid_id(e, E))
             atomicAdd(&mycnt[e], 1);
     }
@@ -215,7 +229,7 @@ align_place_kernel(const int32_t *__restrict__ ids, int MK, int E, int b, int nc
     for (int base = s0; base < s1; base += 32) {
         const int r = base + lane;
         const bool in = r < s1;
-        const int e = in ? ids[r] : -1;
+        const int e = in ? s_ids[r - r0] : -1;
         const bool ok = in && valid_id(e, E);
         const unsigned key = ok ? static_cast<unsigned>(e) : 0xffffffffu;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
@@ -294,17 +308,40 @@ MOE_API moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, in
 
     const int nchunks = static_cast<int>(mk > 0 ? (mk + kChunk - 1) / kChunk : 1);
     cudaStream_t s = as_stream(stream);
-    const size_t place_smem = static_cast<size_t>(3 + kAlignWarps) * E * sizeof(int32_t);
     int32_t *hist = nullptr;
     if (nchunks > 1) {
         hist = static_cast<int32_t *>(ws);
-        align_hist_kernel<<<nchunks, kAlignThreads, E * sizeof(int32_t), s>>>(
-            topk_ids, static_cast<int>(mk), E, hist, dev_status);
-        if (launch_status() != MOE_OK)
+        if (launch_pdl(align_hist_kernel, dim3(nchunks), dim3(kAlignThreads), E * sizeof(int32_t), s, topk_ids,
+                       static_cast<int>(mk), E, hist, dev_status) != cudaSuccess)
             return MOE_ERR_CUDA;
+        const size_t smem = (static_cast<size_t>(3 + kAlignThreads / 32) * E + kChunk) * sizeof(int32_t);
+        static std::once_flag once_m;
+        static bool attr_m = false;
+        std::call_once(once_m, [] {
+            attr_m = cudaFuncSetAttribute(align_place_kernel<kAlignThreads>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) == cudaSuccess;
+        });
+        if (!attr_m || smem > 100 * 1024)
+            return MOE_ERR_CUDA;
+        return launch_pdl(align_place_kernel<kAlignThreads>, dim3(nchunks), dim3(kAlignThreads), smem, s, topk_ids,
+                          static_cast<int>(mk), E, b, nchunks, static_cast<const int32_t *>(hist), sorted_route_ids,
+                          expert_ids, num_rows_post_pad, cap_rows, cap_blocks, dev_status) == cudaSuccess
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
     }
-    align_place_kernel<<<nchunks, kAlignThreads, place_smem, s>>>(
-        topk_ids, static_cast<int>(mk), E, b, nchunks, hist, sorted_route_ids, expert_ids,
-        num_rows_post_pad, cap_rows, cap_blocks, dev_status);
-    return launch_status();
+    // one chunk: a single CTA of 1024 threads does everything
+    const size_t smem = (static_cast<size_t>(3 + kAlignThreads1 / 32) * E + kChunk) * sizeof(int32_t);
+    static std::once_flag once;
+    static bool attr_ok = false;
+    std::call_once(once, [] {
+        attr_ok = cudaFuncSetAttribute(align_place_kernel<kAlignThreads1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       200 * 1024) == cudaSuccess;
+    });
+    if (!attr_ok || smem > 200 * 1024)
+        return MOE_ERR_CUDA;
+    return launch_pdl(align_place_kernel<kAlignThreads1>, dim3(1), dim3(kAlignThreads1), smem, s, topk_ids,
+                      static_cast<int>(mk), E, b, 1, static_cast<const int32_t *>(nullptr), sorted_route_ids,
+                      expert_ids, num_rows_post_pad, cap_rows, cap_blocks, dev_status) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }

@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__r
                                                         const int32_t *__restrict__ npp, int b, int nsf,
                                                         uint8_t *__restrict__ xq, uint8_t *__restrict__ xs)
 {
+    // chained by programmatic dependent launch: the alignment must be done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int rows = *npp;
     const int nblk = d / 32, KT = d / 128;
@@ -227,6 +230,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // set-up above overlapped the previous kernel; its outputs are read below
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 
     const int n_blocks = *a.npp / a.b;
     const int total = n_blocks * a.n_mt;
@@ -443,6 +449,8 @@ template <typename YT>
 __global__ void combine_kernel(const float *__restrict__ yr, const int32_t *__restrict__ ids, int M, int k, int d,
                                int E, YT *__restrict__ y)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int d4 = d >> 2;
     const int total = M * d4;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -564,11 +572,11 @@ moe_status_t grouped_combine_launch(const float *yr, const int32_t *ids, int M, 
 {
     const int64_t n = static_cast<int64_t>(M) * (d / 4);
     const int cb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    if (y_f32)
-        gg::combine_kernel<float><<<cb, 256, 0, s>>>(yr, ids, M, k, d, E, static_cast<float *>(y));
-    else
-        gg::combine_kernel<__nv_bfloat16><<<cb, 256, 0, s>>>(yr, ids, M, k, d, E, static_cast<__nv_bfloat16 *>(y));
-    return launch_status();
+    const cudaError_t e = y_f32 ? launch_pdl(gg::combine_kernel<float>, dim3(cb), dim3(256), 0, s, yr, ids, M, k, d, E,
+                                             static_cast<float *>(y))
+                                : launch_pdl(gg::combine_kernel<__nv_bfloat16>, dim3(cb), dim3(256), 0, s, yr, ids, M, k,
+                                             d, E, static_cast<__nv_bfloat16 *>(y));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe
@@ -691,9 +699,8 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         !tmap_u8(&tB2, hq, I, cap_rows, n_mma))
         return MOE_ERR_CUDA;
 
-    act_quant_kernel<<<sm_count() * 4, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk),
-                                                    sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs);
-    if (launch_status() != MOE_OK)
+    if (launch_pdl(act_quant_kernel, dim3(sm_count() * 4), dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(x), d,
+                   k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     const int stage_bytes = (16384 + n_mma * 128 + 512 + nsf * 512 + 1023) & ~1023;
@@ -716,13 +723,11 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
 
     Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
             hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I, stages};
-    gemm_kernel<1><<<grid, kThreads, smem, s>>>(tA1, tB1, a1);
-    if (launch_status() != MOE_OK)
+    if (launch_pdl(gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, tA1, tB1, a1) != cudaSuccess)
         return MOE_ERR_CUDA;
     Args a2{static_cast<const uint8_t *>(sfa2), hs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
             nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d, stages};
-    gemm_kernel<2><<<grid, kThreads, smem, s>>>(tA2, tB2, a2);
-    if (launch_status() != MOE_OK)
+    if (launch_pdl(gemm_kernel<2>, dim3(grid), dim3(kThreads), smem, s, tA2, tB2, a2) != cudaSuccess)
         return MOE_ERR_CUDA;
     return grouped_combine_launch(yr, topk_ids, M, k, d, E, y, ydt == MOE_FP32, s);
 }

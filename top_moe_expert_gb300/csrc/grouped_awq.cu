@@ -134,6 +134,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 
     const int n_blocks = *a.npp / a.b;
     const int total = n_blocks * a.n_mt;
@@ -367,6 +369,8 @@ template <typename XT>
 __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, const int32_t *__restrict__ sorted,
                               const int32_t *__restrict__ npp, __half *__restrict__ xg)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int rows = *npp;
     const int d8 = d / 8;
     const int64_t total = static_cast<int64_t>(rows) * d8;
@@ -444,13 +448,12 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
         return MOE_ERR_CUDA;
 
     const int gblocks = grouped_sm_count() * 4;
-    if (x_bf16)
-        gather_kernel<__nv_bfloat16><<<gblocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), d, k,
-                                                             static_cast<int>(mk), sorted, npp, xg);
-    else
-        gather_kernel<__half><<<gblocks, 256, 0, s>>>(static_cast<const __half *>(x), d, k, static_cast<int>(mk),
-                                                      sorted, npp, xg);
-    if (launch_status() != MOE_OK)
+    const cudaError_t ge =
+        x_bf16 ? launch_pdl(gather_kernel<__nv_bfloat16>, dim3(gblocks), dim3(256), 0, s,
+                            static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk), sorted, npp, xg)
+               : launch_pdl(gather_kernel<__half>, dim3(gblocks), dim3(256), 0, s, static_cast<const __half *>(x), d, k,
+                            static_cast<int>(mk), sorted, npp, xg);
+    if (ge != cudaSuccess)
         return MOE_ERR_CUDA;
 
     const int G1 = d / 128, G2 = I / 128, Gmax = G1 > G2 ? G1 : G2;
@@ -474,13 +477,11 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     const int grid = grouped_sm_count();
     Args a1{static_cast<const uint16_t *>(w13->scale), static_cast<const int32_t *>(w13->zero), expert_ids, npp, sorted,
             wts, hg, nullptr, dev_status, b, n_mma, I / 64, d / 64, I, d, static_cast<int>(mk), 2 * I, G1, stages};
-    gemm_kernel<1><<<grid, kThreads, smem, s>>>(tQ1, tB1, a1);
-    if (launch_status() != MOE_OK)
+    if (launch_pdl(gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, a1) != cudaSuccess)
         return MOE_ERR_CUDA;
     Args a2{static_cast<const uint16_t *>(w2->scale), static_cast<const int32_t *>(w2->zero), expert_ids, npp, sorted,
             wts, nullptr, yr, dev_status, b, n_mma, d / 128, I / 64, I, d, static_cast<int>(mk), d, G2, stages};
-    gemm_kernel<2><<<grid, kThreads, smem, s>>>(tQ2, tB2, a2);
-    if (launch_status() != MOE_OK)
+    if (launch_pdl(gemm_kernel<2>, dim3(grid), dim3(kThreads), smem, s, tQ2, tB2, a2) != cudaSuccess)
         return MOE_ERR_CUDA;
     return grouped_combine_launch(yr, ids, M, k, d, E, y, y_f32, s);
 }

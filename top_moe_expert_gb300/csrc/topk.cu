@@ -13,7 +13,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 topk_softmax_kernel(const float *__restrict__ logits, int M, int E, int k,
                     int32_t *__restrict__ ids, float *__restrict__ wts)
 {
-    // let the next kernel (the layer) get resident; it waits for us itself
+    // the logits may come from the previous kernel; the next kernel may get
+    // resident now (it waits for this one itself)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
@@ -44,13 +46,14 @@ MOE_API moe_status_t moe_topk_softmax(const float *logits, int32_t M, int32_t E,
     dim3 grid((M + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
     cudaStream_t s = as_stream(stream);
     int per_lane = (E + 31) / 32;
+    cudaError_t e;
     if (per_lane <= 4)
-        topk_softmax_kernel<4><<<grid, block, 0, s>>>(logits, M, E, k, topk_ids, topk_w);
+        e = launch_pdl(topk_softmax_kernel<4>, grid, block, 0, s, logits, M, E, k, topk_ids, topk_w);
     else if (per_lane <= 16)
-        topk_softmax_kernel<16><<<grid, block, 0, s>>>(logits, M, E, k, topk_ids, topk_w);
+        e = launch_pdl(topk_softmax_kernel<16>, grid, block, 0, s, logits, M, E, k, topk_ids, topk_w);
     else if (per_lane <= 32)
-        topk_softmax_kernel<32><<<grid, block, 0, s>>>(logits, M, E, k, topk_ids, topk_w);
+        e = launch_pdl(topk_softmax_kernel<32>, grid, block, 0, s, logits, M, E, k, topk_ids, topk_w);
     else
-        topk_softmax_kernel<kTopkMaxPerLane><<<grid, block, 0, s>>>(logits, M, E, k, topk_ids, topk_w);
-    return launch_status();
+        e = launch_pdl(topk_softmax_kernel<kTopkMaxPerLane>, grid, block, 0, s, logits, M, E, k, topk_ids, topk_w);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
