@@ -65,7 +65,8 @@ struct Args {
     int y_f32, k, d, I, E;
 };
 
-// stage layout: gate rows | up rows | W2 columns | gate E8M0 | up E8M0 | W2 E8M0 row
+// stage layout: gate rows | up rows | W2 columns | gate E8M0 | up E8M0 |
+// W2 E8M0 row of the block the stage opens | of the block it crosses into
 struct Geo {
     int d;
     __host__ __device__ int gate_off() const { return 0; }
@@ -74,7 +75,7 @@ struct Geo {
     __host__ __device__ int gs_off() const { return 3 * kR * d; }
     __host__ __device__ int us_off() const { return 3 * kR * d + kR * (d / 32); }
     __host__ __device__ int s2_off() const { return 3 * kR * d + 2 * kR * (d / 32); }
-    __host__ __device__ int bytes() const { return 3 * kR * d + 2 * kR * (d / 32) + d; }
+    __host__ __device__ int bytes() const { return 3 * kR * d + 2 * kR * (d / 32) + 2 * d; }
 };
 
 __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two)
@@ -124,13 +125,12 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t h2)
     return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
 }
 
-// neurons [n, n + nr) of the next stage: at most kR, never across a route or
-// a 32-neuron scale block, never past the CTA's range
+// neurons [n, n + nr) of the next stage: at most kR, never across a route,
+// never past the CTA's range (a stage may straddle one 32-neuron scale block
+// boundary: kR < 32)
 __device__ __forceinline__ int stage_rows(int n, int left, int I)
 {
     int nr = kR;
-    const int to_blk = 32 - (n & 31);
-    nr = nr < to_blk ? nr : to_blk;
     nr = nr < I - n ? nr : I - n;
     return nr < left ? nr : left;
 }
@@ -146,7 +146,8 @@ __device__ __forceinline__ void set_status(int32_t *dev_status, int code)
 struct StageIt {
     int p, n, r, nr, s;
     uint32_t ph;
-    bool opens;      // first stage of a 32-neuron block in this CTA
+    bool opens;      // the stage's first neuron starts a 32-neuron block in this CTA
+    int cross;       // > 0: neuron `cross` of the stage starts the next block
     __device__ __forceinline__ void init(int p0, int p1, int I)
     {
         p = p0;
@@ -156,6 +157,7 @@ struct StageIt {
         ph = 0;
         opens = true;
         nr = p < p1 ? stage_rows(n, p1 - p, I) : 0;
+        cross = (n & 31) + nr > 32 ? 32 - (n & 31) : 0;
     }
     __device__ __forceinline__ void next(int p1, int I)
     {
@@ -171,6 +173,7 @@ struct StageIt {
         }
         opens = (n & 31) == 0;
         nr = p < p1 ? stage_rows(n, p1 - p, I) : 0;
+        cross = (n & 31) + nr > 32 ? 32 - (n & 31) : 0;
     }
 };
 
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
                 go = tc::mbar_wait(empty0 + 8 * it.s, it.ph ^ 1u, abort_flag, kWaitNs) ? 1 : 0;
                 if (go)
                     tc::mbar_arrive_expect_tx(full0 + 8 * it.s, static_cast<uint32_t>(it.nr) * (3 * d + 2 * (d / 32)) +
-                                                                    (it.opens ? d : 0));
+                                                                    (it.opens ? d : 0) + (it.cross ? d : 0));
             }
             if (!__shfl_sync(0xffffffffu, go, 0))
                 break;
@@ -280,6 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
                     tc::bulk_prefetch_l2(a.s13 + (grow + I) * (d / 32), pf.nr * (d / 32));
                     if (pf.opens)
                         tc::bulk_prefetch_l2(a.s2t + (static_cast<int64_t>(ex) * (I / 32) + (pf.n >> 5)) * d, d);
+                    if (pf.cross)
+                        tc::bulk_prefetch_l2(a.s2t + (static_cast<int64_t>(ex) * (I / 32) + (pf.n >> 5) + 1) * d, d);
                 }
             }
             // gate rows, up rows, W2 columns, gate E8M0, up E8M0, and the
@@ -298,6 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
                 if (it.opens)
                     tc::bulk_load(tc::smem_u32(st + geo.s2_off()),
                                   a.s2t + (static_cast<int64_t>(ex) * (I / 32) + (it.n >> 5)) * d, d, b);
+                if (it.cross)
+                    tc::bulk_load(tc::smem_u32(st + geo.s2_off() + d),
+                                  a.s2t + (static_cast<int64_t>(ex) * (I / 32) + (it.n >> 5) + 1) * d, d, b);
             }
             __syncwarp();
         }
@@ -387,20 +395,21 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
             if (store && lane == 0)
                 hbuf[par * 2 * kR + row * kR + wn] = acc;
         };
-        // a stage opening a block: close the previous block, take the new scales
-        auto open_block = [&](const StageIt &it, bool have) {
-            if (have) {
+        // close the current block: its products times its E8M0 scales
+        auto close_block = [&]() {
 #pragma unroll
-                for (int j = 0; j < OPL; ++j) {
-                    yacc[j] = fmaf(e8m0f((sblk >> (8 * j)) & 0xFFu), tacc[j], yacc[j]);
-                    tacc[j] = 0.f;
-                }
+            for (int j = 0; j < OPL; ++j) {
+                yacc[j] = fmaf(e8m0f((sblk >> (8 * j)) & 0xFFu), tacc[j], yacc[j]);
+                tacc[j] = 0.f;
             }
-            const uint8_t *sr = stages + it.s * geo.bytes() + geo.s2_off() + obase;
+        };
+        // this lane's E8M0 bytes of scale row `slot` of stage `it`
+        auto scale_row = [&](const StageIt &it, int slot) -> uint32_t {
+            const uint8_t *sr = stages + it.s * geo.bytes() + geo.s2_off() + slot * d + obase;
             if constexpr (OPL == 4)
-                sblk = *reinterpret_cast<const uint32_t *>(sr);
+                return *reinterpret_cast<const uint32_t *>(sr);
             else
-                sblk = *reinterpret_cast<const uint16_t *>(sr);
+                return *reinterpret_cast<const uint16_t *>(sr);
         };
 
         StageIt it;
@@ -411,9 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
                 set_status(a.dev_status, MOE_ERR_TIMEOUT);
             dot_phase(it, si & 1, wn < it.nr);
             if (it.opens) {
-                open_block(it, have);
+                if (have)
+                    close_block();
+                sblk = scale_row(it, 0);
                 have = true;
             }
+            const uint32_t sblk_next = it.cross ? scale_row(it, 1) : 0u;
             tc::named_bar(1, kWarps * 32);
             // outer phase: h of neuron `lane` of the stage, then the stage's
             // columns applied to this warp's outputs
@@ -436,6 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
             for (int nn = 0; nn < kR; ++nn) {
                 const float h = __shfl_sync(0xffffffffu, hl, nn);
                 const float2 hh = make_float2(h, h);
+                if (nn > 0 && nn == it.cross) {      // neuron nn starts the next block
+                    close_block();
+                    sblk = sblk_next;
+                }
                 if constexpr (OPL == 4) {
                     const float2 lo = half2_to_float2(e4m3x2_f16x2(qv[nn] & 0xFFFFu));
                     const float2 hi = half2_to_float2(e4m3x2_f16x2(qv[nn] >> 16));
@@ -503,14 +519,21 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
         const int c1 = static_cast<int>(static_cast<unsigned>(nch) * (blockIdx.x + 1) / gridDim.x);
         const int G = gridDim.x;
         const int g0 = G * lane / 32, g1 = G * (lane + 1) / 32;
+        constexpr int kMaxPer = 8;                 // partial rows per lane (G <= 256)
         for (int ch = c0 + warp; ch < c1; ch += kWarps + 1) {
+            // all of the lane's loads in flight at once, then added in order
+            float4 v[kMaxPer];
+#pragma unroll
+            for (int i = 0; i < kMaxPer; ++i)
+                v[i] = g0 + i < g1 ? __ldcg(reinterpret_cast<const float4 *>(a.partial + static_cast<int64_t>(g0 + i) * d) + ch)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int g = g0; g < g1; ++g) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.partial + static_cast<int64_t>(g) * d) + ch);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+#pragma unroll
+            for (int i = 0; i < kMaxPer; ++i) {
+                acc.x += v[i].x;
+                acc.y += v[i].y;
+                acc.z += v[i].z;
+                acc.w += v[i].w;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -551,8 +574,9 @@ static int m1_num_sms()
 
 bool decode_m1_eligible(int M, int k, int d, int I, int E)
 {
-    // (route, neuron) indices times the grid stay within 32 bits
-    return M == 1 && k >= 1 && k <= dm::kMaxK && (d == 1024 || d == 2048) && I % 32 == 0 && I >= 32 &&
+    // (route, neuron) indices times the grid stay within 32 bits; the final
+    // reduction takes at most 8 partial rows per lane (grid <= 256)
+    return m1_num_sms() <= 256 && M == 1 && k >= 1 && k <= dm::kMaxK && (d == 1024 || d == 2048) && I % 32 == 0 && I >= 32 &&
            I <= 65536 && E >= 1;
 }
 
