@@ -234,6 +234,21 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
  *     Hs uint8 [cap_rows/b][I/128][nsf][512]  their scales (same layout)
  *     Yr f32 [M*k][d]           w_route * (W2 h) per route
  *   with nsf = ceil(roundup16(b) / 128).
+ * 4-bit AWQ weights ("Route-Block Membership Selects Packed-AWQ
+ * Arithmetic", opening paragraph): w13 and w2 both MOE_W_AWQ4, x MOE_FP16
+ * or MOE_BF16, sfa13 / sfa2 unused (NULL).  The tensor cores take fp16 x fp16
+ * (tcgen05 kind::f16, FP32 accumulate): each weight tile is dequantized on
+ * chip to fp16 (q - z) * s (one rounding), x is rounded to fp16 and
+ * h = SiLU(g) * u is rounded to fp16 before the second GEMM.  ws is laid out
+ * as [Xg | Hg | Yr], each part rounded up to 256 bytes:
+ *     Xg fp16 [cap_rows][d]     x per aligned row (padding rows zero)
+ *     Hg fp16 [cap_rows][I]     h per aligned row
+ *     Yr f32 [M*k][d]           w_route * (W2 h) per route
+ *   Inside every run of 8 columns Xg and Hg hold the values in the order
+ *   0, 4, 1, 5, 2, 6, 3, 7 (the order the on-chip dequantization produces).
+ *   Extra limits: b <= 128, d % 256 == 0, d / 128 <= 64, I / 128 <= 64,
+ *   and b <= 112 when d > 8064 (MOE_ERR_UNSUPPORTED); scale and zero arrays
+ *   16-byte aligned (MOE_ERR_INVALID_ARG).
  * Limits: d % 128 == 0, I % 128 == 0, M * d / 4 <= INT32_MAX
  * (MOE_ERR_UNSUPPORTED otherwise); x and y 16-byte aligned
  * (MOE_ERR_INVALID_ARG otherwise). */

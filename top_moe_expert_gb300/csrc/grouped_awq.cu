@@ -15,16 +15,28 @@
 //   gemm_kernel<1>  : [g;u] = W13_e Xg^T; epilogue h = SiLU(g) * u -> fp16 Hg
 //   gemm_kernel<2>  : W2_e Hg^T; epilogue Yr[route] = w_route * acc
 //   combine         : y[t] = sum over slots j (in order) of Yr[t*k + j]
-// The A operand is dequantized on chip: TMA brings each stage's packed tile
-// (128 rows x 64 values = 32 bytes per row) and the activation tile into
-// shared memory; eight dequantizing warps turn the nibbles into fp16
+// The A operand is dequantized on chip into tensor memory: TMA brings each
+// k-step's packed tile (128 rows x 64 values = 32 bytes per row) and the
+// activation tile into shared memory, bulk copies bring each tile's group
+// scales and zeros, and dequantizing warps turn the nibbles into fp16
 // w = (q - z) * s -- (q - z) exactly through the 0x6400 exponent trick, one
-// rounding in the multiply -- written in the 128-byte-swizzled K-major layout
-// the MMA reads; a proxy fence then hands the tile to the MMA warp.
+// rounding in the multiply -- and store them with tcgen05.st as the MMA's A
+// operand: row m in TMEM lane m, two values per column.  Four warps (one per
+// TMEM lane quadrant) dequantize one k-step; kDqGroups such groups take the
+// k-steps in turn, so each has several k-steps' time for its chain of waits
+// and stores.  Shared memory then holds only the packed ring, deep enough to
+// cover DRAM latency.
 //
-// Roles (one CTA per SM, persistent over tiles): warp 0 TMA, warp 1 TMEM and
-// MMA issue, warps 2..5 epilogue, warps 6..13 dequantization.  Every
-// mbarrier wait is bounded; an expired wait records MOE_ERR_TIMEOUT in
+// K order inside the tensor-core operands.  One AND-OR of a packed word with
+// 0x000F000F | 0x64006400 yields nibbles i and i + 4 as an fp16 pair, so the
+// dequantized row holds each run of 8 values in the order
+// 0, 4, 1, 5, 2, 6, 3, 7.  The contraction does not care about the order of
+// its terms as long as both operands use the same one: the gather writes Xg
+// and the GEMM1 epilogue writes Hg in that order too (interleave_pos).
+//
+// Roles (one CTA per SM, persistent over tiles): warp 0 TMA and bulk copies,
+// warp 1 TMEM and MMA issue, warps 2..5 epilogue, warps 6.. dequantization.
+// Every mbarrier wait is bounded; an expired wait records MOE_ERR_TIMEOUT in
 // dev_status[1].
 #include <cuda.h>
 
@@ -38,13 +50,20 @@
 namespace moe {
 namespace ga {
 
-constexpr int kMaxStages = 12;
-constexpr int kDqWarps = 8;
-constexpr int kThreads = (6 + kDqWarps) * 32;   // 448
-constexpr uint32_t kTmemCols = 256;
-constexpr int kHeaderBytes = 512;
+constexpr int kMaxStages = 32;                   // packed ring
+constexpr int kDqGroups = 3;                     // groups of 4 dequantizing warps
+constexpr int kDqWarps = 4 * kDqGroups;
+constexpr int kEpiWarp0 = 3;                     // warps 3..6: epilogue
+constexpr int kDqWarp0 = 7;                      // warps 7..18: dequantization
+constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;   // 608
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxASlots = 7;                    // dequantized half-k-steps in TMEM, 64 columns each
+constexpr int kHeaderBytes = 1024;
 constexpr int kMaxG = 64;                        // K <= 8192
 constexpr uint64_t kWaitNs = 2000000000ull;
+
+// position of value j (0..7) inside its run of 8 in the operand order
+__host__ __device__ constexpr int interleave_pos(int j) { return ((j & 3) << 1) | (j >> 2); }
 
 struct Args {
     const uint16_t *s;        // scales [E*N][K/128] fp16 bits
@@ -56,35 +75,59 @@ struct Args {
     __half *hg;               // kind 1: [cap_rows][I]
     float *yr;                // kind 2: [MK][d]
     int32_t *dev_status;
-    int b, n_mma, n_mt, KT, I, d, MK, N, G, stages;
+    int b, n_mma, n_t, KT, I, d, MK, N, G, stages, aslots, acc_cols, nbuf;
 };
 
-// Stage: A tile (fp16 [128][64], swizzled) | B tile (fp16 [n_mma][64],
-// swizzled) | packed A [128][32 bytes]
+// A tile is 256 weight rows of one expert, in two halves of 128 that two MMA
+// issuers (warps 1 and 2) accumulate independently -- one issuing thread
+// cannot keep the tensor core busy with N = 16 MMAs.  Kind 1 pairs the gate
+// rows of 128 neurons (half 0) with the up rows of the same neurons (half 1),
+// so the SwiGLU epilogue finds g and u in the same TMEM lane; kind 2 takes
+// 256 consecutive output rows.
+//
+// A k-step covers 128 values of K -- one quantization group, so one scale
+// and zero per weight row.  A stage of the packed ring holds what TMA brings
+// for one k-step: the B operand as two 64-wide tiles (fp16 [n_mma][64] each,
+// 128-byte swizzled), shared by both halves, and the packed A tile
+// ([256][64 bytes]).  It is free again once the dequantizing warps have read
+// the packed bytes and both issuers' MMAs that read B have completed.  A
+// dequantized half-k-step ("unit") occupies 64 TMEM columns.
 struct Geo {
     int n_mma;
-    __host__ __device__ int a_off() const { return 0; }
-    __host__ __device__ int b_off() const { return 16384; }
-    __host__ __device__ int raw_off() const { return 16384 + n_mma * 128; }
-    __host__ __device__ int bytes() const { return (16384 + n_mma * 128 + 4096 + 1023) & ~1023; }
+    __host__ __device__ int b_off() const { return 0; }
+    __host__ __device__ int raw_off() const { return n_mma * 256; }
+    __host__ __device__ int bytes() const { return n_mma * 256 + 16384; }   // multiple of 1024 (n_mma % 8 == 0)
 };
 
-// row of expert e's weight matrix held by row m of an m-tile: kind 1 pairs
-// 64 gate rows with the same 64 neurons' up rows
-__device__ __forceinline__ int tile_row(int kind, int mt, int m, int I)
+// Nibbles 0 and 4 of `w` (bits 0..3 and 16..19) minus zero, times scale, as
+// an fp16 pair: 0x6400 | n is exactly 1024 + n in fp16, and zb holds 1024 + z.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w, uint32_t zb, uint32_t sc)
 {
-    return kind == 1 ? (m < 64 ? 64 * mt + m : I + 64 * mt + (m - 64)) : 128 * mt + m;
-}
-
-// Two 4-bit values (bits 0..3 and 4..7 of `byte`) minus zero, times scale,
-// as an fp16 pair: 0x6400 | n is exactly 1024 + n in fp16.
-__device__ __forceinline__ uint32_t dq_pair(uint32_t byte, __half2 zb, __half2 sc)
-{
-    const uint32_t v = 0x64006400u | (byte & 0xFu) | ((byte & 0xF0u) << 12);
-    const __half2 q = *reinterpret_cast<const __half2 *>(&v);
-    const __half2 r = __hmul2(__hsub2(q, zb), sc);
+    uint32_t v;
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(v) : "r"(w));   // (w & a) | b
+    const __half2 r = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&v), *reinterpret_cast<const __half2 *>(&zb)),
+                              *reinterpret_cast<const __half2 *>(&sc));
     return *reinterpret_cast<const uint32_t *>(&r);
 }
+
+// 32 packed values (4 words) -> 16 fp16 pairs, each run of 8 in the order
+// 0, 4, 1, 5, 2, 6, 3, 7
+__device__ __forceinline__ void dq_words(const uint4 &a, const uint4 &b, uint32_t zb2, uint32_t sc2, uint32_t (&out)[32])
+{
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        out[4 * c] = dq_pair(wd[c], zb2, sc2);
+        out[4 * c + 1] = dq_pair(wd[c] >> 4, zb2, sc2);
+        out[4 * c + 2] = dq_pair(wd[c] >> 8, zb2, sc2);
+        out[4 * c + 3] = dq_pair(wd[c] >> 12, zb2, sc2);
+    }
+}
+
+// Per-tile group scales and zeros, as copied from global memory: the scale
+// rows of the tile's 256 weight rows, [256][G] fp16, then their zero words,
+// [32][G] int32 (row r's zero in nibble r % 8 of word [r / 8][g]).
+__host__ __device__ inline int sbuf_bytes(int G) { return 640 * G; }
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -95,30 +138,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     const uint32_t raw = tc::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const Geo geo{a.n_mma};
-    const int S = a.stages, SB = geo.bytes();
+    // kDqGroups <= AS, ceil(AS / 2) < S
+    const int S = a.stages, SB = geo.bytes(), AS = a.aslots, NB = a.nbuf;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * SB);
-    const uint32_t rfull0 = tc::smem_u32(bars), afull0 = rfull0 + 8 * S, empty0 = afull0 + 8 * S;
-    const uint32_t accf0 = empty0 + 8 * S, acce0 = accf0 + 16, fin = acce0 + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 5);
+    const uint32_t rfull0 = tc::smem_u32(bars), rempty0 = rfull0 + 8 * S, afull0 = rempty0 + 8 * S;
+    const uint32_t accf0 = afull0 + 8 * AS;      // [half][buf]
+    const uint32_t acce0 = accf0 + 32;           // [half][buf]
+    const uint32_t sfull0 = acce0 + 32, sempty0 = sfull0 + 16, fin0 = sempty0 + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + AS + 14);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *ubuf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + kHeaderBytes);   // [2][2][32][33]
-    int *t_route = reinterpret_cast<int *>(ubuf + 4 * 32 * 33);                               // [256]
-    float *t_w = reinterpret_cast<float *>(t_route + 256);                                    // [256]
-    __half *sc_s = reinterpret_cast<__half *>(t_w + 256);                                     // [128][G]
-    uint8_t *zs_s = reinterpret_cast<uint8_t *>(sc_s + 128 * a.G);                            // [128][G]
-    const int nbuf = a.n_mma <= 128 ? 2 : 1;
+    int *t_route = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + kHeaderBytes);   // [256]
+    float *t_w = reinterpret_cast<float *>(t_route + 256);                                       // [256]
+    uint8_t *sbuf = reinterpret_cast<uint8_t *>(t_w + 256);                                      // [2][sbuf_bytes]
+    const int SBUF = sbuf_bytes(a.G);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(rfull0 + 8 * s, 1);
-            tc::mbar_init(afull0 + 8 * s, kDqWarps);
-            tc::mbar_init(empty0 + 8 * s, 1);
+            tc::mbar_init(rempty0 + 8 * s, 8 + 2);   // the k-step's two units' dequantizing warps + two commits
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int s = 0; s < AS; ++s)
+            tc::mbar_init(afull0 + 8 * s, 4);
+        for (int i = 0; i < 4; ++i) {
             tc::mbar_init(accf0 + 8 * i, 1);
             tc::mbar_init(acce0 + 8 * i, 4);
         }
-        tc::mbar_init(fin, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(sfull0 + 8 * i, 1);
+            tc::mbar_init(sempty0 + 8 * i, kDqWarps);
+            tc::mbar_init(fin0 + 8 * i, 1);
+        }
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -138,41 +187,59 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     asm volatile("griddepcontrol.launch_dependents;");
 
     const int n_blocks = *a.npp / a.b;
-    const int total = n_blocks * a.n_mt;
+    const int total = n_blocks * a.n_t;
     const int KT = a.KT;
+    const int G = a.G;
+    const uint32_t a_base = static_cast<uint32_t>(2 * NB * a.acc_cols);   // first A-unit column
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int s = 0, issued = 0;
+            int s = 0, issued = 0, ti = 0;
             uint32_t ph = 0;
-            const uint32_t tx = 128u * 32u + static_cast<uint32_t>(a.n_mma) * 128u;
-            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-                const int jb = t / a.n_mt, mt = t % a.n_mt;
+            const uint32_t tx = static_cast<uint32_t>(SB);
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
+                const int jb = t / a.n_t, T = t % a.n_t;
                 const int e = a.expert_ids[jb];
                 const int row0 = e * a.N;
+                // first weight row of each half
+                const int r0 = KIND == 1 ? row0 + 128 * T : row0 + 256 * T;
+                const int r1 = KIND == 1 ? row0 + a.I + 128 * T : row0 + 256 * T + 128;
+                // the tile's scales and zeros (buffer ti % 2, freed by the
+                // dequantizing warps when they finish tile ti - 2)
+                const int sb = ti & 1;
+                if (!tc::mbar_wait(sempty0 + 8 * sb, ((ti >> 1) & 1) ^ 1u, abort_flag, kWaitNs))
+                    break;
+                {
+                    const uint32_t fb = sfull0 + 8 * sb;
+                    const uint32_t dst = tc::smem_u32(sbuf + sb * SBUF);
+                    const int64_t zr0 = static_cast<int64_t>(e) * (a.N / 8) + (r0 - row0) / 8;
+                    const int64_t zr1 = static_cast<int64_t>(e) * (a.N / 8) + (r1 - row0) / 8;
+                    tc::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(SBUF));
+                    tc::bulk_load(dst, a.s + static_cast<int64_t>(r0) * G, 256u * G, fb);
+                    tc::bulk_load(dst + 256u * G, a.s + static_cast<int64_t>(r1) * G, 256u * G, fb);
+                    tc::bulk_load(dst + 512u * G, a.z + zr0 * G, 64u * G, fb);
+                    tc::bulk_load(dst + 576u * G, a.z + zr1 * G, 64u * G, fb);
+                }
                 for (int kt = 0; kt < KT; ++kt, ++issued) {
-                    if (!tc::mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, kWaitNs))
+                    if (!tc::mbar_wait(rempty0 + 8 * s, ph ^ 1u, abort_flag, kWaitNs))
                         break;
                     uint8_t *st = smem + s * SB;
                     const uint32_t fb = rfull0 + 8 * s;
                     tc::mbar_arrive_expect_tx(fb, tx);
-                    // packed A rows: 32 bytes (64 values) of each, x in bytes
-                    if (KIND == 1) {
-                        tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), &tmQ, kt * 32, row0 + 64 * mt, fb);
-                        tc::tma_load_2d(tc::smem_u32(st + geo.raw_off() + 64 * 32), &tmQ, kt * 32,
-                                        row0 + a.I + 64 * mt, fb);
-                    } else {
-                        tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), &tmQ, kt * 32, row0 + 128 * mt, fb);
-                    }
-                    // B tile: n_mma rows of 64 fp16, x in elements
-                    tc::tma_load_2d(tc::smem_u32(st + geo.b_off()), &tmB, kt * 64, jb * a.b, fb);
+                    // packed A rows: 64 bytes (128 values) of each, x in bytes
+                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), &tmQ, kt * 64, r0, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off() + 8192), &tmQ, kt * 64, r1, fb);
+                    // B: two tiles of n_mma rows x 64 fp16, x in elements
+                    tc::tma_load_2d(tc::smem_u32(st + geo.b_off()), &tmB, kt * 128, jb * a.b, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + geo.b_off() + a.n_mma * 128), &tmB, kt * 128 + 64, jb * a.b, fb);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
             }
+            // copies still in flight land before the CTA exits
             volatile int never = 0;
             const int n = issued < S ? issued : S;
             for (int i = 1; i <= n; ++i) {
@@ -184,54 +251,77 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 }
                 tc::mbar_wait(rfull0 + 8 * st, pp, &never, kWaitNs);
             }
+            for (int i = 1; i <= 2 && i <= ti; ++i)
+                tc::mbar_wait(sfull0 + 8 * ((ti - i) & 1), ((ti - i) >> 1) & 1u, &never, kWaitNs);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------ MMA issuers (warp 1: half 0, warp 2: half 1)
+        // The issuing thread's own instructions serialize with the MMA issue,
+        // so the loop keeps them few: descriptors advance by constants, one
+        // wait and one commit per k-step of 8 MMAs.  afull implies the
+        // stage's TMA data landed (the dequantizing warps waited for it
+        // before arriving), and the commit to rempty both frees the packed
+        // stage (with the other issuer's) and tells the dequantizing warps
+        // that the unit's TMEM columns have been read.
         if (lane == 0) {
-            int s = 0, ti = 0;
-            uint32_t ph = 0;
+            const int h = warp - 1;
+            int s = 0, ti = 0, sa = h;                // unit 2 i + h of k-step i sits in slot (2 i + h) % AS
+            uint32_t pha = 0;
             const uint32_t idesc = tc::idesc_f16(128, a.n_mma, false);
+            const uint64_t bd0 = tc::smem_desc(tc::smem_u32(smem + geo.b_off()), 16, 1024, tc::kLayoutSw128);
+            const uint64_t bd_step = static_cast<uint64_t>(SB >> 4);
+            const uint64_t bd_half = static_cast<uint64_t>(a.n_mma * 8);   // second B tile: n_mma * 128 bytes on
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
-                const int buf = nbuf == 2 ? (ti & 1) : 0;
-                const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
-                if (!tc::mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag, kWaitNs))
+                const int buf = NB == 2 ? (ti & 1) : 0;
+                const uint32_t use = static_cast<uint32_t>(NB == 2 ? (ti >> 1) : ti);
+                const int ab = h * 2 + buf;
+                if (!tc::mbar_wait(acce0 + 8 * ab, (use & 1u) ^ 1u, abort_flag, kWaitNs))
                     break;
                 tc::tc_fence_after();
-                const uint32_t acc = tmem + 128 * buf;
+                const uint32_t acc = tmem + static_cast<uint32_t>((h * NB + buf) * a.acc_cols);
+                uint64_t bd = bd0 + bd_step * static_cast<uint64_t>(s);
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!tc::mbar_wait(rfull0 + 8 * s, ph, abort_flag, kWaitNs) ||
-                        !tc::mbar_wait(afull0 + 8 * s, ph, abort_flag, kWaitNs))
+                    if (!tc::mbar_wait(afull0 + 8 * sa, pha, abort_flag, kWaitNs))
                         break;
                     tc::tc_fence_after();
-                    const uint32_t sa = tc::smem_u32(smem + s * SB + geo.a_off());
-                    const uint32_t sb = tc::smem_u32(smem + s * SB + geo.b_off());
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = tc::smem_desc(sa + 32 * kk, 16, 1024, tc::kLayoutSw128);
-                        const uint64_t bd = tc::smem_desc(sb + 32 * kk, 16, 1024, tc::kLayoutSw128);
-                        tc::mma_f16(acc, ad, bd, idesc, (kt | kk) != 0 ? 1u : 0u);
-                    }
-                    tc::tc_commit(empty0 + 8 * s);
+                    const uint32_t a_t = tmem + a_base + 64 * sa;
+                    // 16 values of K per MMA: 8 TMEM columns of A, 32 bytes of B
+                    tc::mma_f16_ts(acc, a_t, bd, idesc, kt != 0 ? 1u : 0u);
+                    tc::mma_f16_ts(acc, a_t + 8, bd + 2, idesc, 1u);
+                    tc::mma_f16_ts(acc, a_t + 16, bd + 4, idesc, 1u);
+                    tc::mma_f16_ts(acc, a_t + 24, bd + 6, idesc, 1u);
+                    tc::mma_f16_ts(acc, a_t + 32, bd + bd_half, idesc, 1u);
+                    tc::mma_f16_ts(acc, a_t + 40, bd + bd_half + 2, idesc, 1u);
+                    tc::mma_f16_ts(acc, a_t + 48, bd + bd_half + 4, idesc, 1u);
+                    tc::mma_f16_ts(acc, a_t + 56, bd + bd_half + 6, idesc, 1u);
+                    tc::tc_commit(rempty0 + 8 * s);
                     if (++s == S) {
                         s = 0;
-                        ph ^= 1u;
+                        bd = bd0;
+                    } else {
+                        bd += bd_step;
+                    }
+                    if ((sa += 2) >= AS) {
+                        sa -= AS;
+                        pha ^= 1u;
                     }
                 }
-                tc::tc_commit(accf0 + 8 * buf);
+                tc::tc_commit(accf0 + 8 * ab);
             }
-            tc::tc_commit(fin);
+            tc::tc_commit(fin0 + 8 * h);
             volatile int never = 0;
-            tc::mbar_wait(fin, 0, &never, kWaitNs);
+            tc::mbar_wait(fin0 + 8 * h, 0, &never, kWaitNs);
         }
-    } else if (warp < 6) {
-        // ------------------------------------------------ epilogue (warps 2..5)
+    } else if (warp < kDqWarp0) {
+        // ------------------------------------------------ epilogue (warps 3..6)
         const int q = warp & 3;                       // TMEM lane quadrant
-        const int etid = threadIdx.x - 64;
+        const int etid = threadIdx.x - kEpiWarp0 * 32;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
         int ti = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
-            const int jb = t / a.n_mt, mt = t % a.n_mt;
-            const int buf = nbuf == 2 ? (ti & 1) : 0;
-            const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
+            const int jb = t / a.n_t, T = t % a.n_t;
+            const int buf = NB == 2 ? (ti & 1) : 0;
+            const uint32_t use = static_cast<uint32_t>(NB == 2 ? (ti >> 1) : ti);
             const int rho0 = jb * a.b;
             if (KIND == 2) {
                 for (int c = etid; c < a.b; c += 128) {
@@ -240,120 +330,124 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     t_w[c] = r < a.MK ? a.wts[r] : 0.f;
                 }
             }
-            if (!tc::mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag, kWaitNs) && a.dev_status)
+            bool ok = tc::mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag, kWaitNs);
+            ok = tc::mbar_wait(accf0 + 8 * (2 + buf), use & 1u, abort_flag, kWaitNs) && ok;
+            if (!ok && a.dev_status)
                 atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
             tc::tc_fence_after();
             tc::named_bar(1, 128);
-            for (int c0 = 0, chunk = 0; c0 < a.b; c0 += 32, ++chunk) {
-                uint32_t v[32];
-                tc::tmem_ld_32x32b_x32(tmem + 128 * buf + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
-                tc::tmem_ld_wait();
+            const uint32_t acc0 = tmem + lane_off + static_cast<uint32_t>(buf * a.acc_cols);
+            const uint32_t acc1 = tmem + lane_off + static_cast<uint32_t>((NB + buf) * a.acc_cols);
+            for (int c0 = 0; c0 < a.b; c0 += 32) {
                 const int ncol = min(32, a.b - c0);
                 if (KIND == 1) {
-                    // gate quadrant q pairs with up quadrant q ^ 2 (same 32
-                    // neurons); each finishes half of the chunk's columns
-                    const bool is_gate = q < 2;
-                    float *ub = ubuf + ((chunk & 1) * 2 + (q & 1)) * 32 * 33 + lane * 33;
-                    const int keep = is_gate ? 0 : 16;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        ub[16 - keep + c] = __uint_as_float(is_gate ? v[16 + c] : v[c]);
-                    tc::named_bar(1, 128);
-                    const int n = 64 * mt + 32 * (q & 1) + lane;
-                    __half *hrow = a.hg + static_cast<int64_t>(rho0 + c0 + keep) * a.I + n;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float mine = __uint_as_float(is_gate ? v[c] : v[16 + c]);
-                        const float other = ub[keep + c];
-                        const float hv = is_gate ? silu_mul(mine, other) : silu_mul(other, mine);
-                        if (keep + c < ncol)
-                            hrow[static_cast<int64_t>(c) * a.I] = __float2half_rn(hv);
-                    }
-                } else {
-                    const int o = 128 * mt + 32 * q + lane;
-                    int rr[32];
-                    float ww[32];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int4 r4 = reinterpret_cast<const int4 *>(t_route + c0)[i];
-                        const float4 w4 = reinterpret_cast<const float4 *>(t_w + c0)[i];
-                        rr[4 * i] = r4.x;
-                        rr[4 * i + 1] = r4.y;
-                        rr[4 * i + 2] = r4.z;
-                        rr[4 * i + 3] = r4.w;
-                        ww[4 * i] = w4.x;
-                        ww[4 * i + 1] = w4.y;
-                        ww[4 * i + 2] = w4.z;
-                        ww[4 * i + 3] = w4.w;
-                    }
-                    float *yo = a.yr + o;
+                    // gate and up of neuron n share the lane; h -> column n of Hg in the operand order
+                    uint32_t g[32], u[32];
+                    tc::tmem_ld_32x32b_x32(acc0 + c0, g);
+                    tc::tmem_ld_32x32b_x32(acc1 + c0, u);
+                    tc::tmem_ld_wait();
+                    const int n = 128 * T + 32 * q + lane;
+                    __half *hrow = a.hg + static_cast<int64_t>(rho0 + c0) * a.I + (n & ~7) + interleave_pos(n & 7);
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        if (c < ncol && rr[c] < a.MK)
-                            yo[static_cast<int64_t>(rr[c]) * a.d] = ww[c] * __uint_as_float(v[c]);
+                        if (c < ncol)
+                            hrow[static_cast<int64_t>(c) * a.I] =
+                                __float2half_rn(silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c])));
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[32];
+                        tc::tmem_ld_32x32b_x32((h ? acc1 : acc0) + c0, v);
+                        tc::tmem_ld_wait();
+                        float *yo = a.yr + 256 * T + 128 * h + 32 * q + lane;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int r = t_route[c0 + c];   // same address in every lane: broadcast
+                            if (c < ncol && r < a.MK)
+                                yo[static_cast<int64_t>(r) * a.d] = t_w[c0 + c] * __uint_as_float(v[c]);
+                        }
+                    }
                 }
             }
             tc::tc_fence_before();
             tc::named_bar(1, 128);
-            if (lane == 0)
+            if (lane == 0) {
                 tc::mbar_arrive(acce0 + 8 * buf);
+                tc::mbar_arrive(acce0 + 8 * (2 + buf));
+            }
         }
     } else {
-        // ------------------------------------------------ dequantization (warps 6..13)
-        const int dt = threadIdx.x - 6 * 32;           // 0 .. 255
-        const int m = dt >> 1, half = dt & 1;          // row of the tile, 32-value half of its 64
-        int s = 0;
+        // ------------------------------------------------ dequantization (warps 7..18)
+        // Unit v = 2 i + h is half h of the CTA's k-step i (counted over all
+        // of its tiles); group g of four warps takes units g, g + kDqGroups,
+        // ...  Each thread dequantizes row m = 32 * quadrant + lane of the
+        // half into TMEM slot v % AS.
+        const int g = (warp - kDqWarp0) >> 2, q = warp & 3;
+        const int m = 32 * q + lane;
+        const int zsh = 4 * (m & 7);
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + a_base;
+        int v = g, sa = g, ti = 0;
+        int s = v >> 1;                               // stage of k-step v / 2 (< S) and its phase
         uint32_t ph = 0;
-        // every dequantizing thread walks all tiles (the named barriers below
-        // need all of them); after a timeout the waits return at once
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const int jb = t / a.n_mt, mt = t % a.n_mt;
-            const int e = a.expert_ids[jb];
-            // the tile's scales and zeros: row m's G groups
-            tc::named_bar(2, kDqWarps * 32);           // previous tile's values no longer read
-            {
-                const int row = tile_row(KIND, mt, m, a.I);
-                const int64_t gr = static_cast<int64_t>(e) * a.N + row;
-                const int64_t zr = (static_cast<int64_t>(e) * (a.N / 8) + row / 8) * a.G;
-                for (int g = half; g < a.G; g += 2) {
-                    sc_s[m * a.G + g] = __ushort_as_half(a.s[gr * a.G + g]);
-                    zs_s[m * a.G + g] = static_cast<uint8_t>((static_cast<uint32_t>(a.z[zr + g]) >> (4 * (row & 7))) & 0xFu);
-                }
-            }
-            tc::named_bar(2, kDqWarps * 32);
-            for (int kt = 0; kt < KT; ++kt) {
+        // after a timeout the waits return at once and the loops run out
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
+            const int sb = ti & 1;
+            if (!tc::mbar_wait(sfull0 + 8 * sb, (ti >> 1) & 1u, abort_flag, kWaitNs) && a.dev_status)
+                atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+            const uint16_t *sc = reinterpret_cast<const uint16_t *>(sbuf + sb * SBUF);
+            const uint32_t *zs = reinterpret_cast<const uint32_t *>(sbuf + sb * SBUF + 512 * G);
+            for (; (v >> 1) < (ti + 1) * KT;) {
+                const int i = v >> 1, h = v & 1;
+                const int kt = i - ti * KT;            // = the quantization group
+                const int r = 128 * h + m;             // row of the tile
+                const uint32_t sv = sc[r * G + kt];
+                const uint32_t zv = (zs[(r >> 3) * G + kt] >> zsh) & 0xFu;
+                const uint32_t sc2 = sv | (sv << 16), zb2 = 0x64006400u | zv | (zv << 16);
                 if (!tc::mbar_wait(rfull0 + 8 * s, ph, abort_flag, kWaitNs) && a.dev_status)
                     atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
-                uint8_t *st = smem + s * SB;
-                const uint4 w = *reinterpret_cast<const uint4 *>(st + geo.raw_off() + m * 32 + half * 16);
-                const int g = kt >> 1;                 // a 64-value k-tile lies in one group of 128
-                const __half sv = sc_s[m * a.G + g];
-                const __half zv = __float2half_rn(1024.0f + static_cast<float>(zs_s[m * a.G + g]));
-                const __half2 sc2 = __halves2half2(sv, sv), zb2 = __halves2half2(zv, zv);
-                const uint32_t ws_[4] = {w.x, w.y, w.z, w.w};
-                uint8_t *arow = st + geo.a_off() + m * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    // word c: values 8c .. 8c + 7 of this half -> 16-byte chunk 4 half + c
-                    const uint32_t wd = ws_[c];
-                    uint4 out;
-                    out.x = dq_pair(wd & 0xFFu, zb2, sc2);
-                    out.y = dq_pair((wd >> 8) & 0xFFu, zb2, sc2);
-                    out.z = dq_pair((wd >> 16) & 0xFFu, zb2, sc2);
-                    out.w = dq_pair(wd >> 24, zb2, sc2);
-                    const int chunk = 4 * half + c;
-                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (m & 7)) << 4)) = out;
-                }
-                // generic-proxy writes become visible to the tensor core
-                tc::fence_proxy_async_smem();
+                const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * SB + geo.raw_off() + r * 64);
+                const uint4 w0 = src[0], w1 = src[1], w2 = src[2], w3 = src[3];
                 __syncwarp();
                 if (lane == 0)
-                    tc::mbar_arrive(afull0 + 8 * s);
-                if (++s == a.stages) {
-                    s = 0;
+                    tc::mbar_arrive(rempty0 + 8 * s);  // packed bytes read
+                // slot sa is free once the MMAs of unit v - AS completed: the
+                // commits completed phase (i' / S) of k-step i' = (v - AS) / 2's stage
+                if (v >= AS) {
+                    const int ip = (v - AS) >> 1;
+                    if (!tc::mbar_wait(rempty0 + 8 * (ip % S), static_cast<uint32_t>(ip / S) & 1u, abort_flag,
+                                       kWaitNs) &&
+                        a.dev_status)
+                        atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+                }
+                tc::tc_fence_after();
+                {
+                    uint32_t out[32];
+                    dq_words(w0, w1, zb2, sc2, out);   // values 0..63 -> columns 0..31
+                    tc::tmem_st_32x32b_x32(a_lane + 64 * sa, out);
+                }
+                {
+                    uint32_t out[32];
+                    dq_words(w2, w3, zb2, sc2, out);   // values 64..127 -> columns 32..63
+                    tc::tmem_st_32x32b_x32(a_lane + 64 * sa + 32, out);
+                }
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(afull0 + 8 * sa);
+                // next unit: v + kDqGroups
+                const int di = ((v + kDqGroups) >> 1) - i;
+                v += kDqGroups;
+                if ((s += di) >= S) {
+                    s -= S;
                     ph ^= 1u;
                 }
+                if ((sa += kDqGroups) >= AS)
+                    sa -= AS;
             }
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive(sempty0 + 8 * sb);
         }
     }
     tc::tc_fence_before();
@@ -364,7 +458,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
 }
 
-// Xg[rho] = x[route / k] as fp16 (zero rows for padding); 8 values per thread
+// Xg[rho] = x[route / k] as fp16 (zero rows for padding), each run of 8 in
+// the operand order 0, 4, 1, 5, 2, 6, 3, 7; 8 values per thread
 template <typename XT>
 __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, const int32_t *__restrict__ sorted,
                               const int32_t *__restrict__ npp, __half *__restrict__ xg)
@@ -381,18 +476,16 @@ __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, co
         uint4 out = make_uint4(0, 0, 0, 0);
         if (r < MK) {
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(r / k) * d) + c);
-            if constexpr (sizeof(XT) == 2 && std::is_same<XT, __half>::value) {
-                out = v;
-            } else {
-                const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-                uint32_t o[4];
+            uint32_t o[4] = {v.x, v.y, v.z, v.w};     // fp16 pairs (0,1) (2,3) (4,5) (6,7)
+            if constexpr (!std::is_same<XT, __half>::value) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const __half2 h = __floats2half2_rn(__uint_as_float(vv[j] << 16), __uint_as_float(vv[j] & 0xFFFF0000u));
+                    const __half2 h = __floats2half2_rn(__uint_as_float(o[j] << 16), __uint_as_float(o[j] & 0xFFFF0000u));
                     o[j] = *reinterpret_cast<const uint32_t *>(&h);
                 }
-                out = make_uint4(o[0], o[1], o[2], o[3]);
             }
+            out = make_uint4(__byte_perm(o[0], o[2], 0x5410), __byte_perm(o[0], o[2], 0x7632),
+                             __byte_perm(o[1], o[3], 0x5410), __byte_perm(o[1], o[3], 0x7632));
         }
         reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(rho) * d)[c] = out;
     }
@@ -437,12 +530,40 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     __half *hg = reinterpret_cast<__half *>(w + L.hg);
     float *yr = reinterpret_cast<float *>(w + L.yr);
 
+    // launch configuration first: every check comes before the first launch
+    const int G1 = d / 128, G2 = I / 128, Gmax = G1 > G2 ? G1 : G2;
+    if (Gmax > kMaxG || n_mma > 128 || d % 256)
+        return MOE_ERR_UNSUPPORTED;
+    const int stage_bytes = Geo{n_mma}.bytes();
+    const size_t fixed = 1024 + kHeaderBytes + 512 * 4 + 2 * static_cast<size_t>(sbuf_bytes(Gmax));
+    int stages = static_cast<int>((227 * 1024 - fixed) / stage_bytes);
+    stages = stages > kMaxStages ? kMaxStages : stages;
+    // TMEM: accumulators [half][buf] of acc_cols columns, then the A units
+    const int acc_cols = (n_mma + 31) / 32 * 32;
+    const int nbuf = 4 * acc_cols + 64 * kDqGroups <= static_cast<int>(kTmemCols) ? 2 : 1;
+    int aslots = (static_cast<int>(kTmemCols) - 2 * nbuf * acc_cols) / 64;
+    aslots = aslots > kMaxASlots ? kMaxASlots : aslots;
+    aslots = aslots > 2 * stages - 2 ? 2 * stages - 2 : aslots;
+    const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
+    if (aslots < kDqGroups || smem > 227 * 1024)
+        return MOE_ERR_UNSUPPORTED;
+    static std::once_flag once;
+    static bool attr_ok = false;
+    std::call_once(once, [] {
+        attr_ok = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+                      cudaSuccess &&
+                  cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+                      cudaSuccess;
+    });
+    if (!attr_ok)
+        return MOE_ERR_CUDA;
+
     // tensor maps: packed weights as bytes [E*N][K/2]; activations fp16 [cap_rows][K]
     CUtensorMap tQ1, tB1, tQ2, tB2;
-    if (!grouped_tmap_2d(&tQ1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w13->q, d / 2, static_cast<uint64_t>(E) * 2 * I, 32,
-                         64, false) ||
+    if (!grouped_tmap_2d(&tQ1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w13->q, d / 2, static_cast<uint64_t>(E) * 2 * I, 64,
+                         128, false) ||
         !grouped_tmap_2d(&tB1, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xg, d, cap_rows, 64, n_mma, true) ||
-        !grouped_tmap_2d(&tQ2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w2->q, I / 2, static_cast<uint64_t>(E) * d, 32, 128,
+        !grouped_tmap_2d(&tQ2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w2->q, I / 2, static_cast<uint64_t>(E) * d, 64, 128,
                          false) ||
         !grouped_tmap_2d(&tB2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hg, I, cap_rows, 64, n_mma, true))
         return MOE_ERR_CUDA;
@@ -455,32 +576,15 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
                             static_cast<int>(mk), sorted, npp, xg);
     if (ge != cudaSuccess)
         return MOE_ERR_CUDA;
-
-    const int G1 = d / 128, G2 = I / 128, Gmax = G1 > G2 ? G1 : G2;
-    if (Gmax > kMaxG)
-        return MOE_ERR_UNSUPPORTED;
-    const int stage_bytes = Geo{n_mma}.bytes();
-    const size_t fixed = 1024 + kHeaderBytes + 4 * 32 * 33 * sizeof(float) + 512 * 4 + static_cast<size_t>(128) * Gmax * 3;
-    int stages = static_cast<int>((227 * 1024 - fixed) / stage_bytes);
-    stages = stages > kMaxStages ? kMaxStages : stages;
-    const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
-    static std::once_flag once;
-    static bool attr_ok = false;
-    std::call_once(once, [] {
-        attr_ok = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                      cudaSuccess &&
-                  cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                      cudaSuccess;
-    });
-    if (!attr_ok || stages < 2 || smem > 227 * 1024)
-        return MOE_ERR_CUDA;
     const int grid = grouped_sm_count();
     Args a1{static_cast<const uint16_t *>(w13->scale), static_cast<const int32_t *>(w13->zero), expert_ids, npp, sorted,
-            wts, hg, nullptr, dev_status, b, n_mma, I / 64, d / 64, I, d, static_cast<int>(mk), 2 * I, G1, stages};
+            wts, hg, nullptr, dev_status, b, n_mma, I / 128, d / 128, I, d, static_cast<int>(mk), 2 * I, G1, stages,
+            aslots, acc_cols, nbuf};
     if (launch_pdl(gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, a1) != cudaSuccess)
         return MOE_ERR_CUDA;
     Args a2{static_cast<const uint16_t *>(w2->scale), static_cast<const int32_t *>(w2->zero), expert_ids, npp, sorted,
-            wts, nullptr, yr, dev_status, b, n_mma, d / 128, I / 64, I, d, static_cast<int>(mk), d, G2, stages};
+            wts, nullptr, yr, dev_status, b, n_mma, d / 256, I / 128, I, d, static_cast<int>(mk), d, G2, stages,
+            aslots, acc_cols, nbuf};
     if (launch_pdl(gemm_kernel<2>, dim3(grid), dim3(kThreads), smem, s, tQ2, tB2, a2) != cudaSuccess)
         return MOE_ERR_CUDA;
     return grouped_combine_launch(yr, ids, M, k, d, E, y, y_f32, s);
