@@ -99,29 +99,49 @@ struct Geo {
     __host__ __device__ int bytes() const { return n_mma * 256 + 16384; }   // multiple of 1024 (n_mma % 8 == 0)
 };
 
-// Nibbles 0 and 4 of `w` (bits 0..3 and 16..19) minus zero, times scale, as
-// an fp16 pair: 0x6400 | n is exactly 1024 + n in fp16, and zb holds 1024 + z.
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w, uint32_t zb, uint32_t sc)
+// Packed word -> four fp16 pairs (n0, n4) (n1, n5) (n2, n6) (n3, n7), each
+// (n - z) * s with one rounding.  An AND-OR with 0x64006400 turns the nibbles
+// at bits 0..3 / 16..19 into 1024 + n (exact in fp16) and those at bits
+// 4..7 / 20..23 into 1024 + 16 n; (1024 + n) - (1024 + z) and
+// (1024 + 16 n) / 16 - (64 + z) are exact small integers, so the only
+// rounding is the multiply by s.  One shift per word reaches nibbles 2, 3,
+// 6 and 7; the integer pipe (half the rate of the fp16 pipe) does 5
+// operations per word.
+//   zb: 1024 + z in both halves; zb16: -(64 + z) in both halves; sc: s in both
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop_or(uint32_t w)
 {
     uint32_t v;
-    asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(v) : "r"(w));   // (w & a) | b
-    const __half2 r = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&v), *reinterpret_cast<const __half2 *>(&zb)),
-                              *reinterpret_cast<const __half2 *>(&sc));
-    return *reinterpret_cast<const uint32_t *>(&r);
+    asm("lop3.b32 %0, %1, %2, 0x64006400, 0xEA;" : "=r"(v) : "r"(w), "n"(MASK));   // (w & MASK) | 0x64006400
+    return v;
+}
+
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t zb, uint32_t zb16, uint32_t sc, uint32_t *out)
+{
+    const __half2 z2 = *reinterpret_cast<const __half2 *>(&zb), z16 = *reinterpret_cast<const __half2 *>(&zb16);
+    const __half2 s2 = *reinterpret_cast<const __half2 *>(&sc);
+    const __half2 r16 = __float2half2_rn(0.0625f);
+    const uint32_t w8 = w >> 8;
+    uint32_t t[4] = {lop_or<0x000F000Fu>(w), lop_or<0x00F000F0u>(w), lop_or<0x000F000Fu>(w8), lop_or<0x00F000F0u>(w8)};
+    __half2 r[4];
+    r[0] = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&t[0]), z2), s2);
+    r[1] = __hmul2(__hfma2(*reinterpret_cast<const __half2 *>(&t[1]), r16, z16), s2);
+    r[2] = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&t[2]), z2), s2);
+    r[3] = __hmul2(__hfma2(*reinterpret_cast<const __half2 *>(&t[3]), r16, z16), s2);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        out[j] = *reinterpret_cast<const uint32_t *>(&r[j]);
 }
 
 // 32 packed values (4 words) -> 16 fp16 pairs, each run of 8 in the order
 // 0, 4, 1, 5, 2, 6, 3, 7
-__device__ __forceinline__ void dq_words(const uint4 &a, const uint4 &b, uint32_t zb2, uint32_t sc2, uint32_t (&out)[32])
+__device__ __forceinline__ void dq_words(const uint4 &a, const uint4 &b, uint32_t zb2, uint32_t zb16, uint32_t sc2,
+                                         uint32_t (&out)[32])
 {
     const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        out[4 * c] = dq_pair(wd[c], zb2, sc2);
-        out[4 * c + 1] = dq_pair(wd[c] >> 4, zb2, sc2);
-        out[4 * c + 2] = dq_pair(wd[c] >> 8, zb2, sc2);
-        out[4 * c + 3] = dq_pair(wd[c] >> 12, zb2, sc2);
-    }
+    for (int c = 0; c < 8; ++c)
+        dq_word(wd[c], zb2, zb16, sc2, out + 4 * c);
 }
 
 // Per-tile group scales and zeros, as copied from global memory: the scale
@@ -403,6 +423,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 const uint32_t sv = sc[r * G + kt];
                 const uint32_t zv = (zs[(r >> 3) * G + kt] >> zsh) & 0xFu;
                 const uint32_t sc2 = sv | (sv << 16), zb2 = 0x64006400u | zv | (zv << 16);
+                const uint32_t zb16 = 0xD400D400u | (zv << 4) | (zv << 20);   // -(64 + z): ulp 1/16 in [64, 128)
                 if (!tc::mbar_wait(rfull0 + 8 * s, ph, abort_flag, kWaitNs) && a.dev_status)
                     atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
                 const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * SB + geo.raw_off() + r * 64);
@@ -422,12 +443,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 tc::tc_fence_after();
                 {
                     uint32_t out[32];
-                    dq_words(w0, w1, zb2, sc2, out);   // values 0..63 -> columns 0..31
+                    dq_words(w0, w1, zb2, zb16, sc2, out);   // values 0..63 -> columns 0..31
                     tc::tmem_st_32x32b_x32(a_lane + 64 * sa, out);
                 }
                 {
                     uint32_t out[32];
-                    dq_words(w2, w3, zb2, sc2, out);   // values 64..127 -> columns 32..63
+                    dq_words(w2, w3, zb2, zb16, sc2, out);   // values 64..127 -> columns 32..63
                     tc::tmem_st_32x32b_x32(a_lane + 64 * sa + 32, out);
                 }
                 tc::tmem_st_wait();
