@@ -540,10 +540,14 @@ def run_ours(args, rank, world, device):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "awq4-weights/fp16-act/f32-accum" if st.awq else "mxfp8-weights/bf16-act/f32-accum",
-        "data": "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
-                "N(0,1) router logits; fresh routing every step)",
+        "data": ("synthetic (seeded uniform 4-bit q and zeros, fp16 group scales U(0.005, 0.02), N(0,1) fp16 "
+                 "activations, the fixture-A routing of the packed-AWQ study)" if st.awq else
+                 "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
+                 "N(0,1) router logits; fresh routing every step)"),
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "path": ("expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
+                   "path": ("expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
+                            "dequantized into tensor memory + combine, b=%d)" % st.b if st.awq else
+                            "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
                             % st.b if st.path == "grouped" else
                             "single-token decode: routing + gate/up + SwiGLU + down + combine in one kernel"
                             if st.routed_in_layer else

@@ -1,5 +1,5 @@
-"""GPU parity of the 4-bit AWQ grouped path (tcgen05 kind::f16 after
-in-shared-memory dequantization) on the packed-AWQ study's alignment shape.
+"""GPU parity of the 4-bit AWQ grouped path (tcgen05 kind::f16 on weights
+dequantized into tensor memory) on the packed-AWQ study's alignment shape.
 
 The oracle runs with h rounded to fp16 (the GEMM2 operand of this path).
 Checked: the alignment of fixture A (168 routes -> 400 aligned rows in 50
@@ -86,3 +86,21 @@ def test_awq_grouped_small(xdt, b):
     ref = oracle.moe_layer(gs.x_exact(x.to(torch.float16)), ids, w.astype(np.float64), wl.E, layer.host13,
                            layer.host2, mode=oracle.MODE_H16)["y"]
     gs.assert_layer_close(y, ref)
+
+
+@pytest.mark.parametrize("d,b", [(1024, 136), (1152, 16)])
+def test_awq_grouped_limits_rejected(d, b):
+    """Blocks above 128 rows and d not a multiple of 256 are refused on the
+    host with MOE_ERR_UNSUPPORTED (before anything is launched)."""
+    wl = inputs.Workload("awq_grouped_limits", M=8, d=d, I=256, E=16, k=4, fmt="awq4", seed=9)
+    layer = gs.AwqLayer(wl)
+    x = inputs.activations(wl, dtype=torch.float16)
+    ids, w = gs.routing(wl)
+    tid = torch.from_numpy(ids).cuda()
+    aligned = moe.moe_align_block_size(tid, wl.E, b)
+    ws = torch.zeros(moe.moe_ffn_grouped_workspace_size(wl.M, wl.k, d, wl.I, b, aligned[0].numel()),
+                     dtype=torch.uint8, device="cuda")
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_ffn_grouped(x.cuda(), tid, torch.from_numpy(w).cuda(), layer.w13, layer.w2, None, None, aligned, b,
+                            ws=ws)
+    assert err.value.status == 2
