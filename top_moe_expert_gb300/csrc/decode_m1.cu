@@ -156,7 +156,12 @@ struct StageIt {
         s = 0;
         ph = 0;
         opens = true;
-        nr = p < p1 ? stage_rows(n, p1 - p, I) : 0;
+        // the range's remainder rows (beyond a multiple of kR) form the first
+        // stage: that short stage lands early and frees its slot for a full
+        // one, so a CTA with one row more than its neighbours does not wait
+        // an extra stage round trip at the end
+        const int f = (p1 - p0) % kR;
+        nr = p < p1 ? stage_rows(n, f ? f : kR, I) : 0;
         cross = (n & 31) + nr > 32 ? 32 - (n & 31) : 0;
     }
     __device__ __forceinline__ void next(int p1, int I)
@@ -200,15 +205,22 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
     const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kStages;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the grid barrier's epoch: the arrival counter is a multiple of the grid
+    // size between launches, and this CTA has not arrived yet, so the count
+    // read now rounds down to the arrivals of earlier launches
+    unsigned long long bar_epoch = 0;
+    if (tid == 0)
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(bar_epoch) : "l"(a.bar) : "memory");
 
     if (warp == kWarps) {
         // ------------------------------------------------ producer warp
         int e;
-        float w;
+        float w = 0.f, sl = 0.f;
         if constexpr (ROUTE_PL > 0) {
             // the logits are the first bytes the step needs: their loads go
-            // out first, the barriers are set up while they arrive
-            topk_warp<ROUTE_PL>(a.logits, a.E, a.k, lane, e, w, [&] {
+            // out first, the barriers are set up while they arrive; the
+            // weights are computed after the first copies are out
+            topk_select<ROUTE_PL>(a.logits, a.E, a.k, lane, e, sl, [&] {
                 if (lane == 0) {
                     for (int s = 0; s < kStages; ++s) {
                         tc::mbar_init(full0 + 8 * s, 1);
@@ -218,12 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
                     tc::fence_mbar_init();
                 }
             });
-            if (blockIdx.x == 0 && lane < a.k) {
-                if (a.ids_out)
-                    a.ids_out[lane] = e;
-                if (a.wts_out)
-                    a.wts_out[lane] = w;
-            }
         } else {
             e = lane < a.k ? __ldcg(a.ids + lane) : -1;
             w = lane < a.k ? __ldcg(a.wts + lane) : 0.f;
@@ -238,11 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
         }
         const bool ok = lane < a.k && e >= 0 && e < a.E;
         const unsigned vm = __ballot_sync(0xffffffffu, ok);
-        if (ok) {
-            const int i = __popc(vm & ((1u << lane) - 1u));
-            r_e[i] = e;
-            r_w[i] = w;
-        }
+        const int vi = __popc(vm & ((1u << lane) - 1u));
+        if (ok)
+            r_e[vi] = e;
         const int nv = __popc(vm);
         if (lane == 0) {
             *n_valid = nv;
@@ -250,8 +254,25 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
                 atomicAdd(a.dev_status, a.k - nv);
         }
         __syncwarp();
-        // routes and barriers are ready: release the compute warps, stream
-        tc::named_arrive(2, kThreads);
+        // the routing weights, then the compute warps go: done once the
+        // first ring-full of copies is out (those need only the expert ids)
+        bool released = false;
+        auto release = [&] {
+            if constexpr (ROUTE_PL > 0) {
+                w = topk_weight(sl, a.k, lane);
+                if (blockIdx.x == 0 && lane < a.k) {
+                    if (a.ids_out)
+                        a.ids_out[lane] = e;
+                    if (a.wts_out)
+                        a.wts_out[lane] = w;
+                }
+            }
+            if (ok)
+                r_w[vi] = w;
+            __syncwarp();
+            tc::named_arrive(2, kThreads);
+            released = true;
+        };
         const unsigned Ptot = static_cast<unsigned>(nv) * I;
         const int p0 = static_cast<int>(Ptot * blockIdx.x / gridDim.x);
         const int p1 = static_cast<int>(Ptot * (blockIdx.x + 1) / gridDim.x);
@@ -259,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
         it.init(p0, p1, I);
         int issued = 0;
         for (; it.p < p1; it.next(p1, I), ++issued) {
+            if (issued == kStages && !released)
+                release();
             int go = 1;
             if (lane == 0) {
                 go = tc::mbar_wait(empty0 + 8 * it.s, it.ph ^ 1u, abort_flag, kWaitNs) ? 1 : 0;
@@ -309,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
             }
             __syncwarp();
         }
+        if (!released)
+            release();
         // every issued copy lands before the CTA may finish
         if (lane == 0) {
             volatile int never = 0;
@@ -485,10 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
     // ---- grid barrier: every CTA's partial is visible before any is read
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
+        // a release add needs no reply: the CTA's partial (ordered before it
+        // by the barrier above) is visible to whoever sees the new count
         const unsigned long long G = gridDim.x;
-        const unsigned long long mine = atomicAdd(a.bar, 1ull);
-        const unsigned long long target = (mine / G + 1) * G;
+        const unsigned long long target = (bar_epoch / G + 1) * G;
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(a.bar) : "memory");
         const long long t0 = clock64();
         const long long limit = static_cast<long long>(kWaitNs) * 5 / 2;
         int ok = 1;
