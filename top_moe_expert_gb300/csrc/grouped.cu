@@ -444,7 +444,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
 // ---------------------------------------------------------------- combine
 // Four consecutive outputs per thread (d is a multiple of 128): 16-byte
-// loads of the k route rows, summed in slot order.
+// loads of the k route rows, summed in slot order.  The slot ids of a group
+// of 8 slots are loaded together, then all their rows, so a thread waits for
+// two memory round trips per 8 slots instead of two per slot.
 template <typename YT>
 __global__ void combine_kernel(const float *__restrict__ yr, const int32_t *__restrict__ ids, int M, int k, int d,
                                int E, YT *__restrict__ y)
@@ -456,14 +458,25 @@ __global__ void combine_kernel(const float *__restrict__ yr, const int32_t *__re
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
         const int t = i / d4, o4 = i - t * d4;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int e = __ldg(ids + t * k + j);
-            if (e >= 0 && e < E) {
-                const float4 v = __ldcs(reinterpret_cast<const float4 *>(yr + static_cast<int64_t>(t * k + j) * d) + o4);
-                s.x += v.x;
-                s.y += v.y;
-                s.z += v.z;
-                s.w += v.w;
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            int e[8];
+            float4 v[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                e[jj] = j0 + jj < k ? __ldg(ids + t * k + j0 + jj) : -1;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                v[jj] = e[jj] >= 0 && e[jj] < E
+                            ? __ldcs(reinterpret_cast<const float4 *>(yr + static_cast<int64_t>(t * k + j0 + jj) * d) + o4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (e[jj] >= 0 && e[jj] < E) {
+                    s.x += v[jj].x;
+                    s.y += v[jj].y;
+                    s.z += v[jj].z;
+                    s.w += v[jj].w;
+                }
             }
         }
         if constexpr (sizeof(YT) == 4) {
