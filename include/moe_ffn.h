@@ -224,7 +224,7 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
  *   of moe_align_block_size for the same ids, E and b (8 <= b <= 256,
  *   b % 8 == 0); y [M][d] bf16 or fp32;
  *   ws: moe_ffn_grouped_workspace_size bytes, 256-aligned, laid out as
- *   [Xq | Xs | Hq | Hs | Yr], each part rounded up to 256 bytes:
+ *   [Xq | Xs | Hq | Hs | Yr | D], each part rounded up to 256 bytes:
  *     Xq uint8 [cap_rows][d]    MXFP8 codes of x per aligned row (rows of
  *                               padding sentinels are zero)
  *     Xs uint8 [cap_rows/b][d/128][nsf][512]  their E8M0 scales, in the
@@ -233,6 +233,10 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
  *     Hq uint8 [cap_rows][I]    MXFP8 codes of SiLU(g)*u per aligned row
  *     Hs uint8 [cap_rows/b][I/128][nsf][512]  their scales (same layout)
  *     Yr f32 [M*k][d]           w_route * (W2 h) per route
+ *     D  int32 [cap_rows/b]     per block, how many first-GEMM tiles have
+ *                               written Hq/Hs (set by the call itself; both
+ *                               GEMMs run in one persistent kernel and a
+ *                               block's second-GEMM tiles wait for it)
  *   with nsf = ceil(roundup16(b) / 128).
  * 4-bit AWQ weights ("Route-Block Membership Selects Packed-AWQ
  * Arithmetic", opening paragraph): w13 and w2 both MOE_W_AWQ4, x MOE_FP16

@@ -100,13 +100,17 @@ __device__ __forceinline__ uint32_t to_e4m3(float u)
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__restrict__ x, int d, int k, int MK,
                                                         const int32_t *__restrict__ sorted,
                                                         const int32_t *__restrict__ npp, int b, int nsf,
-                                                        uint8_t *__restrict__ xq, uint8_t *__restrict__ xs)
+                                                        uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                                        int32_t *__restrict__ done)
 {
     // chained by programmatic dependent launch: the alignment must be done
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int rows = *npp;
+    // the GEMM's per-block counters of finished first-GEMM tiles start at 0
+    for (int jb = blockIdx.x * blockDim.x + threadIdx.x; jb < rows / b; jb += gridDim.x * blockDim.x)
+        done[jb] = 0;
     const int nblk = d / 32, KT = d / 128;
     const int nw = gridDim.x * (blockDim.x >> 5);
     for (int rho = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rho < rows; rho += nw) {
@@ -179,19 +183,44 @@ __global__ void prepare_sfa_kernel(const uint8_t *__restrict__ s, int E, int N, 
     }
 }
 
-// ---------------------------------------------------------------- the GEMM
-template <int KIND>
+// ---------------------------------------------------------------- the GEMMs
+// Both expert GEMMs in one persistent kernel.  The tile list is every
+// first-GEMM tile (W13 against the quantized activations; epilogue SwiGLU and
+// requantization into Hq/Hs), block-major, then every second-GEMM tile (W2
+// against Hq; epilogue w_route * acc per route).  CTA c takes tiles c,
+// c + grid, ..., so it finishes its first-GEMM tiles before any second-GEMM
+// tile.  A second-GEMM tile of block jb waits until all first-GEMM tiles of
+// jb have published Hq/Hs (a per-block counter, release/acquire, plus proxy
+// fences because TMA reads what generic stores wrote).  SMs that run out of
+// first-GEMM tiles start on the second GEMM instead of idling at a kernel
+// boundary.  Progress needs every CTA resident: the grid is one CTA per SM.
+__device__ __forceinline__ int tile_kind(int t, int total1, int n_mt1, int n_mt2, int &jb, int &mt)
+{
+    if (t < total1) {
+        jb = t / n_mt1;
+        mt = t - jb * n_mt1;
+        return 1;
+    }
+    t -= total1;
+    jb = t / n_mt2;
+    mt = t - jb * n_mt2;
+    return 2;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a)
+gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+            const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, const Args a1,
+            const Args a2, int32_t *done)
 {
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 1024-byte aligned base for the 128-byte swizzled tiles
     const uint32_t raw = tc::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const int NB = a.n_mma * 128;                                  // B tile bytes
-    const int stage_bytes = (16384 + NB + 512 + a.nsf * 512 + 1023) & ~1023;
-    const int kStages = a.stages;
+    const int n_mma = a1.n_mma, nsf = a1.nsf;                      // the same for both GEMMs
+    const int NB = n_mma * 128;                                    // B tile bytes
+    const int stage_bytes = (16384 + NB + 512 + nsf * 512 + 1023) & ~1023;
+    const int kStages = a1.stages;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * stage_bytes);
     const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kStages;
     const uint32_t accf0 = full0 + 16 * kStages, acce0 = accf0 + 16, fin = acce0 + 16;   // accf[2], acce[2]
@@ -203,7 +232,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     float *t_w = reinterpret_cast<float *>(t_route + 256);         // [256] their weights
     // two accumulator buffers (columns 0 and 128) when a tile fits in 128
     // columns, so the MMA of the next tile overlaps this tile's epilogue
-    const int nbuf = a.n_mma <= 128 ? 2 : 1;
+    const int nbuf = n_mma <= 128 ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -223,8 +252,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tc::tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        tc::prefetch_tmap(&tmA);
-        tc::prefetch_tmap(&tmB);
+        tc::prefetch_tmap(&tmA1);
+        tc::prefetch_tmap(&tmB1);
+        tc::prefetch_tmap(&tmA2);
+        tc::prefetch_tmap(&tmB2);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -234,19 +265,46 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
 
-    const int n_blocks = *a.npp / a.b;
-    const int total = n_blocks * a.n_mt;
-    const int KT = a.KT;
+    const int n_blocks = *a1.npp / a1.b;
+    const int n_mt1 = a1.n_mt, n_mt2 = a2.n_mt;
+    const int total1 = n_blocks * n_mt1, total = total1 + n_blocks * n_mt2;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             int s = 0, issued = 0;
             uint32_t ph = 0;
-            const uint32_t tx = 16384u + NB + 512u + a.nsf * 512u;
+            const uint32_t tx = 16384u + NB + 512u + nsf * 512u;
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-                const int jb = t / a.n_mt, mt = t % a.n_mt;
-                const int e = a.expert_ids[jb];
+                int jb, mt;
+                const int kind = tile_kind(t, total1, n_mt1, n_mt2, jb, mt);
+                const int e = a1.expert_ids[jb];
+                const int KT = kind == 1 ? a1.KT : a2.KT;
+                const int n_mt = kind == 1 ? n_mt1 : n_mt2;
+                const int a_rows = kind == 1 ? a1.a_rows : a2.a_rows;
+                const CUtensorMap *tA = kind == 1 ? &tmA1 : &tmA2;
+                const CUtensorMap *tB = kind == 1 ? &tmB1 : &tmB2;
+                const uint8_t *sfa = kind == 1 ? a1.sfa : a2.sfa;
+                const uint8_t *sfb = kind == 1 ? a1.sfb : a2.sfb;
+                if (kind == 2) {
+                    // block jb's Hq/Hs: every first-GEMM tile of jb published
+                    const long long t0 = clock64();
+                    const long long limit = static_cast<long long>(kWaitNs) * 5 / 2;
+                    int v;
+                    for (;;) {
+                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(done + jb) : "memory");
+                        if (v >= n_mt1)
+                            break;
+                        if (*abort_flag || clock64() - t0 > limit) {
+                            *abort_flag = 1;
+                            break;
+                        }
+                    }
+                    if (v < n_mt1)
+                        break;
+                    // the tensor-memory-access proxy reads what generic stores wrote
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 for (int kt = 0; kt < KT; ++kt, ++issued) {
                     if (!tc::mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, kWaitNs))
                         break;
@@ -254,17 +312,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t fb = full0 + 8 * s;
                     tc::mbar_arrive_expect_tx(fb, tx);
                     const int x = kt * 128;
-                    if (KIND == 1) {
-                        tc::tma_load_2d(tc::smem_u32(st), &tmA, x, e * a.a_rows + 64 * mt, fb);
-                        tc::tma_load_2d(tc::smem_u32(st + 8192), &tmA, x, e * a.a_rows + a.I + 64 * mt, fb);
+                    if (kind == 1) {
+                        tc::tma_load_2d(tc::smem_u32(st), tA, x, e * a_rows + 64 * mt, fb);
+                        tc::tma_load_2d(tc::smem_u32(st + 8192), tA, x, e * a_rows + a1.I + 64 * mt, fb);
                     } else {
-                        tc::tma_load_2d(tc::smem_u32(st), &tmA, x, e * a.a_rows + 128 * mt, fb);
+                        tc::tma_load_2d(tc::smem_u32(st), tA, x, e * a_rows + 128 * mt, fb);
                     }
-                    tc::tma_load_2d(tc::smem_u32(st + 16384), &tmB, x, jb * a.b, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + 16384), tB, x, jb * a1.b, fb);
                     tc::bulk_load(tc::smem_u32(st + 16384 + NB),
-                                  a.sfa + ((static_cast<int64_t>(e) * a.n_mt + mt) * KT + kt) * 512, 512, fb);
+                                  sfa + ((static_cast<int64_t>(e) * n_mt + mt) * KT + kt) * 512, 512, fb);
                     tc::bulk_load(tc::smem_u32(st + 16384 + NB + 512),
-                                  a.sfb + (static_cast<int64_t>(jb) * KT + kt) * a.nsf * 512, a.nsf * 512, fb);
+                                  sfb + (static_cast<int64_t>(jb) * KT + kt) * nsf * 512, nsf * 512, fb);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
@@ -289,8 +347,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (lane == 0) {
             int s = 0, ti = 0;
             uint32_t ph = 0;
-            bool any = false;
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
+                const int KT = t < total1 ? a1.KT : a2.KT;
                 const int buf = nbuf == 2 ? (ti & 1) : 0;
                 const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
                 if (!tc::mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag, kWaitNs))
@@ -306,13 +364,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t ssfa = sb + NB, ssfb = ssfa + 512;
                     const uint32_t tsfa = tmem + 256 + s * 16, tsfb = tsfa + 4;
                     tc::tc_cp_32x128b_x4(tsfa, tc::smem_desc(ssfa, 0, 128, tc::kLayoutNone));
-                    for (int q = 0; q < a.nsf; ++q)
+                    for (int q = 0; q < nsf; ++q)
                         tc::tc_cp_32x128b_x4(tsfb + 4 * q, tc::smem_desc(ssfb + 512 * q, 0, 128, tc::kLayoutNone));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = tc::smem_desc(sa + 32 * kk, 16, 1024, tc::kLayoutSw128);
                         const uint64_t bd = tc::smem_desc(sb + 32 * kk, 16, 1024, tc::kLayoutSw128);
-                        tc::mma_mxf8(acc, ad, bd, tc::idesc_mxf8(128, a.n_mma, kk, kk), tsfa, tsfb,
+                        tc::mma_mxf8(acc, ad, bd, tc::idesc_mxf8(128, n_mma, kk, kk), tsfa, tsfb,
                                      (kt | kk) != 0 ? 1u : 0u);
                     }
                     tc::tc_commit(empty0 + 8 * s);
@@ -322,42 +380,42 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     }
                 }
                 tc::tc_commit(accf0 + 8 * buf);
-                any = true;
             }
             // all MMAs of this CTA complete before TMEM is released
             tc::tc_commit(fin);
             volatile int never = 0;
             tc::mbar_wait(fin, 0, &never, kWaitNs);
-            (void)any;
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;                       // TMEM lane quadrant
         const int etid = threadIdx.x - 64;
         int ti = 0;
+        const int b = a1.b;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
-            const int jb = t / a.n_mt, mt = t % a.n_mt;
+            int jb, mt;
+            const int kind = tile_kind(t, total1, n_mt1, n_mt2, jb, mt);
             const int buf = nbuf == 2 ? (ti & 1) : 0;
             const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
-            const int rho0 = jb * a.b;
-            if (KIND == 2) {
+            const int rho0 = jb * b;
+            if (kind == 2) {
                 // routes and routing weights of the tile's rows, loaded once
-                for (int c = etid; c < a.b; c += 128) {
-                    const int r = a.sorted[rho0 + c];
+                for (int c = etid; c < b; c += 128) {
+                    const int r = a2.sorted[rho0 + c];
                     t_route[c] = r;
-                    t_w[c] = r < a.MK ? a.wts[r] : 0.f;
+                    t_w[c] = r < a2.MK ? a2.wts[r] : 0.f;
                 }
             }
-            if (!tc::mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag, kWaitNs) && a.dev_status)
-                atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+            if (!tc::mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag, kWaitNs) && a1.dev_status)
+                atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
             tc::tc_fence_after();
             tc::named_bar(1, 128);
-            for (int c0 = 0, chunk = 0; c0 < a.b; c0 += 32, ++chunk) {
+            for (int c0 = 0, chunk = 0; c0 < b; c0 += 32, ++chunk) {
                 uint32_t v[32];
                 tc::tmem_ld_32x32b_x32(tmem + 128 * buf + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
                 tc::tmem_ld_wait();
-                const int ncol = min(32, a.b - c0);
-                if (KIND == 1) {
+                const int ncol = min(32, b - c0);
+                if (kind == 1) {
                     // Lanes 0..63 of the tile are gate rows, 64..127 up rows:
                     // quadrant q pairs with q ^ 2 (same 32 neurons).  The
                     // gate quadrant finishes columns 0..15 of the chunk, the
@@ -387,13 +445,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         am[c] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[c])));
                     const int n = 64 * mt + 32 * (q & 1) + lane;     // neuron of this lane
                     const int kblk = 2 * mt + (q & 1);                // its 32-neuron block
-                    uint8_t *hrow = a.hq + static_cast<int64_t>(rho0 + c0 + keep) * a.I + n;
-                    uint8_t *hsa = a.hs + ((static_cast<int64_t>(jb) * (a.I / 128) + kblk / 4) * a.nsf) * 512;
+                    uint8_t *hrow = a1.hq + static_cast<int64_t>(rho0 + c0 + keep) * a1.I + n;
+                    uint8_t *hsa = a1.hs + ((static_cast<int64_t>(jb) * (a1.I / 128) + kblk / 4) * nsf) * 512;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
                         const int X = mx_exp(am[c]);
                         if (keep + c < ncol) {
-                            hrow[static_cast<int64_t>(c) * a.I] = static_cast<uint8_t>(to_e4m3(hv[c] * mx_inv(X)));
+                            hrow[static_cast<int64_t>(c) * a1.I] = static_cast<uint8_t>(to_e4m3(hv[c] * mx_inv(X)));
                             if (lane == 0) {
                                 const int m = c0 + keep + c;
                                 hsa[(m / 128) * 512 + atom_off(m & 127, kblk & 3)] = static_cast<uint8_t>(X + 127);
@@ -419,18 +477,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         ww[4 * i + 2] = w4.z;
                         ww[4 * i + 3] = w4.w;
                     }
-                    float *yo = a.yr + o;
+                    float *yo = a2.yr + o;
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        if (c < ncol && rr[c] < a.MK)
-                            yo[static_cast<int64_t>(rr[c]) * a.d] = ww[c] * __uint_as_float(v[c]);
+                        if (c < ncol && rr[c] < a2.MK)
+                            yo[static_cast<int64_t>(rr[c]) * a2.d] = ww[c] * __uint_as_float(v[c]);
                     }
                 }
             }
+            if (kind == 1)
+                asm volatile("fence.proxy.async.global;" ::: "memory");   // Hq/Hs are read by TMA
             tc::tc_fence_before();
             tc::named_bar(1, 128);                    // t_route / t_w reuse by the next tile
             if (lane == 0)
                 tc::mbar_arrive(acce0 + 8 * buf);
+            if (kind == 1 && etid == 0)                // every epilogue thread's stores are ordered before this
+                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(done + jb) : "memory");
         }
         (void)etid;
     }
@@ -537,7 +599,7 @@ static int sm_count()
 }
 
 struct WsLayout {
-    size_t xq, xs, hq, hs, yr, total;
+    size_t xq, xs, hq, hs, yr, done, total;
 };
 
 static WsLayout ws_layout(int M, int k, int d, int I, int b, int cap_rows)
@@ -557,6 +619,8 @@ static WsLayout ws_layout(int M, int k, int d, int I, int b, int cap_rows)
     off += ws_round(static_cast<size_t>(cap_blocks) * (I / 128) * nsf * 512);
     L.yr = off;
     off += ws_round(static_cast<size_t>(M) * k * d * sizeof(float));
+    L.done = off;
+    off += ws_round(static_cast<size_t>(cap_blocks) * sizeof(int32_t));
     L.total = off;
     return L;
 }
@@ -700,6 +764,7 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
     uint8_t *w = static_cast<uint8_t *>(ws);
     uint8_t *xq = w + L.xq, *xs = w + L.xs, *hq = w + L.hq, *hs = w + L.hs;
     float *yr = reinterpret_cast<float *>(w + L.yr);
+    int32_t *done = reinterpret_cast<int32_t *>(w + L.done);
     const int n_mma = (b + 15) / 16 * 16;
     const int nsf = (n_mma + 127) / 128;
     cudaStream_t s = as_stream(stream);
@@ -713,7 +778,7 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         return MOE_ERR_CUDA;
 
     if (launch_pdl(act_quant_kernel, dim3(sm_count() * 4), dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(x), d,
-                   k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs) != cudaSuccess)
+                   k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs, done) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     const int stage_bytes = (16384 + n_mma * 128 + 512 + nsf * 512 + 1023) & ~1023;
@@ -725,10 +790,8 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
     static std::once_flag attr_once;
     static bool attr_ok = false;
     std::call_once(attr_once, [] {
-        attr_ok = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                      cudaSuccess &&
-                  cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                      cudaSuccess;
+        attr_ok = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+                  cudaSuccess;
     });
     if (!attr_ok || stages < 2 || smem > 227 * 1024)
         return MOE_ERR_CUDA;
@@ -736,11 +799,10 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
 
     Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
             hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I, stages};
-    if (launch_pdl(gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, tA1, tB1, a1) != cudaSuccess)
-        return MOE_ERR_CUDA;
     Args a2{static_cast<const uint8_t *>(sfa2), hs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
             nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d, stages};
-    if (launch_pdl(gemm_kernel<2>, dim3(grid), dim3(kThreads), smem, s, tA2, tB2, a2) != cudaSuccess)
+    if (launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tA1, tB1, tA2, tB2, a1, a2, done) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     return grouped_combine_launch(yr, topk_ids, M, k, d, E, y, ydt == MOE_FP32, s);
 }
