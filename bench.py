@@ -179,8 +179,8 @@ def committed_traffic(kernel_key: str, src_hash: str):
 SRC_FILES = {
     "decode": ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "decode_internal.h", "topk.cu",
                "topk.cuh", "common.cuh", "tc.cuh"),
-    "grouped": ("grouped.cu", "grouped_awq.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh",
-                "tc.cuh"),
+    "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh"),
+    "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh"),
 }
 
 
@@ -346,7 +346,7 @@ class DecodeStep:
         if self.awq:
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel<1> + ga::gemm_kernel<2> + combine"
         if self.path == "grouped":
-            return "moe_ffn_grouped: act_quant + gemm_kernel<1> + gemm_kernel<2> + combine"
+            return "moe_ffn_grouped: act_quant + gemm_kernel (both GEMMs, one persistent kernel) + combine"
         if self.routed_in_layer:
             return "moe_ffn_decode_logits: dm::m1_kernel (top-k routing + gate/up + SwiGLU + down + combine), one kernel"
         if self.fused:
@@ -392,7 +392,7 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     t_hbm = total_bytes / (peak_gbs * 1e9)
     t_mma = flops / (peak_tf * 1e12)
     kern = st.layer_kernels()
-    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash(st.path))
+    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash("awq" if st.awq else st.path))
     if t_mma > t_hbm:
         ach = flops / sec / 1e12 / world
         return {"kernel": kern, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_tf,
