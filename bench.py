@@ -344,7 +344,7 @@ class DecodeStep:
 
     def layer_kernels(self) -> str:
         if self.awq:
-            return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel<1> + ga::gemm_kernel<2> + combine"
+            return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
         if self.path == "grouped":
             return "moe_ffn_grouped: act_quant + gemm_kernel (both GEMMs, one persistent kernel) + combine"
         if self.routed_in_layer:

@@ -244,10 +244,12 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
  * (tcgen05 kind::f16, FP32 accumulate): each weight tile is dequantized on
  * chip to fp16 (q - z) * s (one rounding), x is rounded to fp16 and
  * h = SiLU(g) * u is rounded to fp16 before the second GEMM.  ws is laid out
- * as [Xg | Hg | Yr], each part rounded up to 256 bytes:
+ * as [Xg | Hg | Yr | D], each part rounded up to 256 bytes:
  *     Xg fp16 [cap_rows][d]     x per aligned row (padding rows zero)
  *     Hg fp16 [cap_rows][I]     h per aligned row
  *     Yr f32 [M*k][d]           w_route * (W2 h) per route
+ *     D  int32 [cap_rows/b]     per-block counters of the fused GEMM kernel
+ *                               (set by the call itself)
  *   Inside every run of 8 columns Xg and Hg hold the values in the order
  *   0, 4, 1, 5, 2, 6, 3, 7 (the order the on-chip dequantization produces).
  *   Extra limits: b <= 128, d % 256 == 0, d / 128 <= 64, I / 128 <= 64,

@@ -72,7 +72,7 @@ def _r256(n):
                                        (8, 8, 7168, 2048, 16), (3, 4, 1024, 256, 136)])
 def test_grouped_workspace_size_matches_documented_layout(M, k, d, I, b):
     """moe_ffn_grouped_workspace_size is the larger of the two documented
-    layouts: MXFP8 [Xq | Xs | Hq | Hs | Yr | D] and AWQ [Xg | Hg | Yr], each
+    layouts: MXFP8 [Xq | Xs | Hq | Hs | Yr | D] and AWQ [Xg | Hg | Yr | D], each
     part rounded up to 256 bytes."""
     cap_rows = moe.moe_align_capacity(M, k, 128, b)[0]
     cap_blocks = cap_rows // b
@@ -80,7 +80,7 @@ def test_grouped_workspace_size_matches_documented_layout(M, k, d, I, b):
     nsf = (n_mma + 127) // 128
     mx = (_r256(cap_rows * d) + _r256(cap_blocks * (d // 128) * nsf * 512) + _r256(cap_rows * I)
           + _r256(cap_blocks * (I // 128) * nsf * 512) + _r256(M * k * d * 4) + _r256(cap_blocks * 4))
-    awq = _r256(cap_rows * d * 2) + _r256(cap_rows * I * 2) + _r256(M * k * d * 4)
+    awq = _r256(cap_rows * d * 2) + _r256(cap_rows * I * 2) + _r256(M * k * d * 4) + _r256(cap_blocks * 4)
     assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(mx, awq)
 
 

@@ -699,7 +699,7 @@ MOE_API moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_
     if (M < 0 || k < 1 || d < 1 || I < 1 || b < 1 || cap_rows < 0 || !bytes)
         return MOE_ERR_INVALID_ARG;
     // one size for both weight formats: the MXFP8 layout or the AWQ one
-    const size_t mx = ws_layout(M, k, d, I, b, cap_rows).total, aw = grouped_awq_workspace(M, k, d, I, cap_rows);
+    const size_t mx = ws_layout(M, k, d, I, b, cap_rows).total, aw = grouped_awq_workspace(M, k, d, I, b, cap_rows);
     *bytes = mx > aw ? mx : aw;
     return MOE_OK;
 }

@@ -149,17 +149,40 @@ __device__ __forceinline__ void dq_words(const uint4 &a, const uint4 &b, uint32_
 // [32][G] int32 (row r's zero in nibble r % 8 of word [r / 8][g]).
 __host__ __device__ inline int sbuf_bytes(int G) { return 640 * G; }
 
-template <int KIND>
+// Both GEMMs in one persistent kernel: the tile list is every first-GEMM
+// tile (gate/up, SwiGLU into Hg), block-major, then every second-GEMM tile
+// (down, w_route * acc into Yr).  CTA c takes tiles c, c + grid, ..., so it
+// finishes its first-GEMM tiles first; a second-GEMM tile of block jb waits
+// (bounded) until every first-GEMM tile of jb has published Hg through a
+// per-block counter (release add after proxy fences; acquire load and proxy
+// fence before the TMA reads).  SMs that run out of first-GEMM tiles start on
+// the second GEMM instead of idling at a kernel boundary.  Every CTA must be
+// resident: the grid is one CTA per SM.
+__device__ __forceinline__ int tile_kind(int t, int total1, int n_t1, int n_t2, int &jb, int &T)
+{
+    if (t < total1) {
+        jb = t / n_t1;
+        T = t - jb * n_t1;
+        return 1;
+    }
+    t -= total1;
+    jb = t / n_t2;
+    T = t - jb * n_t2;
+    return 2;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmB, const Args a)
+gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CUtensorMap tmB1,
+            const __grid_constant__ CUtensorMap tmQ2, const __grid_constant__ CUtensorMap tmB2, const Args a1,
+            const Args a2, int32_t *done, int sbuf_g)
 {
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw = tc::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const Geo geo{a.n_mma};
+    const Geo geo{a1.n_mma};
     // kDqGroups <= AS, ceil(AS / 2) < S
-    const int S = a.stages, SB = geo.bytes(), AS = a.aslots, NB = a.nbuf;
+    const int S = a1.stages, SB = geo.bytes(), AS = a1.aslots, NB = a1.nbuf;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * SB);
     const uint32_t rfull0 = tc::smem_u32(bars), rempty0 = rfull0 + 8 * S, afull0 = rempty0 + 8 * S;
     const uint32_t accf0 = afull0 + 8 * AS;      // [half][buf]
@@ -170,7 +193,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     int *t_route = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + kHeaderBytes);   // [256]
     float *t_w = reinterpret_cast<float *>(t_route + 256);                                       // [256]
     uint8_t *sbuf = reinterpret_cast<uint8_t *>(t_w + 256);                                      // [2][sbuf_bytes]
-    const int SBUF = sbuf_bytes(a.G);
+    const int SBUF = sbuf_bytes(sbuf_g);                                                        // both GEMMs' G fit
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -196,8 +219,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tc::tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        tc::prefetch_tmap(&tmQ);
-        tc::prefetch_tmap(&tmB);
+        tc::prefetch_tmap(&tmQ1);
+        tc::prefetch_tmap(&tmB1);
+        tc::prefetch_tmap(&tmQ2);
+        tc::prefetch_tmap(&tmB2);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -206,11 +231,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
 
-    const int n_blocks = *a.npp / a.b;
-    const int total = n_blocks * a.n_t;
-    const int KT = a.KT;
-    const int G = a.G;
-    const uint32_t a_base = static_cast<uint32_t>(2 * NB * a.acc_cols);   // first A-unit column
+    const int b = a1.b;
+    const int n_blocks = *a1.npp / b;
+    const int n_t1 = a1.n_t, n_t2 = a2.n_t;
+    const int total1 = n_blocks * n_t1, total = total1 + n_blocks * n_t2;
+    const uint32_t a_base = static_cast<uint32_t>(2 * NB * a1.acc_cols);   // first A-unit column
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -219,12 +244,37 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             uint32_t ph = 0;
             const uint32_t tx = static_cast<uint32_t>(SB);
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
-                const int jb = t / a.n_t, T = t % a.n_t;
-                const int e = a.expert_ids[jb];
-                const int row0 = e * a.N;
+                int jb, T;
+                const int kind = tile_kind(t, total1, n_t1, n_t2, jb, T);
+                const int e = a1.expert_ids[jb];
+                const int N = kind == 1 ? a1.N : a2.N, G = kind == 1 ? a1.G : a2.G, KT = kind == 1 ? a1.KT : a2.KT;
+                const uint16_t *sp = kind == 1 ? a1.s : a2.s;
+                const int32_t *zp = kind == 1 ? a1.z : a2.z;
+                const CUtensorMap *tQ = kind == 1 ? &tmQ1 : &tmQ2;
+                const CUtensorMap *tB = kind == 1 ? &tmB1 : &tmB2;
+                const int row0 = e * N;
                 // first weight row of each half
-                const int r0 = KIND == 1 ? row0 + 128 * T : row0 + 256 * T;
-                const int r1 = KIND == 1 ? row0 + a.I + 128 * T : row0 + 256 * T + 128;
+                const int r0 = kind == 1 ? row0 + 128 * T : row0 + 256 * T;
+                const int r1 = kind == 1 ? row0 + a1.I + 128 * T : row0 + 256 * T + 128;
+                if (kind == 2) {
+                    // block jb's Hg: every first-GEMM tile of jb published
+                    const long long t0 = clock64();
+                    const long long limit = static_cast<long long>(kWaitNs) * 5 / 2;
+                    int v;
+                    for (;;) {
+                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(done + jb) : "memory");
+                        if (v >= n_t1)
+                            break;
+                        if (*abort_flag || clock64() - t0 > limit) {
+                            *abort_flag = 1;
+                            break;
+                        }
+                    }
+                    if (v < n_t1)
+                        break;
+                    // the tensor-memory-access proxy reads what generic stores wrote
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 // the tile's scales and zeros (buffer ti % 2, freed by the
                 // dequantizing warps when they finish tile ti - 2)
                 const int sb = ti & 1;
@@ -233,13 +283,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 {
                     const uint32_t fb = sfull0 + 8 * sb;
                     const uint32_t dst = tc::smem_u32(sbuf + sb * SBUF);
-                    const int64_t zr0 = static_cast<int64_t>(e) * (a.N / 8) + (r0 - row0) / 8;
-                    const int64_t zr1 = static_cast<int64_t>(e) * (a.N / 8) + (r1 - row0) / 8;
-                    tc::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(SBUF));
-                    tc::bulk_load(dst, a.s + static_cast<int64_t>(r0) * G, 256u * G, fb);
-                    tc::bulk_load(dst + 256u * G, a.s + static_cast<int64_t>(r1) * G, 256u * G, fb);
-                    tc::bulk_load(dst + 512u * G, a.z + zr0 * G, 64u * G, fb);
-                    tc::bulk_load(dst + 576u * G, a.z + zr1 * G, 64u * G, fb);
+                    const int64_t zr0 = static_cast<int64_t>(e) * (N / 8) + (r0 - row0) / 8;
+                    const int64_t zr1 = static_cast<int64_t>(e) * (N / 8) + (r1 - row0) / 8;
+                    tc::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(sbuf_bytes(G)));
+                    tc::bulk_load(dst, sp + static_cast<int64_t>(r0) * G, 256u * G, fb);
+                    tc::bulk_load(dst + 256u * G, sp + static_cast<int64_t>(r1) * G, 256u * G, fb);
+                    tc::bulk_load(dst + 512u * G, zp + zr0 * G, 64u * G, fb);
+                    tc::bulk_load(dst + 576u * G, zp + zr1 * G, 64u * G, fb);
                 }
                 for (int kt = 0; kt < KT; ++kt, ++issued) {
                     if (!tc::mbar_wait(rempty0 + 8 * s, ph ^ 1u, abort_flag, kWaitNs))
@@ -248,11 +298,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     const uint32_t fb = rfull0 + 8 * s;
                     tc::mbar_arrive_expect_tx(fb, tx);
                     // packed A rows: 64 bytes (128 values) of each, x in bytes
-                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), &tmQ, kt * 64, r0, fb);
-                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off() + 8192), &tmQ, kt * 64, r1, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), tQ, kt * 64, r0, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off() + 8192), tQ, kt * 64, r1, fb);
                     // B: two tiles of n_mma rows x 64 fp16, x in elements
-                    tc::tma_load_2d(tc::smem_u32(st + geo.b_off()), &tmB, kt * 128, jb * a.b, fb);
-                    tc::tma_load_2d(tc::smem_u32(st + geo.b_off() + a.n_mma * 128), &tmB, kt * 128 + 64, jb * a.b, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + geo.b_off()), tB, kt * 128, jb * b, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + geo.b_off() + geo.n_mma * 128), tB, kt * 128 + 64, jb * b, fb);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -287,18 +337,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             const int h = warp - 1;
             int s = 0, ti = 0, sa = h;                // unit 2 i + h of k-step i sits in slot (2 i + h) % AS
             uint32_t pha = 0;
-            const uint32_t idesc = tc::idesc_f16(128, a.n_mma, false);
+            const uint32_t idesc = tc::idesc_f16(128, geo.n_mma, false);
             const uint64_t bd0 = tc::smem_desc(tc::smem_u32(smem + geo.b_off()), 16, 1024, tc::kLayoutSw128);
             const uint64_t bd_step = static_cast<uint64_t>(SB >> 4);
-            const uint64_t bd_half = static_cast<uint64_t>(a.n_mma * 8);   // second B tile: n_mma * 128 bytes on
+            const uint64_t bd_half = static_cast<uint64_t>(geo.n_mma * 8);   // second B tile: n_mma * 128 bytes on
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
+                const int KT = t < total1 ? a1.KT : a2.KT;
                 const int buf = NB == 2 ? (ti & 1) : 0;
                 const uint32_t use = static_cast<uint32_t>(NB == 2 ? (ti >> 1) : ti);
                 const int ab = h * 2 + buf;
                 if (!tc::mbar_wait(acce0 + 8 * ab, (use & 1u) ^ 1u, abort_flag, kWaitNs))
                     break;
                 tc::tc_fence_after();
-                const uint32_t acc = tmem + static_cast<uint32_t>((h * NB + buf) * a.acc_cols);
+                const uint32_t acc = tmem + static_cast<uint32_t>((h * NB + buf) * a1.acc_cols);
                 uint64_t bd = bd0 + bd_step * static_cast<uint64_t>(s);
                 for (int kt = 0; kt < KT; ++kt) {
                     if (!tc::mbar_wait(afull0 + 8 * sa, pha, abort_flag, kWaitNs))
@@ -339,39 +390,40 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
         int ti = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
-            const int jb = t / a.n_t, T = t % a.n_t;
+            int jb, T;
+            const int kind = tile_kind(t, total1, n_t1, n_t2, jb, T);
             const int buf = NB == 2 ? (ti & 1) : 0;
             const uint32_t use = static_cast<uint32_t>(NB == 2 ? (ti >> 1) : ti);
-            const int rho0 = jb * a.b;
-            if (KIND == 2) {
-                for (int c = etid; c < a.b; c += 128) {
-                    const int r = a.sorted[rho0 + c];
+            const int rho0 = jb * b;
+            if (kind == 2) {
+                for (int c = etid; c < b; c += 128) {
+                    const int r = a2.sorted[rho0 + c];
                     t_route[c] = r;
-                    t_w[c] = r < a.MK ? a.wts[r] : 0.f;
+                    t_w[c] = r < a2.MK ? a2.wts[r] : 0.f;
                 }
             }
             bool ok = tc::mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag, kWaitNs);
             ok = tc::mbar_wait(accf0 + 8 * (2 + buf), use & 1u, abort_flag, kWaitNs) && ok;
-            if (!ok && a.dev_status)
-                atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+            if (!ok && a1.dev_status)
+                atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
             tc::tc_fence_after();
             tc::named_bar(1, 128);
-            const uint32_t acc0 = tmem + lane_off + static_cast<uint32_t>(buf * a.acc_cols);
-            const uint32_t acc1 = tmem + lane_off + static_cast<uint32_t>((NB + buf) * a.acc_cols);
-            for (int c0 = 0; c0 < a.b; c0 += 32) {
-                const int ncol = min(32, a.b - c0);
-                if (KIND == 1) {
+            const uint32_t acc0 = tmem + lane_off + static_cast<uint32_t>(buf * a1.acc_cols);
+            const uint32_t acc1 = tmem + lane_off + static_cast<uint32_t>((NB + buf) * a1.acc_cols);
+            for (int c0 = 0; c0 < b; c0 += 32) {
+                const int ncol = min(32, b - c0);
+                if (kind == 1) {
                     // gate and up of neuron n share the lane; h -> column n of Hg in the operand order
                     uint32_t g[32], u[32];
                     tc::tmem_ld_32x32b_x32(acc0 + c0, g);
                     tc::tmem_ld_32x32b_x32(acc1 + c0, u);
                     tc::tmem_ld_wait();
                     const int n = 128 * T + 32 * q + lane;
-                    __half *hrow = a.hg + static_cast<int64_t>(rho0 + c0) * a.I + (n & ~7) + interleave_pos(n & 7);
+                    __half *hrow = a1.hg + static_cast<int64_t>(rho0 + c0) * a1.I + (n & ~7) + interleave_pos(n & 7);
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         if (c < ncol)
-                            hrow[static_cast<int64_t>(c) * a.I] =
+                            hrow[static_cast<int64_t>(c) * a1.I] =
                                 __float2half_rn(silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c])));
                 } else {
 #pragma unroll
@@ -379,22 +431,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                         uint32_t v[32];
                         tc::tmem_ld_32x32b_x32((h ? acc1 : acc0) + c0, v);
                         tc::tmem_ld_wait();
-                        float *yo = a.yr + 256 * T + 128 * h + 32 * q + lane;
+                        float *yo = a2.yr + 256 * T + 128 * h + 32 * q + lane;
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             const int r = t_route[c0 + c];   // same address in every lane: broadcast
-                            if (c < ncol && r < a.MK)
-                                yo[static_cast<int64_t>(r) * a.d] = t_w[c0 + c] * __uint_as_float(v[c]);
+                            if (c < ncol && r < a2.MK)
+                                yo[static_cast<int64_t>(r) * a2.d] = t_w[c0 + c] * __uint_as_float(v[c]);
                         }
                     }
                 }
             }
+            if (kind == 1)
+                asm volatile("fence.proxy.async.global;" ::: "memory");   // Hg is read by TMA
             tc::tc_fence_before();
             tc::named_bar(1, 128);
             if (lane == 0) {
                 tc::mbar_arrive(acce0 + 8 * buf);
                 tc::mbar_arrive(acce0 + 8 * (2 + buf));
             }
+            if (kind == 1 && etid == 0)                // every epilogue thread's stores are ordered before this
+                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(done + jb) : "memory");
         }
     } else {
         // ------------------------------------------------ dequantization (warps 7..18)
@@ -409,23 +465,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         int v = g, sa = g, ti = 0;
         int s = v >> 1;                               // stage of k-step v / 2 (< S) and its phase
         uint32_t ph = 0;
+        int kbase = 0;                                // the CTA's k-steps before this tile
         // after a timeout the waits return at once and the loops run out
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
             const int sb = ti & 1;
-            if (!tc::mbar_wait(sfull0 + 8 * sb, (ti >> 1) & 1u, abort_flag, kWaitNs) && a.dev_status)
-                atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+            const int G = t < total1 ? a1.G : a2.G, KT = t < total1 ? a1.KT : a2.KT;
+            if (!tc::mbar_wait(sfull0 + 8 * sb, (ti >> 1) & 1u, abort_flag, kWaitNs) && a1.dev_status)
+                atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
             const uint16_t *sc = reinterpret_cast<const uint16_t *>(sbuf + sb * SBUF);
             const uint32_t *zs = reinterpret_cast<const uint32_t *>(sbuf + sb * SBUF + 512 * G);
-            for (; (v >> 1) < (ti + 1) * KT;) {
+            for (; (v >> 1) < kbase + KT;) {
                 const int i = v >> 1, h = v & 1;
-                const int kt = i - ti * KT;            // = the quantization group
+                const int kt = i - kbase;              // = the quantization group
                 const int r = 128 * h + m;             // row of the tile
                 const uint32_t sv = sc[r * G + kt];
                 const uint32_t zv = (zs[(r >> 3) * G + kt] >> zsh) & 0xFu;
                 const uint32_t sc2 = sv | (sv << 16), zb2 = 0x64006400u | zv | (zv << 16);
                 const uint32_t zb16 = 0xD400D400u | (zv << 4) | (zv << 20);   // -(64 + z): ulp 1/16 in [64, 128)
-                if (!tc::mbar_wait(rfull0 + 8 * s, ph, abort_flag, kWaitNs) && a.dev_status)
-                    atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+                if (!tc::mbar_wait(rfull0 + 8 * s, ph, abort_flag, kWaitNs) && a1.dev_status)
+                    atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
                 const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * SB + geo.raw_off() + r * 64);
                 const uint4 w0 = src[0], w1 = src[1], w2 = src[2], w3 = src[3];
                 __syncwarp();
@@ -437,8 +495,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     const int ip = (v - AS) >> 1;
                     if (!tc::mbar_wait(rempty0 + 8 * (ip % S), static_cast<uint32_t>(ip / S) & 1u, abort_flag,
                                        kWaitNs) &&
-                        a.dev_status)
-                        atomicCAS(a.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
+                        a1.dev_status)
+                        atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
                 }
                 tc::tc_fence_after();
                 {
@@ -469,6 +527,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             __syncwarp();
             if (lane == 0)
                 tc::mbar_arrive(sempty0 + 8 * sb);
+            kbase += KT;
         }
     }
     tc::tc_fence_before();
@@ -483,11 +542,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 // the operand order 0, 4, 1, 5, 2, 6, 3, 7; 8 values per thread
 template <typename XT>
 __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, const int32_t *__restrict__ sorted,
-                              const int32_t *__restrict__ npp, __half *__restrict__ xg)
+                              const int32_t *__restrict__ npp, __half *__restrict__ xg, int b, int32_t *__restrict__ done)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int rows = *npp;
+    // the GEMM's per-block counters of finished first-GEMM tiles start at 0
+    for (int jb = blockIdx.x * blockDim.x + threadIdx.x; jb < rows / b; jb += gridDim.x * blockDim.x)
+        done[jb] = 0;
     const int d8 = d / 8;
     const int64_t total = static_cast<int64_t>(rows) * d8;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -513,10 +575,10 @@ __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, co
 }
 
 struct WsLayout {
-    size_t xg, hg, yr, total;
+    size_t xg, hg, yr, done, total;
 };
 
-static WsLayout ws_layout(int M, int k, int d, int I, int cap_rows)
+static WsLayout ws_layout(int M, int k, int d, int I, int b, int cap_rows)
 {
     WsLayout L;
     size_t off = 0;
@@ -526,15 +588,17 @@ static WsLayout ws_layout(int M, int k, int d, int I, int cap_rows)
     off += ws_round(static_cast<size_t>(cap_rows) * I * 2);
     L.yr = off;
     off += ws_round(static_cast<size_t>(M) * k * d * sizeof(float));
+    L.done = off;
+    off += ws_round(static_cast<size_t>(cap_rows / b) * sizeof(int32_t));
     L.total = off;
     return L;
 }
 
 }  // namespace ga
 
-size_t grouped_awq_workspace(int M, int k, int d, int I, int cap_rows)
+size_t grouped_awq_workspace(int M, int k, int d, int I, int b, int cap_rows)
 {
-    return ga::ws_layout(M, k, d, I, cap_rows).total;
+    return ga::ws_layout(M, k, d, I, b, cap_rows).total;
 }
 
 moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
@@ -545,11 +609,12 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     using namespace ga;
     const int64_t mk = static_cast<int64_t>(M) * k;
     const int n_mma = (b + 15) / 16 * 16;
-    const WsLayout L = ws_layout(M, k, d, I, cap_rows);
+    const WsLayout L = ws_layout(M, k, d, I, b, cap_rows);
     uint8_t *w = static_cast<uint8_t *>(ws);
     __half *xg = reinterpret_cast<__half *>(w + L.xg);
     __half *hg = reinterpret_cast<__half *>(w + L.hg);
     float *yr = reinterpret_cast<float *>(w + L.yr);
+    int32_t *done = reinterpret_cast<int32_t *>(w + L.done);
 
     // launch configuration first: every check comes before the first launch
     const int G1 = d / 128, G2 = I / 128, Gmax = G1 > G2 ? G1 : G2;
@@ -571,10 +636,8 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     static std::once_flag once;
     static bool attr_ok = false;
     std::call_once(once, [] {
-        attr_ok = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                      cudaSuccess &&
-                  cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                      cudaSuccess;
+        attr_ok = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+                  cudaSuccess;
     });
     if (!attr_ok)
         return MOE_ERR_CUDA;
@@ -592,21 +655,20 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     const int gblocks = grouped_sm_count() * 4;
     const cudaError_t ge =
         x_bf16 ? launch_pdl(gather_kernel<__nv_bfloat16>, dim3(gblocks), dim3(256), 0, s,
-                            static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk), sorted, npp, xg)
+                            static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk), sorted, npp, xg, b, done)
                : launch_pdl(gather_kernel<__half>, dim3(gblocks), dim3(256), 0, s, static_cast<const __half *>(x), d, k,
-                            static_cast<int>(mk), sorted, npp, xg);
+                            static_cast<int>(mk), sorted, npp, xg, b, done);
     if (ge != cudaSuccess)
         return MOE_ERR_CUDA;
     const int grid = grouped_sm_count();
     Args a1{static_cast<const uint16_t *>(w13->scale), static_cast<const int32_t *>(w13->zero), expert_ids, npp, sorted,
             wts, hg, nullptr, dev_status, b, n_mma, I / 128, d / 128, I, d, static_cast<int>(mk), 2 * I, G1, stages,
             aslots, acc_cols, nbuf};
-    if (launch_pdl(gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, a1) != cudaSuccess)
-        return MOE_ERR_CUDA;
     Args a2{static_cast<const uint16_t *>(w2->scale), static_cast<const int32_t *>(w2->zero), expert_ids, npp, sorted,
             wts, nullptr, yr, dev_status, b, n_mma, d / 256, I / 128, I, d, static_cast<int>(mk), d, G2, stages,
             aslots, acc_cols, nbuf};
-    if (launch_pdl(gemm_kernel<2>, dim3(grid), dim3(kThreads), smem, s, tQ2, tB2, a2) != cudaSuccess)
+    if (launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, tQ2, tB2, a1, a2, done, Gmax) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     return grouped_combine_launch(yr, ids, M, k, d, E, y, y_f32, s);
 }

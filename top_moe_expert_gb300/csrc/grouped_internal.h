@@ -20,7 +20,7 @@ moe_status_t grouped_combine_launch(const float *yr, const int32_t *ids, int M, 
                                     bool y_f32, cudaStream_t s);
 
 // 4-bit AWQ grouped path (kind::f16 after in-shared-memory dequantization)
-size_t grouped_awq_workspace(int M, int k, int d, int I, int cap_rows);
+size_t grouped_awq_workspace(int M, int k, int d, int I, int b, int cap_rows);
 moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
                                 const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
                                 const int32_t *sorted, const int32_t *expert_ids, const int32_t *npp, int b,
