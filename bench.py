@@ -250,8 +250,12 @@ class DecodeStep:
         self.x_host = torch.stack([inputs.activations(wl, i) for i in range(self.n_inputs)])
         self.logits_all = self.logits_host.to(device)
         self.x_all = self.x_host.to(device)
-        self.logits = torch.empty((M, E), dtype=torch.float32, device=device)
-        self.x = torch.empty((M, d), dtype=torch.bfloat16, device=device)
+        # x and the router logits share one device buffer, so a step's inputs
+        # arrive in one host-to-device copy
+        self.io = torch.empty(M * d * 2 + M * E * 4, dtype=torch.uint8, device=device)
+        self.x = self.io[:M * d * 2].view(torch.bfloat16).view(M, d)
+        self.logits = self.io[M * d * 2:].view(torch.float32).view(M, E)
+        self.io_host = ("x_host", "logits_host")     # host tensors packed into io, in order
         self.ids = torch.empty((M, k), dtype=torch.int32, device=device)
         self.w = torch.empty((M, k), dtype=torch.float32, device=device)
         self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
@@ -292,7 +296,10 @@ class DecodeStep:
         self.logits_all = self.logits_host.to(device)
         self.x_all = self.x_host.to(device)
         self.logits = torch.empty((M, E), dtype=torch.float32, device=device)
-        self.x = torch.empty((M, d), dtype=torch.float16, device=device)
+        # the routing is fixed: x is the step's only input
+        self.io = torch.empty(M * d * 2, dtype=torch.uint8, device=device)
+        self.x = self.io.view(torch.float16).view(M, d)
+        self.io_host = ("x_host",)
         self.ids = torch.from_numpy(self.fixed_ids).to(device)
         self.w = torch.from_numpy(inputs.fixture_a_weights(M, k, wl.seed)).to(device)
         self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
@@ -466,8 +473,11 @@ def run_ours(args, rank, world, device):
     # e2e: the same steps through the public API with host buffers (pinned)
     Ke = min(K, 2000)
     sel = [(W + i) % st.n_inputs for i in range(Ke)]
-    x_pin = st.x_host[sel].pin_memory() if wl.M <= 64 else st.x_host.pin_memory()
-    l_pin = st.logits_host[sel].pin_memory() if wl.M <= 64 else st.logits_host.pin_memory()
+    # each step's inputs packed in one pinned row, laid out as st.io
+    sel_rows = sel if wl.M <= 64 else list(range(st.n_inputs))
+    io_pin = torch.cat([getattr(st, n)[sel_rows].reshape(len(sel_rows), -1).view(torch.uint8) for n in st.io_host],
+                       dim=1).pin_memory()
+    assert io_pin.shape[1] == st.io.numel()
     y_pin = torch.empty((Ke, wl.M, wl.d), dtype=torch.bfloat16).pin_memory()
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
@@ -477,8 +487,7 @@ def run_ours(args, rank, world, device):
             flush.fill_(float(i))
             e0[i].record(s)
             pi = i if wl.M <= 64 else sel[i]
-            st.x.copy_(x_pin[pi], non_blocking=True)
-            st.logits.copy_(l_pin[pi], non_blocking=True)
+            st.io.copy_(io_pin[pi], non_blocking=True)
             st.launch(s)
             y_pin[i].copy_(st.y, non_blocking=True)
             e1[i].record(s)
@@ -557,7 +566,7 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
                 "us_per_layer": round(e2e_ms * 1e3 / Ke, 3), "steps": Ke,
-                "h2d_bytes_per_step": wl.M * wl.d * 2 + wl.M * wl.E * 4,
+                "h2d_bytes_per_step": st.io.numel(),
                 "d2h_bytes_per_step": wl.M * wl.d * 2},
         "gpu_launches": st.launches_per_step() * K,
         "roofline": roofline_obj(st, wl, layer_ms, Kl, layer_total_bytes, world),
