@@ -10,11 +10,13 @@
 // of "Route-Block Membership Selects Packed-AWQ Arithmetic" (stable
 // construction), one MMA N-tile per MoE block of b rows.
 //
-// Kernels (one CTA per SM for the GEMMs, persistent over tiles):
+// Kernels:
 //   act_quant_kernel : x[t] of every aligned row -> MXFP8 codes + E8M0 atoms
-//   gemm_kernel<1>   : [g;u] = W13_e Xq^T on tcgen05 kind::mxf8f6f4 with
-//                      block scaling; epilogue h = SiLU(g) * u -> MXFP8
-//   gemm_kernel<2>   : W2_e Hq^T; epilogue Yr[route] = w_route * acc
+//   gemm_kernel      : both GEMMs, one CTA per SM, persistent over tiles --
+//                      first-GEMM tiles [g;u] = W13_e Xq^T on tcgen05
+//                      kind::mxf8f6f4 with block scaling, epilogue
+//                      h = SiLU(g) * u -> MXFP8; then second-GEMM tiles
+//                      W2_e Hq^T, epilogue Yr[route] = w_route * acc
 //   combine_kernel   : y[t] = sum over slots j (in order) of Yr[t*k + j]
 // K-reduction order: every output element accumulates its K-tiles in
 // ascending order in one TMEM accumulator; no split-K, no atomics, so the

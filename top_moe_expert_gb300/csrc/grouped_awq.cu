@@ -12,20 +12,22 @@
 //
 // The tensor cores take fp16 x fp16 (tcgen05 kind::f16, FP32 accumulate):
 //   gather_kernel   : Xg[rho] = x[route(rho) / k] as fp16 (zero for padding)
-//   gemm_kernel<1>  : [g;u] = W13_e Xg^T; epilogue h = SiLU(g) * u -> fp16 Hg
-//   gemm_kernel<2>  : W2_e Hg^T; epilogue Yr[route] = w_route * acc
+//   gemm_kernel     : both GEMMs in one persistent kernel -- first-GEMM tiles
+//                     [g;u] = W13_e Xg^T, epilogue h = SiLU(g) * u -> fp16 Hg;
+//                     then second-GEMM tiles W2_e Hg^T, epilogue
+//                     Yr[route] = w_route * acc
 //   combine         : y[t] = sum over slots j (in order) of Yr[t*k + j]
 // The A operand is dequantized on chip into tensor memory: TMA brings each
-// k-step's packed tile (128 rows x 64 values = 32 bytes per row) and the
+// k-step's packed tile (256 rows x 128 values = 64 bytes per row) and the
 // activation tile into shared memory, bulk copies bring each tile's group
 // scales and zeros, and dequantizing warps turn the nibbles into fp16
 // w = (q - z) * s -- (q - z) exactly through the 0x6400 exponent trick, one
 // rounding in the multiply -- and store them with tcgen05.st as the MMA's A
 // operand: row m in TMEM lane m, two values per column.  Four warps (one per
-// TMEM lane quadrant) dequantize one k-step; kDqGroups such groups take the
-// k-steps in turn, so each has several k-steps' time for its chain of waits
-// and stores.  Shared memory then holds only the packed ring, deep enough to
-// cover DRAM latency.
+// TMEM lane quadrant) dequantize one half of a k-step (a "unit", 128 rows);
+// kDqGroups such groups take the units in turn, so each has several units'
+// time for its chain of waits and stores.  Shared memory then holds only the
+// packed ring, deep enough to cover DRAM latency.
 //
 // K order inside the tensor-core operands.  One AND-OR of a packed word with
 // 0x000F000F | 0x64006400 yields nibbles i and i + 4 as an fp16 pair, so the
@@ -35,7 +37,8 @@
 // and the GEMM1 epilogue writes Hg in that order too (interleave_pos).
 //
 // Roles (one CTA per SM, persistent over tiles): warp 0 TMA and bulk copies,
-// warp 1 TMEM and MMA issue, warps 2..5 epilogue, warps 6.. dequantization.
+// warps 1 and 2 TMEM and MMA issue (one per 128-row half of a tile), warps
+// 3..6 epilogue, warps 7..18 dequantization.
 // Every mbarrier wait is bounded; an expired wait records MOE_ERR_TIMEOUT in
 // dev_status[1].
 #include <cuda.h>

@@ -19,7 +19,7 @@ int grouped_sm_count();
 moe_status_t grouped_combine_launch(const float *yr, const int32_t *ids, int M, int k, int d, int E, void *y,
                                     bool y_f32, cudaStream_t s);
 
-// 4-bit AWQ grouped path (kind::f16 after in-shared-memory dequantization)
+// 4-bit AWQ grouped path (kind::f16 on weights dequantized into tensor memory)
 size_t grouped_awq_workspace(int M, int k, int d, int I, int b, int cap_rows);
 moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
                                 const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
