@@ -118,3 +118,14 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(moe, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         moe.lib()
+
+
+def test_python_layout_helper_matches_library():
+    """grouped_workspace_layout (used by the tests to find Xq/Hq/Hs) totals the
+    MXFP8 layout the library sizes, where that layout is the larger one."""
+    for M, k, d, I, b in ((64, 8, 2048, 768, 16), (512, 8, 2048, 768, 64)):
+        cap_rows = moe.moe_align_capacity(M, k, 128, b)[0]
+        L = moe.grouped_workspace_layout(M, k, d, I, b, cap_rows)
+        assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) >= L["total"]
+        awq = _r256(cap_rows * d * 2) + _r256(cap_rows * I * 2) + _r256(M * k * d * 4) + _r256(cap_rows // b * 4)
+        assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(L["total"], awq)

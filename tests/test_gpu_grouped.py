@@ -200,3 +200,25 @@ def test_grouped_compute_probe_sampled():
     ref = oracle.moe_layer(gs.x_exact(x)[tok], ids[tok], w[tok].astype(np.float64), wl.E, w13, w2,
                            mode=oracle.MODE_MX)["y"]
     gs.assert_layer_close(y[torch.from_numpy(tok).cuda()], ref)
+
+
+def test_grouped_workspace_reused_across_shapes():
+    """One workspace serves calls of different batch and block sizes in turn
+    (the fused GEMM's per-block counters are reset by each call): every
+    output equals the one computed with a fresh workspace."""
+    runs = []
+    for M, b in ((21, 16), (64, 8), (21, 8)):
+        wl = inputs.Workload(f"reuse_m{M}", M=M, d=512, I=256, E=128, k=8, seed=11)
+        layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+        fresh, _, aligned = _run(layer, sfa13, sfa2, x, ids, w, b)
+        runs.append((layer, sfa13, sfa2, x, ids, w, b, aligned, fresh))
+    size = max(moe.moe_ffn_grouped_workspace_size(r[3].shape[0], 8, 512, 256, r[6], r[7][0].numel()) for r in runs)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        for layer, sfa13, sfa2, x, ids, w, b, aligned, fresh in runs:
+            st = torch.zeros(2, dtype=torch.int32, device="cuda")
+            y = moe.moe_ffn_grouped(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), layer.w13,
+                                    layer.w2, sfa13, sfa2, aligned, b, out_dtype=torch.float32, ws=ws, dev_status=st)
+            torch.cuda.synchronize()
+            assert st.tolist() == [0, 0]
+            assert torch.equal(y, fresh)

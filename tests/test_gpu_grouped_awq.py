@@ -104,3 +104,26 @@ def test_awq_grouped_limits_rejected(d, b):
         moe.moe_ffn_grouped(x.cuda(), tid, torch.from_numpy(w).cuda(), layer.w13, layer.w2, None, None, aligned, b,
                             ws=ws)
     assert err.value.status == 2
+
+
+def test_awq_grouped_workspace_reused_across_shapes():
+    """One workspace serves AWQ calls of different batch and block sizes in
+    turn; every output equals the one computed with a fresh workspace."""
+    runs = []
+    for M, b in ((40, 16), (12, 8)):
+        wl = inputs.Workload(f"awq_reuse_m{M}", M=M, d=1024, I=256, E=16, k=4, fmt="awq4", seed=12)
+        layer = gs.AwqLayer(wl)
+        x = inputs.activations(wl, dtype=torch.float16)
+        ids, w = gs.routing(wl)
+        fresh, aligned = _run(layer, x, ids, w, b)
+        runs.append((wl, layer, x, ids, w, b, aligned, fresh))
+    size = max(moe.moe_ffn_grouped_workspace_size(r[0].M, r[0].k, r[0].d, r[0].I, r[5], r[6][0].numel()) for r in runs)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        for wl, layer, x, ids, w, b, aligned, fresh in runs:
+            st = torch.zeros(2, dtype=torch.int32, device="cuda")
+            y = moe.moe_ffn_grouped(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), layer.w13,
+                                    layer.w2, None, None, aligned, b, out_dtype=torch.float32, ws=ws, dev_status=st)
+            torch.cuda.synchronize()
+            assert st.tolist() == [0, 0]
+            assert torch.equal(y, fresh)

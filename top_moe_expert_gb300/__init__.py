@@ -301,15 +301,15 @@ def _round256(n):
 
 
 def grouped_workspace_layout(M, k, d, I, b, cap_rows):
-    """Byte offsets of Xq, Xs, Hq, Hs, Yr inside the grouped workspace (the
-    layout include/moe_ffn.h documents) and the total."""
+    """Byte offsets of Xq, Xs, Hq, Hs, Yr and D inside the MXFP8 grouped
+    workspace (the layout include/moe_ffn.h documents) and its total."""
     n_mma = (b + 15) // 16 * 16
     nsf = (n_mma + 127) // 128
     cap_blocks = cap_rows // b
     off, out = 0, {}
     for name, size in (("xq", cap_rows * d), ("xs", cap_blocks * (d // 128) * nsf * 512),
                        ("hq", cap_rows * I), ("hs", cap_blocks * (I // 128) * nsf * 512),
-                       ("yr", M * k * d * 4)):
+                       ("yr", M * k * d * 4), ("done", cap_blocks * 4)):
         out[name] = off
         off += _round256(size)
     out["total"] = off
