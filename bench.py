@@ -2,7 +2,7 @@
 """Benchmark of the routed MoE expert-FFN layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode_m1|tiny|sweep_m<M>[_zipf]|large_m1|large_m8]
+                    [--workload decode_m1|tiny|sweep_m<M>[_zipf]|large_m1|large_m8|awq_fixture_a|awq_m1|probe_m16384]
 
 A step is one pass of the hot path over one batch of fresh synthetic input:
 top-k routing of the step's router logits, then the layer (output-centric
@@ -57,6 +57,10 @@ def workload_from_name(name: str):
         return inputs.LARGE_M8
     if name == "awq_fixture_a":
         return inputs.AWQ_FIXTURE
+    if name == "awq_m1":
+        # one token of the fixture-A closed-form routing: 8 distinct experts
+        return inputs.Workload("awq_m1_d2048_i768_e128_k8", M=1, d=2048, I=768, E=128, k=8, fmt="awq4",
+                               routing="fixture_a", seed=3)
     if name == "probe_m16384":
         return inputs.Workload("grouped_probe_m16384_d2048_i768_e128_k8", M=16384, d=2048, I=768, E=128, k=8,
                                seed=2)
@@ -275,11 +279,11 @@ class DecodeStep:
 
     def _init_awq(self, wl, nsteps, device, block):
         """The 4-bit AWQ layer on its fixed closed-form routing (fixture A):
-        a step is alignment + the grouped layer; activations fp16."""
+        a step is alignment + the grouped layer, or the output-centric decode
+        layer alone; activations fp16."""
         moe = self.moe
         from top_moe_expert_gb300 import inputs
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
-        assert self.path == "grouped", "the AWQ layer runs on the grouped path"
         dev_t = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
         q13, s13, z13 = inputs.awq_weights(wl, "w13")
         q2, s2, z2 = inputs.awq_weights(wl, "w2")
@@ -309,8 +313,11 @@ class DecodeStep:
                         torch.empty(1, dtype=torch.int32, device=device))
         na = moe.moe_align_workspace_size(M, k, E, self.b)
         self.ws_align = torch.empty(max(na, 256), dtype=torch.uint8, device=device) if na else None
-        self.ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, k, d, I, self.b, cr), dtype=torch.uint8,
-                              device=device)
+        if self.path == "grouped":
+            self.ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, k, d, I, self.b, cr), dtype=torch.uint8,
+                                  device=device)
+        else:
+            self.ws = torch.zeros(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device)
         torch.cuda.synchronize()
 
@@ -327,7 +334,9 @@ class DecodeStep:
         if self.routed_in_layer:
             return
         if self.awq:
-            moe.moe_align_block_size(self.ids, self.wl.E, self.b, out=self.aligned, ws=self.ws_align, stream=stream)
+            if self.path == "grouped":
+                moe.moe_align_block_size(self.ids, self.wl.E, self.b, out=self.aligned, ws=self.ws_align,
+                                         stream=stream)
             return
         moe.moe_topk_softmax(self.logits, self.wl.k, self.ids, self.w, stream=stream)
         if self.path == "grouped":
@@ -350,8 +359,10 @@ class DecodeStep:
         self.launch_layer(stream)
 
     def layer_kernels(self) -> str:
-        if self.awq:
+        if self.awq and self.path == "grouped":
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
+        if self.awq:
+            return "moe_ffn_decode (AWQ-4bit): decode_gate_up_kernel<AWQ> + decode_down_kernel<AWQ>"
         if self.path == "grouped":
             return "moe_ffn_grouped: act_quant + gemm_kernel (both GEMMs, one persistent kernel) + combine"
         if self.routed_in_layer:
@@ -362,8 +373,11 @@ class DecodeStep:
 
     def launches_per_step(self) -> int:
         if self.path == "grouped":
+            # (top-k), alignment, act-quant or gather, the GEMM kernel, combine
             na = 2 if self.ws_align is not None else 1
-            return na + 4 if self.awq else 1 + na + 4
+            return na + 3 if self.awq else 1 + na + 3
+        if self.awq:
+            return 2                       # fixed routing: the two decode kernels
         return 1 if self.routed_in_layer else 3
 
     def capture(self):
@@ -555,7 +569,9 @@ def run_ours(args, rank, world, device):
                  "N(0,1) router logits; fresh routing every step)"),
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
                    "path": ("expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
-                            "dequantized into tensor memory + combine, b=%d)" % st.b if st.awq else
+                            "dequantized into tensor memory + combine, b=%d)" % st.b
+                            if st.awq and st.path == "grouped" else
+                            "output-centric AWQ decode (gate/up + down on CUDA cores, fixed routing)" if st.awq else
                             "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
                             % st.b if st.path == "grouped" else
                             "single-token decode: routing + gate/up + SwiGLU + down + combine in one kernel"
