@@ -15,8 +15,8 @@
 //          of equal expert with __match_any_sync, so the position of route r
 //          is off[e] + (#routes of e before r) exactly as the definition.
 // No atomics decide a position, so repeated calls give identical bits.
-#include <mutex>
 
+#include "attr.h"
 #include "common.cuh"
 
 namespace moe {
@@ -315,13 +315,9 @@ MOE_API moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, in
                        static_cast<int>(mk), E, hist, dev_status) != cudaSuccess)
             return MOE_ERR_CUDA;
         const size_t smem = (static_cast<size_t>(3 + kAlignThreads / 32) * E + kChunk) * sizeof(int32_t);
-        static std::once_flag once_m;
-        static bool attr_m = false;
-        std::call_once(once_m, [] {
-            attr_m = cudaFuncSetAttribute(align_place_kernel<kAlignThreads>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) == cudaSuccess;
-        });
-        if (!attr_m || smem > 100 * 1024)
+        static std::atomic<uint64_t> attr_m{0};
+        if (smem > 100 * 1024 ||
+            !smem_attr_once(attr_m, reinterpret_cast<const void *>(align_place_kernel<kAlignThreads>), 100 * 1024))
             return MOE_ERR_CUDA;
         return launch_pdl(align_place_kernel<kAlignThreads>, dim3(nchunks), dim3(kAlignThreads), smem, s, topk_ids,
                           static_cast<int>(mk), E, b, nchunks, static_cast<const int32_t *>(hist), sorted_route_ids,
@@ -331,13 +327,9 @@ MOE_API moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, in
     }
     // one chunk: a single CTA of 1024 threads does everything
     const size_t smem = (static_cast<size_t>(3 + kAlignThreads1 / 32) * E + kChunk) * sizeof(int32_t);
-    static std::once_flag once;
-    static bool attr_ok = false;
-    std::call_once(once, [] {
-        attr_ok = cudaFuncSetAttribute(align_place_kernel<kAlignThreads1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       200 * 1024) == cudaSuccess;
-    });
-    if (!attr_ok || smem > 200 * 1024)
+    static std::atomic<uint64_t> attr_1{0};
+    if (smem > 200 * 1024 ||
+        !smem_attr_once(attr_1, reinterpret_cast<const void *>(align_place_kernel<kAlignThreads1>), 200 * 1024))
         return MOE_ERR_CUDA;
     return launch_pdl(align_place_kernel<kAlignThreads1>, dim3(1), dim3(kAlignThreads1), smem, s, topk_ids,
                       static_cast<int>(mk), E, b, 1, static_cast<const int32_t *>(nullptr), sorted_route_ids,

@@ -33,6 +33,7 @@
 
 #include <mutex>
 
+#include "attr.h"
 #include "common.cuh"
 #include "grouped_internal.h"
 #include "tc.cuh"
@@ -789,13 +790,9 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
                            ? static_cast<int>((227 * 1024 - fixed) / stage_bytes)
                            : kMaxStages;
     const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
-    static std::once_flag attr_once;
-    static bool attr_ok = false;
-    std::call_once(attr_once, [] {
-        attr_ok = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                  cudaSuccess;
-    });
-    if (!attr_ok || stages < 2 || smem > 227 * 1024)
+    static std::atomic<uint64_t> attr_done{0};
+    if (stages < 2 || smem > 227 * 1024 ||
+        !smem_attr_once(attr_done, reinterpret_cast<const void *>(gemm_kernel), 227 * 1024))
         return MOE_ERR_CUDA;
     const int grid = sm_count();
 

@@ -43,9 +43,9 @@
 // dev_status[1].
 #include <cuda.h>
 
-#include <mutex>
 #include <type_traits>
 
+#include "attr.h"
 #include "common.cuh"
 #include "grouped_internal.h"
 #include "tc.cuh"
@@ -636,13 +636,8 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
     if (aslots < kDqGroups || smem > 227 * 1024)
         return MOE_ERR_UNSUPPORTED;
-    static std::once_flag once;
-    static bool attr_ok = false;
-    std::call_once(once, [] {
-        attr_ok = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-                  cudaSuccess;
-    });
-    if (!attr_ok)
+    static std::atomic<uint64_t> attr_done{0};
+    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(gemm_kernel), 227 * 1024))
         return MOE_ERR_CUDA;
 
     // tensor maps: packed weights as bytes [E*N][K/2]; activations fp16 [cap_rows][K]
