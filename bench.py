@@ -429,6 +429,21 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
             "tensor_frac": round(flops / sec / 1e12 / world / peak_tf, 4)}
 
 
+def gather_replicas(times, sizes, world, device=None):
+    """Whole-job figures of N independent replicas: the slowest rank's time
+    (MAX over ranks) for each entry of `times` and the SUM over ranks of each
+    entry of `sizes`.  Every rank gets the result; world == 1 returns the
+    inputs unchanged."""
+    times, sizes = [float(v) for v in times], [float(v) for v in sizes]
+    if world <= 1:
+        return times, sizes
+    tmax = torch.tensor(times, dtype=torch.float64, device=device)
+    tsum = torch.tensor(sizes, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
+    return tmax.tolist(), tsum.tolist()
+
+
 def run_ours(args, rank, world, device):
     wl = workload_from_name(args.workload)
     K, W = args.steps, args.warmup
@@ -531,16 +546,8 @@ def run_ours(args, rank, world, device):
     lb = step_bytes if st.routed_in_layer else layer_bytes
     layer_total_bytes = float(sum(lb(wl, st.step_ids((W + i) % st.n_inputs)) for i in range(Kl)))
 
-    # gather across replicas: max time, summed bytes
-    t = torch.tensor([total_ms, total_bytes, e2e_ms, e2e_bytes, layer_ms, layer_total_bytes], dtype=torch.float64,
-                     device=device)
-    if world > 1:
-        tmax = t.clone()
-        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
-        tsum = t.clone()
-        torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
-        total_ms, e2e_ms, layer_ms = float(tmax[0]), float(tmax[2]), float(tmax[4])
-        total_bytes, e2e_bytes, layer_total_bytes = float(tsum[1]), float(tsum[3]), float(tsum[5])
+    (total_ms, e2e_ms, layer_ms), (total_bytes, e2e_bytes, layer_total_bytes) = gather_replicas(
+        [total_ms, e2e_ms, layer_ms], [total_bytes, e2e_bytes, layer_total_bytes], world, device)
     if rank != 0:
         return None
 
