@@ -9,6 +9,7 @@ present, calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import dataclasses
 import os
@@ -96,28 +97,90 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+# Every pointer handed to the library is checked first: a host tensor, a
+# tensor on another GPU, a strided view, a wrong element type or a short
+# output buffer would otherwise reach a kernel as a bad address or a bad
+# size.  The checks raise ValueError; nothing is launched.
+
+def _is_gpu(t: torch.Tensor) -> bool:
+    return t.device.type == "cuda"
+
+
+def _need(t, name: str, dtypes=None, shape=None, min_numel=None, device=None):
+    """Check one tensor argument: a contiguous CUDA tensor on `device`, of one
+    of `dtypes`, of exactly `shape` or at least `min_numel` elements."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor, not {type(t).__name__}")
+    if not _is_gpu(t):
+        raise ValueError(f"{name} must be a CUDA tensor (it is on {t.device})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}; the call's tensors are on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}; expected {' or '.join(str(d) for d in dtypes)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {tuple(shape)}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call needs at least {min_numel}")
+    return t
 
 
 def _dev(t: torch.Tensor, name: str):
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+    _need(t, name)
 
 
-@dataclasses.dataclass
+def _opt(t, name: str, **kw):
+    """_need for an optional argument (None passes)."""
+    return None if t is None else _need(t, name, **kw)
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def _guard(device):
+    """Make the tensors' GPU current for the call (the library launches on
+    the current device)."""
+    return torch.cuda.device(device) if device.type == "cuda" else contextlib.nullcontext()
+
+
+def _stream(stream=None, device=None):
+    """The stream handle: `stream`, or the current stream of `device`."""
+    if stream is None:
+        s = torch.cuda.current_stream(device)
+    else:
+        s = stream
+        sd = getattr(s, "device", None)
+        if device is not None and sd is not None and sd != device:
+            raise ValueError(f"stream is on {sd}; the call's tensors are on {device}")
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+_IDS = (torch.int32,)
+_F32 = (torch.float32,)
+_U8 = (torch.uint8,)
+_YDT = (torch.bfloat16, torch.float32)
+
+
+@dataclasses.dataclass(frozen=True)
 class Weights:
     """One projection of all experts: MXFP8 (q uint8 [E,N,K], scale uint8
     [E,N,K/32]), MXFP8_T (the same values K-outer: q uint8 [E,K,N], scale
     uint8 [E,K/32,N]) or AWQ4 (q int32 [E,N,K/8], scale fp16 [E,N,K/128],
-    zero int32 [E,N/8,K/128])."""
+    zero int32 [E,N/8,K/128]).  The tensors are checked against the format
+    when the object is made (device, contiguity, dtype, shapes), and the
+    object is immutable, so the layer calls only compare its device."""
     fmt: int
     q: torch.Tensor
     scale: torch.Tensor
     zero: torch.Tensor | None = None
+
+    def __post_init__(self):
+        object.__setattr__(self, "device", self._check())
+        object.__setattr__(self, "_struct", moe_weights_t(
+            self.fmt, self.E, self.N, self.K, self.q.data_ptr(), self.scale.data_ptr(),
+            self.zero.data_ptr() if self.zero is not None else None))
 
     @property
     def E(self):
@@ -133,20 +196,60 @@ class Weights:
             return self.q.shape[1]
         return self.q.shape[2] * (8 if self.fmt == MOE_W_AWQ4 else 1)
 
+    def _check(self):
+        q = _need(self.q, "weights.q")
+        device = q.device
+        if q.dim() != 3:
+            raise ValueError(f"weights.q must be 3-D [E, ., .], not {tuple(q.shape)}")
+        E, N, K = self.E, self.N, self.K
+        if self.fmt == MOE_W_MXFP8:
+            _need(q, "weights.q", _U8)
+            if K % 32:
+                raise ValueError(f"weights: K = {K} is not a multiple of 32")
+            _need(self.scale, "weights.scale", _U8, (E, N, K // 32), device=device)
+        elif self.fmt == MOE_W_MXFP8_T:
+            _need(q, "weights.q", _U8)
+            if K % 32:
+                raise ValueError(f"weights: K = {K} is not a multiple of 32")
+            _need(self.scale, "weights.scale", _U8, (E, K // 32, N), device=device)
+        elif self.fmt == MOE_W_AWQ4:
+            _need(q, "weights.q", _IDS)
+            if K % 128 or N % 8:
+                raise ValueError(f"weights: AWQ needs K % 128 == 0 and N % 8 == 0 (K = {K}, N = {N})")
+            _need(self.scale, "weights.scale", (torch.float16,), (E, N, K // 128), device=device)
+            if self.zero is None:
+                raise ValueError("weights.zero is required for AWQ weights")
+            _need(self.zero, "weights.zero", _IDS, (E, N // 8, K // 128), device=device)
+        else:
+            raise ValueError(f"weights: unknown format {self.fmt}")
+        if self.fmt != MOE_W_AWQ4 and self.zero is not None:
+            raise ValueError("weights.zero must be None for MXFP8 weights")
+        return device
+
+    def on(self, name: str, device):
+        """Raise unless the weights live on `device`."""
+        if self.device != device:
+            raise ValueError(f"{name} is on {self.device}; the call's tensors are on {device}")
+
     def c_struct(self) -> moe_weights_t:
-        return moe_weights_t(self.fmt, self.E, self.N, self.K, self.q.data_ptr(),
-                             self.scale.data_ptr(), self.zero.data_ptr() if self.zero is not None else None)
+        return self._struct
 
 
 # ---------------------------------------------------------------- routing
 
 def moe_topk_softmax(logits: torch.Tensor, k: int, topk_ids=None, topk_w=None, stream=None):
-    _dev(logits, "logits")
+    _need(logits, "logits", _F32)
+    if logits.dim() != 2:
+        raise ValueError(f"logits must be [M, E], not {tuple(logits.shape)}")
+    dev = logits.device
     M, E = logits.shape
-    ids = topk_ids if topk_ids is not None else torch.empty((M, k), dtype=torch.int32, device=logits.device)
-    w = topk_w if topk_w is not None else torch.empty((M, k), dtype=torch.float32, device=logits.device)
-    _check(lib().moe_topk_softmax(_ptr(logits), M, E, k, _ptr(ids), _ptr(w), _stream(stream)),
-           "moe_topk_softmax")
+    ids = topk_ids if topk_ids is not None else torch.empty((M, k), dtype=torch.int32, device=dev)
+    w = topk_w if topk_w is not None else torch.empty((M, k), dtype=torch.float32, device=dev)
+    _need(ids, "topk_ids", _IDS, (M, k), device=dev)
+    _need(w, "topk_w", _F32, (M, k), device=dev)
+    with _guard(dev):
+        _check(lib().moe_topk_softmax(_ptr(logits), M, E, k, _ptr(ids), _ptr(w), _stream(stream, dev)),
+               "moe_topk_softmax")
     return ids, w
 
 
@@ -168,22 +271,34 @@ def moe_align_block_size(topk_ids: torch.Tensor, E: int, b: int, cap_rows=None, 
                          out=None, ws=None, dev_status=None, stream=None):
     """Returns (sorted_route_ids [cap_rows], expert_ids [cap_blocks],
     num_rows_post_pad [1]) as int32 device tensors."""
-    _dev(topk_ids, "topk_ids")
+    _need(topk_ids, "topk_ids", _IDS)
+    if topk_ids.dim() != 2:
+        raise ValueError(f"topk_ids must be [M, k], not {tuple(topk_ids.shape)}")
     M, k = topk_ids.shape
-    cr, cb = moe_align_capacity(M, k, E, b)
-    cap_rows = cr if cap_rows is None else cap_rows
-    cap_blocks = cb if cap_blocks is None else cap_blocks
     dev = topk_ids.device
     if out is None:
+        cr, cb = moe_align_capacity(M, k, E, b)
+        cap_rows = cr if cap_rows is None else cap_rows
+        cap_blocks = cb if cap_blocks is None else cap_blocks
         out = (torch.empty(cap_rows, dtype=torch.int32, device=dev),
                torch.empty(cap_blocks, dtype=torch.int32, device=dev),
                torch.empty(1, dtype=torch.int32, device=dev))
+    else:
+        # capacities default to the given buffers' lengths
+        cap_rows = out[0].numel() if cap_rows is None else cap_rows
+        cap_blocks = out[1].numel() if cap_blocks is None else cap_blocks
+    _need(out[0], "sorted_route_ids", _IDS, min_numel=cap_rows, device=dev)
+    _need(out[1], "expert_ids", _IDS, min_numel=cap_blocks, device=dev)
+    _need(out[2], "num_rows_post_pad", _IDS, min_numel=1, device=dev)
     need = moe_align_workspace_size(M, k, E, b)
     if ws is None and need:
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    _check(lib().moe_align_block_size(_ptr(topk_ids), M, k, E, b, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
-                                      cap_rows, cap_blocks, _ptr(ws), ws.numel() if ws is not None else 0,
-                                      _ptr(dev_status), _stream(stream)), "moe_align_block_size")
+    _opt(ws, "ws", device=dev)
+    _opt(dev_status, "dev_status", dtypes=_IDS, min_numel=2, device=dev)
+    with _guard(dev):
+        _check(lib().moe_align_block_size(_ptr(topk_ids), M, k, E, b, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                          cap_rows, cap_blocks, _ptr(ws), _nbytes(ws), _ptr(dev_status),
+                                          _stream(stream, dev)), "moe_align_block_size")
     return out
 
 
@@ -191,28 +306,58 @@ def moe_align_block_size(topk_ids: torch.Tensor, E: int, b: int, cap_rows=None, 
 
 def moe_mxfp8_quantize(v: torch.Tensor, q=None, s=None, stream=None):
     """MXFP8 codes and E8M0 scales of v [rows, K] (fp32 or bf16)."""
-    _dev(v, "v")
+    _need(v, "v", (torch.float32, torch.bfloat16))
+    dev = v.device
     K = v.shape[-1]
-    rows = v.numel() // K
-    q = q if q is not None else torch.empty(v.shape, dtype=torch.uint8, device=v.device)
-    s = s if s is not None else torch.empty((*v.shape[:-1], K // 32), dtype=torch.uint8, device=v.device)
-    _check(lib().moe_mxfp8_quantize(_ptr(v), _DT[v.dtype], rows, K, _ptr(q), _ptr(s), _stream(stream)),
-           "moe_mxfp8_quantize")
+    if K % 32:
+        raise ValueError(f"v's last dimension ({K}) is not a multiple of 32")
+    rows = v.numel() // K if K else 0
+    q = q if q is not None else torch.empty(v.shape, dtype=torch.uint8, device=dev)
+    s = s if s is not None else torch.empty((*v.shape[:-1], K // 32), dtype=torch.uint8, device=dev)
+    _need(q, "q", _U8, min_numel=rows * K, device=dev)
+    _need(s, "s", _U8, min_numel=rows * (K // 32), device=dev)
+    with _guard(dev):
+        _check(lib().moe_mxfp8_quantize(_ptr(v), _DT[v.dtype], rows, K, _ptr(q), _ptr(s), _stream(stream, dev)),
+               "moe_mxfp8_quantize")
     return q, s
 
 
 def moe_mxfp8_transpose(w: Weights, stream=None) -> Weights:
     """The same MXFP8 weights re-laid K-outer (MOE_W_MXFP8_T)."""
-    assert w.fmt == MOE_W_MXFP8
-    q_t = torch.empty((w.E, w.K, w.N), dtype=torch.uint8, device=w.q.device)
-    s_t = torch.empty((w.E, w.K // 32, w.N), dtype=torch.uint8, device=w.q.device)
+    if w.fmt != MOE_W_MXFP8:
+        raise ValueError("moe_mxfp8_transpose takes MOE_W_MXFP8 weights")
+    dev = w.device
+    q_t = torch.empty((w.E, w.K, w.N), dtype=torch.uint8, device=dev)
+    s_t = torch.empty((w.E, w.K // 32, w.N), dtype=torch.uint8, device=dev)
     a = w.c_struct()
-    _check(lib().moe_mxfp8_transpose(ctypes.byref(a), _ptr(q_t), _ptr(s_t), _stream(stream)),
-           "moe_mxfp8_transpose")
+    with _guard(dev):
+        _check(lib().moe_mxfp8_transpose(ctypes.byref(a), _ptr(q_t), _ptr(s_t), _stream(stream, dev)),
+               "moe_mxfp8_transpose")
     return Weights(MOE_W_MXFP8_T, q_t, s_t)
 
 
 # ---------------------------------------------------------------- the layer
+
+def _layer_args(x, topk_ids, topk_w, w13: Weights, w2: Weights, y, out_dtype, dev_status):
+    """Check the common arguments of the layer calls; returns (device, M, d,
+    k, y) with y allocated when not given."""
+    _need(x, "x", tuple(_DT))
+    if x.dim() != 2:
+        raise ValueError(f"x must be [M, d], not {tuple(x.shape)}")
+    dev = x.device
+    M, d = x.shape
+    _need(topk_ids, "topk_ids", _IDS, device=dev)
+    if topk_ids.dim() != 2 or topk_ids.shape[0] != M:
+        raise ValueError(f"topk_ids must be [M={M}, k], not {tuple(topk_ids.shape)}")
+    k = topk_ids.shape[1]
+    _need(topk_w, "topk_w", _F32, (M, k), device=dev)
+    w13.on("w13", dev)
+    w2.on("w2", dev)
+    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=dev)
+    _need(y, "y", _YDT, (M, d), device=dev)
+    _opt(dev_status, "dev_status", dtypes=_IDS, min_numel=2, device=dev)
+    return dev, M, d, k, y
+
 
 def moe_ffn_decode_workspace_size(M: int, k: int, d: int, I: int) -> int:
     n = ctypes.c_size_t()
@@ -223,20 +368,18 @@ def moe_ffn_decode_workspace_size(M: int, k: int, d: int, I: int) -> int:
 def moe_ffn_decode(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, w13: Weights, w2: Weights,
                    out_dtype=torch.bfloat16, y=None, ws=None, dev_status=None, stream=None):
     """Output-centric decode path: y [M, d] = sum_j w_j * FFN_{e_j}(x)."""
-    for t, n in ((x, "x"), (topk_ids, "topk_ids"), (topk_w, "topk_w")):
-        _dev(t, n)
-    M, d = x.shape
-    k = topk_ids.shape[1]
+    dev, M, d, k, y = _layer_args(x, topk_ids, topk_w, w13, w2, y, out_dtype, dev_status)
     I = w2.K
-    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
     if ws is None:
         # zeroed: the single-token path keeps its grid-barrier counters in the
         # first 256 bytes and needs them zero before the first call
-        ws = torch.zeros(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=x.device)
+        ws = torch.zeros(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=dev)
+    _need(ws, "ws", device=dev)
     a, b = w13.c_struct(), w2.c_struct()
-    _check(lib().moe_ffn_decode(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
-                                ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype], _ptr(ws),
-                                ws.numel(), _ptr(dev_status), _stream(stream)), "moe_ffn_decode")
+    with _guard(dev):
+        _check(lib().moe_ffn_decode(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                    ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype], _ptr(ws),
+                                    _nbytes(ws), _ptr(dev_status), _stream(stream, dev)), "moe_ffn_decode")
     return y
 
 
@@ -246,20 +389,28 @@ def moe_ffn_decode_logits(logits: torch.Tensor, x: torch.Tensor, k: int, w13: We
     """Routing + decode layer in one call (one kernel for a single token on the
     single-pass layout): returns (y, topk_ids, topk_w), identical to
     moe_topk_softmax followed by moe_ffn_decode."""
-    for t, n in ((logits, "logits"), (x, "x")):
-        _dev(t, n)
+    _need(x, "x", tuple(_DT))
+    if x.dim() != 2:
+        raise ValueError(f"x must be [M, d], not {tuple(x.shape)}")
+    dev = x.device
     M, d = x.shape
+    _need(logits, "logits", _F32, device=dev)
+    if logits.dim() != 2 or logits.shape[0] != M or logits.shape[1] != w13.E:
+        raise ValueError(f"logits must be [M={M}, E={w13.E}], not {tuple(logits.shape)}")
+    topk_ids = topk_ids if topk_ids is not None else torch.empty((M, k), dtype=torch.int32, device=dev)
+    topk_w = topk_w if topk_w is not None else torch.empty((M, k), dtype=torch.float32, device=dev)
+    _need(topk_ids, "topk_ids", _IDS, (M, k), device=dev)
+    dev, M, d, k, y = _layer_args(x, topk_ids, topk_w, w13, w2, y, out_dtype, dev_status)
     I = w2.K
-    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
-    topk_ids = topk_ids if topk_ids is not None else torch.empty((M, k), dtype=torch.int32, device=x.device)
-    topk_w = topk_w if topk_w is not None else torch.empty((M, k), dtype=torch.float32, device=x.device)
     if ws is None:
-        ws = torch.zeros(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=x.device)
+        ws = torch.zeros(moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=dev)
+    _need(ws, "ws", device=dev)
     a, b = w13.c_struct(), w2.c_struct()
-    _check(lib().moe_ffn_decode_logits(_ptr(logits), _ptr(x), _DT[x.dtype], M, d, k, ctypes.byref(a),
-                                       ctypes.byref(b), _ptr(topk_ids), _ptr(topk_w), _ptr(y), _DT[y.dtype],
-                                       _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream)),
-           "moe_ffn_decode_logits")
+    with _guard(dev):
+        _check(lib().moe_ffn_decode_logits(_ptr(logits), _ptr(x), _DT[x.dtype], M, d, k, ctypes.byref(a),
+                                           ctypes.byref(b), _ptr(topk_ids), _ptr(topk_w), _ptr(y), _DT[y.dtype],
+                                           _ptr(ws), _nbytes(ws), _ptr(dev_status), _stream(stream, dev)),
+               "moe_ffn_decode_logits")
     return y, topk_ids, topk_w
 
 
@@ -269,15 +420,12 @@ def moe_ffn_decode_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torc
     library device memory: the intermediate lives in a fixed 4 MiB array
     inside the library (MXFP8 two-kernel path only; first call on a device
     outside stream capture; calls must not overlap on the GPU)."""
-    for t, nm in ((x, "x"), (topk_ids, "topk_ids"), (topk_w, "topk_w")):
-        _dev(t, nm)
-    M, d = x.shape
-    k = topk_ids.shape[1]
-    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
+    dev, M, d, k, y = _layer_args(x, topk_ids, topk_w, w13, w2, y, out_dtype, dev_status)
     a, b = w13.c_struct(), w2.c_struct()
-    _check(lib().moe_ffn_decode_noalloc(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
-                                        ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype],
-                                        _ptr(dev_status), _stream(stream)), "moe_ffn_decode_noalloc")
+    with _guard(dev):
+        _check(lib().moe_ffn_decode_noalloc(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                            ctypes.byref(a), ctypes.byref(b), _ptr(y), _DT[y.dtype],
+                                            _ptr(dev_status), _stream(stream, dev)), "moe_ffn_decode_noalloc")
     return y
 
 
@@ -285,14 +433,17 @@ def moe_ffn_decode_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torc
 
 def moe_grouped_prepare(w13: Weights, w2: Weights, stream=None):
     """Scale atoms of both projections in the tensor-core layout."""
+    dev = w13.device
+    w2.on("w2", dev)
     a, b = w13.c_struct(), w2.c_struct()
     n13, n2 = ctypes.c_size_t(), ctypes.c_size_t()
     _check(lib().moe_grouped_prepare_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(n13), ctypes.byref(n2)),
            "moe_grouped_prepare_size")
-    sfa13 = torch.empty(n13.value, dtype=torch.uint8, device=w13.q.device)
-    sfa2 = torch.empty(n2.value, dtype=torch.uint8, device=w13.q.device)
-    _check(lib().moe_grouped_prepare(ctypes.byref(a), ctypes.byref(b), _ptr(sfa13), _ptr(sfa2), _stream(stream)),
-           "moe_grouped_prepare")
+    sfa13 = torch.empty(n13.value, dtype=torch.uint8, device=dev)
+    sfa2 = torch.empty(n2.value, dtype=torch.uint8, device=dev)
+    with _guard(dev):
+        _check(lib().moe_grouped_prepare(ctypes.byref(a), ctypes.byref(b), _ptr(sfa13), _ptr(sfa2),
+                                         _stream(stream, dev)), "moe_grouped_prepare")
     return sfa13, sfa2
 
 
@@ -328,21 +479,33 @@ def moe_ffn_grouped(x, topk_ids, topk_w, w13: Weights, w2: Weights, sfa13, sfa2,
                     out_dtype=torch.bfloat16, y=None, ws=None, dev_status=None, stream=None):
     """Expert-centric grouped path; `aligned` = (sorted_route_ids,
     expert_ids, num_rows_post_pad) from moe_align_block_size with the same b."""
-    for t, nm in ((x, "x"), (topk_ids, "topk_ids"), (topk_w, "topk_w")):
-        _dev(t, nm)
-    M, d = x.shape
-    k = topk_ids.shape[1]
+    dev, M, d, k, y = _layer_args(x, topk_ids, topk_w, w13, w2, y, out_dtype, dev_status)
     I = w2.K
+    if b < 1:
+        raise ValueError(f"block size b = {b} must be positive")
     sorted_ids, expert_ids, npp = aligned
+    _need(sorted_ids, "sorted_route_ids", _IDS, device=dev)
     cap_rows = sorted_ids.numel()
-    y = y if y is not None else torch.empty((M, d), dtype=out_dtype, device=x.device)
-    if ws is None:
-        ws = torch.empty(moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows), dtype=torch.uint8,
-                         device=x.device)
+    _need(expert_ids, "expert_ids", _IDS, min_numel=cap_rows // b, device=dev)
+    _need(npp, "num_rows_post_pad", _IDS, min_numel=1, device=dev)
     a, bb = w13.c_struct(), w2.c_struct()
-    _check(lib().moe_ffn_grouped(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
-                                 ctypes.byref(a), ctypes.byref(bb), _ptr(sfa13), _ptr(sfa2),
-                                 _ptr(sorted_ids), _ptr(expert_ids), _ptr(npp), b, cap_rows,
-                                 _ptr(y), _DT[y.dtype], _ptr(ws), ws.numel(), _ptr(dev_status),
-                                 _stream(stream)), "moe_ffn_grouped")
+    if w13.fmt == MOE_W_MXFP8 and w2.fmt == MOE_W_MXFP8:
+        # the block-scaled MMA reads the scale atoms moe_grouped_prepare wrote
+        n13, n2 = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().moe_grouped_prepare_size(ctypes.byref(a), ctypes.byref(bb), ctypes.byref(n13),
+                                              ctypes.byref(n2)), "moe_grouped_prepare_size")
+        _need(sfa13, "sfa13", _U8, min_numel=n13.value, device=dev)
+        _need(sfa2, "sfa2", _U8, min_numel=n2.value, device=dev)
+    else:
+        _opt(sfa13, "sfa13", device=dev)
+        _opt(sfa2, "sfa2", device=dev)
+    if ws is None:
+        ws = torch.empty(moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows), dtype=torch.uint8, device=dev)
+    _need(ws, "ws", device=dev)
+    with _guard(dev):
+        _check(lib().moe_ffn_grouped(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                     ctypes.byref(a), ctypes.byref(bb), _ptr(sfa13), _ptr(sfa2),
+                                     _ptr(sorted_ids), _ptr(expert_ids), _ptr(npp), b, cap_rows,
+                                     _ptr(y), _DT[y.dtype], _ptr(ws), _nbytes(ws), _ptr(dev_status),
+                                     _stream(stream, dev)), "moe_ffn_grouped")
     return y
