@@ -185,6 +185,8 @@ SRC_FILES = {
                "topk.cuh", "common.cuh", "tc.cuh"),
     "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh"),
     "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh"),
+    "awq_decode": ("decode.cu", "decode_awq_m1.cu", "decode_awq_m1.cuh", "decode_internal.h", "common.cuh",
+                   "tc.cuh", "attr.h"),
 }
 
 
@@ -361,6 +363,8 @@ class DecodeStep:
     def layer_kernels(self) -> str:
         if self.awq and self.path == "grouped":
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
+        if self.awq and self.wl.M == 1:
+            return "moe_ffn_decode (AWQ-4bit, one token): da1::awq_m1_kernel (gate/up + SwiGLU + down), one kernel"
         if self.awq:
             return "moe_ffn_decode (AWQ-4bit): decode_gate_up_kernel<AWQ> + decode_down_kernel<AWQ>"
         if self.path == "grouped":
@@ -377,7 +381,8 @@ class DecodeStep:
             na = 2 if self.ws_align is not None else 1
             return na + 3 if self.awq else 1 + na + 3
         if self.awq:
-            return 2                       # fixed routing: the two decode kernels
+            # fixed routing: the single-token kernel, or the two decode kernels
+            return 1 if self.wl.M == 1 else 2
         return 1 if self.routed_in_layer else 3
 
     def capture(self):
@@ -413,7 +418,8 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     t_hbm = total_bytes / (peak_gbs * 1e9)
     t_mma = flops / (peak_tf * 1e12)
     kern = st.layer_kernels()
-    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash("awq" if st.awq else st.path))
+    src = ("awq" if st.path == "grouped" else "awq_decode") if st.awq else st.path
+    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash(src))
     if t_mma > t_hbm:
         ach = flops / sec / 1e12 / world
         return {"kernel": kern, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_tf,
@@ -578,6 +584,8 @@ def run_ours(args, rank, world, device):
                    "path": ("expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
                             "dequantized into tensor memory + combine, b=%d)" % st.b
                             if st.awq and st.path == "grouped" else
+                            ("single-token AWQ decode: gate/up + SwiGLU + down in one kernel, f16 mma.sync dot "
+                             "products on raw 4-bit codes, zero folded in FP32, fixed routing") if st.awq and wl.M == 1 else
                             "output-centric AWQ decode (gate/up + down on CUDA cores, fixed routing)" if st.awq else
                             "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
                             % st.b if st.path == "grouped" else

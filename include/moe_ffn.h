@@ -173,8 +173,11 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  * MOE_W_MXFP8_T cases -> one streaming pass (gate/up rows and down columns of
  * each neuron together, per-SM partial outputs) plus a fixed-order reduction
  * kernel; MXFP8 with M*k <= 512 -> a gate/up kernel and a
- * down kernel chained by programmatic dependent launch; otherwise one warp
- * per intermediate / output scalar.  Every output's summation order is fixed
+ * down kernel chained by programmatic dependent launch; AWQ4 with M == 1 ->
+ * one kernel (gate/up dots on f16 mma.sync over the raw 4-bit codes with the
+ * zero folded out in FP32, a grid-wide barrier whose counter lives in
+ * ws[0..8), then the down projection), when its shared-memory plan fits;
+ * otherwise one warp per intermediate / output scalar.  Every output's summation order is fixed
  * by the shapes, the path and (single-pass path) the set of routed experts,
  * so identical inputs give identical bits; the two-kernel and per-scalar
  * paths are also independent of the other tokens in the batch.

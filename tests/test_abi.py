@@ -62,6 +62,9 @@ def test_decode_workspace_size():
     assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 8 * 768 * 4
     assert moe.moe_ffn_decode_workspace_size(3, 8, 512, 100) % 256 == 0
     assert moe.moe_ffn_decode_workspace_size(64, 8, 2048, 768) == 64 * 8 * 768 * 4
+    # one token, d % 1024 == 0: at least the single-token AWQ kernel's barrier
+    # counter (256 B) and its phase-1 pieces [k * 2I / 8][4][8] f32
+    assert moe.moe_ffn_decode_workspace_size(1, 8, 2048, 768) >= 256 + 8 * (2 * 768 // 8) * 4 * 8 * 4
 
 
 def _r256(n):

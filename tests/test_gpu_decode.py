@@ -144,6 +144,76 @@ def test_awq_decode_fixture_shape():
     gs.assert_layer_close(y, ref)
 
 
+# ---- one token, 4-bit AWQ: the single-kernel path (gate/up, SwiGLU, down)
+
+AWQ_M1 = inputs.Workload("awq_m1_d2048_i768_e128_k8", M=1, d=2048, I=768, E=128, k=8, fmt="awq4", seed=3)
+AWQ_M1_SMALL = inputs.Workload("awq_m1_d1024_i256_e16_k4", M=1, d=1024, I=256, E=16, k=4, fmt="awq4", seed=7)
+_awq_layers = {}
+
+
+def awq_layer(wl):
+    if wl.name not in _awq_layers:
+        _awq_layers.clear()
+        torch.cuda.empty_cache()
+        _awq_layers[wl.name] = gs.AwqLayer(wl)
+    return _awq_layers[wl.name]
+
+
+def oracle_awq(layer, x, ids, w):
+    return oracle.moe_layer(gs.x_exact(x), ids, np.asarray(w, dtype=np.float64), layer.wl.E, layer.host13,
+                            layer.host2)["y"]
+
+
+def run_awq(layer, x, ids, w, out_dtype=torch.float32, **kw):
+    return moe.moe_ffn_decode(x.cuda(), torch.as_tensor(ids, dtype=torch.int32).cuda(),
+                              torch.as_tensor(w, dtype=torch.float32).cuda(), layer.w13, layer.w2,
+                              out_dtype=out_dtype, **kw)
+
+
+@pytest.mark.parametrize("wl", [AWQ_M1_SMALL, AWQ_M1], ids=lambda w: w.name)
+@pytest.mark.parametrize("xdt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_awq_single_token(wl, xdt, out_dtype):
+    layer = awq_layer(wl)
+    x = inputs.activations(wl, dtype=xdt)
+    ids, w = gs.routing(wl)
+    y = run_awq(layer, x, ids, w, out_dtype)
+    gs.assert_layer_close(y, oracle_awq(layer, x, ids, w))
+
+
+def test_awq_single_token_activation_scales():
+    # x is staged in f16 after an exact power-of-two rescale
+    wl = AWQ_M1
+    layer = awq_layer(wl)
+    ids, w = gs.routing(wl)
+    for scale, xdt in ((1e-3, torch.float16), (3e3, torch.bfloat16)):
+        x = (inputs.activations(wl, dtype=torch.float32) * scale).to(xdt)
+        gs.assert_layer_close(run_awq(layer, x, ids, w), oracle_awq(layer, x, ids, w))
+
+
+def test_awq_single_token_routes_repeats_and_barrier_counter():
+    wl = AWQ_M1_SMALL
+    layer = awq_layer(wl)
+    x = inputs.activations(wl, dtype=torch.float16)
+    ids = np.array([[3, 3, -1, wl.E]], dtype=np.int32)           # a duplicate and two invalid routes
+    w = np.array([[0.4, 0.3, 0.2, 0.1]], dtype=np.float32)
+    ws = torch.zeros(moe.moe_ffn_decode_workspace_size(1, wl.k, wl.d, wl.I), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ys = [run_awq(layer, x, ids, w, ws=ws, dev_status=st) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert st.tolist() == [6, 0]
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])                              # repeats are bit-identical
+    gs.assert_layer_close(ys[0], oracle_awq(layer, x, ids, w))
+    # each call adds one arrival per CTA (one CTA per SM) to the counter in ws[0..8)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ws[:8].view(torch.int64).item() == 3 * sms
+    # no valid route: y = 0
+    y0 = run_awq(layer, x, np.array([[-1, wl.E, 99, -5]], dtype=np.int32), w, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y0).item() == 0
+
+
 @pytest.mark.parametrize("wl", [inputs.LARGE_M1, inputs.LARGE_M8], ids=lambda w: w.name)
 def test_large_expert_decode(wl):
     ids, w = gs.routing(wl)

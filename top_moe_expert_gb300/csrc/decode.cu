@@ -323,6 +323,10 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
         const size_t m1 = decode_m1_workspace(d);
         part = part > m1 ? part : m1;
     }
+    if (M == 1 && k <= 32 && d % 1024 == 0 && I % 128 == 0) {
+        const size_t a1 = decode_awq_m1_workspace(k, I);
+        part = part > a1 ? part : a1;
+    }
     *bytes = h > part ? h : part;
     return MOE_OK;
 }
@@ -409,6 +413,9 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         return MOE_ERR_WORKSPACE;
     float *h = static_cast<float *>(ws);
     cudaStream_t s = as_stream(stream);
+    if (fmt == MOE_W_AWQ4 && decode_awq_m1_eligible(M, k, d, I, w13->E))
+        return decode_awq_m1_launch(x, xdt == MOE_BF16, topk_ids, topk_w, k, d, I, w13->E, w13->q, w13->scale,
+                                    w13->zero, w2->q, w2->scale, w2->zero, y, ydt == MOE_FP32, ws, dev_status, s);
     if (fmt == MOE_W_MXFP8 && decode_stream_eligible(M, k, d, I, w13->E, w13->q, w13->scale, w2->q, w2->scale)) {
         const moe_status_t st2 = decode_stream_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
                                     static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),

@@ -1,0 +1,475 @@
+// decode_awq_m1.cu -- single-token (M = 1) decode of the routed 4-bit AWQ
+// expert layer in one kernel.
+//
+// Output-centric decode ("Warp decode", cursor.com blog, sections on what
+// changed and how the two kernels work): for each routed expert
+//     h_j = w_j SiLU(Wg_{e_j} x) (Wu_{e_j} x),   y = sum_j W2_{e_j} h_j,
+// weights streamed once with on-the-fly dequantisation and FP32 sums, no
+// alignment, padding or combine buffers.  The routing weight is applied to h
+// (equal, in exact arithmetic, to applying it in the down accumulation).
+// Dot products use the f16 MMA trick described in decode_awq_m1.cuh.
+//
+// One CTA per SM, 16 warps:
+//  * Prologue: the valid routes compacted in slot order; x scaled by an
+//    exact power of two into f16 range and staged in the MMA order with its
+//    per-group sums; warp 0 starts cp.async.bulk copies of this CTA's W2 rows
+//    (its blocks of 8 outputs, every valid slot) into shared memory.
+//  * Phase 1: the items (unit = 8 rows of W13 of one slot; group of 128 K
+//    values) are split evenly over the CTAs and, within a CTA, over the
+//    warps; a warp keeps its next items' loads in flight while it runs one
+//    item's eight MMAs.  A unit's partial sums are combined in a fixed order:
+//    within the CTA through shared memory, across CTAs as pieces in the
+//    workspace (a unit spans at most kMaxPieces CTAs).
+//  * The CTA stages its phase-2 scales and zeros; grid barrier (one arrival
+//    per CTA on a never-reset 64-bit counter in ws[0..8); bounded spin).
+//  * Phase 2: h from the pieces in a fixed order; per slot an exact power of
+//    two into f16 range and an f16 hi + lo split (staged in the MMA order,
+//    with group sums); units (slot, block of 8 outputs) over the warps,
+//    2 x 8 MMAs per group with W2 from shared memory; y = the slots' results
+//    added in slot order.
+// Every output's summation order depends only on the shapes and the grid,
+// so repeats are bit-identical.  The grid is one CTA per SM, all resident
+// together; dependent launches start after the barrier.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include <atomic>
+
+#include "attr.h"
+#include "common.cuh"
+#include "decode_awq_m1.cuh"
+#include "decode_internal.h"
+#include "tc.cuh"
+
+namespace moe {
+namespace da1 {
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kPF = 4;                  // phase-1 items in flight per warp
+
+__device__ __forceinline__ void set_err(int32_t *st, int code)
+{
+    if (st)
+        atomicCAS(st + 1, 0, code);
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Exponent sigma with m 2^sigma in [2^14, 2^15) (0 for m == 0).
+__device__ __forceinline__ int f16_sigma(float m)
+{
+    if (!(m > 0.f))
+        return 0;
+    int ex;
+    frexpf(m, &ex);                      // m = f 2^ex, f in [0.5, 1)
+    return 15 - ex;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) awq_m1_kernel(const Args a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int d = a.d, I = a.I, NG = d / 128, G2 = I / 128, RB = 2 * I / 8;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = lane & 3, gl = lane >> 2;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int B2 = d / 8, blk0 = split_lo(B2, b, G), nb = split_lo(B2, b + 1, G) - blk0;
+    const Smem L{d, I, a.k, nb};
+    __half *xp = reinterpret_cast<__half *>(smem + L.xp());
+    float *xsum = reinterpret_cast<float *>(smem + L.xsum());
+    int *r_e = reinterpret_cast<int *>(smem + L.route());
+    float *r_w = reinterpret_cast<float *>(r_e + kMaxK);
+    int *r_sig = reinterpret_cast<int *>(r_w + kMaxK);
+    const uint32_t mbar = tc::smem_u32(smem + L.mbar());
+    float *p1v = reinterpret_cast<float *>(smem + L.part1());           // [16][4][8]
+    int *p1u = reinterpret_cast<int *>(p1v + kWarps * 4 * 8);          // [16][4]
+    uint32_t *w2s = reinterpret_cast<uint32_t *>(smem + L.w2());
+    float *sc2 = reinterpret_cast<float *>(smem + L.sz2());
+    float *zz2 = sc2 + a.k * nb * 8 * G2;
+    float *hf = reinterpret_cast<float *>(smem + L.hf());
+    __half *hp = reinterpret_cast<__half *>(smem + L.hp());            // [2][k][I]
+    float *hsum = reinterpret_cast<float *>(smem + L.hsum());
+    float *part2 = reinterpret_cast<float *>(smem + L.part2());
+    __shared__ int s_nv, s_ok, s_abort, s_sigx;
+    __shared__ unsigned long long s_epoch;
+    __shared__ float s_wmax[kWarps];
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) {
+        unsigned long long v;
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.bar) : "memory");
+        s_epoch = v;
+        s_abort = 0;
+        tc::mbar_init(mbar, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        const int e = lane < a.k ? a.ids[lane] : -1;
+        const bool ok = lane < a.k && e >= 0 && e < a.E;
+        const unsigned vm = __ballot_sync(0xffffffffu, ok);
+        if (ok) {
+            const int i = __popc(vm & ((1u << lane) - 1u));
+            r_e[i] = e;
+            r_w[i] = a.wts[lane];
+        }
+        if (lane == 0) {
+            s_nv = __popc(vm);
+            if (b == 0 && a.k > __popc(vm) && a.dev_status)
+                atomicAdd(a.dev_status, a.k - __popc(vm));
+        }
+    }
+    // max |x| for the f16 scale of x
+    float xm = 0.f;
+    for (int i = tid; i < d; i += kThreads) {
+        const float v = a.x_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.x)[i])
+                                 : __half2float(reinterpret_cast<const __half *>(a.x)[i]);
+        xm = fmaxf(xm, fabsf(v));
+    }
+    xm = warp_max(xm);
+    if (lane == 0)
+        s_wmax[warp] = xm;
+    for (int i = tid; i < kWarps * 4; i += kThreads)
+        p1u[i] = -1;
+    __syncthreads();
+    const int nv = s_nv;
+    if (tid == 0) {
+        float m = 0.f;
+        for (int w = 0; w < kWarps; ++w)
+            m = fmaxf(m, s_wmax[w]);
+        s_sigx = f16_sigma(m);
+    }
+    // W2 rows of this CTA into shared memory
+    const int rowb = I / 2;
+    if (warp == 0) {
+        if (lane == 0)
+            tc::mbar_arrive_expect_tx(mbar, static_cast<uint32_t>(nv * nb * 8 * rowb));
+        __syncwarp();
+        for (int r = lane; r < nv * nb * 8; r += 32) {
+            const int j = r / (nb * 8), o = blk0 * 8 + (r - j * nb * 8);
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(a.q2) + (static_cast<int64_t>(r_e[j]) * d + o) * rowb;
+            tc::bulk_load(tc::smem_u32(w2s) + r * rowb, src, rowb, mbar);
+        }
+    }
+    __syncthreads();
+    const int sigx = s_sigx;
+    for (int i = tid; i < d; i += kThreads) {
+        const int src = (i & ~7) + interleave(i & 7);
+        const float v = a.x_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.x)[src])
+                                 : __half2float(reinterpret_cast<const __half *>(a.x)[src]);
+        xp[i] = __float2half_rn(ldexpf(v, sigx));
+    }
+    __syncthreads();
+    for (int g = warp; g < NG; g += kWarps) {
+        float v = 0.f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            v += __half2float(xp[g * 128 + t * 32 + lane]);
+        v = warp_sum(v);
+        if (lane == 0)
+            xsum[g] = v;
+    }
+    __syncthreads();
+
+    // ---- phase 1
+    const int T = nv * RB * NG;
+    const int c0 = split_lo(T, b, G), c1 = split_lo(T, b + 1, G);
+    {
+        const int n = c1 - c0;
+        const int i0 = c0 + split_lo(n, warp, kWarps), i1 = c0 + split_lo(n, warp + 1, kWarps);
+        const uint32_t *x32 = reinterpret_cast<const uint32_t *>(xp);
+        P1Ld ring[kPF];
+#pragma unroll
+        for (int s = 0; s < kPF; ++s)
+            if (i0 + s < i1)
+                p1_load(a, r_e, i0 + s, NG, lane, ring[s]);
+        float acc[2] = {0.f, 0.f};
+        int cur = i0 < i1 ? i0 / NG : -1, slot = 0;
+        for (int ib = i0; ib < i1; ib += kPF) {
+#pragma unroll
+            for (int s = 0; s < kPF; ++s) {
+                const int i = ib + s;
+                if (i < i1) {
+                    const int u = i / NG, g = i - u * NG;
+                    if (u != cur) {
+                        // at most 4 units per warp (the host's size check)
+                        if (gl == 0 && slot < 4) {
+                            p1v[(warp * 4 + slot) * 8 + 2 * q] = acc[0];
+                            p1v[(warp * 4 + slot) * 8 + 2 * q + 1] = acc[1];
+                        }
+                        if (lane == 0 && slot < 4)
+                            p1u[warp * 4 + slot] = cur;
+                        ++slot;
+                        cur = u;
+                        acc[0] = acc[1] = 0.f;
+                    }
+                    uint32_t bb[8][2];
+                    chunk_b(ring[s].c, bb);
+                    const float sv[2] = {ring[s].s[0], ring[s].s[1]};
+                    const uint32_t zw = ring[s].zw;
+                    if (i + kPF < i1)
+                        p1_load(a, r_e, i + kPF, NG, lane, ring[s]);
+                    const uint32_t *h32 = x32 + (g * 128 + 32 * q) / 2;
+                    float dd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        uint32_t aa[4];
+                        chunk_a(h32, t, aa);
+                        mma16816(dd, aa, bb[t][0], bb[t][1]);
+                    }
+                    fold(acc, dd, sv, zw, lane, xsum[g]);
+                }
+            }
+        }
+        if (cur >= 0 && slot < 4) {
+            if (gl == 0) {
+                p1v[(warp * 4 + slot) * 8 + 2 * q] = acc[0];
+                p1v[(warp * 4 + slot) * 8 + 2 * q + 1] = acc[1];
+            }
+            if (lane == 0)
+                p1u[warp * 4 + slot] = cur;
+        }
+        if (slot >= 4 && lane == 0)
+            set_err(a.dev_status, MOE_ERR_UNSUPPORTED);
+    }
+    __syncthreads();
+    // combine the warps' partials of each unit of this CTA (warp, slot order)
+    if (c1 > c0) {
+        const int u0 = c0 / NG, u1 = (c1 - 1) / NG;
+        const float unscale = ldexpf(1.0f, -sigx);
+        for (int t = tid; t < (u1 - u0 + 1) * 8; t += kThreads) {
+            const int u = u0 + t / 8, r = t % 8;
+            float v = 0.f;
+            for (int w = 0; w < kWarps * 4; ++w)
+                if (p1u[w] == u)
+                    v += p1v[w * 8 + r];
+            const int piece = b - owner(u * NG, T, G);
+            __stcg(a.gp + (static_cast<int64_t>(u) * kMaxPieces + piece) * 8 + r, v * unscale);
+        }
+    }
+    // phase-2 scales and zeros of this CTA's rows
+    for (int i = tid; i < nv * nb * 8 * G2; i += kThreads) {
+        const int r = i / G2, g = i - r * G2;
+        const int j = r / (nb * 8), o = blk0 * 8 + (r - j * nb * 8);
+        const int64_t e = r_e[j];
+        sc2[i] = f16bits(__ldg(reinterpret_cast<const unsigned short *>(a.s2) + (e * d + o) * G2 + g));
+        zz2[i] = nib(static_cast<uint32_t>(__ldg(a.z2 + (e * (d / 8) + o / 8) * G2 + g)), o & 7);
+    }
+
+    // ---- grid barrier: every piece is visible before any is read
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned long long GG = G, target = (s_epoch / GG + 1) * GG;
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(a.bar) : "memory");
+        const long long t0 = clock64(), limit = static_cast<long long>(kWaitNs) * 5 / 2;
+        int ok = 1;
+        unsigned long long v;
+        for (;;) {
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.bar) : "memory");
+            if (v >= target)
+                break;
+            if (clock64() - t0 > limit) {
+                ok = 0;
+                break;
+            }
+        }
+        s_ok = ok;
+        if (!ok)
+            set_err(a.dev_status, MOE_ERR_TIMEOUT);
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (!s_ok) {
+        if (!tc::mbar_wait(mbar, 0, &s_abort, kWaitNs))
+            set_err(a.dev_status, MOE_ERR_TIMEOUT);
+        return;
+    }
+
+    // ---- phase 2: h of every slot
+    for (int t = tid; t < nv * I; t += kThreads) {
+        const int j = t / I, n = t - j * I;
+        const int ug = j * RB + n / 8, uu = j * RB + (I + n) / 8, r = n % 8;
+        float gv = 0.f, uv = 0.f;
+        const int pg = owner(ug * NG + NG - 1, T, G) - owner(ug * NG, T, G) + 1;
+        const int pu = owner(uu * NG + NG - 1, T, G) - owner(uu * NG, T, G) + 1;
+        for (int p = 0; p < pg; ++p)
+            gv += __ldcg(a.gp + (static_cast<int64_t>(ug) * kMaxPieces + p) * 8 + r);
+        for (int p = 0; p < pu; ++p)
+            uv += __ldcg(a.gp + (static_cast<int64_t>(uu) * kMaxPieces + p) * 8 + r);
+        hf[t] = r_w[j] * silu_mul(gv, uv);
+    }
+    __syncthreads();
+    for (int j = warp; j < nv; j += kWarps) {
+        float m = 0.f;
+        for (int n = lane; n < I; n += 32)
+            m = fmaxf(m, fabsf(hf[j * I + n]));
+        m = warp_max(m);
+        if (lane == 0)
+            r_sig[j] = f16_sigma(m);
+    }
+    __syncthreads();
+    for (int t = tid; t < nv * I; t += kThreads) {
+        const int j = t / I, n = t - j * I;
+        const float v = ldexpf(hf[j * I + (n & ~7) + interleave(n & 7)], r_sig[j]);
+        const __half hi = __float2half_rn(v);
+        hp[t] = hi;
+        hp[nv * I + t] = __float2half_rn(v - __half2float(hi));
+    }
+    __syncthreads();
+    for (int t = warp; t < nv * G2; t += kWarps) {
+        float v = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int idx = t * 128 + c * 32 + lane;
+            v += __half2float(hp[idx]) + __half2float(hp[nv * I + idx]);
+        }
+        v = warp_sum(v);
+        if (lane == 0)
+            hsum[t] = v;
+    }
+    if (!tc::mbar_wait(mbar, 0, &s_abort, kWaitNs))
+        set_err(a.dev_status, MOE_ERR_TIMEOUT);
+    __syncthreads();
+    if (s_abort)
+        return;
+
+    // ---- phase 2: units (slot j, output block) over the warps
+    const uint32_t *h32 = reinterpret_cast<const uint32_t *>(hp);
+    const int rw = I / 8;
+    for (int v = warp; v < nv * nb; v += kWarps) {
+        const int j = v / nb, bl = v - j * nb;
+        const int rbase = j * nb * 8 + bl * 8;
+        float acc[2] = {0.f, 0.f};
+        for (int g = 0; g < G2; ++g) {
+            const uint4 c = *reinterpret_cast<const uint4 *>(w2s + static_cast<int64_t>(rbase + gl) * rw + g * 16 + q * 4);
+            uint32_t bb[8][2];
+            chunk_b(c, bb);
+            const uint32_t *hh = h32 + (j * I + g * 128 + 32 * q) / 2;
+            const uint32_t *hl = h32 + (nv * I + j * I + g * 128 + 32 * q) / 2;
+            float dd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                uint32_t aa[4];
+                chunk_a(hh, t, aa);
+                mma16816(dd, aa, bb[t][0], bb[t][1]);
+                chunk_a(hl, t, aa);
+                mma16816(dd, aa, bb[t][0], bb[t][1]);
+            }
+            const int r0 = rbase + 2 * q;
+            const float hs = hsum[j * G2 + g];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                acc[r] = fmaf(sc2[(r0 + r) * G2 + g], fmaf(-(1024.0f + zz2[(r0 + r) * G2 + g]), hs, dd[r]), acc[r]);
+        }
+        if (gl == 0) {
+            const float un = ldexpf(1.0f, -r_sig[j]);
+            part2[(j * nb + bl) * 8 + 2 * q] = acc[0] * un;
+            part2[(j * nb + bl) * 8 + 2 * q + 1] = acc[1] * un;
+        }
+    }
+    __syncthreads();
+    for (int t = tid; t < nb * 8; t += kThreads) {
+        float yo = 0.f;
+        for (int j = 0; j < nv; ++j)
+            yo += part2[(j * nb + t / 8) * 8 + t % 8];
+        const int o = blk0 * 8 + t;
+        if (a.y_f32)
+            reinterpret_cast<float *>(a.y)[o] = yo;
+        else
+            reinterpret_cast<__nv_bfloat16 *>(a.y)[o] = __float2bfloat16_rn(yo);
+    }
+}
+
+}  // namespace da1
+
+static int num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+// Whether the phase-1 item split of this grid keeps (a) every unit within
+// kMaxPieces CTAs and (b) every warp within 4 units.  CTAs own floor / ceil
+// of T / G consecutive items; with at least one item each, a unit of NG items
+// crosses at most ceil((NG - 1) / min) CTA boundaries.  With T < G some CTAs
+// own nothing, and the piece numbering (CTA index minus the unit's first CTA)
+// would leave gaps, so only single-item units (NG == 1) are allowed there.
+static bool split_fits(int nv, int d, int I, int G)
+{
+    const int NG = d / 128, T = nv * (2 * I / 8) * NG;
+    const int min_cta = T / G;
+    if (min_cta == 0)
+        return NG == 1;
+    if ((NG - 1 + min_cta - 1) / min_cta + 1 > da1::kMaxPieces)
+        return false;
+    const int max_cta = (T + G - 1) / G;
+    const int max_warp = (max_cta + da1::kWarps - 1) / da1::kWarps;
+    return (max_warp - 1 + NG - 1) / NG + 1 <= 4;
+}
+
+bool decode_awq_m1_eligible(int M, int k, int d, int I, int E)
+{
+    const int G = num_sms();
+    if (M != 1 || k < 1 || k > da1::kMaxK || E < 1 || d % 128 || d < 128 || I % 128 || I < 128 || G > 1024 ||
+        static_cast<int64_t>(k) * 2 * I / 8 * (d / 128) > INT32_MAX / 2)
+        return false;
+    const da1::Smem L{d, I, k, (d / 8 + G - 1) / G};
+    if (L.bytes() > 220 * 1024)
+        return false;
+    for (int nv = 1; nv <= k; ++nv)                  // any number of valid routes
+        if (!split_fits(nv, d, I, G))
+            return false;
+    return true;
+}
+
+size_t decode_awq_m1_workspace(int k, int I)
+{
+    return 256 + ws_round(static_cast<size_t>(k) * (2 * I / 8) * da1::kMaxPieces * 8 * sizeof(float));
+}
+
+moe_status_t decode_awq_m1_launch(const void *x, bool x_bf16, const int32_t *ids, const float *wts, int k, int d,
+                                  int I, int E, const void *q13, const void *s13, const void *z13, const void *q2,
+                                  const void *s2, const void *z2, void *y, bool y_f32, void *ws,
+                                  int32_t *dev_status, cudaStream_t stream)
+{
+    const int G = num_sms();
+    if (!decode_awq_m1_eligible(1, k, d, I, E) || !aligned(q13, 16) || !aligned(q2, 16) || !aligned(ws, 256))
+        return MOE_ERR_UNSUPPORTED;
+    const da1::Smem L{d, I, k, (d / 8 + G - 1) / G};
+    const int smem = L.bytes();
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    const da1::Args a{x, ids, wts, static_cast<const uint32_t *>(q13), static_cast<const uint16_t *>(s13),
+                      static_cast<const int32_t *>(z13), static_cast<const uint32_t *>(q2),
+                      static_cast<const uint16_t *>(s2), static_cast<const int32_t *>(z2),
+                      reinterpret_cast<unsigned long long *>(w), reinterpret_cast<float *>(w + 256), y, dev_status,
+                      x_bf16 ? 1 : 0, y_f32 ? 1 : 0, k, d, I, E};
+    static std::atomic<uint64_t> attr_done{0};
+    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(da1::awq_m1_kernel), smem))
+        return MOE_ERR_CUDA;
+    return launch_pdl(da1::awq_m1_kernel, dim3(G), dim3(da1::kThreads), static_cast<size_t>(smem), stream, a) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

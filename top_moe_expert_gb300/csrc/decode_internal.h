@@ -1,5 +1,6 @@
-// decode_internal.h -- entry of the streaming MXFP8 decode kernels
-// (decode_stream.cu), called by moe_ffn_decode when the shape qualifies.
+// decode_internal.h -- entries of the specialised decode kernels
+// (decode_stream.cu, decode_fused.cu, decode_m1.cu, decode_awq_m1.cu), called
+// by moe_ffn_decode when the shape qualifies.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -33,5 +34,14 @@ moe_status_t decode_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const
                               const float *logits, int32_t *ids_out, float *wts_out, int k, const uint8_t *q13,
                               const uint8_t *s13, const uint8_t *q2t, const uint8_t *s2t, void *y, bool y_f32,
                               void *ws, int32_t *dev_status, cudaStream_t stream);
+
+// single-token 4-bit AWQ layer in one kernel (decode_awq_m1.cu); ws holds the
+// grid-barrier counter in its first 8 bytes (zero before the first use)
+bool decode_awq_m1_eligible(int M, int k, int d, int I, int E);
+size_t decode_awq_m1_workspace(int k, int I);
+moe_status_t decode_awq_m1_launch(const void *x, bool x_bf16, const int32_t *ids, const float *wts, int k, int d,
+                                  int I, int E, const void *q13, const void *s13, const void *z13, const void *q2,
+                                  const void *s2, const void *z2, void *y, bool y_f32, void *ws,
+                                  int32_t *dev_status, cudaStream_t stream);
 
 }  // namespace moe
