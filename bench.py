@@ -182,9 +182,10 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 SRC_FILES = {
     "decode": ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "decode_internal.h", "topk.cu",
-               "topk.cuh", "common.cuh", "tc.cuh"),
-    "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh"),
-    "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh"),
+               "topk.cuh", "common.cuh", "tc.cuh", "attr.h"),
+    "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh",
+                "attr.h"),
+    "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
     "awq_decode": ("decode.cu", "decode_awq_m1.cu", "decode_awq_m1.cuh", "decode_internal.h", "common.cuh",
                    "tc.cuh", "attr.h"),
 }

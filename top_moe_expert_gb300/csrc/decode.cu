@@ -19,6 +19,7 @@
 // waits for the gate/up grid, so the W2 stream overlaps the gate/up tail.
 // Per-output summation order depends only on (d, I, k) and the lane layout,
 // never on M, on other tokens or on the grid, so results are bit-stable.
+#include "attr.h"
 #include "common.cuh"
 #include "decode_internal.h"
 
@@ -299,8 +300,7 @@ moe_status_t decode_launch(const void *x, int M, int d, const int32_t *ids, cons
         return MOE_ERR_CUDA;
     const size_t smem = static_cast<size_t>(k) * I * sizeof(float);
     auto kd = decode_down_kernel<FMT, YT>;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    if (smem > 48 * 1024 && !smem_attr(reinterpret_cast<const void *>(kd), 200 * 1024))
         return MOE_ERR_CUDA;
     dim3 g2((d + kDecWarps - 1) / kDecWarps, M);
     if (launch_pdl(kd, g2, dim3(kDecWarps * 32), smem, s, static_cast<const float *>(h), d, I, ids, wts,

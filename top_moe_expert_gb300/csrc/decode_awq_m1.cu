@@ -395,19 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) awq_m1_kernel(const Args a)
 
 }  // namespace da1
 
-static int num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 // Whether the phase-1 item split of this grid keeps (a) every unit within
 // kMaxPieces CTAs and (b) every warp within 4 units.  CTAs own floor / ceil
 // of T / G consecutive items; with at least one item each, a unit of NG items
@@ -429,7 +416,7 @@ static bool split_fits(int nv, int d, int I, int G)
 
 bool decode_awq_m1_eligible(int M, int k, int d, int I, int E)
 {
-    const int G = num_sms();
+    const int G = device_sm_count();
     if (M != 1 || k < 1 || k > da1::kMaxK || E < 1 || d % 128 || d < 128 || I % 128 || I < 128 || G > 1024 ||
         static_cast<int64_t>(k) * 2 * I / 8 * (d / 128) > INT32_MAX / 2)
         return false;
@@ -452,7 +439,7 @@ moe_status_t decode_awq_m1_launch(const void *x, bool x_bf16, const int32_t *ids
                                   const void *s2, const void *z2, void *y, bool y_f32, void *ws,
                                   int32_t *dev_status, cudaStream_t stream)
 {
-    const int G = num_sms();
+    const int G = device_sm_count();
     if (!decode_awq_m1_eligible(1, k, d, I, E) || !aligned(q13, 16) || !aligned(q2, 16) || !aligned(ws, 256))
         return MOE_ERR_UNSUPPORTED;
     const da1::Smem L{d, I, k, (d / 8 + G - 1) / G};
@@ -464,7 +451,7 @@ moe_status_t decode_awq_m1_launch(const void *x, bool x_bf16, const int32_t *ids
                       reinterpret_cast<unsigned long long *>(w), reinterpret_cast<float *>(w + 256), y, dev_status,
                       x_bf16 ? 1 : 0, y_f32 ? 1 : 0, k, d, I, E};
     static std::atomic<uint64_t> attr_done{0};
-    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(da1::awq_m1_kernel), smem))
+    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(da1::awq_m1_kernel), 220 * 1024))
         return MOE_ERR_CUDA;
     return launch_pdl(da1::awq_m1_kernel, dim3(G), dim3(da1::kThreads), static_cast<size_t>(smem), stream, a) ==
                    cudaSuccess

@@ -26,6 +26,7 @@
 // rescale, so the inner product uses the mixed-precision fma.rn.f32.f16
 // (FP32 accumulate); the rescale is exact for every element within 2^28 of
 // the token's largest magnitude (bf16 carries 8 significant bits).
+#include "attr.h"
 #include "common.cuh"
 #include "decode_internal.h"
 #include "tc.cuh"
@@ -790,22 +791,9 @@ __global__ void __launch_bounds__(256) reduce_kernel(const float *__restrict__ p
 
 // ---------------------------------------------------------------- host side
 
-static int fused_num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 size_t decode_fused_workspace(int M, int d)
 {
-    return ws_round(static_cast<size_t>(fused_num_sms()) * M * d * sizeof(float));
+    return ws_round(static_cast<size_t>(device_sm_count()) * M * d * sizeof(float));
 }
 
 bool decode_fused_eligible(int M, int k, int d, int I, int E)
@@ -819,7 +807,7 @@ moe_status_t decode_fused_launch(const __nv_bfloat16 *x, int M, int d, int I, in
                                  int32_t *dev_status, cudaStream_t stream)
 {
     using namespace df;
-    const int G = fused_num_sms();
+    const int G = device_sm_count();
     const int MK = M * k;
     // neurons per stage: as many as keep three stages within ~150 KB (at most
     // one per dot warp); wpn = 8 / R dot warps per neuron split its rows
@@ -841,7 +829,7 @@ moe_status_t decode_fused_launch(const __nv_bfloat16 *x, int M, int d, int I, in
         return MOE_ERR_UNSUPPORTED;
     Args a{x, ids, wts, q13, s13, q2t, s2t, partial, dev_status, M, k, d, I, E, R, stages};
     auto pick = [&](auto kern) -> moe_status_t {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+        if (!smem_attr(reinterpret_cast<const void *>(kern), 220 * 1024))
             return MOE_ERR_CUDA;
         return launch_pdl(kern, dim3(G), dim3(kThreads), smem, stream, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     };

@@ -34,6 +34,7 @@
 //     the next multiple of the grid size above a (the counter starts at 0).
 // The CTAs of the grid must be resident together: the grid is one CTA per SM
 // and the kernel lets dependent launches start only after the barrier.
+#include "attr.h"
 #include "common.cuh"
 #include "decode_internal.h"
 #include "tc.cuh"
@@ -585,30 +586,17 @@ __global__ void __launch_bounds__(kThreads, 1) m1_kernel(const Args a)
 
 }  // namespace dm
 
-static int m1_num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 bool decode_m1_eligible(int M, int k, int d, int I, int E)
 {
     // (route, neuron) indices times the grid stay within 32 bits; the final
     // reduction takes at most 8 partial rows per lane (grid <= 256)
-    return m1_num_sms() <= 256 && M == 1 && k >= 1 && k <= dm::kMaxK && (d == 1024 || d == 2048) && I % 32 == 0 && I >= 32 &&
+    return device_sm_count() <= 256 && M == 1 && k >= 1 && k <= dm::kMaxK && (d == 1024 || d == 2048) && I % 32 == 0 && I >= 32 &&
            I <= 65536 && E >= 1;
 }
 
 size_t decode_m1_workspace(int d)
 {
-    return 256 + ws_round(static_cast<size_t>(m1_num_sms()) * d * sizeof(float));
+    return 256 + ws_round(static_cast<size_t>(device_sm_count()) * d * sizeof(float));
 }
 
 bool decode_m1_route_eligible(int E, int k)
@@ -622,7 +610,7 @@ moe_status_t decode_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const
                               void *ws, int32_t *dev_status, cudaStream_t stream)
 {
     using namespace dm;
-    const int G = m1_num_sms();
+    const int G = device_sm_count();
     const Geo geo{d};
     const size_t smem = static_cast<size_t>(kStages) * geo.bytes() + 4 * kR * sizeof(float) +
                         2 * kStages * sizeof(uint64_t) + 2 * kMaxK * sizeof(int) + 4 * sizeof(int);
@@ -632,8 +620,7 @@ moe_status_t decode_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const
     Args a{x,  ids, wts, logits, ids_out, wts_out, q13, s13, q2t, s2t, reinterpret_cast<unsigned long long *>(w),
            reinterpret_cast<float *>(w + 256), y, dev_status, y_f32 ? 1 : 0, k, d, I, E};
     auto go = [&](auto kern) -> moe_status_t {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess)
+        if (!smem_attr(reinterpret_cast<const void *>(kern), 220 * 1024))
             return MOE_ERR_CUDA;
         return launch_pdl(kern, dim3(G), dim3(kThreads), smem, stream, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     };

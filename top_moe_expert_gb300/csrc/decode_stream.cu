@@ -25,6 +25,7 @@
 // Summation order per output is fixed by (d, I) and the lane layout only, so
 // the result for a token does not depend on M, on the other tokens, or on the
 // grid size.
+#include "attr.h"
 #include "common.cuh"
 #include "decode_internal.h"
 #include "tc.cuh"
@@ -558,19 +559,6 @@ bool decode_stream_eligible(int M, int k, int d, int I, int E, const void *q13, 
            aligned(q13, 16) && aligned(s13, 16) && aligned(q2, 16) && aligned(s2, 16);
 }
 
-static int num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 moe_status_t decode_stream_launch(const __nv_bfloat16 *x, int M, int d, int I, int E, const int32_t *ids,
                                   const float *wts, int k, const uint8_t *q13, const uint8_t *s13,
                                   const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32, float *h,
@@ -578,7 +566,7 @@ moe_status_t decode_stream_launch(const __nv_bfloat16 *x, int M, int d, int I, i
 {
     using namespace ds;
     const int MK = M * k;
-    const int G = num_sms();
+    const int G = device_sm_count();
     // ---- kernel A
     const size_t stage_a = 2 * kRowsA * (d + d / 32);
     int stages_a = static_cast<int>((128 * 1024) / stage_a);
@@ -611,8 +599,8 @@ moe_status_t decode_stream_launch(const __nv_bfloat16 *x, int M, int d, int I, i
     auto ka = (M == 1 && d == 2048) ? gate_up_kernel<4>
             : (M == 1 && d == 1024) ? gate_up_kernel<2>
             : (M == 1 && d == 512) ? gate_up_kernel<1> : gate_up_kernel<0>;
-    if (cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_a)) != cudaSuccess ||
-        cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_b)) != cudaSuccess)
+    if (!smem_attr(reinterpret_cast<const void *>(ka), 200 * 1024) ||
+        !smem_attr(reinterpret_cast<const void *>(down_kernel), 200 * 1024))
         return MOE_ERR_CUDA;
     if (launch_pdl(ka, dim3(G), dim3(kThreads), smem_a, stream, aa) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -588,19 +588,6 @@ static bool tmap_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t r
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int sm_count()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 struct WsLayout {
     size_t xq, xs, hq, hs, yr, done, total;
 };
@@ -645,7 +632,7 @@ bool grouped_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, int elem_bytes, con
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int grouped_sm_count() { return gg::sm_count(); }
+int grouped_sm_count() { return device_sm_count(); }
 
 moe_status_t grouped_combine_launch(const float *yr, const int32_t *ids, int M, int k, int d, int E, void *y,
                                     bool y_f32, cudaStream_t s)
@@ -780,7 +767,7 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         !tmap_u8(&tB2, hq, I, cap_rows, n_mma))
         return MOE_ERR_CUDA;
 
-    if (launch_pdl(act_quant_kernel, dim3(sm_count() * 4), dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(x), d,
+    if (launch_pdl(act_quant_kernel, dim3(device_sm_count() * 4), dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(x), d,
                    k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs, done) != cudaSuccess)
         return MOE_ERR_CUDA;
 
@@ -794,7 +781,7 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
     if (stages < 2 || smem > 227 * 1024 ||
         !smem_attr_once(attr_done, reinterpret_cast<const void *>(gemm_kernel), 227 * 1024))
         return MOE_ERR_CUDA;
-    const int grid = sm_count();
+    const int grid = device_sm_count();
 
     Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
             hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I, stages};
