@@ -222,3 +222,32 @@ def test_grouped_workspace_reused_across_shapes():
             torch.cuda.synchronize()
             assert st.tolist() == [0, 0]
             assert torch.equal(y, fresh)
+
+
+@pytest.mark.parametrize("M", [8, 64])
+def test_accuracy_decode_path_closer_to_exact_than_grouped(M):
+    """The accuracy comparison of "Warp decode" (section on higher accuracy),
+    on this layer: both paths against the exact oracle (binary64, activations
+    and h unquantized) on the same inputs and routing.  The grouped path
+    quantizes x and h to MXFP8 before its block-scaled MMAs; the decode path
+    keeps them in FP32.  The errors and their ratio are printed (pytest -s)
+    and the decode path must be the closer one."""
+    wl = inputs.sweep(M)
+    b = 16
+    layer, sfa13, sfa2, x, ids, w = _setup(wl, b)
+    y_dec = moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), layer.w13,
+                               layer.w2, out_dtype=torch.float32)
+    y_grp, _, _ = _run(layer, sfa13, sfa2, x, ids, w, b)
+    w13, w2 = layer.oracle_weights(np.unique(ids))
+    ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, w13, w2)["y"]
+    scale = np.abs(ref).max()
+    rms = np.sqrt((ref * ref).mean())
+    out = {}
+    for name, y in (("decode", y_dec), ("grouped", y_grp)):
+        e = y.double().cpu().numpy() - ref
+        out[name] = (np.abs(e).max() / scale, np.sqrt((e * e).mean()) / rms)
+    print(f"accuracy M={M}: decode max {out['decode'][0]:.3e} rms {out['decode'][1]:.3e}; "
+          f"grouped max {out['grouped'][0]:.3e} rms {out['grouped'][1]:.3e}; "
+          f"ratio (rms) {out['grouped'][1] / max(out['decode'][1], 1e-300):.1f}")
+    gs.assert_layer_close(y_dec, ref)
+    assert out["decode"][1] < out["grouped"][1]
