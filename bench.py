@@ -185,7 +185,8 @@ SRC_FILES = {
                "topk.cuh", "common.cuh", "tc.cuh", "attr.h"),
     "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh",
                 "attr.h"),
-    "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
+    "awq": ("grouped_awq.cu", "grouped_awq_mma.cu", "grouped_awq_mma.cuh", "decode_awq_m1.cuh", "grouped.cu",
+            "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
     "awq_decode": ("decode.cu", "decode_awq_m1.cu", "decode_awq_m1.cuh", "decode_internal.h", "common.cuh",
                    "tc.cuh", "attr.h"),
 }
@@ -362,6 +363,9 @@ class DecodeStep:
         self.launch_layer(stream)
 
     def layer_kernels(self) -> str:
+        if self.awq and self.path == "grouped" and self.b <= 16:
+            return ("moe_ffn_grouped (AWQ-4bit, b <= 16): gsm::awq_mma_kernel (both GEMMs on mma.sync over the raw "
+                    "codes, one kernel) + combine")
         if self.awq and self.path == "grouped":
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
         if self.awq and self.wl.M == 1:
@@ -380,7 +384,10 @@ class DecodeStep:
         if self.path == "grouped":
             # (top-k), alignment, act-quant or gather, the GEMM kernel, combine
             na = 2 if self.ws_align is not None else 1
-            return na + 3 if self.awq else 1 + na + 3
+            if self.awq:
+                # the b <= 16 AWQ path: one kernel for both GEMMs, then the combine
+                return na + (2 if self.b <= 16 else 3)
+            return 1 + na + 3
         if self.awq:
             # fixed routing: the single-token kernel, or the two decode kernels
             return 1 if self.wl.M == 1 else 2
@@ -582,7 +589,10 @@ def run_ours(args, rank, world, device):
                  "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
                  "N(0,1) router logits; fresh routing every step)"),
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "path": ("expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
+                   "path": ("expert-centric grouped AWQ, blocks of at most 16 rows (align + one kernel for both "
+                            "GEMMs on mma.sync over the raw 4-bit codes, zero folded out in FP32 + combine, b=%d)"
+                            % st.b if st.awq and st.path == "grouped" and st.b <= 16 else
+                            "expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
                             "dequantized into tensor memory + combine, b=%d)" % st.b
                             if st.awq and st.path == "grouped" else
                             ("single-token AWQ decode: gate/up + SwiGLU + down in one kernel, f16 mma.sync dot "

@@ -258,6 +258,19 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
  *   Extra limits: b <= 128, d % 256 == 0, d / 128 <= 64, I / 128 <= 64,
  *   and b <= 112 when d > 8064 (MOE_ERR_UNSUPPORTED); scale and zero arrays
  *   16-byte aligned (MOE_ERR_INVALID_ARG).
+ *   Blocks of b <= 16 rows take a different kernel when its shared-memory
+ *   plan fits (d and I up to about 3.5K): each block is one M-tile of
+ *   mma.sync m16n8k16 (f16 x f16, FP32 accumulate) whose B operand is the raw
+ *   4-bit codes as f16 (1024 + q); the zero, the offset and the scale are
+ *   applied in FP32 once per group of 128, x and h enter as f16 after an
+ *   exact per-row power-of-two rescale (h as an f16 hi + lo pair), so no
+ *   value is rounded to fp16 beyond that split.  Its ws is
+ *   [D | GU | Yr], each part rounded up to 256 bytes:
+ *     D  int32 [cap_rows/b]     gate/up units finished per block (zeroed by
+ *                               the call itself)
+ *     GU f32 [M*k][2I]          gate and up values per route
+ *     Yr f32 [M*k][d]           w_route * (W2 h) per route
+ *   and d % 256 need not hold.
  * Limits: d % 128 == 0, I % 128 == 0, M * d / 4 <= INT32_MAX
  * (MOE_ERR_UNSUPPORTED otherwise); x and y 16-byte aligned
  * (MOE_ERR_INVALID_ARG otherwise). */

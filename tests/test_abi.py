@@ -74,9 +74,10 @@ def _r256(n):
 @pytest.mark.parametrize("M,k,d,I,b", [(21, 8, 2048, 768, 8), (64, 8, 2048, 768, 16), (512, 8, 2048, 768, 64),
                                        (8, 8, 7168, 2048, 16), (3, 4, 1024, 256, 136)])
 def test_grouped_workspace_size_matches_documented_layout(M, k, d, I, b):
-    """moe_ffn_grouped_workspace_size is the larger of the two documented
-    layouts: MXFP8 [Xq | Xs | Hq | Hs | Yr | D] and AWQ [Xg | Hg | Yr | D], each
-    part rounded up to 256 bytes."""
+    """moe_ffn_grouped_workspace_size is the largest of the documented
+    layouts: MXFP8 [Xq | Xs | Hq | Hs | Yr | D], AWQ [Xg | Hg | Yr | D] and, for
+    b <= 16, the AWQ mma.sync layout [D | GU | Yr], each part rounded up to 256
+    bytes."""
     cap_rows = moe.moe_align_capacity(M, k, 128, b)[0]
     cap_blocks = cap_rows // b
     n_mma = (b + 15) // 16 * 16
@@ -84,7 +85,8 @@ def test_grouped_workspace_size_matches_documented_layout(M, k, d, I, b):
     mx = (_r256(cap_rows * d) + _r256(cap_blocks * (d // 128) * nsf * 512) + _r256(cap_rows * I)
           + _r256(cap_blocks * (I // 128) * nsf * 512) + _r256(M * k * d * 4) + _r256(cap_blocks * 4))
     awq = _r256(cap_rows * d * 2) + _r256(cap_rows * I * 2) + _r256(M * k * d * 4) + _r256(cap_blocks * 4)
-    assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(mx, awq)
+    small = _r256(cap_blocks * 4) + _r256(M * k * 2 * I * 4) + _r256(M * k * d * 4) if b <= 16 else 0
+    assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(mx, awq, small)
 
 
 def test_host_validation_rejects_before_launch(L):

@@ -69,11 +69,16 @@ def test_awq_grouped_repeats_bit_identical(fixture_a):
 
 
 def test_awq_grouped_independent_of_block_size(fixture_a):
-    wl, layer, x, ids, w, _ = fixture_a
+    """Each path's per-route results do not depend on the block size: blocks
+    of up to 16 rows take the mma.sync kernel, larger ones the tcgen05 one."""
+    wl, layer, x, ids, w, ref = fixture_a
     y8, _ = _run(layer, x, ids, w, 8)
     y16, _ = _run(layer, x, ids, w, 16)
     y32, _ = _run(layer, x, ids, w, 32)
-    assert torch.equal(y8, y16) and torch.equal(y8, y32)
+    y64, _ = _run(layer, x, ids, w, 64)
+    assert torch.equal(y8, y16) and torch.equal(y32, y64)
+    gs.assert_layer_close(y8, ref)
+    gs.assert_layer_close(y32, ref)
 
 
 @pytest.mark.parametrize("xdt,b", [(torch.float16, 16), (torch.bfloat16, 8), (torch.float16, 64)])
@@ -88,10 +93,22 @@ def test_awq_grouped_small(xdt, b):
     gs.assert_layer_close(y, ref)
 
 
-@pytest.mark.parametrize("d,b", [(1024, 136), (1152, 16)])
+def test_awq_grouped_small_blocks_any_multiple_of_128():
+    """The b <= 16 path takes d and I that are multiples of 128 but not 256."""
+    wl = inputs.Workload("awq_grouped_1152", M=9, d=1152, I=384, E=8, k=3, fmt="awq4", seed=4)
+    layer = gs.AwqLayer(wl)
+    x = inputs.activations(wl, dtype=torch.float16)
+    ids, w = gs.routing(wl)
+    y, _ = _run(layer, x, ids, w, 16)
+    ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, layer.host13, layer.host2)["y"]
+    gs.assert_layer_close(y, ref)
+
+
+@pytest.mark.parametrize("d,b", [(1024, 136), (1152, 32)])
 def test_awq_grouped_limits_rejected(d, b):
-    """Blocks above 128 rows and d not a multiple of 256 are refused on the
-    host with MOE_ERR_UNSUPPORTED (before anything is launched)."""
+    """Blocks above 128 rows, and d not a multiple of 256 on the tcgen05 path
+    (blocks above 16 rows), are refused on the host with MOE_ERR_UNSUPPORTED
+    (before anything is launched)."""
     wl = inputs.Workload("awq_grouped_limits", M=8, d=d, I=256, E=16, k=4, fmt="awq4", seed=9)
     layer = gs.AwqLayer(wl)
     x = inputs.activations(wl, dtype=torch.float16)
