@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0)
         s_abort = 0;
-    const int nblk = __ldg(a.npp) / b;
+    const int nblk = min(max(__ldg(a.npp), 0) / b, a.cap_blocks);
 
     // ---------------------------------------------------------------- phase 1
     {
@@ -121,9 +121,12 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
             const int blk = u / RB1, seg_end = min(c1, (blk + 1) * RB1);
             __syncthreads();                                   // the previous block's operand is no longer read
             // the block's rows: route, scale exponent, x in f16 (MMA order), group sums
+            const int e_raw = __ldg(a.expert_ids + blk);
+            const bool e_ok = e_raw >= 0 && e_raw < a.E;           // a block of an invalid expert writes nothing
+            const int e = e_ok ? e_raw : 0;
             if (tid < kRows) {
                 const int route = tid < b ? __ldg(a.sorted + static_cast<int64_t>(blk) * b + tid) : a.mk;
-                r_route[tid] = route >= 0 && route < a.mk ? route : -1;
+                r_route[tid] = e_ok && route >= 0 && route < a.mk ? route : -1;
             }
             __syncthreads();
             for (int r = warp; r < kRows; r += kWarps) {
@@ -154,10 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
                         sums[r * NG1 + g] = v;
                 }
             }
-            const int e_raw = __ldg(a.expert_ids + blk);
-            const int e = e_raw >= 0 && e_raw < a.E ? e_raw : 0;     // an invalid block writes nothing
-            if (e != e_raw && tid < kRows)
-                r_route[tid] = -1;
             __syncthreads();
             // the warps split the block's units [u, seg_end); items (unit, group)
             const int n = seg_end - u;
@@ -239,9 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
                     }
                 }
             }
+            const int e_raw = __ldg(a.expert_ids + blk);
+            const bool e_ok = e_raw >= 0 && e_raw < a.E;
+            const int e = e_ok ? e_raw : 0;
             if (tid < kRows) {
                 const int route = tid < b ? __ldg(a.sorted + static_cast<int64_t>(blk) * b + tid) : a.mk;
-                r_route[tid] = route >= 0 && route < a.mk ? route : -1;
+                r_route[tid] = e_ok && route >= 0 && route < a.mk ? route : -1;
             }
             __syncthreads();
             if (s_abort)
@@ -283,10 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
                         sums[r * NG2 + g] = v;
                 }
             }
-            const int e_raw = __ldg(a.expert_ids + blk);
-            const int e = e_raw >= 0 && e_raw < a.E ? e_raw : 0;
-            if (e != e_raw && tid < kRows)
-                r_route[tid] = -1;
             __syncthreads();
             const int n = seg_end - u;
             const int v0 = u + n * warp / kWarps, v1 = u + n * (warp + 1) / kWarps;
@@ -376,7 +374,7 @@ moe_status_t grouped_awq_mma_launch(const void *x, bool x_bf16, int M, int d, in
                       static_cast<const uint16_t *>(w13->scale), static_cast<const int32_t *>(w13->zero),
                       static_cast<const uint32_t *>(w2->q), static_cast<const uint16_t *>(w2->scale),
                       static_cast<const int32_t *>(w2->zero), done, gu, yr, dev_status, x_bf16 ? 1 : 0,
-                      M, k, d, I, E, b, static_cast<int>(mk)};
+                      M, k, d, I, E, b, static_cast<int>(mk), cap_rows / b};
     if (launch_pdl(gsm::awq_mma_kernel, dim3(device_sm_count()), dim3(gsm::kThreads),
                    static_cast<size_t>(L.bytes()), s, a) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -40,6 +40,7 @@ struct Args {
     int32_t *dev_status;
     int x_bf16;
     int M, k, d, I, E, b, mk;
+    int cap_blocks;                       // entries of expert_ids / done: the blocks read are clamped to it
 };
 
 // Shared memory: the A operand of one block (rows padded by 16 bytes so
