@@ -181,8 +181,9 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 
 SRC_FILES = {
-    "decode": ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "decode_internal.h", "topk.cu",
-               "topk.cuh", "common.cuh", "tc.cuh", "attr.h"),
+    "decode": ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "decode_mx_m1.cu",
+               "decode_mx_m1.cuh", "decode_awq_m1.cuh", "decode_internal.h", "topk.cu", "topk.cuh", "common.cuh",
+               "tc.cuh", "attr.h"),
     "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh",
                 "attr.h"),
     "awq": ("grouped_awq.cu", "grouped_awq_mma.cu", "grouped_awq_mma.cuh", "decode_awq_m1.cuh", "grouped.cu",
@@ -218,11 +219,12 @@ class DecodeStep:
     """Device-resident workload + a CUDA graph of one step: top-k routing and
     the layer (decode path), or top-k, alignment and the grouped layer."""
 
-    def __init__(self, wl, nsteps: int, device, path: str = "decode", block: int = 0):
+    def __init__(self, wl, nsteps: int, device, path: str = "decode", block: int = 0, w2_layout: str = "auto"):
         import top_moe_expert_gb300 as moe
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
         self.routed_in_layer = False
+        self.w2_standard = w2_layout == "standard"
         self.awq = wl.fmt == "awq4"
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
         if self.awq:
@@ -244,9 +246,12 @@ class DecodeStep:
         else:
             # small batches take the single-pass kernel, which reads the down
             # projection neuron-major: pack it once (same bytes, K-outer order)
-            self.fused = M <= 4 and d % 1024 == 0
+            self.fused = M <= 4 and d % 1024 == 0 and not self.w2_standard
             # one token on that layout: routing runs inside the layer's kernel
             self.routed_in_layer = self.fused and M == 1 and d in (1024, 2048) and E <= 512
+            if self.w2_standard and M == 1 and E <= 512:
+                # one token on the standard layout: the single-kernel path, routing inside
+                self.routed_in_layer = True
             if self.fused:
                 self.w2 = moe.moe_mxfp8_transpose(self.w2)
                 del self.q2, self.s2
@@ -374,6 +379,9 @@ class DecodeStep:
             return "moe_ffn_decode (AWQ-4bit): decode_gate_up_kernel<AWQ> + decode_down_kernel<AWQ>"
         if self.path == "grouped":
             return "moe_ffn_grouped: act_quant + gemm_kernel (both GEMMs, one persistent kernel) + combine"
+        if self.routed_in_layer and self.w2_standard:
+            return ("moe_ffn_decode_logits (standard W2 layout): dx1::mx_m1_kernel (top-k routing + gate/up on "
+                    "mma.sync + SwiGLU + down), one kernel")
         if self.routed_in_layer:
             return "moe_ffn_decode_logits: dm::m1_kernel (top-k routing + gate/up + SwiGLU + down + combine), one kernel"
         if self.fused:
@@ -427,7 +435,8 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     t_mma = flops / (peak_tf * 1e12)
     kern = st.layer_kernels()
     src = ("awq" if st.path == "grouped" else "awq_decode") if st.awq else st.path
-    traffic = committed_traffic(f"{st.path}:{wl.name}", decode_src_hash(src))
+    key = f"{st.path}{'-w2std' if getattr(st, 'w2_standard', False) else ''}:{wl.name}"
+    traffic = committed_traffic(key, decode_src_hash(src))
     if t_mma > t_hbm:
         ach = flops / sec / 1e12 / world
         return {"kernel": kern, "bound": "tensor", "achieved": round(ach, 1), "peak": peak_tf,
@@ -464,7 +473,7 @@ def run_ours(args, rank, world, device):
     # measured crossover at d=2048, I=768, E=128, k=8: the output-centric path
     # wins for a single token, the grouped path from M = 4 on
     path = args.path if args.path != "auto" else ("decode" if wl.M <= 2 else "grouped")
-    st = DecodeStep(wl, K + W, device, path, args.block)
+    st = DecodeStep(wl, K + W, device, path, args.block, args.w2)
     st.capture()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     s = st.stream
@@ -600,6 +609,8 @@ def run_ours(args, rank, world, device):
                             "output-centric AWQ decode (gate/up + down on CUDA cores, fixed routing)" if st.awq else
                             "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
                             % st.b if st.path == "grouped" else
+                            ("single-token decode on the standard W2 layout: routing + gate/up + SwiGLU + down "
+                             "in one kernel (mma.sync dot products)") if st.routed_in_layer and st.w2_standard else
                             "single-token decode: routing + gate/up + SwiGLU + down + combine in one kernel"
                             if st.routed_in_layer else
                             "single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
@@ -805,6 +816,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "grouped"])
     ap.add_argument("--block", type=int, default=0, help="MoE block size b of the grouped path (0: automatic)")
+    ap.add_argument("--w2", default="auto", choices=["auto", "standard"],
+                    help="decode path: keep W2 K-contiguous (standard) instead of the neuron-major packing "
+                         "small batches use by default")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

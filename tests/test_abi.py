@@ -59,7 +59,10 @@ def test_align_capacity_bound():
 def test_decode_workspace_size():
     # h [M*k][I] f32 (the two-kernel paths); d % 1024 != 0 rules out the
     # single-pass path and its per-SM partial outputs
-    assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 8 * 768 * 4
+    assert moe.moe_ffn_decode_workspace_size(2, 8, 512, 768) == 2 * 8 * 768 * 4
+    # one token: the single-kernel MXFP8 path's barrier counter (256 B) and
+    # phase-1 pieces [k * 2I / 8][4][8] f32
+    assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 256 + 8 * (2 * 768 // 8) * 4 * 8 * 4
     assert moe.moe_ffn_decode_workspace_size(3, 8, 512, 100) % 256 == 0
     assert moe.moe_ffn_decode_workspace_size(64, 8, 2048, 768) == 64 * 8 * 768 * 4
     # one token, d % 1024 == 0: at least the single-token AWQ kernel's barrier

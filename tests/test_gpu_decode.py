@@ -86,10 +86,14 @@ def test_decode_is_bit_reproducible_and_independent_of_batch():
     ys = [run_decode(layer, x, ids, w, torch.float32) for _ in range(5)]
     digests = {hashlib.sha256(y.cpu().numpy().tobytes()).hexdigest() for y in ys}
     assert len(digests) == 1
-    # a token computed alone gives the same bits as inside the batch
-    for t in (0, 7, 15):
+    # tokens computed in a smaller batch give the same bits as inside the
+    # batch (a single token takes the one-kernel path, checked against the
+    # oracle instead)
+    for t in (0, 7, 14):
+        y2 = run_decode(layer, x[t:t + 2], ids[t:t + 2], w[t:t + 2], torch.float32)
+        assert torch.equal(y2, ys[0][t:t + 2])
         y1 = run_decode(layer, x[t:t + 1], ids[t:t + 1], w[t:t + 1], torch.float32)
-        assert torch.equal(y1[0], ys[0][t])
+        gs.assert_layer_close(y1, oracle_decode(layer, x[t:t + 1], ids[t:t + 1], w[t:t + 1]))
 
 
 def test_decode_invalid_routes_counted_and_skipped():
@@ -142,6 +146,41 @@ def test_awq_decode_fixture_shape():
                            layer.w13, layer.w2, out_dtype=torch.float32)
     ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, layer.host13, layer.host2)["y"]
     gs.assert_layer_close(y, ref)
+
+
+# ---- one token, MXFP8 on the standard layout: the single-kernel path
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_mx_single_token_standard_layout(out_dtype):
+    wl = inputs.DECODE
+    layer = mx_layer(wl)
+    for step in range(2):
+        x = inputs.activations(wl, step)
+        ids, w = gs.routing(wl, step)
+        gs.assert_layer_close(run_decode(layer, x, ids, w, out_dtype), oracle_decode(layer, x, ids, w))
+
+
+def test_mx_single_token_activation_scales_routes_and_counter():
+    wl = inputs.DECODE
+    layer = mx_layer(wl)
+    ids, w = gs.routing(wl)
+    for scale in (1e-3, 3e3):
+        x = (inputs.activations(wl, dtype=torch.float32) * scale).to(torch.bfloat16)
+        gs.assert_layer_close(run_decode(layer, x, ids, w, torch.float32), oracle_decode(layer, x, ids, w))
+    x = inputs.activations(wl)
+    ids2 = ids.copy()
+    ids2[0, 1] = ids2[0, 0]                                      # a duplicate
+    ids2[0, 5] = -1                                              # and an invalid route
+    ws = torch.zeros(moe.moe_ffn_decode_workspace_size(1, wl.k, wl.d, wl.I), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ys = [run_decode(layer, x, ids2, w, torch.float32, ws=ws, dev_status=st) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert st.tolist() == [3, 0]
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+    gs.assert_layer_close(ys[0], oracle_decode(layer, x, ids2, w))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ws[:8].view(torch.int64).item() == 3 * sms
 
 
 # ---- one token, 4-bit AWQ: the single-kernel path (gate/up, SwiGLU, down)

@@ -35,6 +35,16 @@ moe_status_t decode_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const
                               const uint8_t *s13, const uint8_t *q2t, const uint8_t *s2t, void *y, bool y_f32,
                               void *ws, int32_t *dev_status, cudaStream_t stream);
 
+// single-token MXFP8 layer in one kernel on the standard (K-contiguous) layout
+// of both projections, optionally with the routing (decode_mx_m1.cu); ws holds
+// the grid-barrier counter in its first 8 bytes (zero before the first use)
+bool decode_mx_m1_eligible(int M, int k, int d, int I, int E);
+size_t decode_mx_m1_workspace(int k, int I);
+moe_status_t decode_mx_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const int32_t *ids, const float *wts,
+                                 const float *logits, int32_t *ids_out, float *wts_out, int k, const uint8_t *q13,
+                                 const uint8_t *s13, const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32,
+                                 void *ws, int32_t *dev_status, cudaStream_t stream);
+
 // single-token 4-bit AWQ layer in one kernel (decode_awq_m1.cu); ws holds the
 // grid-barrier counter in its first 8 bytes (zero before the first use)
 bool decode_awq_m1_eligible(int M, int k, int d, int I, int E);
