@@ -166,7 +166,13 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  *            multiple of the grid size (after a call that reports
  *            MOE_ERR_TIMEOUT they must be zeroed again)
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
- * Kernels by case: w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
+ * Kernels by case: MOE_W_MXFP8 (standard layout) with M == 1 -> one kernel
+ * (gate/up dots on mma.sync with each E4M3 pair converted exactly to f16 and
+ * the E8M0 scale applied per 32-value block in FP32, a grid-wide barrier
+ * whose counter lives in ws[0..8), then the down projection from W2 rows
+ * staged in shared memory; with moe_ffn_decode_logits the routing runs in
+ * it too), when its shared-memory plan fits;
+ * w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
  * streaming kernel (each warp owns whole neurons: gate/up dots and the
  * down-column outer product; per-SM partial outputs reduced in a fixed order
  * after a grid-wide barrier whose counter lives in ws[0..8)); other
