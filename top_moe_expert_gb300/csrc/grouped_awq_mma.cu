@@ -128,6 +128,19 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
                 const int route = tid < b ? __ldg(a.sorted + static_cast<int64_t>(blk) * b + tid) : a.mk;
                 r_route[tid] = e_ok && route >= 0 && route < a.mk ? route : -1;
             }
+            // the warps split the block's units [u, seg_end); items (unit, group).
+            // Their first weight loads go out before the operand is staged.
+            const int n = seg_end - u;
+            const int v0 = u + n * warp / kWarps, v1 = u + n * (warp + 1) / kWarps;
+            const int items = (v1 - v0) * NG1;
+            Ld ring[kPF];
+#pragma unroll
+            for (int s = 0; s < kPF; ++s)
+                if (s < items) {
+                    const int v = v0 + s / NG1, g = s % NG1;
+                    load_item(a.q13, a.s13, a.z13, static_cast<int64_t>(e) * 2 * I + (v - blk * RB1) * 8, d, g,
+                              lane, ring[s]);
+                }
             __syncthreads();
             for (int r = warp; r < kRows; r += kWarps) {
                 const int route = r_route[r];
@@ -158,18 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
                 }
             }
             __syncthreads();
-            // the warps split the block's units [u, seg_end); items (unit, group)
-            const int n = seg_end - u;
-            const int v0 = u + n * warp / kWarps, v1 = u + n * (warp + 1) / kWarps;
-            const int items = (v1 - v0) * NG1;
-            Ld ring[kPF];
-#pragma unroll
-            for (int s = 0; s < kPF; ++s)
-                if (s < items) {
-                    const int v = v0 + s / NG1, g = s % NG1;
-                    load_item(a.q13, a.s13, a.z13, static_cast<int64_t>(e) * 2 * I + (v - blk * RB1) * 8, d, g,
-                              lane, ring[s]);
-                }
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int ib = 0; ib < items; ib += kPF) {
 #pragma unroll
@@ -223,6 +224,22 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
         for (int u = c0; u < c1;) {
             const int blk = u / RB2, seg_end = min(c1, (blk + 1) * RB2);
             __syncthreads();
+            const int e_raw = __ldg(a.expert_ids + blk);
+            const bool e_ok = e_raw >= 0 && e_raw < a.E;
+            const int e = e_ok ? e_raw : 0;
+            // the warps split the block's units; their first weight loads go
+            // out before the wait for the block's gate/up values
+            const int n = seg_end - u;
+            const int v0 = u + n * warp / kWarps, v1 = u + n * (warp + 1) / kWarps;
+            const int items = (v1 - v0) * NG2;
+            Ld ring[kPF];
+#pragma unroll
+            for (int s = 0; s < kPF; ++s)
+                if (s < items) {
+                    const int v = v0 + s / NG2, g = s % NG2;
+                    load_item(a.q2, a.s2, a.z2, static_cast<int64_t>(e) * d + (v - blk * RB2) * 8, I, g, lane,
+                              ring[s]);
+                }
             if (tid == 0) {
                 // every gate/up unit of the block has written its values
                 const long long t0 = clock64(), limit = static_cast<long long>(kWaitNs) * 5 / 2;
@@ -238,9 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
                     }
                 }
             }
-            const int e_raw = __ldg(a.expert_ids + blk);
-            const bool e_ok = e_raw >= 0 && e_raw < a.E;
-            const int e = e_ok ? e_raw : 0;
             if (tid < kRows) {
                 const int route = tid < b ? __ldg(a.sorted + static_cast<int64_t>(blk) * b + tid) : a.mk;
                 r_route[tid] = e_ok && route >= 0 && route < a.mk ? route : -1;
@@ -286,17 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1) awq_mma_kernel(const Args a)
                 }
             }
             __syncthreads();
-            const int n = seg_end - u;
-            const int v0 = u + n * warp / kWarps, v1 = u + n * (warp + 1) / kWarps;
-            const int items = (v1 - v0) * NG2;
-            Ld ring[kPF];
-#pragma unroll
-            for (int s = 0; s < kPF; ++s)
-                if (s < items) {
-                    const int v = v0 + s / NG2, g = s % NG2;
-                    load_item(a.q2, a.s2, a.z2, static_cast<int64_t>(e) * d + (v - blk * RB2) * 8, I, g, lane,
-                              ring[s]);
-                }
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int ib = 0; ib < items; ib += kPF) {
 #pragma unroll
