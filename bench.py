@@ -386,6 +386,9 @@ class DecodeStep:
             return "moe_ffn_decode_logits: dm::m1_kernel (top-k routing + gate/up + SwiGLU + down + combine), one kernel"
         if self.fused:
             return "moe_ffn_decode: df::fused_kernel + df::reduce_kernel, PDL-chained"
+        if self.w2_standard and 2 <= self.wl.M <= 64:
+            return ("moe_ffn_decode (standard W2 layout, 2 <= M <= 64): alignment into blocks of 16 + "
+                    "gmx::mx_mma_kernel (both GEMMs on mma.sync) + combine")
         return "moe_ffn_decode: ds::gate_up_kernel + ds::down_kernel, PDL-chained"
 
     def launches_per_step(self) -> int:
@@ -399,6 +402,8 @@ class DecodeStep:
         if self.awq:
             # fixed routing: the single-token kernel, or the two decode kernels
             return 1 if self.wl.M == 1 else 2
+        if self.w2_standard and 2 <= self.wl.M <= 64:
+            return 4                       # top-k, alignment, the GEMM kernel, combine
         return 1 if self.routed_in_layer else 3
 
     def capture(self):
@@ -614,6 +619,9 @@ def run_ours(args, rank, world, device):
                             "single-token decode: routing + gate/up + SwiGLU + down + combine in one kernel"
                             if st.routed_in_layer else
                             "single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
+                            else ("small-batch decode on the standard W2 layout (topk + alignment into blocks of 16 "
+                                  "+ one kernel for both GEMMs on mma.sync + combine)")
+                            if st.w2_standard and 2 <= wl.M <= 64
                             else "output-centric decode (topk + gate/up + down)") + ", CUDA graph",
                    "l2": "flushed between timed steps (512 MiB write, outside the timed interval)",
                    "parallelism": f"replicas x{world}"},

@@ -172,6 +172,12 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  * whose counter lives in ws[0..8), then the down projection from W2 rows
  * staged in shared memory; with moe_ffn_decode_logits the routing runs in
  * it too), when its shared-memory plan fits;
+ * MOE_W_MXFP8 (standard layout) with 2 <= M <= 64 -> the routes aligned
+ * into blocks of 16 rows per expert (moe_align_block_size, which counts the
+ * invalid routes), one kernel for both GEMMs (mma.sync, each block one
+ * M-tile, x and h unquantized as above, per-block hand-off counters), and
+ * the slot-ordered combine; ws then holds that alignment, the gate/up values
+ * and the per-route down rows (moe_ffn_decode_workspace_size);
  * w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
  * streaming kernel (each warp owns whole neurons: gate/up dots and the
  * down-column outer product; per-SM partial outputs reduced in a fixed order

@@ -331,6 +331,11 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
         const size_t x1 = decode_mx_m1_workspace(k, I);
         part = part > x1 ? part : x1;
     }
+    if (M >= 2 && M <= 64 && k <= 32 && d % 64 == 0 && I % 64 == 0) {
+        // the alignment capacity is largest when every route has its own expert
+        const size_t xs = decode_mx_small_workspace(M, k, d, I, M * k);
+        part = part > xs ? part : xs;
+    }
     *bytes = h > part ? h : part;
     return MOE_OK;
 }
@@ -429,6 +434,16 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
             dev_status, s);
         if (st1 != MOE_ERR_UNSUPPORTED)
             return st1;
+    }
+    if (fmt == MOE_W_MXFP8 && decode_mx_small_eligible(M, k, d, I, w13->E)) {
+        // a small batch on the standard layout: aligned blocks, one kernel for both GEMMs, combine
+        const moe_status_t st2 = decode_mx_small_launch(
+            static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
+            static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
+            static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws,
+            ws_bytes, dev_status, s);
+        if (st2 != MOE_ERR_UNSUPPORTED)
+            return st2;
     }
     if (fmt == MOE_W_MXFP8 && decode_stream_eligible(M, k, d, I, w13->E, w13->q, w13->scale, w2->q, w2->scale)) {
         const moe_status_t st2 = decode_stream_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,

@@ -45,6 +45,16 @@ moe_status_t decode_mx_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, co
                                  const uint8_t *s13, const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32,
                                  void *ws, int32_t *dev_status, cudaStream_t stream);
 
+// MXFP8 layer for 2 <= M <= 64 on the standard layout (grouped_mx_mma.cu):
+// alignment into blocks of 16 rows, one mma.sync kernel for both GEMMs, then
+// the combine; ws as laid out there
+bool decode_mx_small_eligible(int M, int k, int d, int I, int E);
+size_t decode_mx_small_workspace(int M, int k, int d, int I, int E);
+moe_status_t decode_mx_small_launch(const __nv_bfloat16 *x, int M, int d, int I, int E, const int32_t *ids,
+                                    const float *wts, int k, const uint8_t *q13, const uint8_t *s13,
+                                    const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32, void *ws,
+                                    size_t ws_bytes, int32_t *dev_status, cudaStream_t s);
+
 // single-token 4-bit AWQ layer in one kernel (decode_awq_m1.cu); ws holds the
 // grid-barrier counter in its first 8 bytes (zero before the first use)
 bool decode_awq_m1_eligible(int M, int k, int d, int I, int E);
