@@ -375,6 +375,9 @@ class DecodeStep:
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
         if self.awq and self.wl.M == 1:
             return "moe_ffn_decode (AWQ-4bit, one token): da1::awq_m1_kernel (gate/up + SwiGLU + down), one kernel"
+        if self.awq and 2 <= self.wl.M <= 64:
+            return ("moe_ffn_decode (AWQ-4bit, 2 <= M <= 64): alignment into blocks of 16 + gsm::awq_mma_kernel "
+                    "(both GEMMs on mma.sync) + combine")
         if self.awq:
             return "moe_ffn_decode (AWQ-4bit): decode_gate_up_kernel<AWQ> + decode_down_kernel<AWQ>"
         if self.path == "grouped":
@@ -400,8 +403,9 @@ class DecodeStep:
                 return na + (2 if self.b <= 16 else 3)
             return 1 + na + 3
         if self.awq:
-            # fixed routing: the single-token kernel, or the two decode kernels
-            return 1 if self.wl.M == 1 else 2
+            # fixed routing: the single-token kernel; alignment, the GEMM kernel and the
+            # combine up to 64 tokens; the two decode kernels beyond
+            return 1 if self.wl.M == 1 else (3 if self.wl.M <= 64 else 2)
         if self.w2_standard and 2 <= self.wl.M <= 64:
             return 4                       # top-k, alignment, the GEMM kernel, combine
         return 1 if self.routed_in_layer else 3
@@ -611,6 +615,9 @@ def run_ours(args, rank, world, device):
                             if st.awq and st.path == "grouped" else
                             ("single-token AWQ decode: gate/up + SwiGLU + down in one kernel, f16 mma.sync dot "
                              "products on raw 4-bit codes, zero folded in FP32, fixed routing") if st.awq and wl.M == 1 else
+                            ("small-batch AWQ decode (alignment into blocks of 16 + one kernel for both GEMMs on "
+                             "mma.sync over the raw 4-bit codes + combine, fixed routing)")
+                            if st.awq and 2 <= wl.M <= 64 else
                             "output-centric AWQ decode (gate/up + down on CUDA cores, fixed routing)" if st.awq else
                             "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
                             % st.b if st.path == "grouped" else

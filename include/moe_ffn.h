@@ -178,6 +178,9 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  * M-tile, x and h unquantized as above, per-block hand-off counters), and
  * the slot-ordered combine; ws then holds that alignment, the gate/up values
  * and the per-route down rows (moe_ffn_decode_workspace_size);
+ * MOE_W_AWQ4 with 2 <= M <= 64 -> the same chain with the small-block AWQ
+ * kernel of moe_ffn_grouped (raw 4-bit codes as f16, zero and scale applied
+ * in FP32 per group, x and h unquantized);
  * w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
  * streaming kernel (each warp owns whole neurons: gate/up dots and the
  * down-column outer product; per-SM partial outputs reduced in a fixed order

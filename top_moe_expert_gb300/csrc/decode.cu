@@ -422,6 +422,13 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         return MOE_ERR_WORKSPACE;
     float *h = static_cast<float *>(ws);
     cudaStream_t s = as_stream(stream);
+    if (fmt == MOE_W_AWQ4 && decode_awq_small_eligible(M, k, d, I, w13->E)) {
+        // a small batch: aligned blocks of 16 rows, one kernel for both GEMMs, combine
+        const moe_status_t st3 = decode_awq_small_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k,
+                                                         w13, w2, y, ydt == MOE_FP32, ws, ws_bytes, dev_status, s);
+        if (st3 != MOE_ERR_UNSUPPORTED)
+            return st3;
+    }
     if (fmt == MOE_W_AWQ4 && decode_awq_m1_eligible(M, k, d, I, w13->E))
         return decode_awq_m1_launch(x, xdt == MOE_BF16, topk_ids, topk_w, k, d, I, w13->E, w13->q, w13->scale,
                                     w13->zero, w2->q, w2->scale, w2->zero, y, ydt == MOE_FP32, ws, dev_status, s);

@@ -45,6 +45,23 @@ moe_status_t decode_mx_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, co
                                  const uint8_t *s13, const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32,
                                  void *ws, int32_t *dev_status, cudaStream_t stream);
 
+// Workspace of the small-batch paths (2 <= M <= 64), each part rounded up to
+// 256 bytes: [align ws | sorted route ids | expert ids | rows after padding |
+// done | gu | yr], the alignment in blocks of 16 rows
+struct SmallWs {
+    size_t align_ws, sorted, expert, npp, done, gu, yr, total;
+    int cap_rows, cap_blocks;
+};
+SmallWs small_ws_layout(int M, int k, int d, int I, int E);
+
+// 4-bit AWQ layer for 2 <= M <= 64 through moe_ffn_decode (grouped_awq_mma.cu):
+// alignment into blocks of 16 rows, the small-block AWQ kernel, the combine
+bool decode_awq_small_eligible(int M, int k, int d, int I, int E);
+moe_status_t decode_awq_small_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
+                                     const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                     void *y, bool y_f32, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                     cudaStream_t s);
+
 // MXFP8 layer for 2 <= M <= 64 on the standard layout (grouped_mx_mma.cu):
 // alignment into blocks of 16 rows, one mma.sync kernel for both GEMMs, then
 // the combine; ws as laid out there

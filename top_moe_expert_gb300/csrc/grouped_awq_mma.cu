@@ -35,6 +35,7 @@
 
 #include "attr.h"
 #include "common.cuh"
+#include "decode_internal.h"
 #include "grouped_awq_mma.cuh"
 #include "grouped_internal.h"
 
@@ -378,6 +379,54 @@ moe_status_t grouped_awq_mma_launch(const void *x, bool x_bf16, int M, int d, in
                       static_cast<const uint32_t *>(w2->q), static_cast<const uint16_t *>(w2->scale),
                       static_cast<const int32_t *>(w2->zero), done, gu, yr, dev_status, x_bf16 ? 1 : 0,
                       M, k, d, I, E, b, static_cast<int>(mk), cap_rows / b};
+    if (launch_pdl(gsm::awq_mma_kernel, dim3(device_sm_count()), dim3(gsm::kThreads),
+                   static_cast<size_t>(L.bytes()), s, a) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return grouped_combine_launch(yr, ids, M, k, d, E, y, y_f32, s);
+}
+
+bool decode_awq_small_eligible(int M, int k, int d, int I, int E)
+{
+    return M >= 2 && M <= 64 && k >= 1 && k <= 32 && E >= 1 && grouped_awq_mma_eligible(gsm::kRows, d, I) &&
+           static_cast<int64_t>(M) * k * (2 * I + d) * 4 < (int64_t(1) << 31);
+}
+
+moe_status_t decode_awq_small_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
+                                     const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                     void *y, bool y_f32, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                     cudaStream_t s)
+{
+    if (!decode_awq_small_eligible(M, k, d, I, E) || !aligned(ws, 256) || !aligned(w13->q, 16) ||
+        !aligned(w2->q, 16))
+        return MOE_ERR_UNSUPPORTED;
+    const SmallWs W = small_ws_layout(M, k, d, I, E);
+    if (ws_bytes < W.total)
+        return MOE_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    int32_t *sorted = reinterpret_cast<int32_t *>(w + W.sorted);
+    int32_t *expert = reinterpret_cast<int32_t *>(w + W.expert);
+    int32_t *npp = reinterpret_cast<int32_t *>(w + W.npp);
+    int32_t *done = reinterpret_cast<int32_t *>(w + W.done);
+    float *gu = reinterpret_cast<float *>(w + W.gu);
+    float *yr = reinterpret_cast<float *>(w + W.yr);
+    static std::atomic<uint64_t> attr_done{0};
+    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(gsm::awq_mma_kernel), 220 * 1024))
+        return MOE_ERR_CUDA;
+    // the routes in blocks of 16 rows per expert (invalid ids are counted here)
+    const moe_status_t st = moe_align_block_size(ids, M, k, E, gsm::kRows, sorted, expert, npp, W.cap_rows,
+                                                 W.cap_blocks, w + W.align_ws, W.sorted - W.align_ws, dev_status,
+                                                 s);
+    if (st != MOE_OK)
+        return st;
+    if (cudaMemsetAsync(done, 0, static_cast<size_t>(W.cap_blocks) * 4, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const gsm::Smem L{d, I};
+    const size_t mk = static_cast<size_t>(M) * k;
+    const gsm::Args a{x, wts, sorted, expert, npp, static_cast<const uint32_t *>(w13->q),
+                      static_cast<const uint16_t *>(w13->scale), static_cast<const int32_t *>(w13->zero),
+                      static_cast<const uint32_t *>(w2->q), static_cast<const uint16_t *>(w2->scale),
+                      static_cast<const int32_t *>(w2->zero), done, gu, yr, dev_status, x_bf16 ? 1 : 0,
+                      M, k, d, I, E, gsm::kRows, static_cast<int>(mk), W.cap_blocks};
     if (launch_pdl(gsm::awq_mma_kernel, dim3(device_sm_count()), dim3(gsm::kThreads),
                    static_cast<size_t>(L.bytes()), s, a) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -334,18 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_mma_kernel(const Args a)
 }  // namespace gmx
 
 
-namespace {
-
-// Workspace of this path, each part rounded up to 256 bytes:
-// [align ws | sorted route ids | expert ids | rows after padding | done | gu | yr]
-struct MxWs {
-    size_t align_ws, sorted, expert, npp, done, gu, yr, total;
-    int cap_rows, cap_blocks;
-};
-
-MxWs mx_ws(int M, int k, int d, int I, int E)
+SmallWs small_ws_layout(int M, int k, int d, int I, int E)
 {
-    MxWs w{};
+    SmallWs w{};
     int32_t cr = 0, cb = 0;
     size_t na = 0;
     moe_align_capacity(M, k, E, gmx::kRows, &cr, &cb);
@@ -365,8 +356,6 @@ MxWs mx_ws(int M, int k, int d, int I, int E)
     return w;
 }
 
-}  // namespace
-
 bool decode_mx_small_eligible(int M, int k, int d, int I, int E)
 {
     const gmx::Smem L{d, I};
@@ -376,7 +365,7 @@ bool decode_mx_small_eligible(int M, int k, int d, int I, int E)
 
 size_t decode_mx_small_workspace(int M, int k, int d, int I, int E)
 {
-    return mx_ws(M, k, d, I, E).total;
+    return small_ws_layout(M, k, d, I, E).total;
 }
 
 moe_status_t decode_mx_small_launch(const __nv_bfloat16 *x, int M, int d, int I, int E, const int32_t *ids,
@@ -387,7 +376,7 @@ moe_status_t decode_mx_small_launch(const __nv_bfloat16 *x, int M, int d, int I,
     if (!decode_mx_small_eligible(M, k, d, I, E) || !aligned(ws, 256) || !aligned(q13, 8) || !aligned(q2, 8) ||
         !aligned(s13, 2) || !aligned(s2, 2))
         return MOE_ERR_UNSUPPORTED;
-    const MxWs W = mx_ws(M, k, d, I, E);
+    const SmallWs W = small_ws_layout(M, k, d, I, E);
     if (ws_bytes < W.total)
         return MOE_ERR_WORKSPACE;
     uint8_t *w = static_cast<uint8_t *>(ws);
