@@ -48,7 +48,7 @@ namespace moe {
 namespace dx1 {
 
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr int kPF = 4;                  // phase-1 items in flight per warp
+constexpr int kPF = 8;                  // phase-1 items in flight per warp (16 bytes each per lane)
 
 __device__ __forceinline__ void set_err(int32_t *st, int code)
 {
