@@ -102,7 +102,7 @@ static void emu_item(float (&acc)[32][2], const Ld (&ld)[32], const uint32_t *a3
 
 extern "C" int mx_m1_emulate(const uint16_t *x_bf16, const int32_t *ids, const float *wts, const uint8_t *q13,
                              const uint8_t *s13, const uint8_t *q2, const uint8_t *s2, float *gp, float *y, int k,
-                             int d, int I, int E, int G, int *status)
+                             int d, int I, int E, int G, int stage, int *status)
 {
     const int NG = d / 64, NG2 = I / 64, RB = 2 * I / 8;
     int r_e[kMaxK], nv = 0;
@@ -191,7 +191,7 @@ extern "C" int mx_m1_emulate(const uint16_t *x_bf16, const int32_t *ids, const f
     const int B2 = d / 8;
     for (int b = 0; b < G; ++b) {
         const int blk0 = split_lo(B2, b, G), nb = split_lo(B2, b + 1, G) - blk0;
-        const Smem L{d, I, k, nb};
+        const Smem L{d, I, k, nb, stage};
         if (L.bytes() > maxsmem)
             maxsmem = L.bytes();
         std::vector<uint8_t> sm(L.bytes(), 0xFF);
@@ -200,14 +200,14 @@ extern "C" int mx_m1_emulate(const uint16_t *x_bf16, const int32_t *ids, const f
         float *hf = reinterpret_cast<float *>(sm.data() + L.hf());
         uint16_t *hp = reinterpret_cast<uint16_t *>(sm.data() + L.hp());
         float *part2 = reinterpret_cast<float *>(sm.data() + L.part2());
-        for (int r = 0; r < nv * nb * 8; ++r) {
+        for (int r = 0; stage && r < nv * nb * 8; ++r) {
             const int j = r / (nb * 8), o = blk0 * 8 + (r - j * nb * 8);
             const uint8_t *src = q2 + (static_cast<int64_t>(r_e[j]) * d + o) * I;
             if ((reinterpret_cast<uintptr_t>(src) & 15) || ((L.w2() + r * I) & 15) || (I & 15))
                 return -5;
             memcpy(w2s + r * I, src, I);
         }
-        for (int i = 0; i < nv * nb * 8 * (I / 32); ++i) {
+        for (int i = 0; stage && i < nv * nb * 8 * (I / 32); ++i) {
             const int r = i / (I / 32), c = i - r * (I / 32);
             const int j = r / (nb * 8), o = blk0 * 8 + (r - j * nb * 8);
             s2s[i] = s2[(static_cast<int64_t>(r_e[j]) * d + o) * (I / 32) + c];
@@ -243,7 +243,10 @@ extern "C" int mx_m1_emulate(const uint16_t *x_bf16, const int32_t *ids, const f
             for (int c = 0; c < NG2; ++c) {
                 Ld ld[32];
                 for (int l = 0; l < 32; ++l)
-                    mx_load(w2s, s2s, rbase, I, c, l, ld[l]);
+                    if (stage)
+                        mx_load(w2s, s2s, rbase, I, c, l, ld[l]);
+                    else
+                        mx_load(q2, s2, static_cast<int64_t>(r_e[j]) * d + (blk0 + bl) * 8, I, c, l, ld[l]);
                 emu_item(acc, ld, h32 + j * I / 2, c * 64);
                 emu_item(acc, ld, h32 + (nv + j) * I / 2, c * 64);
             }

@@ -53,7 +53,7 @@ def _weights(wl):
     return [np.ascontiguousarray(a) for a in (q13, s13, q2, s2)]
 
 
-def _run(emu, wl, G, ids=None, w=None, weights=None, xscale=1.0):
+def _run(emu, wl, G, ids=None, w=None, weights=None, xscale=1.0, stage=1):
     x = (inputs.activations(wl, dtype=torch.float32) * xscale).to(torch.bfloat16)[:1]
     if ids is None:
         ids, w = oracle.topk_softmax(inputs.router_logits(wl, 0), wl.k)
@@ -65,7 +65,7 @@ def _run(emu, wl, G, ids=None, w=None, weights=None, xscale=1.0):
     st = np.zeros(2, dtype=np.int32)
     xb = inputs.bits16(x)
     rc = emu.mx_m1_emulate(_p(xb), _p(ids), _p(w), _p(q13), _p(s13), _p(q2), _p(s2), _p(gp), _p(y), wl.k, wl.d,
-                           wl.I, wl.E, G, _p(st))
+                           wl.I, wl.E, G, stage, _p(st))
     assert rc > 0, (rc, st)
     assert rc <= 220 * 1024
     ref = oracle.moe_layer(x.to(torch.float64).numpy(), ids, w.astype(np.float64), wl.E,
@@ -86,6 +86,9 @@ def test_decode_shape_matches_oracle_and_grid_independent(emu):
     y152 = _run(emu, DECODE8, 152, weights=weights)
     y148 = _run(emu, DECODE8, 148, weights=weights)
     assert np.allclose(y152, y148, rtol=1e-5, atol=1e-7 * np.abs(y152).max())
+    # W2 read from global memory (the form used when its rows do not fit in
+    # shared memory) gives the same bits
+    assert np.array_equal(_run(emu, DECODE8, 152, weights=weights, stage=0), y152)
 
 
 def test_small_shapes_scales_and_routes(emu):
@@ -95,3 +98,9 @@ def test_small_shapes_scales_and_routes(emu):
     _run(emu, wl, 37, weights=weights, xscale=1e-3)
     _run(emu, wl, 152, weights=weights, xscale=3e3)
     _run(emu, wl, 152, ids=[3, 3, -1, 16], w=[0.4, 0.3, 0.2, 0.1], weights=weights)
+
+
+def test_large_expert_shape_reads_w2_from_global(emu):
+    # d = 7168, I = 2048: the CTA's W2 rows do not fit in shared memory
+    wl = inputs.Workload("mx_m1_host_large", M=1, d=7168, I=2048, E=8, k=8, seed=4)
+    _run(emu, wl, 152, stage=0)

@@ -49,6 +49,7 @@ namespace dx1 {
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kPF = 8;                  // phase-1 items in flight per warp (16 bytes each per lane)
+constexpr int kPF2 = 4;                 // phase-2 items in flight per warp
 
 __device__ __forceinline__ void set_err(int32_t *st, int code)
 {
@@ -99,7 +100,7 @@ __device__ __forceinline__ void item(float (&acc)[2], const Ld &ld, const uint32
     }
 }
 
-template <int ROUTE_PL>
+template <int ROUTE_PL, bool STAGE_W2>
 __global__ void __launch_bounds__(kThreads, 1) mx_m1_kernel(const Args a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_m1_kernel(const Args a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = lane & 3, gl = lane >> 2;
     const int G = gridDim.x, b = blockIdx.x;
     const int B2 = d / 8, blk0 = split_lo(B2, b, G), nb = split_lo(B2, b + 1, G) - blk0;
-    const Smem L{d, I, a.k, nb};
+    const Smem L{d, I, a.k, nb, STAGE_W2 ? 1 : 0};
     __half *xp = reinterpret_cast<__half *>(smem + L.xp());
     int *r_e = reinterpret_cast<int *>(smem + L.route());
     float *r_w = reinterpret_cast<float *>(r_e + kMaxK);
@@ -177,14 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1) mx_m1_kernel(const Args a)
             m = fmaxf(m, s_wmax[w]);
         s_sigx = f16_sigma(m);
     }
-    // W2 rows of this CTA into shared memory (I bytes each)
+    // W2 rows of this CTA (I bytes each): into shared memory, or (rows that
+    // do not fit) into L2 for phase 2 to read
     if (warp == 0) {
         if (lane == 0)
-            tc::mbar_arrive_expect_tx(mbar, static_cast<uint32_t>(nv * nb * 8 * I));
+            tc::mbar_arrive_expect_tx(mbar, STAGE_W2 ? static_cast<uint32_t>(nv * nb * 8 * I) : 0u);
         __syncwarp();
         for (int r = lane; r < nv * nb * 8; r += 32) {
             const int j = r / (nb * 8), o = blk0 * 8 + (r - j * nb * 8);
-            tc::bulk_load(tc::smem_u32(w2s) + r * I, a.q2 + (static_cast<int64_t>(r_e[j]) * d + o) * I, I, mbar);
+            const uint8_t *src = a.q2 + (static_cast<int64_t>(r_e[j]) * d + o) * I;
+            if constexpr (STAGE_W2)
+                tc::bulk_load(tc::smem_u32(w2s) + r * I, src, I, mbar);
+            else
+                tc::bulk_prefetch_l2(src, I);
         }
     }
     __syncthreads();
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_m1_kernel(const Args a)
         }
     }
     // W2 scale bytes of this CTA's rows
-    for (int i = tid; i < nv * nb * 8 * (I / 32); i += kThreads) {
+    for (int i = tid; STAGE_W2 && i < nv * nb * 8 * (I / 32); i += kThreads) {
         const int r = i / (I / 32), c = i - r * (I / 32);
         const int j = r / (nb * 8), o = blk0 * 8 + (r - j * nb * 8);
         s2s[i] = __ldg(a.s2 + (static_cast<int64_t>(r_e[j]) * d + o) * (I / 32) + c);
@@ -334,22 +340,49 @@ __global__ void __launch_bounds__(kThreads, 1) mx_m1_kernel(const Args a)
     if (s_abort)
         return;
 
-    // ---- phase 2: units (slot j, output block) over the warps
+    // ---- phase 2: units (slot j, output block) over the warps: warp w takes
+    // units w, w + 16, ...; its items (unit, chunk) run with kPF2 in flight
     const uint32_t *h32 = reinterpret_cast<const uint32_t *>(hp);
-    for (int v = warp; v < nv * nb; v += kWarps) {
-        const int j = v / nb, bl = v - j * nb;
-        const int rbase = j * nb * 8 + bl * 8;
+    {
+        const int nunits = nv * nb;
+        const int my_units = nunits > warp ? (nunits - warp + kWarps - 1) / kWarps : 0;
+        const int items = my_units * NG2;
+        auto load2 = [&](int it, Ld &o) {
+            const int v = warp + kWarps * (it / NG2), c = it % NG2;
+            const int j = v / nb, bl = v - j * nb;
+            if constexpr (STAGE_W2)
+                mx_load(w2s, s2s, j * nb * 8 + bl * 8, I, c, lane, o);
+            else
+                mx_load(a.q2, a.s2, static_cast<int64_t>(r_e[j]) * d + (blk0 + bl) * 8, I, c, lane, o);
+        };
+        Ld ring[kPF2];
+#pragma unroll
+        for (int s = 0; s < kPF2; ++s)
+            if (s < items)
+                load2(s, ring[s]);
         float acc[2] = {0.f, 0.f};
-        for (int c = 0; c < NG2; ++c) {
-            Ld ld;
-            mx_load(w2s, s2s, rbase, I, c, lane, ld);
-            item(acc, ld, h32 + j * I / 2, c * 64, lane);
-            item(acc, ld, h32 + (nv + j) * I / 2, c * 64, lane);
-        }
-        if (gl == 0) {
-            const float un = ldexpf(1.0f, -r_sig[j]);
-            part2[(j * nb + bl) * 8 + 2 * q] = acc[0] * un;
-            part2[(j * nb + bl) * 8 + 2 * q + 1] = acc[1] * un;
+        for (int ib = 0; ib < items; ib += kPF2) {
+#pragma unroll
+            for (int s = 0; s < kPF2; ++s) {
+                const int it = ib + s;
+                if (it < items) {
+                    const int v = warp + kWarps * (it / NG2), c = it % NG2;
+                    const int j = v / nb, bl = v - j * nb;
+                    const Ld ld = ring[s];
+                    if (it + kPF2 < items)
+                        load2(it + kPF2, ring[s]);
+                    item(acc, ld, h32 + j * I / 2, c * 64, lane);
+                    item(acc, ld, h32 + (nv + j) * I / 2, c * 64, lane);
+                    if (c == NG2 - 1) {
+                        if (gl == 0) {
+                            const float un = ldexpf(1.0f, -r_sig[j]);
+                            part2[(j * nb + bl) * 8 + 2 * q] = acc[0] * un;
+                            part2[(j * nb + bl) * 8 + 2 * q + 1] = acc[1] * un;
+                        }
+                        acc[0] = acc[1] = 0.f;
+                    }
+                }
+            }
         }
     }
     __syncthreads();
@@ -388,7 +421,7 @@ bool decode_mx_m1_eligible(int M, int k, int d, int I, int E)
     if (M != 1 || k < 1 || k > dx1::kMaxK || E < 1 || d % 64 || d < 64 || I % 64 || I < 64 || G > 1024 ||
         static_cast<int64_t>(k) * 2 * I / 8 * (d / 64) > INT32_MAX / 2)
         return false;
-    const dx1::Smem L{d, I, k, (d / 8 + G - 1) / G};
+    const dx1::Smem L{d, I, k, (d / 8 + G - 1) / G, 0};         // W2 read from global if it does not fit
     if (L.bytes() > 220 * 1024)
         return false;
     for (int nv = 1; nv <= k; ++nv)
@@ -412,8 +445,9 @@ moe_status_t decode_mx_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, co
         !aligned(s13, 2) ||
         (logits && (E > 512 || E < k)))
         return MOE_ERR_UNSUPPORTED;
-    const dx1::Smem L{d, I, k, (d / 8 + G - 1) / G};
-    const int smem = L.bytes();
+    const dx1::Smem Ls{d, I, k, (d / 8 + G - 1) / G, 1}, Lg{d, I, k, (d / 8 + G - 1) / G, 0};
+    const bool stage = Ls.bytes() <= 220 * 1024;
+    const int smem = stage ? Ls.bytes() : Lg.bytes();
     uint8_t *w = static_cast<uint8_t *>(ws);
     const dx1::Args a{x, ids, wts, logits, ids_out, wts_out, q13, s13, q2, s2,
                       reinterpret_cast<unsigned long long *>(w), reinterpret_cast<float *>(w + 256), y, dev_status,
@@ -425,10 +459,12 @@ moe_status_t decode_mx_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, co
                    ? MOE_OK
                    : MOE_ERR_CUDA;
     };
-    if (!logits)
-        return go(dx1::mx_m1_kernel<0>);
-    const int pl = (E + 31) / 32;
-    return pl <= 4 ? go(dx1::mx_m1_kernel<4>) : pl <= 8 ? go(dx1::mx_m1_kernel<8>) : go(dx1::mx_m1_kernel<16>);
+    const int pl = !logits ? 0 : (E + 31) / 32 <= 4 ? 4 : (E + 31) / 32 <= 8 ? 8 : 16;
+    if (stage)
+        return pl == 0 ? go(dx1::mx_m1_kernel<0, true>) : pl == 4 ? go(dx1::mx_m1_kernel<4, true>)
+               : pl == 8 ? go(dx1::mx_m1_kernel<8, true>) : go(dx1::mx_m1_kernel<16, true>);
+    return pl == 0 ? go(dx1::mx_m1_kernel<0, false>) : pl == 4 ? go(dx1::mx_m1_kernel<4, false>)
+           : pl == 8 ? go(dx1::mx_m1_kernel<8, false>) : go(dx1::mx_m1_kernel<16, false>);
 }
 
 }  // namespace moe

@@ -138,17 +138,19 @@ DA1_HD void mx_fold(float (&acc)[2], const float (&dd)[4], const Ld &o, int p)
 }
 
 // Shared-memory plan (bytes from the dynamic base, 16-byte aligned regions).
-//   nb: output blocks of 8 of this CTA (phase 2)
+//   nb: output blocks of 8 of this CTA (phase 2); stage: 1 when the CTA's W2
+//   rows and their scales are staged in shared memory, 0 when phase 2 reads
+//   them from global memory (shapes whose rows do not fit)
 struct Smem {
-    int d, I, k, nb;
+    int d, I, k, nb, stage;
     DA1_HD static int al(int v) { return (v + 15) & ~15; }
     DA1_HD int xp() const { return 0; }                                   // [d] f16
     DA1_HD int route() const { return al(xp() + 2 * d); }                 // e [32], w [32], sigma [32]
     DA1_HD int mbar() const { return route() + 3 * kMaxK * 4; }           // u64
     DA1_HD int part1() const { return al(mbar() + 8); }                   // [16][4][8] f32 + [16][4] unit ids
     DA1_HD int w2() const { return al(part1() + kWarps * 4 * 8 * 4 + kWarps * 4 * 4); }  // [k][nb*8][I] E4M3
-    DA1_HD int s2() const { return al(w2() + k * nb * 8 * I); }          // [k][nb*8][I/32] E8M0
-    DA1_HD int hf() const { return al(s2() + k * nb * 8 * (I / 32)); }   // [k][I] f32 (h)
+    DA1_HD int s2() const { return al(w2() + stage * k * nb * 8 * I); }  // [k][nb*8][I/32] E8M0
+    DA1_HD int hf() const { return al(s2() + stage * k * nb * 8 * (I / 32)); }   // [k][I] f32 (h)
     DA1_HD int hp() const { return al(hf() + 4 * k * I); }               // [2][k][I] f16 hi / lo
     DA1_HD int part2() const { return al(hp() + 2 * 2 * k * I); }        // [k][nb][8] f32
     DA1_HD int bytes() const { return al(part2() + 4 * k * nb * 8); }
