@@ -226,6 +226,8 @@ class DecodeStep:
         self.routed_in_layer = False
         self.w2_standard = w2_layout == "standard"
         self.awq = wl.fmt == "awq4"
+        # the library's opt-in kernels (MOE_FFN_CANDIDATE_KERNELS=1) decide several paths below
+        self.cand = bool(moe.moe_candidate_kernels_enabled())
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
         if self.awq:
             self._init_awq(wl, nsteps, device, block)
@@ -249,7 +251,7 @@ class DecodeStep:
             self.fused = M <= 4 and d % 1024 == 0 and not self.w2_standard
             # one token on that layout: routing runs inside the layer's kernel
             self.routed_in_layer = self.fused and M == 1 and d in (1024, 2048) and E <= 512
-            if self.w2_standard and M == 1 and E <= 512:
+            if self.w2_standard and M == 1 and E <= 512 and self.cand:
                 # one token on the standard layout: the single-kernel path, routing inside
                 self.routed_in_layer = True
             if self.fused:
@@ -368,14 +370,14 @@ class DecodeStep:
         self.launch_layer(stream)
 
     def layer_kernels(self) -> str:
-        if self.awq and self.path == "grouped" and self.b <= 16:
+        if self.awq and self.path == "grouped" and self.b <= 16 and self.cand:
             return ("moe_ffn_grouped (AWQ-4bit, b <= 16): gsm::awq_mma_kernel (both GEMMs on mma.sync over the raw "
                     "codes, one kernel) + combine")
         if self.awq and self.path == "grouped":
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
-        if self.awq and self.wl.M == 1:
+        if self.awq and self.wl.M == 1 and self.cand:
             return "moe_ffn_decode (AWQ-4bit, one token): da1::awq_m1_kernel (gate/up + SwiGLU + down), one kernel"
-        if self.awq and 2 <= self.wl.M <= 64:
+        if self.awq and 2 <= self.wl.M <= 64 and self.cand:
             return ("moe_ffn_decode (AWQ-4bit, 2 <= M <= 64): alignment into blocks of 16 + gsm::awq_mma_kernel "
                     "(both GEMMs on mma.sync) + combine")
         if self.awq:
@@ -389,7 +391,7 @@ class DecodeStep:
             return "moe_ffn_decode_logits: dm::m1_kernel (top-k routing + gate/up + SwiGLU + down + combine), one kernel"
         if self.fused:
             return "moe_ffn_decode: df::fused_kernel + df::reduce_kernel, PDL-chained"
-        if self.w2_standard and 2 <= self.wl.M <= 64:
+        if self.w2_standard and 2 <= self.wl.M <= 64 and self.cand:
             return ("moe_ffn_decode (standard W2 layout, 2 <= M <= 64): alignment into blocks of 16 + "
                     "gmx::mx_mma_kernel (both GEMMs on mma.sync) + combine")
         return "moe_ffn_decode: ds::gate_up_kernel + ds::down_kernel, PDL-chained"
@@ -400,13 +402,15 @@ class DecodeStep:
             na = 2 if self.ws_align is not None else 1
             if self.awq:
                 # the b <= 16 AWQ path: one kernel for both GEMMs, then the combine
-                return na + (2 if self.b <= 16 else 3)
+                return na + (2 if self.b <= 16 and self.cand else 3)
             return 1 + na + 3
         if self.awq:
             # fixed routing: the single-token kernel; alignment, the GEMM kernel and the
             # combine up to 64 tokens; the two decode kernels beyond
+            if not self.cand:
+                return 2
             return 1 if self.wl.M == 1 else (3 if self.wl.M <= 64 else 2)
-        if self.w2_standard and 2 <= self.wl.M <= 64:
+        if self.w2_standard and 2 <= self.wl.M <= 64 and self.cand:
             return 4                       # top-k, alignment, the GEMM kernel, combine
         return 1 if self.routed_in_layer else 3
 
@@ -444,7 +448,9 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     t_mma = flops / (peak_tf * 1e12)
     kern = st.layer_kernels()
     src = ("awq" if st.path == "grouped" else "awq_decode") if st.awq else st.path
-    key = f"{st.path}{'-w2std' if getattr(st, 'w2_standard', False) else ''}:{wl.name}"
+    # the opt-in kernels replace some paths' kernels: their counters are keyed apart
+    key = (f"{st.path}{'-w2std' if getattr(st, 'w2_standard', False) else ''}"
+           f"{'-cand' if getattr(st, 'cand', False) else ''}:{wl.name}")
     traffic = committed_traffic(key, decode_src_hash(src))
     if t_mma > t_hbm:
         ach = flops / sec / 1e12 / world
@@ -609,15 +615,15 @@ def run_ours(args, rank, world, device):
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
                    "path": ("expert-centric grouped AWQ, blocks of at most 16 rows (align + one kernel for both "
                             "GEMMs on mma.sync over the raw 4-bit codes, zero folded out in FP32 + combine, b=%d)"
-                            % st.b if st.awq and st.path == "grouped" and st.b <= 16 else
+                            % st.b if st.awq and st.path == "grouped" and st.b <= 16 and st.cand else
                             "expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
                             "dequantized into tensor memory + combine, b=%d)" % st.b
                             if st.awq and st.path == "grouped" else
                             ("single-token AWQ decode: gate/up + SwiGLU + down in one kernel, f16 mma.sync dot "
-                             "products on raw 4-bit codes, zero folded in FP32, fixed routing") if st.awq and wl.M == 1 else
+                             "products on raw 4-bit codes, zero folded in FP32, fixed routing") if st.awq and wl.M == 1 and st.cand else
                             ("small-batch AWQ decode (alignment into blocks of 16 + one kernel for both GEMMs on "
                              "mma.sync over the raw 4-bit codes + combine, fixed routing)")
-                            if st.awq and 2 <= wl.M <= 64 else
+                            if st.awq and 2 <= wl.M <= 64 and st.cand else
                             "output-centric AWQ decode (gate/up + down on CUDA cores, fixed routing)" if st.awq else
                             "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
                             % st.b if st.path == "grouped" else
@@ -628,7 +634,7 @@ def run_ours(args, rank, world, device):
                             "single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
                             else ("small-batch decode on the standard W2 layout (topk + alignment into blocks of 16 "
                                   "+ one kernel for both GEMMs on mma.sync + combine)")
-                            if st.w2_standard and 2 <= wl.M <= 64
+                            if st.w2_standard and 2 <= wl.M <= 64 and st.cand
                             else "output-centric decode (topk + gate/up + down)") + ", CUDA graph",
                    "l2": "flushed between timed steps (512 MiB write, outside the timed interval)",
                    "parallelism": f"replicas x{world}"},

@@ -91,6 +91,19 @@ typedef struct {
 const char *moe_status_string(moe_status_t s);
 /* MOE_FFN_ABI_VERSION of the loaded library. */
 int32_t moe_abi_version(void);
+/* Opt-in kernels.  Five kernels are built but taken by dispatch only on
+ * request: for MOE_W_MXFP8 on the standard layout, the one-kernel path for
+ * M == 1 (moe_ffn_decode and moe_ffn_decode_logits) and the aligned
+ * small-batch path for 2 <= M <= 64 (moe_ffn_decode); for MOE_W_AWQ4, the
+ * one-kernel path for M == 1 and the aligned small-batch path for
+ * 2 <= M <= 64 (moe_ffn_decode), and the kernel for blocks of b <= 16 rows
+ * (moe_ffn_grouped).  The request is the environment variable
+ * MOE_FFN_CANDIDATE_KERNELS set to exactly "1"; the library reads it once,
+ * at its first dispatch, and keeps the answer for the life of the process.
+ * Without it the same calls, with the same arguments, workspace sizes and
+ * tolerances, run the other kernels listed for each case below.  Returns 1
+ * when the opt-in kernels are taken, else 0. */
+int32_t moe_candidate_kernels_enabled(void);
 
 /* ---------------------------------------------------------------- routing
  * Top-k softmax routing ("Warp decode", section on the conventional MoE
@@ -166,19 +179,21 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  *            multiple of the grid size (after a call that reports
  *            MOE_ERR_TIMEOUT they must be zeroed again)
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
- * Kernels by case: MOE_W_MXFP8 (standard layout) with M == 1 -> one kernel
+ * Kernels by case (cases marked [opt-in] are taken only when
+ * moe_candidate_kernels_enabled() is 1): MOE_W_MXFP8 (standard layout) with
+ * M == 1 [opt-in] -> one kernel
  * (gate/up dots on mma.sync with each E4M3 pair converted exactly to f16 and
  * the E8M0 scale applied per 32-value block in FP32, a grid-wide barrier
  * whose counter lives in ws[0..8), then the down projection from W2 rows
  * staged in shared memory; with moe_ffn_decode_logits the routing runs in
  * it too), when its shared-memory plan fits;
- * MOE_W_MXFP8 (standard layout) with 2 <= M <= 64 -> the routes aligned
+ * MOE_W_MXFP8 (standard layout) with 2 <= M <= 64 [opt-in] -> the routes aligned
  * into blocks of 16 rows per expert (moe_align_block_size, which counts the
  * invalid routes), one kernel for both GEMMs (mma.sync, each block one
  * M-tile, x and h unquantized as above, per-block hand-off counters), and
  * the slot-ordered combine; ws then holds that alignment, the gate/up values
  * and the per-route down rows (moe_ffn_decode_workspace_size);
- * MOE_W_AWQ4 with 2 <= M <= 64 -> the same chain with the small-block AWQ
+ * MOE_W_AWQ4 with 2 <= M <= 64 [opt-in] -> the same chain with the small-block AWQ
  * kernel of moe_ffn_grouped (raw 4-bit codes as f16, zero and scale applied
  * in FP32 per group, x and h unquantized);
  * w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
@@ -188,8 +203,8 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  * MOE_W_MXFP8_T cases -> one streaming pass (gate/up rows and down columns of
  * each neuron together, per-SM partial outputs) plus a fixed-order reduction
  * kernel; MXFP8 with M*k <= 512 -> a gate/up kernel and a
- * down kernel chained by programmatic dependent launch; AWQ4 with M == 1 ->
- * one kernel (gate/up dots on f16 mma.sync over the raw 4-bit codes with the
+ * down kernel chained by programmatic dependent launch; AWQ4 with M == 1
+ * [opt-in] -> one kernel (gate/up dots on f16 mma.sync over the raw 4-bit codes with the
  * zero folded out in FP32, a grid-wide barrier whose counter lives in
  * ws[0..8), then the down projection), when its shared-memory plan fits;
  * otherwise one warp per intermediate / output scalar.  Every output's summation order is fixed
@@ -211,7 +226,8 @@ moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
  * "Warp decode" (section on the conventional MoE path: route, then the
  * experts): for a single token (M == 1) on the single-pass layout
  * (w2 MOE_W_MXFP8_T, d in {1024, 2048}, E <= 512) it is one kernel that
- * routes the token itself in every CTA; otherwise it launches the two calls.
+ * routes the token itself in every CTA (on the standard layout too when
+ * moe_candidate_kernels_enabled() is 1); otherwise it launches the two calls.
  *   logits   fp32 [M][E] router logits, E = w13->E
  *   topk_ids int32 [M][k], topk_w fp32 [M][k]: outputs (the routing used)
  *   other arguments and the workspace contract as moe_ffn_decode. */
@@ -274,7 +290,7 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
  *   and b <= 112 when d > 8064 (MOE_ERR_UNSUPPORTED); scale and zero arrays
  *   16-byte aligned (MOE_ERR_INVALID_ARG).
  *   Blocks of b <= 16 rows take a different kernel when its shared-memory
- *   plan fits (d and I up to about 3.5K): each block is one M-tile of
+ *   plan fits and moe_candidate_kernels_enabled() is 1 (d and I up to about 3.5K): each block is one M-tile of
  *   mma.sync m16n8k16 (f16 x f16, FP32 accumulate) whose B operand is the raw
  *   4-bit codes as f16 (1024 + q); the zero, the offset and the scale are
  *   applied in FP32 once per group of 128, x and h enter as f16 after an

@@ -11,6 +11,7 @@ from __future__ import annotations
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -27,6 +28,13 @@ def need_gpu():
     if not torch.cuda.is_available():
         raise RuntimeError("GPU test run without a CUDA device")
     moe.lib()
+
+
+def need_candidates():
+    """Skip a test of an opt-in kernel's own behaviour unless the library
+    takes the opt-in kernels (MOE_FFN_CANDIDATE_KERNELS=1)."""
+    if not moe.moe_candidate_kernels_enabled():
+        pytest.skip("opt-in kernels not requested (MOE_FFN_CANDIDATE_KERNELS=1)")
 
 
 def bf16_half_ulp(v: np.ndarray) -> np.ndarray:

@@ -145,3 +145,18 @@ def test_python_layout_helper_matches_library():
         assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) >= L["total"]
         awq = _r256(cap_rows * d * 2) + _r256(cap_rows * I * 2) + _r256(M * k * d * 4) + _r256(cap_rows // b * 4)
         assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(L["total"], awq)
+
+
+@pytest.mark.parametrize("value,expect", [(None, 0), ("1", 1), ("0", 0), ("yes", 0)])
+def test_candidate_kernel_switch(L, value, expect):
+    """The opt-in kernels are taken only when MOE_FFN_CANDIDATE_KERNELS is
+    exactly "1"; the library reads it once per process (a fresh process per
+    case here)."""
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k != "MOE_FFN_CANDIDATE_KERNELS"}
+    if value is not None:
+        env["MOE_FFN_CANDIDATE_KERNELS"] = value
+    code = "import top_moe_expert_gb300 as m; print(m.moe_candidate_kernels_enabled())"
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, check=True)
+    assert out.stdout.strip() == str(bool(expect))

@@ -179,8 +179,11 @@ def test_mx_single_token_activation_scales_routes_and_counter():
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
     gs.assert_layer_close(ys[0], oracle_decode(layer, x, ids2, w))
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert ws[:8].view(torch.int64).item() == 3 * sms
+    if moe.moe_candidate_kernels_enabled():
+        # the one-kernel path: each call adds one arrival per CTA (one CTA
+        # per SM) to the grid-barrier counter in ws[0..8)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert ws[:8].view(torch.int64).item() == 3 * sms
 
 
 # ---- one token, 4-bit AWQ: the single-kernel path (gate/up, SwiGLU, down)
@@ -244,9 +247,11 @@ def test_awq_single_token_routes_repeats_and_barrier_counter():
     for y in ys[1:]:
         assert torch.equal(y, ys[0])                              # repeats are bit-identical
     gs.assert_layer_close(ys[0], oracle_awq(layer, x, ids, w))
-    # each call adds one arrival per CTA (one CTA per SM) to the counter in ws[0..8)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert ws[:8].view(torch.int64).item() == 3 * sms
+    if moe.moe_candidate_kernels_enabled():
+        # the one-kernel path: each call adds one arrival per CTA (one CTA
+        # per SM) to the grid-barrier counter in ws[0..8)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert ws[:8].view(torch.int64).item() == 3 * sms
     # no valid route: y = 0
     y0 = run_awq(layer, x, np.array([[-1, wl.E, 99, -5]], dtype=np.int32), w, ws=ws)
     torch.cuda.synchronize()

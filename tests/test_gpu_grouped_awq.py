@@ -95,6 +95,7 @@ def test_awq_grouped_small(xdt, b):
 
 def test_awq_grouped_small_blocks_any_multiple_of_128():
     """The b <= 16 path takes d and I that are multiples of 128 but not 256."""
+    gs.need_candidates()
     wl = inputs.Workload("awq_grouped_1152", M=9, d=1152, I=384, E=8, k=3, fmt="awq4", seed=4)
     layer = gs.AwqLayer(wl)
     x = inputs.activations(wl, dtype=torch.float16)

@@ -49,6 +49,7 @@ _I32, _I64, _P, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_
 _PROTOS = {
     "moe_status_string": (ctypes.c_char_p, [_I32]),
     "moe_abi_version": (_I32, []),
+    "moe_candidate_kernels_enabled": (_I32, []),
     "moe_topk_softmax": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "moe_align_capacity": (_I32, [_I32, _I32, _I32, _I32, _P, _P]),
     "moe_align_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
@@ -254,6 +255,13 @@ def moe_topk_softmax(logits: torch.Tensor, k: int, topk_ids=None, topk_w=None, s
 
 
 # ---------------------------------------------------------------- alignment
+
+def moe_candidate_kernels_enabled() -> bool:
+    """Whether the library dispatches to its opt-in kernels (the environment
+    variable MOE_FFN_CANDIDATE_KERNELS=1, read once when the library first
+    dispatches)."""
+    return bool(lib().moe_candidate_kernels_enabled())
+
 
 def moe_align_capacity(M: int, k: int, E: int, b: int):
     cr, cb = ctypes.c_int32(), ctypes.c_int32()

@@ -422,17 +422,18 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         return MOE_ERR_WORKSPACE;
     float *h = static_cast<float *>(ws);
     cudaStream_t s = as_stream(stream);
-    if (fmt == MOE_W_AWQ4 && decode_awq_small_eligible(M, k, d, I, w13->E)) {
+    const bool cand = candidate_kernels_enabled();
+    if (cand && fmt == MOE_W_AWQ4 && decode_awq_small_eligible(M, k, d, I, w13->E)) {
         // a small batch: aligned blocks of 16 rows, one kernel for both GEMMs, combine
         const moe_status_t st3 = decode_awq_small_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k,
                                                          w13, w2, y, ydt == MOE_FP32, ws, ws_bytes, dev_status, s);
         if (st3 != MOE_ERR_UNSUPPORTED)
             return st3;
     }
-    if (fmt == MOE_W_AWQ4 && decode_awq_m1_eligible(M, k, d, I, w13->E))
+    if (cand && fmt == MOE_W_AWQ4 && decode_awq_m1_eligible(M, k, d, I, w13->E))
         return decode_awq_m1_launch(x, xdt == MOE_BF16, topk_ids, topk_w, k, d, I, w13->E, w13->q, w13->scale,
                                     w13->zero, w2->q, w2->scale, w2->zero, y, ydt == MOE_FP32, ws, dev_status, s);
-    if (fmt == MOE_W_MXFP8 && decode_mx_m1_eligible(M, k, d, I, w13->E) && aligned(w2->q, 16)) {
+    if (cand && fmt == MOE_W_MXFP8 && decode_mx_m1_eligible(M, k, d, I, w13->E) && aligned(w2->q, 16)) {
         // one token on the standard layout: one kernel (gate/up, SwiGLU, down)
         const moe_status_t st1 = decode_mx_m1_launch(
             static_cast<const __nv_bfloat16 *>(x), d, I, w13->E, topk_ids, topk_w, nullptr, nullptr, nullptr, k,
@@ -442,7 +443,7 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         if (st1 != MOE_ERR_UNSUPPORTED)
             return st1;
     }
-    if (fmt == MOE_W_MXFP8 && decode_mx_small_eligible(M, k, d, I, w13->E)) {
+    if (cand && fmt == MOE_W_MXFP8 && decode_mx_small_eligible(M, k, d, I, w13->E)) {
         // a small batch on the standard layout: aligned blocks, one kernel for both GEMMs, combine
         const moe_status_t st2 = decode_mx_small_launch(
             static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
@@ -503,7 +504,7 @@ MOE_API moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, i
                                 as_stream(stream));
     }
     // one token on the standard layout: one kernel with the routing inside
-    if (M == 1 && w2->fmt == MOE_W_MXFP8 && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
+    if (candidate_kernels_enabled() && M == 1 && w2->fmt == MOE_W_MXFP8 && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
         (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
         check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_mx_m1_eligible(1, k, d, I, E) && E >= k &&
         E <= 512 && aligned(w2->q, 16) && x && y && aligned(x, 16)) {

@@ -742,7 +742,7 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows, &need);
         if (!ws || ws_bytes < need || !aligned(ws, 256))
             return MOE_ERR_WORKSPACE;
-        if (grouped_awq_mma_eligible(b, d, I))
+        if (candidate_kernels_enabled() && grouped_awq_mma_eligible(b, d, I))
             return grouped_awq_mma_launch(x, xdt == MOE_BF16, M, d, I, E, topk_ids, topk_w, k, w13, w2,
                                           sorted_route_ids, expert_ids, num_rows_post_pad, b, cap_rows, y,
                                           ydt == MOE_FP32, ws, dev_status, as_stream(stream));
