@@ -485,10 +485,15 @@ def gather_replicas(times, sizes, world, device=None):
 def run_ours(args, rank, world, device):
     wl = workload_from_name(args.workload)
     K, W = args.steps, args.warmup
-    # measured crossover at d=2048, I=768, E=128, k=8: the output-centric path
-    # wins for a single token, the grouped path from M = 4 on
-    path = args.path if args.path != "auto" else ("decode" if wl.M <= 2 else "grouped")
-    st = DecodeStep(wl, K + W, device, path, args.block, args.w2)
+    path, block = args.path, args.block
+    if path == "auto":
+        # the library's choice at the measured crossover of the two paths
+        import top_moe_expert_gb300 as moe
+        fmt = moe.MOE_W_AWQ4 if wl.fmt == "awq4" else moe.MOE_W_MXFP8
+        p, b = moe.moe_ffn_select_path(wl.M, wl.k, wl.E, wl.d, wl.I, fmt)
+        path = "decode" if p == moe.MOE_PATH_DECODE else "grouped"
+        block = block or b
+    st = DecodeStep(wl, K + W, device, path, block, args.w2)
     st.capture()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     s = st.stream

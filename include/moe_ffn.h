@@ -77,6 +77,7 @@ typedef enum {
 
 typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1, MOE_W_MXFP8_T = 2 } moe_wfmt_t;
 typedef enum { MOE_BF16 = 0, MOE_FP16 = 1, MOE_FP32 = 2 } moe_dtype_t;
+typedef enum { MOE_PATH_DECODE = 0, MOE_PATH_GROUPED = 1 } moe_path_t;
 
 /* One projection of all experts; see "Weight formats" above. */
 typedef struct {
@@ -319,6 +320,30 @@ moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d,
                              const int32_t *num_rows_post_pad, int32_t b, int32_t cap_rows,
                              void *y, int32_t ydt, void *ws, size_t ws_bytes,
                              int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------- path selection
+ * Which of the two paths to run for a batch ("Warp decode", sections on
+ * what changed and on hardware efficiency: the output-centric path for few
+ * tokens, the expert-centric grouped path for large batches), at the
+ * crossover measured on GB300 at d = 2048, I = 768, E = 128, k = 8:
+ *   MOE_W_MXFP8: MOE_PATH_DECODE for M <= 2, else MOE_PATH_GROUPED
+ *                (decode 23.8 us against grouped 220 us at M = 1; grouped
+ *                53.5 against 76.5 us at M = 4 and faster at every larger M);
+ *   MOE_W_AWQ4:  MOE_PATH_GROUPED (43.4 against 43.9 us at M = 1, 62.6
+ *                against 396 us at M = 21).
+ * When the preferred path does not take the shape (the limits of
+ * moe_ffn_decode and moe_ffn_grouped on d, I and k), the other one is
+ * returned; when neither does, MOE_ERR_UNSUPPORTED.
+ *   fmt    MOE_W_MXFP8 or MOE_W_AWQ4 (MOE_ERR_UNSUPPORTED otherwise)
+ *   path   out: a moe_path_t
+ *   block  out: the block size b for moe_align_block_size and
+ *          moe_ffn_grouped when the path is grouped (twice the expected
+ *          rows per expert, 2*M*k/E, rounded up to a power of two within
+ *          [16, 128] for MXFP8 and [8, 128] for AWQ, at most 64 for AWQ
+ *          with d > 8064), else 0.
+ * Host only; launches nothing. */
+moe_status_t moe_ffn_select_path(int32_t M, int32_t k, int32_t E, int32_t d, int32_t I, int32_t fmt,
+                                 int32_t *path, int32_t *block);
 
 /* ------------------------------------------------ allocation-free decode
  * No counterpart on the pages: a convenience for callers that cannot hand

@@ -160,3 +160,31 @@ def test_candidate_kernel_switch(L, value, expect):
     code = "import top_moe_expert_gb300 as m; print(m.moe_candidate_kernels_enabled())"
     out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, check=True)
     assert out.stdout.strip() == str(bool(expect))
+
+
+def test_select_path_at_the_measured_crossover(L):
+    """Path choice (host only): MXFP8 takes the output-centric path up to two
+    tokens and the grouped path from there; 4-bit AWQ takes the grouped
+    path.  The block size is twice the expected rows per expert rounded up
+    to a power of two within the format's range."""
+    D, G = moe.MOE_PATH_DECODE, moe.MOE_PATH_GROUPED
+    mx, awq = moe.MOE_W_MXFP8, moe.MOE_W_AWQ4
+    sel = lambda M, fmt=mx, k=8, E=128, d=2048, I=768: moe.moe_ffn_select_path(M, k, E, d, I, fmt)
+    assert sel(1) == (D, 0) and sel(2) == (D, 0)
+    # 2*M*k/E rows per expert: 0.5 .. 64 -> 16 up to 64; 128 caps
+    assert [sel(M) for M in (3, 4, 64, 256, 512, 16384)] == [(G, 16), (G, 16), (G, 16), (G, 32), (G, 64), (G, 128)]
+    assert sel(0) == (D, 0)                                  # an empty batch: the cheap path
+    # AWQ: grouped at every M; fixture A (M=21, k=8, E=128) gets b = 8
+    assert sel(1, awq) == (G, 8) and sel(21, awq) == (G, 8) and sel(512, awq) == (G, 64)
+    # shapes one path does not take go to the other
+    assert sel(1, d=1152, I=384) == (G, 16)                  # decode needs d % 512 == 0
+    assert sel(64, d=1536, I=96) == (D, 0)                   # grouped needs I % 128 == 0
+    assert sel(21, awq, d=9216, I=256) == (D, 0)             # AWQ grouped: d / 128 <= 64
+    assert sel(21, awq, d=3072, I=256) == (G, 8)
+    with pytest.raises(moe.MoeError) as err:
+        sel(4, d=1152, I=96)                                 # neither path
+    assert err.value.status == 2
+    with pytest.raises(moe.MoeError):
+        sel(21, awq, d=1152, I=256)                          # AWQ: neither (d % 256, d % 1024)
+    with pytest.raises(moe.MoeError):
+        moe.moe_ffn_select_path(4, 8, 128, 2048, 768, moe.MOE_W_MXFP8_T)

@@ -26,6 +26,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 6: "MOE_ERR_TIMEOUT"}
 MOE_W_MXFP8, MOE_W_AWQ4, MOE_W_MXFP8_T = 0, 1, 2
 MOE_BF16, MOE_FP16, MOE_FP32 = 0, 1, 2
+MOE_PATH_DECODE, MOE_PATH_GROUPED = 0, 1
 
 _DT = {torch.bfloat16: MOE_BF16, torch.float16: MOE_FP16, torch.float32: MOE_FP32}
 
@@ -50,6 +51,7 @@ _PROTOS = {
     "moe_status_string": (ctypes.c_char_p, [_I32]),
     "moe_abi_version": (_I32, []),
     "moe_candidate_kernels_enabled": (_I32, []),
+    "moe_ffn_select_path": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_topk_softmax": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "moe_align_capacity": (_I32, [_I32, _I32, _I32, _I32, _P, _P]),
     "moe_align_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
@@ -255,6 +257,15 @@ def moe_topk_softmax(logits: torch.Tensor, k: int, topk_ids=None, topk_w=None, s
 
 
 # ---------------------------------------------------------------- alignment
+
+def moe_ffn_select_path(M: int, k: int, E: int, d: int, I: int, fmt: int = None):
+    """(path, b): MOE_PATH_DECODE with b = 0, or MOE_PATH_GROUPED with the
+    block size for alignment, at the measured crossover of the two paths."""
+    fmt = MOE_W_MXFP8 if fmt is None else fmt
+    p, b = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().moe_ffn_select_path(M, k, E, d, I, fmt, ctypes.byref(p), ctypes.byref(b)), "moe_ffn_select_path")
+    return p.value, b.value
+
 
 def moe_candidate_kernels_enabled() -> bool:
     """Whether the library dispatches to its opt-in kernels (the environment
