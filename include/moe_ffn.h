@@ -178,7 +178,10 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  *            it (e.g. cudaMemset once) and then left alone: they hold a
  *            grid-barrier arrival counter that every call advances by a
  *            multiple of the grid size (after a call that reports
- *            MOE_ERR_TIMEOUT they must be zeroed again)
+ *            MOE_ERR_TIMEOUT they must be zeroed again).  Every other
+ *            path keeps its data after these 256 bytes, so one workspace
+ *            sized for the largest batch serves calls of any batch size
+ *            and layout in turn.
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
  * Kernels by case (cases marked [opt-in] are taken only when
  * moe_candidate_kernels_enabled() is 1): MOE_W_MXFP8 (standard layout) with
@@ -192,8 +195,9 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  * into blocks of 16 rows per expert (moe_align_block_size, which counts the
  * invalid routes), one kernel for both GEMMs (mma.sync, each block one
  * M-tile, x and h unquantized as above, per-block hand-off counters), and
- * the slot-ordered combine; ws then holds that alignment, the gate/up values
- * and the per-route down rows (moe_ffn_decode_workspace_size);
+ * the slot-ordered combine; ws past its first 256 bytes then holds that
+ * alignment, the gate/up values and the per-route down rows
+ * (moe_ffn_decode_workspace_size);
  * MOE_W_AWQ4 with 2 <= M <= 64 [opt-in] -> the same chain with the small-block AWQ
  * kernel of moe_ffn_grouped (raw 4-bit codes as f16, zero and scale applied
  * in FP32 per group, x and h unquantized);

@@ -58,9 +58,10 @@ def test_align_capacity_bound():
 
 def test_decode_workspace_size():
     _r256 = lambda n: (n + 255) // 256 * 256
-    # h [M*k][I] f32 (the two-kernel paths); d % 1024 != 0 rules out the
+    # 256 reserved bytes (the single-token paths' barrier counter), then h
+    # [M*k][I] f32 (the two-kernel paths); d % 1024 != 0 rules out the
     # single-pass path and its per-SM partial outputs
-    assert moe.moe_ffn_decode_workspace_size(65, 8, 512, 768) == 65 * 8 * 768 * 4
+    assert moe.moe_ffn_decode_workspace_size(65, 8, 512, 768) == 256 + 65 * 8 * 768 * 4
     # one token: the single-kernel MXFP8 path's barrier counter (256 B) and
     # phase-1 pieces [k * 2I / 8][4][8] f32
     assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 256 + 8 * (2 * 768 // 8) * 4 * 8 * 4
@@ -72,7 +73,7 @@ def test_decode_workspace_size():
         cap_rows = mk * 16
         small = (_r256(cap_rows * 4) + _r256(mk * 4) + 256 + _r256(mk * 4) + _r256(mk * 2 * I * 4)
                  + _r256(mk * d * 4))
-        assert moe.moe_ffn_decode_workspace_size(M, k, d, I) == max(small, mk * I * 4)
+        assert moe.moe_ffn_decode_workspace_size(M, k, d, I) == 256 + max(small, mk * I * 4)
     # one token, d % 1024 == 0: at least the single-token AWQ kernel's barrier
     # counter (256 B) and its phase-1 pieces [k * 2I / 8][4][8] f32
     assert moe.moe_ffn_decode_workspace_size(1, 8, 2048, 768) >= 256 + 8 * (2 * 768 // 8) * 4 * 8 * 4

@@ -323,6 +323,32 @@ def test_fused_decode_duplicates_invalid_bf16_and_repeatability():
     gs.assert_layer_close(run_fused(layer, x1, ids1, w1, torch.float32), oracle_decode(layer, x1, ids1, w1))
 
 
+def test_one_workspace_serves_every_batch_size():
+    """One workspace, sized for the largest batch, reused by calls of other
+    batch sizes and both W2 layouts in turn: every output equals the one
+    computed with a fresh workspace, and the grid-barrier counter in
+    ws[0..8) holds exactly one arrival per CTA for each call of a one-kernel
+    single-token path (the other paths keep their data past ws[256])."""
+    layer = _fused_layer(5)
+    wl = dataclasses.replace(inputs.DECODE, name="ws_reuse_m8", M=8, seed=7)
+    x = inputs.activations(wl)
+    ids, w = gs.routing(wl)
+    ws = torch.zeros(max(moe.moe_ffn_decode_workspace_size(M, wl.k, wl.d, wl.I) for M in (1, 3, 4, 8)),
+                     dtype=torch.uint8, device="cuda")
+    calls = [(1, True), (3, True), (8, False), (1, True), (4, False), (1, False), (1, True)]
+    for M, neuron_major in calls:
+        run = run_fused if neuron_major else run_decode
+        args = (layer, x[:M], ids[:M], w[:M], torch.float32)
+        fresh = run(*args)
+        assert torch.equal(run(*args, ws=ws), fresh), (M, neuron_major)
+    torch.cuda.synchronize()
+    # one-kernel single-token calls: the neuron-major layout always, the
+    # standard layout with the opt-in kernels
+    n_one_kernel = sum(1 for M, nm in calls if M == 1 and (nm or moe.moe_candidate_kernels_enabled()))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ws[:8].view(torch.int64).item() == n_one_kernel * sms
+
+
 def test_fused_decode_large_expert_m1():
     wl = inputs.LARGE_M1
     ids, w = gs.routing(wl)

@@ -317,8 +317,12 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
 {
     if (M < 0 || k < 1 || d < 1 || I < 1 || !bytes)
         return MOE_ERR_INVALID_ARG;
-    size_t h = ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
-    size_t part = (M <= 4 && d % 1024 == 0) ? decode_fused_workspace(M, d) : 0;
+    // The first kWsReserved bytes hold the grid-barrier counter of the
+    // one-kernel single-token paths (ws[0..8)).  Every other path starts its
+    // data after them, so one workspace serves calls of any batch size in
+    // turn without disturbing the counter.
+    size_t h = kWsReserved + ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
+    size_t part = (M <= 4 && d % 1024 == 0) ? kWsReserved + decode_fused_workspace(M, d) : 0;
     if (M == 1 && (d == 1024 || d == 2048)) {
         const size_t m1 = decode_m1_workspace(d);
         part = part > m1 ? part : m1;
@@ -333,7 +337,7 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
     }
     if (M >= 2 && M <= 64 && k <= 32 && d % 64 == 0 && I % 64 == 0) {
         // the alignment capacity is largest when every route has its own expert
-        const size_t xs = decode_mx_small_workspace(M, k, d, I, M * k);
+        const size_t xs = kWsReserved + decode_mx_small_workspace(M, k, d, I, M * k);
         part = part > xs ? part : xs;
     }
     *bytes = h > part ? h : part;
@@ -395,7 +399,8 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         return decode_fused_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
                                    static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
                                    static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y,
-                                   ydt == MOE_FP32, static_cast<float *>(ws), dev_status, as_stream(stream));
+                                   ydt == MOE_FP32, reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWsReserved),
+                                   dev_status, as_stream(stream));
     }
     if (w13->fmt != w2->fmt)
         return MOE_ERR_INVALID_ARG;
@@ -420,13 +425,18 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     moe_ffn_decode_workspace_size(M, k, d, I, &need);
     if (!ws || ws_bytes < need || !aligned(ws, 256))
         return MOE_ERR_WORKSPACE;
-    float *h = static_cast<float *>(ws);
+    // past the reserved bytes: h of the two-kernel and per-scalar paths, the
+    // data of the small-batch paths
+    void *ws_data = static_cast<uint8_t *>(ws) + kWsReserved;
+    const size_t ws_data_bytes = ws_bytes - kWsReserved;
+    float *h = static_cast<float *>(ws_data);
     cudaStream_t s = as_stream(stream);
     const bool cand = candidate_kernels_enabled();
     if (cand && fmt == MOE_W_AWQ4 && decode_awq_small_eligible(M, k, d, I, w13->E)) {
         // a small batch: aligned blocks of 16 rows, one kernel for both GEMMs, combine
         const moe_status_t st3 = decode_awq_small_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k,
-                                                         w13, w2, y, ydt == MOE_FP32, ws, ws_bytes, dev_status, s);
+                                                         w13, w2, y, ydt == MOE_FP32, ws_data, ws_data_bytes,
+                                                         dev_status, s);
         if (st3 != MOE_ERR_UNSUPPORTED)
             return st3;
     }
@@ -448,8 +458,8 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         const moe_status_t st2 = decode_mx_small_launch(
             static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
             static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
-            static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws,
-            ws_bytes, dev_status, s);
+            static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws_data,
+            ws_data_bytes, dev_status, s);
         if (st2 != MOE_ERR_UNSUPPORTED)
             return st2;
     }

@@ -11,6 +11,11 @@
 
 namespace moe {
 
+// Bytes at the start of a decode workspace reserved for the grid-barrier
+// counter of the one-kernel single-token paths; the other decode paths place
+// their data after them.
+constexpr size_t kWsReserved = 256;
+
 bool decode_stream_eligible(int M, int k, int d, int I, int E, const void *q13, const void *s13,
                             const void *q2, const void *s2);
 
