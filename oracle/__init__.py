@@ -58,6 +58,8 @@ class _Weights(ctypes.Structure):
         ("q8", ctypes.c_void_p), ("s8", ctypes.c_void_p),
         ("q4", ctypes.c_void_p), ("s16", ctypes.c_void_p), ("z4", ctypes.c_void_p),
         ("slot", ctypes.c_void_p),
+        ("v4", ctypes.c_void_p), ("m4", ctypes.c_void_p), ("sc8", ctypes.c_void_p),
+        ("alpha", ctypes.c_void_p),
     ]
 
 
@@ -78,6 +80,17 @@ def _load():
             lib.orc_mxfp8_quantize.restype = None
             lib.orc_mxfp8_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                                ctypes.c_void_p, ctypes.c_void_p]
+            lib.orc_e2m1_value.restype = ctypes.c_double
+            lib.orc_e2m1_value.argtypes = [ctypes.c_uint8]
+            lib.orc_ue4m3_value.restype = ctypes.c_double
+            lib.orc_ue4m3_value.argtypes = [ctypes.c_uint8]
+            lib.orc_pair_pattern.restype = ctypes.c_int
+            lib.orc_pair_pattern.argtypes = [ctypes.c_uint8, ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_int)]
+            lib.orc_nvfp4s_quantize.restype = None
+            lib.orc_nvfp4s_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p]
             lib.orc_topk_softmax.restype = None
             lib.orc_topk_softmax.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                                              ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
@@ -146,6 +159,54 @@ def bf16_value(bits) -> np.ndarray:
     b = np.asarray(bits, dtype=np.uint16)
     table = np.array([lib.orc_bf16_value(i) for i in range(65536)], dtype=np.float64)
     return table[b]
+
+
+def e2m1_value(codes) -> np.ndarray:
+    """Exact value of FP4 E2M1 codes (low nibble) [SQ App. A, Figure 3]."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    table = np.array([lib.orc_e2m1_value(i & 0xF) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def ue4m3_value(codes) -> np.ndarray:
+    """Exact value of UE4M3 scale codes (NaN for 0x7F and codes >= 0x80)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    table = np.array([lib.orc_ue4m3_value(i) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def pair_pattern(nibble: int):
+    """(p0, p1), the kept pair indices of a paired 4:8 metadata nibble, or
+    None when the nibble is not one of the six patterns."""
+    a, b = ctypes.c_int(), ctypes.c_int()
+    return (a.value, b.value) if _load().orc_pair_pattern(nibble, ctypes.byref(a), ctypes.byref(b)) else None
+
+
+def nvfp4s_quantize(W) -> dict:
+    """Paired 4:8 sparse NVFP4 packing of W [N, K] (K % 32 == 0) [SQ App. A,
+    Eq. 5-7]: {"v": [N, K/4] kept E2M1 codes, "m": [N, K/16] pattern nibbles,
+    "s": [N, K/32] UE4M3 codes, "alpha": float32 per-matrix constant}."""
+    lib = _load()
+    W = np.ascontiguousarray(W, dtype=np.float64)
+    N, K = W.shape
+    assert K % 32 == 0
+    v = np.empty((N, K // 4), dtype=np.uint8)
+    m = np.empty((N, K // 16), dtype=np.uint8)
+    sc = np.empty((N, K // 32), dtype=np.uint8)
+    alpha = np.empty(1, dtype=np.float32)
+    lib.orc_nvfp4s_quantize(_ptr(W), N, K, _ptr(v), _ptr(m), _ptr(sc), _ptr(alpha))
+    return {"v": v, "m": m, "s": sc, "alpha": alpha[0]}
+
+
+def nvfp4s_quantize_3d(W) -> dict:
+    """nvfp4s_quantize of each expert's matrix of W [E, N, K]; the format
+    dict the layer takes ({"fmt": "nvfp4s", "v", "m", "s", "alpha" [E]})."""
+    parts = [nvfp4s_quantize(W[e]) for e in range(W.shape[0])]
+    return {"fmt": "nvfp4s", "v": np.stack([p["v"] for p in parts]), "m": np.stack([p["m"] for p in parts]),
+            "s": np.stack([p["s"] for p in parts]),
+            "alpha": np.array([p["alpha"] for p in parts], dtype=np.float32)}
 
 
 def mxfp8_quantize(v) -> tuple[np.ndarray, np.ndarray]:
@@ -254,6 +315,10 @@ def split_k_schedule(n_moe_blocks: int, N: int, K: int, thread_n: int, thread_k:
 # The layer
 # --------------------------------------------------------------------------
 
+# the six paired 4:8 patterns as metadata nibbles p0 | p1 << 2, p0 < p1
+_PAIR_NIBBLES = np.array([a | (b << 2) for a in range(4) for b in range(a + 1, 4)], dtype=np.uint8)
+
+
 def _weights_struct(w: dict, E: int, keep: list):
     st = _Weights()
     fmt = w["fmt"]
@@ -273,6 +338,19 @@ def _weights_struct(w: dict, E: int, keep: list):
         assert s.shape == (S, N, K // 128) and z.shape == (S, N // 8, K // 128)
         st.fmt, st.q4, st.s16, st.z4 = 1, _ptr(q), _ptr(s), _ptr(z)
         keep += [q, s, z]
+    elif fmt == "nvfp4s":
+        v = np.ascontiguousarray(w["v"], dtype=np.uint8)
+        m = np.ascontiguousarray(w["m"], dtype=np.uint8)
+        sc = np.ascontiguousarray(w["s"], dtype=np.uint8)
+        alpha = np.ascontiguousarray(w["alpha"], dtype=np.float32)
+        S, N, K4 = v.shape
+        K = K4 * 4
+        assert m.shape == (S, N, K // 16) and sc.shape == (S, N, K // 32) and alpha.shape == (S,)
+        nib = np.stack([m & 0xF, m >> 4], axis=-1)
+        if not np.isin(nib, _PAIR_NIBBLES).all():
+            raise ValueError("a paired 4:8 metadata nibble is not one of the six patterns")
+        st.fmt, st.v4, st.m4, st.sc8, st.alpha = 2, _ptr(v), _ptr(m), _ptr(sc), _ptr(alpha)
+        keep += [v, m, sc, alpha]
     else:
         raise ValueError(fmt)
     st.E, st.N, st.K = E, N, K

@@ -33,6 +33,11 @@
  *     (so a negative value that rounds to zero is -0, code 0x80).
  *   - AWQ-4bit: w = (q - z) * s, q and z unsigned nibbles, s fp16, one
  *     (s, z) per group of 128 along K; plain nibble order.
+ *   - Paired 4:8 sparse NVFP4 ([SQ] App. A): per group of 8 weights along
+ *     K, two kept adjacent pairs named by a nibble p0 | p1 << 2 (p0 < p1),
+ *     four kept E2M1 codes, one UE4M3 scale per 32 weights, one binary32
+ *     constant per matrix; quantizer by Eq. 5 with the pattern chosen by
+ *     pair energy (the page chooses by learned logits).
  *   - Alignment: valid route = expert id in [0,E); order (expert, route id);
  *     pad each active expert to a multiple of b with sentinel M*k; experts
  *     with no route get no block; unused tails: sentinel rows, -1 blocks.
@@ -50,6 +55,7 @@
 
 #define ORC_MXFP8 0
 #define ORC_AWQ4 1
+#define ORC_NVFP4S 2
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
@@ -112,6 +118,46 @@ double orc_bf16_value(uint16_t h)
     else
         mag = ldexp(1.0 + (double)m / 128.0, e - 127);
     return sign ? -mag : mag;
+}
+
+/* FP4 E2M1, the value grid of [SQ] App. A, Figure 3 caption
+ * ({0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}): 1 sign bit, 2 exponent bits
+ * with bias 1, 1 mantissa bit; exponent field 0 is subnormal (m/2); every
+ * code is finite. */
+double orc_e2m1_value(uint8_t c)
+{
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 0x3;
+    int m = c & 0x1;
+    double mag = e == 0 ? (double)m / 2.0 : ldexp(1.0 + (double)m / 2.0, e - 1);
+    return sign ? -mag : mag;
+}
+
+/* UE4M3, the unsigned FP8 block scale of [SQ] App. A ("G_s contains UE4M3
+ * scales"; Figure 3 caption "UE4M3 (unsigned FP8)"): the E4M3 codes with the
+ * sign bit clear, 0x00..0x7E; 0x7F and codes with bit 7 set are not scales
+ * (NaN). */
+double orc_ue4m3_value(uint8_t c)
+{
+    if (c & 0x80)
+        return NAN;
+    return orc_e4m3_value(c);
+}
+
+/* Paired 4:8 sparsity metadata ([SQ] App. A: a group of m = 8 weights keeps
+ * two of its four adjacent pairs, six patterns; 4 bits of metadata per
+ * group, Eq. 7).  Encoding (a reading; the page fixes the count of bits, not
+ * their meaning): nibble = p0 | p1 << 2 with p0 < p1 the indices of the kept
+ * pairs (pair j = positions 2j, 2j+1 of the group).  Returns 1 and the two
+ * indices for one of the six patterns, 0 for any other nibble. */
+int orc_pair_pattern(uint8_t nib, int *p0, int *p1)
+{
+    int a = nib & 0x3, b = (nib >> 2) & 0x3;
+    if ((nib & 0xF0) || a >= b)
+        return 0;
+    *p0 = a;
+    *p1 = b;
+    return 1;
 }
 
 /* The 127 non-negative finite E4M3 values, codes 0x00..0x7E, which are in
@@ -189,6 +235,135 @@ void orc_mxfp8_quantize(const double *v, int64_t rows, int64_t K, uint8_t *q, ui
     }
 }
 
+/* Round-to-nearest-even of a non-negative finite value onto the E2M1
+ * magnitudes (codes 0..7 in increasing order of value), saturating at 6; on
+ * an exact tie the code whose mantissa bit is 0 wins. */
+static uint8_t e2m1_rne_magnitude(double a)
+{
+    int c;
+    if (a >= 6.0)
+        return 7;
+    for (c = 0; c < 7; ++c) {
+        double lo = orc_e2m1_value((uint8_t)c), hi = orc_e2m1_value((uint8_t)(c + 1));
+        if (a < hi) {
+            if (a - lo < hi - a)
+                return (uint8_t)c;
+            if (hi - a < a - lo)
+                return (uint8_t)(c + 1);
+            return (uint8_t)((c & 1) == 0 ? c : c + 1);
+        }
+    }
+    return 7;
+}
+
+/* Paired 4:8 sparse NVFP4 quantizer of one matrix W [N][K], K a multiple of
+ * 32 ([SQ] App. A feasible set, Eq. 6; block scales by Eq. 5, Sec. 3.4):
+ *  1. pattern: in every group of 8 consecutive weights along K, keep the two
+ *     adjacent pairs of largest energy (sum of squares; ties to the lower
+ *     pair index).  The page keeps the highest-logit pattern of a trained
+ *     model; without training, magnitude is the plain reading.
+ *  2. Y = W with the other pairs zeroed; amax_b = max |Y| over each block of
+ *     32 weights; gamma = 448 / (max_b amax_b / 6) (Eq. 5); an all-zero Y
+ *     takes gamma = 1.
+ *  3. alpha = 1/gamma rounded to binary32: the per-matrix constant ("UE4M3
+ *     scales up to a per-matrix constant", App. A), stored in FP32.
+ *  4. block scale code = RNE_E4M3(gamma * amax_b / 6) (at most 448 by the
+ *     choice of gamma).
+ *  5. each kept weight: E2M1 code = RNE(|y| / (alpha * UE4M3(code))),
+ *     saturating at 6, sign kept (a negative weight that rounds to zero is
+ *     code 0x8); a zero scale gives code 0.
+ * Layout: vals [N][K/4] (group g's four kept codes in bytes 2g, 2g+1, low
+ * nibble first, pair p0's two values then pair p1's), meta [N][K/16]
+ * (group g's pattern nibble in byte g/2, low nibble for even g), sc
+ * [N][K/32] UE4M3 codes, *alpha. */
+void orc_nvfp4s_quantize(const double *W, int64_t N, int64_t K, uint8_t *vals, uint8_t *meta,
+                         uint8_t *sc, float *alpha)
+{
+    int64_t n, g, b;
+    int *keep = (int *)malloc(sizeof(int) * (size_t)(N * (K / 8) * 2));
+    double ymax = 0.0, gamma, a;
+    /* 1. patterns */
+    for (n = 0; n < N; ++n)
+        for (g = 0; g < K / 8; ++g) {
+            const double *w = W + n * K + 8 * g;
+            double en[4];
+            int j, p0 = 0, p1 = 1, t;
+            for (j = 0; j < 4; ++j)
+                en[j] = w[2 * j] * w[2 * j] + w[2 * j + 1] * w[2 * j + 1];
+            /* the largest, then the largest of the rest (lower index on ties) */
+            for (j = 1; j < 4; ++j)
+                if (en[j] > en[p0])
+                    p0 = j;
+            p1 = p0 == 0 ? 1 : 0;
+            for (j = 0; j < 4; ++j)
+                if (j != p0 && en[j] > en[p1])
+                    p1 = j;
+            if (p1 < p0) {
+                t = p0;
+                p0 = p1;
+                p1 = t;
+            }
+            keep[(n * (K / 8) + g) * 2] = p0;
+            keep[(n * (K / 8) + g) * 2 + 1] = p1;
+        }
+    /* 2. block maxima of the pruned matrix, gamma */
+    for (n = 0; n < N; ++n)
+        for (g = 0; g < K / 8; ++g) {
+            int i;
+            for (i = 0; i < 4; ++i) {
+                int pj = keep[(n * (K / 8) + g) * 2 + i / 2];
+                double v = fabs(W[n * K + 8 * g + 2 * pj + i % 2]);
+                if (v > ymax)
+                    ymax = v;
+            }
+        }
+    gamma = ymax > 0.0 ? 448.0 / (ymax / 6.0) : 1.0;
+    /* 3. the per-matrix constant */
+    *alpha = (float)(1.0 / gamma);
+    a = (double)*alpha;
+    for (n = 0; n < N; ++n) {
+        for (b = 0; b < K / 32; ++b) {
+            double amax = 0.0, s;
+            uint8_t code;
+            int64_t gg;
+            for (gg = 4 * b; gg < 4 * b + 4; ++gg) {
+                int i;
+                for (i = 0; i < 4; ++i) {
+                    int pj = keep[(n * (K / 8) + gg) * 2 + i / 2];
+                    double v = fabs(W[n * K + 8 * gg + 2 * pj + i % 2]);
+                    if (v > amax)
+                        amax = v;
+                }
+            }
+            /* 4. the block's scale code */
+            code = e4m3_rne_magnitude(gamma * amax / 6.0);
+            sc[n * (K / 32) + b] = code;
+            s = a * orc_ue4m3_value(code);
+            /* 5. the kept values */
+            for (gg = 4 * b; gg < 4 * b + 4; ++gg) {
+                int p0 = keep[(n * (K / 8) + gg) * 2], p1 = keep[(n * (K / 8) + gg) * 2 + 1], i;
+                uint8_t *vb = vals + n * (K / 4) + 2 * gg;
+                uint8_t *mb = meta + n * (K / 16) + gg / 2;
+                uint8_t nib = (uint8_t)(p0 | (p1 << 2));
+                if (gg % 2 == 0)
+                    *mb = nib;
+                else
+                    *mb = (uint8_t)(*mb | (nib << 4));
+                vb[0] = vb[1] = 0;
+                for (i = 0; i < 4; ++i) {
+                    int pj = i < 2 ? p0 : p1;
+                    double y = W[n * K + 8 * gg + 2 * pj + i % 2];
+                    uint8_t c = s > 0.0 ? e2m1_rne_magnitude(fabs(y) / s) : 0;
+                    if (y < 0.0 || (y == 0.0 && signbit(y)))
+                        c = (uint8_t)(c | 0x8);
+                    vb[i / 2] = (uint8_t)(vb[i / 2] | (c << (4 * (i % 2))));
+                }
+            }
+        }
+    }
+    free(keep);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Expert weights                                                            */
 /* ------------------------------------------------------------------------ */
@@ -197,7 +372,7 @@ void orc_mxfp8_quantize(const double *v, int64_t rows, int64_t K, uint8_t *q, ui
  * the index of its slab in the arrays (NULL = identity), which lets a caller
  * hand over only the experts a routing touches; -1 = not supplied. */
 typedef struct {
-    int32_t fmt;             /* ORC_MXFP8 or ORC_AWQ4 */
+    int32_t fmt;             /* ORC_MXFP8, ORC_AWQ4 or ORC_NVFP4S */
     int32_t E;
     int64_t N, K;
     const uint8_t *q8;       /* MXFP8 codes   [slots][N][K]          */
@@ -206,6 +381,10 @@ typedef struct {
     const uint16_t *s16;     /* AWQ fp16 scale[slots][N][K/128]      */
     const int32_t *z4;       /* AWQ zeros     [slots][N/8][K/128]    */
     const int32_t *slot;     /* [E] or NULL                          */
+    const uint8_t *v4;       /* NVFP4S kept E2M1 codes [slots][N][K/4]  */
+    const uint8_t *m4;       /* NVFP4S pattern nibbles [slots][N][K/16] */
+    const uint8_t *sc8;      /* NVFP4S UE4M3 scales    [slots][N][K/32] */
+    const float *alpha;      /* NVFP4S per-matrix constant [slots]      */
 } orc_weights;
 
 static int64_t weight_slot(const orc_weights *w, int32_t e)
@@ -229,6 +408,29 @@ int orc_dequant_row(const orc_weights *w, int32_t e, int64_t n, double *out)
         const uint8_t *sr = w->s8 + (sl * w->N + n) * (w->K / 32);
         for (kk = 0; kk < w->K; ++kk)
             out[kk] = orc_e4m3_value(qr[kk]) * orc_e8m0_value(sr[kk / 32]);
+    } else if (w->fmt == ORC_NVFP4S) {
+        /* w = alpha * UE4M3(scale of the 32-block) * E2M1(code) at the kept
+         * positions of each group of 8, 0 elsewhere ([SQ] App. A, Eq. 6 and
+         * Eq. 7 storage; layout as orc_nvfp4s_quantize writes it).  A pattern
+         * nibble that is not one of the six returns -2. */
+        const uint8_t *vr = w->v4 + (sl * w->N + n) * (w->K / 4);
+        const uint8_t *mr = w->m4 + (sl * w->N + n) * (w->K / 16);
+        const uint8_t *sr = w->sc8 + (sl * w->N + n) * (w->K / 32);
+        const double a = (double)w->alpha[sl];
+        int64_t g;
+        for (kk = 0; kk < w->K; ++kk)
+            out[kk] = 0.0;
+        for (g = 0; g < w->K / 8; ++g) {
+            int p0, p1, i;
+            const double s = a * orc_ue4m3_value(sr[(8 * g) / 32]);
+            if (!orc_pair_pattern((uint8_t)((mr[g / 2] >> (4 * (g % 2))) & 0xF), &p0, &p1))
+                return -2;
+            for (i = 0; i < 4; ++i) {
+                int pj = i < 2 ? p0 : p1;
+                uint8_t c = (uint8_t)((vr[2 * g + i / 2] >> (4 * (i % 2))) & 0xF);
+                out[8 * g + 2 * pj + i % 2] = orc_e2m1_value(c) * s;
+            }
+        }
     } else {
         const int32_t *qr = w->q4 + (sl * w->N + n) * (w->K / 8);
         const uint16_t *sr = w->s16 + (sl * w->N + n) * (w->K / 128);
