@@ -50,6 +50,19 @@
  *                produced from MOE_W_MXFP8 by moe_mxfp8_transpose.  Accepted
  *                for w2 by moe_ffn_decode (its single-pass small-batch path
  *                streams each neuron's down-projection column contiguously).
+ *   MOE_W_NVFP4S: paired 4:8 sparse NVFP4 ("Hardware-Native Joint Sparse-
+ *                Quantization ...", App. A, Eq. 6 and 7): in every group of
+ *                8 weights along K two adjacent pairs are kept, 2.75 bits
+ *                per weight.  q uint8 [E][N][K/4]: group g's four kept E2M1
+ *                codes in bytes 2g, 2g+1, low nibble first, the two values
+ *                of pair p0 then those of pair p1; zero uint8 [E][N][K/16]:
+ *                group g's pattern nibble p0 | p1 << 2 (p0 < p1, the kept
+ *                pair indices) in byte g/2, low nibble for even g; scale
+ *                uint8 [E][N][K/32] UE4M3 codes (0x00..0x7E); alpha fp32
+ *                [E].  weight = alpha[e] * UE4M3(scale) * E2M1(code) at the
+ *                kept positions, 0 elsewhere.  K % 64 == 0.  A nibble that
+ *                is not one of the six patterns gives undefined values (every
+ *                read stays inside its group).
  *   W13 is the fused gate/up projection: N = 2I (rows 0..I-1 gate, rows
  *   I..2I-1 up), K = d.  W2 is the down projection: N = d, K = I.
  */
@@ -63,7 +76,7 @@
 extern "C" {
 #endif
 
-#define MOE_FFN_ABI_VERSION 1
+#define MOE_FFN_ABI_VERSION 2
 
 typedef enum {
     MOE_OK = 0,
@@ -75,7 +88,7 @@ typedef enum {
     MOE_ERR_TIMEOUT = 6       /* a bounded device wait expired (dev_status[1]) */
 } moe_status_t;
 
-typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1, MOE_W_MXFP8_T = 2 } moe_wfmt_t;
+typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1, MOE_W_MXFP8_T = 2, MOE_W_NVFP4S = 3 } moe_wfmt_t;
 typedef enum { MOE_BF16 = 0, MOE_FP16 = 1, MOE_FP32 = 2 } moe_dtype_t;
 typedef enum { MOE_PATH_DECODE = 0, MOE_PATH_GROUPED = 1 } moe_path_t;
 
@@ -85,7 +98,9 @@ typedef struct {
     int32_t E, N, K;
     const void *q;       /* codes / packed nibbles                       */
     const void *scale;   /* E8M0 bytes / fp16 group scales               */
-    const void *zero;    /* NULL / packed zero nibbles                   */
+    const void *zero;    /* NULL / packed zero nibbles / NVFP4S patterns */
+    const float *alpha;  /* MOE_W_NVFP4S: fp32 [E] per-expert constant;
+                            read for no other format (may be left unset) */
 } moe_weights_t;
 
 /* Human-readable name of a status code (static storage). */
@@ -212,6 +227,10 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  * [opt-in] -> one kernel (gate/up dots on f16 mma.sync over the raw 4-bit codes with the
  * zero folded out in FP32, a grid-wide barrier whose counter lives in
  * ws[0..8), then the down projection), when its shared-memory plan fits;
+ * MOE_W_NVFP4S [opt-in] -> a gate/up kernel and a down kernel, one warp per
+ * intermediate / output scalar, 16-byte loads of 64 packed weights, the
+ * kept values decoded on the fly, FP32 sums, h in ws past its first 256
+ * bytes; d % 64 == 0, I % 64 == 0, x MOE_BF16 or MOE_FP16;
  * otherwise one warp per intermediate / output scalar.  Every output's summation order is fixed
  * by the shapes, the path and (single-pass path) the set of routed experts,
  * so identical inputs give identical bits; the two-kernel and per-scalar

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(L):
 def test_status_names_and_version(L):
     for code, name in moe.STATUS_NAMES.items():
         assert L.moe_status_string(code).decode() == name
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
 
 
 def test_align_capacity_bound():

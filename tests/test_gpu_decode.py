@@ -397,3 +397,51 @@ def test_decode_logits_equals_topk_then_decode(M, transposed):
         assert np.array_equal(ids1.cpu().numpy(), ids_ref)
         np.testing.assert_allclose(w1.cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
         gs.assert_layer_close(y1, oracle_decode(layer, x.cpu(), ids_ref, w_ref.astype(np.float32)))
+
+
+# ------------------------------------------------ paired 4:8 sparse NVFP4 (opt-in kernels)
+
+NV4 = inputs.Workload("nvfp4s_m4_d1024_i512_e16_k4", M=4, d=1024, I=512, E=16, k=4, seed=21)
+
+
+def _nvfp4s_layer(wl):
+    """Packed weights from the oracle's quantizer (the format is packed
+    offline), on the device, and the same packing for the oracle."""
+    p13 = oracle.nvfp4s_quantize_3d(inputs.weights_fp32(wl, "w13").astype(np.float64))
+    p2 = oracle.nvfp4s_quantize_3d(inputs.weights_fp32(wl, "w2").astype(np.float64))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    mk = lambda p: moe.Weights(moe.MOE_W_NVFP4S, dev(p["v"]), dev(p["s"]), dev(p["m"]), dev(p["alpha"]))
+    return mk(p13), mk(p2), p13, p2
+
+
+def test_nvfp4s_decode_is_opt_in():
+    if moe.moe_candidate_kernels_enabled():
+        pytest.skip("opt-in kernels requested: the parity test below covers the path")
+    w13, w2, _, _ = _nvfp4s_layer(NV4)
+    ids, w = gs.routing(NV4)
+    with pytest.raises(moe.MoeError) as err:                  # refused on the host, nothing launched
+        moe.moe_ffn_decode(inputs.activations(NV4).cuda(), torch.from_numpy(ids).cuda(),
+                           torch.from_numpy(w).cuda(), w13, w2)
+    assert err.value.status == 2
+
+
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float16])
+def test_nvfp4s_decode_matches_oracle(xdt):
+    gs.need_candidates()
+    w13, w2, p13, p2 = _nvfp4s_layer(NV4)
+    x = inputs.activations(NV4, dtype=xdt)
+    ids, w = gs.routing(NV4)
+    ids = ids.copy()
+    ids[1, 2] = -1                                            # an invalid route
+    ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), NV4.E, p13, p2)["y"]
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for out_dtype in (torch.float32, torch.bfloat16):
+        y = moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), w13, w2,
+                               out_dtype=out_dtype, dev_status=st)
+        gs.assert_layer_close(y, ref)
+    torch.cuda.synchronize()
+    assert st.tolist() == [2, 0]
+    y1 = moe.moe_ffn_decode(x[:1].cuda(), torch.from_numpy(ids[:1]).cuda(), torch.from_numpy(w[:1]).cuda(), w13, w2,
+                            out_dtype=torch.float32)
+    assert torch.equal(y1[0], moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
+                                                 w13, w2, out_dtype=torch.float32)[0])

@@ -24,7 +24,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CAPACITY", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_TIMEOUT"}
-MOE_W_MXFP8, MOE_W_AWQ4, MOE_W_MXFP8_T = 0, 1, 2
+MOE_W_MXFP8, MOE_W_AWQ4, MOE_W_MXFP8_T, MOE_W_NVFP4S = 0, 1, 2, 3
 MOE_BF16, MOE_FP16, MOE_FP32 = 0, 1, 2
 MOE_PATH_DECODE, MOE_PATH_GROUPED = 0, 1
 
@@ -40,7 +40,7 @@ class MoeError(RuntimeError):
 class moe_weights_t(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("E", ctypes.c_int32), ("N", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("q", ctypes.c_void_p), ("scale", ctypes.c_void_p),
-                ("zero", ctypes.c_void_p)]
+                ("zero", ctypes.c_void_p), ("alpha", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -171,19 +171,23 @@ class Weights:
     """One projection of all experts: MXFP8 (q uint8 [E,N,K], scale uint8
     [E,N,K/32]), MXFP8_T (the same values K-outer: q uint8 [E,K,N], scale
     uint8 [E,K/32,N]) or AWQ4 (q int32 [E,N,K/8], scale fp16 [E,N,K/128],
-    zero int32 [E,N/8,K/128]).  The tensors are checked against the format
+    zero int32 [E,N/8,K/128]) or NVFP4S, paired 4:8 sparse NVFP4 (q uint8
+    [E,N,K/4] kept E2M1 codes, scale uint8 [E,N,K/32] UE4M3, zero uint8
+    [E,N,K/16] pattern nibbles, alpha float32 [E]).  The tensors are checked against the format
     when the object is made (device, contiguity, dtype, shapes), and the
     object is immutable, so the layer calls only compare its device."""
     fmt: int
     q: torch.Tensor
     scale: torch.Tensor
     zero: torch.Tensor | None = None
+    alpha: torch.Tensor | None = None
 
     def __post_init__(self):
         object.__setattr__(self, "device", self._check())
         object.__setattr__(self, "_struct", moe_weights_t(
             self.fmt, self.E, self.N, self.K, self.q.data_ptr(), self.scale.data_ptr(),
-            self.zero.data_ptr() if self.zero is not None else None))
+            self.zero.data_ptr() if self.zero is not None else None,
+            self.alpha.data_ptr() if self.alpha is not None else None))
 
     @property
     def E(self):
@@ -197,7 +201,7 @@ class Weights:
     def K(self):
         if self.fmt == MOE_W_MXFP8_T:
             return self.q.shape[1]
-        return self.q.shape[2] * (8 if self.fmt == MOE_W_AWQ4 else 1)
+        return self.q.shape[2] * {MOE_W_AWQ4: 8, MOE_W_NVFP4S: 4}.get(self.fmt, 1)
 
     def _check(self):
         q = _need(self.q, "weights.q")
@@ -223,10 +227,21 @@ class Weights:
             if self.zero is None:
                 raise ValueError("weights.zero is required for AWQ weights")
             _need(self.zero, "weights.zero", _IDS, (E, N // 8, K // 128), device=device)
+        elif self.fmt == MOE_W_NVFP4S:
+            _need(q, "weights.q", _U8)
+            if K % 64:
+                raise ValueError(f"weights: NVFP4S needs K % 64 == 0 (K = {K})")
+            _need(self.scale, "weights.scale", _U8, (E, N, K // 32), device=device)
+            if self.zero is None or self.alpha is None:
+                raise ValueError("weights.zero (patterns) and weights.alpha are required for NVFP4S weights")
+            _need(self.zero, "weights.zero", _U8, (E, N, K // 16), device=device)
+            _need(self.alpha, "weights.alpha", _F32, (E,), device=device)
         else:
             raise ValueError(f"weights: unknown format {self.fmt}")
-        if self.fmt != MOE_W_AWQ4 and self.zero is not None:
+        if self.fmt not in (MOE_W_AWQ4, MOE_W_NVFP4S) and self.zero is not None:
             raise ValueError("weights.zero must be None for MXFP8 weights")
+        if self.fmt != MOE_W_NVFP4S and self.alpha is not None:
+            raise ValueError("weights.alpha is only for NVFP4S weights")
         return device
 
     def on(self, name: str, device):

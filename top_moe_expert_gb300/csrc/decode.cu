@@ -354,6 +354,9 @@ static moe_status_t check_weights(const moe_weights_t *w, int N, int K)
     } else if (w->fmt == MOE_W_AWQ4) {
         if (!w->zero || K % 128 != 0 || N % 8 != 0)
             return MOE_ERR_INVALID_ARG;
+    } else if (w->fmt == MOE_W_NVFP4S) {
+        if (!w->zero || !w->alpha || K % 64 != 0)
+            return MOE_ERR_INVALID_ARG;
     } else {
         return MOE_ERR_INVALID_ARG;
     }
@@ -409,6 +412,8 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         return MOE_ERR_UNSUPPORTED;
     if (fmt == MOE_W_AWQ4 && (d % 1024 != 0 || I % 128 != 0))
         return MOE_ERR_UNSUPPORTED;
+    if (fmt == MOE_W_NVFP4S && (!candidate_kernels_enabled() || !decode_nvfp4s_eligible(k, d, I)))
+        return MOE_ERR_UNSUPPORTED;
     if (ydt != MOE_BF16 && ydt != MOE_FP32)
         return MOE_ERR_UNSUPPORTED;
     if (fmt == MOE_W_MXFP8 ? xdt != MOE_BF16 : (xdt != MOE_BF16 && xdt != MOE_FP16))
@@ -432,6 +437,9 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     float *h = static_cast<float *>(ws_data);
     cudaStream_t s = as_stream(stream);
     const bool cand = candidate_kernels_enabled();
+    if (fmt == MOE_W_NVFP4S)
+        return decode_nvfp4s_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k, w13, w2, y,
+                                    ydt == MOE_FP32, h, dev_status, s);
     if (cand && fmt == MOE_W_AWQ4 && decode_awq_small_eligible(M, k, d, I, w13->E)) {
         // a small batch: aligned blocks of 16 rows, one kernel for both GEMMs, combine
         const moe_status_t st3 = decode_awq_small_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k,

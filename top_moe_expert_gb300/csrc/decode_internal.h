@@ -86,4 +86,11 @@ moe_status_t decode_awq_m1_launch(const void *x, bool x_bf16, const int32_t *ids
                                   const void *s2, const void *z2, void *y, bool y_f32, void *ws,
                                   int32_t *dev_status, cudaStream_t stream);
 
+// paired 4:8 sparse NVFP4 decode (decode_nvfp4s.cu): a gate/up kernel and a
+// down kernel, h [M*k][I] f32 in `h`
+bool decode_nvfp4s_eligible(int k, int d, int I);
+moe_status_t decode_nvfp4s_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
+                                  const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                  void *y, bool y_f32, float *h, int32_t *dev_status, cudaStream_t s);
+
 }  // namespace moe
