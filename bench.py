@@ -5,12 +5,19 @@
                     [--workload decode_m1|tiny|sweep_m<M>[_zipf]|large_m1|large_m8|awq_fixture_a|awq_m1|probe_m16384]
 
 A step is one pass of the hot path over one batch of fresh synthetic input:
-top-k routing of the step's router logits, then the layer (output-centric
-decode kernels).  The default workload is the 128-expert d=2048 / I=768
-top-8 layer at M=1 with MXFP8 weights (623 MB resident), fresh routing every
-step.  The L2 is flushed (a 512 MiB write) between timed steps, outside the
-timed interval.  Each step's device time is taken with CUDA events on the
-launching stream around a CUDA-graph replay of the step.
+top-k routing of the step's router logits, then the layer (at one token the
+routing runs inside the layer's single kernel; the grouped path adds the
+alignment).  The default workload is the 128-expert d=2048 / I=768 top-8
+layer at M=1 with MXFP8 weights, fresh routing every step.
+
+Timing: K steps run back to back in CUDA graphs, bracketed by one pair of
+CUDA events on the launching stream, as a model runs its stack of MoE layers.
+Each step reads the next of L copies of the layer's weights (16 at M=1, 10 GB)
+with its own input, so its weights were last read L steps earlier: the inputs
+of the timed steps are larger than the L2 and no flush is needed.  Also
+reported: one isolated call (the L2 evicted by a 1 GiB read before it), the
+layer call alone back to back (routing computed ahead of time) for the
+roofline, and the end-to-end call through the public API with host buffers.
 
 Metric: achieved HBM TB/s of the layer = algorithmic bytes (the distinct
 routed experts' MXFP8 weights incl. scales, plus x, the router logits and y)
@@ -215,218 +222,230 @@ def grouped_block(wl) -> int:
     return b
 
 
-class DecodeStep:
-    """Device-resident workload + a CUDA graph of one step: top-k routing and
-    the layer (decode path), or top-k, alignment and the grouped layer."""
+def layer_copies(wl, step_bytes_est: int, layer_weight_bytes: int) -> int:
+    """Copies of the layer's weights the timed steps rotate through (a model's
+    stack of MoE layers): enough that a step's weights were last read at
+    least 1.5 GB of other traffic ago (about 12 times the L2), at most 16
+    copies and 48 GB."""
+    want = -(-int(1.5e9) // max(1, step_bytes_est))
+    cap = max(1, int(48e9 // max(1, layer_weight_bytes)))
+    return max(1, min(16, want, cap))
 
-    def __init__(self, wl, nsteps: int, device, path: str = "decode", block: int = 0, w2_layout: str = "auto"):
+
+class Step:
+    """Device-resident workload: L copies of the layer's weights, a pool of
+    fresh inputs (router logits, activations) and the buffers of one step.
+    A step is top-k routing and the layer (decode path; at one token the
+    routing runs inside the layer's kernel), or top-k, alignment and the
+    grouped layer; with the fixed-routing AWQ workloads, the layer alone (with
+    its alignment on the grouped path)."""
+
+    def __init__(self, wl, n_inputs, device, path: str = "decode", block: int = 0, w2_layout: str = "auto"):
         import top_moe_expert_gb300 as moe
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
-        self.routed_in_layer = False
-        self.w2_standard = w2_layout == "standard"
         self.awq = wl.fmt == "awq4"
-        # the library's opt-in kernels (MOE_FFN_CANDIDATE_KERNELS=1) decide several paths below
-        self.cand = bool(moe.moe_candidate_kernels_enabled())
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
+        self.n_inputs = n_inputs
+        # ---- layer 0's weights
         if self.awq:
-            self._init_awq(wl, nsteps, device, block)
-            return
-        self.q13 = torch.empty((E, 2 * I, d), dtype=torch.uint8, device=device)
-        self.s13 = torch.empty((E, 2 * I, d // 32), dtype=torch.uint8, device=device)
-        self.q2 = torch.empty((E, d, I), dtype=torch.uint8, device=device)
-        self.s2 = torch.empty((E, d, I // 32), dtype=torch.uint8, device=device)
-        for e in range(E):
-            moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w13", e, device), self.q13[e], self.s13[e])
-            moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), self.q2[e], self.s2[e])
-        self.w13 = moe.Weights(moe.MOE_W_MXFP8, self.q13, self.s13)
-        self.w2 = moe.Weights(moe.MOE_W_MXFP8, self.q2, self.s2)
-        self.fused = False
-        if path == "grouped":
-            self.b = block or grouped_block(wl)
-            self.sfa13, self.sfa2 = moe.moe_grouped_prepare(self.w13, self.w2)
+            dev_t = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
+            q13, s13, z13 = inputs.awq_weights(wl, "w13")
+            q2, s2, z2 = inputs.awq_weights(wl, "w2")
+            w0 = ((dev_t(q13), dev_t(s13).view(torch.float16), dev_t(z13)),
+                  (dev_t(q2), dev_t(s2).view(torch.float16), dev_t(z2)))
+            del q13, s13, z13, q2, s2, z2
         else:
-            # small batches take the single-pass kernel, which reads the down
-            # projection neuron-major: pack it once (same bytes, K-outer order)
-            self.fused = M <= 4 and d % 1024 == 0 and not self.w2_standard
-            # one token on that layout: routing runs inside the layer's kernel
-            self.routed_in_layer = self.fused and M == 1 and d in (1024, 2048) and E <= 512
-            if self.w2_standard and M == 1 and E <= 512 and self.cand:
-                # one token on the standard layout: the single-kernel path, routing inside
-                self.routed_in_layer = True
-            if self.fused:
-                self.w2 = moe.moe_mxfp8_transpose(self.w2)
-                del self.q2, self.s2
-                torch.cuda.empty_cache()
-        # fresh routing and activations for every step (large batches cycle
-        # through a pool of distinct steps to bound host memory)
-        self.n_inputs = nsteps if M <= 64 else min(nsteps, 16)
-        self.logits_host = torch.from_numpy(np.stack([inputs.router_logits(wl, i) for i in range(self.n_inputs)]))
-        self.x_host = torch.stack([inputs.activations(wl, i) for i in range(self.n_inputs)])
+            q13 = torch.empty((E, 2 * I, d), dtype=torch.uint8, device=device)
+            s13 = torch.empty((E, 2 * I, d // 32), dtype=torch.uint8, device=device)
+            q2 = torch.empty((E, d, I), dtype=torch.uint8, device=device)
+            s2 = torch.empty((E, d, I // 32), dtype=torch.uint8, device=device)
+            for e in range(E):
+                moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w13", e, device), q13[e], s13[e])
+                moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), q2[e], s2[e])
+            w0 = ((q13, s13, None), (q2, s2, None))
+        # the single-pass small-batch kernel reads the down projection
+        # neuron-major: packed once (same bytes, K-outer order)
+        self.neuron_major = (not self.awq and path == "decode" and w2_layout != "standard" and 2 <= M <= 4
+                             and d % 1024 == 0)
+        self.routed_in_layer = (not self.awq and path == "decode" and M == 1 and E <= 768
+                                and not self.neuron_major)
+        lw_bytes = sum(t.numel() * t.element_size() for p in w0 for t in p if t is not None)
+        self.ids_host = [self._host_ids(j) for j in range(n_inputs)]
+        est = max(step_bytes(wl, ids) for ids in self.ids_host[:8])
+        self.L = layer_copies(wl, est, lw_bytes)
+        self.layer_weight_bytes = lw_bytes
+        self.layers = []
+        for l in range(self.L):
+            (a13, b13, c13), (a2, b2, c2) = w0 if l == 0 else tuple(
+                tuple(t.clone() if t is not None else None for t in p) for p in w0)
+            if self.awq:
+                w13 = moe.Weights(moe.MOE_W_AWQ4, a13, b13, c13)
+                w2 = moe.Weights(moe.MOE_W_AWQ4, a2, b2, c2)
+            else:
+                w13 = moe.Weights(moe.MOE_W_MXFP8, a13, b13)
+                w2 = moe.Weights(moe.MOE_W_MXFP8, a2, b2)
+                if self.neuron_major:
+                    w2 = moe.moe_mxfp8_transpose(w2)
+            sfa = moe.moe_grouped_prepare(w13, w2) if (path == "grouped" and not self.awq) else (None, None)
+            self.layers.append((w13, w2, sfa))
+        del w0
+        torch.cuda.empty_cache()
+        # ---- inputs
+        if self.awq:
+            self.logits_host = torch.zeros((n_inputs, M, E), dtype=torch.float32)     # routing is fixed
+            self.x_host = torch.stack([inputs.activations(wl, i, dtype=torch.float16) for i in range(n_inputs)])
+        else:
+            self.logits_host = torch.from_numpy(np.stack([inputs.router_logits(wl, i) for i in range(n_inputs)]))
+            self.x_host = torch.stack([inputs.activations(wl, i) for i in range(n_inputs)])
         self.logits_all = self.logits_host.to(device)
         self.x_all = self.x_host.to(device)
-        # x and the router logits share one device buffer, so a step's inputs
-        # arrive in one host-to-device copy
-        self.io = torch.empty(M * d * 2 + M * E * 4, dtype=torch.uint8, device=device)
-        self.x = self.io[:M * d * 2].view(torch.bfloat16).view(M, d)
-        self.logits = self.io[M * d * 2:].view(torch.float32).view(M, E)
-        self.io_host = ("x_host", "logits_host")     # host tensors packed into io, in order
-        self.ids = torch.empty((M, k), dtype=torch.int32, device=device)
-        self.w = torch.empty((M, k), dtype=torch.float32, device=device)
+        # x and the router logits share one device buffer, so an end-to-end
+        # step's inputs arrive in one host-to-device copy
+        xb = M * d * 2
+        self.io = torch.empty(xb + (0 if self.awq else M * E * 4), dtype=torch.uint8, device=device)
+        self.x = self.io[:xb].view(self.x_all.dtype).view(M, d)
+        self.logits = (torch.empty((M, E), dtype=torch.float32, device=device) if self.awq
+                       else self.io[xb:].view(torch.float32).view(M, E))
+        self.io_host = ("x_host",) if self.awq else ("x_host", "logits_host")
         self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
+        if self.awq:
+            fid = torch.from_numpy(inputs.fixture_a_ids(M, k, E)).to(device)
+            fw = torch.from_numpy(inputs.fixture_a_weights(M, k, wl.seed)).to(device)
+            self.ids, self.w = fid, fw
+            self.ids_all = fid.expand(n_inputs, M, k)
+            self.w_all = fw.expand(n_inputs, M, k)
+        else:
+            self.ids = torch.empty((M, k), dtype=torch.int32, device=device)
+            self.w = torch.empty((M, k), dtype=torch.float32, device=device)
+            # the routing of every input, for the layer-only timing
+            self.ids_all = torch.empty((n_inputs, M, k), dtype=torch.int32, device=device)
+            self.w_all = torch.empty((n_inputs, M, k), dtype=torch.float32, device=device)
+            for j in range(n_inputs):
+                moe.moe_topk_softmax(self.logits_all[j], k, self.ids_all[j], self.w_all[j])
         if path == "grouped":
+            self.b = block or (wl.b if self.awq else grouped_block(wl))
             cr, cb = moe.moe_align_capacity(M, k, E, self.b)
-            self.aligned = (torch.empty(cr, dtype=torch.int32, device=device),
-                            torch.empty(cb, dtype=torch.int32, device=device),
-                            torch.empty(1, dtype=torch.int32, device=device))
+            mk = lambda: (torch.empty(cr, dtype=torch.int32, device=device),
+                          torch.empty(cb, dtype=torch.int32, device=device),
+                          torch.empty(1, dtype=torch.int32, device=device))
+            self.aligned = mk()
             na = moe.moe_align_workspace_size(M, k, E, self.b)
             self.ws_align = torch.empty(max(na, 256), dtype=torch.uint8, device=device) if na else None
             self.ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, k, d, I, self.b, cr), dtype=torch.uint8,
                                   device=device)
+            # the alignment of every input (fixed routing: one), for the layer-only timing
+            na_in = 1 if self.awq else n_inputs
+            self.aligned_all = [mk() for _ in range(na_in)]
+            for j in range(na_in):
+                moe.moe_align_block_size(self.ids_all[j], E, self.b, out=self.aligned_all[j], ws=self.ws_align)
         else:
+            self.b = 0
             self.ws = torch.zeros(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
         self.stream = torch.cuda.Stream(device)
         torch.cuda.synchronize()
 
-    def _init_awq(self, wl, nsteps, device, block):
-        """The 4-bit AWQ layer on its fixed closed-form routing (fixture A):
-        a step is alignment + the grouped layer, or the output-centric decode
-        layer alone; activations fp16."""
-        moe = self.moe
+    def _host_ids(self, j: int) -> np.ndarray:
         from top_moe_expert_gb300 import inputs
-        E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
-        dev_t = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
-        q13, s13, z13 = inputs.awq_weights(wl, "w13")
-        q2, s2, z2 = inputs.awq_weights(wl, "w2")
-        self.w13 = moe.Weights(moe.MOE_W_AWQ4, dev_t(q13), dev_t(s13).view(torch.float16), dev_t(z13))
-        self.w2 = moe.Weights(moe.MOE_W_AWQ4, dev_t(q2), dev_t(s2).view(torch.float16), dev_t(z2))
-        del q13, s13, z13, q2, s2, z2
-        self.fused = False
-        self.b = block or wl.b
-        self.sfa13 = self.sfa2 = None
-        self.fixed_ids = inputs.fixture_a_ids(M, k, E)
-        self.n_inputs = min(nsteps, 64)
-        self.logits_host = torch.zeros((self.n_inputs, M, E), dtype=torch.float32)   # routing is fixed
-        self.x_host = torch.stack([inputs.activations(wl, i, dtype=torch.float16) for i in range(self.n_inputs)])
-        self.logits_all = self.logits_host.to(device)
-        self.x_all = self.x_host.to(device)
-        self.logits = torch.empty((M, E), dtype=torch.float32, device=device)
-        # the routing is fixed: x is the step's only input
-        self.io = torch.empty(M * d * 2, dtype=torch.uint8, device=device)
-        self.x = self.io.view(torch.float16).view(M, d)
-        self.io_host = ("x_host",)
-        self.ids = torch.from_numpy(self.fixed_ids).to(device)
-        self.w = torch.from_numpy(inputs.fixture_a_weights(M, k, wl.seed)).to(device)
-        self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
-        cr, cb = moe.moe_align_capacity(M, k, E, self.b)
-        self.aligned = (torch.empty(cr, dtype=torch.int32, device=device),
-                        torch.empty(cb, dtype=torch.int32, device=device),
-                        torch.empty(1, dtype=torch.int32, device=device))
-        na = moe.moe_align_workspace_size(M, k, E, self.b)
-        self.ws_align = torch.empty(max(na, 256), dtype=torch.uint8, device=device) if na else None
-        if self.path == "grouped":
-            self.ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, k, d, I, self.b, cr), dtype=torch.uint8,
-                                  device=device)
-        else:
-            self.ws = torch.zeros(moe.moe_ffn_decode_workspace_size(M, k, d, I), dtype=torch.uint8, device=device)
-        self.stream = torch.cuda.Stream(device)
-        torch.cuda.synchronize()
-
-    def step_ids(self, j: int) -> np.ndarray:
-        """Expert ids of input j (to count the distinct experts a step reads)."""
         if self.awq:
-            return self.fixed_ids
-        return host_topk_ids(self.logits_host[j].numpy(), self.wl.k)
+            return inputs.fixture_a_ids(self.wl.M, self.wl.k, self.wl.E)
+        return host_topk_ids(inputs.router_logits(self.wl, j), self.wl.k)
 
-    def launch_pre(self, stream=None):
-        """Routing of the step: top-k (and, for the grouped path, alignment);
-        nothing when the layer call routes the token itself."""
-        moe = self.moe
+    def step_ids(self, i: int) -> np.ndarray:
+        """Expert ids of step i (to count the distinct experts it reads)."""
+        return self.ids_host[i % self.n_inputs]
+
+    # ---- launches
+    def launch_step(self, i: int, stream, x=None, logits=None):
+        """Step i: input i mod n_inputs (or the given x / logits), layer i mod L."""
+        moe, wl = self.moe, self.wl
+        j, (w13, w2, (sfa13, sfa2)) = i % self.n_inputs, self.layers[i % self.L]
+        x = self.x_all[j] if x is None else x
+        logits = self.logits_all[j] if logits is None else logits
         if self.routed_in_layer:
+            moe.moe_ffn_decode_logits(logits, x, wl.k, w13, w2, y=self.y, topk_ids=self.ids, topk_w=self.w,
+                                      ws=self.ws, stream=stream)
             return
-        if self.awq:
-            if self.path == "grouped":
-                moe.moe_align_block_size(self.ids, self.wl.E, self.b, out=self.aligned, ws=self.ws_align,
-                                         stream=stream)
-            return
-        moe.moe_topk_softmax(self.logits, self.wl.k, self.ids, self.w, stream=stream)
+        if not self.awq:
+            moe.moe_topk_softmax(logits, wl.k, self.ids, self.w, stream=stream)
         if self.path == "grouped":
-            moe.moe_align_block_size(self.ids, self.wl.E, self.b, out=self.aligned, ws=self.ws_align, stream=stream)
-
-    def launch_layer(self, stream=None):
-        """The layer call itself (one C-ABI call)."""
-        moe = self.moe
-        if self.path == "grouped":
-            moe.moe_ffn_grouped(self.x, self.ids, self.w, self.w13, self.w2, self.sfa13, self.sfa2, self.aligned,
-                                self.b, y=self.y, ws=self.ws, stream=stream)
-        elif self.routed_in_layer:
-            moe.moe_ffn_decode_logits(self.logits, self.x, self.wl.k, self.w13, self.w2, y=self.y, topk_ids=self.ids,
-                                      topk_w=self.w, ws=self.ws, stream=stream)
+            moe.moe_align_block_size(self.ids, wl.E, self.b, out=self.aligned, ws=self.ws_align, stream=stream)
+            moe.moe_ffn_grouped(x, self.ids, self.w, w13, w2, sfa13, sfa2, self.aligned, self.b, y=self.y,
+                                ws=self.ws, stream=stream)
         else:
-            moe.moe_ffn_decode(self.x, self.ids, self.w, self.w13, self.w2, y=self.y, ws=self.ws, stream=stream)
+            moe.moe_ffn_decode(x, self.ids, self.w, w13, w2, y=self.y, ws=self.ws, stream=stream)
 
-    def launch(self, stream=None):
-        self.launch_pre(stream)
-        self.launch_layer(stream)
+    def launch_layer(self, i: int, stream):
+        """The layer call of step i alone, on that input's routing computed
+        ahead of time (one kernel at one token: routing included)."""
+        moe, wl = self.moe, self.wl
+        j, (w13, w2, (sfa13, sfa2)) = i % self.n_inputs, self.layers[i % self.L]
+        if self.routed_in_layer:
+            self.launch_step(i, stream)
+            return
+        if self.path == "grouped":
+            al = self.aligned_all[0 if self.awq else j]
+            moe.moe_ffn_grouped(self.x_all[j], self.ids_all[j], self.w_all[j], w13, w2, sfa13, sfa2, al, self.b,
+                                y=self.y, ws=self.ws, stream=stream)
+        else:
+            moe.moe_ffn_decode(self.x_all[j], self.ids_all[j], self.w_all[j], w13, w2, y=self.y, ws=self.ws,
+                               stream=stream)
 
+    def graph(self, i0: int, n: int, layer_only: bool = False):
+        """A CUDA graph of steps i0 .. i0+n-1 back to back on self.stream."""
+        fn = self.launch_layer if layer_only else self.launch_step
+        with torch.cuda.stream(self.stream):
+            fn(i0, self.stream)                  # warm (outside capture)
+        self.stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(i0, i0 + n):
+                fn(i, self.stream)
+        self.stream.synchronize()
+        return g
+
+    def bytes_of(self, i0: int, n: int, layer_only: bool = False) -> float:
+        f = layer_bytes if (layer_only and not self.routed_in_layer) else step_bytes
+        return float(sum(f(self.wl, self.step_ids(i)) for i in range(i0, i0 + n)))
+
+    # ---- descriptions
     def layer_kernels(self) -> str:
-        if self.awq and self.path == "grouped" and self.b <= 16 and self.cand:
-            return ("moe_ffn_grouped (AWQ-4bit, b <= 16): gsm::awq_mma_kernel (both GEMMs on mma.sync over the raw "
-                    "codes, one kernel) + combine")
         if self.awq and self.path == "grouped":
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
-        if self.awq and self.wl.M == 1 and self.cand:
-            return "moe_ffn_decode (AWQ-4bit, one token): da1::awq_m1_kernel (gate/up + SwiGLU + down), one kernel"
-        if self.awq and 2 <= self.wl.M <= 64 and self.cand:
-            return ("moe_ffn_decode (AWQ-4bit, 2 <= M <= 64): alignment into blocks of 16 + gsm::awq_mma_kernel "
-                    "(both GEMMs on mma.sync) + combine")
         if self.awq:
             return "moe_ffn_decode (AWQ-4bit): decode_gate_up_kernel<AWQ> + decode_down_kernel<AWQ>"
         if self.path == "grouped":
             return "moe_ffn_grouped: act_quant + gemm_kernel (both GEMMs, one persistent kernel) + combine"
-        if self.routed_in_layer and self.w2_standard:
-            return ("moe_ffn_decode_logits (standard W2 layout): dx1::mx_m1_kernel (top-k routing + gate/up on "
-                    "mma.sync + SwiGLU + down), one kernel")
         if self.routed_in_layer:
-            return "moe_ffn_decode_logits: dm::m1_kernel (top-k routing + gate/up + SwiGLU + down + combine), one kernel"
-        if self.fused:
+            return ("moe_ffn_decode_logits: dp::pipe_kernel (top-k routing + gate/up + SwiGLU + down + "
+                    "routing-weighted sum), one kernel")
+        if self.neuron_major:
             return "moe_ffn_decode: df::fused_kernel + df::reduce_kernel, PDL-chained"
-        if self.w2_standard and 2 <= self.wl.M <= 64 and self.cand:
-            return ("moe_ffn_decode (standard W2 layout, 2 <= M <= 64): alignment into blocks of 16 + "
-                    "gmx::mx_mma_kernel (both GEMMs on mma.sync) + combine")
         return "moe_ffn_decode: ds::gate_up_kernel + ds::down_kernel, PDL-chained"
+
+    def path_text(self) -> str:
+        wl = self.wl
+        if self.awq and self.path == "grouped":
+            return ("expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
+                    "dequantized in shared memory + combine, b=%d), fixed routing" % self.b)
+        if self.awq:
+            return "output-centric AWQ decode (gate/up + down on CUDA cores), fixed routing"
+        if self.path == "grouped":
+            return "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)" % self.b
+        if self.routed_in_layer:
+            return "single-token decode: routing + gate/up + SwiGLU + down in one kernel, h exchanged through L2"
+        if self.neuron_major:
+            return "single-pass decode (topk + fused gate/up/down + partial reduction)"
+        return "output-centric decode (topk + gate/up + down)"
 
     def launches_per_step(self) -> int:
         if self.path == "grouped":
-            # (top-k), alignment, act-quant or gather, the GEMM kernel, combine
             na = 2 if self.ws_align is not None else 1
-            if self.awq:
-                # the b <= 16 AWQ path: one kernel for both GEMMs, then the combine
-                return na + (2 if self.b <= 16 and self.cand else 3)
-            return 1 + na + 3
+            # (top-k), alignment, act-quant or gather, the GEMM kernel, combine
+            return (0 if self.awq else 1) + na + 3
         if self.awq:
-            # fixed routing: the single-token kernel; alignment, the GEMM kernel and the
-            # combine up to 64 tokens; the two decode kernels beyond
-            if not self.cand:
-                return 2
-            return 1 if self.wl.M == 1 else (3 if self.wl.M <= 64 else 2)
-        if self.w2_standard and 2 <= self.wl.M <= 64 and self.cand:
-            return 4                       # top-k, alignment, the GEMM kernel, combine
+            return 2
         return 1 if self.routed_in_layer else 3
-
-    def capture(self):
-        with torch.cuda.stream(self.stream):
-            self.launch(self.stream)            # warm, outside capture
-        self.stream.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph, stream=self.stream):
-            self.launch(self.stream)
-        self.stream.synchronize()
-        # the layer call alone, for the roofline of the dominant kernels
-        self.layer_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.layer_graph, stream=self.stream):
-            self.launch_layer(self.stream)
-        self.stream.synchronize()
 
 
 def host_topk_ids(logits: np.ndarray, k: int) -> np.ndarray:
@@ -448,9 +467,7 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     t_mma = flops / (peak_tf * 1e12)
     kern = st.layer_kernels()
     src = ("awq" if st.path == "grouped" else "awq_decode") if st.awq else st.path
-    # the opt-in kernels replace some paths' kernels: their counters are keyed apart
-    key = (f"{st.path}{'-w2std' if getattr(st, 'w2_standard', False) else ''}"
-           f"{'-cand' if getattr(st, 'cand', False) else ''}:{wl.name}")
+    key = f"{st.path}:{wl.name}"
     traffic = committed_traffic(key, decode_src_hash(src))
     if t_mma > t_hbm:
         ach = flops / sec / 1e12 / world
@@ -482,6 +499,12 @@ def gather_replicas(times, sizes, world, device=None):
     return tmax.tolist(), tsum.tolist()
 
 
+def read_flush(buf):
+    """Evict the L2 by reading a buffer several times its size: a read leaves
+    no dirty lines behind, so nothing is written back during the next step."""
+    torch.sum(buf, dim=0, keepdim=True)
+
+
 def run_ours(args, rank, world, device):
     wl = workload_from_name(args.workload)
     K, W = args.steps, args.warmup
@@ -493,61 +516,86 @@ def run_ours(args, rank, world, device):
         p, b = moe.moe_ffn_select_path(wl.M, wl.k, wl.E, wl.d, wl.I, fmt)
         path = "decode" if p == moe.MOE_PATH_DECODE else "grouped"
         block = block or b
-    st = DecodeStep(wl, K + W, device, path, block, args.w2)
-    st.capture()
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    Kg = min(K, 1000 if wl.M <= 64 else 50)              # steps per captured graph
+    n_inputs = min(Kg + W, 1024 if wl.M <= 64 else 16)
+    st = Step(wl, n_inputs, device, path, block, args.w2)
     s = st.stream
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    # ---- the timed steps: graphs of Kg steps back to back (inputs already in
+    # HBM, each step on its own input and the next layer copy: no L2 flush)
+    R, rem = divmod(K, Kg)
+    g_main = st.graph(0, Kg)
+    g_rem = st.graph(0, rem) if rem else None
+    g_warm = st.graph(0, W)
+    steps_bytes = R * st.bytes_of(0, Kg) + (st.bytes_of(0, rem) if rem else 0.0)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device.index if device.index is not None else 0)
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
-    with torch.cuda.stream(s):
-        for i in range(W):
-            st.x.copy_(st.x_all[i % st.n_inputs], non_blocking=True)
-            st.logits.copy_(st.logits_all[i % st.n_inputs], non_blocking=True)
-            flush.fill_(float(i))
-            st.graph.replay()
+    g_warm.replay()
     torch.cuda.synchronize()
     sampler.start()
-    with torch.cuda.stream(s):                  # keep the GPU busy while the sampler starts
-        for i in range(400):
-            flush.fill_(float(i))
-            st.graph.replay()
-    torch.cuda.synchronize()
+    t_keep = time.perf_counter()
+    while time.perf_counter() - t_keep < 0.25:         # the sampler sees the GPU busy before the timed region
+        g_main.replay()
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     with torch.cuda.stream(s):
-        for i in range(K):
-            j = (W + i) % st.n_inputs
-            st.x.copy_(st.x_all[j], non_blocking=True)
-            st.logits.copy_(st.logits_all[j], non_blocking=True)
-            flush.fill_(float(j))
-            ev0[i].record(s)
-            st.graph.replay()
-            ev1[i].record(s)
+        ev0.record(s)
+        for _ in range(R):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(s)
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
-    t_wall = t_wall1 - t_wall0
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop(t_wall0, t_wall1)
-    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
-    total_ms = sum(step_ms)
+    total_ms = ev0.elapsed_time(ev1)
+    del g_rem, g_warm
 
-    # bytes of every timed step (distinct experts of that step's routing)
-    bytes_steps = [step_bytes(wl, st.step_ids((W + i) % st.n_inputs)) for i in range(K)]
-    total_bytes = float(sum(bytes_steps))
+    # ---- the layer call alone, back to back (routing computed ahead of time
+    # for each input): the roofline of the dominant kernel(s)
+    Kl = min(K, Kg)
+    g_layer = st.graph(0, Kl, layer_only=True)
+    Rl = max(1, min(R, 20))
+    layer_bytes_total = Rl * st.bytes_of(0, Kl, layer_only=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for _ in range(Rl):
+            g_layer.replay()
+        ev1.record(s)
+    torch.cuda.synchronize()
+    layer_ms = ev0.elapsed_time(ev1)
+    del g_layer
 
-    # e2e: the same steps through the public API with host buffers (pinned)
-    Ke = min(K, 2000)
-    sel = [(W + i) % st.n_inputs for i in range(Ke)]
-    # each step's inputs packed in one pinned row, laid out as st.io
-    sel_rows = sel if wl.M <= 64 else list(range(st.n_inputs))
-    io_pin = torch.cat([getattr(st, n)[sel_rows].reshape(len(sel_rows), -1).view(torch.uint8) for n in st.io_host],
+    # ---- one isolated call (a one-step graph), L2 evicted by a read before it
+    Kc = min(K, 300)
+    flushbuf = torch.ones(2 ** 28, dtype=torch.float32, device=device)      # 1 GiB
+    g_one = st.graph(0, 1)
+    c0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kc)]
+    c1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kc)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(Kc):
+            read_flush(flushbuf)
+            c0[i].record(s)
+            g_one.replay()
+            c1[i].record(s)
+    torch.cuda.synchronize()
+    call_us = sorted(a.elapsed_time(b) * 1e3 for a, b in zip(c0, c1))
+    call_bytes = st.bytes_of(0, 1)
+    del g_one
+
+    # ---- e2e: the same steps through the public API with host buffers
+    # (pinned): inputs copied in and y copied out inside the timed interval
+    Ke = min(K, 1000)
+    rows = list(range(min(Ke, st.n_inputs)))
+    io_pin = torch.cat([getattr(st, n)[rows].reshape(len(rows), -1).view(torch.uint8) for n in st.io_host],
                        dim=1).pin_memory()
     assert io_pin.shape[1] == st.io.numel()
     y_pin = torch.empty((Ke, wl.M, wl.d), dtype=torch.bfloat16).pin_memory()
@@ -556,48 +604,26 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         for i in range(Ke):
-            flush.fill_(float(i))
+            read_flush(flushbuf)
             e0[i].record(s)
-            pi = i if wl.M <= 64 else sel[i]
-            st.io.copy_(io_pin[pi], non_blocking=True)
-            st.launch(s)
+            st.io.copy_(io_pin[i % len(rows)], non_blocking=True)
+            st.launch_step(i % len(rows), s, x=st.x, logits=st.logits)
             y_pin[i].copy_(st.y, non_blocking=True)
             e1[i].record(s)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
-    e2e_bytes = float(sum(bytes_steps[:Ke]))
+    e2e_bytes = st.bytes_of(0, Ke) if Ke <= st.n_inputs else float(
+        sum(step_bytes(wl, st.step_ids(i % len(rows))) for i in range(Ke)))
+    del flushbuf
 
-    # the layer call alone (roofline of the dominant kernels): routing of the
-    # step runs first, outside the events; L2 flushed before each call
-    Kl = min(K, 2000)
-    l0 = [torch.cuda.Event(enable_timing=True) for _ in range(Kl)]
-    l1 = [torch.cuda.Event(enable_timing=True) for _ in range(Kl)]
-    torch.cuda.synchronize()
-    with torch.cuda.stream(s):
-        for i in range(Kl):
-            j = (W + i) % st.n_inputs
-            st.x.copy_(st.x_all[j], non_blocking=True)
-            st.logits.copy_(st.logits_all[j], non_blocking=True)
-            st.launch_pre(s)
-            flush.fill_(float(j))
-            l0[i].record(s)
-            st.layer_graph.replay()
-            l1[i].record(s)
-    torch.cuda.synchronize()
-    layer_ms = sum(a.elapsed_time(b) for a, b in zip(l0, l1))
-    # (a layer call that routes the token itself also reads the logits)
-    lb = step_bytes if st.routed_in_layer else layer_bytes
-    layer_total_bytes = float(sum(lb(wl, st.step_ids((W + i) % st.n_inputs)) for i in range(Kl)))
-
-    (total_ms, e2e_ms, layer_ms), (total_bytes, e2e_bytes, layer_total_bytes) = gather_replicas(
-        [total_ms, e2e_ms, layer_ms], [total_bytes, e2e_bytes, layer_total_bytes], world, device)
+    (total_ms, e2e_ms, layer_ms), (steps_bytes, e2e_bytes, layer_bytes_total) = gather_replicas(
+        [total_ms, e2e_ms, layer_ms], [steps_bytes, e2e_bytes, layer_bytes_total], world, device)
     if rank != 0:
         return None
 
-    tbps = total_bytes / (total_ms * 1e-3) / 1e12
-    us_layer = total_ms * 1e3 / K
-    peak_gbs, peak_kind = measured_peak()
-    achieved_gbs = tbps * 1e3 / world
+    tbps = steps_bytes / (total_ms * 1e-3) / 1e12
+    us_step = total_ms * 1e3 / K
+    med_call = call_us[len(call_us) // 2]
     line = {
         "metric": METRIC,
         "value": round(tbps, 4),
@@ -606,7 +632,7 @@ def run_ours(args, rank, world, device):
         "steps": K,
         "warmup": W,
         "ms_per_step": round(total_ms / K, 6),
-        "us_per_layer": round(us_layer, 3),
+        "us_per_layer": round(us_step, 3),
         "tokens_per_s": round(wl.M * world / (total_ms * 1e-3 / K), 1),
         "frac_of_8TBps": round(tbps / world / 8.0, 4),
         "higher_is_better": True,
@@ -618,52 +644,60 @@ def run_ours(args, rank, world, device):
                  "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
                  "N(0,1) router logits; fresh routing every step)"),
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "path": ("expert-centric grouped AWQ, blocks of at most 16 rows (align + one kernel for both "
-                            "GEMMs on mma.sync over the raw 4-bit codes, zero folded out in FP32 + combine, b=%d)"
-                            % st.b if st.awq and st.path == "grouped" and st.b <= 16 and st.cand else
-                            "expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
-                            "dequantized into tensor memory + combine, b=%d)" % st.b
-                            if st.awq and st.path == "grouped" else
-                            ("single-token AWQ decode: gate/up + SwiGLU + down in one kernel, f16 mma.sync dot "
-                             "products on raw 4-bit codes, zero folded in FP32, fixed routing") if st.awq and wl.M == 1 and st.cand else
-                            ("small-batch AWQ decode (alignment into blocks of 16 + one kernel for both GEMMs on "
-                             "mma.sync over the raw 4-bit codes + combine, fixed routing)")
-                            if st.awq and 2 <= wl.M <= 64 and st.cand else
-                            "output-centric AWQ decode (gate/up + down on CUDA cores, fixed routing)" if st.awq else
-                            "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)"
-                            % st.b if st.path == "grouped" else
-                            ("single-token decode on the standard W2 layout: routing + gate/up + SwiGLU + down "
-                             "in one kernel (mma.sync dot products)") if st.routed_in_layer and st.w2_standard else
-                            "single-token decode: routing + gate/up + SwiGLU + down + combine in one kernel"
-                            if st.routed_in_layer else
-                            "single-pass decode (topk + fused gate/up/down + partial reduction)" if st.fused
-                            else ("small-batch decode on the standard W2 layout (topk + alignment into blocks of 16 "
-                                  "+ one kernel for both GEMMs on mma.sync + combine)")
-                            if st.w2_standard and 2 <= wl.M <= 64 and st.cand
-                            else "output-centric decode (topk + gate/up + down)") + ", CUDA graph",
-                   "l2": "flushed between timed steps (512 MiB write, outside the timed interval)",
+                   "path": st.path_text() + ", CUDA graphs",
+                   "l2": (f"not flushed: inputs larger than L2 -- each step reads the next of {st.L} copies of the "
+                          f"layer's weights ({st.L * st.layer_weight_bytes / 1e9:.1f} GB, a model's stack of MoE "
+                          f"layers) with its own fresh input, so its weights were last read "
+                          f"{st.L} steps earlier"),
+                   "timing": (f"{K} steps back to back in CUDA graphs of {Kg} steps, one pair of CUDA events "
+                              f"around all of them"),
                    "parallelism": f"replicas x{world}"},
+        "latency_us": {"median": round(med_call, 3), "p10": round(call_us[len(call_us) // 10], 3),
+                       "p90": round(call_us[len(call_us) * 9 // 10], 3), "calls": Kc,
+                       "tbps_at_median": round(call_bytes / (med_call * 1e-6) / 1e12, 4),
+                       "how": "one step alone (a one-step graph between CUDA events), the L2 evicted by a "
+                              "1 GiB read before each call"},
         "e2e": {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
                 "us_per_layer": round(e2e_ms * 1e3 / Ke, 3), "steps": Ke,
                 "h2d_bytes_per_step": st.io.numel(),
                 "d2h_bytes_per_step": wl.M * wl.d * 2},
         "gpu_launches": st.launches_per_step() * K,
-        "roofline": roofline_obj(st, wl, layer_ms, Kl, layer_total_bytes, world),
+        "roofline": roofline_obj(st, wl, layer_ms, Rl * Kl, layer_bytes_total, world),
         "clocks": clocks,
-        "wall_s_timed_loop": round(t_wall, 3),
+        "wall_s_timed_loop": round(t_wall1 - t_wall0, 3),
         "_path": st.path,
     }
     return line
 
 
-def cpu_baseline(wl, device, path="decode", seconds=12.0):
-    """The oracle, as it stands, on the host cores: steps (top-k + layer) of
-    the same workload with fresh routing, on at most 4 tokens per step,
-    until ~`seconds` of timed CPU work.  The oracle runs in the mode the path
-    computes (exact for decode, block-scaled for grouped).  Expert weights
-    are quantized by the oracle from the same fp32 draws (setup, not timed)."""
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(wl, device, path="decode", seconds=8.0):
+    """The oracle, as it stands, on the host cores: single-thread (one
+    token per call) and all-core (one token per core per call, each token a
+    step of its own with fresh routing; the oracle parallelises over tokens),
+    until ~`seconds` of timed CPU work each.  The oracle runs in the mode the
+    path computes (exact for decode, block-scaled for grouped).  Expert weights
+    are quantized by the oracle from the same fp32 draws (set-up, not timed)."""
     import oracle
     from top_moe_expert_gb300 import inputs
+    if wl.fmt == "awq4":
+        return _cpu_baseline_awq(wl, seconds)
     cache = {}
 
     def expert(which, e):
@@ -672,34 +706,46 @@ def cpu_baseline(wl, device, path="decode", seconds=12.0):
             cache[(which, e)] = oracle.mxfp8_quantize(f)
         return cache[(which, e)]
 
-    if wl.fmt == "awq4":
-        return _cpu_baseline_awq(wl, seconds)
     mode = oracle.MODE_MX if path == "grouped" else oracle.MODE_EXACT
-    S = min(wl.M, 4)
-    t_total, nbytes, steps = 0.0, 0, 0
-    while t_total < seconds and steps < 64:
-        logits = inputs.router_logits(wl, 10_000 + steps)[:S]
-        ids, _ = oracle.topk_softmax(logits, wl.k)
-        experts = sorted(set(ids.reshape(-1).tolist()))
-        slot = np.full(wl.E, -1, dtype=np.int32)
-        slot[experts] = np.arange(len(experts), dtype=np.int32)
-        ws = {}
-        for which in ("w13", "w2"):
-            qs = [expert(which, e) for e in experts]
-            ws[which] = {"fmt": "mxfp8", "q": np.stack([q for q, _ in qs]),
-                         "s": np.stack([s for _, s in qs]), "slot": slot}
-        x = inputs.activations(wl, 10_000 + steps)[:S].to(torch.float64).numpy()
-        t0 = time.perf_counter()
-        ids2, w2 = oracle.topk_softmax(logits, wl.k)
-        oracle.moe_layer(x, ids2, w2, wl.E, ws["w13"], ws["w2"], mode=mode)
-        t_total += time.perf_counter() - t0
-        nbytes += len(experts) * expert_bytes(wl) + S * (4 * wl.d + 4 * wl.E)
-        steps += 1
-    threads = min(oracle.num_threads(), S)     # the oracle parallelises over tokens
-    return {"value": nbytes / t_total / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{steps} steps (top-k + layer, binary64, {'block-scaled' if mode else 'exact'} mode) "
-                      f"of {wl.name} on {S} token(s) each, fresh routing, {t_total:.1f} s timed",
-            "us_per_token": round(t_total / steps / S * 1e6, 1)}
+    ncores = os.cpu_count() or 1
+
+    def run(threads, S):
+        oracle.set_num_threads(threads)
+        t_total, nbytes, calls, seed = 0.0, 0, 0, 10_000
+        while t_total < seconds and calls < 64:
+            # S tokens, each with the routing and activation of a step of its own
+            logits = np.concatenate([inputs.router_logits(wl, seed + t)[:1] for t in range(S)])
+            x = torch.cat([inputs.activations(wl, seed + t)[:1] for t in range(S)]).to(torch.float64).numpy()
+            ids, _ = oracle.topk_softmax(logits, wl.k)
+            experts = sorted(set(ids.reshape(-1).tolist()))
+            slot = np.full(wl.E, -1, dtype=np.int32)
+            slot[experts] = np.arange(len(experts), dtype=np.int32)
+            ws = {}
+            for which in ("w13", "w2"):
+                qs = [expert(which, e) for e in experts]
+                ws[which] = {"fmt": "mxfp8", "q": np.stack([q for q, _ in qs]),
+                             "s": np.stack([s for _, s in qs]), "slot": slot}
+            t0 = time.perf_counter()
+            ids2, w2 = oracle.topk_softmax(logits, wl.k)
+            oracle.moe_layer(x, ids2, w2, wl.E, ws["w13"], ws["w2"], mode=mode)
+            t_total += time.perf_counter() - t0
+            # each token is one step of the M=1 workload: its own distinct experts
+            nbytes += sum(len(np.unique(ids[t])) * expert_bytes(wl) + 4 * wl.d + 4 * wl.E for t in range(S))
+            calls += 1
+            seed += S
+        return nbytes / t_total / 1e12, calls, t_total
+
+    v1, c1, t1 = run(1, 1)
+    vn, cn, tn = run(ncores, ncores)
+    oracle.set_num_threads(ncores)
+    return {"value": vn, "unit": "TB/s", "cores": ncores, "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": (f"{cn} calls of {ncores} tokens (each token one step of {wl.name}: top-k + layer, binary64, "
+                       f"{'block-scaled' if mode else 'exact'} mode, its own fresh routing), {ncores} OpenMP "
+                       f"threads, {tn:.1f} s timed"),
+            "single_thread": {"value": v1, "unit": "TB/s", "cores": 1,
+                              "sample": f"{c1} single-token steps, 1 thread, {t1:.1f} s timed",
+                              "us_per_token": round(t1 / c1 * 1e6, 1)},
+            "us_per_token": round(tn / (cn * ncores) * 1e6, 1)}
 
 
 def _cpu_baseline_awq(wl, seconds):
@@ -835,7 +881,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_m1")

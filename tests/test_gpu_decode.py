@@ -179,11 +179,10 @@ def test_mx_single_token_activation_scales_routes_and_counter():
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
     gs.assert_layer_close(ys[0], oracle_decode(layer, x, ids2, w))
-    if moe.moe_candidate_kernels_enabled():
-        # the one-kernel path: each call adds one arrival per CTA (one CTA
-        # per SM) to the grid-barrier counter in ws[0..8)
-        sms = torch.cuda.get_device_properties(0).multi_processor_count
-        assert ws[:8].view(torch.int64).item() == 3 * sms
+    # the one-kernel path: each call adds one arrival per CTA (one CTA per
+    # SM) to the arrival counter in ws[0..8)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ws[:8].view(torch.int64).item() == 3 * sms
 
 
 # ---- one token, 4-bit AWQ: the single-kernel path (gate/up, SwiGLU, down)
@@ -342,9 +341,8 @@ def test_one_workspace_serves_every_batch_size():
         fresh = run(*args)
         assert torch.equal(run(*args, ws=ws), fresh), (M, neuron_major)
     torch.cuda.synchronize()
-    # one-kernel single-token calls: the neuron-major layout always, the
-    # standard layout with the opt-in kernels
-    n_one_kernel = sum(1 for M, nm in calls if M == 1 and (nm or moe.moe_candidate_kernels_enabled()))
+    # one-kernel single-token calls (both layouts) each add one arrival per CTA
+    n_one_kernel = sum(1 for M, nm in calls if M == 1)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert ws[:8].view(torch.int64).item() == n_one_kernel * sms
 

@@ -331,6 +331,10 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
         const size_t a1 = decode_awq_m1_workspace(k, I);
         part = part > a1 ? part : a1;
     }
+    if (M == 1 && k <= 32) {
+        const size_t p1 = decode_pipe_workspace(k, I);
+        part = part > p1 ? part : p1;
+    }
     if (M == 1 && k <= 32 && d % 64 == 0 && I % 64 == 0) {
         const size_t x1 = decode_mx_m1_workspace(k, I);
         part = part > x1 ? part : x1;
@@ -451,6 +455,14 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     if (cand && fmt == MOE_W_AWQ4 && decode_awq_m1_eligible(M, k, d, I, w13->E))
         return decode_awq_m1_launch(x, xdt == MOE_BF16, topk_ids, topk_w, k, d, I, w13->E, w13->q, w13->scale,
                                     w13->zero, w2->q, w2->scale, w2->zero, y, ydt == MOE_FP32, ws, dev_status, s);
+    if (fmt == MOE_W_MXFP8 && decode_pipe_eligible(M, k, d, I, w13->E) && aligned(w13->scale, 16) &&
+        aligned(w2->q, 16)) {
+        // one token on the standard layout: one kernel (gate/up, SwiGLU, down)
+        return decode_pipe_launch(static_cast<const __nv_bfloat16 *>(x), d, I, w13->E, topk_ids, topk_w, nullptr,
+                                  nullptr, nullptr, k, static_cast<const uint8_t *>(w13->q),
+                                  static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
+                                  static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status, s);
+    }
     if (cand && fmt == MOE_W_MXFP8 && decode_mx_m1_eligible(M, k, d, I, w13->E) && aligned(w2->q, 16)) {
         // one token on the standard layout: one kernel (gate/up, SwiGLU, down)
         const moe_status_t st1 = decode_mx_m1_launch(
@@ -522,6 +534,20 @@ MOE_API moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, i
                                 as_stream(stream));
     }
     // one token on the standard layout: one kernel with the routing inside
+    if (M == 1 && w2->fmt == MOE_W_MXFP8 && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
+        (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
+        check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_pipe_eligible(1, k, d, I, E) &&
+        decode_pipe_route_eligible(E, k) && aligned(w13->scale, 16) && x && y && aligned(x, 16)) {
+        size_t need;
+        moe_ffn_decode_workspace_size(M, k, d, I, &need);
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return MOE_ERR_WORKSPACE;
+        return decode_pipe_launch(static_cast<const __nv_bfloat16 *>(x), d, I, E, nullptr, nullptr, logits,
+                                  topk_ids, topk_w, k, static_cast<const uint8_t *>(w13->q),
+                                  static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
+                                  static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status,
+                                  as_stream(stream));
+    }
     if (candidate_kernels_enabled() && M == 1 && w2->fmt == MOE_W_MXFP8 && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
         (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
         check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_mx_m1_eligible(1, k, d, I, E) && E >= k &&

@@ -11,9 +11,9 @@
 
 namespace moe {
 
-// Bytes at the start of a decode workspace reserved for the grid-barrier
-// counter of the one-kernel single-token paths; the other decode paths place
-// their data after them.
+// Bytes at the start of a decode workspace reserved for the arrival counter
+// of the one-kernel single-token paths (ws[0..8), zero before the first use);
+// the other decode paths place their data after them.
 constexpr size_t kWsReserved = 256;
 
 bool decode_stream_eligible(int M, int k, int d, int I, int E, const void *q13, const void *s13,
@@ -30,6 +30,17 @@ moe_status_t decode_fused_launch(const __nv_bfloat16 *x, int M, int d, int I, in
                                  const float *wts, int k, const uint8_t *q13, const uint8_t *s13,
                                  const uint8_t *q2t, const uint8_t *s2t, void *y, bool y_f32, float *partial,
                                  int32_t *dev_status, cudaStream_t stream);
+
+// single-token MXFP8 layer in one kernel on the standard layout, optionally
+// with the routing (decode_pipe.cu); ws holds the arrival counter in its first
+// 8 bytes (zero before the first use), then h past kWsReserved
+bool decode_pipe_eligible(int M, int k, int d, int I, int E);
+bool decode_pipe_route_eligible(int E, int k);
+size_t decode_pipe_workspace(int k, int I);
+moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, const int32_t *ids, const float *wts,
+                                const float *logits, int32_t *ids_out, float *wts_out, int k, const uint8_t *q13,
+                                const uint8_t *s13, const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32,
+                                void *ws, int32_t *dev_status, cudaStream_t stream);
 
 bool decode_m1_eligible(int M, int k, int d, int I, int E);
 size_t decode_m1_workspace(int d);

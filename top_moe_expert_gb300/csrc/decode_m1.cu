@@ -596,7 +596,7 @@ bool decode_m1_eligible(int M, int k, int d, int I, int E)
 
 size_t decode_m1_workspace(int d)
 {
-    return 256 + ws_round(static_cast<size_t>(device_sm_count()) * d * sizeof(float));
+    return kWsReserved + ws_round(static_cast<size_t>(device_sm_count()) * d * sizeof(float));
 }
 
 bool decode_m1_route_eligible(int E, int k)
@@ -618,7 +618,7 @@ moe_status_t decode_m1_launch(const __nv_bfloat16 *x, int d, int I, int E, const
         return MOE_ERR_UNSUPPORTED;
     uint8_t *w = static_cast<uint8_t *>(ws);
     Args a{x,  ids, wts, logits, ids_out, wts_out, q13, s13, q2t, s2t, reinterpret_cast<unsigned long long *>(w),
-           reinterpret_cast<float *>(w + 256), y, dev_status, y_f32 ? 1 : 0, k, d, I, E};
+           reinterpret_cast<float *>(w + kWsReserved), y, dev_status, y_f32 ? 1 : 0, k, d, I, E};
     auto go = [&](auto kern) -> moe_status_t {
         if (!smem_attr(reinterpret_cast<const void *>(kern), 220 * 1024))
             return MOE_ERR_CUDA;
