@@ -266,10 +266,9 @@ class Step:
             w0 = ((q13, s13, None), (q2, s2, None))
         # the single-pass small-batch kernel reads the down projection
         # neuron-major: packed once (same bytes, K-outer order)
-        self.neuron_major = (not self.awq and path == "decode" and w2_layout != "standard" and 2 <= M <= 4
-                             and d % 1024 == 0)
-        self.routed_in_layer = (not self.awq and path == "decode" and M == 1 and E <= 768
-                                and not self.neuron_major)
+        self.neuron_major = (not self.awq and path == "decode" and d % 1024 == 0 and
+                             ((w2_layout == "auto" and 2 <= M <= 4) or (w2_layout == "neuron_major" and M <= 4)))
+        self.routed_in_layer = not self.awq and path == "decode" and M == 1 and E <= 512
         lw_bytes = sum(t.numel() * t.element_size() for p in w0 for t in p if t is not None)
         self.ids_host = [self._host_ids(j) for j in range(n_inputs)]
         est = max(step_bytes(wl, ids) for ids in self.ids_host[:8])
@@ -419,6 +418,8 @@ class Step:
         if self.routed_in_layer:
             return ("moe_ffn_decode_logits: dp::pipe_kernel (top-k routing + gate/up + SwiGLU + down + "
                     "routing-weighted sum), one kernel")
+        if self.neuron_major and self.routed_in_layer:
+            return "moe_ffn_decode_logits (neuron-major W2): dm::m1_kernel, one kernel"
         if self.neuron_major:
             return "moe_ffn_decode: df::fused_kernel + df::reduce_kernel, PDL-chained"
         return "moe_ffn_decode: ds::gate_up_kernel + ds::down_kernel, PDL-chained"
@@ -888,7 +889,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "grouped"])
     ap.add_argument("--block", type=int, default=0, help="MoE block size b of the grouped path (0: automatic)")
-    ap.add_argument("--w2", default="auto", choices=["auto", "standard"],
+    ap.add_argument("--w2", default="auto", choices=["auto", "standard", "neuron_major"],
                     help="decode path: keep W2 K-contiguous (standard) instead of the neuron-major packing "
                          "small batches use by default")
     args = ap.parse_args()

@@ -68,6 +68,7 @@ constexpr int kBarRoutes = 1;                         // named barriers: routes 
 constexpr int kBarTail = 2;                           //   the compute warps
 constexpr int kBarGroup0 = 3;                         //   gate/up group g: kBarGroup0 + g
 constexpr int kBarRank = kBarGroup0 + kGroups;        //   the compute warps ranking the logits
+constexpr int kBarScales = kBarRank + 1;              //   gate/up E8M0 rows staged (wait/copy warps arrive)
 constexpr int kSmemMax = 227 * 1024;
 constexpr bool kHiLo = true;                          // h into the down projection as fp16 hi + lo
 
@@ -92,12 +93,14 @@ struct Args {
 struct Plan {
     int d, I, k, G;
     __host__ __device__ int rows_max() const { return (d + G - 1) / G; }
-    __host__ __device__ int s1() const { return kPS * (2 * d + 2 * (d / 32)); }
+    __host__ __device__ int s1() const { return kPS * 2 * d; }                   // gate rows | up rows
+    __host__ __device__ int pmax() const { return (k * I + G - 1) / G; }        // pairs of a CTA, at most
     __host__ __device__ int s2() const { return rows_max() * I; }
     __host__ __device__ static int up16(int v) { return (v + 15) & ~15; }
     __host__ __device__ int o_w2() const { return up16(k * I * 4); }            // in the ring, after h
     __host__ __device__ int o_s2s() const { return kSlots * s1(); }
-    __host__ __device__ int o_gpart() const { return o_s2s() + k * rows_max() * (I / 32) * 4; }
+    __host__ __device__ int o_gsc() const { return o_s2s() + k * rows_max() * (I / 32) * 4; }
+    __host__ __device__ int o_gpart() const { return o_gsc() + up16(pmax() * 2 * (d / 32)); }
     __host__ __device__ int o_dpart() const { return o_gpart() + kGroups * 2 * kGW * 2 * kPS * 4; }
     __host__ __device__ int o_bars() const { return o_dpart() + up16(k * rows_max() * 4); }
     __host__ __device__ int o_route() const { return o_bars() + (2 * kSlots + k + 1) * 8; }
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     float *hbuf = reinterpret_cast<float *>(smem);                       // [nv][I], the tail's h
     uint8_t *slot2 = smem + pl.o_w2();                                   // the tail's [k][RM][I] down rows
     float *s2s = reinterpret_cast<float *>(smem + pl.o_s2s());           // [k][RM][I/32] down scales
+    uint8_t *gsc = smem + pl.o_gsc();                                    // [P][2][d/32] gate/up E8M0 rows
     float *gpart = reinterpret_cast<float *>(smem + pl.o_gpart());       // [grp][2][kGW][2 kPS]
     float *dpart = reinterpret_cast<float *>(smem + pl.o_dpart());       // [k][RM]
     const uint32_t full1 = tc::smem_u32(smem + pl.o_bars());
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     if (warp == 0) {
         // ------------------------------------------------ producer
         if (lane == 0) {
-            const int64_t rowb = d, sclb = d / 32;
+            const int64_t rowb = d;
             tc::fence_proxy_async_smem();          // the ring held the routing's keys
             bool go = true;
             int s = 0;
@@ -365,34 +369,31 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                     break;
                 }
                 const int q0 = q_lo + s * kPS, q1 = q_lo + min(s * kPS + kPS, P);
-                tc::mbar_arrive_expect_tx(full1 + 8 * sl, static_cast<uint32_t>(q1 - q0) * (2 * d + 2 * (d / 32)));
+                tc::mbar_arrive_expect_tx(full1 + 8 * sl, static_cast<uint32_t>(q1 - q0) * (2 * d));
                 uint8_t *st = slot1 + sl * S1;
                 const uint32_t bar = full1 + 8 * sl;
                 for (int q = q0; q < q1;) {
-                    // a run of neurons of one route: gate rows, up rows, their E8M0 rows
+                    // a run of neurons of one route: gate rows, up rows
                     const int r = q / I, n = q - r * I, len = min(q1 - q, I - n), i = q - q0;
                     const int64_t grow = static_cast<int64_t>(r_e[r]) * 2 * I + n;
                     tc::bulk_load(tc::smem_u32(st + i * rowb), a.q13 + grow * rowb, len * rowb, bar);
                     tc::bulk_load(tc::smem_u32(st + (kPS + i) * rowb), a.q13 + (grow + I) * rowb, len * rowb, bar);
-                    tc::bulk_load(tc::smem_u32(st + 2 * kPS * rowb + i * sclb), a.s13 + grow * sclb, len * sclb, bar);
-                    tc::bulk_load(tc::smem_u32(st + 2 * kPS * rowb + (kPS + i) * sclb), a.s13 + (grow + I) * sclb,
-                                  len * sclb, bar);
                     q += len;
                 }
-                if (s == min(S, kSlots) - 1 && nrows > 0)
-                    // the ring is full: this CTA's down-projection rows of every
-                    // routed expert go to L2 now, while the gate/up rows stream
-                    for (int r = 0; r < nv; ++r)
-                        tc::bulk_prefetch_l2(a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I, nrows * I);
             }
+            // this CTA's down-projection rows of every routed expert go to L2
+            // once its last gate/up stage has landed: they stream while h is
+            // formed and exchanged, and do not slow the gate/up stream
+            if (go && S > 0)
+                go = tc::mbar_wait(full1 + 8 * ((S - 1) % kSlots), ((S - 1) / kSlots) & 1u, s_abort, kWaitNs);
+            if (go && nrows > 0)
+                for (int r = 0; r < nv; ++r)
+                    tc::bulk_prefetch_l2(a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I, nrows * I);
             // once every gate/up stage is consumed the ring is idle: the down
             // rows move from L2 into it while the grid's last CTAs finish
             for (int t = max(0, s - kSlots); t < s && go; ++t)
                 go = tc::mbar_wait(empty1 + 8 * (t % kSlots), (t / kSlots) & 1u, s_abort, kWaitNs);
             if (go && nrows > 0) {
-                if (S == 0)
-                    for (int r = 0; r < nv; ++r)
-                        tc::bulk_prefetch_l2(a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I, nrows * I);
                 tc::fence_proxy_async_smem();
                 for (int r = 0; r < nv; ++r) {
                     tc::mbar_arrive_expect_tx(full2 + 8 * r, static_cast<uint32_t>(nrows * I));
@@ -452,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             }
         }
         const int sclb = d / 32;
+        tc::named_bar(kBarScales, kCW * 32);               // the E8M0 rows are staged
         for (int s = grp, m = 0; s < S; s += kGroups, ++m) {
             const int sl = s % kSlots, buf = m & 1;
             const uint32_t ph = (s / kSlots) & 1u;
@@ -472,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
 #pragma unroll
                         for (int t = 0; t < KPL / 4; ++t)
                             acc = dot4(wq[t], xw[2 * t], xw[2 * t + 1], acc);
-                        v[i] = acc * e8m0_to_float(st[2 * kPS * d + i * sclb + (kbase >> 5)]);
+                        // E8M0 of pair s*kPS + i%kPS, gate (i < kPS) or up row, this lane's block
+                        v[i] = acc * e8m0_to_float(gsc[((s * kPS + i % kPS) * 2 + i / kPS) * sclb + (kbase >> 5)]);
                     }
                 }
                 const float tot = reduce8(v, lane) * xinv;
@@ -498,17 +501,28 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                     u += gp[w2 * 2 * kPS + kPS + lane];
                 }
                 __stcg(a.h + q_lo + s * kPS + lane, silu_mul(g, u));
-                if (atom_add_acq_rel_cta(s_done, 1u) + 1u == static_cast<uint32_t>(P)) {
-                    // every h of this CTA is written: arrive
-                    __threadfence();
+                if (atom_add_acq_rel_cta(s_done, 1u) + 1u == static_cast<uint32_t>(P))
+                    // every h of this CTA is written (the CTA-scope acquire above
+                    // orders the other lanes' stores before this release): arrive
                     red_release_add(a.ctr);
-                }
             }
         }
     } else {
         // ------------------------------------------------ wait/copy warps
         const int tw = warp - kWarpT0, tt = tid - kWarpT0 * 32;
         const int nb2 = I / 32;
+        {
+            // the gate and up E8M0 rows of this CTA's pairs, 16 bytes per load
+            const int nb1 = d / 32, w16 = nb1 / 16;            // d % 512 == 0: whole 16-byte pieces
+            for (int i = tt; i < P * 2 * w16; i += kTW * 32) {
+                const int pr = i / (2 * w16), rem = i - pr * 2 * w16, up = rem / w16, wv = rem - up * w16;
+                const int q = q_lo + pr, r = q / I, n = q - r * I;
+                const int64_t row = static_cast<int64_t>(r_e[r]) * 2 * I + n + (up ? I : 0);
+                reinterpret_cast<uint4 *>(gsc + (pr * 2 + up) * nb1)[wv] =
+                    __ldg(reinterpret_cast<const uint4 *>(a.s13 + row * nb1) + wv);
+            }
+            tc::named_arrive(kBarScales, kCW * 32);
+        }
         if constexpr (ROUTE) {
             if (tw == 0) {
                 // the renormalised weights of the chosen routes (needed only at the end)
