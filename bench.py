@@ -188,15 +188,12 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 
 SRC_FILES = {
-    "decode": ("decode.cu", "decode_fused.cu", "decode_stream.cu", "decode_m1.cu", "decode_mx_m1.cu",
-               "decode_mx_m1.cuh", "decode_awq_m1.cuh", "decode_internal.h", "topk.cu", "topk.cuh", "common.cuh",
-               "tc.cuh", "attr.h"),
+    "decode": ("decode.cu", "decode_pipe.cu", "decode_stream.cu", "decode_internal.h", "topk.cu", "topk.cuh",
+               "common.cuh", "tc.cuh", "attr.h"),
     "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh",
                 "attr.h"),
-    "awq": ("grouped_awq.cu", "grouped_awq_mma.cu", "grouped_awq_mma.cuh", "decode_awq_m1.cuh", "grouped.cu",
-            "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
-    "awq_decode": ("decode.cu", "decode_awq_m1.cu", "decode_awq_m1.cuh", "decode_internal.h", "common.cuh",
-                   "tc.cuh", "attr.h"),
+    "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
+    "awq_decode": ("decode.cu", "decode_internal.h", "common.cuh", "tc.cuh", "attr.h"),
 }
 
 
@@ -240,7 +237,7 @@ class Step:
     grouped layer; with the fixed-routing AWQ workloads, the layer alone (with
     its alignment on the grouped path)."""
 
-    def __init__(self, wl, n_inputs, device, path: str = "decode", block: int = 0, w2_layout: str = "auto"):
+    def __init__(self, wl, n_inputs, device, path: str = "decode", block: int = 0):
         import top_moe_expert_gb300 as moe
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
@@ -264,11 +261,7 @@ class Step:
                 moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w13", e, device), q13[e], s13[e])
                 moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), q2[e], s2[e])
             w0 = ((q13, s13, None), (q2, s2, None))
-        # the single-pass small-batch kernel reads the down projection
-        # neuron-major: packed once (same bytes, K-outer order)
-        self.neuron_major = (not self.awq and path == "decode" and d % 1024 == 0 and
-                             ((w2_layout == "auto" and 2 <= M <= 4) or (w2_layout == "neuron_major" and M <= 4)))
-        self.routed_in_layer = not self.awq and path == "decode" and M == 1 and E <= 512
+        self.routed_in_layer = not self.awq and path == "decode" and M == 1 and E <= 768
         lw_bytes = sum(t.numel() * t.element_size() for p in w0 for t in p if t is not None)
         self.ids_host = [self._host_ids(j) for j in range(n_inputs)]
         est = max(step_bytes(wl, ids) for ids in self.ids_host[:8])
@@ -284,8 +277,6 @@ class Step:
             else:
                 w13 = moe.Weights(moe.MOE_W_MXFP8, a13, b13)
                 w2 = moe.Weights(moe.MOE_W_MXFP8, a2, b2)
-                if self.neuron_major:
-                    w2 = moe.moe_mxfp8_transpose(w2)
             sfa = moe.moe_grouped_prepare(w13, w2) if (path == "grouped" and not self.awq) else (None, None)
             self.layers.append((w13, w2, sfa))
         del w0
@@ -418,10 +409,6 @@ class Step:
         if self.routed_in_layer:
             return ("moe_ffn_decode_logits: dp::pipe_kernel (top-k routing + gate/up + SwiGLU + down + "
                     "routing-weighted sum), one kernel")
-        if self.neuron_major and self.routed_in_layer:
-            return "moe_ffn_decode_logits (neuron-major W2): dm::m1_kernel, one kernel"
-        if self.neuron_major:
-            return "moe_ffn_decode: df::fused_kernel + df::reduce_kernel, PDL-chained"
         return "moe_ffn_decode: ds::gate_up_kernel + ds::down_kernel, PDL-chained"
 
     def path_text(self) -> str:
@@ -435,8 +422,6 @@ class Step:
             return "expert-centric grouped (topk + align + act-quant + tcgen05 GEMM1/GEMM2 + combine, b=%d)" % self.b
         if self.routed_in_layer:
             return "single-token decode: routing + gate/up + SwiGLU + down in one kernel, h exchanged through L2"
-        if self.neuron_major:
-            return "single-pass decode (topk + fused gate/up/down + partial reduction)"
         return "output-centric decode (topk + gate/up + down)"
 
     def launches_per_step(self) -> int:
@@ -519,7 +504,7 @@ def run_ours(args, rank, world, device):
         block = block or b
     Kg = min(K, 1000 if wl.M <= 64 else 50)              # steps per captured graph
     n_inputs = min(Kg + W, 1024 if wl.M <= 64 else 16)
-    st = Step(wl, n_inputs, device, path, block, args.w2)
+    st = Step(wl, n_inputs, device, path, block)
     s = st.stream
 
     # ---- the timed steps: graphs of Kg steps back to back (inputs already in
@@ -889,9 +874,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "grouped"])
     ap.add_argument("--block", type=int, default=0, help="MoE block size b of the grouped path (0: automatic)")
-    ap.add_argument("--w2", default="auto", choices=["auto", "standard", "neuron_major"],
-                    help="decode path: keep W2 K-contiguous (standard) instead of the neuron-major packing "
-                         "small batches use by default")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

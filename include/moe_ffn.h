@@ -44,12 +44,6 @@
  *                zero int32 [E][N/8][K/128], the zero of row 8a+i in nibble i
  *                of word a; weight = (q - zero) * scale.  K % 128 == 0,
  *                N % 8 == 0.
- *   MOE_W_MXFP8_T: the same MXFP8 values stored K-outer ("transposed"):
- *                q uint8 [E][K][N], scale uint8 [E][K/32][N] (the E8M0 of
- *                block (n, k/32) at [k/32][n]).  Same bytes, different order;
- *                produced from MOE_W_MXFP8 by moe_mxfp8_transpose.  Accepted
- *                for w2 by moe_ffn_decode (its single-pass small-batch path
- *                streams each neuron's down-projection column contiguously).
  *   MOE_W_NVFP4S: paired 4:8 sparse NVFP4 ("Hardware-Native Joint Sparse-
  *                Quantization ...", App. A, Eq. 6 and 7): in every group of
  *                8 weights along K two adjacent pairs are kept, 2.75 bits
@@ -88,7 +82,8 @@ typedef enum {
     MOE_ERR_TIMEOUT = 6       /* a bounded device wait expired (dev_status[1]) */
 } moe_status_t;
 
-typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1, MOE_W_MXFP8_T = 2, MOE_W_NVFP4S = 3 } moe_wfmt_t;
+/* (value 2 is retired: it named an MXFP8 layout stored K-outer) */
+typedef enum { MOE_W_MXFP8 = 0, MOE_W_AWQ4 = 1, MOE_W_NVFP4S = 3 } moe_wfmt_t;
 typedef enum { MOE_BF16 = 0, MOE_FP16 = 1, MOE_FP32 = 2 } moe_dtype_t;
 typedef enum { MOE_PATH_DECODE = 0, MOE_PATH_GROUPED = 1 } moe_path_t;
 
@@ -107,20 +102,6 @@ typedef struct {
 const char *moe_status_string(moe_status_t s);
 /* MOE_FFN_ABI_VERSION of the loaded library. */
 int32_t moe_abi_version(void);
-/* Opt-in kernels.  Five kernels are built but taken by dispatch only on
- * request: for MOE_W_MXFP8 on the standard layout, the one-kernel path for
- * M == 1 (moe_ffn_decode and moe_ffn_decode_logits) and the aligned
- * small-batch path for 2 <= M <= 64 (moe_ffn_decode); for MOE_W_AWQ4, the
- * one-kernel path for M == 1 and the aligned small-batch path for
- * 2 <= M <= 64 (moe_ffn_decode), and the kernel for blocks of b <= 16 rows
- * (moe_ffn_grouped).  The request is the environment variable
- * MOE_FFN_CANDIDATE_KERNELS set to exactly "1"; the library reads it once,
- * at its first dispatch, and keeps the answer for the life of the process.
- * Without it the same calls, with the same arguments, workspace sizes and
- * tolerances, run the other kernels listed for each case below.  Returns 1
- * when the opt-in kernels are taken, else 0. */
-int32_t moe_candidate_kernels_enabled(void);
-
 /* ---------------------------------------------------------------- routing
  * Top-k softmax routing ("Warp decode", section on the conventional MoE
  * path: each token selects k of E experts, e.g. 8 of 128).
@@ -170,12 +151,6 @@ moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, int32_t k,
 moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_t K,
                                 uint8_t *q, uint8_t *s, void *stream);
 
-/* Re-layout of MXFP8 weights into MOE_W_MXFP8_T (a one-time packing step,
- * like the offline packing of expert weights on the sparse-quantization
- * page, App. D.1).  w: MOE_W_MXFP8 [E][N][K]; q_t: uint8 [E][K][N];
- * scale_t: uint8 [E][K/32][N] (caller-allocated device buffers). */
-moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_t, void *stream);
-
 /* ------------------------------------------------------------ the layer
  * Output-centric decode path ("Warp decode", sections on what changed and
  * how the two kernels work): parallelism over outputs, weight rows streamed
@@ -185,8 +160,7 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  *   x        [M][d] of xdt (MOE_BF16; MOE_FP16 or MOE_BF16 for AWQ)
  *   topk_ids int32 [M][k], topk_w fp32 [M][k]
  *   w13      N = 2I, K = d (MOE_W_MXFP8 or MOE_W_AWQ4)
- *   w2       N = d, K = I, same format as w13, or MOE_W_MXFP8_T with
- *            MXFP8 w13 (then M <= 4, M*k <= 64 and d % 1024 == 0)
+ *   w2       N = d, K = I, same format as w13
  *   y        [M][d] of ydt (MOE_BF16 or MOE_FP32)
  *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned; its
  *            first 256 bytes must be zero before the first call that uses
@@ -198,41 +172,24 @@ moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_
  *            sized for the largest batch serves calls of any batch size
  *            and layout in turn.
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
- * Kernels by case (cases marked [opt-in] are taken only when
- * moe_candidate_kernels_enabled() is 1): MOE_W_MXFP8 (standard layout) with
- * M == 1 [opt-in] -> one kernel
- * (gate/up dots on mma.sync with each E4M3 pair converted exactly to f16 and
- * the E8M0 scale applied per 32-value block in FP32, a grid-wide barrier
- * whose counter lives in ws[0..8), then the down projection from W2 rows
- * staged in shared memory; with moe_ffn_decode_logits the routing runs in
- * it too), when its shared-memory plan fits;
- * MOE_W_MXFP8 (standard layout) with 2 <= M <= 64 [opt-in] -> the routes aligned
- * into blocks of 16 rows per expert (moe_align_block_size, which counts the
- * invalid routes), one kernel for both GEMMs (mma.sync, each block one
- * M-tile, x and h unquantized as above, per-block hand-off counters), and
- * the slot-ordered combine; ws past its first 256 bytes then holds that
- * alignment, the gate/up values and the per-route down rows
- * (moe_ffn_decode_workspace_size);
- * MOE_W_AWQ4 with 2 <= M <= 64 [opt-in] -> the same chain with the small-block AWQ
- * kernel of moe_ffn_grouped (raw 4-bit codes as f16, zero and scale applied
- * in FP32 per group, x and h unquantized);
- * w2 in MOE_W_MXFP8_T with M == 1, d in {1024, 2048} -> one
- * streaming kernel (each warp owns whole neurons: gate/up dots and the
- * down-column outer product; per-SM partial outputs reduced in a fixed order
- * after a grid-wide barrier whose counter lives in ws[0..8)); other
- * MOE_W_MXFP8_T cases -> one streaming pass (gate/up rows and down columns of
- * each neuron together, per-SM partial outputs) plus a fixed-order reduction
- * kernel; MXFP8 with M*k <= 512 -> a gate/up kernel and a
- * down kernel chained by programmatic dependent launch; AWQ4 with M == 1
- * [opt-in] -> one kernel (gate/up dots on f16 mma.sync over the raw 4-bit codes with the
- * zero folded out in FP32, a grid-wide barrier whose counter lives in
- * ws[0..8), then the down projection), when its shared-memory plan fits;
- * MOE_W_NVFP4S [opt-in] -> a gate/up kernel and a down kernel, one warp per
+ * Kernels by case: MOE_W_MXFP8 (standard layout) with M == 1,
+ * (d, I) in {(512, 256), (1024, 512), (2048, 512), (2048, 768)}, k <= 8 or
+ * so (the shared-memory plan decides) -> one kernel, one CTA per SM (each
+ * CTA an even share of the (route, neuron) pairs: gate/up rows streamed by
+ * cp.async.bulk, h = SiLU(g)*u written to ws past its first 256 bytes, one
+ * arrival per CTA on a counter in ws[0..8); then each CTA forms its own
+ * d / #SM output rows of every route's down projection from h staged in
+ * shared memory as fp16 after an exact power-of-two rescale per route, and
+ * the routing-weighted sum over the k slots; with moe_ffn_decode_logits the
+ * routing runs in it too);
+ * MXFP8 with M*k <= 512 -> a gate/up kernel and a
+ * down kernel chained by programmatic dependent launch;
+ * MOE_W_NVFP4S -> a gate/up kernel and a down kernel, one warp per
  * intermediate / output scalar, 16-byte loads of 64 packed weights, the
  * kept values decoded on the fly, FP32 sums, h in ws past its first 256
  * bytes; d % 64 == 0, I % 64 == 0, x MOE_BF16 or MOE_FP16;
  * otherwise one warp per intermediate / output scalar.  Every output's summation order is fixed
- * by the shapes, the path and (single-pass path) the set of routed experts,
+ * by the shapes, the path and (one-kernel path) the grid size,
  * so identical inputs give identical bits; the two-kernel and per-scalar
  * paths are also independent of the other tokens in the batch.
  * Limits: d % 512 == 0 and I % 32 == 0 (MXFP8); d % 1024 == 0 and
@@ -248,10 +205,11 @@ moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
  * moe_topk_softmax(logits, M, w13->E, k, topk_ids, topk_w) followed by
  * moe_ffn_decode(x, ..., topk_ids, topk_w, ...).  The whole decode step of
  * "Warp decode" (section on the conventional MoE path: route, then the
- * experts): for a single token (M == 1) on the single-pass layout
- * (w2 MOE_W_MXFP8_T, d in {1024, 2048}, E <= 512) it is one kernel that
- * routes the token itself in every CTA (on the standard layout too when
- * moe_candidate_kernels_enabled() is 1); otherwise it launches the two calls.
+ * experts): for a single token (M == 1) with the shapes of moe_ffn_decode's
+ * one-kernel case and E <= 768 it is one kernel that routes the token itself
+ * in every CTA (each CTA ranks the logits: an expert's slot is the number of
+ * experts with a larger logit, or an equal one and a lower id); otherwise it
+ * launches the two calls.
  *   logits   fp32 [M][E] router logits, E = w13->E
  *   topk_ids int32 [M][k], topk_w fp32 [M][k]: outputs (the routing used)
  *   other arguments and the workspace contract as moe_ffn_decode. */
@@ -259,6 +217,18 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
                                    int32_t k, const moe_weights_t *w13, const moe_weights_t *w2,
                                    int32_t *topk_ids, float *topk_w, void *y, int32_t ydt, void *ws,
                                    size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/* Failure-detection test hook (no counterpart on the pages).  The one-kernel
+ * single-token path waits, in every CTA, until all CTAs of the grid have
+ * arrived on the counter in ws[0..8) -- a wait bounded by a time limit of
+ * about 2 s, after which the CTA stops, writes MOE_ERR_TIMEOUT to
+ * dev_status[1] and returns, leaving the context usable.  This call makes
+ * the launches that follow it expect n arrivals more than the grid provides,
+ * so that a test can make that wait run out without faulting or hanging the
+ * GPU; n = 0 (the default) restores normal operation.  The counter still
+ * ends each launch at a multiple of the grid size, so the workspace stays
+ * valid.  Process-wide; 0 <= n <= 1024, else MOE_ERR_INVALID_ARG. */
+moe_status_t moe_debug_arrival_shortfall(int32_t n);
 
 /* ------------------------------------------------- expert-centric path
  * Grouped path for larger batches ("Hardware-Native Joint Sparse-
@@ -313,19 +283,6 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
  *   Extra limits: b <= 128, d % 256 == 0, d / 128 <= 64, I / 128 <= 64,
  *   and b <= 112 when d > 8064 (MOE_ERR_UNSUPPORTED); scale and zero arrays
  *   16-byte aligned (MOE_ERR_INVALID_ARG).
- *   Blocks of b <= 16 rows take a different kernel when its shared-memory
- *   plan fits and moe_candidate_kernels_enabled() is 1 (d and I up to about 3.5K): each block is one M-tile of
- *   mma.sync m16n8k16 (f16 x f16, FP32 accumulate) whose B operand is the raw
- *   4-bit codes as f16 (1024 + q); the zero, the offset and the scale are
- *   applied in FP32 once per group of 128, x and h enter as f16 after an
- *   exact per-row power-of-two rescale (h as an f16 hi + lo pair), so no
- *   value is rounded to fp16 beyond that split.  Its ws is
- *   [D | GU | Yr], each part rounded up to 256 bytes:
- *     D  int32 [cap_rows/b]     gate/up units finished per block (zeroed by
- *                               the call itself)
- *     GU f32 [M*k][2I]          gate and up values per route
- *     Yr f32 [M*k][d]           w_route * (W2 h) per route
- *   and d % 256 need not hold.
  * Limits: d % 128 == 0, I % 128 == 0, M * d / 4 <= INT32_MAX
  * (MOE_ERR_UNSUPPORTED otherwise); x and y 16-byte aligned
  * (MOE_ERR_INVALID_ARG otherwise). */

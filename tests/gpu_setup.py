@@ -30,13 +30,6 @@ def need_gpu():
     moe.lib()
 
 
-def need_candidates():
-    """Skip a test of an opt-in kernel's own behaviour unless the library
-    takes the opt-in kernels (MOE_FFN_CANDIDATE_KERNELS=1)."""
-    if not moe.moe_candidate_kernels_enabled():
-        pytest.skip("opt-in kernels not requested (MOE_FFN_CANDIDATE_KERNELS=1)")
-
-
 def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
     a = np.abs(v)
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))

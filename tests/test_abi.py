@@ -62,21 +62,13 @@ def test_decode_workspace_size():
     # [M*k][I] f32 (the two-kernel paths); d % 1024 != 0 rules out the
     # single-pass path and its per-SM partial outputs
     assert moe.moe_ffn_decode_workspace_size(65, 8, 512, 768) == 256 + 65 * 8 * 768 * 4
-    # one token: the single-kernel MXFP8 path's barrier counter (256 B) and
-    # phase-1 pieces [k * 2I / 8][4][8] f32
-    assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 256 + 8 * (2 * 768 // 8) * 4 * 8 * 4
+    # one token: the counter (256 B), then h [k][I] f32 of the single-kernel path
+    assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 256 + 8 * 768 * 4
     assert moe.moe_ffn_decode_workspace_size(3, 8, 512, 100) % 256 == 0
-    # 2 <= M <= 64: [align ws | sorted | expert ids | npp | done | gu | yr] with the
-    # alignment capacity of blocks of 16 rows when every route has its own expert
-    for M, k, d, I in ((2, 8, 512, 768), (64, 8, 2048, 768)):
-        mk = M * k
-        cap_rows = mk * 16
-        small = (_r256(cap_rows * 4) + _r256(mk * 4) + 256 + _r256(mk * 4) + _r256(mk * 2 * I * 4)
-                 + _r256(mk * d * 4))
-        assert moe.moe_ffn_decode_workspace_size(M, k, d, I) == 256 + max(small, mk * I * 4)
-    # one token, d % 1024 == 0: at least the single-token AWQ kernel's barrier
-    # counter (256 B) and its phase-1 pieces [k * 2I / 8][4][8] f32
-    assert moe.moe_ffn_decode_workspace_size(1, 8, 2048, 768) >= 256 + 8 * (2 * 768 // 8) * 4 * 8 * 4
+    # 2 <= M <= 64, d % 1024 != 0: the counter, then h [M*k][I] f32
+    for M, k, d, I in ((2, 8, 512, 768), (64, 8, 512, 768)):
+        assert moe.moe_ffn_decode_workspace_size(M, k, d, I) == 256 + _r256(M * k * I * 4)
+    assert moe.moe_ffn_decode_workspace_size(1, 8, 2048, 768) == 256 + 8 * 768 * 4
 
 
 def _r256(n):
@@ -86,10 +78,9 @@ def _r256(n):
 @pytest.mark.parametrize("M,k,d,I,b", [(21, 8, 2048, 768, 8), (64, 8, 2048, 768, 16), (512, 8, 2048, 768, 64),
                                        (8, 8, 7168, 2048, 16), (3, 4, 1024, 256, 136)])
 def test_grouped_workspace_size_matches_documented_layout(M, k, d, I, b):
-    """moe_ffn_grouped_workspace_size is the largest of the documented
-    layouts: MXFP8 [Xq | Xs | Hq | Hs | Yr | D], AWQ [Xg | Hg | Yr | D] and, for
-    b <= 16, the AWQ mma.sync layout [D | GU | Yr], each part rounded up to 256
-    bytes."""
+    """moe_ffn_grouped_workspace_size is the larger of the documented
+    layouts: MXFP8 [Xq | Xs | Hq | Hs | Yr | D] and AWQ [Xg | Hg | Yr | D],
+    each part rounded up to 256 bytes."""
     cap_rows = moe.moe_align_capacity(M, k, 128, b)[0]
     cap_blocks = cap_rows // b
     n_mma = (b + 15) // 16 * 16
@@ -97,8 +88,7 @@ def test_grouped_workspace_size_matches_documented_layout(M, k, d, I, b):
     mx = (_r256(cap_rows * d) + _r256(cap_blocks * (d // 128) * nsf * 512) + _r256(cap_rows * I)
           + _r256(cap_blocks * (I // 128) * nsf * 512) + _r256(M * k * d * 4) + _r256(cap_blocks * 4))
     awq = _r256(cap_rows * d * 2) + _r256(cap_rows * I * 2) + _r256(M * k * d * 4) + _r256(cap_blocks * 4)
-    small = _r256(cap_blocks * 4) + _r256(M * k * 2 * I * 4) + _r256(M * k * d * 4) if b <= 16 else 0
-    assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(mx, awq, small)
+    assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(mx, awq)
 
 
 def test_host_validation_rejects_before_launch(L):
@@ -148,32 +138,17 @@ def test_python_layout_helper_matches_library():
         assert moe.moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) == max(L["total"], awq)
 
 
-@pytest.mark.parametrize("value,expect", [(None, 0), ("1", 1), ("0", 0), ("yes", 0)])
-def test_candidate_kernel_switch(L, value, expect):
-    """The opt-in kernels are taken only when MOE_FFN_CANDIDATE_KERNELS is
-    exactly "1"; the library reads it once per process (a fresh process per
-    case here)."""
-    import subprocess
-    import sys
-    env = {k: v for k, v in os.environ.items() if k != "MOE_FFN_CANDIDATE_KERNELS"}
-    if value is not None:
-        env["MOE_FFN_CANDIDATE_KERNELS"] = value
-    code = "import top_moe_expert_gb300 as m; print(m.moe_candidate_kernels_enabled())"
-    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, check=True)
-    assert out.stdout.strip() == str(bool(expect))
-
-
 def test_select_path_at_the_measured_crossover(L):
-    """Path choice (host only): MXFP8 takes the output-centric path up to two
-    tokens and the grouped path from there; 4-bit AWQ takes the grouped
-    path.  The block size is twice the expected rows per expert rounded up
+    """Path choice (host only): MXFP8 takes the output-centric path for one
+    token and the grouped path from two; 4-bit AWQ takes the grouped path.  The block size is twice the expected rows per expert rounded up
     to a power of two within the format's range."""
     D, G = moe.MOE_PATH_DECODE, moe.MOE_PATH_GROUPED
     mx, awq = moe.MOE_W_MXFP8, moe.MOE_W_AWQ4
     sel = lambda M, fmt=mx, k=8, E=128, d=2048, I=768: moe.moe_ffn_select_path(M, k, E, d, I, fmt)
-    assert sel(1) == (D, 0) and sel(2) == (D, 0)
-    # 2*M*k/E rows per expert: 0.5 .. 64 -> 16 up to 64; 128 caps
-    assert [sel(M) for M in (3, 4, 64, 256, 512, 16384)] == [(G, 16), (G, 16), (G, 16), (G, 32), (G, 64), (G, 128)]
+    assert sel(1) == (D, 0)
+    # 2*M*k/E rows per expert: 0.25 .. 64 -> 16 up to 64; 128 caps
+    assert [sel(M) for M in (2, 3, 4, 64, 256, 512, 16384)] == [(G, 16), (G, 16), (G, 16), (G, 16), (G, 32), (G, 64),
+                                                                 (G, 128)]
     assert sel(0) == (D, 0)                                  # an empty batch: the cheap path
     # AWQ: grouped at every M; fixture A (M=21, k=8, E=128) gets b = 8
     assert sel(1, awq) == (G, 8) and sel(21, awq) == (G, 8) and sel(512, awq) == (G, 64)
@@ -188,4 +163,4 @@ def test_select_path_at_the_measured_crossover(L):
     with pytest.raises(moe.MoeError):
         sel(21, awq, d=1152, I=256)                          # AWQ: neither (d % 256, d % 1024)
     with pytest.raises(moe.MoeError):
-        moe.moe_ffn_select_path(4, 8, 128, 2048, 768, moe.MOE_W_MXFP8_T)
+        moe.moe_ffn_select_path(4, 8, 128, 2048, 768, 2)       # the retired K-outer MXFP8 layout

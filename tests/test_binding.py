@@ -16,7 +16,7 @@ import torch
 
 import top_moe_expert_gb300 as moe
 
-_LAUNCHING = {"moe_topk_softmax", "moe_align_block_size", "moe_mxfp8_quantize", "moe_mxfp8_transpose",
+_LAUNCHING = {"moe_topk_softmax", "moe_align_block_size", "moe_mxfp8_quantize",
               "moe_ffn_decode", "moe_ffn_decode_logits", "moe_ffn_decode_noalloc", "moe_grouped_prepare",
               "moe_ffn_grouped"}
 
@@ -78,7 +78,6 @@ def test_valid_calls_reach_the_library_once(rec):
     moe.moe_topk_softmax(torch.zeros((M, E)), k)
     aligned = moe.moe_align_block_size(ids, E, 8)
     moe.moe_mxfp8_quantize(torch.zeros((5, 64)))
-    moe.moe_mxfp8_transpose(w2)
     y = moe.moe_ffn_decode(x, ids, w, w13, w2, out_dtype=torch.float32)
     moe.moe_ffn_decode_logits(torch.zeros((M, E)), x, k, w13, w2)
     moe.moe_ffn_decode_noalloc(x, ids, w, w13, w2)
@@ -88,12 +87,12 @@ def test_valid_calls_reach_the_library_once(rec):
     moe.moe_ffn_decode(x.half(), ids, w, a13, a2)
     moe.moe_ffn_grouped(x.half(), ids, w, a13, a2, None, None, aligned, 8)
     names = [c[0] for c in rec.calls]
-    assert names == ["moe_topk_softmax", "moe_align_block_size", "moe_mxfp8_quantize", "moe_mxfp8_transpose",
+    assert names == ["moe_topk_softmax", "moe_align_block_size", "moe_mxfp8_quantize",
                      "moe_ffn_decode", "moe_ffn_decode_logits", "moe_ffn_decode_noalloc", "moe_grouped_prepare",
                      "moe_ffn_grouped", "moe_ffn_decode", "moe_ffn_grouped"]
     assert y.shape == (M, d) and y.dtype == torch.float32
     # the decode call passes M, d, k and the workspace size in bytes
-    args = rec.calls[4][1]
+    args = rec.calls[3][1]
     assert (args[2], args[3], args[6]) == (M, d, k)
     assert args[12] == moe.moe_ffn_decode_workspace_size(M, k, d, I)
 

@@ -185,6 +185,35 @@ def test_mx_single_token_activation_scales_routes_and_counter():
     assert ws[:8].view(torch.int64).item() == 3 * sms
 
 
+def test_single_token_wait_runs_out_and_reports_timeout():
+    """Failure detection without a GPU fault: the one-kernel path's counter
+    wait is bounded.  Made to expect one arrival more than the grid gives, it
+    gives up after its time limit, reports MOE_ERR_TIMEOUT in dev_status[1]
+    and returns; the context stays usable and the workspace valid, so the
+    next call on the same workspace matches the oracle."""
+    wl = inputs.TINY
+    layer = mx_layer(wl)
+    x = inputs.activations(wl)[:1]
+    ids, w = gs.routing(wl)
+    ids, w = ids[:1], w[:1]
+    ws = torch.zeros(moe.moe_ffn_decode_workspace_size(1, wl.k, wl.d, wl.I), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    moe.moe_debug_arrival_shortfall(1)
+    try:
+        run_decode(layer, x, ids, w, torch.float32, ws=ws, dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_debug_arrival_shortfall(0)
+    assert st.tolist() == [0, 6]                                   # MOE_ERR_TIMEOUT
+    assert ws[:8].view(torch.int64).item() == sms                  # every CTA still arrived once
+    st.zero_()
+    y = run_decode(layer, x, ids, w, torch.float32, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.tolist() == [0, 0]
+    gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
+
+
 # ---- one token, 4-bit AWQ: the single-kernel path (gate/up, SwiGLU, down)
 
 AWQ_M1 = inputs.Workload("awq_m1_d2048_i768_e128_k8", M=1, d=2048, I=768, E=128, k=8, fmt="awq4", seed=3)
@@ -246,11 +275,6 @@ def test_awq_single_token_routes_repeats_and_barrier_counter():
     for y in ys[1:]:
         assert torch.equal(y, ys[0])                              # repeats are bit-identical
     gs.assert_layer_close(ys[0], oracle_awq(layer, x, ids, w))
-    if moe.moe_candidate_kernels_enabled():
-        # the one-kernel path: each call adds one arrival per CTA (one CTA
-        # per SM) to the grid-barrier counter in ws[0..8)
-        sms = torch.cuda.get_device_properties(0).multi_processor_count
-        assert ws[:8].view(torch.int64).item() == 3 * sms
     # no valid route: y = 0
     y0 = run_awq(layer, x, np.array([[-1, wl.E, 99, -5]], dtype=np.int32), w, ws=ws)
     torch.cuda.synchronize()
@@ -266,129 +290,47 @@ def test_large_expert_decode(wl):
     gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
 
 
-# ------------------------------------------------ single-pass path (W2 packed K-outer)
-
-def test_transpose_is_a_pure_relayout():
-    layer = mx_layer(inputs.TINY)
-    t = moe.moe_mxfp8_transpose(layer.w2)
-    assert torch.equal(t.q, layer.q2.transpose(1, 2).contiguous())
-    assert torch.equal(t.scale, layer.s2.transpose(1, 2).contiguous())
-
-
-def _fused_layer(seed):
-    layer = mx_layer(dataclasses.replace(inputs.DECODE, name=f"fused_layer_{seed}", seed=seed))
-    if not hasattr(layer, "w2t"):
-        layer.w2t = moe.moe_mxfp8_transpose(layer.w2)
-    return layer
-
-
-def run_fused(layer, x, ids, w, out_dtype, **kw):
-    return moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
-                              layer.w13, layer.w2t, out_dtype=out_dtype, **kw)
-
-
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
-def test_fused_decode_matches_oracle(M):
-    layer = _fused_layer(5)
-    wl = dataclasses.replace(inputs.DECODE, name=f"fused_m{M}", M=M, seed=5)
-    for step in range(2):
-        x = inputs.activations(wl, step)
-        ids, w = gs.routing(wl, step)
-        y = run_fused(layer, x, ids, w, torch.float32)
-        gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
-
-
-def test_fused_decode_duplicates_invalid_bf16_and_repeatability():
-    layer = _fused_layer(5)
-    wl = dataclasses.replace(inputs.DECODE, name="fused_m3", M=3, seed=6)
-    x = inputs.activations(wl)
-    ids, w = gs.routing(wl)
-    ids = ids.copy()
-    ids[0, 1] = ids[0, 0]            # one expert twice for token 0 (more routes than kept in registers)
-    ids[1, :3] = ids[2, :3]          # tokens sharing experts
-    ids[2, 5] = -7                   # invalid route
-    st = torch.zeros(2, dtype=torch.int32, device="cuda")
-    y = run_fused(layer, x, ids, w, torch.bfloat16, dev_status=st)
-    torch.cuda.synchronize()
-    assert st.tolist() == [1, 0]
-    gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
-    ys = {hashlib.sha256(run_fused(layer, x, ids, w, torch.float32).cpu().numpy().tobytes()).hexdigest()
-          for _ in range(4)}
-    assert len(ys) == 1
-    # M=1 with a duplicated expert exercises the per-batch flush
-    x1 = inputs.activations(wl, 3)[:1]
-    ids1 = np.array([[4, 4, 9, 100, 4, 17, 33, 90]], dtype=np.int32)
-    w1 = np.full((1, 8), 0.125, dtype=np.float32)
-    gs.assert_layer_close(run_fused(layer, x1, ids1, w1, torch.float32), oracle_decode(layer, x1, ids1, w1))
-
+# ------------------------------------------------ workspace reuse, routing in the layer call
 
 def test_one_workspace_serves_every_batch_size():
     """One workspace, sized for the largest batch, reused by calls of other
-    batch sizes and both W2 layouts in turn: every output equals the one
-    computed with a fresh workspace, and the grid-barrier counter in
-    ws[0..8) holds exactly one arrival per CTA for each call of a one-kernel
-    single-token path (the other paths keep their data past ws[256])."""
-    layer = _fused_layer(5)
+    batch sizes in turn: every output equals the one computed with a fresh
+    workspace, and the arrival counter in ws[0..8) holds exactly one arrival
+    per CTA for each call of the one-kernel single-token path (the other
+    paths keep their data past ws[256])."""
+    layer = mx_layer(dataclasses.replace(inputs.DECODE, name="ws_reuse_layer", seed=5))
     wl = dataclasses.replace(inputs.DECODE, name="ws_reuse_m8", M=8, seed=7)
     x = inputs.activations(wl)
     ids, w = gs.routing(wl)
     ws = torch.zeros(max(moe.moe_ffn_decode_workspace_size(M, wl.k, wl.d, wl.I) for M in (1, 3, 4, 8)),
                      dtype=torch.uint8, device="cuda")
-    calls = [(1, True), (3, True), (8, False), (1, True), (4, False), (1, False), (1, True)]
-    for M, neuron_major in calls:
-        run = run_fused if neuron_major else run_decode
+    calls = [1, 3, 8, 1, 4, 1, 1]
+    for M in calls:
         args = (layer, x[:M], ids[:M], w[:M], torch.float32)
-        fresh = run(*args)
-        assert torch.equal(run(*args, ws=ws), fresh), (M, neuron_major)
+        fresh = run_decode(*args)
+        assert torch.equal(run_decode(*args, ws=ws), fresh), M
     torch.cuda.synchronize()
-    # one-kernel single-token calls (both layouts) each add one arrival per CTA
-    n_one_kernel = sum(1 for M, nm in calls if M == 1)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert ws[:8].view(torch.int64).item() == n_one_kernel * sms
+    assert ws[:8].view(torch.int64).item() == calls.count(1) * sms
 
 
-def test_fused_decode_large_expert_m1():
-    wl = inputs.LARGE_M1
-    ids, w = gs.routing(wl)
-    layer = mx_layer(wl, experts=tuple(np.unique(ids).tolist()))
-    w2t = moe.moe_mxfp8_transpose(layer.w2)
-    x = inputs.activations(wl)
-    y = moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
-                           layer.w13, w2t, out_dtype=torch.bfloat16)
-    del w2t
-    gs.assert_layer_close(y, oracle_decode(layer, x, ids, w))
-
-
-def test_fused_path_rejects_large_batches():
-    layer = _fused_layer(5)
-    wl = dataclasses.replace(inputs.DECODE, name="fused_m16", M=16, seed=5)
-    x = inputs.activations(wl)
-    ids, w = gs.routing(wl)
-    with pytest.raises(moe.MoeError) as ei:
-        run_fused(layer, x, ids, w, torch.float32)
-    assert ei.value.status == 2
-
-
-# ------------------------------------------------ routing fused into the layer call
-
-@pytest.mark.parametrize("M,transposed", [(1, True), (1, False), (3, True)])
-def test_decode_logits_equals_topk_then_decode(M, transposed):
+@pytest.mark.parametrize("M", [1, 3])
+def test_decode_logits_equals_topk_then_decode(M):
     """moe_ffn_decode_logits is, bit for bit, moe_topk_softmax followed by
-    moe_ffn_decode (one kernel at M = 1 on the single-pass layout, two calls
-    otherwise); its routing equals the oracle's top-k and its output the
+    moe_ffn_decode (one kernel that routes the token itself at M = 1, two
+    calls otherwise); its routing equals the oracle's top-k and its output the
     oracle's layer."""
-    layer = _fused_layer(7)
-    w2 = layer.w2t if transposed else layer.w2
+    layer = mx_layer(dataclasses.replace(inputs.DECODE, name="logits_layer", seed=7))
     wl = dataclasses.replace(inputs.DECODE, name=f"logits_m{M}", M=M, seed=7)
     for step in range(3):
         logits_np = inputs.router_logits(wl, step)
         logits = torch.from_numpy(logits_np).cuda()
         x = inputs.activations(wl, step).cuda()
-        y1, ids1, w1 = moe.moe_ffn_decode_logits(logits, x, wl.k, layer.w13, w2, out_dtype=torch.float32)
+        y1, ids1, w1 = moe.moe_ffn_decode_logits(logits, x, wl.k, layer.w13, layer.w2, out_dtype=torch.float32)
         ids2 = torch.empty((M, wl.k), dtype=torch.int32, device="cuda")
         w2_ = torch.empty((M, wl.k), dtype=torch.float32, device="cuda")
         moe.moe_topk_softmax(logits, wl.k, ids2, w2_)
-        y2 = moe.moe_ffn_decode(x, ids2, w2_, layer.w13, w2, out_dtype=torch.float32)
+        y2 = moe.moe_ffn_decode(x, ids2, w2_, layer.w13, layer.w2, out_dtype=torch.float32)
         assert torch.equal(ids1, ids2) and torch.equal(w1, w2_)
         assert torch.equal(y1, y2)
         ids_ref, w_ref = oracle.topk_softmax(logits_np, wl.k)
@@ -397,7 +339,23 @@ def test_decode_logits_equals_topk_then_decode(M, transposed):
         gs.assert_layer_close(y1, oracle_decode(layer, x.cpu(), ids_ref, w_ref.astype(np.float32)))
 
 
-# ------------------------------------------------ paired 4:8 sparse NVFP4 (opt-in kernels)
+def test_decode_logits_ties_go_to_the_lower_expert():
+    """The in-kernel routing ranks the logits: equal logits go to the lower
+    expert id, slots in descending order -- the same as the oracle."""
+    wl = inputs.DECODE
+    layer = mx_layer(wl)
+    logits_np = np.zeros((1, wl.E), dtype=np.float32)
+    logits_np[0, [5, 77, 3, 100, 64, 2, 9, 40, 41]] = [2.0, 2.0, 1.5, 1.5, 1.5, 1.0, 1.0, 0.5, 0.5]
+    x = inputs.activations(wl).cuda()
+    y, ids, w = moe.moe_ffn_decode_logits(torch.from_numpy(logits_np).cuda(), x, wl.k, layer.w13, layer.w2,
+                                          out_dtype=torch.float32)
+    ids_ref, w_ref = oracle.topk_softmax(logits_np, wl.k)
+    assert ids.cpu().numpy().tolist() == ids_ref.tolist() == [[5, 77, 3, 64, 100, 2, 9, 40]]
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
+    gs.assert_layer_close(y, oracle_decode(layer, x.cpu(), ids_ref, w_ref.astype(np.float32)))
+
+
+# ------------------------------------------------ paired 4:8 sparse NVFP4
 
 NV4 = inputs.Workload("nvfp4s_m4_d1024_i512_e16_k4", M=4, d=1024, I=512, E=16, k=4, seed=21)
 
@@ -412,20 +370,8 @@ def _nvfp4s_layer(wl):
     return mk(p13), mk(p2), p13, p2
 
 
-def test_nvfp4s_decode_is_opt_in():
-    if moe.moe_candidate_kernels_enabled():
-        pytest.skip("opt-in kernels requested: the parity test below covers the path")
-    w13, w2, _, _ = _nvfp4s_layer(NV4)
-    ids, w = gs.routing(NV4)
-    with pytest.raises(moe.MoeError) as err:                  # refused on the host, nothing launched
-        moe.moe_ffn_decode(inputs.activations(NV4).cuda(), torch.from_numpy(ids).cuda(),
-                           torch.from_numpy(w).cuda(), w13, w2)
-    assert err.value.status == 2
-
-
 @pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float16])
 def test_nvfp4s_decode_matches_oracle(xdt):
-    gs.need_candidates()
     w13, w2, p13, p2 = _nvfp4s_layer(NV4)
     x = inputs.activations(NV4, dtype=xdt)
     ids, w = gs.routing(NV4)

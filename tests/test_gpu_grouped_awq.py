@@ -1,12 +1,15 @@
 """GPU parity of the 4-bit AWQ grouped path (tcgen05 kind::f16 on weights
 dequantized into tensor memory) on the packed-AWQ study's alignment shape.
 
-The oracle runs with h rounded to fp16 (the GEMM2 operand of this path).
-Checked: the alignment of fixture A (168 routes -> 400 aligned rows in 50
-blocks), the layer output within the layer tolerance, bit-identical outputs
-across five repeats, and bit-identical outputs under another block size (the
-result does not depend on block membership: every output accumulates its
-K-tiles in one fixed order, no split-K).
+The oracle takes the exact activations (bf16 or fp16, as given) and runs in
+two modes: exact (the layer's mathematics) and with h rounded to fp16, the
+precision of this path's second-GEMM operand (fp16 tensor-core surfaces, as
+the packed-AWQ study's path uses).  Every output is checked against both at
+the layer tolerance.  Checked: the alignment of fixture A (168 routes -> 400
+aligned rows in 50 blocks), the layer output, bit-identical outputs across
+five repeats, and bit-identical outputs under another block size (the result
+does not depend on block membership: every output accumulates its K-tiles in
+one fixed order, no split-K).
 """
 import hashlib
 
@@ -35,7 +38,8 @@ def fixture_a():
     ids, w = gs.routing(wl)
     ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, layer.host13, layer.host2,
                            mode=oracle.MODE_H16)["y"]
-    return wl, layer, x, ids, w, ref
+    exact = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, layer.host13, layer.host2)["y"]
+    return wl, layer, x, ids, w, (ref, exact)
 
 
 def _run(layer, x, ids, w, b, out_dtype=torch.float32):
@@ -59,7 +63,8 @@ def test_awq_grouped_fixture_a(fixture_a):
     assert int(aligned[2].item()) == 400
     ex = aligned[1].cpu().numpy()
     assert int((ex >= 0).sum()) == 50
-    gs.assert_layer_close(y, ref)
+    gs.assert_layer_close(y, ref[0])
+    gs.assert_layer_close(y, ref[1])
 
 
 def test_awq_grouped_repeats_bit_identical(fixture_a):
@@ -69,16 +74,16 @@ def test_awq_grouped_repeats_bit_identical(fixture_a):
 
 
 def test_awq_grouped_independent_of_block_size(fixture_a):
-    """Each path's per-route results do not depend on the block size: blocks
-    of up to 16 rows take the mma.sync kernel, larger ones the tcgen05 one."""
+    """A route's result does not depend on the block size: every output
+    accumulates its K-tiles in one fixed order, whatever the block holds."""
     wl, layer, x, ids, w, ref = fixture_a
     y8, _ = _run(layer, x, ids, w, 8)
     y16, _ = _run(layer, x, ids, w, 16)
     y32, _ = _run(layer, x, ids, w, 32)
     y64, _ = _run(layer, x, ids, w, 64)
-    assert torch.equal(y8, y16) and torch.equal(y32, y64)
-    gs.assert_layer_close(y8, ref)
-    gs.assert_layer_close(y32, ref)
+    assert torch.equal(y8, y16) and torch.equal(y16, y32) and torch.equal(y32, y64)
+    gs.assert_layer_close(y8, ref[0])
+    gs.assert_layer_close(y8, ref[1])
 
 
 @pytest.mark.parametrize("xdt,b", [(torch.float16, 16), (torch.bfloat16, 8), (torch.float16, 64)])
@@ -88,28 +93,16 @@ def test_awq_grouped_small(xdt, b):
     x = inputs.activations(wl, dtype=xdt)
     ids, w = gs.routing(wl)
     y, _ = _run(layer, x, ids, w, b, out_dtype=torch.bfloat16)
-    ref = oracle.moe_layer(gs.x_exact(x.to(torch.float16)), ids, w.astype(np.float64), wl.E, layer.host13,
-                           layer.host2, mode=oracle.MODE_H16)["y"]
-    gs.assert_layer_close(y, ref)
-
-
-def test_awq_grouped_small_blocks_any_multiple_of_128():
-    """The b <= 16 path takes d and I that are multiples of 128 but not 256."""
-    gs.need_candidates()
-    wl = inputs.Workload("awq_grouped_1152", M=9, d=1152, I=384, E=8, k=3, fmt="awq4", seed=4)
-    layer = gs.AwqLayer(wl)
-    x = inputs.activations(wl, dtype=torch.float16)
-    ids, w = gs.routing(wl)
-    y, _ = _run(layer, x, ids, w, 16)
-    ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, layer.host13, layer.host2)["y"]
-    gs.assert_layer_close(y, ref)
+    for mode in (oracle.MODE_H16, oracle.MODE_EXACT):
+        ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, layer.host13, layer.host2,
+                               mode=mode)["y"]
+        gs.assert_layer_close(y, ref)
 
 
 @pytest.mark.parametrize("d,b", [(1024, 136), (1152, 32)])
 def test_awq_grouped_limits_rejected(d, b):
-    """Blocks above 128 rows, and d not a multiple of 256 on the tcgen05 path
-    (blocks above 16 rows), are refused on the host with MOE_ERR_UNSUPPORTED
-    (before anything is launched)."""
+    """Blocks above 128 rows, and d not a multiple of 256, are refused on the
+    host with MOE_ERR_UNSUPPORTED (before anything is launched)."""
     wl = inputs.Workload("awq_grouped_limits", M=8, d=d, I=256, E=16, k=4, fmt="awq4", seed=9)
     layer = gs.AwqLayer(wl)
     x = inputs.activations(wl, dtype=torch.float16)

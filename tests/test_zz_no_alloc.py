@@ -1,4 +1,5 @@
-"""The allocation-free decode entry point against the regular one.
+"""The allocation-free decode entry point against the regular one and the
+oracle.
 
 moe_ffn_decode_noalloc serves callers that cannot hand the library device
 memory (strict graph capture, pre-planned serving memory, operator plugins);
@@ -35,6 +36,16 @@ def _layer():
             moe.Weights(moe.MOE_W_MXFP8, q13, s13), moe.Weights(moe.MOE_W_MXFP8, q2, s2))
 
 
+def _oracle_y(wl, x, ids, w):
+    """The oracle's exact-mode layer on its own MXFP8 codes of the same fp32
+    draws (checked equal to the device codes by the other GPU tests)."""
+    oq13, os13 = oracle.mxfp8_quantize_3d(inputs.weights_fp32(wl, "w13").astype(np.float64))
+    oq2, os2 = oracle.mxfp8_quantize_3d(inputs.weights_fp32(wl, "w2").astype(np.float64))
+    return oracle.moe_layer(x.cpu().to(torch.float64).numpy(), ids.cpu().numpy(),
+                            w.cpu().numpy().astype(np.float64), wl.E, {"fmt": "mxfp8", "q": oq13, "s": os13},
+                            {"fmt": "mxfp8", "q": oq2, "s": os2})["y"]
+
+
 def _call_c_abi(x, ids, w, w13, w2, y, status):
     """Straight through the C ABI (ctypes), no Python wrapper logic."""
     L = moe.lib()
@@ -51,6 +62,8 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
     wl, x, ids, w, w13, w2 = _layer()
     ref = moe.moe_ffn_decode(x, ids, w, w13, w2, out_dtype=torch.float32)
     scale = float(ref.abs().max())
+    exact = _oracle_y(wl, x, ids, w)
+    escale = float(np.abs(exact).max())
     for call in range(2):                  # the shared array is reused by the second call
         y = torch.full_like(ref, float("nan"))
         status = torch.zeros(2, dtype=torch.int32, device="cuda")
@@ -59,6 +72,10 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
         assert status.tolist() == [0, 0]
         err = float((y - ref).abs().max())
         assert err <= REL_TOL * scale, (call, err, scale)
+        # the same kernels with the same summation order: the same bits
+        assert torch.equal(y, ref), call
+        eerr = float(np.abs(y.cpu().double().numpy() - exact).max())
+        assert eerr <= REL_TOL * escale, (call, eerr, escale)
     # a second, different batch through the same array
     x2 = inputs.activations(wl, step=1).to("cuda")
     ref2 = moe.moe_ffn_decode(x2, ids, w, w13, w2, out_dtype=torch.float32)

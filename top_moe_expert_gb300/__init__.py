@@ -24,7 +24,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CAPACITY", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_TIMEOUT"}
-MOE_W_MXFP8, MOE_W_AWQ4, MOE_W_MXFP8_T, MOE_W_NVFP4S = 0, 1, 2, 3
+MOE_W_MXFP8, MOE_W_AWQ4, MOE_W_NVFP4S = 0, 1, 3
 MOE_BF16, MOE_FP16, MOE_FP32 = 0, 1, 2
 MOE_PATH_DECODE, MOE_PATH_GROUPED = 0, 1
 
@@ -50,14 +50,12 @@ _I32, _I64, _P, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_
 _PROTOS = {
     "moe_status_string": (ctypes.c_char_p, [_I32]),
     "moe_abi_version": (_I32, []),
-    "moe_candidate_kernels_enabled": (_I32, []),
     "moe_ffn_select_path": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_topk_softmax": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "moe_align_capacity": (_I32, [_I32, _I32, _I32, _I32, _P, _P]),
     "moe_align_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
     "moe_align_block_size": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _I32, _P, _SZ, _P, _P]),
     "moe_mxfp8_quantize": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P]),
-    "moe_mxfp8_transpose": (_I32, [ctypes.POINTER(moe_weights_t), _P, _P, _P]),
     "moe_ffn_decode_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _P]),
     "moe_ffn_decode": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                               ctypes.POINTER(moe_weights_t), _P, _I32, _P, _SZ, _P, _P]),
@@ -71,6 +69,7 @@ _PROTOS = {
                                _P, _SZ, _P, _P]),
     "moe_ffn_decode_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                                       ctypes.POINTER(moe_weights_t), _P, _I32, _P, _P]),
+    "moe_debug_arrival_shortfall": (_I32, [_I32]),
 }
 
 
@@ -169,8 +168,7 @@ _YDT = (torch.bfloat16, torch.float32)
 @dataclasses.dataclass(frozen=True)
 class Weights:
     """One projection of all experts: MXFP8 (q uint8 [E,N,K], scale uint8
-    [E,N,K/32]), MXFP8_T (the same values K-outer: q uint8 [E,K,N], scale
-    uint8 [E,K/32,N]) or AWQ4 (q int32 [E,N,K/8], scale fp16 [E,N,K/128],
+    [E,N,K/32]) or AWQ4 (q int32 [E,N,K/8], scale fp16 [E,N,K/128],
     zero int32 [E,N/8,K/128]) or NVFP4S, paired 4:8 sparse NVFP4 (q uint8
     [E,N,K/4] kept E2M1 codes, scale uint8 [E,N,K/32] UE4M3, zero uint8
     [E,N,K/16] pattern nibbles, alpha float32 [E]).  The tensors are checked against the format
@@ -195,12 +193,10 @@ class Weights:
 
     @property
     def N(self):
-        return self.q.shape[2] if self.fmt == MOE_W_MXFP8_T else self.q.shape[1]
+        return self.q.shape[1]
 
     @property
     def K(self):
-        if self.fmt == MOE_W_MXFP8_T:
-            return self.q.shape[1]
         return self.q.shape[2] * {MOE_W_AWQ4: 8, MOE_W_NVFP4S: 4}.get(self.fmt, 1)
 
     def _check(self):
@@ -214,11 +210,6 @@ class Weights:
             if K % 32:
                 raise ValueError(f"weights: K = {K} is not a multiple of 32")
             _need(self.scale, "weights.scale", _U8, (E, N, K // 32), device=device)
-        elif self.fmt == MOE_W_MXFP8_T:
-            _need(q, "weights.q", _U8)
-            if K % 32:
-                raise ValueError(f"weights: K = {K} is not a multiple of 32")
-            _need(self.scale, "weights.scale", _U8, (E, K // 32, N), device=device)
         elif self.fmt == MOE_W_AWQ4:
             _need(q, "weights.q", _IDS)
             if K % 128 or N % 8:
@@ -282,11 +273,12 @@ def moe_ffn_select_path(M: int, k: int, E: int, d: int, I: int, fmt: int = None)
     return p.value, b.value
 
 
-def moe_candidate_kernels_enabled() -> bool:
-    """Whether the library dispatches to its opt-in kernels (the environment
-    variable MOE_FFN_CANDIDATE_KERNELS=1, read once when the library first
-    dispatches)."""
-    return bool(lib().moe_candidate_kernels_enabled())
+def moe_debug_arrival_shortfall(n: int) -> None:
+    """Failure-detection test hook: the single-token one-kernel launches that
+    follow expect n arrivals more than their grid provides, so their bounded
+    counter wait runs out and reports MOE_ERR_TIMEOUT in dev_status[1]; 0
+    restores normal operation."""
+    _check(lib().moe_debug_arrival_shortfall(int(n)), "moe_debug_arrival_shortfall")
 
 
 def moe_align_capacity(M: int, k: int, E: int, b: int):
@@ -355,22 +347,6 @@ def moe_mxfp8_quantize(v: torch.Tensor, q=None, s=None, stream=None):
                "moe_mxfp8_quantize")
     return q, s
 
-
-def moe_mxfp8_transpose(w: Weights, stream=None) -> Weights:
-    """The same MXFP8 weights re-laid K-outer (MOE_W_MXFP8_T)."""
-    if w.fmt != MOE_W_MXFP8:
-        raise ValueError("moe_mxfp8_transpose takes MOE_W_MXFP8 weights")
-    dev = w.device
-    q_t = torch.empty((w.E, w.K, w.N), dtype=torch.uint8, device=dev)
-    s_t = torch.empty((w.E, w.K // 32, w.N), dtype=torch.uint8, device=dev)
-    a = w.c_struct()
-    with _guard(dev):
-        _check(lib().moe_mxfp8_transpose(ctypes.byref(a), _ptr(q_t), _ptr(s_t), _stream(stream, dev)),
-               "moe_mxfp8_transpose")
-    return Weights(MOE_W_MXFP8_T, q_t, s_t)
-
-
-# ---------------------------------------------------------------- the layer
 
 def _layer_args(x, topk_ids, topk_w, w13: Weights, w2: Weights, y, out_dtype, dev_status):
     """Check the common arguments of the layer calls; returns (device, M, d,

@@ -1,5 +1,4 @@
 // abi.cu -- library-wide entry points of libmoe_ffn (status names, version).
-#include "attr.h"
 #include "common.cuh"
 
 MOE_API const char *moe_status_string(moe_status_t s)
@@ -17,5 +16,3 @@ MOE_API const char *moe_status_string(moe_status_t s)
 }
 
 MOE_API int32_t moe_abi_version(void) { return MOE_FFN_ABI_VERSION; }
-
-MOE_API int32_t moe_candidate_kernels_enabled(void) { return moe::candidate_kernels_enabled() ? 1 : 0; }

@@ -10,8 +10,6 @@
 
 #include <atomic>
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
 #include <mutex>
 #include <unordered_map>
 
@@ -82,20 +80,6 @@ inline int device_sm_count()
     if (dev >= 0 && dev < 64)
         cache[dev].store(n, std::memory_order_relaxed);
     return n;
-}
-
-// The opt-in kernels: the single-token and small-batch decode kernels on
-// the standard layout (MXFP8 and AWQ) and the small-block AWQ grouped kernel.
-// Dispatch takes them only when the environment variable
-// MOE_FFN_CANDIDATE_KERNELS is exactly "1" at the library's first dispatch
-// (read once per process); otherwise the same calls run the general kernels.
-inline bool candidate_kernels_enabled()
-{
-    static const bool on = [] {
-        const char *v = std::getenv("MOE_FFN_CANDIDATE_KERNELS");
-        return v != nullptr && std::strcmp(v, "1") == 0;
-    }();
-    return on;
 }
 
 }  // namespace moe

@@ -317,32 +317,15 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
 {
     if (M < 0 || k < 1 || d < 1 || I < 1 || !bytes)
         return MOE_ERR_INVALID_ARG;
-    // The first kWsReserved bytes hold the grid-barrier counter of the
-    // one-kernel single-token paths (ws[0..8)).  Every other path starts its
-    // data after them, so one workspace serves calls of any batch size in
-    // turn without disturbing the counter.
+    // The first kWsReserved bytes hold the arrival counter of the one-kernel
+    // single-token path (ws[0..8)).  Every other path starts its data after
+    // them, so one workspace serves calls of any batch size in turn without
+    // disturbing the counter.
     size_t h = kWsReserved + ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
-    size_t part = (M <= 4 && d % 1024 == 0) ? kWsReserved + decode_fused_workspace(M, d) : 0;
-    if (M == 1 && (d == 1024 || d == 2048)) {
-        const size_t m1 = decode_m1_workspace(d);
-        part = part > m1 ? part : m1;
-    }
-    if (M == 1 && k <= 32 && d % 1024 == 0 && I % 128 == 0) {
-        const size_t a1 = decode_awq_m1_workspace(k, I);
-        part = part > a1 ? part : a1;
-    }
+    size_t part = 0;
     if (M == 1 && k <= 32) {
         const size_t p1 = decode_pipe_workspace(k, I);
         part = part > p1 ? part : p1;
-    }
-    if (M == 1 && k <= 32 && d % 64 == 0 && I % 64 == 0) {
-        const size_t x1 = decode_mx_m1_workspace(k, I);
-        part = part > x1 ? part : x1;
-    }
-    if (M >= 2 && M <= 64 && k <= 32 && d % 64 == 0 && I % 64 == 0) {
-        // the alignment capacity is largest when every route has its own expert
-        const size_t xs = kWsReserved + decode_mx_small_workspace(M, k, d, I, M * k);
-        part = part > xs ? part : xs;
     }
     *bytes = h > part ? h : part;
     return MOE_OK;
@@ -352,7 +335,7 @@ static moe_status_t check_weights(const moe_weights_t *w, int N, int K)
 {
     if (!w || !w->q || !w->scale || w->N != N || w->K != K || w->E < 1)
         return MOE_ERR_INVALID_ARG;
-    if (w->fmt == MOE_W_MXFP8 || w->fmt == MOE_W_MXFP8_T) {
+    if (w->fmt == MOE_W_MXFP8) {
         if (K % 32 != 0)
             return MOE_ERR_INVALID_ARG;
     } else if (w->fmt == MOE_W_AWQ4) {
@@ -381,34 +364,8 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     moe_status_t st;
     if ((st = check_weights(w13, 2 * I, d)) != MOE_OK || (st = check_weights(w2, d, I)) != MOE_OK)
         return st;
-    if (w13->fmt == MOE_W_MXFP8_T)
-        return MOE_ERR_INVALID_ARG;
     if (w13->E != w2->E)
         return MOE_ERR_INVALID_ARG;
-    if (w2->fmt == MOE_W_MXFP8_T) {
-        // single-pass small-batch path: W2 given neuron-major
-        if (w13->fmt != MOE_W_MXFP8 || xdt != MOE_BF16 || (ydt != MOE_BF16 && ydt != MOE_FP32))
-            return MOE_ERR_UNSUPPORTED;
-        if (!decode_fused_eligible(M, k, d, I, w13->E) || !aligned(w13->scale, 16) || !aligned(w2->scale, 16))
-            return M == 0 ? MOE_OK : MOE_ERR_UNSUPPORTED;
-        if (!x || !topk_ids || !topk_w || !y || !aligned(x, 16))
-            return MOE_ERR_INVALID_ARG;
-        size_t need;
-        moe_ffn_decode_workspace_size(M, k, d, I, &need);
-        if (!ws || ws_bytes < need || !aligned(ws, 256))
-            return MOE_ERR_WORKSPACE;
-        if (decode_m1_eligible(M, k, d, I, w13->E) && aligned(y, 16))
-            return decode_m1_launch(static_cast<const __nv_bfloat16 *>(x), d, I, w13->E, topk_ids, topk_w, nullptr,
-                                    nullptr, nullptr, k, static_cast<const uint8_t *>(w13->q),
-                                    static_cast<const uint8_t *>(w13->scale),
-                                    static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y,
-                                    ydt == MOE_FP32, ws, dev_status, as_stream(stream));
-        return decode_fused_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
-                                   static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
-                                   static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y,
-                                   ydt == MOE_FP32, reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWsReserved),
-                                   dev_status, as_stream(stream));
-    }
     if (w13->fmt != w2->fmt)
         return MOE_ERR_INVALID_ARG;
     const int fmt = w13->fmt;
@@ -416,7 +373,7 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
         return MOE_ERR_UNSUPPORTED;
     if (fmt == MOE_W_AWQ4 && (d % 1024 != 0 || I % 128 != 0))
         return MOE_ERR_UNSUPPORTED;
-    if (fmt == MOE_W_NVFP4S && (!candidate_kernels_enabled() || !decode_nvfp4s_eligible(k, d, I)))
+    if (fmt == MOE_W_NVFP4S && !decode_nvfp4s_eligible(k, d, I))
         return MOE_ERR_UNSUPPORTED;
     if (ydt != MOE_BF16 && ydt != MOE_FP32)
         return MOE_ERR_UNSUPPORTED;
@@ -434,54 +391,19 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     moe_ffn_decode_workspace_size(M, k, d, I, &need);
     if (!ws || ws_bytes < need || !aligned(ws, 256))
         return MOE_ERR_WORKSPACE;
-    // past the reserved bytes: h of the two-kernel and per-scalar paths, the
-    // data of the small-batch paths
-    void *ws_data = static_cast<uint8_t *>(ws) + kWsReserved;
-    const size_t ws_data_bytes = ws_bytes - kWsReserved;
-    float *h = static_cast<float *>(ws_data);
+    // past the reserved bytes: h of the two-kernel and per-scalar paths
+    float *h = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWsReserved);
     cudaStream_t s = as_stream(stream);
-    const bool cand = candidate_kernels_enabled();
     if (fmt == MOE_W_NVFP4S)
         return decode_nvfp4s_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k, w13, w2, y,
                                     ydt == MOE_FP32, h, dev_status, s);
-    if (cand && fmt == MOE_W_AWQ4 && decode_awq_small_eligible(M, k, d, I, w13->E)) {
-        // a small batch: aligned blocks of 16 rows, one kernel for both GEMMs, combine
-        const moe_status_t st3 = decode_awq_small_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k,
-                                                         w13, w2, y, ydt == MOE_FP32, ws_data, ws_data_bytes,
-                                                         dev_status, s);
-        if (st3 != MOE_ERR_UNSUPPORTED)
-            return st3;
-    }
-    if (cand && fmt == MOE_W_AWQ4 && decode_awq_m1_eligible(M, k, d, I, w13->E))
-        return decode_awq_m1_launch(x, xdt == MOE_BF16, topk_ids, topk_w, k, d, I, w13->E, w13->q, w13->scale,
-                                    w13->zero, w2->q, w2->scale, w2->zero, y, ydt == MOE_FP32, ws, dev_status, s);
     if (fmt == MOE_W_MXFP8 && decode_pipe_eligible(M, k, d, I, w13->E) && aligned(w13->scale, 16) &&
-        aligned(w2->q, 16)) {
+        aligned(w2->q, 16) && aligned(w2->scale, 8)) {
         // one token on the standard layout: one kernel (gate/up, SwiGLU, down)
         return decode_pipe_launch(static_cast<const __nv_bfloat16 *>(x), d, I, w13->E, topk_ids, topk_w, nullptr,
                                   nullptr, nullptr, k, static_cast<const uint8_t *>(w13->q),
                                   static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
                                   static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status, s);
-    }
-    if (cand && fmt == MOE_W_MXFP8 && decode_mx_m1_eligible(M, k, d, I, w13->E) && aligned(w2->q, 16)) {
-        // one token on the standard layout: one kernel (gate/up, SwiGLU, down)
-        const moe_status_t st1 = decode_mx_m1_launch(
-            static_cast<const __nv_bfloat16 *>(x), d, I, w13->E, topk_ids, topk_w, nullptr, nullptr, nullptr, k,
-            static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
-            static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws,
-            dev_status, s);
-        if (st1 != MOE_ERR_UNSUPPORTED)
-            return st1;
-    }
-    if (cand && fmt == MOE_W_MXFP8 && decode_mx_small_eligible(M, k, d, I, w13->E)) {
-        // a small batch on the standard layout: aligned blocks, one kernel for both GEMMs, combine
-        const moe_status_t st2 = decode_mx_small_launch(
-            static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
-            static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
-            static_cast<const uint8_t *>(w2->q), static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws_data,
-            ws_data_bytes, dev_status, s);
-        if (st2 != MOE_ERR_UNSUPPORTED)
-            return st2;
     }
     if (fmt == MOE_W_MXFP8 && decode_stream_eligible(M, k, d, I, w13->E, w13->q, w13->scale, w2->q, w2->scale)) {
         const moe_status_t st2 = decode_stream_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
@@ -517,27 +439,12 @@ MOE_API moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, i
     if (!logits || !topk_ids || !topk_w)
         return MOE_ERR_INVALID_ARG;
     const int I = w2->K, E = w13->E;
-    // one kernel for a single token on the neuron-major single-pass layout
-    if (M == 1 && w2->fmt == MOE_W_MXFP8_T && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
-        (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
-        check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_m1_eligible(1, k, d, I, E) &&
-        decode_m1_route_eligible(E, k) && aligned(w13->scale, 16) && aligned(w2->scale, 16) && x && y &&
-        aligned(x, 16) && aligned(y, 16)) {
-        size_t need;
-        moe_ffn_decode_workspace_size(M, k, d, I, &need);
-        if (!ws || ws_bytes < need || !aligned(ws, 256))
-            return MOE_ERR_WORKSPACE;
-        return decode_m1_launch(static_cast<const __nv_bfloat16 *>(x), d, I, E, nullptr, nullptr, logits, topk_ids,
-                                topk_w, k, static_cast<const uint8_t *>(w13->q),
-                                static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
-                                static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status,
-                                as_stream(stream));
-    }
     // one token on the standard layout: one kernel with the routing inside
     if (M == 1 && w2->fmt == MOE_W_MXFP8 && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
         (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
         check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_pipe_eligible(1, k, d, I, E) &&
-        decode_pipe_route_eligible(E, k) && aligned(w13->scale, 16) && x && y && aligned(x, 16)) {
+        decode_pipe_route_eligible(E, k) && aligned(w13->scale, 16) && aligned(w2->q, 16) &&
+        aligned(w2->scale, 8) && x && y && aligned(x, 16)) {
         size_t need;
         moe_ffn_decode_workspace_size(M, k, d, I, &need);
         if (!ws || ws_bytes < need || !aligned(ws, 256))
@@ -547,20 +454,6 @@ MOE_API moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, i
                                   static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
                                   static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status,
                                   as_stream(stream));
-    }
-    if (candidate_kernels_enabled() && M == 1 && w2->fmt == MOE_W_MXFP8 && w13->fmt == MOE_W_MXFP8 && xdt == MOE_BF16 &&
-        (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
-        check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_mx_m1_eligible(1, k, d, I, E) && E >= k &&
-        E <= 512 && aligned(w2->q, 16) && x && y && aligned(x, 16)) {
-        size_t need;
-        moe_ffn_decode_workspace_size(M, k, d, I, &need);
-        if (!ws || ws_bytes < need || !aligned(ws, 256))
-            return MOE_ERR_WORKSPACE;
-        return decode_mx_m1_launch(static_cast<const __nv_bfloat16 *>(x), d, I, E, nullptr, nullptr, logits,
-                                   topk_ids, topk_w, k, static_cast<const uint8_t *>(w13->q),
-                                   static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
-                                   static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status,
-                                   as_stream(stream));
     }
     // otherwise: routing, then the layer
     moe_status_t st = moe_topk_softmax(logits, M, E, k, topk_ids, topk_w, stream);

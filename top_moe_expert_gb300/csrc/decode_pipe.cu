@@ -28,8 +28,8 @@
 //     wait until every CTA has written its share of h (one arrival per CTA on
 //     a counter in the workspace) and copy all of h into shared memory.
 // Tail: the 24 compute warps form this CTA's output rows of every route's
-// down projection (h split into fp16 hi + lo after an exact power-of-two
-// rescale, one warp per (route, row), butterfly sums); y is the
+// down projection (h as fp16 after an exact power-of-two rescale per route,
+// one warp per (route, row), butterfly sums); y is the
 // routing-weighted sum over routes in slot order.  The (route, neuron) space
 // is split evenly over the CTAs and each CTA owns d / G output rows, so no
 // output is reduced across CTAs.
@@ -43,6 +43,8 @@
 // dependent launches start only after this CTA has seen every arrival.
 // Every output's summation order depends only on the shapes and the grid,
 // so repeats are bit-identical.
+#include <atomic>
+
 #include "attr.h"
 #include "common.cuh"
 #include "decode_internal.h"
@@ -70,7 +72,6 @@ constexpr int kBarGroup0 = 3;                         //   gate/up group g: kBar
 constexpr int kBarRank = kBarGroup0 + kGroups;        //   the compute warps ranking the logits
 constexpr int kBarScales = kBarRank + 1;              //   gate/up E8M0 rows staged (wait/copy warps arrive)
 constexpr int kSmemMax = 227 * 1024;
-constexpr bool kHiLo = true;                          // h into the down projection as fp16 hi + lo
 
 struct Args {
     const __nv_bfloat16 *x;      // [d]
@@ -86,6 +87,7 @@ struct Args {
     void *y;
     int32_t *dev_status;
     int y_f32, k, d, I, E;
+    int shortfall;               // arrivals the counter wait expects beyond the grid (failure-detection test)
 };
 
 // Shared-memory plan (bytes), identical on host and device.  The tail's h and
@@ -98,15 +100,16 @@ struct Plan {
     __host__ __device__ int s2() const { return rows_max() * I; }
     __host__ __device__ static int up16(int v) { return (v + 15) & ~15; }
     __host__ __device__ int o_w2() const { return up16(k * I * 4); }            // in the ring, after h
+    __host__ __device__ int o_hh() const { return o_w2() + k * s2(); }          // in the ring: h as fp16
     __host__ __device__ int o_s2s() const { return kSlots * s1(); }
     __host__ __device__ int o_gsc() const { return o_s2s() + k * rows_max() * (I / 32) * 4; }
     __host__ __device__ int o_gpart() const { return o_gsc() + up16(pmax() * 2 * (d / 32)); }
     __host__ __device__ int o_dpart() const { return o_gpart() + kGroups * 2 * kGW * 2 * kPS * 4; }
-    __host__ __device__ int o_bars() const { return o_dpart() + up16(k * rows_max() * 4); }
+    __host__ __device__ int o_bars() const { return o_dpart() + up16(k * rows_max() * 4 + k * 4); }  // + 1/scale of h
     __host__ __device__ int o_route() const { return o_bars() + (2 * kSlots + k + 1) * 8; }
     // route data: r_e[kMaxK] | r_w[kMaxK] | r_l[kMaxK] | target u64 | nv, done, abort, tabort, gabort[kGroups]
     __host__ __device__ int bytes() const { return o_route() + 3 * kMaxK * 4 + 8 + 16 + kGroups * 4; }
-    __host__ __device__ bool fits() const { return bytes() <= kSmemMax && o_w2() + k * s2() <= kSlots * s1(); }
+    __host__ __device__ bool fits() const { return bytes() <= kSmemMax && o_hh() + k * I * 2 <= kSlots * s1(); }
 };
 
 __device__ __forceinline__ void set_err(int32_t *st, int code)
@@ -312,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
         if (lane == 0) {
             // the arrival counter's epoch, read before this CTA arrives
             const unsigned long long v = ld_relaxed_u64(a.ctr);
-            *target = v / static_cast<unsigned>(G) * static_cast<unsigned>(G) + static_cast<unsigned>(G);
+            *target = v / static_cast<unsigned>(G) * static_cast<unsigned>(G) + static_cast<unsigned>(G) +
+                  static_cast<unsigned>(a.shortfall);
         }
     } else if constexpr (ROUTE) {
         // top-k of the router logits by rank: thread e (of the 24 compute
@@ -575,49 +579,57 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     // ---------------------------------------------------------------- tail
     tc::named_bar(kBarTail, kCW * 32);
     const bool work = !*tabort && nv > 0 && nrows > 0;
-    if (work) {
-        const bool got = tc::mbar_wait(hbar, 0, s_abort, kWaitNs);
-        if (!got)
-            set_err(a.dev_status, MOE_ERR_TIMEOUT);
+    const bool got = work && tc::mbar_wait(hbar, 0, s_abort, kWaitNs);
+    if (work && !got)
+        set_err(a.dev_status, MOE_ERR_TIMEOUT);
+    // h of every route once, by one warp per route: fp16 after an exact
+    // power-of-two rescale that puts the route's largest magnitude in
+    // [2^14, 2^15) (relative rounding at most 2^-12 of each element)
+    __half2 *h16 = reinterpret_cast<__half2 *>(slot1 + pl.o_hh());        // [nv][I/2]
+    float *hinv = dpart + pl.k * RM;                                     // [nv]
+    for (int r = cw; got && r < nv; r += kCW) {
+        float hv[HPL];
+        const float4 *hp = reinterpret_cast<const float4 *>(hbuf + r * I + HPL * lane);
+#pragma unroll
+        for (int i = 0; i < HPL / 4; ++i) {
+            const float4 f = hp[i];
+            hv[4 * i] = f.x; hv[4 * i + 1] = f.y; hv[4 * i + 2] = f.z; hv[4 * i + 3] = f.w;
+        }
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < HPL; ++i)
+            m = fmaxf(m, fabsf(hv[i]));
+        const int pw = f16_shift(warp_max(m));
+        const float sc = ldexpf(1.0f, pw);
+        if (lane == 0)
+            hinv[r] = ldexpf(1.0f, -pw);
+#pragma unroll
+        for (int i = 0; i < HPL / 2; ++i)
+            h16[(r * I + HPL * lane) / 2 + i] = __floats2half2_rn(hv[2 * i] * sc, hv[2 * i + 1] * sc);
+    }
+    tc::named_bar(kBarTail, kCW * 32);
+    if (got) {
         // the (route, row) units of this CTA, a contiguous block per warp
         const int U = nv * nrows, nb2 = I / 32;
         const int u0 = U * cw / kCW, u1 = U * (cw + 1) / kCW;
         int cur = -1;
-        uint32_t hh[HPL / 2], hl[HPL / 2];
+        uint32_t hh[HPL / 2];
         float inv = 1.f;
-        for (int u = u0; u < u1 && got;) {
+        for (int u = u0; u < u1;) {
             const int r = u / nrows, rho = u - r * nrows;
             if (r != cur) {
-                // h of route r: this lane's HPL elements, fp16 hi + lo after
-                // an exact power-of-two rescale of the route's largest magnitude
                 cur = r;
                 if (!tc::mbar_wait(full2 + 8 * r, 0, s_abort, kWaitNs)) {
                     set_err(a.dev_status, MOE_ERR_TIMEOUT);
                     break;
                 }
-                float hv[HPL];
-                const float4 *hp = reinterpret_cast<const float4 *>(hbuf + r * I + HPL * lane);
+                const uint4 *ph = reinterpret_cast<const uint4 *>(h16 + (r * I + HPL * lane) / 2);
 #pragma unroll
-                for (int i = 0; i < HPL / 4; ++i) {
-                    const float4 f = hp[i];
-                    hv[4 * i] = f.x; hv[4 * i + 1] = f.y; hv[4 * i + 2] = f.z; hv[4 * i + 3] = f.w;
+                for (int i = 0; i < HPL / 8; ++i) {
+                    const uint4 v = ph[i];
+                    hh[4 * i] = v.x; hh[4 * i + 1] = v.y; hh[4 * i + 2] = v.z; hh[4 * i + 3] = v.w;
                 }
-                float m = 0.f;
-#pragma unroll
-                for (int i = 0; i < HPL; ++i)
-                    m = fmaxf(m, fabsf(hv[i]));
-                const int pw = f16_shift(warp_max(m));
-                const float sc = ldexpf(1.0f, pw);
-                inv = ldexpf(1.0f, -pw);
-#pragma unroll
-                for (int i = 0; i < HPL / 2; ++i) {
-                    const float a0 = hv[2 * i] * sc, a1 = hv[2 * i + 1] * sc;
-                    const __half2 hi = __floats2half2_rn(a0, a1);
-                    const float2 hf = __half22float2(hi);
-                    const __half2 lo = __floats2half2_rn(a0 - hf.x, a1 - hf.y);
-                    hh[i] = *reinterpret_cast<const uint32_t *>(&hi);
-                    hl[i] = *reinterpret_cast<const uint32_t *>(&lo);
-                }
+                inv = hinv[r];
             }
             // two rows of the same route at once when the block has them
             const bool two = u + 1 < u1 && rho + 1 < nrows;
@@ -642,13 +654,6 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 for (int i = 0; i < 4; ++i) {
                     p0 = fma2(a[i], hh[4 * c8 + i], p0);
                     p1 = fma2(b[i], hh[4 * c8 + i], p1);
-                }
-                if constexpr (kHiLo) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        p0 = fma2(a[i], hl[4 * c8 + i], p0);
-                        p1 = fma2(b[i], hl[4 * c8 + i], p1);
-                    }
                 }
                 acc0 = fmaf(p0, sr0[sb], acc0);
                 acc1 = fmaf(p1, sr1[sb], acc1);
@@ -707,6 +712,12 @@ inline bool shape_ok(int d, int I)
 
 }  // namespace dp
 
+// Arrivals the next launches' counter wait expects beyond the grid size: 0
+// in normal use; moe_debug_arrival_shortfall sets it so that a test can make
+// the wait run out (it gives up after its time limit and reports
+// MOE_ERR_TIMEOUT) without faulting or hanging the GPU.
+static std::atomic<int> g_shortfall{0};
+
 bool decode_pipe_eligible(int M, int k, int d, int I, int E)
 {
     if (M != 1 || k < 1 || k > dp::kMaxK || E < 1 || !dp::shape_ok(d, I))
@@ -751,6 +762,7 @@ moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, con
     a.d = d;
     a.I = I;
     a.E = E;
+    a.shortfall = g_shortfall.load(std::memory_order_relaxed);
     const int smem = pl.bytes();
     switch (d * 10000 + I) {
     case 512 * 10000 + 256: return launch_route<4, 8>(a, G, smem, s);
@@ -763,3 +775,11 @@ moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, con
 }
 
 }  // namespace moe
+
+MOE_API moe_status_t moe_debug_arrival_shortfall(int32_t n)
+{
+    if (n < 0 || n > 1024)
+        return MOE_ERR_INVALID_ARG;
+    moe::g_shortfall.store(n, std::memory_order_relaxed);
+    return MOE_OK;
+}

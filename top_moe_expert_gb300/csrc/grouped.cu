@@ -688,15 +688,9 @@ MOE_API moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_
 {
     if (M < 0 || k < 1 || d < 1 || I < 1 || b < 1 || cap_rows < 0 || !bytes)
         return MOE_ERR_INVALID_ARG;
-    // one size for every weight format and block size: the MXFP8 layout, the
-    // AWQ one, or (b <= 16) the AWQ layout of the mma.sync kernel
+    // one size for both weight formats: the larger of the MXFP8 and AWQ layouts
     const size_t mx = ws_layout(M, k, d, I, b, cap_rows).total, aw = grouped_awq_workspace(M, k, d, I, b, cap_rows);
-    size_t n = mx > aw ? mx : aw;
-    if (b <= 16) {
-        const size_t am = grouped_awq_mma_workspace(M, k, d, I, b, cap_rows);
-        n = n > am ? n : am;
-    }
-    *bytes = n;
+    *bytes = mx > aw ? mx : aw;
     return MOE_OK;
 }
 
@@ -742,10 +736,6 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows, &need);
         if (!ws || ws_bytes < need || !aligned(ws, 256))
             return MOE_ERR_WORKSPACE;
-        if (candidate_kernels_enabled() && grouped_awq_mma_eligible(b, d, I))
-            return grouped_awq_mma_launch(x, xdt == MOE_BF16, M, d, I, E, topk_ids, topk_w, k, w13, w2,
-                                          sorted_route_ids, expert_ids, num_rows_post_pad, b, cap_rows, y,
-                                          ydt == MOE_FP32, ws, dev_status, as_stream(stream));
         return grouped_awq_launch(x, xdt == MOE_BF16, M, d, I, E, topk_ids, topk_w, k, w13, w2, sorted_route_ids,
                                   expert_ids, num_rows_post_pad, b, cap_rows, y, ydt == MOE_FP32, ws, dev_status,
                                   as_stream(stream));

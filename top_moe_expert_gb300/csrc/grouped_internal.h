@@ -26,14 +26,4 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
                                 const int32_t *sorted, const int32_t *expert_ids, const int32_t *npp, int b,
                                 int cap_rows, void *y, bool y_f32, void *ws, int32_t *dev_status, cudaStream_t s);
 
-// 4-bit AWQ grouped path for blocks of b <= 16 rows (mma.sync on the raw
-// codes, grouped_awq_mma.cu): [done: cap_rows / b int32 | gu: M*k*2I f32 |
-// yr: M*k*d f32]
-size_t grouped_awq_mma_workspace(int M, int k, int d, int I, int b, int cap_rows);
-bool grouped_awq_mma_eligible(int b, int d, int I);
-moe_status_t grouped_awq_mma_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
-                                    const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
-                                    const int32_t *sorted, const int32_t *expert_ids, const int32_t *npp, int b,
-                                    int cap_rows, void *y, bool y_f32, void *ws, int32_t *dev_status, cudaStream_t s);
-
 }  // namespace moe

@@ -93,45 +93,3 @@ MOE_API moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows
     return launch_status();
 }
 
-// ---------------------------------------------------------------- transpose
-// dst[e][c][r] = src[e][r][c] for bytes, 32x32 tiles through shared memory.
-namespace moe {
-__global__ void __launch_bounds__(256) transpose_u8_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
-                                                           int R, int C)
-{
-    __shared__ uint8_t tile[32][33];
-    const int e = blockIdx.z;
-    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-    const uint8_t *s = src + static_cast<int64_t>(e) * R * C;
-    uint8_t *d = dst + static_cast<int64_t>(e) * R * C;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int i = ty; i < 32; i += 8) {
-        const int r = r0 + i, c = c0 + tx;
-        if (r < R && c < C)
-            tile[i][tx] = s[static_cast<int64_t>(r) * C + c];
-    }
-    __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-        const int c = c0 + i, r = r0 + tx;
-        if (r < R && c < C)
-            d[static_cast<int64_t>(c) * R + r] = tile[tx][i];
-    }
-}
-}  // namespace moe
-
-MOE_API moe_status_t moe_mxfp8_transpose(const moe_weights_t *w, void *q_t, void *scale_t, void *stream)
-{
-    if (!w || w->fmt != MOE_W_MXFP8 || w->E < 1 || w->N < 1 || w->K < 32 || w->K % 32 != 0)
-        return MOE_ERR_INVALID_ARG;
-    if (!w->q || !w->scale || !q_t || !scale_t)
-        return MOE_ERR_INVALID_ARG;
-    cudaStream_t s = as_stream(stream);
-    dim3 g1((w->K + 31) / 32, (w->N + 31) / 32, w->E);
-    transpose_u8_kernel<<<g1, 256, 0, s>>>(static_cast<const uint8_t *>(w->q), static_cast<uint8_t *>(q_t), w->N, w->K);
-    if (launch_status() != MOE_OK)
-        return MOE_ERR_CUDA;
-    dim3 g2((w->K / 32 + 31) / 32, (w->N + 31) / 32, w->E);
-    transpose_u8_kernel<<<g2, 256, 0, s>>>(static_cast<const uint8_t *>(w->scale), static_cast<uint8_t *>(scale_t), w->N,
-                                           w->K / 32);
-    return launch_status();
-}

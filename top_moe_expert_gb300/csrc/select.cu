@@ -53,8 +53,8 @@ MOE_API moe_status_t moe_ffn_select_path(int32_t M, int32_t k, int32_t E, int32_
     if (fmt == MOE_W_AWQ4 && d > 8064 && b > 64)
         b = 64;
     const bool dec = decode_shape_ok(k, d, I, fmt), grp = grouped_shape_ok(d, I, b, fmt);
-    // MXFP8: the output-centric path up to two tokens; AWQ: the grouped path
-    const bool want_decode = fmt == MOE_W_MXFP8 && M <= 2;
+    // MXFP8: the output-centric path for one token; AWQ: the grouped path
+    const bool want_decode = fmt == MOE_W_MXFP8 && M <= 1;
     if (want_decode ? dec : !grp) {
         if (!dec)
             return MOE_ERR_UNSUPPORTED;

@@ -1,5 +1,5 @@
 // topk.cu -- top-k softmax routing (one warp per token); the selection
-// itself is topk_warp (topk.cuh), shared with the fused single-token layer.
+// itself is topk_warp (topk.cuh).
 #include "common.cuh"
 #include "topk.cuh"
 
