@@ -237,7 +237,7 @@ class Step:
     grouped layer; with the fixed-routing AWQ workloads, the layer alone (with
     its alignment on the grouped path)."""
 
-    def __init__(self, wl, n_inputs, device, path: str = "decode", block: int = 0):
+    def __init__(self, wl, n_inputs, device, path: str = "decode", block: int = 0, layers: int = 0):
         import top_moe_expert_gb300 as moe
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
@@ -265,7 +265,7 @@ class Step:
         lw_bytes = sum(t.numel() * t.element_size() for p in w0 for t in p if t is not None)
         self.ids_host = [self._host_ids(j) for j in range(n_inputs)]
         est = max(step_bytes(wl, ids) for ids in self.ids_host[:8])
-        self.L = layer_copies(wl, est, lw_bytes)
+        self.L = layers if layers > 0 else layer_copies(wl, est, lw_bytes)
         self.layer_weight_bytes = lw_bytes
         self.layers = []
         for l in range(self.L):
@@ -504,7 +504,7 @@ def run_ours(args, rank, world, device):
         block = block or b
     Kg = min(K, 1000 if wl.M <= 64 else 50)              # steps per captured graph
     n_inputs = min(Kg + W, 1024 if wl.M <= 64 else 16)
-    st = Step(wl, n_inputs, device, path, block)
+    st = Step(wl, n_inputs, device, path, block, args.layers)
     s = st.stream
 
     # ---- the timed steps: graphs of Kg steps back to back (inputs already in
@@ -874,6 +874,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "grouped"])
     ap.add_argument("--block", type=int, default=0, help="MoE block size b of the grouped path (0: automatic)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="copies of the layer's weights the steps rotate through (0: enough that the inputs of "
+                         "the timed steps exceed the L2; 1 keeps a profiling run small)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
