@@ -33,6 +33,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -197,12 +198,23 @@ SRC_FILES = {
 }
 
 
+_C_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with its comments and blank lines removed (string
+    and character literals kept), so that a comment edit leaves the hash of
+    the compiled code unchanged."""
+    text = _C_TOKENS.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def decode_src_hash(path: str = "decode") -> str:
-    """SHA-256 over the kernel sources of one path (the ncu counters in
-    profiles/traffic.json are valid only for these exact sources)."""
+    """SHA-256 over the kernel sources of one path, comments removed (the ncu
+    counters in profiles/traffic.json are valid only for this code)."""
     h = hashlib.sha256()
     for f in SRC_FILES[path]:
-        h.update(open(os.path.join(ROOT, "top_moe_expert_gb300", "csrc", f), "rb").read())
+        h.update(code_only(open(os.path.join(ROOT, "top_moe_expert_gb300", "csrc", f)).read()).encode())
     return h.hexdigest()
 
 

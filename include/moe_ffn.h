@@ -306,11 +306,15 @@ moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d,
  * what changed and on hardware efficiency: the output-centric path for few
  * tokens, the expert-centric grouped path for large batches), at the
  * crossover measured on GB300 at d = 2048, I = 768, E = 128, k = 8:
- *   MOE_W_MXFP8: MOE_PATH_DECODE for M <= 2, else MOE_PATH_GROUPED
- *                (decode 23.8 us against grouped 220 us at M = 1; grouped
- *                53.5 against 76.5 us at M = 4 and faster at every larger M);
- *   MOE_W_AWQ4:  MOE_PATH_GROUPED (43.4 against 43.9 us at M = 1, 62.6
- *                against 396 us at M = 21).
+ *   MOE_W_MXFP8: MOE_PATH_DECODE for M <= 1 where the single-kernel decode
+ *                is built for (k, d, I) on GB300's 152 SMs (d = 512,
+ *                I = 256; d = 1024, I = 512; d = 2048, I = 512, 768 or
+ *                1024; k small enough for its shared-memory plan, k <= 12
+ *                at d = 2048, I = 768), else MOE_PATH_GROUPED (decode 15.4
+ *                against grouped 27.8 us at M = 1; grouped 41.5 against
+ *                179 us at M = 4 and faster at every larger M; at d = 7168,
+ *                I = 2048, M = 1, grouped 80.9 against 250 us);
+ *   MOE_W_AWQ4:  MOE_PATH_GROUPED (35.0 against 38.0 us at M = 1).
  * When the preferred path does not take the shape (the limits of
  * moe_ffn_decode and moe_ffn_grouped on d, I and k), the other one is
  * returned; when neither does, MOE_ERR_UNSUPPORTED.

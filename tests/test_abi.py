@@ -140,8 +140,10 @@ def test_python_layout_helper_matches_library():
 
 def test_select_path_at_the_measured_crossover(L):
     """Path choice (host only): MXFP8 takes the output-centric path for one
-    token and the grouped path from two; 4-bit AWQ takes the grouped path.  The block size is twice the expected rows per expert rounded up
-    to a power of two within the format's range."""
+    token where its single-kernel form is built and the grouped path
+    otherwise; 4-bit AWQ takes the grouped path.  The block size is twice
+    the expected rows per expert rounded up to a power of two within the
+    format's range."""
     D, G = moe.MOE_PATH_DECODE, moe.MOE_PATH_GROUPED
     mx, awq = moe.MOE_W_MXFP8, moe.MOE_W_AWQ4
     sel = lambda M, fmt=mx, k=8, E=128, d=2048, I=768: moe.moe_ffn_select_path(M, k, E, d, I, fmt)
@@ -154,6 +156,12 @@ def test_select_path_at_the_measured_crossover(L):
     assert sel(1, awq) == (G, 8) and sel(21, awq) == (G, 8) and sel(512, awq) == (G, 64)
     # shapes one path does not take go to the other
     assert sel(1, d=1152, I=384) == (G, 16)                  # decode needs d % 512 == 0
+    # one token takes the decode path only where its single-kernel form is
+    # built (the large-expert shape and k beyond its shared-memory plan go
+    # to the grouped path, which is faster there than the two-kernel decode)
+    assert sel(1, d=7168, I=2048, E=384) == (G, 16)
+    assert sel(1, k=12) == (D, 0) and sel(1, k=13) == (G, 16)
+    assert sel(1, d=2048, I=1024, k=9) == (D, 0) and sel(1, d=2048, I=1024, k=10) == (G, 16)
     assert sel(64, d=1536, I=96) == (D, 0)                   # grouped needs I % 128 == 0
     assert sel(21, awq, d=9216, I=256) == (D, 0)             # AWQ grouped: d / 128 <= 64
     assert sel(21, awq, d=3072, I=256) == (G, 8)

@@ -28,6 +28,8 @@ moe_status_t decode_stream_launch(const __nv_bfloat16 *x, int M, int d, int I, i
 // with the routing (decode_pipe.cu); ws holds the arrival counter in its first
 // 8 bytes (zero before the first use), then h past kWsReserved
 bool decode_pipe_eligible(int M, int k, int d, int I, int E);
+// the shape check alone, for a grid of G CTAs (host only, no device query)
+bool decode_pipe_shape_fits(int k, int d, int I, int G);
 bool decode_pipe_route_eligible(int E, int k);
 size_t decode_pipe_workspace(int k, int I);
 moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, const int32_t *ids, const float *wts,

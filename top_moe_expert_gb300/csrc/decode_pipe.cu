@@ -13,20 +13,24 @@
 // (38.9 MB at d = 2048, I = 768, k = 8).  One CTA per SM, with warp roles:
 //   * warp 0, producer: routes the token (or reads the given routing),
 //     publishes the valid routes in slot order, then streams this CTA's gate
-//     and up rows and their E8M0 rows with cp.async.bulk through a ring of 8
-//     slots of 4 neurons each (about 135 KB in flight per SM: enough to keep
-//     HBM busy, few enough that the other loads do not queue for long), and
-//     after the last gate/up stage this CTA's rows of every routed expert's
-//     down projection into slots of their own.
+//     and up rows with cp.async.bulk through a ring of 12 slots of 4 neurons
+//     each (192 KB in flight per SM at d = 2048).  Once its last gate/up
+//     stage has landed it sends this CTA's rows of every routed expert's down
+//     projection to L2 (a bulk prefetch), and once the ring is drained it
+//     copies them from L2 into the idle ring.
+//   * warp 1: reads the arrival counter's epoch (below) before this CTA can
+//     arrive; a CTA with no (route, neuron) pair arrives at once.
 //   * warps 2..17, gate/up: 4 groups of 4 warps.  Group g takes stages g,
 //     g+4, g+8, ...; its warps split K, each holding its slice of x in
 //     registers (fp16 after an exact power-of-two rescale), and form the
 //     slice's partial dot products with mixed fp16 x fp16 -> FP32 FMAs.  The
 //     group adds the partials in a fixed order, forms h = SiLU(g) * u in
-//     FP32 and writes it to the workspace.
-//   * warps 18..25: load this CTA's E8M0 bytes of the down projection, then
-//     wait until every CTA has written its share of h (one arrival per CTA on
-//     a counter in the workspace) and copy all of h into shared memory.
+//     FP32 and writes it to the workspace; the CTA's last h arrives on the
+//     counter.
+//   * warps 18..25: load the E8M0 rows of this CTA's gate/up neurons (before
+//     the first stage is consumed) and of its down-projection rows, then one
+//     lane waits until every CTA has arrived and copies all of h into
+//     shared memory in one bulk copy.
 // Tail: the 24 compute warps form this CTA's output rows of every route's
 // down projection (h as fp16 after an exact power-of-two rescale per route,
 // one warp per (route, row), butterfly sums); y is the
@@ -718,11 +722,14 @@ inline bool shape_ok(int d, int I)
 // MOE_ERR_TIMEOUT) without faulting or hanging the GPU.
 static std::atomic<int> g_shortfall{0};
 
+bool decode_pipe_shape_fits(int k, int d, int I, int G)
+{
+    return k >= 1 && k <= dp::kMaxK && G >= 1 && dp::shape_ok(d, I) && dp::Plan{d, I, k, G}.fits();
+}
+
 bool decode_pipe_eligible(int M, int k, int d, int I, int E)
 {
-    if (M != 1 || k < 1 || k > dp::kMaxK || E < 1 || !dp::shape_ok(d, I))
-        return false;
-    return dp::Plan{d, I, k, device_sm_count()}.fits();
+    return M == 1 && E >= 1 && decode_pipe_shape_fits(k, d, I, device_sm_count());
 }
 
 bool decode_pipe_route_eligible(int E, int k) { return E >= k && E <= dp::kCW * 32; }

@@ -5,15 +5,21 @@
 // uses the output-centric path where few tokens make the grouped path's
 // alignment, padding and combine dominant.  Where the two cross is a matter
 // of measurement; the rule below follows the crossover measured on GB300 at
-// d = 2048, I = 768, E = 128, k = 8 (µs per step, routing included):
+// d = 2048, I = 768, E = 128, k = 8 (us per step, routing included, steps
+// back to back over copies of the layer's weights larger than the L2):
 //
-//     M                    1      4      8     16     32     64    512
-//     MXFP8 decode      23.8   76.5    357    701   1319   2384      -
-//     MXFP8 grouped      220   53.5   73.6  101.8  124.8  136.6  159.1
+//     M                    1      2      4      8     16     32     64    512
+//     MXFP8 decode      15.4      -    179      -    696      -      -      -
+//     MXFP8 grouped     27.8   34.0   41.5   57.3   80.5  102.0  113.8  144.6
 //
-// and, for 4-bit AWQ, 43.9 (decode) against 43.4 µs (grouped) at M = 1 and
-// 396 against 62.6 µs at M = 21.  Host only: nothing here touches a GPU.
+// At M = 1 the decode figure is the single-kernel form, built for a few
+// (d, I) pairs; elsewhere the decode path runs its two-kernel form, which
+// loses to the grouped path at every M measured (at d = 7168, I = 2048,
+// E = 384, M = 1: 250 us against 80.9 us).  For 4-bit AWQ the grouped path
+// is ahead at one token (35.0 against 38.0 us) and far ahead at M = 21.
+// Host only: nothing here touches a GPU.
 #include "common.cuh"
+#include "decode_internal.h"
 
 namespace moe {
 
@@ -32,6 +38,10 @@ static bool grouped_shape_ok(int d, int I, int b, int fmt)
         return d % 256 == 0 && d / 128 <= 64 && I / 128 <= 64 && b <= 128 && (d <= 8064 || b <= 112);
     return true;
 }
+
+// The SM count the single-kernel decode is planned for (GB300); a GPU with
+// another count re-checks the plan at dispatch and falls back if it misses.
+constexpr int kSelectSMs = 152;
 
 }  // namespace moe
 
@@ -53,8 +63,9 @@ MOE_API moe_status_t moe_ffn_select_path(int32_t M, int32_t k, int32_t E, int32_
     if (fmt == MOE_W_AWQ4 && d > 8064 && b > 64)
         b = 64;
     const bool dec = decode_shape_ok(k, d, I, fmt), grp = grouped_shape_ok(d, I, b, fmt);
-    // MXFP8: the output-centric path for one token; AWQ: the grouped path
-    const bool want_decode = fmt == MOE_W_MXFP8 && M <= 1;
+    // MXFP8: the output-centric path for one token where its single-kernel
+    // form is built; AWQ: the grouped path
+    const bool want_decode = fmt == MOE_W_MXFP8 && M <= 1 && decode_pipe_shape_fits(k, d, I, kSelectSMs);
     if (want_decode ? dec : !grp) {
         if (!dec)
             return MOE_ERR_UNSUPPORTED;
