@@ -163,25 +163,26 @@ moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_
  *   w2       N = d, K = I, same format as w13
  *   y        [M][d] of ydt (MOE_BF16 or MOE_FP32)
  *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned; its
- *            first 256 bytes must be zero before the first call that uses
- *            it (e.g. cudaMemset once) and then left alone: they hold a
- *            grid-barrier arrival counter that every call advances by a
- *            multiple of the grid size (after a call that reports
- *            MOE_ERR_TIMEOUT they must be zeroed again).  Every other
- *            path keeps its data after these 256 bytes, so one workspace
- *            sized for the largest batch serves calls of any batch size
- *            and layout in turn.
+ *            first 82176 bytes (256 + 80 KiB) must be zero before the
+ *            first call that uses it (e.g. cudaMemset once) and then left
+ *            alone: the single-token kernel keeps there a count of its CTAs
+ *            over all calls, which gives each call its own tag, and its
+ *            exchange of h, each value written with the tag of its call.
+ *            Every other path keeps its data after those bytes, so one
+ *            workspace sized for the largest batch serves calls of any
+ *            batch size in turn.  A tag repeats only after 2^32 calls.
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
  * Kernels by case: MOE_W_MXFP8 (standard layout) with M == 1,
- * (d, I) in {(512, 256), (1024, 512), (2048, 512), (2048, 768)}, k <= 8 or
- * so (the shared-memory plan decides) -> one kernel, one CTA per SM (each
- * CTA an even share of the (route, neuron) pairs: gate/up rows streamed by
- * cp.async.bulk, h = SiLU(g)*u written to ws past its first 256 bytes, one
- * arrival per CTA on a counter in ws[0..8); then each CTA forms its own
- * d / #SM output rows of every route's down projection from h staged in
- * shared memory as fp16 after an exact power-of-two rescale per route, and
- * the routing-weighted sum over the k slots; with moe_ffn_decode_logits the
- * routing runs in it too);
+ * (d, I) in {(512, 256), (1024, 512), (2048, 512), (2048, 768),
+ * (2048, 1024)}, k small enough for the shared-memory plan (k <= 10 at
+ * d = 2048, I = 768 on 152 SMs) -> one kernel, one CTA per SM (each CTA an
+ * even share of the (route, neuron) pairs: gate/up rows streamed by
+ * cp.async.bulk, h = SiLU(g)*u published in ws with the call's tag; each
+ * CTA reads all of h back once every value carries the tag, then forms its
+ * own d / #SM output rows of every route's down projection, from those rows
+ * streamed into the same ring and h as fp16 after an exact power-of-two
+ * rescale per lane, and the routing-weighted sum over the k slots; with
+ * moe_ffn_decode_logits the routing runs in it too);
  * MXFP8 with M*k <= 512 -> a gate/up kernel and a
  * down kernel chained by programmatic dependent launch;
  * MOE_W_NVFP4S -> a gate/up kernel and a down kernel, one warp per
@@ -219,16 +220,15 @@ moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, int32_t x
                                    size_t ws_bytes, int32_t *dev_status, void *stream);
 
 /* Failure-detection test hook (no counterpart on the pages).  The one-kernel
- * single-token path waits, in every CTA, until all CTAs of the grid have
- * arrived on the counter in ws[0..8) -- a wait bounded by a time limit of
- * about 2 s, after which the CTA stops, writes MOE_ERR_TIMEOUT to
- * dev_status[1] and returns, leaving the context usable.  This call makes
- * the launches that follow it expect n arrivals more than the grid provides,
- * so that a test can make that wait run out without faulting or hanging the
- * GPU; n = 0 (the default) restores normal operation.  The counter still
- * ends each launch at a multiple of the grid size, so the workspace stays
- * valid.  Process-wide; 0 <= n <= 1024, else MOE_ERR_INVALID_ARG. */
-moe_status_t moe_debug_arrival_shortfall(int32_t n);
+ * single-token path waits, in every CTA, until every value of h carries the
+ * call's tag -- a wait bounded by a time limit of about 2 s, after which the
+ * CTA stops, writes MOE_ERR_TIMEOUT to dev_status[1] and returns, leaving
+ * the context usable.  on = 1 makes the launches that follow wait for a tag
+ * that no CTA writes, so that a test can make that wait run out without
+ * faulting or hanging the GPU; on = 0 (the default) restores normal
+ * operation.  The workspace stays valid: the next call takes a new tag.
+ * Process-wide; on other than 0 or 1 returns MOE_ERR_INVALID_ARG. */
+moe_status_t moe_debug_exchange_stall(int32_t on);
 
 /* ------------------------------------------------- expert-centric path
  * Grouped path for larger batches ("Hardware-Native Joint Sparse-

@@ -40,6 +40,12 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) <= set(moe._PROTOS), set(names) - set(moe._PROTOS)
 
 
+def test_exchange_stall_hook_validates_its_argument(L):
+    # host only: sets a process-wide flag read at the next launch
+    assert L.moe_debug_exchange_stall(2) == 1 and L.moe_debug_exchange_stall(-1) == 1
+    assert L.moe_debug_exchange_stall(1) == 0 and L.moe_debug_exchange_stall(0) == 0
+
+
 def test_status_names_and_version(L):
     for code, name in moe.STATUS_NAMES.items():
         assert L.moe_status_string(code).decode() == name
@@ -58,17 +64,14 @@ def test_align_capacity_bound():
 
 def test_decode_workspace_size():
     _r256 = lambda n: (n + 255) // 256 * 256
-    # 256 reserved bytes (the single-token paths' barrier counter), then h
-    # [M*k][I] f32 (the two-kernel paths); d % 1024 != 0 rules out the
-    # single-pass path and its per-SM partial outputs
-    assert moe.moe_ffn_decode_workspace_size(65, 8, 512, 768) == 256 + 65 * 8 * 768 * 4
-    # one token: the counter (256 B), then h [k][I] f32 of the single-kernel path
-    assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == 256 + 8 * 768 * 4
+    # 256 + 80 KiB reserved for the single-token kernel (its CTA count and its
+    # h exchange words), then h [M*k][I] f32 of every other decode path
+    R = 256 + 80 * 1024
+    assert moe.moe_ffn_decode_workspace_size(65, 8, 512, 768) == R + 65 * 8 * 768 * 4
+    assert moe.moe_ffn_decode_workspace_size(1, 8, 512, 768) == R + 8 * 768 * 4
     assert moe.moe_ffn_decode_workspace_size(3, 8, 512, 100) % 256 == 0
-    # 2 <= M <= 64, d % 1024 != 0: the counter, then h [M*k][I] f32
-    for M, k, d, I in ((2, 8, 512, 768), (64, 8, 512, 768)):
-        assert moe.moe_ffn_decode_workspace_size(M, k, d, I) == 256 + _r256(M * k * I * 4)
-    assert moe.moe_ffn_decode_workspace_size(1, 8, 2048, 768) == 256 + 8 * 768 * 4
+    for M, k, d, I in ((2, 8, 512, 768), (64, 8, 512, 768), (1, 8, 2048, 768)):
+        assert moe.moe_ffn_decode_workspace_size(M, k, d, I) == R + _r256(M * k * I * 4)
 
 
 def _r256(n):
@@ -160,7 +163,7 @@ def test_select_path_at_the_measured_crossover(L):
     # built (the large-expert shape and k beyond its shared-memory plan go
     # to the grouped path, which is faster there than the two-kernel decode)
     assert sel(1, d=7168, I=2048, E=384) == (G, 16)
-    assert sel(1, k=12) == (D, 0) and sel(1, k=13) == (G, 16)
+    assert sel(1, k=10) == (D, 0) and sel(1, k=11) == (G, 16)
     assert sel(1, d=2048, I=1024, k=9) == (D, 0) and sel(1, d=2048, I=1024, k=10) == (G, 16)
     assert sel(64, d=1536, I=96) == (D, 0)                   # grouped needs I % 128 == 0
     assert sel(21, awq, d=9216, I=256) == (D, 0)             # AWQ grouped: d / 128 <= 64

@@ -179,18 +179,18 @@ def test_mx_single_token_activation_scales_routes_and_counter():
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
     gs.assert_layer_close(ys[0], oracle_decode(layer, x, ids2, w))
-    # the one-kernel path: each call adds one arrival per CTA (one CTA per
-    # SM) to the arrival counter in ws[0..8)
+    # the one-kernel path: each call adds one per CTA (one CTA per SM) to the
+    # CTA count in ws[0..8)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert ws[:8].view(torch.int64).item() == 3 * sms
 
 
 def test_single_token_wait_runs_out_and_reports_timeout():
-    """Failure detection without a GPU fault: the one-kernel path's counter
-    wait is bounded.  Made to expect one arrival more than the grid gives, it
-    gives up after its time limit, reports MOE_ERR_TIMEOUT in dev_status[1]
-    and returns; the context stays usable and the workspace valid, so the
-    next call on the same workspace matches the oracle."""
+    """Failure detection without a GPU fault: the one-kernel path's wait for
+    h is bounded.  Made to wait for a tag that no CTA writes, it gives up
+    after its time limit, reports MOE_ERR_TIMEOUT in dev_status[1] and
+    returns; the context stays usable and the workspace valid, so the next
+    call on the same workspace matches the oracle."""
     wl = inputs.TINY
     layer = mx_layer(wl)
     x = inputs.activations(wl)[:1]
@@ -199,14 +199,14 @@ def test_single_token_wait_runs_out_and_reports_timeout():
     ws = torch.zeros(moe.moe_ffn_decode_workspace_size(1, wl.k, wl.d, wl.I), dtype=torch.uint8, device="cuda")
     st = torch.zeros(2, dtype=torch.int32, device="cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    moe.moe_debug_arrival_shortfall(1)
+    moe.moe_debug_exchange_stall(True)
     try:
         run_decode(layer, x, ids, w, torch.float32, ws=ws, dev_status=st)
         torch.cuda.synchronize()
     finally:
-        moe.moe_debug_arrival_shortfall(0)
+        moe.moe_debug_exchange_stall(False)
     assert st.tolist() == [0, 6]                                   # MOE_ERR_TIMEOUT
-    assert ws[:8].view(torch.int64).item() == sms                  # every CTA still arrived once
+    assert ws[:8].view(torch.int64).item() == sms                  # every CTA still counted once
     st.zero_()
     y = run_decode(layer, x, ids, w, torch.float32, ws=ws, dev_status=st)
     torch.cuda.synchronize()
@@ -295,9 +295,10 @@ def test_large_expert_decode(wl):
 def test_one_workspace_serves_every_batch_size():
     """One workspace, sized for the largest batch, reused by calls of other
     batch sizes in turn: every output equals the one computed with a fresh
-    workspace, and the arrival counter in ws[0..8) holds exactly one arrival
-    per CTA for each call of the one-kernel single-token path (the other
-    paths keep their data past ws[256])."""
+    workspace; the CTA count in ws[0..8) holds exactly one per CTA for each
+    call of the one-kernel single-token path, and its h exchange words in
+    ws[256..) all carry the last such call's tag (the call's index, from 1):
+    the other paths keep their data past the reserved start."""
     layer = mx_layer(dataclasses.replace(inputs.DECODE, name="ws_reuse_layer", seed=5))
     wl = dataclasses.replace(inputs.DECODE, name="ws_reuse_m8", M=8, seed=7)
     x = inputs.activations(wl)
@@ -311,7 +312,11 @@ def test_one_workspace_serves_every_batch_size():
         assert torch.equal(run_decode(*args, ws=ws), fresh), M
     torch.cuda.synchronize()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert ws[:8].view(torch.int64).item() == calls.count(1) * sms
+    n1 = calls.count(1)
+    assert ws[:8].view(torch.int64).item() == n1 * sms
+    words = ws[256:256 + wl.k * wl.I * 8].view(torch.int32).view(-1, 2).cpu()
+    assert bool((words[:, 1] == n1).all())
+    assert bool(torch.isfinite(words[:, 0].view(torch.float32)).all())
 
 
 @pytest.mark.parametrize("M", [1, 3])

@@ -69,7 +69,7 @@ _PROTOS = {
                                _P, _SZ, _P, _P]),
     "moe_ffn_decode_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                                       ctypes.POINTER(moe_weights_t), _P, _I32, _P, _P]),
-    "moe_debug_arrival_shortfall": (_I32, [_I32]),
+    "moe_debug_exchange_stall": (_I32, [_I32]),
 }
 
 
@@ -273,12 +273,12 @@ def moe_ffn_select_path(M: int, k: int, E: int, d: int, I: int, fmt: int = None)
     return p.value, b.value
 
 
-def moe_debug_arrival_shortfall(n: int) -> None:
+def moe_debug_exchange_stall(on: bool) -> None:
     """Failure-detection test hook: the single-token one-kernel launches that
-    follow expect n arrivals more than their grid provides, so their bounded
-    counter wait runs out and reports MOE_ERR_TIMEOUT in dev_status[1]; 0
+    follow wait for h values tagged with a tag no CTA writes, so their bounded
+    wait runs out and reports MOE_ERR_TIMEOUT in dev_status[1]; False
     restores normal operation."""
-    _check(lib().moe_debug_arrival_shortfall(int(n)), "moe_debug_arrival_shortfall")
+    _check(lib().moe_debug_exchange_stall(1 if on else 0), "moe_debug_exchange_stall")
 
 
 def moe_align_capacity(M: int, k: int, E: int, b: int):

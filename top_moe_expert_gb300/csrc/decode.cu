@@ -317,17 +317,12 @@ MOE_API moe_status_t moe_ffn_decode_workspace_size(int32_t M, int32_t k, int32_t
 {
     if (M < 0 || k < 1 || d < 1 || I < 1 || !bytes)
         return MOE_ERR_INVALID_ARG;
-    // The first kWsReserved bytes hold the arrival counter of the one-kernel
-    // single-token path (ws[0..8)).  Every other path starts its data after
-    // them, so one workspace serves calls of any batch size in turn without
-    // disturbing the counter.
-    size_t h = kWsReserved + ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
-    size_t part = 0;
-    if (M == 1 && k <= 32) {
-        const size_t p1 = decode_pipe_workspace(k, I);
-        part = part > p1 ? part : p1;
-    }
-    *bytes = h > part ? h : part;
+    // The first kWsReserved bytes belong to the one-kernel single-token path
+    // (its CTA count and its h exchange words); every other path starts its
+    // data after them, so one workspace serves calls of any batch size in
+    // turn without disturbing them.
+    const size_t h = kWsReserved + ws_round(static_cast<size_t>(M) * k * I * sizeof(float));
+    *bytes = h;
     return MOE_OK;
 }
 

@@ -11,10 +11,14 @@
 
 namespace moe {
 
-// Bytes at the start of a decode workspace reserved for the arrival counter
-// of the one-kernel single-token paths (ws[0..8), zero before the first use);
-// the other decode paths place their data after them.
-constexpr size_t kWsReserved = 256;
+// The start of a decode workspace is reserved for the single-token kernel
+// (zero before the first use): its CTA count over all launches in
+// ws[0..8), then, from kWsCounterBytes, its h exchange words (8 bytes per
+// (route, neuron), at most kWsTagBytes).  No other path writes there: the
+// other decode paths place their data after kWsReserved.
+constexpr size_t kWsCounterBytes = 256;
+constexpr size_t kWsTagBytes = 80 * 1024;
+constexpr size_t kWsReserved = kWsCounterBytes + kWsTagBytes;
 
 bool decode_stream_eligible(int M, int k, int d, int I, int E, const void *q13, const void *s13,
                             const void *q2, const void *s2);
@@ -25,13 +29,11 @@ moe_status_t decode_stream_launch(const __nv_bfloat16 *x, int M, int d, int I, i
                                   int32_t *dev_status, cudaStream_t stream);
 
 // single-token MXFP8 layer in one kernel on the standard layout, optionally
-// with the routing (decode_pipe.cu); ws holds the arrival counter in its first
-// 8 bytes (zero before the first use), then h past kWsReserved
+// with the routing (decode_pipe.cu); it uses only the reserved start of ws
 bool decode_pipe_eligible(int M, int k, int d, int I, int E);
 // the shape check alone, for a grid of G CTAs (host only, no device query)
 bool decode_pipe_shape_fits(int k, int d, int I, int G);
 bool decode_pipe_route_eligible(int E, int k);
-size_t decode_pipe_workspace(int k, int I);
 moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, const int32_t *ids, const float *wts,
                                 const float *logits, int32_t *ids_out, float *wts_out, int k, const uint8_t *q13,
                                 const uint8_t *s13, const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32,

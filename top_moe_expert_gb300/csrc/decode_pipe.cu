@@ -13,40 +13,40 @@
 // (38.9 MB at d = 2048, I = 768, k = 8).  One CTA per SM, with warp roles:
 //   * warp 0, producer: routes the token (or reads the given routing),
 //     publishes the valid routes in slot order, then streams this CTA's gate
-//     and up rows with cp.async.bulk through a ring of 12 slots of 4 neurons
-//     each (192 KB in flight per SM at d = 2048).  Once its last gate/up
-//     stage has landed it sends this CTA's rows of every routed expert's down
-//     projection to L2 (a bulk prefetch), and once the ring is drained it
-//     copies them from L2 into the idle ring.
-//   * warp 1: reads the arrival counter's epoch (below) before this CTA can
-//     arrive; a CTA with no (route, neuron) pair arrives at once.
+//     and up rows, 4 neurons per stage, through a ring of up to 11 slots
+//     (7 at d = 2048, I = 768: 112 KB in flight per SM); once the ring is
+//     first full it sends this CTA's rows of every routed expert's down
+//     projection into buffers of their own, one bulk copy per route, so
+//     they stream behind the first gate/up stages.
+//   * warp 1: reads the launch's epoch from the call counter and advances it.
 //   * warps 2..17, gate/up: 4 groups of 4 warps.  Group g takes stages g,
 //     g+4, g+8, ...; its warps split K, each holding its slice of x in
 //     registers (fp16 after an exact power-of-two rescale), and form the
 //     slice's partial dot products with mixed fp16 x fp16 -> FP32 FMAs.  The
 //     group adds the partials in a fixed order, forms h = SiLU(g) * u in
-//     FP32 and writes it to the workspace; the CTA's last h arrives on the
-//     counter.
+//     FP32 and publishes it as one 8-byte (value, launch tag) word.
 //   * warps 18..25: load the E8M0 rows of this CTA's gate/up neurons (before
-//     the first stage is consumed) and of its down-projection rows, then one
-//     lane waits until every CTA has arrived and copies all of h into
-//     shared memory in one bulk copy.
-// Tail: the 24 compute warps form this CTA's output rows of every route's
-// down projection (h as fp16 after an exact power-of-two rescale per route,
-// one warp per (route, row), butterfly sums); y is the
+//     the first stage is consumed) and of its down-projection rows.
+// Exchange: the 24 compute warps read every route's h words until each
+// carries this launch's tag, into shared memory (the drained ring).  No
+// flag, fence or barrier across CTAs: a word is written once per launch and
+// read atomically, so a value is taken only when its own tag says it
+// belongs to this launch.
+// Tail: each warp forms (route, row) units of this CTA's output rows of the
+// down projection, two rows at a time, from the down-row buffers and
+// h converted per lane to fp16 after an exact power-of-two rescale; y is the
 // routing-weighted sum over routes in slot order.  The (route, neuron) space
 // is split evenly over the CTAs and each CTA owns d / G output rows, so no
 // output is reduced across CTAs.
 //
-// Arrival counter (the first 8 bytes of the workspace, zero before the first
-// use): it only grows; every launch adds exactly one per CTA, so between
-// launches it is a multiple of the grid size.  A CTA reads it before it
-// arrives; the count rounded down to a multiple of the grid is the epoch, and
-// every CTA has arrived once the count reaches the epoch plus the grid size.
-// All CTAs must be resident together: the grid is one CTA per SM, and
-// dependent launches start only after this CTA has seen every arrival.
-// Every output's summation order depends only on the shapes and the grid,
-// so repeats are bit-identical.
+// Launch tag: the first 8 bytes of the workspace count CTAs over all
+// launches (zero before the first use).  Every launch adds exactly one per
+// CTA, and a launch starts only after the previous one has completed, so
+// every CTA of launch n reads a count in [nG, nG + G) and takes n + 1 as
+// its tag.  The exchange words sit in the workspace's reserved area, which
+// no other path writes, so a word's stale tag is that of an earlier launch
+// of this kernel.  Every output's summation order depends only on the
+// shapes and the grid, so repeats are bit-identical.
 #include <atomic>
 
 #include "attr.h"
@@ -61,20 +61,23 @@ namespace dp {
 constexpr int kMaxK = 32;
 constexpr int kGW = 4;                                // warps of a gate/up group (they split K)
 constexpr int kGroups = 4;                            // gate/up groups
-constexpr int kPS = 4;                                // neurons per gate/up stage
-constexpr int kSlots = 3 * kGroups;                   // gate/up ring: three slots per group
-constexpr int kTW = 8;                                // warps of the wait/copy role
+constexpr int kPS = 4;                                // neurons per gate/up stage (4 or 8)
+constexpr int kMaxSlots = 11;                         // gate/up ring slots, at most
+constexpr int kMinSlots = 4;
+constexpr int kTW = 8;                                // warps of the scale-staging role
 constexpr int kWarpGU0 = 2;
 constexpr int kWarpT0 = kWarpGU0 + kGW * kGroups;     // 18
 constexpr int kWarps = kWarpT0 + kTW;                 // 26
 constexpr int kThreads = kWarps * 32;                 // 832
-constexpr int kCW = kWarps - kWarpGU0;                // compute warps of the tail: 24
+constexpr int kCW = kWarps - kWarpGU0;                // compute warps of the exchange and tail: 24
+constexpr int kMaxPerLane = 32;                       // exchange words per lane, at most
 constexpr uint64_t kWaitNs = 2000000000ull;           // 2 s
 constexpr int kBarRoutes = 1;                         // named barriers: routes published (all warps)
 constexpr int kBarTail = 2;                           //   the compute warps
 constexpr int kBarGroup0 = 3;                         //   gate/up group g: kBarGroup0 + g
 constexpr int kBarRank = kBarGroup0 + kGroups;        //   the compute warps ranking the logits
-constexpr int kBarScales = kBarRank + 1;              //   gate/up E8M0 rows staged (wait/copy warps arrive)
+constexpr int kBarScales = kBarRank + 1;              //   gate/up E8M0 rows staged (staging warps arrive)
+
 constexpr int kSmemMax = 227 * 1024;
 
 struct Args {
@@ -86,34 +89,50 @@ struct Args {
     float *wts_out;
     const uint8_t *q13, *s13;    // [E][2I][d], [E][2I][d/32]
     const uint8_t *q2, *s2;      // [E][d][I],  [E][d][I/32]
-    unsigned long long *ctr;     // arrival counter
-    float *h;                    // [kMaxK][I]
+    unsigned long long *ctr;     // CTA count over all launches
+    unsigned long long *xh;      // exchange words [k][I]: value bits | tag << 32
     void *y;
     int32_t *dev_status;
     int y_f32, k, d, I, E;
-    int shortfall;               // arrivals the counter wait expects beyond the grid (failure-detection test)
+    int stall;                   // readers expect a tag nobody writes (failure-detection test)
 };
 
-// Shared-memory plan (bytes), identical on host and device.  The tail's h and
-// down-projection rows reuse the gate/up ring, which is idle by then.
+// Shared-memory plan (bytes), identical on host and device: the gate/up
+// ring (h of every route is staged there once the ring has drained), this
+// CTA's down rows of every route, the E8M0 scales, small buffers, barriers.
 struct Plan {
     int d, I, k, G;
     __host__ __device__ int rows_max() const { return (d + G - 1) / G; }
-    __host__ __device__ int s1() const { return kPS * 2 * d; }                   // gate rows | up rows
+    __host__ __device__ int s1() const { return kPS * 2 * d; }                   // slot: gate rows | up rows
     __host__ __device__ int pmax() const { return (k * I + G - 1) / G; }        // pairs of a CTA, at most
-    __host__ __device__ int s2() const { return rows_max() * I; }
+    __host__ __device__ int s2() const { return rows_max() * I; }               // one route's down rows
     __host__ __device__ static int up16(int v) { return (v + 15) & ~15; }
-    __host__ __device__ int o_w2() const { return up16(k * I * 4); }            // in the ring, after h
-    __host__ __device__ int o_hh() const { return o_w2() + k * s2(); }          // in the ring: h as fp16
-    __host__ __device__ int o_s2s() const { return kSlots * s1(); }
+    __host__ __device__ int n_bars() const { return 2 * kMaxSlots + kMaxK; }   // full, empty, down rows
+    // everything but the ring
+    __host__ __device__ int fixed() const
+    {
+        return k * s2() + k * rows_max() * (I / 32) * 4 + up16(pmax() * 2 * (d / 32)) +
+               kGroups * 2 * kGW * 2 * kPS * 4 + up16(k * rows_max() * 4) + n_bars() * 8 + 3 * kMaxK * 4 + 32;
+    }
+    __host__ __device__ int slots() const
+    {
+        const int n = (kSmemMax - fixed()) / s1();
+        return n > kMaxSlots ? kMaxSlots : n;
+    }
+    __host__ __device__ int o_w2() const { return slots() * s1(); }            // [k][RM][I] down rows
+    __host__ __device__ int o_s2s() const { return o_w2() + k * s2(); }
     __host__ __device__ int o_gsc() const { return o_s2s() + k * rows_max() * (I / 32) * 4; }
     __host__ __device__ int o_gpart() const { return o_gsc() + up16(pmax() * 2 * (d / 32)); }
     __host__ __device__ int o_dpart() const { return o_gpart() + kGroups * 2 * kGW * 2 * kPS * 4; }
-    __host__ __device__ int o_bars() const { return o_dpart() + up16(k * rows_max() * 4 + k * 4); }  // + 1/scale of h
-    __host__ __device__ int o_route() const { return o_bars() + (2 * kSlots + k + 1) * 8; }
-    // route data: r_e[kMaxK] | r_w[kMaxK] | r_l[kMaxK] | target u64 | nv, done, abort, tabort, gabort[kGroups]
-    __host__ __device__ int bytes() const { return o_route() + 3 * kMaxK * 4 + 8 + 16 + kGroups * 4; }
-    __host__ __device__ bool fits() const { return bytes() <= kSmemMax && o_hh() + k * I * 2 <= kSlots * s1(); }
+    __host__ __device__ int o_bars() const { return o_dpart() + up16(k * rows_max() * 4); }
+    __host__ __device__ int o_route() const { return o_bars() + n_bars() * 8; }
+    // route data: r_e[kMaxK] | r_w[kMaxK] | r_l[kMaxK] | tag, nv, abort, tabort, gabort[kGroups]
+    __host__ __device__ int bytes() const { return o_route() + 3 * kMaxK * 4 + 32; }
+    __host__ __device__ bool fits() const
+    {
+        return s2() > 0 && slots() >= kMinSlots && bytes() <= kSmemMax && k * I * 4 <= slots() * s1() &&
+               static_cast<size_t>(k) * I * 8 <= kWsTagBytes && k * I <= kCW * 32 * kMaxPerLane;
+    }
 };
 
 __device__ __forceinline__ void set_err(int32_t *st, int code)
@@ -216,13 +235,6 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
 {
     unsigned long long v;
@@ -230,22 +242,23 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
-__device__ __forceinline__ void red_release_add(unsigned long long *p)
-{
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(p) : "memory");
-}
-
 __device__ __forceinline__ void red_relaxed_add(unsigned long long *p)
 {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p) : "memory");
 }
 
-__device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t *p, uint32_t v)
+// one (value, tag) word of the h exchange: 8-byte aligned, so single-copy atomic
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
 {
-    uint32_t old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
-                 : "=r"(old) : "r"(tc::smem_u32(p)), "r"(v) : "memory");
-    return old;
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// two consecutive exchange words (16-byte aligned); each word is read
+// single-copy atomically on its own
+__device__ __forceinline__ void ld_relaxed_u64x2(const unsigned long long *p, unsigned long long &a,
+                                                 unsigned long long &b)
+{
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
 // KPL: gate/up elements per lane of a warp's K slice (d = 32 * kGW * KPL);
@@ -258,40 +271,38 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     const int d = a.d, I = a.I, k = a.k, G = gridDim.x, c = blockIdx.x;
     const Plan pl{d, I, k, G};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int RM = pl.rows_max(), S1 = pl.s1(), S2 = pl.s2();
-    uint8_t *slot1 = smem;
-    float *hbuf = reinterpret_cast<float *>(smem);                       // [nv][I], the tail's h
-    uint8_t *slot2 = smem + pl.o_w2();                                   // the tail's [k][RM][I] down rows
+    const int RM = pl.rows_max(), S1 = pl.s1(), S2 = pl.s2(), NS = pl.slots();
+    uint8_t *ring = smem;
+    float *hbuf = reinterpret_cast<float *>(smem);                       // [nv][I] h, in the drained ring
+    uint8_t *w2s = smem + pl.o_w2();                                     // [k][RM][I] down rows
     float *s2s = reinterpret_cast<float *>(smem + pl.o_s2s());           // [k][RM][I/32] down scales
     uint8_t *gsc = smem + pl.o_gsc();                                    // [P][2][d/32] gate/up E8M0 rows
     float *gpart = reinterpret_cast<float *>(smem + pl.o_gpart());       // [grp][2][kGW][2 kPS]
     float *dpart = reinterpret_cast<float *>(smem + pl.o_dpart());       // [k][RM]
-    const uint32_t full1 = tc::smem_u32(smem + pl.o_bars());
-    const uint32_t empty1 = full1 + 8 * kSlots, full2 = empty1 + 8 * kSlots, hbar = full2 + 8 * k;
+    const uint32_t full = tc::smem_u32(smem + pl.o_bars());
+    const uint32_t empty = full + 8 * kMaxSlots, full2 = empty + 8 * kMaxSlots;
     int *r_e = reinterpret_cast<int *>(smem + pl.o_route());
     float *r_w = reinterpret_cast<float *>(r_e + kMaxK);
     float *r_l = r_w + kMaxK;                                            // logits of the chosen routes
-    unsigned long long *target = reinterpret_cast<unsigned long long *>(r_l + kMaxK);
-    int *s_nv = reinterpret_cast<int *>(target + 1);
-    uint32_t *s_done = reinterpret_cast<uint32_t *>(s_nv + 1);            // neurons of this CTA with h written
-    volatile int *s_abort = s_nv + 2;
-    volatile int *tabort = s_nv + 3;                                     // decided before the first tail barrier
-    volatile int *gabort = s_nv + 4;                                     // [kGroups]
+    uint32_t *s_tag = reinterpret_cast<uint32_t *>(r_l + kMaxK);
+    int *s_nv = reinterpret_cast<int *>(s_tag + 1);
+    volatile int *s_abort = s_nv + 1;
+    volatile int *tabort = s_nv + 2;                                     // decided before the first tail barrier
+    volatile int *gabort = s_nv + 3;                                     // [kGroups]
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---------------------------------------------------------------- set-up
     if (warp == 0) {
         if (lane == 0) {
-            for (int i = 0; i < kSlots; ++i) {
-                tc::mbar_init(full1 + 8 * i, 1);
-                tc::mbar_init(empty1 + 8 * i, kGW);
+            for (int i = 0; i < NS; ++i) {
+                tc::mbar_init(full + 8 * i, 1);
+                tc::mbar_init(empty + 8 * i, kGW);
             }
-            for (int i = 0; i <= k; ++i)
-                tc::mbar_init(full2 + 8 * i, 1);                   // k down slots, then h of the tail
+            for (int i = 0; i < k; ++i)
+                tc::mbar_init(full2 + 8 * i, 1);
             *s_abort = 0;
             *tabort = 0;
-            *s_done = 0;
             for (int g = 0; g < kGroups; ++g)
                 gabort[g] = 0;
             if constexpr (ROUTE)
@@ -317,17 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // the arrival counter's epoch, read before this CTA arrives
+            // this launch's tag, from the count read before this CTA adds its one
             const unsigned long long v = ld_relaxed_u64(a.ctr);
-            *target = v / static_cast<unsigned>(G) * static_cast<unsigned>(G) + static_cast<unsigned>(G) +
-                  static_cast<unsigned>(a.shortfall);
+            *s_tag = static_cast<uint32_t>(v / static_cast<unsigned>(G)) + 1u;
+            red_relaxed_add(a.ctr);
         }
     } else if constexpr (ROUTE) {
         // top-k of the router logits by rank: thread e (of the 24 compute
         // warps) holds expert e's order-preserving key; its slot is the
         // number of experts ahead of it -- larger logit, or equal logit and
         // lower id -- which is the order the top-k routing defines.  The
-        // keys sit in the gate/up ring, idle until the routes are out.
+        // keys sit in the ring, idle until the routes are out.
         uint32_t *keys = reinterpret_cast<uint32_t *>(smem);
         const int e = tid - kWarpGU0 * 32, Ep = (a.E + 3) & ~3;
         float l = 0.f;
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
 
     const int nv = *s_nv;
     // this CTA's (route, neuron) pairs: a contiguous range of q = r * I + n,
-    // the whole space split evenly over the CTAs (h[q] is written here)
+    // the whole space split evenly over the CTAs (h[q] is formed here)
     const int q_lo = static_cast<int>(static_cast<int64_t>(nv) * I * c / G);
     const int P = static_cast<int>(static_cast<int64_t>(nv) * I * (c + 1) / G) - q_lo;
     const int S = (P + kPS - 1) / kPS;                                              // gate/up stages
@@ -367,21 +378,31 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
         if (lane == 0) {
             const int64_t rowb = d;
             tc::fence_proxy_async_smem();          // the ring held the routing's keys
-            bool go = true;
-            int s = 0;
-            for (; s < S; ++s) {
-                const int sl = s % kSlots;
-                const uint32_t ph = (s / kSlots) & 1u;
-                if (!tc::mbar_wait(empty1 + 8 * sl, ph ^ 1u, s_abort, kWaitNs)) {
-                    go = false;
-                    break;
+            int t = 0;
+            bool w2_sent = nrows == 0;
+            for (; t < S; ++t) {
+                if (!w2_sent && t == NS) {
+                    // the ring is full: this CTA's down rows of every route
+                    // go out next, into their own buffers, so they stream
+                    // behind the first gate/up stages and land long before
+                    // the tail needs them
+                    for (int r = 0; r < nv; ++r) {
+                        tc::mbar_arrive_expect_tx(full2 + 8 * r, static_cast<uint32_t>(nrows * I));
+                        tc::bulk_load(tc::smem_u32(w2s + r * S2), a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I,
+                                      nrows * I, full2 + 8 * r);
+                    }
+                    w2_sent = true;
                 }
-                const int q0 = q_lo + s * kPS, q1 = q_lo + min(s * kPS + kPS, P);
-                tc::mbar_arrive_expect_tx(full1 + 8 * sl, static_cast<uint32_t>(q1 - q0) * (2 * d));
-                uint8_t *st = slot1 + sl * S1;
-                const uint32_t bar = full1 + 8 * sl;
+                const int sl = t % NS;
+                const uint32_t ph = (t / NS) & 1u;
+                if (!tc::mbar_wait(empty + 8 * sl, ph ^ 1u, s_abort, kWaitNs))
+                    break;
+                uint8_t *st = ring + sl * S1;
+                const uint32_t bar = full + 8 * sl;
+                // gate/up stage t: runs of neurons of one route, gate rows then up rows
+                const int q0 = q_lo + t * kPS, q1 = q_lo + min(t * kPS + kPS, P);
+                tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(q1 - q0) * (2 * d));
                 for (int q = q0; q < q1;) {
-                    // a run of neurons of one route: gate rows, up rows
                     const int r = q / I, n = q - r * I, len = min(q1 - q, I - n), i = q - q0;
                     const int64_t grow = static_cast<int64_t>(r_e[r]) * 2 * I + n;
                     tc::bulk_load(tc::smem_u32(st + i * rowb), a.q13 + grow * rowb, len * rowb, bar);
@@ -389,43 +410,29 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                     q += len;
                 }
             }
-            // this CTA's down-projection rows of every routed expert go to L2
-            // once its last gate/up stage has landed: they stream while h is
-            // formed and exchanged, and do not slow the gate/up stream
-            if (go && S > 0)
-                go = tc::mbar_wait(full1 + 8 * ((S - 1) % kSlots), ((S - 1) / kSlots) & 1u, s_abort, kWaitNs);
-            if (go && nrows > 0)
-                for (int r = 0; r < nv; ++r)
-                    tc::bulk_prefetch_l2(a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I, nrows * I);
-            // once every gate/up stage is consumed the ring is idle: the down
-            // rows move from L2 into it while the grid's last CTAs finish
-            for (int t = max(0, s - kSlots); t < s && go; ++t)
-                go = tc::mbar_wait(empty1 + 8 * (t % kSlots), (t / kSlots) & 1u, s_abort, kWaitNs);
-            if (go && nrows > 0) {
-                tc::fence_proxy_async_smem();
+            if (!w2_sent && t == S) {
                 for (int r = 0; r < nv; ++r) {
                     tc::mbar_arrive_expect_tx(full2 + 8 * r, static_cast<uint32_t>(nrows * I));
-                    tc::bulk_load(tc::smem_u32(slot2 + r * S2), a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I,
+                    tc::bulk_load(tc::smem_u32(w2s + r * S2), a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I,
                                   nrows * I, full2 + 8 * r);
                 }
+                w2_sent = true;
             }
-            // every issued copy lands before the CTA may finish
+            // every issued copy lands before the CTA may finish (the stages
+            // before t - NS were consumed, so they have landed)
             volatile int never = 0;
-            for (int t = max(0, s - kSlots); t < s; ++t)
-                tc::mbar_wait(full1 + 8 * (t % kSlots), (t / kSlots) & 1u, &never, kWaitNs);
-            if (go && nrows > 0)
-                for (int r = 0; r < nv; ++r)
+            for (int u = max(0, t - NS); u < t; ++u)
+                tc::mbar_wait(full + 8 * (u % NS), (u / NS) & 1u, &never, kWaitNs);
+            if (w2_sent)
+                for (int r = 0; r < nv && nrows > 0; ++r)
                     tc::mbar_wait(full2 + 8 * r, 0, &never, kWaitNs);
         }
         return;
     }
-    if (warp == 1) {
-        // nothing to compute here: arrive at once
-        if (lane == 0 && P == 0)
-            red_release_add(a.ctr);
+    if (warp == 1)
         return;
-    }
     const int cw = warp - kWarpGU0;                      // compute warp 0..23
+    const uint32_t tag = *s_tag;
     if (warp < kWarpT0) {
         // ------------------------------------------------ gate/up warps
         const int grp = cw / kGW, om = cw % kGW;
@@ -463,14 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
         const int sclb = d / 32;
         tc::named_bar(kBarScales, kCW * 32);               // the E8M0 rows are staged
         for (int s = grp, m = 0; s < S; s += kGroups, ++m) {
-            const int sl = s % kSlots, buf = m & 1;
-            const uint32_t ph = (s / kSlots) & 1u;
-            const bool got = tc::mbar_wait(full1 + 8 * sl, ph, s_abort, kWaitNs);
+            const int sl = s % NS, buf = m & 1;
+            const uint32_t ph = (s / NS) & 1u;
+            const bool got = tc::mbar_wait(full + 8 * sl, ph, s_abort, kWaitNs);
             if (!got)
                 gabort[grp] = 1;
             const int npairs = min(kPS, P - s * kPS);
             if (got) {
-                const uint8_t *st = slot1 + sl * S1;
+                const uint8_t *st = ring + sl * S1;
                 float v[2 * kPS];
 #pragma unroll
                 for (int i = 0; i < 2 * kPS; ++i) {
@@ -480,16 +487,24 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                         lds_codes<KPL>(st + i * d + kbase, wq);
                         float acc = 0.f;
 #pragma unroll
-                        for (int t = 0; t < KPL / 4; ++t)
-                            acc = dot4(wq[t], xw[2 * t], xw[2 * t + 1], acc);
+                        for (int u = 0; u < KPL / 4; ++u)
+                            acc = dot4(wq[u], xw[2 * u], xw[2 * u + 1], acc);
                         // E8M0 of pair s*kPS + i%kPS, gate (i < kPS) or up row, this lane's block
                         v[i] = acc * e8m0_to_float(gsc[((s * kPS + i % kPS) * 2 + i / kPS) * sclb + (kbase >> 5)]);
                     }
                 }
-                const float tot = reduce8(v, lane) * xinv;
-                if ((lane & 3) == 0) {
-                    const int vi = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-                    gpart[((grp * 2 + buf) * kGW + om) * 2 * kPS + vi] = tot;
+                // 8 rows' sums at a time (gate rows, then up rows)
+#pragma unroll
+                for (int h8 = 0; h8 < 2 * kPS / 8; ++h8) {
+                    float v8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v8[i] = v[8 * h8 + i];
+                    const float tot = reduce8(v8, lane) * xinv;
+                    if ((lane & 3) == 0) {
+                        const int vi = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+                        gpart[((grp * 2 + buf) * kGW + om) * 2 * kPS + 8 * h8 + vi] = tot;
+                    }
                 }
             }
             tc::named_bar(kBarGroup0 + grp, kGW * 32);
@@ -498,9 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 break;
             }
             if (lane == 0)
-                tc::mbar_arrive(empty1 + 8 * sl);
+                tc::mbar_arrive(empty + 8 * sl);
             if (om == 0 && lane < npairs) {
-                // h of neuron `lane` of the stage: partials added in warp order
+                // h of neuron `lane` of the stage: partials added in warp order,
+                // published with this launch's tag
                 const float *gp = gpart + (grp * 2 + buf) * kGW * 2 * kPS;
                 float g = gp[lane], u = gp[kPS + lane];
 #pragma unroll
@@ -508,15 +524,14 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                     g += gp[w2 * 2 * kPS + lane];
                     u += gp[w2 * 2 * kPS + kPS + lane];
                 }
-                __stcg(a.h + q_lo + s * kPS + lane, silu_mul(g, u));
-                if (atom_add_acq_rel_cta(s_done, 1u) + 1u == static_cast<uint32_t>(P))
-                    // every h of this CTA is written (the CTA-scope acquire above
-                    // orders the other lanes' stores before this release): arrive
-                    red_release_add(a.ctr);
+                const unsigned long long word =
+                    static_cast<unsigned long long>(__float_as_uint(silu_mul(g, u))) |
+                    (static_cast<unsigned long long>(tag) << 32);
+                st_relaxed_u64(a.xh + q_lo + s * kPS + lane, word);
             }
         }
     } else {
-        // ------------------------------------------------ wait/copy warps
+        // ------------------------------------------------ scale-staging warps
         const int tw = warp - kWarpT0, tt = tid - kWarpT0 * 32;
         const int nb2 = I / 32;
         {
@@ -550,75 +565,68 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             s2s[(r * RM + rho) * nb2 + b] =
                 e8m0_to_float(__ldg(a.s2 + (static_cast<int64_t>(r_e[r]) * d + o0 + rho) * nb2 + b));
         }
-        if (tw == 0 && lane == 0) {
-            // every CTA has written its share of h (one lane polls, with a
-            // short back-off, so that the L2 slice holding the counter keeps
-            // serving the stream), then h comes to shared memory in one copy
-            const unsigned long long want = *target;
-            const uint64_t t0 = tc::globaltimer_ns();
-            bool ok = true;
-            for (uint32_t it = 0; ld_relaxed_u64(a.ctr) < want; ++it) {
-                __nanosleep(64);
-                if ((it & 15u) == 15u && (*s_abort || tc::globaltimer_ns() - t0 > kWaitNs)) {
-                    ok = false;
-                    break;
+    }
+
+    // ---------------------------------------------------------------- exchange
+    // every compute warp is done with its own gate/up work and staging: read
+    // all of h, warp cw taking words (j * kCW + cw) * 64 + 2 * lane (+1),
+    // until each carries this launch's tag
+    tc::named_bar(kBarTail, kCW * 32);
+    const bool work = !*tabort && nv > 0 && nrows > 0;
+    if (work) {
+        const int NP = nv * I;                                      // words; NP % 64 == 0 (I % 64 == 0)
+        const int nj = (NP / 64 + kCW - 1) / kCW;                   // 16-byte loads per lane
+        const uint32_t want = a.stall ? tag ^ 0x80000000u : tag;
+        uint32_t pend = 0;
+        for (int j = 0; j < nj; ++j)
+            if ((j * kCW + cw) * 64 < NP)
+                pend |= 1u << j;
+        const uint64_t t0 = tc::globaltimer_ns();
+        for (uint32_t it = 0; pend; ++it) {
+            for (int j0 = 0; j0 < nj; j0 += 4) {
+                unsigned long long v0[4], v1[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    v0[u] = v1[u] = 0;
+                    if ((pend >> (j0 + u)) & 1u)
+                        ld_relaxed_u64x2(a.xh + ((j0 + u) * kCW + cw) * 64 + 2 * lane, v0[u], v1[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = j0 + u;
+                    if (((pend >> j) & 1u) && static_cast<uint32_t>(v0[u] >> 32) == want &&
+                        static_cast<uint32_t>(v1[u] >> 32) == want) {
+                        *reinterpret_cast<float2 *>(hbuf + (j * kCW + cw) * 64 + 2 * lane) =
+                            make_float2(__uint_as_float(static_cast<uint32_t>(v0[u])),
+                                        __uint_as_float(static_cast<uint32_t>(v1[u])));
+                        pend &= ~(1u << j);
+                    }
                 }
             }
-            if (ok) {
-                asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-                if (nv > 0 && nrows > 0) {
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive_expect_tx(hbar, static_cast<uint32_t>(nv * I * 4));
-                    tc::bulk_load(tc::smem_u32(hbuf), a.h, nv * I * 4, hbar);
-                }
-            } else {
+            if (!pend)
+                break;
+            __nanosleep(64);
+            if ((it & 15u) == 15u && (*s_abort || tc::globaltimer_ns() - t0 > kWaitNs)) {
                 *s_abort = 1;
                 *tabort = 1;
                 set_err(a.dev_status, MOE_ERR_TIMEOUT);
+                break;
             }
         }
     }
+    tc::named_bar(kBarTail, kCW * 32);
+    if (cw == 0 && lane == 0 && !*tabort)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---------------------------------------------------------------- tail
-    tc::named_bar(kBarTail, kCW * 32);
-    const bool work = !*tabort && nv > 0 && nrows > 0;
-    const bool got = work && tc::mbar_wait(hbar, 0, s_abort, kWaitNs);
-    if (work && !got)
-        set_err(a.dev_status, MOE_ERR_TIMEOUT);
-    // h of every route once, by one warp per route: fp16 after an exact
-    // power-of-two rescale that puts the route's largest magnitude in
-    // [2^14, 2^15) (relative rounding at most 2^-12 of each element)
-    __half2 *h16 = reinterpret_cast<__half2 *>(slot1 + pl.o_hh());        // [nv][I/2]
-    float *hinv = dpart + pl.k * RM;                                     // [nv]
-    for (int r = cw; got && r < nv; r += kCW) {
-        float hv[HPL];
-        const float4 *hp = reinterpret_cast<const float4 *>(hbuf + r * I + HPL * lane);
-#pragma unroll
-        for (int i = 0; i < HPL / 4; ++i) {
-            const float4 f = hp[i];
-            hv[4 * i] = f.x; hv[4 * i + 1] = f.y; hv[4 * i + 2] = f.z; hv[4 * i + 3] = f.w;
-        }
-        float m = 0.f;
-#pragma unroll
-        for (int i = 0; i < HPL; ++i)
-            m = fmaxf(m, fabsf(hv[i]));
-        const int pw = f16_shift(warp_max(m));
-        const float sc = ldexpf(1.0f, pw);
-        if (lane == 0)
-            hinv[r] = ldexpf(1.0f, -pw);
-#pragma unroll
-        for (int i = 0; i < HPL / 2; ++i)
-            h16[(r * I + HPL * lane) / 2 + i] = __floats2half2_rn(hv[2 * i] * sc, hv[2 * i + 1] * sc);
-    }
-    tc::named_bar(kBarTail, kCW * 32);
-    if (got) {
+    if (work && !*tabort) {
         // the (route, row) units of this CTA, a contiguous block per warp
         const int U = nv * nrows, nb2 = I / 32;
         const int u0 = U * cw / kCW, u1 = U * (cw + 1) / kCW;
         int cur = -1;
         uint32_t hh[HPL / 2];
         float inv = 1.f;
+        const uint8_t *w2r = w2s;
         for (int u = u0; u < u1;) {
             const int r = u / nrows, rho = u - r * nrows;
             if (r != cur) {
@@ -627,19 +635,35 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                     set_err(a.dev_status, MOE_ERR_TIMEOUT);
                     break;
                 }
-                const uint4 *ph = reinterpret_cast<const uint4 *>(h16 + (r * I + HPL * lane) / 2);
+                w2r = w2s + r * S2;
+                // this lane's HPL values of h_r as fp16 after an exact
+                // power-of-two rescale of the lane's largest magnitude into
+                // [2^14, 2^15) (relative rounding at most 2^-12 each)
+                float hv[HPL];
+                const float4 *hp = reinterpret_cast<const float4 *>(hbuf + r * I + HPL * lane);
 #pragma unroll
-                for (int i = 0; i < HPL / 8; ++i) {
-                    const uint4 v = ph[i];
-                    hh[4 * i] = v.x; hh[4 * i + 1] = v.y; hh[4 * i + 2] = v.z; hh[4 * i + 3] = v.w;
+                for (int i = 0; i < HPL / 4; ++i) {
+                    const float4 f = hp[i];
+                    hv[4 * i] = f.x; hv[4 * i + 1] = f.y; hv[4 * i + 2] = f.z; hv[4 * i + 3] = f.w;
                 }
-                inv = hinv[r];
+                float mx = 0.f;
+#pragma unroll
+                for (int i = 0; i < HPL; ++i)
+                    mx = fmaxf(mx, fabsf(hv[i]));
+                const int pw = f16_shift(mx);
+                const float sc = ldexpf(1.0f, pw);
+                inv = ldexpf(1.0f, -pw);
+#pragma unroll
+                for (int i = 0; i < HPL / 2; ++i) {
+                    const __half2 h2 = __floats2half2_rn(hv[2 * i] * sc, hv[2 * i + 1] * sc);
+                    hh[i] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
             }
             // two rows of the same route at once when the block has them
             const bool two = u + 1 < u1 && rho + 1 < nrows;
             const int rho1 = two ? rho + 1 : rho;
-            const uint8_t *w0 = slot2 + r * S2 + rho * I + HPL * lane;
-            const uint8_t *w1 = slot2 + r * S2 + rho1 * I + HPL * lane;
+            const uint8_t *w0 = w2r + rho * I + HPL * lane;
+            const uint8_t *w1 = w2r + rho1 * I + HPL * lane;
             const float *sr0 = s2s + (r * RM + rho) * nb2 + ((HPL * lane) >> 5);
             const float *sr1 = s2s + (r * RM + rho1) * nb2 + ((HPL * lane) >> 5);
             float acc0 = 0.f, acc1 = 0.f;
@@ -649,29 +673,31 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 const uint2 q1 = *reinterpret_cast<const uint2 *>(w1 + 8 * c8);
                 const int sb = (((HPL * lane) & 31) + 8 * c8) >> 5;
                 float p0 = 0.f, p1 = 0.f;
-                uint32_t a[4], b[4];
-                cvt_e4m3x4(q0.x, a[0], a[1]);
-                cvt_e4m3x4(q0.y, a[2], a[3]);
-                cvt_e4m3x4(q1.x, b[0], b[1]);
-                cvt_e4m3x4(q1.y, b[2], b[3]);
+                uint32_t wa[4], wb[4];
+                cvt_e4m3x4(q0.x, wa[0], wa[1]);
+                cvt_e4m3x4(q0.y, wa[2], wa[3]);
+                cvt_e4m3x4(q1.x, wb[0], wb[1]);
+                cvt_e4m3x4(q1.y, wb[2], wb[3]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    p0 = fma2(a[i], hh[4 * c8 + i], p0);
-                    p1 = fma2(b[i], hh[4 * c8 + i], p1);
+                    p0 = fma2(wa[i], hh[4 * c8 + i], p0);
+                    p1 = fma2(wb[i], hh[4 * c8 + i], p1);
                 }
                 acc0 = fmaf(p0, sr0[sb], acc0);
                 acc1 = fmaf(p1, sr1[sb], acc1);
             }
+            acc0 *= inv;
+            acc1 *= inv;
             // both sums at once: lanes 0..15 end with row rho's, 16..31 with rho1's
             const bool up = lane & 16;
-            float t = (up ? acc1 : acc0) + __shfl_xor_sync(0xffffffffu, up ? acc0 : acc1, 16);
+            float tsum = (up ? acc1 : acc0) + __shfl_xor_sync(0xffffffffu, up ? acc0 : acc1, 16);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1)
-                t += __shfl_xor_sync(0xffffffffu, t, o);
+                tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
             if (lane == 0)
-                dpart[r * RM + rho] = t * inv;
+                dpart[r * RM + rho] = tsum;
             if (two && lane == 16)
-                dpart[r * RM + rho1] = t * inv;
+                dpart[r * RM + rho1] = tsum;
             u += two ? 2 : 1;
         }
     }
@@ -712,15 +738,12 @@ inline bool shape_ok(int d, int I)
     return (d == 512 && I == 256) || (d == 1024 && I == 512) || (d == 2048 && (I == 512 || I == 768 || I == 1024));
 }
 
-
-
 }  // namespace dp
 
-// Arrivals the next launches' counter wait expects beyond the grid size: 0
-// in normal use; moe_debug_arrival_shortfall sets it so that a test can make
-// the wait run out (it gives up after its time limit and reports
-// MOE_ERR_TIMEOUT) without faulting or hanging the GPU.
-static std::atomic<int> g_shortfall{0};
+// When set, the next launches' exchange waits for a tag that no CTA writes:
+// the wait gives up after its time limit and reports MOE_ERR_TIMEOUT, which
+// lets a test exercise the failure path without faulting or hanging the GPU.
+static std::atomic<int> g_stall{0};
 
 bool decode_pipe_shape_fits(int k, int d, int I, int G)
 {
@@ -733,11 +756,6 @@ bool decode_pipe_eligible(int M, int k, int d, int I, int E)
 }
 
 bool decode_pipe_route_eligible(int E, int k) { return E >= k && E <= dp::kCW * 32; }
-
-size_t decode_pipe_workspace(int k, int I)
-{
-    return kWsReserved + ws_round(static_cast<size_t>(k) * I * sizeof(float));
-}
 
 moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, const int32_t *ids, const float *wts,
                                 const float *logits, int32_t *ids_out, float *wts_out, int k, const uint8_t *q13,
@@ -761,7 +779,7 @@ moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, con
     a.q2 = q2;
     a.s2 = s2;
     a.ctr = static_cast<unsigned long long *>(ws);
-    a.h = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWsReserved);
+    a.xh = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + kWsCounterBytes);
     a.y = y;
     a.dev_status = dev_status;
     a.y_f32 = y_f32 ? 1 : 0;
@@ -769,7 +787,7 @@ moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, con
     a.d = d;
     a.I = I;
     a.E = E;
-    a.shortfall = g_shortfall.load(std::memory_order_relaxed);
+    a.stall = g_stall.load(std::memory_order_relaxed);
     const int smem = pl.bytes();
     switch (d * 10000 + I) {
     case 512 * 10000 + 256: return launch_route<4, 8>(a, G, smem, s);
@@ -783,10 +801,10 @@ moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, con
 
 }  // namespace moe
 
-MOE_API moe_status_t moe_debug_arrival_shortfall(int32_t n)
+MOE_API moe_status_t moe_debug_exchange_stall(int32_t on)
 {
-    if (n < 0 || n > 1024)
+    if (on != 0 && on != 1)
         return MOE_ERR_INVALID_ARG;
-    moe::g_shortfall.store(n, std::memory_order_relaxed);
+    moe::g_stall.store(on, std::memory_order_relaxed);
     return MOE_OK;
 }
