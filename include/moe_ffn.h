@@ -174,7 +174,7 @@ moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
  * Kernels by case: MOE_W_MXFP8 (standard layout) with M == 1,
  * (d, I) in {(512, 256), (1024, 512), (2048, 512), (2048, 768),
- * (2048, 1024)}, k small enough for the shared-memory plan (k <= 10 at
+ * (2048, 1024)}, k small enough for the shared-memory plan (k <= 12 at
  * d = 2048, I = 768 on 152 SMs) -> one kernel, one CTA per SM (each CTA an
  * even share of the (route, neuron) pairs: gate/up rows streamed by
  * cp.async.bulk, h = SiLU(g)*u published in ws with the call's tag; each
