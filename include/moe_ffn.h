@@ -174,7 +174,7 @@ moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
  * Kernels by case: MOE_W_MXFP8 (standard layout) with M == 1,
  * (d, I) in {(512, 256), (1024, 512), (2048, 512), (2048, 768),
- * (2048, 1024)}, k small enough for the shared-memory plan (k <= 12 at
+ * (2048, 1024)}, k small enough for the shared-memory plan (k <= 10 at
  * d = 2048, I = 768 on 152 SMs) -> one kernel, one CTA per SM (each CTA an
  * even share of the (route, neuron) pairs: gate/up rows streamed by
  * cp.async.bulk, h = SiLU(g)*u published in ws with the call's tag; each
@@ -309,7 +309,7 @@ moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d,
  *   MOE_W_MXFP8: MOE_PATH_DECODE for M <= 1 where the single-kernel decode
  *                is built for (k, d, I) on GB300's 152 SMs (d = 512,
  *                I = 256; d = 1024, I = 512; d = 2048, I = 512, 768 or
- *                1024; k small enough for its shared-memory plan, k <= 12
+ *                1024; k small enough for its shared-memory plan, k <= 10
  *                at d = 2048, I = 768), else MOE_PATH_GROUPED (decode 15.4
  *                against grouped 27.8 us at M = 1; grouped 41.5 against
  *                179 us at M = 4 and faster at every larger M; at d = 7168,

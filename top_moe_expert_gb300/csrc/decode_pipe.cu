@@ -12,12 +12,11 @@
 // At one token the layer is an HBM stream of the k routed experts' weights
 // (38.9 MB at d = 2048, I = 768, k = 8).  One CTA per SM, with warp roles:
 //   * warp 0, producer: routes the token (or reads the given routing),
-//     publishes the valid routes in slot order, then streams this CTA's gate
-//     and up rows, 4 neurons per stage, through a ring of up to 11 slots
-//     (7 at d = 2048, I = 768: 112 KB in flight per SM); once the ring is
-//     first full it sends this CTA's rows of every routed expert's down
-//     projection into buffers of their own, one bulk copy per route, so
-//     they stream behind the first gate/up stages.
+//     publishes the valid routes in slot order, then streams through one
+//     ring of up to 11 slots (176 KB in flight per SM at d = 2048): first
+//     this CTA's gate and up rows, 4 neurons per stage, then this CTA's rows
+//     of every routed expert's down projection, one or more routes per
+//     stage, each issued as soon as its slot is free.
 //   * warp 1: reads the launch's epoch from the call counter and advances it.
 //   * warps 2..17, gate/up: 4 groups of 4 warps.  Group g takes stages g,
 //     g+4, g+8, ...; its warps split K, each holding its slice of x in
@@ -28,12 +27,11 @@
 //   * warps 18..25: load the E8M0 rows of this CTA's gate/up neurons (before
 //     the first stage is consumed) and of its down-projection rows.
 // Exchange: the 24 compute warps read every route's h words until each
-// carries this launch's tag, into shared memory (the drained ring).  No
-// flag, fence or barrier across CTAs: a word is written once per launch and
-// read atomically, so a value is taken only when its own tag says it
-// belongs to this launch.
+// carries this launch's tag, into shared memory.  No flag, fence or barrier
+// across CTAs: a word is written once per launch and read atomically, so a
+// value is taken only when its own tag says it belongs to this launch.
 // Tail: each warp forms (route, row) units of this CTA's output rows of the
-// down projection, two rows at a time, from the down-row buffers and
+// down projection, two rows at a time, from the down rows in the ring and
 // h converted per lane to fp16 after an exact power-of-two rescale; y is the
 // routing-weighted sum over routes in slot order.  The (route, neuron) space
 // is split evenly over the CTAs and each CTA owns d / G output rows, so no
@@ -62,7 +60,7 @@ constexpr int kMaxK = 32;
 constexpr int kGW = 4;                                // warps of a gate/up group (they split K)
 constexpr int kGroups = 4;                            // gate/up groups
 constexpr int kPS = 4;                                // neurons per gate/up stage (4 or 8)
-constexpr int kMaxSlots = 11;                         // gate/up ring slots, at most
+constexpr int kMaxSlots = 11;                         // ring slots, at most
 constexpr int kMinSlots = 4;
 constexpr int kTW = 8;                                // warps of the scale-staging role
 constexpr int kWarpGU0 = 2;
@@ -77,7 +75,6 @@ constexpr int kBarTail = 2;                           //   the compute warps
 constexpr int kBarGroup0 = 3;                         //   gate/up group g: kBarGroup0 + g
 constexpr int kBarRank = kBarGroup0 + kGroups;        //   the compute warps ranking the logits
 constexpr int kBarScales = kBarRank + 1;              //   gate/up E8M0 rows staged (staging warps arrive)
-
 constexpr int kSmemMax = 227 * 1024;
 
 struct Args {
@@ -97,40 +94,39 @@ struct Args {
     int stall;                   // readers expect a tag nobody writes (failure-detection test)
 };
 
-// Shared-memory plan (bytes), identical on host and device: the gate/up
-// ring (h of every route is staged there once the ring has drained), this
-// CTA's down rows of every route, the E8M0 scales, small buffers, barriers.
+// Shared-memory plan (bytes), identical on host and device.
 struct Plan {
     int d, I, k, G;
     __host__ __device__ int rows_max() const { return (d + G - 1) / G; }
     __host__ __device__ int s1() const { return kPS * 2 * d; }                   // slot: gate rows | up rows
     __host__ __device__ int pmax() const { return (k * I + G - 1) / G; }        // pairs of a CTA, at most
     __host__ __device__ int s2() const { return rows_max() * I; }               // one route's down rows
+    __host__ __device__ int rps() const { return s1() / s2(); }                 // routes per down stage
+    __host__ __device__ int w2_stages() const { return (k + rps() - 1) / rps(); }
     __host__ __device__ static int up16(int v) { return (v + 15) & ~15; }
-    __host__ __device__ int n_bars() const { return 2 * kMaxSlots + kMaxK; }   // full, empty, down rows
     // everything but the ring
     __host__ __device__ int fixed() const
     {
-        return k * s2() + k * rows_max() * (I / 32) * 4 + up16(pmax() * 2 * (d / 32)) +
-               kGroups * 2 * kGW * 2 * kPS * 4 + up16(k * rows_max() * 4) + n_bars() * 8 + 3 * kMaxK * 4 + 32;
+        return up16(k * I * 4) + k * rows_max() * (I / 32) * 4 + up16(pmax() * 2 * (d / 32)) +
+               kGroups * 2 * kGW * 2 * kPS * 4 + up16(k * rows_max() * 4) + 2 * kMaxSlots * 8 + 3 * kMaxK * 4 + 32;
     }
     __host__ __device__ int slots() const
     {
         const int n = (kSmemMax - fixed()) / s1();
         return n > kMaxSlots ? kMaxSlots : n;
     }
-    __host__ __device__ int o_w2() const { return slots() * s1(); }            // [k][RM][I] down rows
-    __host__ __device__ int o_s2s() const { return o_w2() + k * s2(); }
+    __host__ __device__ int o_h() const { return slots() * s1(); }             // h [k][I] f32
+    __host__ __device__ int o_s2s() const { return o_h() + up16(k * I * 4); }
     __host__ __device__ int o_gsc() const { return o_s2s() + k * rows_max() * (I / 32) * 4; }
     __host__ __device__ int o_gpart() const { return o_gsc() + up16(pmax() * 2 * (d / 32)); }
     __host__ __device__ int o_dpart() const { return o_gpart() + kGroups * 2 * kGW * 2 * kPS * 4; }
     __host__ __device__ int o_bars() const { return o_dpart() + up16(k * rows_max() * 4); }
-    __host__ __device__ int o_route() const { return o_bars() + n_bars() * 8; }
-    // route data: r_e[kMaxK] | r_w[kMaxK] | r_l[kMaxK] | tag, nv, abort, tabort, gabort[kGroups]
+    __host__ __device__ int o_route() const { return o_bars() + 2 * kMaxSlots * 8; }
+    // route data: r_e[kMaxK] | r_w[kMaxK] | r_l[kMaxK] | tag, nv, abort, tabort (32 bytes kept)
     __host__ __device__ int bytes() const { return o_route() + 3 * kMaxK * 4 + 32; }
     __host__ __device__ bool fits() const
     {
-        return s2() > 0 && slots() >= kMinSlots && bytes() <= kSmemMax && k * I * 4 <= slots() * s1() &&
+        return s2() > 0 && s2() <= s1() && slots() >= kMinSlots && w2_stages() <= slots() && bytes() <= kSmemMax &&
                static_cast<size_t>(k) * I * 8 <= kWsTagBytes && k * I <= kCW * 32 * kMaxPerLane;
     }
 };
@@ -271,16 +267,15 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     const int d = a.d, I = a.I, k = a.k, G = gridDim.x, c = blockIdx.x;
     const Plan pl{d, I, k, G};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int RM = pl.rows_max(), S1 = pl.s1(), S2 = pl.s2(), NS = pl.slots();
+    const int RM = pl.rows_max(), S1 = pl.s1(), S2 = pl.s2(), NS = pl.slots(), RPS = pl.rps();
     uint8_t *ring = smem;
-    float *hbuf = reinterpret_cast<float *>(smem);                       // [nv][I] h, in the drained ring
-    uint8_t *w2s = smem + pl.o_w2();                                     // [k][RM][I] down rows
+    float *hbuf = reinterpret_cast<float *>(smem + pl.o_h());           // [nv][I] h of every route
     float *s2s = reinterpret_cast<float *>(smem + pl.o_s2s());           // [k][RM][I/32] down scales
     uint8_t *gsc = smem + pl.o_gsc();                                    // [P][2][d/32] gate/up E8M0 rows
     float *gpart = reinterpret_cast<float *>(smem + pl.o_gpart());       // [grp][2][kGW][2 kPS]
     float *dpart = reinterpret_cast<float *>(smem + pl.o_dpart());       // [k][RM]
     const uint32_t full = tc::smem_u32(smem + pl.o_bars());
-    const uint32_t empty = full + 8 * kMaxSlots, full2 = empty + 8 * kMaxSlots;
+    const uint32_t empty = full + 8 * kMaxSlots;
     int *r_e = reinterpret_cast<int *>(smem + pl.o_route());
     float *r_w = reinterpret_cast<float *>(r_e + kMaxK);
     float *r_l = r_w + kMaxK;                                            // logits of the chosen routes
@@ -288,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     int *s_nv = reinterpret_cast<int *>(s_tag + 1);
     volatile int *s_abort = s_nv + 1;
     volatile int *tabort = s_nv + 2;                                     // decided before the first tail barrier
-    volatile int *gabort = s_nv + 3;                                     // [kGroups]
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -299,12 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 tc::mbar_init(full + 8 * i, 1);
                 tc::mbar_init(empty + 8 * i, kGW);
             }
-            for (int i = 0; i < k; ++i)
-                tc::mbar_init(full2 + 8 * i, 1);
             *s_abort = 0;
             *tabort = 0;
-            for (int g = 0; g < kGroups; ++g)
-                gabort[g] = 0;
             if constexpr (ROUTE)
                 *s_nv = k;                                         // E >= k: every chosen route is valid
             tc::fence_mbar_init();
@@ -372,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     const int S = (P + kPS - 1) / kPS;                                              // gate/up stages
     const int o0 = static_cast<int>(static_cast<int64_t>(d) * c / G);
     const int nrows = static_cast<int>(static_cast<int64_t>(d) * (c + 1) / G) - o0;
+    const int SW = nrows > 0 ? (nv + RPS - 1) / RPS : 0;                           // down stages
 
     if (warp == 0) {
         // ------------------------------------------------ producer
@@ -379,53 +370,39 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             const int64_t rowb = d;
             tc::fence_proxy_async_smem();          // the ring held the routing's keys
             int t = 0;
-            bool w2_sent = nrows == 0;
-            for (; t < S; ++t) {
-                if (!w2_sent && t == NS) {
-                    // the ring is full: this CTA's down rows of every route
-                    // go out next, into their own buffers, so they stream
-                    // behind the first gate/up stages and land long before
-                    // the tail needs them
-                    for (int r = 0; r < nv; ++r) {
-                        tc::mbar_arrive_expect_tx(full2 + 8 * r, static_cast<uint32_t>(nrows * I));
-                        tc::bulk_load(tc::smem_u32(w2s + r * S2), a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I,
-                                      nrows * I, full2 + 8 * r);
-                    }
-                    w2_sent = true;
-                }
+            for (; t < S + SW; ++t) {
                 const int sl = t % NS;
                 const uint32_t ph = (t / NS) & 1u;
                 if (!tc::mbar_wait(empty + 8 * sl, ph ^ 1u, s_abort, kWaitNs))
                     break;
                 uint8_t *st = ring + sl * S1;
                 const uint32_t bar = full + 8 * sl;
-                // gate/up stage t: runs of neurons of one route, gate rows then up rows
-                const int q0 = q_lo + t * kPS, q1 = q_lo + min(t * kPS + kPS, P);
-                tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(q1 - q0) * (2 * d));
-                for (int q = q0; q < q1;) {
-                    const int r = q / I, n = q - r * I, len = min(q1 - q, I - n), i = q - q0;
-                    const int64_t grow = static_cast<int64_t>(r_e[r]) * 2 * I + n;
-                    tc::bulk_load(tc::smem_u32(st + i * rowb), a.q13 + grow * rowb, len * rowb, bar);
-                    tc::bulk_load(tc::smem_u32(st + (kPS + i) * rowb), a.q13 + (grow + I) * rowb, len * rowb, bar);
-                    q += len;
+                if (t < S) {
+                    // gate/up stage t: runs of neurons of one route, gate rows then up rows
+                    const int q0 = q_lo + t * kPS, q1 = q_lo + min(t * kPS + kPS, P);
+                    tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(q1 - q0) * (2 * d));
+                    for (int q = q0; q < q1;) {
+                        const int r = q / I, n = q - r * I, len = min(q1 - q, I - n), i = q - q0;
+                        const int64_t grow = static_cast<int64_t>(r_e[r]) * 2 * I + n;
+                        tc::bulk_load(tc::smem_u32(st + i * rowb), a.q13 + grow * rowb, len * rowb, bar);
+                        tc::bulk_load(tc::smem_u32(st + (kPS + i) * rowb), a.q13 + (grow + I) * rowb, len * rowb,
+                                      bar);
+                        q += len;
+                    }
+                } else {
+                    // down stage: this CTA's rows of routes r0 .. r1-1, S2 bytes apart
+                    const int r0 = (t - S) * RPS, r1 = min(nv, r0 + RPS);
+                    tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>((r1 - r0) * nrows * I));
+                    for (int r = r0; r < r1; ++r)
+                        tc::bulk_load(tc::smem_u32(st + (r - r0) * S2),
+                                      a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I, nrows * I, bar);
                 }
-            }
-            if (!w2_sent && t == S) {
-                for (int r = 0; r < nv; ++r) {
-                    tc::mbar_arrive_expect_tx(full2 + 8 * r, static_cast<uint32_t>(nrows * I));
-                    tc::bulk_load(tc::smem_u32(w2s + r * S2), a.q2 + (static_cast<int64_t>(r_e[r]) * d + o0) * I,
-                                  nrows * I, full2 + 8 * r);
-                }
-                w2_sent = true;
             }
             // every issued copy lands before the CTA may finish (the stages
             // before t - NS were consumed, so they have landed)
             volatile int never = 0;
             for (int u = max(0, t - NS); u < t; ++u)
                 tc::mbar_wait(full + 8 * (u % NS), (u / NS) & 1u, &never, kWaitNs);
-            if (w2_sent)
-                for (int r = 0; r < nv && nrows > 0; ++r)
-                    tc::mbar_wait(full2 + 8 * r, 0, &never, kWaitNs);
         }
         return;
     }
@@ -473,8 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             const int sl = s % NS, buf = m & 1;
             const uint32_t ph = (s / NS) & 1u;
             const bool got = tc::mbar_wait(full + 8 * sl, ph, s_abort, kWaitNs);
-            if (!got)
-                gabort[grp] = 1;
             const int npairs = min(kPS, P - s * kPS);
             if (got) {
                 const uint8_t *st = ring + sl * S1;
@@ -507,9 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                     }
                 }
             }
-            tc::named_bar(kBarGroup0 + grp, kGW * 32);
-            if (gabort[grp]) {
-                *tabort = 1;
+            if (tc::named_bar_or(kBarGroup0 + grp, kGW * 32, !got)) {
+                *tabort = 1;                               // the stage never landed: the group stops together
                 break;
             }
             if (lane == 0)
@@ -626,16 +600,17 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
         int cur = -1;
         uint32_t hh[HPL / 2];
         float inv = 1.f;
-        const uint8_t *w2r = w2s;
+        const uint8_t *w2r = ring;
         for (int u = u0; u < u1;) {
             const int r = u / nrows, rho = u - r * nrows;
             if (r != cur) {
                 cur = r;
-                if (!tc::mbar_wait(full2 + 8 * r, 0, s_abort, kWaitNs)) {
+                const int t = S + r / RPS;                         // the down stage holding route r
+                if (!tc::mbar_wait(full + 8 * (t % NS), (t / NS) & 1u, s_abort, kWaitNs)) {
                     set_err(a.dev_status, MOE_ERR_TIMEOUT);
                     break;
                 }
-                w2r = w2s + r * S2;
+                w2r = ring + (t % NS) * S1 + (r % RPS) * S2;
                 // this lane's HPL values of h_r as fp16 after an exact
                 // power-of-two rescale of the lane's largest magnitude into
                 // [2^14, 2^15) (relative rounding at most 2^-12 each)

@@ -276,5 +276,17 @@ __device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count)
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// A named barrier that also ORs a predicate over every participating
+// thread: all of them leave with the same answer, so a decision taken from
+// it keeps their later barrier sequences identical.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.or.pred q, %2, %3, p;\n"
+                 " selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r) : "r"(pred ? 1u : 0u), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+
 }  // namespace tc
 }  // namespace moe
