@@ -876,6 +876,113 @@ def run_reference(args, rank, world):
             "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------ Table 8 sweep
+
+TABLE8 = {
+    # model: (d, I, N sweep, G sweep) -- gate/up (2I, d) and down (d, I) of the
+    # grouped-GEMM benchmark shapes ("Hardware-Native Joint Sparse-
+    # Quantization ...", App. D.2, Table 8)
+    "qwen": (2048, 768, (16, 32, 64, 128, 256, 512, 1024), (8, 16, 32, 64, 128)),
+    "kimi": (7168, 2048, (32, 64, 128, 256, 512, 1024), (24, 48, 96, 192, 384)),
+}
+
+
+def run_table8(model: str, device, reps: int = 20, out=sys.stdout):
+    """The grouped layer over the benchmark's (N, G) grid with per-expert token
+    counts {N, 3N/4, N/2, N/4} repeated over the G experts (one route per
+    token, weight 1), on the aligned and on the fixed-capacity layout.  One
+    step is the alignment and the layer call (activation quantization, both
+    GEMMs, combine), timed back to back in a CUDA graph over copies of the
+    weights that together exceed the L2.  One JSON line per (G, N, layout):
+    the page's effective TFLOP/s (2 * (2I*d + d*I) * sum N_g / t) and the
+    fraction of the measured HBM bandwidth the weight and activation bytes
+    reach."""
+    import top_moe_expert_gb300 as moe
+    from top_moe_expert_gb300 import inputs
+    d, I, Ns, Gs = TABLE8[model]
+    peak_gbs, _ = measured_peak()
+    for G in Gs:
+        wl = inputs.Workload(f"table8_{model}_g{G}", M=1, d=d, I=I, E=G, k=1, seed=30)
+        lw = G * 3 * I * d * 33 // 32
+        n_copies = max(1, min(8, -(-4 * 130 * 2 ** 20 // lw)))
+        layers = []
+        for c in range(n_copies):
+            q13 = torch.empty((G, 2 * I, d), dtype=torch.uint8, device=device)
+            s13 = torch.empty((G, 2 * I, d // 32), dtype=torch.uint8, device=device)
+            q2 = torch.empty((G, d, I), dtype=torch.uint8, device=device)
+            s2 = torch.empty((G, d, I // 32), dtype=torch.uint8, device=device)
+            for e in range(G):
+                if c == 0:
+                    moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w13", e, device), q13[e], s13[e])
+                    moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), q2[e], s2[e])
+            if c > 0:
+                q13.copy_(layers[0][0].q); s13.copy_(layers[0][0].scale)
+                q2.copy_(layers[0][1].q); s2.copy_(layers[0][1].scale)
+            w13, w2 = moe.Weights(moe.MOE_W_MXFP8, q13, s13), moe.Weights(moe.MOE_W_MXFP8, q2, s2)
+            layers.append((w13, w2, moe.moe_grouped_prepare(w13, w2)))
+        for N in Ns:
+            ids_np = inputs.imbalanced_routing(N, G)
+            M = ids_np.shape[0]
+            ids = torch.from_numpy(ids_np).to(device)
+            w = torch.ones((M, 1), dtype=torch.float32, device=device)
+            x = inputs.activations(inputs.Workload("t8x", M=M, d=d, I=I, E=G, k=1, seed=31)).to(device)
+            y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
+            b = moe.moe_ffn_select_path(M, 1, G, d, I)[1] or 16
+            C = -(-N // b) * b
+            cr, cb = moe.moe_align_capacity(M, 1, G, b)
+            for layout in ("aligned", "fixed"):
+                if layout == "aligned":
+                    al = (torch.empty(cr, dtype=torch.int32, device=device),
+                          torch.empty(cb, dtype=torch.int32, device=device),
+                          torch.empty(1, dtype=torch.int32, device=device))
+                    na = moe.moe_align_workspace_size(M, 1, G, b)
+                    wsa = torch.empty(max(na, 256), dtype=torch.uint8, device=device) if na else None
+                    rows = cr
+                else:
+                    al = moe.moe_align_fixed_capacity(ids, G, b, C)
+                    wsa, rows = None, G * C
+                ws = torch.empty(moe.moe_ffn_grouped_workspace_size(M, 1, d, I, b, rows), dtype=torch.uint8,
+                                 device=device)
+                def step(i):
+                    # every launch on the current stream (the capture stream
+                    # while the graph is being recorded)
+                    w13, w2, sfa = layers[i % n_copies]
+                    if layout == "aligned":
+                        moe.moe_align_block_size(ids, G, b, out=al, ws=wsa)
+                    else:
+                        moe.moe_align_fixed_capacity(ids, G, b, C, out=al)
+                    moe.moe_ffn_grouped(x, ids, w, w13, w2, sfa[0], sfa[1], al, b, y=y, ws=ws)
+
+                for i in range(3):
+                    step(i)
+                torch.cuda.synchronize(device)
+                n_steps = n_copies * max(1, reps // n_copies)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(n_steps):
+                        step(i)
+                g.replay()
+                torch.cuda.synchronize(device)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(3):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize(device)          # the graph is done before its buffers are freed
+                us = e0.elapsed_time(e1) * 1e3 / (3 * n_steps)
+                flop = 2.0 * (2 * I * d + d * I) * M
+                nbytes = lw + M * d * 2 + M * d * 2
+                print(json.dumps({"table8": model, "G": G, "N": N, "tokens": M, "layout": layout, "b": b,
+                                  "us_per_step": round(us, 2), "eff_tflops": round(flop / (us * 1e-6) / 1e12, 2),
+                                  "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peak_gbs, 4),
+                                  "weight_copies": n_copies}), file=out, flush=True)
+                del g, ws, al
+                torch.cuda.synchronize(device)
+            del ids, w, x, y
+        del layers
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -886,6 +993,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "grouped"])
     ap.add_argument("--block", type=int, default=0, help="MoE block size b of the grouped path (0: automatic)")
+    ap.add_argument("--table8", choices=sorted(TABLE8), default=None,
+                    help="run the grouped-GEMM benchmark grid (one JSON line per point) instead of the bench line")
     ap.add_argument("--layers", type=int, default=0,
                     help="copies of the layer's weights the steps rotate through (0: enough that the inputs of "
                          "the timed steps exceed the L2; 1 keeps a profiling run small)")
@@ -914,6 +1023,9 @@ def main():
     __graft_entry__.build()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.table8:
+        run_table8(args.table8, device)
+        return
     line = run_ours(args, rank, world, device)
     if line is not None:
         if world == 1 and not args.no_cpu_baseline:

@@ -139,6 +139,30 @@ moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, int32_t k,
                                   int32_t *num_rows_post_pad, int32_t cap_rows, int32_t cap_blocks,
                                   void *ws, size_t ws_bytes, int32_t *dev_status, void *stream);
 
+/* Fixed-capacity (batched) layout, the alternative to alignment that
+ * "Hardware-Native Joint Sparse-Quantization ...", App. D.1 uses: expert e
+ * owns rows e*C .. e*C + C - 1 of the operands at a fixed stride, so no
+ * prefix over experts is needed, and only its ceil(N_e / b) active blocks
+ * are computed.  Inside an expert the routes keep the stable-construction
+ * order (route id ascending).
+ *   C        rows per expert, a multiple of b; it must be at least every
+ *            expert's route count N_e (the page takes the largest count):
+ *            routes past C get no row, are counted in dev_status[0] with the
+ *            invalid routes, and their tokens' layer output is then not
+ *            defined
+ *   sorted_route_ids int32 [E*C]: row e*C + i holds the i-th route of
+ *            expert e, rows past N_e the sentinel M*k
+ *   expert_ids, block_rows int32 [E*C/b]: the active blocks in expert
+ *            order, compacted: block j is expert expert_ids[j]'s rows
+ *            block_rows[j] .. block_rows[j] + b - 1; the tail -1 / 0
+ *   num_rows_post_pad int32 [1]: b * (number of active blocks)
+ * Deterministic (the same bits on every call).  Limits: E <= 1024,
+ * 1 <= b <= 256, E*C < 2^31.  No workspace. */
+moe_status_t moe_align_fixed_capacity(const int32_t *topk_ids, int32_t M, int32_t k, int32_t E, int32_t b,
+                                      int32_t C, int32_t *sorted_route_ids, int32_t *expert_ids,
+                                      int32_t *block_rows, int32_t *num_rows_post_pad,
+                                      int32_t *dev_status, void *stream);
+
 /* ---------------------------------------------------------- quantization
  * MXFP8 quantization of rows of K values, per 32-element block along K
  * ("Hardware-Native Joint Sparse-Quantization ...", Sec. 3.4 / App. D.1:
@@ -301,6 +325,21 @@ moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d,
                              void *y, int32_t ydt, void *ws, size_t ws_bytes,
                              int32_t *dev_status, void *stream);
 
+/* moe_ffn_grouped on the fixed-capacity layout of moe_align_fixed_capacity
+ * (MOE_W_MXFP8 only; AWQ returns MOE_ERR_UNSUPPORTED): the same arguments
+ * plus block_rows, with cap_rows = E*C (any multiple of b) and ws sized by
+ * moe_ffn_grouped_workspace_size for that cap_rows.  Every route's result
+ * is the same, bit for bit, as on the aligned layout: a route's output does
+ * not depend on the rows it shares a block with. */
+moe_status_t moe_ffn_grouped_batched(const void *x, int32_t xdt, int32_t M, int32_t d,
+                                     const int32_t *topk_ids, const float *topk_w, int32_t k,
+                                     const moe_weights_t *w13, const moe_weights_t *w2,
+                                     const void *sfa13, const void *sfa2,
+                                     const int32_t *sorted_route_ids, const int32_t *expert_ids,
+                                     const int32_t *block_rows, const int32_t *num_rows_post_pad, int32_t b,
+                                     int32_t cap_rows, void *y, int32_t ydt, void *ws, size_t ws_bytes,
+                                     int32_t *dev_status, void *stream);
+
 /* ------------------------------------------------------- path selection
  * Which of the two paths to run for a batch ("Warp decode", sections on
  * what changed and on hardware efficiency: the output-centric path for few
@@ -328,6 +367,21 @@ moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d,
  * Host only; launches nothing. */
 moe_status_t moe_ffn_select_path(int32_t M, int32_t k, int32_t E, int32_t d, int32_t I, int32_t fmt,
                                  int32_t *path, int32_t *block);
+
+/* ---------------------------------------------- expert-parallel sharding
+ * "Hardware-Native Joint Sparse-Quantization ...", App. D.3 (serving with the
+ * experts sharded over an expert-parallel group).  The rank that owns experts
+ * [e_lo, e_hi) keeps them as its own weights, indexed 0 .. e_hi - e_lo - 1;
+ * this maps the routing to those indices: local_ids[i] = topk_ids[i] - e_lo
+ * for e_lo <= topk_ids[i] < e_hi, else -1 (an invalid route, which every
+ * layer call skips and counts in dev_status[0]).  Running the layer on the
+ * rank's weights with the mapped routing gives that rank's experts' share of
+ * y; the shares of all ranks sum to the full layer.
+ *   topk_ids, local_ids  int32 device arrays of n elements (may be the same)
+ * n = 0 is a no-op; n < 0, e_lo < 0, e_hi < e_lo or null arrays return
+ * MOE_ERR_INVALID_ARG before anything is launched. */
+moe_status_t moe_ep_local_routes(const int32_t *topk_ids, int64_t n, int32_t e_lo, int32_t e_hi,
+                                 int32_t *local_ids, void *stream);
 
 /* ------------------------------------------------ allocation-free decode
  * No counterpart on the pages: a convenience for callers that cannot hand

@@ -273,6 +273,36 @@ def align(ids, E: int, b: int, cap_rows: int | None = None, cap_blocks: int | No
     return sorted_ids, expert_ids, int(npp[0]), int(ninv[0])
 
 
+def align_fixed_capacity(ids, E: int, b: int, C: int):
+    """Fixed-capacity (batched) layout [SQ App. D.1]: expert e owns rows
+    e*C .. e*C + C - 1; its valid routes in route-id order fill the first
+    min(N_e, C) of them, the sentinel M*k the rest; the active blocks, the
+    first ceil(min(N_e, C) / b) of each expert in expert order, are listed
+    compacted.  Returns (sorted_route_ids [E*C], expert_ids [E*C/b],
+    block_rows [E*C/b], num_rows_post_pad, n_dropped_or_invalid).  A plain
+    statement of the definition in Python loops (small cases only)."""
+    ids = np.asarray(ids, dtype=np.int64)
+    M, k = ids.shape
+    sentinel = M * k
+    flat = ids.reshape(-1)
+    sorted_ids = np.full(E * C, sentinel, dtype=np.int32)
+    expert_ids = np.full(E * C // b, -1, dtype=np.int32)
+    block_rows = np.zeros(E * C // b, dtype=np.int32)
+    bad = int(np.sum((flat < 0) | (flat >= E)))
+    j = 0
+    for e in range(E):
+        routes = [r for r in range(M * k) if flat[r] == e]
+        kept = routes[:C]
+        bad += len(routes) - len(kept)
+        for i, r in enumerate(kept):
+            sorted_ids[e * C + i] = r
+        for t in range(-(-len(kept) // b)):
+            expert_ids[j] = e
+            block_rows[j] = e * C + t * b
+            j += 1
+    return sorted_ids, expert_ids, block_rows, j * b, bad
+
+
 def block_identity(sorted_route_ids, expert_ids, num_rows_post_pad: int, b: int, sentinel: int):
     """Mode identity of an aligned sequence [RB, block-membership paragraph].
 

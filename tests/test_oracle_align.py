@@ -152,3 +152,34 @@ def test_split_k_schedule_reproduces_the_pages_derivation():
         assert got["remainder_start_block"] == case["remainder_start_block"]
         assert got["slices"] == case["slices"]
         assert got["k_tiles_per_slice"] == case["k_tiles_per_slice"]
+
+
+def test_fixed_capacity_layout_by_hand_and_against_alignment():
+    """The fixed-capacity layout [SQ App. D.1] on a hand-checked case, and on
+    random routings: each expert's rows carry the same routes in the same
+    order as its run in the stable-construction alignment, which the worked
+    example and brute force above pin."""
+    # M=3, k=2: routes 0..5 with experts 2,0 | 2,1 | 0,2; E=3, b=2, C=4
+    ids = np.array([[2, 0], [2, 1], [0, 2]], dtype=np.int32)
+    s, e, br, npp, bad = oracle.align_fixed_capacity(ids, 3, 2, 4)
+    S = 6
+    assert s.tolist() == [1, 4, S, S, 3, S, S, S, 0, 2, 5, S]
+    assert e.tolist() == [0, 1, 2, 2, -1, -1] and br.tolist() == [0, 4, 8, 10, 0, 0]
+    assert npp == 8 and bad == 0
+    # capacity 2: expert 2's third route (5) is dropped and counted
+    s, e, br, npp, bad = oracle.align_fixed_capacity(ids, 3, 2, 2)
+    assert s.tolist() == [1, 4, 3, S, 0, 2] and e.tolist() == [0, 1, 2] and br.tolist() == [0, 2, 4]
+    assert npp == 6 and bad == 1
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        M, k, E, b = int(rng.integers(1, 12)), int(rng.integers(1, 5)), int(rng.integers(1, 9)), 4
+        ids = rng.integers(-1, E + 1, (M, k)).astype(np.int32)
+        counts = [int(np.sum(ids == x)) for x in range(E)]
+        C = (max(counts + [1]) + b - 1) // b * b
+        s, e, br, npp, bad = oracle.align_fixed_capacity(ids, E, b, C)
+        sa, ea, nppa, ninv = oracle.align(ids, E, b)
+        assert bad == ninv and npp == nppa               # no drops at C >= max count: the same blocks
+        assert e[:npp // b].tolist() == ea[:nppa // b].tolist()
+        for x in range(E):
+            run = [int(r) for r, ex in zip(sa[:nppa], np.repeat(ea[:nppa // b], b)) if ex == x and r < M * k]
+            assert s[x * C:x * C + counts[x]].tolist() == run

@@ -70,6 +70,11 @@ _PROTOS = {
     "moe_ffn_decode_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                                       ctypes.POINTER(moe_weights_t), _P, _I32, _P, _P]),
     "moe_debug_exchange_stall": (_I32, [_I32]),
+    "moe_ep_local_routes": (_I32, [_P, _I64, _I32, _I32, _P, _P]),
+    "moe_align_fixed_capacity": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "moe_ffn_grouped_batched": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
+                                       ctypes.POINTER(moe_weights_t), _P, _P, _P, _P, _P, _P, _I32, _I32, _P,
+                                       _I32, _P, _SZ, _P, _P]),
 }
 
 
@@ -262,6 +267,20 @@ def moe_topk_softmax(logits: torch.Tensor, k: int, topk_ids=None, topk_w=None, s
     return ids, w
 
 
+def moe_ep_local_routes(topk_ids: torch.Tensor, e_lo: int, e_hi: int, local_ids=None, stream=None):
+    """The routing as seen by the rank that owns experts [e_lo, e_hi): ids
+    of its experts shifted to 0 .. e_hi - e_lo - 1, every other id -1 (an
+    invalid route the layer skips)."""
+    _need(topk_ids, "topk_ids", _IDS)
+    dev = topk_ids.device
+    out = local_ids if local_ids is not None else torch.empty_like(topk_ids)
+    _need(out, "local_ids", _IDS, tuple(topk_ids.shape), device=dev)
+    with _guard(dev):
+        _check(lib().moe_ep_local_routes(_ptr(topk_ids), topk_ids.numel(), int(e_lo), int(e_hi), _ptr(out),
+                                         _stream(stream, dev)), "moe_ep_local_routes")
+    return out
+
+
 # ---------------------------------------------------------------- alignment
 
 def moe_ffn_select_path(M: int, k: int, E: int, d: int, I: int, fmt: int = None):
@@ -325,6 +344,34 @@ def moe_align_block_size(topk_ids: torch.Tensor, E: int, b: int, cap_rows=None, 
         _check(lib().moe_align_block_size(_ptr(topk_ids), M, k, E, b, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
                                           cap_rows, cap_blocks, _ptr(ws), _nbytes(ws), _ptr(dev_status),
                                           _stream(stream, dev)), "moe_align_block_size")
+    return out
+
+
+def moe_align_fixed_capacity(topk_ids: torch.Tensor, E: int, b: int, C: int, out=None, dev_status=None,
+                             stream=None):
+    """Fixed-capacity layout: returns (sorted_route_ids [E*C], expert_ids
+    [E*C/b], block_rows [E*C/b], num_rows_post_pad [1]) as int32 device
+    tensors; C (a multiple of b) must be at least every expert's route count."""
+    _need(topk_ids, "topk_ids", _IDS)
+    if topk_ids.dim() != 2:
+        raise ValueError(f"topk_ids must be [M, k], not {tuple(topk_ids.shape)}")
+    if b < 1 or C < b or C % b:
+        raise ValueError(f"capacity C = {C} must be a positive multiple of b = {b}")
+    M, k = topk_ids.shape
+    dev = topk_ids.device
+    rows, blocks = E * C, E * C // b
+    if out is None:
+        out = (torch.empty(rows, dtype=torch.int32, device=dev), torch.empty(blocks, dtype=torch.int32, device=dev),
+               torch.empty(blocks, dtype=torch.int32, device=dev), torch.empty(1, dtype=torch.int32, device=dev))
+    _need(out[0], "sorted_route_ids", _IDS, (rows,), device=dev)
+    _need(out[1], "expert_ids", _IDS, (blocks,), device=dev)
+    _need(out[2], "block_rows", _IDS, (blocks,), device=dev)
+    _need(out[3], "num_rows_post_pad", _IDS, min_numel=1, device=dev)
+    _opt(dev_status, "dev_status", dtypes=_IDS, min_numel=2, device=dev)
+    with _guard(dev):
+        _check(lib().moe_align_fixed_capacity(_ptr(topk_ids), M, k, E, b, C, _ptr(out[0]), _ptr(out[1]),
+                                              _ptr(out[2]), _ptr(out[3]), _ptr(dev_status), _stream(stream, dev)),
+               "moe_align_fixed_capacity")
     return out
 
 
@@ -488,15 +535,21 @@ def moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows) -> int:
 def moe_ffn_grouped(x, topk_ids, topk_w, w13: Weights, w2: Weights, sfa13, sfa2, aligned, b: int,
                     out_dtype=torch.bfloat16, y=None, ws=None, dev_status=None, stream=None):
     """Expert-centric grouped path; `aligned` = (sorted_route_ids,
-    expert_ids, num_rows_post_pad) from moe_align_block_size with the same b."""
+    expert_ids, num_rows_post_pad) from moe_align_block_size with the same b,
+    or (sorted_route_ids, expert_ids, block_rows, num_rows_post_pad) from
+    moe_align_fixed_capacity (the fixed-capacity layout, MXFP8 only)."""
     dev, M, d, k, y = _layer_args(x, topk_ids, topk_w, w13, w2, y, out_dtype, dev_status)
     I = w2.K
     if b < 1:
         raise ValueError(f"block size b = {b} must be positive")
-    sorted_ids, expert_ids, npp = aligned
+    if len(aligned) == 4:
+        sorted_ids, expert_ids, block_rows, npp = aligned
+    else:
+        (sorted_ids, expert_ids, npp), block_rows = aligned, None
     _need(sorted_ids, "sorted_route_ids", _IDS, device=dev)
     cap_rows = sorted_ids.numel()
     _need(expert_ids, "expert_ids", _IDS, min_numel=cap_rows // b, device=dev)
+    _opt(block_rows, "block_rows", dtypes=_IDS, min_numel=cap_rows // b, device=dev)
     _need(npp, "num_rows_post_pad", _IDS, min_numel=1, device=dev)
     a, bb = w13.c_struct(), w2.c_struct()
     if w13.fmt == MOE_W_MXFP8 and w2.fmt == MOE_W_MXFP8:
@@ -513,9 +566,16 @@ def moe_ffn_grouped(x, topk_ids, topk_w, w13: Weights, w2: Weights, sfa13, sfa2,
         ws = torch.empty(moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows), dtype=torch.uint8, device=dev)
     _need(ws, "ws", device=dev)
     with _guard(dev):
-        _check(lib().moe_ffn_grouped(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
-                                     ctypes.byref(a), ctypes.byref(bb), _ptr(sfa13), _ptr(sfa2),
-                                     _ptr(sorted_ids), _ptr(expert_ids), _ptr(npp), b, cap_rows,
-                                     _ptr(y), _DT[y.dtype], _ptr(ws), _nbytes(ws), _ptr(dev_status),
-                                     _stream(stream, dev)), "moe_ffn_grouped")
+        if block_rows is None:
+            _check(lib().moe_ffn_grouped(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                         ctypes.byref(a), ctypes.byref(bb), _ptr(sfa13), _ptr(sfa2),
+                                         _ptr(sorted_ids), _ptr(expert_ids), _ptr(npp), b, cap_rows,
+                                         _ptr(y), _DT[y.dtype], _ptr(ws), _nbytes(ws), _ptr(dev_status),
+                                         _stream(stream, dev)), "moe_ffn_grouped")
+        else:
+            _check(lib().moe_ffn_grouped_batched(_ptr(x), _DT[x.dtype], M, d, _ptr(topk_ids), _ptr(topk_w), k,
+                                                 ctypes.byref(a), ctypes.byref(bb), _ptr(sfa13), _ptr(sfa2),
+                                                 _ptr(sorted_ids), _ptr(expert_ids), _ptr(block_rows), _ptr(npp),
+                                                 b, cap_rows, _ptr(y), _DT[y.dtype], _ptr(ws), _nbytes(ws),
+                                                 _ptr(dev_status), _stream(stream, dev)), "moe_ffn_grouped_batched")
     return y

@@ -337,3 +337,143 @@ MOE_API moe_status_t moe_align_block_size(const int32_t *topk_ids, int32_t M, in
                ? MOE_OK
                : MOE_ERR_CUDA;
 }
+
+namespace moe {
+
+// ---------------------------------------------------------------- fixed capacity
+// The batched operand layout of "Hardware-Native Joint Sparse-Quantization
+// for Trillion-Scale Mixture-of-Experts", App. D.1: every expert owns C rows
+// at a fixed stride (rows e*C .. e*C + C - 1), so its operands need no
+// prefix sum; a tile list covers only ceil(N_e / b) blocks of expert e.
+// Inside an expert the routes keep the stable-construction order (route id
+// ascending), as in moe_align_block_size.
+
+// One CTA per expert: its routes in route-id order into its C rows (routes
+// past C are dropped and counted), the rest of its rows the sentinel M*k;
+// its route count (capped at C) into cnt[e].
+__global__ void __launch_bounds__(1024) align_fixed_place_kernel(const int32_t *__restrict__ ids, int MK, int E,
+                                                                 int C, int32_t *__restrict__ sorted,
+                                                                 int32_t *__restrict__ cnt,
+                                                                 int32_t *__restrict__ dev_status)
+{
+    __shared__ int warp_tot[32];
+    __shared__ int base_s;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+    int32_t *rows = sorted + static_cast<int64_t>(e) * C;
+    if (tid == 0)
+        base_s = 0;
+    __syncthreads();
+    for (int r0 = 0; r0 < MK; r0 += blockDim.x) {
+        const int r = r0 + tid;
+        const bool mine = r < MK && ids[r] == e;
+        const unsigned m = __ballot_sync(0xffffffffu, mine);
+        if (lane == 0)
+            warp_tot[wid] = __popc(m);
+        __syncthreads();
+        int before = base_s;
+        for (int w = 0; w < wid; ++w)
+            before += warp_tot[w];
+        const int pos = before + __popc(m & ((1u << lane) - 1u));
+        if (mine && pos < C)
+            rows[pos] = r;
+        __syncthreads();
+        if (tid == 0) {
+            int t = 0;
+            for (int w = 0; w < nw; ++w)
+                t += warp_tot[w];
+            base_s += t;
+        }
+        __syncthreads();
+    }
+    const int n = base_s;
+    for (int i = (n < C ? n : C) + tid; i < C; i += blockDim.x)
+        rows[i] = MK;
+    if (tid == 0) {
+        cnt[e] = n < C ? n : C;
+        if (n > C && dev_status)
+            atomicAdd(dev_status, n - C);
+    }
+    if (e == 0 && dev_status) {
+        // invalid routes (ids outside [0, E)) are counted once
+        int bad = 0;
+        for (int r = tid; r < MK; r += blockDim.x)
+            bad += !valid_id(ids[r], E);
+        bad = __reduce_add_sync(0xffffffffu, bad);
+        if (lane == 0 && bad)
+            atomicAdd(dev_status, bad);
+    }
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// One CTA: the active blocks of every expert in expert order, compacted:
+// expert_ids[j], block_rows[j] (the block's first row); the tail -1 / 0;
+// num_rows_post_pad = b * (number of active blocks).
+__global__ void __launch_bounds__(1024) align_fixed_blocks_kernel(int E, int C, int b, int cap_blocks,
+                                                                  int32_t *__restrict__ expert_ids,
+                                                                  int32_t *__restrict__ block_rows,
+                                                                  int32_t *__restrict__ npp)
+{
+    extern __shared__ int32_t sm_nb[];          // [E] blocks per expert, then their exclusive prefix
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int tid = threadIdx.x;
+    // the counts were parked in expert_ids[0 .. E); read them all first
+    for (int e = tid; e < E; e += blockDim.x)
+        sm_nb[e] = (expert_ids[e] + b - 1) / b;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            const int nb = sm_nb[e];
+            sm_nb[E + e] = run;
+            run += nb;
+        }
+        sm_nb[2 * E] = run;
+    }
+    __syncthreads();
+    const int total = sm_nb[2 * E];
+    for (int e = 0; e < E; ++e) {
+        const int nb = sm_nb[e], off = sm_nb[E + e];
+        for (int t = tid; t < nb; t += blockDim.x) {
+            expert_ids[off + t] = e;
+            block_rows[off + t] = e * C + t * b;
+        }
+    }
+    for (int j = total + tid; j < cap_blocks; j += blockDim.x) {
+        expert_ids[j] = -1;
+        block_rows[j] = 0;
+    }
+    if (tid == 0)
+        *npp = total * b;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status_t moe_align_fixed_capacity(const int32_t *topk_ids, int32_t M, int32_t k, int32_t E, int32_t b,
+                                              int32_t C, int32_t *sorted_route_ids, int32_t *expert_ids,
+                                              int32_t *block_rows, int32_t *num_rows_post_pad,
+                                              int32_t *dev_status, void *stream)
+{
+    if (M < 0 || k < 1 || E < 1 || b < 1 || C < 1 || C % b)
+        return MOE_ERR_INVALID_ARG;
+    if (E > kAlignMaxE || b > 256)
+        return MOE_ERR_UNSUPPORTED;
+    const int64_t mk = static_cast<int64_t>(M) * k, rows = static_cast<int64_t>(E) * C;
+    if (rows > INT32_MAX || mk >= INT32_MAX)
+        return MOE_ERR_UNSUPPORTED;
+    if (!sorted_route_ids || !expert_ids || !block_rows || !num_rows_post_pad || (mk > 0 && !topk_ids))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    // per-expert counts go to expert_ids[0 .. E) (E <= E*C/b entries)
+    if (launch_pdl(align_fixed_place_kernel, dim3(E), dim3(1024), 0, s, topk_ids, static_cast<int>(mk), E,
+                   static_cast<int>(C), sorted_route_ids, expert_ids, dev_status) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const size_t smem = (2 * static_cast<size_t>(E) + 1) * sizeof(int32_t);
+    return launch_pdl(align_fixed_blocks_kernel, dim3(1), dim3(1024), smem, s, E, static_cast<int>(C), b,
+                      static_cast<int>(rows / b), expert_ids, block_rows, num_rows_post_pad) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}

@@ -51,6 +51,7 @@ struct Args {
     const uint8_t *sfa;       // A scale atoms  [E][n_mt][KT][512]
     const uint8_t *sfb;       // B scale atoms  [cap_blocks][KT][nsf][512]
     const int32_t *expert_ids;
+    const int32_t *brow;      // first row of each block (fixed-capacity layout), or null: block j at j * b
     const int32_t *npp;       // num_rows_post_pad
     const int32_t *sorted;    // sorted_route_ids
     const float *wts;         // topk_w flattened [MK]
@@ -102,7 +103,8 @@ __device__ __forceinline__ uint32_t to_e4m3(float u)
 // with 16-byte loads and stores (the block's amax stays in the lane).
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__restrict__ x, int d, int k, int MK,
                                                         const int32_t *__restrict__ sorted,
-                                                        const int32_t *__restrict__ npp, int b, int nsf,
+                                                        const int32_t *__restrict__ npp,
+                                                        const int32_t *__restrict__ brow, int b, int nsf,
                                                         uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
                                                         int32_t *__restrict__ done)
 {
@@ -110,15 +112,17 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__r
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
-    const int rows = *npp;
+    const int rows = *npp;                        // b * active blocks
     // the GEMM's per-block counters of finished first-GEMM tiles start at 0
-    for (int jb = blockIdx.x * blockDim.x + threadIdx.x; jb < rows / b; jb += gridDim.x * blockDim.x)
-        done[jb] = 0;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < rows / b; j += gridDim.x * blockDim.x)
+        done[brow ? brow[j] / b : j] = 0;
     const int nblk = d / 32, KT = d / 128;
     const int nw = gridDim.x * (blockDim.x >> 5);
-    for (int rho = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); rho < rows; rho += nw) {
+    for (int cr = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); cr < rows; cr += nw) {
+        // the cr-th row of the active blocks: row rho of row-block jb
+        const int j = cr / b, m = cr - j * b;
+        const int jb = brow ? brow[j] / b : j, rho = jb * b + m;
         const int r = sorted[rho];
-        const int jb = rho / b, m = rho % b;
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(r < MK ? r / k : 0) * d);
         uint4 *qr = reinterpret_cast<uint4 *>(xq + static_cast<int64_t>(rho) * d);
         for (int blk = lane; blk < nblk; blk += 32) {
@@ -282,6 +286,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
                 int jb, mt;
                 const int kind = tile_kind(t, total1, n_mt1, n_mt2, jb, mt);
                 const int e = a1.expert_ids[jb];
+                const int rb = a1.brow ? a1.brow[jb] / a1.b : jb;   // the block's row-block
                 const int KT = kind == 1 ? a1.KT : a2.KT;
                 const int n_mt = kind == 1 ? n_mt1 : n_mt2;
                 const int a_rows = kind == 1 ? a1.a_rows : a2.a_rows;
@@ -295,7 +300,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
                     const long long limit = static_cast<long long>(kWaitNs) * 5 / 2;
                     int v;
                     for (;;) {
-                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(done + jb) : "memory");
+                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(done + rb) : "memory");
                         if (v >= n_mt1)
                             break;
                         if (*abort_flag || clock64() - t0 > limit) {
@@ -321,11 +326,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
                     } else {
                         tc::tma_load_2d(tc::smem_u32(st), tA, x, e * a_rows + 128 * mt, fb);
                     }
-                    tc::tma_load_2d(tc::smem_u32(st + 16384), tB, x, jb * a1.b, fb);
+                    tc::tma_load_2d(tc::smem_u32(st + 16384), tB, x, rb * a1.b, fb);
                     tc::bulk_load(tc::smem_u32(st + 16384 + NB),
                                   sfa + ((static_cast<int64_t>(e) * n_mt + mt) * KT + kt) * 512, 512, fb);
                     tc::bulk_load(tc::smem_u32(st + 16384 + NB + 512),
-                                  sfb + (static_cast<int64_t>(jb) * KT + kt) * nsf * 512, nsf * 512, fb);
+                                  sfb + (static_cast<int64_t>(rb) * KT + kt) * nsf * 512, nsf * 512, fb);
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1u;
@@ -400,7 +405,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
             const int kind = tile_kind(t, total1, n_mt1, n_mt2, jb, mt);
             const int buf = nbuf == 2 ? (ti & 1) : 0;
             const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
-            const int rho0 = jb * b;
+            const int rb = a1.brow ? a1.brow[jb] / b : jb;            // the block's row-block
+            const int rho0 = rb * b;
             if (kind == 2) {
                 // routes and routing weights of the tile's rows, loaded once
                 for (int c = etid; c < b; c += 128) {
@@ -449,7 +455,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
                     const int n = 64 * mt + 32 * (q & 1) + lane;     // neuron of this lane
                     const int kblk = 2 * mt + (q & 1);                // its 32-neuron block
                     uint8_t *hrow = a1.hq + static_cast<int64_t>(rho0 + c0 + keep) * a1.I + n;
-                    uint8_t *hsa = a1.hs + ((static_cast<int64_t>(jb) * (a1.I / 128) + kblk / 4) * nsf) * 512;
+                    uint8_t *hsa = a1.hs + ((static_cast<int64_t>(rb) * (a1.I / 128) + kblk / 4) * nsf) * 512;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
                         const int X = mx_exp(am[c]);
@@ -495,7 +501,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
             if (lane == 0)
                 tc::mbar_arrive(acce0 + 8 * buf);
             if (kind == 1 && etid == 0)                // every epilogue thread's stores are ordered before this
-                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(done + jb) : "memory");
+                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(done + rb) : "memory");
         }
         (void)etid;
     }
@@ -694,12 +700,14 @@ MOE_API moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_
     return MOE_OK;
 }
 
-MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d, const int32_t *topk_ids,
-                                     const float *topk_w, int32_t k, const moe_weights_t *w13,
-                                     const moe_weights_t *w2, const void *sfa13, const void *sfa2,
-                                     const int32_t *sorted_route_ids, const int32_t *expert_ids,
-                                     const int32_t *num_rows_post_pad, int32_t b, int32_t cap_rows, void *y,
-                                     int32_t ydt, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream)
+// The grouped layer on aligned rows (block_rows null: block j is rows j*b ..)
+// or on the fixed-capacity layout (block j starts at row block_rows[j]).
+static moe_status_t grouped_impl(const void *x, int32_t xdt, int32_t M, int32_t d, const int32_t *topk_ids,
+                                 const float *topk_w, int32_t k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                 const void *sfa13, const void *sfa2, const int32_t *sorted_route_ids,
+                                 const int32_t *expert_ids, const int32_t *block_rows,
+                                 const int32_t *num_rows_post_pad, int32_t b, int32_t cap_rows, void *y, int32_t ydt,
+                                 void *ws, size_t ws_bytes, int32_t *dev_status, void *stream)
 {
     if (M < 0 || d < 1 || k < 1 || !w13 || !w2)
         return MOE_ERR_INVALID_ARG;
@@ -716,11 +724,19 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
     if (d % 128 || I % 128 || b < 8 || b > 256 || b % 8)
         return MOE_ERR_UNSUPPORTED;
     const int64_t mk = static_cast<int64_t>(M) * k;
-    int32_t need_rows, need_blocks;
-    if (moe_align_capacity(M, k, E, b, &need_rows, &need_blocks) != MOE_OK)
-        return MOE_ERR_UNSUPPORTED;
-    if (cap_rows < need_rows || cap_rows % b)
-        return MOE_ERR_CAPACITY;
+    if (block_rows) {
+        // fixed capacity: any multiple of b holds the layout it was built for
+        if (cap_rows < b || cap_rows % b)
+            return MOE_ERR_CAPACITY;
+        if (awq)
+            return MOE_ERR_UNSUPPORTED;
+    } else {
+        int32_t need_rows, need_blocks;
+        if (moe_align_capacity(M, k, E, b, &need_rows, &need_blocks) != MOE_OK)
+            return MOE_ERR_UNSUPPORTED;
+        if (cap_rows < need_rows || cap_rows % b)
+            return MOE_ERR_CAPACITY;
+    }
     if (M == 0)
         return MOE_OK;
     if (awq) {
@@ -768,7 +784,8 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         return MOE_ERR_CUDA;
 
     if (launch_pdl(act_quant_kernel, dim3(device_sm_count() * 4), dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(x), d,
-                   k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, b, nsf, xq, xs, done) != cudaSuccess)
+                   k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, block_rows, b, nsf, xq, xs,
+                   done) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     const int stage_bytes = (16384 + n_mma * 128 + 512 + nsf * 512 + 1023) & ~1023;
@@ -783,12 +800,38 @@ MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int3
         return MOE_ERR_CUDA;
     const int grid = device_sm_count();
 
-    Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
+    Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, block_rows, num_rows_post_pad, sorted_route_ids, topk_w,
             hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I, stages};
-    Args a2{static_cast<const uint8_t *>(sfa2), hs, expert_ids, num_rows_post_pad, sorted_route_ids, topk_w,
+    Args a2{static_cast<const uint8_t *>(sfa2), hs, expert_ids, block_rows, num_rows_post_pad, sorted_route_ids, topk_w,
             nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d, stages};
     if (launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tA1, tB1, tA2, tB2, a1, a2, done) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     return grouped_combine_launch(yr, topk_ids, M, k, d, E, y, ydt == MOE_FP32, s);
+}
+
+MOE_API moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d, const int32_t *topk_ids,
+                                     const float *topk_w, int32_t k, const moe_weights_t *w13,
+                                     const moe_weights_t *w2, const void *sfa13, const void *sfa2,
+                                     const int32_t *sorted_route_ids, const int32_t *expert_ids,
+                                     const int32_t *num_rows_post_pad, int32_t b, int32_t cap_rows, void *y,
+                                     int32_t ydt, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream)
+{
+    return grouped_impl(x, xdt, M, d, topk_ids, topk_w, k, w13, w2, sfa13, sfa2, sorted_route_ids, expert_ids,
+                        nullptr, num_rows_post_pad, b, cap_rows, y, ydt, ws, ws_bytes, dev_status, stream);
+}
+
+MOE_API moe_status_t moe_ffn_grouped_batched(const void *x, int32_t xdt, int32_t M, int32_t d,
+                                             const int32_t *topk_ids, const float *topk_w, int32_t k,
+                                             const moe_weights_t *w13, const moe_weights_t *w2, const void *sfa13,
+                                             const void *sfa2, const int32_t *sorted_route_ids,
+                                             const int32_t *expert_ids, const int32_t *block_rows,
+                                             const int32_t *num_rows_post_pad, int32_t b, int32_t cap_rows,
+                                             void *y, int32_t ydt, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                             void *stream)
+{
+    if (!block_rows)
+        return MOE_ERR_INVALID_ARG;
+    return grouped_impl(x, xdt, M, d, topk_ids, topk_w, k, w13, w2, sfa13, sfa2, sorted_route_ids, expert_ids,
+                        block_rows, num_rows_post_pad, b, cap_rows, y, ydt, ws, ws_bytes, dev_status, stream);
 }

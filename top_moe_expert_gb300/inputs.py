@@ -100,6 +100,22 @@ def fixture_a_weights(M: int = 21, k: int = 8, seed: int = 3) -> np.ndarray:
     return (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
 
 
+def imbalanced_counts(N: int, G: int) -> np.ndarray:
+    """Per-expert token counts of the grouped-GEMM benchmark ("Hardware-Native
+    Joint Sparse-Quantization ...", App. D.2): the pattern {N, 3N/4, N/2, N/4}
+    repeated over the G experts (rounded down, at least 1)."""
+    pat = np.array([N, 3 * N // 4, N // 2, N // 4], dtype=np.int64)
+    return np.maximum(pat[np.arange(G) % 4], 1)
+
+
+def imbalanced_routing(N: int, G: int, seed: int = 6) -> np.ndarray:
+    """ids [sum of the counts, 1]: one route per token, expert g taking
+    imbalanced_counts(N, G)[g] tokens; the tokens' order is a seeded
+    permutation (the page fixes only the counts)."""
+    ids = np.repeat(np.arange(G, dtype=np.int32), imbalanced_counts(N, G))
+    return rng(seed, 40 + N + 7 * G).permutation(ids).reshape(-1, 1).astype(np.int32)
+
+
 # ---------------------------------------------------------------- weights
 
 def weights_fp32(wl: Workload, which: str, experts=None) -> np.ndarray:
