@@ -161,6 +161,12 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         inside = [r for (t, r) in self.rows if t0 <= t <= t1]
+        window = "inside the timed region"
+        if not inside:
+            # a timed region shorter than the sampling period: the samples
+            # taken within 0.25 s of it (warm-up and the untimed steps around)
+            inside = [r for (t, r) in self.rows if t0 - 0.25 <= t <= t1 + 0.25]
+            window = "within 0.25 s of a timed region shorter than the sampling period"
         self.rows = inside
         if not self.rows:
             return None
@@ -174,7 +180,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(self.rows)}
+                "reasons": sorted(reasons), "samples": len(self.rows), "window": window}
 
 
 def committed_traffic(kernel_key: str, src_hash: str):
