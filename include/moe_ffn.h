@@ -34,6 +34,13 @@
  *     routes seen; dev_status[1] receives the first error a kernel detected
  *     on the device (MOE_ERR_TIMEOUT when a bounded wait on an mbarrier
  *     expired; the outputs of that call are then undefined).
+ *   - Debug bounds-check build (libmoe_ffn_debug.so, the same sources built
+ *     with MOE_DEBUG_BOUNDS): every global index that a kernel takes from
+ *     device data -- expert ids, route ids, block rows and row counts of the
+ *     alignment outputs -- is checked against its buffer before use; a
+ *     failed check skips the access (and the tile that depends on it) and
+ *     writes MOE_ERR_BOUNDS to dev_status[1].  The release build trusts the
+ *     contracts below and does not check.
  *   - Shapes are int32; M*k and the padded row counts must fit in int32.
  *
  * Weight formats (one projection of all E experts, [E][N][K], K contracted):
@@ -70,7 +77,7 @@
 extern "C" {
 #endif
 
-#define MOE_FFN_ABI_VERSION 2
+#define MOE_FFN_ABI_VERSION 3
 
 typedef enum {
     MOE_OK = 0,
@@ -79,7 +86,9 @@ typedef enum {
     MOE_ERR_CAPACITY = 3,     /* an output capacity is too small         */
     MOE_ERR_WORKSPACE = 4,    /* ws too small or misaligned (256 B)      */
     MOE_ERR_CUDA = 5,         /* a CUDA launch/attribute call failed      */
-    MOE_ERR_TIMEOUT = 6       /* a bounded device wait expired (dev_status[1]) */
+    MOE_ERR_TIMEOUT = 6,      /* a bounded device wait expired (dev_status[1]) */
+    MOE_ERR_BOUNDS = 7        /* debug build only: an index read from device data was out of its
+                                 buffer; the access was skipped (dev_status[1]) */
 } moe_status_t;
 
 /* (value 2 is retired: it named an MXFP8 layout stored K-outer) */

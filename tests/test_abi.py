@@ -49,7 +49,7 @@ def test_exchange_stall_hook_validates_its_argument(L):
 def test_status_names_and_version(L):
     for code, name in moe.STATUS_NAMES.items():
         assert L.moe_status_string(code).decode() == name
-    assert L.moe_abi_version() == 2
+    assert L.moe_abi_version() == 3
 
 
 def test_align_capacity_bound():

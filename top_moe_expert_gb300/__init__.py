@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_ffn.so")
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CAPACITY", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
-                6: "MOE_ERR_TIMEOUT"}
+                6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_BOUNDS"}
 MOE_W_MXFP8, MOE_W_AWQ4, MOE_W_NVFP4S = 0, 1, 3
 MOE_BF16, MOE_FP16, MOE_FP32 = 0, 1, 2
 MOE_PATH_DECODE, MOE_PATH_GROUPED = 0, 1
@@ -76,6 +76,15 @@ _PROTOS = {
                                        ctypes.POINTER(moe_weights_t), _P, _P, _P, _P, _P, _P, _I32, _I32, _P,
                                        _I32, _P, _SZ, _P, _P]),
 }
+
+
+def use_library(path: str) -> None:
+    """Load the library at `path` for the calls that follow (for example the
+    debug bounds-check build, build.LIB_DEBUG); the same entry points."""
+    global _lib, LIB_PATH
+    with _lock:
+        LIB_PATH = path
+        _lib = None
 
 
 def lib() -> ctypes.CDLL:

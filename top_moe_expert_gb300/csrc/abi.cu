@@ -11,6 +11,7 @@ MOE_API const char *moe_status_string(moe_status_t s)
     case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_BOUNDS: return "MOE_ERR_BOUNDS";
     }
     return "MOE_ERR_UNKNOWN";
 }

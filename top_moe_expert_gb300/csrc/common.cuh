@@ -30,6 +30,23 @@ inline size_t ws_round(size_t n) { return (n + 255) & ~size_t(255); }
 
 // ---------------------------------------------------------------- device
 
+// Debug bounds checks.  Built with MOE_DEBUG_BOUNDS, MOE_IN_BOUNDS(cond, st)
+// evaluates cond (an index taken from device data against its buffer) and,
+// when it fails, writes MOE_ERR_BOUNDS to st[1] (if st is not null); the
+// caller skips the access.  In the release build it is the constant true and
+// costs nothing.
+#ifdef MOE_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t *st)
+{
+    if (!ok && st)
+        atomicCAS(st + 1, 0, static_cast<int32_t>(MOE_ERR_BOUNDS));
+    return ok;
+}
+#define MOE_IN_BOUNDS(cond, st) ::moe::in_bounds((cond), (st))
+#else
+#define MOE_IN_BOUNDS(cond, st) true
+#endif
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

@@ -62,6 +62,7 @@ struct Args {
     int b, n_mma, nsf, n_mt, KT, I, d, MK;
     int a_rows;               // rows of one expert in the A tensor (2I or d)
     int stages;               // ring depth (<= kMaxStages)
+    int E, cap_blocks;        // experts, and the row-blocks the operands hold (debug bounds checks)
 };
 
 // Scale-atom byte offset of (row m of a 128-row group, k-block kb of 4):
@@ -105,24 +106,34 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__r
                                                         const int32_t *__restrict__ sorted,
                                                         const int32_t *__restrict__ npp,
                                                         const int32_t *__restrict__ brow, int b, int nsf,
-                                                        uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
-                                                        int32_t *__restrict__ done)
+                                                        int cap_rows, uint8_t *__restrict__ xq,
+                                                        uint8_t *__restrict__ xs, int32_t *__restrict__ done,
+                                                        int32_t *__restrict__ dev_status)
 {
     // chained by programmatic dependent launch: the alignment must be done
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
-    const int rows = *npp;                        // b * active blocks
+    int rows = *npp;                              // b * active blocks
+    if (!MOE_IN_BOUNDS(rows >= 0 && rows <= cap_rows, dev_status))
+        rows = 0;
     // the GEMM's per-block counters of finished first-GEMM tiles start at 0
-    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < rows / b; j += gridDim.x * blockDim.x)
-        done[brow ? brow[j] / b : j] = 0;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < rows / b; j += gridDim.x * blockDim.x) {
+        const int jb = brow ? brow[j] / b : j;
+        if (MOE_IN_BOUNDS(jb >= 0 && jb < cap_rows / b, dev_status))
+            done[jb] = 0;
+    }
     const int nblk = d / 32, KT = d / 128;
     const int nw = gridDim.x * (blockDim.x >> 5);
     for (int cr = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); cr < rows; cr += nw) {
         // the cr-th row of the active blocks: row rho of row-block jb
         const int j = cr / b, m = cr - j * b;
         const int jb = brow ? brow[j] / b : j, rho = jb * b + m;
-        const int r = sorted[rho];
+        if (!MOE_IN_BOUNDS(jb >= 0 && jb < cap_rows / b, dev_status))
+            continue;
+        int r = sorted[rho];
+        if (!MOE_IN_BOUNDS(r >= 0 && r <= MK, dev_status))
+            r = MK;                                   // read as padding
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(r < MK ? r / k : 0) * d);
         uint4 *qr = reinterpret_cast<uint4 *>(xq + static_cast<int64_t>(rho) * d);
         for (int blk = lane; blk < nblk; blk += 32) {
@@ -201,6 +212,15 @@ __global__ void prepare_sfa_kernel(const uint8_t *__restrict__ s, int E, int N, 
 // fences because TMA reads what generic stores wrote).  SMs that run out of
 // first-GEMM tiles start on the second GEMM instead of idling at a kernel
 // boundary.  Progress needs every CTA resident: the grid is one CTA per SM.
+// A tile's block: its expert and row-block, and (debug build) whether both
+// lie inside their buffers; every role takes the same decision for a tile.
+__device__ __forceinline__ bool block_ok(const Args &a, int jb, int &e, int &rb)
+{
+    e = a.expert_ids[jb];
+    rb = a.brow ? a.brow[jb] / a.b : jb;
+    return MOE_IN_BOUNDS(e >= 0 && e < a.E && rb >= 0 && rb < a.cap_blocks, a.dev_status);
+}
+
 __device__ __forceinline__ int tile_kind(int t, int total1, int n_mt1, int n_mt2, int &jb, int &mt)
 {
     if (t < total1) {
@@ -272,7 +292,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
 
-    const int n_blocks = *a1.npp / a1.b;
+    int n_blocks = *a1.npp / a1.b;
+    if (!MOE_IN_BOUNDS(n_blocks >= 0 && n_blocks <= a1.cap_blocks, a1.dev_status))
+        n_blocks = 0;
     const int n_mt1 = a1.n_mt, n_mt2 = a2.n_mt;
     const int total1 = n_blocks * n_mt1, total = total1 + n_blocks * n_mt2;
 
@@ -285,8 +307,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
                 int jb, mt;
                 const int kind = tile_kind(t, total1, n_mt1, n_mt2, jb, mt);
-                const int e = a1.expert_ids[jb];
-                const int rb = a1.brow ? a1.brow[jb] / a1.b : jb;   // the block's row-block
+                int e, rb;                                          // the block's expert and row-block
+                if (!block_ok(a1, jb, e, rb))
+                    continue;
                 const int KT = kind == 1 ? a1.KT : a2.KT;
                 const int n_mt = kind == 1 ? n_mt1 : n_mt2;
                 const int a_rows = kind == 1 ? a1.a_rows : a2.a_rows;
@@ -355,10 +378,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
         if (lane == 0) {
             int s = 0, ti = 0;
             uint32_t ph = 0;
-            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                int jb, mt, e, rb;
+                tile_kind(t, total1, n_mt1, n_mt2, jb, mt);
+                if (!block_ok(a1, jb, e, rb))
+                    continue;
+                const int tix = ti++;                           // this CTA's tiles that run
                 const int KT = t < total1 ? a1.KT : a2.KT;
-                const int buf = nbuf == 2 ? (ti & 1) : 0;
-                const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
+                const int buf = nbuf == 2 ? (tix & 1) : 0;
+                const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (tix >> 1) : tix);
                 if (!tc::mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, abort_flag, kWaitNs))
                     break;
                 tc::tc_fence_after();
@@ -400,17 +428,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
         const int etid = threadIdx.x - 64;
         int ti = 0;
         const int b = a1.b;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
-            int jb, mt;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int jb, mt, e, rb;                                        // the block's expert and row-block
             const int kind = tile_kind(t, total1, n_mt1, n_mt2, jb, mt);
-            const int buf = nbuf == 2 ? (ti & 1) : 0;
-            const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (ti >> 1) : ti);
-            const int rb = a1.brow ? a1.brow[jb] / b : jb;            // the block's row-block
+            if (!block_ok(a1, jb, e, rb))
+                continue;
+            const int tix = ti++;                                     // this CTA's tiles that run
+            const int buf = nbuf == 2 ? (tix & 1) : 0;
+            const uint32_t use = static_cast<uint32_t>(nbuf == 2 ? (tix >> 1) : tix);
             const int rho0 = rb * b;
             if (kind == 2) {
                 // routes and routing weights of the tile's rows, loaded once
                 for (int c = etid; c < b; c += 128) {
-                    const int r = a2.sorted[rho0 + c];
+                    int r = a2.sorted[rho0 + c];
+                    if (!MOE_IN_BOUNDS(r >= 0 && r <= a2.MK, a2.dev_status))
+                        r = a2.MK;                                // read as padding
                     t_route[c] = r;
                     t_w[c] = r < a2.MK ? a2.wts[r] : 0.f;
                 }
@@ -784,8 +816,8 @@ static moe_status_t grouped_impl(const void *x, int32_t xdt, int32_t M, int32_t 
         return MOE_ERR_CUDA;
 
     if (launch_pdl(act_quant_kernel, dim3(device_sm_count() * 4), dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(x), d,
-                   k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, block_rows, b, nsf, xq, xs,
-                   done) != cudaSuccess)
+                   k, static_cast<int>(mk), sorted_route_ids, num_rows_post_pad, block_rows, b, nsf, cap_rows, xq,
+                   xs, done, dev_status) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     const int stage_bytes = (16384 + n_mma * 128 + 512 + nsf * 512 + 1023) & ~1023;
@@ -801,9 +833,11 @@ static moe_status_t grouped_impl(const void *x, int32_t xdt, int32_t M, int32_t 
     const int grid = device_sm_count();
 
     Args a1{static_cast<const uint8_t *>(sfa13), xs, expert_ids, block_rows, num_rows_post_pad, sorted_route_ids, topk_w,
-            hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I, stages};
+            hq, hs, nullptr, dev_status, b, n_mma, nsf, I / 64, d / 128, I, d, static_cast<int>(mk), 2 * I, stages,
+            E, cap_rows / b};
     Args a2{static_cast<const uint8_t *>(sfa2), hs, expert_ids, block_rows, num_rows_post_pad, sorted_route_ids, topk_w,
-            nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d, stages};
+            nullptr, nullptr, yr, dev_status, b, n_mma, nsf, d / 128, I / 128, I, d, static_cast<int>(mk), d, stages,
+            E, cap_rows / b};
     if (launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tA1, tB1, tA2, tB2, a1, a2, done) !=
         cudaSuccess)
         return MOE_ERR_CUDA;

@@ -79,6 +79,7 @@ struct Args {
     float *yr;                // kind 2: [MK][d]
     int32_t *dev_status;
     int b, n_mma, n_t, KT, I, d, MK, N, G, stages, aslots, acc_cols, nbuf;
+    int E, cap_blocks;        // experts, and the blocks the operands hold (debug bounds checks)
 };
 
 // A tile is 256 weight rows of one expert, in two halves of 128 that two MMA
@@ -235,7 +236,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
     asm volatile("griddepcontrol.launch_dependents;");
 
     const int b = a1.b;
-    const int n_blocks = *a1.npp / b;
+    int n_blocks = *a1.npp / b;
+#ifdef MOE_DEBUG_BOUNDS
+    {
+        // debug build: the block count and every block's expert inside
+        // their buffers, or no tile runs at all (every role sees the same)
+        bool bad = n_blocks < 0 || n_blocks > a1.cap_blocks;
+        for (int j = threadIdx.x; !bad && j < n_blocks; j += blockDim.x)
+            bad = a1.expert_ids[j] < 0 || a1.expert_ids[j] >= a1.E;
+        if (__syncthreads_or(bad)) {
+            MOE_IN_BOUNDS(false, a1.dev_status);
+            n_blocks = 0;
+        }
+    }
+#endif
     const int n_t1 = a1.n_t, n_t2 = a2.n_t;
     const int total1 = n_blocks * n_t1, total = total1 + n_blocks * n_t2;
     const uint32_t a_base = static_cast<uint32_t>(2 * NB * a1.acc_cols);   // first A-unit column
@@ -400,7 +414,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
             const int rho0 = jb * b;
             if (kind == 2) {
                 for (int c = etid; c < b; c += 128) {
-                    const int r = a2.sorted[rho0 + c];
+                    int r = a2.sorted[rho0 + c];
+                    if (!MOE_IN_BOUNDS(r >= 0 && r <= a2.MK, a2.dev_status))
+                        r = a2.MK;                            // read as padding
                     t_route[c] = r;
                     t_w[c] = r < a2.MK ? a2.wts[r] : 0.f;
                 }
@@ -545,11 +561,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
 // the operand order 0, 4, 1, 5, 2, 6, 3, 7; 8 values per thread
 template <typename XT>
 __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, const int32_t *__restrict__ sorted,
-                              const int32_t *__restrict__ npp, __half *__restrict__ xg, int b, int32_t *__restrict__ done)
+                              const int32_t *__restrict__ npp, __half *__restrict__ xg, int b, int32_t *__restrict__ done,
+                              int cap_rows, int32_t *__restrict__ dev_status)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    const int rows = *npp;
+    int rows = *npp;
+    if (!MOE_IN_BOUNDS(rows >= 0 && rows <= cap_rows, dev_status))
+        rows = 0;
     // the GEMM's per-block counters of finished first-GEMM tiles start at 0
     for (int jb = blockIdx.x * blockDim.x + threadIdx.x; jb < rows / b; jb += gridDim.x * blockDim.x)
         done[jb] = 0;
@@ -558,7 +577,9 @@ __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, co
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int rho = static_cast<int>(i / d8), c = static_cast<int>(i - static_cast<int64_t>(rho) * d8);
-        const int r = sorted[rho];
+        int r = sorted[rho];
+        if (!MOE_IN_BOUNDS(r >= 0 && r <= MK, dev_status))
+            r = MK;                                   // read as padding
         uint4 out = make_uint4(0, 0, 0, 0);
         if (r < MK) {
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(r / k) * d) + c);
@@ -653,18 +674,19 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     const int gblocks = grouped_sm_count() * 4;
     const cudaError_t ge =
         x_bf16 ? launch_pdl(gather_kernel<__nv_bfloat16>, dim3(gblocks), dim3(256), 0, s,
-                            static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk), sorted, npp, xg, b, done)
+                            static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk), sorted, npp, xg, b, done,
+                            cap_rows, dev_status)
                : launch_pdl(gather_kernel<__half>, dim3(gblocks), dim3(256), 0, s, static_cast<const __half *>(x), d, k,
-                            static_cast<int>(mk), sorted, npp, xg, b, done);
+                            static_cast<int>(mk), sorted, npp, xg, b, done, cap_rows, dev_status);
     if (ge != cudaSuccess)
         return MOE_ERR_CUDA;
     const int grid = grouped_sm_count();
     Args a1{static_cast<const uint16_t *>(w13->scale), static_cast<const int32_t *>(w13->zero), expert_ids, npp, sorted,
             wts, hg, nullptr, dev_status, b, n_mma, I / 128, d / 128, I, d, static_cast<int>(mk), 2 * I, G1, stages,
-            aslots, acc_cols, nbuf};
+            aslots, acc_cols, nbuf, E, cap_rows / b};
     Args a2{static_cast<const uint16_t *>(w2->scale), static_cast<const int32_t *>(w2->zero), expert_ids, npp, sorted,
             wts, nullptr, yr, dev_status, b, n_mma, d / 256, I / 128, I, d, static_cast<int>(mk), d, G2, stages,
-            aslots, acc_cols, nbuf};
+            aslots, acc_cols, nbuf, E, cap_rows / b};
     if (launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, tQ2, tB2, a1, a2, done, Gmax) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
