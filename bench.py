@@ -200,7 +200,7 @@ SRC_FILES = {
     "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh",
                 "attr.h"),
     "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
-    "awq_decode": ("decode.cu", "decode_internal.h", "common.cuh", "tc.cuh", "attr.h"),
+    "awq_decode": ("decode.cu", "decode_pipe_awq.cu", "decode_internal.h", "common.cuh", "tc.cuh", "attr.h"),
 }
 
 
@@ -280,6 +280,8 @@ class Step:
                 moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), q2[e], s2[e])
             w0 = ((q13, s13, None), (q2, s2, None))
         self.routed_in_layer = not self.awq and path == "decode" and M == 1 and E <= 768
+        # one AWQ token: the layer is one kernel (the routing is fixed, so it is not in it)
+        self.awq_pipe = self.awq and path == "decode" and M == 1
         lw_bytes = sum(t.numel() * t.element_size() for p in w0 for t in p if t is not None)
         self.ids_host = [self._host_ids(j) for j in range(n_inputs)]
         est = max(step_bytes(wl, ids) for ids in self.ids_host[:8])
@@ -420,6 +422,8 @@ class Step:
     def layer_kernels(self) -> str:
         if self.awq and self.path == "grouped":
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
+        if self.awq_pipe:
+            return "moe_ffn_decode (AWQ-4bit): dpa::pipe_kernel (gate/up + SwiGLU + down + weighted sum), one kernel"
         if self.awq:
             return "moe_ffn_decode (AWQ-4bit): decode_gate_up_kernel<AWQ> + decode_down_kernel<AWQ>"
         if self.path == "grouped":
@@ -434,6 +438,9 @@ class Step:
         if self.awq and self.path == "grouped":
             return ("expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
                     "dequantized in shared memory + combine, b=%d), fixed routing" % self.b)
+        if self.awq_pipe:
+            return ("single-token AWQ decode: gate/up + SwiGLU + down in one kernel, h exchanged through L2, "
+                    "fixed routing")
         if self.awq:
             return "output-centric AWQ decode (gate/up + down on CUDA cores), fixed routing"
         if self.path == "grouped":
@@ -448,7 +455,7 @@ class Step:
             # (top-k), alignment, act-quant or gather, the GEMM kernel, combine
             return (0 if self.awq else 1) + na + 3
         if self.awq:
-            return 2
+            return 1 if self.awq_pipe else 2
         return 1 if self.routed_in_layer else 3
 
 

@@ -362,7 +362,10 @@ moe_status_t moe_ffn_grouped_batched(const void *x, int32_t xdt, int32_t M, int3
  *                against grouped 27.8 us at M = 1; grouped 41.5 against
  *                179 us at M = 4 and faster at every larger M; at d = 7168,
  *                I = 2048, M = 1, grouped 80.9 against 250 us);
- *   MOE_W_AWQ4:  MOE_PATH_GROUPED (35.0 against 38.0 us at M = 1).
+ *   MOE_W_AWQ4:  MOE_PATH_DECODE for M <= 1 where the single-kernel AWQ
+ *                decode is built for (k, d, I) (d = 1024, I = 256 or 512;
+ *                d = 2048, I = 512 or 768), else MOE_PATH_GROUPED (14.7
+ *                against 34.3 us at M = 1 on the decode shapes).
  * When the preferred path does not take the shape (the limits of
  * moe_ffn_decode and moe_ffn_grouped on d, I and k), the other one is
  * returned; when neither does, MOE_ERR_UNSUPPORTED.

@@ -142,9 +142,9 @@ def test_python_layout_helper_matches_library():
 
 
 def test_select_path_at_the_measured_crossover(L):
-    """Path choice (host only): MXFP8 takes the output-centric path for one
-    token where its single-kernel form is built and the grouped path
-    otherwise; 4-bit AWQ takes the grouped path.  The block size is twice
+    """Path choice (host only): one token takes the output-centric path
+    where its single-kernel form is built for the format (MXFP8 or 4-bit
+    AWQ), and the grouped path otherwise.  The block size is twice
     the expected rows per expert rounded up to a power of two within the
     format's range."""
     D, G = moe.MOE_PATH_DECODE, moe.MOE_PATH_GROUPED
@@ -156,7 +156,8 @@ def test_select_path_at_the_measured_crossover(L):
                                                                  (G, 128)]
     assert sel(0) == (D, 0)                                  # an empty batch: the cheap path
     # AWQ: grouped at every M; fixture A (M=21, k=8, E=128) gets b = 8
-    assert sel(1, awq) == (G, 8) and sel(21, awq) == (G, 8) and sel(512, awq) == (G, 64)
+    assert sel(1, awq) == (D, 0) and sel(21, awq) == (G, 8) and sel(512, awq) == (G, 64)
+    assert sel(1, awq, d=3072, I=256) == (G, 8)              # no single-kernel AWQ form at this shape
     # shapes one path does not take go to the other
     assert sel(1, d=1152, I=384) == (G, 16)                  # decode needs d % 512 == 0
     # one token takes the decode path only where its single-kernel form is

@@ -275,6 +275,9 @@ def test_awq_single_token_routes_repeats_and_barrier_counter():
     for y in ys[1:]:
         assert torch.equal(y, ys[0])                              # repeats are bit-identical
     gs.assert_layer_close(ys[0], oracle_awq(layer, x, ids, w))
+    # the one-kernel path ran: one count per CTA (one CTA per SM) per call
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ws[:8].view(torch.int64).item() == 3 * sms
     # no valid route: y = 0
     y0 = run_awq(layer, x, np.array([[-1, wl.E, 99, -5]], dtype=np.int32), w, ws=ws)
     torch.cuda.synchronize()
@@ -394,3 +397,21 @@ def test_nvfp4s_decode_matches_oracle(xdt):
                             out_dtype=torch.float32)
     assert torch.equal(y1[0], moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
                                                  w13, w2, out_dtype=torch.float32)[0])
+
+
+@pytest.mark.parametrize("xdt", [torch.float16, torch.bfloat16])
+def test_awq_decode_logits_equals_topk_then_decode(xdt):
+    """4-bit AWQ, one token: moe_ffn_decode_logits routes inside the one
+    kernel and gives, bit for bit, moe_topk_softmax followed by
+    moe_ffn_decode, with the same routing written out."""
+    wl = AWQ_M1
+    layer = awq_layer(wl)
+    x = inputs.activations(wl, dtype=xdt).cuda()
+    logits = torch.from_numpy(inputs.router_logits(wl)).cuda()
+    y1, ids1, w1 = moe.moe_ffn_decode_logits(logits, x, wl.k, layer.w13, layer.w2, out_dtype=torch.float32)
+    ids2, w2 = moe.moe_topk_softmax(logits, wl.k)
+    y2 = moe.moe_ffn_decode(x, ids2, w2, layer.w13, layer.w2, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(ids1, ids2) and torch.equal(w1, w2)
+    assert torch.equal(y1, y2)
+    gs.assert_layer_close(y1, oracle_awq(layer, x.cpu(), ids2.cpu().numpy(), w2.cpu().numpy()))

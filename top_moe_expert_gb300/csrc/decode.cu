@@ -400,6 +400,12 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
                                   static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
                                   static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status, s);
     }
+    if (fmt == MOE_W_AWQ4 && decode_pipe_awq_eligible(M, k, d, I, w13->E) && aligned(w13->q, 16) &&
+        aligned(w2->q, 16) && aligned(w13->scale, 16) && aligned(w13->zero, 16)) {
+        // one token, 4-bit AWQ: one kernel (gate/up, SwiGLU, down)
+        return decode_pipe_awq_launch(x, xdt == MOE_BF16, d, I, w13->E, topk_ids, topk_w, nullptr, nullptr, nullptr, k,
+                                      w13, w2, y, ydt == MOE_FP32, ws, dev_status, s);
+    }
     if (fmt == MOE_W_MXFP8 && decode_stream_eligible(M, k, d, I, w13->E, w13->q, w13->scale, w2->q, w2->scale)) {
         const moe_status_t st2 = decode_stream_launch(static_cast<const __nv_bfloat16 *>(x), M, d, I, w13->E, topk_ids, topk_w, k,
                                     static_cast<const uint8_t *>(w13->q), static_cast<const uint8_t *>(w13->scale),
@@ -449,6 +455,20 @@ MOE_API moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, i
                                   static_cast<const uint8_t *>(w13->scale), static_cast<const uint8_t *>(w2->q),
                                   static_cast<const uint8_t *>(w2->scale), y, ydt == MOE_FP32, ws, dev_status,
                                   as_stream(stream));
+    }
+    // one token, 4-bit AWQ: one kernel with the routing inside
+    if (M == 1 && w2->fmt == MOE_W_AWQ4 && w13->fmt == MOE_W_AWQ4 && (xdt == MOE_BF16 || xdt == MOE_FP16) &&
+        (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
+        check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_pipe_awq_eligible(1, k, d, I, E) &&
+        decode_pipe_awq_route_eligible(E, k) && aligned(w13->q, 16) && aligned(w2->q, 16) &&
+        aligned(w13->scale, 16) && aligned(w13->zero, 16) && x && y &&
+        aligned(x, 16)) {
+        size_t need;
+        moe_ffn_decode_workspace_size(M, k, d, I, &need);
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return MOE_ERR_WORKSPACE;
+        return decode_pipe_awq_launch(x, xdt == MOE_BF16, d, I, E, nullptr, nullptr, logits, topk_ids, topk_w, k,
+                                      w13, w2, y, ydt == MOE_FP32, ws, dev_status, as_stream(stream));
     }
     // otherwise: routing, then the layer
     moe_status_t st = moe_topk_softmax(logits, M, E, k, topk_ids, topk_w, stream);

@@ -34,10 +34,22 @@ bool decode_pipe_eligible(int M, int k, int d, int I, int E);
 // the shape check alone, for a grid of G CTAs (host only, no device query)
 bool decode_pipe_shape_fits(int k, int d, int I, int G);
 bool decode_pipe_route_eligible(int E, int k);
+// the failure-detection hook's flag (moe_debug_exchange_stall), read at launch
+int decode_exchange_stall();
 moe_status_t decode_pipe_launch(const __nv_bfloat16 *x, int d, int I, int E, const int32_t *ids, const float *wts,
                                 const float *logits, int32_t *ids_out, float *wts_out, int k, const uint8_t *q13,
                                 const uint8_t *s13, const uint8_t *q2, const uint8_t *s2, void *y, bool y_f32,
                                 void *ws, int32_t *dev_status, cudaStream_t stream);
+
+// single-token 4-bit AWQ layer in one kernel (decode_pipe_awq.cu), the same
+// structure and workspace use as decode_pipe.cu; x fp16 or bf16
+bool decode_pipe_awq_shape_fits(int k, int d, int I, int G);
+bool decode_pipe_awq_eligible(int M, int k, int d, int I, int E);
+bool decode_pipe_awq_route_eligible(int E, int k);
+moe_status_t decode_pipe_awq_launch(const void *x, bool x_bf16, int d, int I, int E, const int32_t *ids,
+                                    const float *wts, const float *logits, int32_t *ids_out, float *wts_out, int k,
+                                    const moe_weights_t *w13, const moe_weights_t *w2, void *y, bool y_f32, void *ws,
+                                    int32_t *dev_status, cudaStream_t s);
 
 // paired 4:8 sparse NVFP4 decode (decode_nvfp4s.cu): a gate/up kernel and a
 // down kernel, h [M*k][I] f32 in `h`

@@ -720,6 +720,8 @@ inline bool shape_ok(int d, int I)
 // lets a test exercise the failure path without faulting or hanging the GPU.
 static std::atomic<int> g_stall{0};
 
+int decode_exchange_stall() { return g_stall.load(std::memory_order_relaxed); }
+
 bool decode_pipe_shape_fits(int k, int d, int I, int G)
 {
     return k >= 1 && k <= dp::kMaxK && G >= 1 && dp::shape_ok(d, I) && dp::Plan{d, I, k, G}.fits();

@@ -15,8 +15,9 @@
 // At M = 1 the decode figure is the single-kernel form, built for a few
 // (d, I) pairs; elsewhere the decode path runs its two-kernel form, which
 // loses to the grouped path at every M measured (at d = 7168, I = 2048,
-// E = 384, M = 1: 250 us against 80.9 us).  For 4-bit AWQ the grouped path
-// is ahead at one token (35.0 against 38.0 us) and far ahead at M = 21.
+// E = 384, M = 1: 250 us against 80.9 us).  For 4-bit AWQ the single-token
+// kernel is ahead at one token (14.7 against 34.3 us for the grouped path)
+// and the grouped path from two tokens (far ahead at M = 21).
 // Host only: nothing here touches a GPU.
 #include "common.cuh"
 #include "decode_internal.h"
@@ -63,9 +64,10 @@ MOE_API moe_status_t moe_ffn_select_path(int32_t M, int32_t k, int32_t E, int32_
     if (fmt == MOE_W_AWQ4 && d > 8064 && b > 64)
         b = 64;
     const bool dec = decode_shape_ok(k, d, I, fmt), grp = grouped_shape_ok(d, I, b, fmt);
-    // MXFP8: the output-centric path for one token where its single-kernel
-    // form is built; AWQ: the grouped path
-    const bool want_decode = fmt == MOE_W_MXFP8 && M <= 1 && decode_pipe_shape_fits(k, d, I, kSelectSMs);
+    // the output-centric path for one token where its single-kernel form is
+    // built for the format; the grouped path otherwise
+    const bool want_decode = M <= 1 && (fmt == MOE_W_MXFP8 ? decode_pipe_shape_fits(k, d, I, kSelectSMs)
+                                                           : decode_pipe_awq_shape_fits(k, d, I, kSelectSMs));
     if (want_decode ? dec : !grp) {
         if (!dec)
             return MOE_ERR_UNSUPPORTED;
