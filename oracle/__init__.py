@@ -109,6 +109,15 @@ def _load():
                 ctypes.POINTER(_Weights), ctypes.POINTER(_Weights), ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_void_p]
+            lib.orc_nvfp4_act_quantize.restype = None
+            lib.orc_nvfp4_act_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                                   ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+            lib.orc_moe_layer_a4.restype = ctypes.c_int
+            lib.orc_moe_layer_a4.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                ctypes.POINTER(_Weights), ctypes.POINTER(_Weights), ctypes.c_float, ctypes.c_float,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             lib.orc_num_threads.restype = ctypes.c_int
             lib.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -207,6 +216,29 @@ def nvfp4s_quantize_3d(W) -> dict:
     return {"fmt": "nvfp4s", "v": np.stack([p["v"] for p in parts]), "m": np.stack([p["m"] for p in parts]),
             "s": np.stack([p["s"] for p in parts]),
             "alpha": np.array([p["alpha"] for p in parts], dtype=np.float32)}
+
+
+def nvfp4_act_quantize(v, alpha: float) -> tuple[np.ndarray, np.ndarray]:
+    """Run-time activation quantizer Q_a [SQ Sec. 3.4, App. D.1, Eq. 5] of
+    v [rows, K] (taken as binary32, K % 32 == 0) with the tensor-wide scale
+    alpha: E2M1 codes [rows, K] (one per byte) and UE4M3 block scales
+    [rows, K/32]; the decisions are binary32 (see moe_oracle.c)."""
+    lib = _load()
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    rows, K = v.shape
+    assert K % 32 == 0 and alpha > 0
+    codes = np.empty((rows, K), dtype=np.uint8)
+    scales = np.empty((rows, K // 32), dtype=np.uint8)
+    lib.orc_nvfp4_act_quantize(_ptr(v), rows, K, ctypes.c_float(alpha), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def nvfp4_act_values(codes, scales) -> np.ndarray:
+    """S * E2M1(code) per element (the quantized activation without its
+    tensor-wide scale alpha), exact in binary64."""
+    codes = np.asarray(codes)
+    rows, K = codes.shape
+    return e2m1_value(codes) * np.repeat(ue4m3_value(scales), 32, axis=1)[:, :K]
 
 
 def mxfp8_quantize(v) -> tuple[np.ndarray, np.ndarray]:
@@ -437,3 +469,36 @@ def moe_layer(x, ids, w, E: int, w13: dict, w2: dict, mode: int = MODE_EXACT,
     if rc != 0:
         raise KeyError("a routed expert's weights were not supplied")
     return {"y": y, "h": h, "hq": hq, "hs": hs}
+
+
+def moe_layer_a4(x, ids, w, E: int, w13: dict, w2: dict, alpha_x: float, alpha_h: float,
+                 hv_in=None, want_xv: bool = False, want_h: bool = False, want_hv: bool = False):
+    """Routed expert-FFN layer with NVFP4-quantized activations, the W4A4
+    grouped path [SQ Sec. 3.4, App. D.1]: Q_a(x; alpha_x) before the first
+    projection, Q_a(h; alpha_h) before the second, exact weights, binary64
+    sums.  Returns dict(y [M,d], xv [M,d]?, h [M*k,I]?, hv [M*k,I]?), xv / hv
+    the quantized values without alpha; hv_in replaces the oracle's own
+    Q_a(h) (stage-wise check)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    M, d = x.shape
+    k = ids.shape[1]
+    keep = []
+    s13 = _weights_struct(w13, E, keep)
+    s2 = _weights_struct(w2, E, keep)
+    I = s2.K
+    assert s13.N == 2 * I and s13.K == d and s2.N == d and d % 32 == 0 and I % 32 == 0
+    y = np.empty((M, d), dtype=np.float64)
+    xv = np.empty((M, d), dtype=np.float64) if want_xv else None
+    h = np.empty((M * k, I), dtype=np.float64) if want_h else None
+    hv = np.empty((M * k, I), dtype=np.float64) if want_hv else None
+    if hv_in is not None:
+        hv_in = np.ascontiguousarray(hv_in, dtype=np.float64).reshape(M * k, I)
+    rc = lib.orc_moe_layer_a4(_ptr(x), M, d, I, _ptr(ids), _ptr(w), k, E, ctypes.byref(s13), ctypes.byref(s2),
+                              ctypes.c_float(alpha_x), ctypes.c_float(alpha_h), _ptr(y), _ptr(xv), _ptr(h),
+                              _ptr(hv_in), _ptr(hv))
+    if rc != 0:
+        raise KeyError("a routed expert's weights were not supplied")
+    return {"y": y, "xv": xv, "h": h, "hv": hv}

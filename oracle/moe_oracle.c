@@ -364,6 +364,61 @@ void orc_nvfp4s_quantize(const double *W, int64_t N, int64_t K, uint8_t *vals, u
     free(keep);
 }
 
+/* Run-time activation quantizer Q_a onto NVFP4 with 32-element scale blocks
+ * ([SQ] Sec. 3.4 and App. D.1: expert activations are quantized at run time
+ * into 32-element blocks, each with one UE4M3 scale, before the first GEMM
+ * and again after SwiGLU; the block scale follows Eq. 5).  Reading: Eq. 5's
+ * tensor-wide factor gamma is 1 / alpha with alpha the activation's
+ * tensor-wide scale, a constant of the layer (App. D.1 folds the tensor-wide
+ * scales of both operands into one factor alpha_e per expert, so alpha does
+ * not change from batch to batch).  The page does not fix the precision of
+ * the rounding decisions; they are taken in binary32, in this order:
+ *   r6   = binary32(1 / (6 alpha))              the quotient in binary64, rounded once
+ *   t    = binary32(amax * r6)                  amax = max |v| over the block
+ *   s    = t rounded to nearest (ties to even) onto UE4M3, saturating at 448
+ *   S    = UE4M3(s); when S = 0 every magnitude code is 0
+ *   q    = binary32(1 / binary32(alpha * S))
+ *   code = sign bit of v | |binary32(v * q)| rounded to nearest (ties to
+ *          even) onto the E2M1 magnitudes, saturating at 6
+ * The activation it stands for is alpha * S * E2M1(code).
+ * v: [rows][K] binary32 (K a multiple of 32); codes: [rows][K] one E2M1 code
+ * per byte; scales: [rows][K/32] UE4M3 codes. */
+void orc_nvfp4_act_quantize(const float *v, int64_t rows, int64_t K, float alpha, uint8_t *codes,
+                            uint8_t *scales)
+{
+    const float r6 = (float)(1.0 / (6.0 * (double)alpha));
+    int64_t r;
+    for (r = 0; r < rows; ++r) {
+        int64_t blk, i;
+        for (blk = 0; blk < K / 32; ++blk) {
+            const float *vb = v + r * K + blk * 32;
+            float amax = 0.0f, t, S, q = 0.0f;
+            uint8_t s;
+            for (i = 0; i < 32; ++i)
+                if (fabsf(vb[i]) > amax)
+                    amax = fabsf(vb[i]);
+            t = amax * r6;
+            s = e4m3_rne_magnitude((double)t);
+            scales[r * (K / 32) + blk] = s;
+            S = (float)orc_ue4m3_value(s);
+            if (S > 0.0f) {
+                const float p = alpha * S;
+                q = 1.0f / p;
+            }
+            for (i = 0; i < 32; ++i) {
+                uint8_t c = 0;
+                if (S > 0.0f) {
+                    const float u = vb[i] * q;
+                    c = e2m1_rne_magnitude((double)fabsf(u));
+                }
+                if (signbit(vb[i]))
+                    c = (uint8_t)(c | 0x8);
+                codes[r * K + blk * 32 + i] = c;
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Expert weights                                                            */
 /* ------------------------------------------------------------------------ */
@@ -682,6 +737,93 @@ int orc_moe_layer(const double *x, int64_t M, int64_t d, int64_t I,
             }
         }
         free(xt); free(row); free(h); free(hx);
+    }
+    return err;
+}
+
+/* The routed expert-FFN layer with NVFP4-quantized activations, the W4A4
+ * grouped path of [SQ] (Sec. 3.4, App. D.1): x is quantized by Q_a with the
+ * constant alpha_x before the first projection, h = SiLU(g) * u by Q_a with
+ * alpha_h before the second; the weights (any format; paired 4:8 sparse
+ * NVFP4 on that path) are dequantized exactly, per-expert constant included.
+ *   x      : [M][d] activation values, taken as binary32
+ *   xv_out : optional [M][d], S * E2M1(code) of Q_a(x) (without alpha_x)
+ *   h_out  : optional [M*k][I], h before quantization (binary64)
+ *   hv_in  : optional [M*k][I], S * E2M1(code) values that replace the
+ *            oracle's own Q_a(h) (stage-wise check of the second projection)
+ *   hv_out : optional [M*k][I], S * E2M1(code) of the oracle's own Q_a(h),
+ *            h rounded to binary32 first (the decisions are binary32)
+ * Otherwise as orc_moe_layer: y[t] = sum_j w[t][j] * W2_{e_j} . (alpha_h hv),
+ * binary64 sums; routes outside [0,E) contribute nothing; rows of invalid
+ * routes in h_out / hv_out are 0.  Returns 0, or -1 if a routed expert's
+ * weights were not supplied. */
+int orc_moe_layer_a4(const double *x, int64_t M, int64_t d, int64_t I,
+                     const int32_t *ids, const double *w, int32_t k, int32_t E,
+                     const orc_weights *w13, const orc_weights *w2, float alpha_x, float alpha_h,
+                     double *y, double *xv_out, double *h_out, const double *hv_in, double *hv_out)
+{
+    int64_t t;
+    int err = 0;
+    for (t = 0; t < M * d; ++t)
+        y[t] = 0.0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (t = 0; t < M; ++t) {
+        float *xf = (float *)malloc(sizeof(float) * (size_t)d);
+        float *hf = (float *)malloc(sizeof(float) * (size_t)I);
+        uint8_t *cd = (uint8_t *)malloc((size_t)(d > I ? d : I));
+        uint8_t *sc = (uint8_t *)malloc((size_t)((d > I ? d : I) / 32));
+        double *xt = (double *)malloc(sizeof(double) * (size_t)d);
+        double *row = (double *)malloc(sizeof(double) * (size_t)(d > I ? d : I));
+        double *h = (double *)malloc(sizeof(double) * (size_t)I);
+        double *hx = (double *)malloc(sizeof(double) * (size_t)I);
+        int32_t j;
+        int64_t n, o, kk;
+        for (kk = 0; kk < d; ++kk)
+            xf[kk] = (float)x[t * d + kk];
+        orc_nvfp4_act_quantize(xf, 1, d, alpha_x, cd, sc);
+        for (kk = 0; kk < d; ++kk) {
+            const double v = orc_e2m1_value(cd[kk]) * orc_ue4m3_value(sc[kk / 32]);
+            if (xv_out)
+                xv_out[t * d + kk] = v;
+            xt[kk] = (double)alpha_x * v;
+        }
+        for (j = 0; j < k; ++j) {
+            int64_t r = t * k + j;
+            int32_t e = ids[r];
+            if (e < 0 || e >= E) {
+                for (n = 0; n < I; ++n) {
+                    if (h_out) h_out[r * I + n] = 0.0;
+                    if (hv_out) hv_out[r * I + n] = 0.0;
+                }
+                continue;
+            }
+            for (n = 0; n < I; ++n) {
+                double g = 0.0, u = 0.0;
+                if (orc_dequant_row(w13, e, n, row)) { err = -1; break; }
+                for (kk = 0; kk < d; ++kk) g += row[kk] * xt[kk];
+                if (orc_dequant_row(w13, e, I + n, row)) { err = -1; break; }
+                for (kk = 0; kk < d; ++kk) u += row[kk] * xt[kk];
+                h[n] = silu(g) * u;
+            }
+            if (h_out)
+                memcpy(h_out + r * I, h, sizeof(double) * (size_t)I);
+            if (hv_in) {
+                for (n = 0; n < I; ++n) hx[n] = hv_in[r * I + n];
+            } else {
+                for (n = 0; n < I; ++n) hf[n] = (float)h[n];
+                orc_nvfp4_act_quantize(hf, 1, I, alpha_h, cd, sc);
+                for (n = 0; n < I; ++n) hx[n] = orc_e2m1_value(cd[n]) * orc_ue4m3_value(sc[n / 32]);
+            }
+            if (hv_out)
+                memcpy(hv_out + r * I, hx, sizeof(double) * (size_t)I);
+            for (o = 0; o < d; ++o) {
+                double acc = 0.0;
+                if (orc_dequant_row(w2, e, o, row)) { err = -1; break; }
+                for (n = 0; n < I; ++n) acc += row[n] * ((double)alpha_h * hx[n]);
+                y[t * d + o] += w[r] * acc;
+            }
+        }
+        free(xf); free(hf); free(cd); free(sc); free(xt); free(row); free(h); free(hx);
     }
     return err;
 }
