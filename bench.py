@@ -72,6 +72,11 @@ def workload_from_name(name: str):
     if name == "probe_m16384":
         return inputs.Workload("grouped_probe_m16384_d2048_i768_e128_k8", M=16384, d=2048, I=768, E=128, k=8,
                                seed=2)
+    if name.startswith("nv4_m"):
+        # paired 4:8 sparse NVFP4 weights (random admissible packing) at the sweep's shapes
+        M = int(name[len("nv4_m"):])
+        return inputs.Workload(f"nv4_m{M}_uniform_d2048_i768_e128_k8", M=M, d=2048, I=768, E=128, k=8,
+                               fmt="nvfp4s", seed=2)
     if name.startswith("sweep_m"):
         rest = name[len("sweep_m"):]
         routing = "zipf" if rest.endswith("_zipf") else "uniform"
@@ -79,29 +84,34 @@ def workload_from_name(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
-def expert_bytes(wl) -> int:
+def expert_bytes(wl, path: str = "decode") -> int:
     """Weight bytes of one expert.  MXFP8: 3*I*d codes + 3*I*d/32 scale
     bytes.  AWQ-4bit: 3*I*d/2 packed values + an fp16 scale and a 4-bit zero
-    per 128 values."""
+    per 128 values.  NVFP4S: 3*I*d/4 bytes of kept codes, plus 3*I*d/16
+    pattern and 3*I*d/32 scale bytes (decode path) or the grouped path's
+    16-byte side record per 128 weights (3*I*d/8), plus the expert's fp32
+    constant (decode) or two per-expert factors (grouped)."""
+    n = 3 * wl.I * wl.d
     if wl.fmt == "awq4":
-        n = 3 * wl.I * wl.d
         return n // 2 + n // 128 * 2 + n // 128 // 2
-    return 3 * wl.I * wl.d * 33 // 32
+    if wl.fmt == "nvfp4s":
+        return n // 4 + (n // 8 + 8 if path == "grouped" else n // 16 + n // 32 + 4)
+    return n * 33 // 32
 
 
-def layer_bytes(wl, ids: np.ndarray) -> int:
+def layer_bytes(wl, ids: np.ndarray, path: str = "decode") -> int:
     """Algorithmic bytes of one layer call: distinct routed experts' weights,
     x and the routing (ids, weights) read, y written (bf16)."""
     distinct = len(np.unique(ids[(ids >= 0) & (ids < wl.E)]))
-    return distinct * expert_bytes(wl) + wl.M * wl.d * 2 + wl.M * wl.k * 8 + wl.M * wl.d * 2
+    return distinct * expert_bytes(wl, path) + wl.M * wl.d * 2 + wl.M * wl.k * 8 + wl.M * wl.d * 2
 
 
-def step_bytes(wl, ids: np.ndarray) -> int:
+def step_bytes(wl, ids: np.ndarray, path: str = "decode") -> int:
     """Algorithmic bytes of one step: distinct routed experts' weights, the
     activations read (x, router logits) and the output written (bf16 y)."""
     distinct = len(np.unique(ids[(ids >= 0) & (ids < wl.E)]))
     routing = wl.M * wl.k * 8 if wl.routing == "fixture_a" else wl.M * wl.E * 4   # fixed ids/w, or logits
-    return distinct * expert_bytes(wl) + wl.M * wl.d * 2 + routing + wl.M * wl.d * 2
+    return distinct * expert_bytes(wl, path) + wl.M * wl.d * 2 + routing + wl.M * wl.d * 2
 
 
 def measured_mxfp8_tflops():
@@ -201,6 +211,10 @@ SRC_FILES = {
                 "attr.h"),
     "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
     "awq_decode": ("decode.cu", "decode_pipe_awq.cu", "decode_internal.h", "common.cuh", "tc.cuh", "attr.h"),
+    "nv4": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh",
+            "tc.cuh", "attr.h"),
+    "nv4_decode": ("decode.cu", "decode_nvfp4s.cu", "nvfp4s.cuh", "decode_internal.h", "topk.cu", "topk.cuh",
+                   "common.cuh", "attr.h"),
 }
 
 
@@ -260,6 +274,7 @@ class Step:
         from top_moe_expert_gb300 import inputs
         self.moe, self.wl, self.dev, self.path = moe, wl, device, path
         self.awq = wl.fmt == "awq4"
+        self.nv4 = wl.fmt == "nvfp4s"
         E, d, I, M, k = wl.E, wl.d, wl.I, wl.M, wl.k
         self.n_inputs = n_inputs
         # ---- layer 0's weights
@@ -270,6 +285,12 @@ class Step:
             w0 = ((dev_t(q13), dev_t(s13).view(torch.float16), dev_t(z13)),
                   (dev_t(q2), dev_t(s2).view(torch.float16), dev_t(z2)))
             del q13, s13, z13, q2, s2, z2
+        elif self.nv4:
+            dev_t = lambda a: torch.from_numpy(a).to(device)
+            v13, m13, c13, a13 = inputs.nvfp4s_weights(wl, "w13")
+            v2, m2, c2, a2 = inputs.nvfp4s_weights(wl, "w2")
+            w0 = ((dev_t(v13), dev_t(c13), dev_t(m13), dev_t(a13)), (dev_t(v2), dev_t(c2), dev_t(m2), dev_t(a2)))
+            del v13, m13, c13, v2, m2, c2
         else:
             q13 = torch.empty((E, 2 * I, d), dtype=torch.uint8, device=device)
             s13 = torch.empty((E, 2 * I, d // 32), dtype=torch.uint8, device=device)
@@ -279,18 +300,28 @@ class Step:
                 moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w13", e, device), q13[e], s13[e])
                 moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), q2[e], s2[e])
             w0 = ((q13, s13, None), (q2, s2, None))
-        self.routed_in_layer = not self.awq and path == "decode" and M == 1 and E <= 768
+        self.routed_in_layer = wl.fmt == "mxfp8" and path == "decode" and M == 1 and E <= 768
         # one AWQ token: the layer is one kernel (the routing is fixed, so it is not in it)
         self.awq_pipe = self.awq and path == "decode" and M == 1
         lw_bytes = sum(t.numel() * t.element_size() for p in w0 for t in p if t is not None)
         self.ids_host = [self._host_ids(j) for j in range(n_inputs)]
-        est = max(step_bytes(wl, ids) for ids in self.ids_host[:8])
+        est = max(step_bytes(wl, ids, path) for ids in self.ids_host[:8])
         self.L = layers if layers > 0 else layer_copies(wl, est, lw_bytes)
         self.layer_weight_bytes = lw_bytes
         self.layers = []
+        # NVFP4S grouped path: the layer's activation scales (constants of the
+        # layer): alpha_x from the largest |x| of the inputs, alpha_h for |h|
+        # up to 16 (the weights' RMS and N(0,1) inputs give |g|, |u| ~ 1)
+        self.alpha_x = self.alpha_h = None
         for l in range(self.L):
-            (a13, b13, c13), (a2, b2, c2) = w0 if l == 0 else tuple(
-                tuple(t.clone() if t is not None else None for t in p) for p in w0)
+            parts = w0 if l == 0 else tuple(tuple(t.clone() if t is not None else None for t in p) for p in w0)
+            if self.nv4:
+                (v13_, c13_, m13_, a13_), (v2_, c2_, m2_, a2_) = parts
+                w13 = moe.Weights(moe.MOE_W_NVFP4S, v13_, c13_, m13_, a13_)
+                w2 = moe.Weights(moe.MOE_W_NVFP4S, v2_, c2_, m2_, a2_)
+                self.layers.append([w13, w2, (None, None)])
+                continue
+            (a13, b13, c13), (a2, b2, c2) = parts
             if self.awq:
                 w13 = moe.Weights(moe.MOE_W_AWQ4, a13, b13, c13)
                 w2 = moe.Weights(moe.MOE_W_AWQ4, a2, b2, c2)
@@ -317,6 +348,12 @@ class Step:
         self.x = self.io[:xb].view(self.x_all.dtype).view(M, d)
         self.logits = (torch.empty((M, E), dtype=torch.float32, device=device) if self.awq
                        else self.io[xb:].view(torch.float32).view(M, E))
+        if self.nv4 and path == "grouped":
+            self.alpha_x = float(self.x_all.abs().max().item()) / (6 * 448)
+            self.alpha_h = 16.0 / (6 * 448)
+            for lay in self.layers:
+                lay[2] = moe.moe_grouped_prepare_nvfp4s(lay[0], lay[1], self.alpha_x, self.alpha_h)
+        self.layers = [tuple(l) for l in self.layers]
         self.io_host = ("x_host",) if self.awq else ("x_host", "logits_host")
         self.y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
         if self.awq:
@@ -416,12 +453,17 @@ class Step:
 
     def bytes_of(self, i0: int, n: int, layer_only: bool = False) -> float:
         f = layer_bytes if (layer_only and not self.routed_in_layer) else step_bytes
-        return float(sum(f(self.wl, self.step_ids(i)) for i in range(i0, i0 + n)))
+        return float(sum(f(self.wl, self.step_ids(i), self.path) for i in range(i0, i0 + n)))
 
     # ---- descriptions
     def layer_kernels(self) -> str:
         if self.awq and self.path == "grouped":
             return "moe_ffn_grouped (AWQ-4bit): ga::gather + ga::gemm_kernel (both GEMMs, one persistent kernel) + combine"
+        if self.nv4 and self.path == "grouped":
+            return ("moe_ffn_grouped (NVFP4S, W4A4): ga::gather_nv4_kernel (Q_a of x) + ga::gemm_kernel<Nv4> "
+                    "(both GEMMs, weights expanded on chip, Q_a of h in the epilogue) + combine")
+        if self.nv4:
+            return "moe_ffn_decode (NVFP4S): dn4::gate_up_kernel + dn4::down_kernel"
         if self.awq_pipe:
             return "moe_ffn_decode (AWQ-4bit): dpa::pipe_kernel (gate/up + SwiGLU + down + weighted sum), one kernel"
         if self.awq:
@@ -438,6 +480,11 @@ class Step:
         if self.awq and self.path == "grouped":
             return ("expert-centric grouped AWQ (align + gather + tcgen05 kind::f16 GEMM1/GEMM2 on weights "
                     "dequantized in shared memory + combine, b=%d), fixed routing" % self.b)
+        if self.nv4 and self.path == "grouped":
+            return ("expert-centric grouped NVFP4S W4A4 (topk + align + Q_a gather + tcgen05 kind::f16 GEMM1/GEMM2 "
+                    "on weights expanded in tensor memory + combine, b=%d)" % self.b)
+        if self.nv4:
+            return "output-centric NVFP4S decode (topk + gate/up + down, activations kept exact)"
         if self.awq_pipe:
             return ("single-token AWQ decode: gate/up + SwiGLU + down in one kernel, h exchanged through L2, "
                     "fixed routing")
@@ -477,7 +524,8 @@ def roofline_obj(st, wl, total_ms, K, total_bytes, world):
     t_hbm = total_bytes / (peak_gbs * 1e9)
     t_mma = flops / (peak_tf * 1e12)
     kern = st.layer_kernels()
-    src = ("awq" if st.path == "grouped" else "awq_decode") if st.awq else st.path
+    src = (("awq" if st.path == "grouped" else "awq_decode") if st.awq else
+           ("nv4" if st.path == "grouped" else "nv4_decode") if st.nv4 else st.path)
     key = f"{st.path}:{wl.name}"
     traffic = committed_traffic(key, decode_src_hash(src))
     if t_mma > t_hbm:
@@ -523,7 +571,7 @@ def run_ours(args, rank, world, device):
     if path == "auto":
         # the library's choice at the measured crossover of the two paths
         import top_moe_expert_gb300 as moe
-        fmt = moe.MOE_W_AWQ4 if wl.fmt == "awq4" else moe.MOE_W_MXFP8
+        fmt = {"awq4": moe.MOE_W_AWQ4, "nvfp4s": moe.MOE_W_NVFP4S}.get(wl.fmt, moe.MOE_W_MXFP8)
         p, b = moe.moe_ffn_select_path(wl.M, wl.k, wl.E, wl.d, wl.I, fmt)
         path = "decode" if p == moe.MOE_PATH_DECODE else "grouped"
         block = block or b
@@ -624,7 +672,7 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
     e2e_bytes = st.bytes_of(0, Ke) if Ke <= st.n_inputs else float(
-        sum(step_bytes(wl, st.step_ids(i % len(rows))) for i in range(Ke)))
+        sum(step_bytes(wl, st.step_ids(i % len(rows)), st.path) for i in range(Ke)))
     del flushbuf
 
     (total_ms, e2e_ms, layer_ms), (steps_bytes, e2e_bytes, layer_bytes_total) = gather_replicas(
@@ -649,9 +697,16 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "awq4-weights/fp16-act/f32-accum" if st.awq else "mxfp8-weights/bf16-act/f32-accum",
+        "dtype": ("awq4-weights/fp16-act/f32-accum" if st.awq else
+                  ("nvfp4s-weights/nvfp4-act/f32-accum" if st.path == "grouped" else
+                   "nvfp4s-weights/bf16-act/f32-accum") if st.nv4 else "mxfp8-weights/bf16-act/f32-accum"),
         "data": ("synthetic (seeded uniform 4-bit q and zeros, fp16 group scales U(0.005, 0.02), N(0,1) fp16 "
                  "activations, the fixture-A routing of the packed-AWQ study)" if st.awq else
+                 ("synthetic (seeded random admissible paired 4:8 NVFP4 packing: uniform E2M1 codes and "
+                  "patterns, UE4M3 scales in [0.5, 2], alpha 0.01; N(0,1) bf16 activations; N(0,1) router "
+                  "logits, fresh routing every step%s)" % (
+                      f"; activation scales alpha_x {st.alpha_x:.3e}, alpha_h {st.alpha_h:.3e}"
+                      if st.alpha_x else "")) if st.nv4 else
                  "synthetic (seeded N(0,0.02) weights quantized to MXFP8, N(0,1) bf16 activations, "
                  "N(0,1) router logits; fresh routing every step)"),
         "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
@@ -709,6 +764,8 @@ def cpu_baseline(wl, device, path="decode", seconds=8.0):
     from top_moe_expert_gb300 import inputs
     if wl.fmt == "awq4":
         return _cpu_baseline_awq(wl, seconds)
+    if wl.fmt == "nvfp4s":
+        return _cpu_baseline_nv4(wl, path, seconds)
     cache = {}
 
     def expert(which, e):
@@ -789,6 +846,52 @@ def _cpu_baseline_awq(wl, seconds):
             "us_per_token": round(t_total / steps / S * 1e6, 1)}
 
 
+def _nv4_sample(wl, path, seed, S):
+    """S tokens of the NVFP4S workload, each with its own routing, and the
+    packed weights of the experts they touch (oracle format dicts)."""
+    import oracle
+    from top_moe_expert_gb300 import inputs
+    logits = np.concatenate([inputs.router_logits(wl, seed + t)[:1] for t in range(S)])
+    x = torch.cat([inputs.activations(wl, seed + t)[:1] for t in range(S)]).to(torch.float64).numpy()
+    ids, w = oracle.topk_softmax(logits, wl.k)
+    experts = sorted(set(ids.reshape(-1).tolist()))
+    slot = np.full(wl.E, -1, dtype=np.int32)
+    slot[experts] = np.arange(len(experts), dtype=np.int32)
+    ws = {}
+    for which in ("w13", "w2"):
+        v, m, sc, a = inputs.nvfp4s_weights(wl, which, experts)
+        ws[which] = {"fmt": "nvfp4s", "v": v, "m": m, "s": sc, "alpha": a, "slot": slot}
+    return logits, x, ids, w, ws
+
+
+def _cpu_baseline_nv4(wl, path, seconds):
+    """The oracle on the NVFP4S layer: exact activations (decode path) or
+    the W4A4 mode (grouped path), S tokens per call, each with its own
+    routing; all cores."""
+    import oracle
+    S = os.cpu_count() or 1
+    a_x, a_h = 5.0 / (6 * 448), 16.0 / (6 * 448)
+    t_total, nbytes, calls, seed = 0.0, 0, 0, 10_000
+    while t_total < seconds and calls < 64:
+        logits, x, ids, _, ws = _nv4_sample(wl, path, seed, S)
+        t0 = time.perf_counter()
+        ids2, w2 = oracle.topk_softmax(logits, wl.k)
+        if path == "grouped":
+            oracle.moe_layer_a4(x, ids2, w2, wl.E, ws["w13"], ws["w2"], a_x, a_h)
+        else:
+            oracle.moe_layer(x, ids2, w2, wl.E, ws["w13"], ws["w2"])
+        t_total += time.perf_counter() - t0
+        nbytes += sum(len(np.unique(ids[t])) * expert_bytes(wl, path) + 4 * wl.d + 4 * wl.E for t in range(S))
+        calls += 1
+        seed += S
+    return {"value": nbytes / t_total / 1e12, "unit": "TB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": (f"{calls} calls of {S} tokens (each token one step of {wl.name}: top-k + layer, binary64, "
+                       f"{'W4A4' if path == 'grouped' else 'exact-activation'} mode, its own routing), "
+                       f"{t_total:.1f} s timed"),
+            "us_per_token": round(t_total / (calls * S) * 1e6, 1)}
+
+
 def _reference_awq(args, wl, world):
     """--impl reference on the AWQ layer: each step one routed expert of
     token 0 restricted to its first 128 neurons (one AWQ group of the down
@@ -834,6 +937,37 @@ def _reference_awq(args, wl, world):
             "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def _reference_nv4(args, wl, world):
+    """--impl reference on the NVFP4S layer: each step one token (its own
+    routing, all k experts) through the oracle in the path's mode, 1 thread."""
+    import oracle
+    K, W = args.steps, args.warmup
+    path = "grouped" if args.path == "grouped" else "decode"
+    oracle.set_num_threads(1)
+    a_x, a_h = 5.0 / (6 * 448), 16.0 / (6 * 448)
+    nbytes, t_total = 0, 0.0
+    for i in range(W + K):
+        logits, x, ids, w, ws = _nv4_sample(wl, path, 20_000 + i, 1)
+        t0 = time.perf_counter()
+        if path == "grouped":
+            oracle.moe_layer_a4(x, ids, w, wl.E, ws["w13"], ws["w2"], a_x, a_h)
+        else:
+            oracle.moe_layer(x, ids, w, wl.E, ws["w13"], ws["w2"])
+        dt = time.perf_counter() - t0
+        if i >= W:
+            t_total += dt
+            nbytes += len(np.unique(ids)) * expert_bytes(wl, path) + 4 * wl.d
+    v = nbytes / t_total / 1e12
+    sample = f"per step: one token of {wl.name} (all its routed experts), binary64 oracle, 1 thread"
+    return {"metric": METRIC, "impl": "reference", "value": v, "unit": "TB/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": t_total * 1e3 / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "M": wl.M, "d": wl.d, "I": wl.I, "E": wl.E, "k": wl.k,
+                       "path": "CPU oracle (sample)"},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": v, "unit": "TB/s"},
+            "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle timed on the host cores (rank 0 only)."""
     if rank != 0:
@@ -849,6 +983,8 @@ def run_reference(args, rank, world):
     K, W = args.steps, args.warmup
     if wl.fmt == "awq4":
         return _reference_awq(args, wl, world)
+    if wl.fmt == "nvfp4s":
+        return _reference_nv4(args, wl, world)
     Is = 64
     logits = inputs.router_logits(wl, 0)
     ids, _ = oracle.topk_softmax(logits, wl.k)

@@ -323,6 +323,36 @@ moe_status_t moe_grouped_prepare_size(const moe_weights_t *w13, const moe_weight
                                       size_t *sfa13_bytes, size_t *sfa2_bytes);
 moe_status_t moe_grouped_prepare(const moe_weights_t *w13, const moe_weights_t *w2,
                                  void *sfa13, void *sfa2, void *stream);
+/* Paired 4:8 sparse NVFP4 weights ("Hardware-Native Joint Sparse-Quantization
+ * for Trillion-Scale Mixture-of-Experts", Sec. 3.4 and App. D.1: the W4A4
+ * grouped path).  moe_grouped_prepare_nvfp4s prepares both projections once
+ * (sizes from moe_grouped_prepare_size with MOE_W_NVFP4S weights; p13 / p2
+ * 256-byte aligned device buffers, passed to moe_ffn_grouped as sfa13 /
+ * sfa2):
+ *   alpha_x, alpha_h  the tensor-wide scales of the layer's activations (the
+ *     block input x and h = SiLU(g) * u), finite and > 0, constants of the
+ *     layer (e.g. calibrated offline); each expert's factor alpha_e =
+ *     alpha_w[e] * alpha_in is formed here;
+ *   p = [head 256 B: alpha_in, binary32(1 / (6 alpha_in)) | alpha_e fp32 [E]
+ *     rounded up to 256 B | side records [E][N][K/128][16 B]: the k-step's 8
+ *     pattern bytes, its 4 UE4M3 scale bytes, 4 zero bytes].
+ * Run time: Q_a quantizes x and h into 32-element blocks of E2M1 codes with
+ * a UE4M3 scale each, every decision in binary32 -- S = the UE4M3 value
+ * nearest (ties to even, saturating at 448) binary32(amax * binary32(1 / (6
+ * alpha))), and each value's code the E2M1 magnitude nearest (ties to even,
+ * saturating at 6) |binary32(v * binary32(1 / binary32(alpha * S)))|, sign
+ * kept (all magnitudes 0 when S = 0).  The tensor cores multiply exact
+ * products of the quantized operands (fp16 S * E2M1 on both sides) in FP32;
+ * the epilogues apply alpha_e (and w_route) to the FP32 accumulators.
+ * moe_ffn_grouped with w13 / w2 MOE_W_NVFP4S (alpha as stated under "Weight
+ * formats"), x MOE_BF16 or MOE_FP16, sfa13 = p13, sfa2 = p2: ws as for AWQ,
+ * [Xg | Hg | Yr | D], where Xg / Hg hold S * E2M1 of Q_a(x) / Q_a(h) as fp16
+ * in natural order (alpha_x / alpha_h left out).  Extra limits: b <= 128,
+ * d % 256 == 0 (MOE_ERR_UNSUPPORTED); p13 / p2 256-byte aligned, w13->q and
+ * w2->q 16-byte aligned (MOE_ERR_INVALID_ARG).  The fixed-capacity layout
+ * (moe_ffn_grouped_batched) returns MOE_ERR_UNSUPPORTED. */
+moe_status_t moe_grouped_prepare_nvfp4s(const moe_weights_t *w13, const moe_weights_t *w2, float alpha_x,
+                                        float alpha_h, void *p13, void *p2, void *stream);
 moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_t d, int32_t I, int32_t b,
                                             int32_t cap_rows, size_t *bytes);
 moe_status_t moe_ffn_grouped(const void *x, int32_t xdt, int32_t M, int32_t d,

@@ -18,7 +18,7 @@ import top_moe_expert_gb300 as moe
 
 _LAUNCHING = {"moe_topk_softmax", "moe_align_block_size", "moe_mxfp8_quantize",
               "moe_ffn_decode", "moe_ffn_decode_logits", "moe_ffn_decode_noalloc", "moe_grouped_prepare",
-              "moe_ffn_grouped"}
+              "moe_ffn_grouped", "moe_grouped_prepare_nvfp4s"}
 
 
 class _Recorder:
@@ -220,3 +220,36 @@ def test_grouped_needs_the_scale_atoms_for_mxfp8(rec):
     with pytest.raises(ValueError):        # expert_ids shorter than the block count of the rows
         moe.moe_ffn_grouped(x, ids, w, w13, w2, sfa13, sfa2, (aligned[0], aligned[1][:1], aligned[2]), 8)
     assert [c[0] for c in rec.calls] == ["moe_align_block_size", "moe_grouped_prepare"]
+
+
+def _nv4(E, N, K):
+    return moe.Weights(moe.MOE_W_NVFP4S, torch.zeros((E, N, K // 4), dtype=torch.uint8),
+                       torch.zeros((E, N, K // 32), dtype=torch.uint8), torch.zeros((E, N, K // 16), dtype=torch.uint8),
+                       torch.ones(E, dtype=torch.float32))
+
+
+def test_grouped_nvfp4s_needs_its_prepared_buffers(rec):
+    M, k, d, I, E = 3, 2, 256, 128, 4
+    ids, w = _route(M, k)
+    x = torch.zeros((M, d), dtype=torch.bfloat16)
+    w13, w2 = _nv4(E, 2 * I, d), _nv4(E, d, I)
+    aligned = moe.moe_align_block_size(ids, E, 8)
+    with pytest.raises(ValueError):                       # the activation scales must be finite and > 0
+        moe.moe_grouped_prepare_nvfp4s(w13, w2, 0.0, 0.1)
+    with pytest.raises(ValueError):
+        moe.moe_grouped_prepare_nvfp4s(w13, w2, 0.1, float("inf"))
+    with pytest.raises(ValueError):                       # MXFP8 weights have no NVFP4S preparation
+        moe.moe_grouped_prepare_nvfp4s(_mx(E, 2 * I, d), _mx(E, d, I), 0.1, 0.1)
+    p13, p2 = moe.moe_grouped_prepare_nvfp4s(w13, w2, 0.01, 0.02)
+    # head + per-expert factors + one 16-byte side record per row and k-step of 128
+    assert p13.numel() == 256 + 256 + E * 2 * I * (d // 128) * 16
+    assert p2.numel() == 256 + 256 + E * d * (I // 128) * 16
+    with pytest.raises(ValueError):
+        moe.moe_ffn_grouped(x, ids, w, w13, w2, None, None, aligned, 8)
+    with pytest.raises(ValueError):
+        moe.moe_ffn_grouped(x, ids, w, w13, w2, p13, p2[:-1], aligned, 8)
+    moe.moe_ffn_grouped(x, ids, w, w13, w2, p13, p2, aligned, 8)
+    names = [c[0] for c in rec.calls]
+    assert names == ["moe_align_block_size", "moe_grouped_prepare_nvfp4s", "moe_ffn_grouped"]
+    args = rec.calls[1][1]
+    assert abs(args[2] - 0.01) < 1e-9 and abs(args[3] - 0.02) < 1e-9

@@ -1,0 +1,142 @@
+"""GPU parity of the paired 4:8 sparse NVFP4 grouped path (W4A4: the weights
+expanded on chip to fp16 UE4M3 * E2M1, activations quantized at run time by
+Q_a, tcgen05 kind::f16 with FP32 accumulation, the per-expert factor in the
+epilogues), against the oracle's W4A4 layer mode.
+
+"Hardware-Native Joint Sparse-Quantization for Trillion-Scale
+Mixture-of-Experts", Sec. 3.4 and App. D.1.  Checked stage by stage, as the
+block-scaled MXFP8 path is: Q_a(x) per aligned row bit for bit; Q_a(h) per
+route against the oracle's (a code may differ only where h, summed in FP32
+on the GPU and in binary64 in the oracle, sits at a rounding boundary: the
+count is bounded and each difference is one grid step); the output against
+the oracle's second projection fed the GPU's own Q_a(h), at the layer
+tolerance.  Repeats and another block size give the same bits.
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import top_moe_expert_gb300 as moe
+from tests import gpu_setup as gs
+from top_moe_expert_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = inputs.Workload("nv4g_m21_d512_i256_e16_k4", M=21, d=512, I=256, E=16, k=4, seed=22)
+MID = inputs.Workload("nv4g_m64_d1024_i512_e16_k4", M=64, d=1024, I=512, E=16, k=4, seed=23)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    gs.need_gpu()
+
+
+def _layer(wl):
+    p13 = oracle.nvfp4s_quantize_3d(inputs.weights_fp32(wl, "w13").astype(np.float64))
+    p2 = oracle.nvfp4s_quantize_3d(inputs.weights_fp32(wl, "w2").astype(np.float64))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    mk = lambda p: moe.Weights(moe.MOE_W_NVFP4S, dev(p["v"]), dev(p["s"]), dev(p["m"]), dev(p["alpha"]))
+    return mk(p13), mk(p2), p13, p2
+
+
+def _scales(wl, x, ids, w, p13, p2):
+    """The layer's activation scales as a calibration would set them: the
+    largest magnitude of x and of the oracle's h over the batch, mapped to the
+    top of the NVFP4 range (6 x 448)."""
+    xe = gs.x_exact(x)
+    a_x = float(np.float32(np.abs(xe).max() / (6 * 448)))
+    h = oracle.moe_layer_a4(xe, ids, w, wl.E, p13, p2, a_x, 1.0, want_h=True)["h"]
+    a_h = float(np.float32(np.abs(h).max() / (6 * 448)))
+    return a_x, a_h
+
+
+def _run(wl, w13, w2, p13d, p2d, x, ids, w, b, out_dtype=torch.float32):
+    tid = torch.from_numpy(ids).cuda()
+    aligned = moe.moe_align_block_size(tid, wl.E, b)
+    M, k = ids.shape
+    cap = aligned[0].numel()
+    ws = torch.zeros(moe.moe_ffn_grouped_workspace_size(M, k, wl.d, wl.I, b, cap), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    y = moe.moe_ffn_grouped(x.cuda(), tid, torch.from_numpy(w).cuda(), w13, w2, p13d, p2d, aligned, b,
+                            out_dtype=out_dtype, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.tolist() == [0, 0] or st.tolist()[1] == 0
+    return y, aligned, ws
+
+
+def _r256(n):
+    return (n + 255) // 256 * 256
+
+
+def _xg_hg(ws, cap, d, I):
+    xb, hb = cap * d * 2, cap * I * 2
+    xg = ws[:xb].view(torch.float16).reshape(cap, d).double().cpu().numpy()
+    hg = ws[_r256(xb):_r256(xb) + hb].view(torch.float16).reshape(cap, I).double().cpu().numpy()
+    return xg, hg
+
+
+def _check(wl, xdt, b, invalid=False):
+    w13, w2, p13, p2 = _layer(wl)
+    x = inputs.activations(wl, dtype=xdt)
+    ids, w = gs.routing(wl)
+    ids = ids.copy()
+    if invalid:
+        ids[1, 1] = -1                                         # an invalid route: skipped, contributes 0
+    w = w.astype(np.float64)
+    a_x, a_h = _scales(wl, x, ids, w, p13, p2)
+    p13d, p2d = moe.moe_grouped_prepare_nvfp4s(w13, w2, a_x, a_h)
+    y, aligned, ws = _run(wl, w13, w2, p13d, p2d, x, ids, w.astype(np.float32), b)
+    ref = oracle.moe_layer_a4(gs.x_exact(x), ids, w, wl.E, p13, p2, a_x, a_h, want_xv=True, want_hv=True)
+    M, k = ids.shape
+    sorted_ids = aligned[0].cpu().numpy()
+    npp = int(aligned[2].item())
+    xg, hg = _xg_hg(ws, sorted_ids.size, wl.d, wl.I)
+    # stage 1: Q_a(x) of every aligned row, bit for bit; padding rows zero
+    rows = sorted_ids[:npp]
+    valid = rows < M * k
+    np.testing.assert_array_equal(xg[:npp][valid], ref["xv"][rows[valid] // k])
+    assert not xg[:npp][~valid].any()
+    # stage 2: Q_a(h) per route; rare one-step differences at rounding boundaries
+    hv_gpu = np.zeros((M * k, wl.I))
+    hv_gpu[rows[valid]] = hg[:npp][valid]
+    diff = hv_gpu != ref["hv"]
+    n_diff, n_all = int(diff.sum()), int(valid.sum()) * wl.I
+    assert n_diff <= max(2, n_all // 10000), f"{n_diff} of {n_all} Q_a(h) values differ"
+    if n_diff:
+        S = np.repeat(np.abs(ref["hv"]).reshape(M * k, wl.I // 32, 32).max(axis=2) / 6, 32, axis=1)
+        assert (np.abs(hv_gpu - ref["hv"])[diff] <= 2 * S[diff] * (1 + 1e-9)).all()
+    # stage 3: the second projection fed the GPU's own Q_a(h)
+    y_ref = oracle.moe_layer_a4(gs.x_exact(x), ids, w, wl.E, p13, p2, a_x, a_h, hv_in=hv_gpu)["y"]
+    err, cos = gs.assert_layer_close(y, y_ref)
+    if n_diff == 0:
+        gs.assert_layer_close(y, ref["y"])
+    print(f"{wl.name} b={b}: Q_a(h) differences {n_diff}/{n_all}, max|err|/max|ref| {err:.2e}, cos {cos:.8f}")
+    return y, (w13, w2, p13d, p2d, x, ids, w.astype(np.float32))
+
+
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float16])
+def test_nv4_grouped_small(xdt):
+    _check(SMALL, xdt, 8, invalid=True)
+
+
+def test_nv4_grouped_mid_and_block_independence():
+    y16, (w13, w2, p13d, p2d, x, ids, w) = _check(MID, torch.bfloat16, 16)
+    digests = set()
+    for b in (16, 16, 32, 8):
+        y, _, _ = _run(MID, w13, w2, p13d, p2d, x, ids, w, b)
+        digests.add(hashlib.sha256(y.cpu().numpy().tobytes()).hexdigest())
+    assert digests == {hashlib.sha256(y16.cpu().numpy().tobytes()).hexdigest()}
+
+
+def test_nv4_grouped_bf16_output():
+    w13, w2, p13, p2 = _layer(SMALL)
+    x = inputs.activations(SMALL, dtype=torch.bfloat16)
+    ids, w = gs.routing(SMALL)
+    a_x, a_h = _scales(SMALL, x, ids, w.astype(np.float64), p13, p2)
+    p13d, p2d = moe.moe_grouped_prepare_nvfp4s(w13, w2, a_x, a_h)
+    y32, _, _ = _run(SMALL, w13, w2, p13d, p2d, x, ids, w, 8)
+    y16, _, _ = _run(SMALL, w13, w2, p13d, p2d, x, ids, w, 8, out_dtype=torch.bfloat16)
+    assert torch.equal(y16, y32.to(torch.bfloat16))

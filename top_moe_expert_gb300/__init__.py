@@ -12,6 +12,7 @@ from __future__ import annotations
 import contextlib
 import ctypes
 import dataclasses
+import math
 import os
 import threading
 
@@ -63,6 +64,8 @@ _PROTOS = {
                                      ctypes.POINTER(moe_weights_t), _P, _P, _P, _I32, _P, _SZ, _P, _P]),
     "moe_grouped_prepare_size": (_I32, [ctypes.POINTER(moe_weights_t), ctypes.POINTER(moe_weights_t), _P, _P]),
     "moe_grouped_prepare": (_I32, [ctypes.POINTER(moe_weights_t), ctypes.POINTER(moe_weights_t), _P, _P, _P]),
+    "moe_grouped_prepare_nvfp4s": (_I32, [ctypes.POINTER(moe_weights_t), ctypes.POINTER(moe_weights_t),
+                                          ctypes.c_float, ctypes.c_float, _P, _P, _P]),
     "moe_ffn_grouped_workspace_size": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "moe_ffn_grouped": (_I32, [_P, _I32, _I32, _I32, _P, _P, _I32, ctypes.POINTER(moe_weights_t),
                                ctypes.POINTER(moe_weights_t), _P, _P, _P, _P, _P, _I32, _I32, _P, _I32,
@@ -513,6 +516,30 @@ def moe_grouped_prepare(w13: Weights, w2: Weights, stream=None):
     return sfa13, sfa2
 
 
+def moe_grouped_prepare_nvfp4s(w13: Weights, w2: Weights, alpha_x: float, alpha_h: float, stream=None):
+    """Prepared buffers (p13, p2) of paired 4:8 sparse NVFP4 weights for the
+    W4A4 grouped path: the activations' tensor-wide scales alpha_x (block
+    input) and alpha_h (SwiGLU output), the per-expert factors and the
+    per-k-step side records; pass them to moe_ffn_grouped as sfa13 / sfa2."""
+    dev = w13.device
+    w2.on("w2", dev)
+    if w13.fmt != MOE_W_NVFP4S or w2.fmt != MOE_W_NVFP4S:
+        raise ValueError("moe_grouped_prepare_nvfp4s takes NVFP4S weights")
+    if not (alpha_x > 0 and alpha_h > 0 and math.isfinite(alpha_x) and math.isfinite(alpha_h)):
+        raise ValueError(f"alpha_x = {alpha_x}, alpha_h = {alpha_h}: both must be finite and > 0")
+    a, b = w13.c_struct(), w2.c_struct()
+    n13, n2 = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().moe_grouped_prepare_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(n13), ctypes.byref(n2)),
+           "moe_grouped_prepare_size")
+    p13 = torch.empty(n13.value, dtype=torch.uint8, device=dev)
+    p2 = torch.empty(n2.value, dtype=torch.uint8, device=dev)
+    with _guard(dev):
+        _check(lib().moe_grouped_prepare_nvfp4s(ctypes.byref(a), ctypes.byref(b), float(alpha_x), float(alpha_h),
+                                                _ptr(p13), _ptr(p2), _stream(stream, dev)),
+               "moe_grouped_prepare_nvfp4s")
+    return p13, p2
+
+
 def _round256(n):
     return (n + 255) // 256 * 256
 
@@ -561,8 +588,9 @@ def moe_ffn_grouped(x, topk_ids, topk_w, w13: Weights, w2: Weights, sfa13, sfa2,
     _opt(block_rows, "block_rows", dtypes=_IDS, min_numel=cap_rows // b, device=dev)
     _need(npp, "num_rows_post_pad", _IDS, min_numel=1, device=dev)
     a, bb = w13.c_struct(), w2.c_struct()
-    if w13.fmt == MOE_W_MXFP8 and w2.fmt == MOE_W_MXFP8:
-        # the block-scaled MMA reads the scale atoms moe_grouped_prepare wrote
+    if w13.fmt == w2.fmt and w13.fmt in (MOE_W_MXFP8, MOE_W_NVFP4S):
+        # the block-scaled MMA reads the scale atoms moe_grouped_prepare wrote;
+        # the NVFP4S path, what moe_grouped_prepare_nvfp4s wrote
         n13, n2 = ctypes.c_size_t(), ctypes.c_size_t()
         _check(lib().moe_grouped_prepare_size(ctypes.byref(a), ctypes.byref(bb), ctypes.byref(n13),
                                               ctypes.byref(n2)), "moe_grouped_prepare_size")

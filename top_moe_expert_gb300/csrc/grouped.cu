@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "attr.h"
@@ -692,11 +693,21 @@ using namespace moe::gg;
 MOE_API moe_status_t moe_grouped_prepare_size(const moe_weights_t *w13, const moe_weights_t *w2, size_t *sfa13_bytes,
                                               size_t *sfa2_bytes)
 {
-    if (!w13 || !w2 || !sfa13_bytes || !sfa2_bytes || w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8)
+    if (!w13 || !w2 || !sfa13_bytes || !sfa2_bytes)
+        return MOE_ERR_INVALID_ARG;
+    const bool nv4 = w13->fmt == MOE_W_NVFP4S && w2->fmt == MOE_W_NVFP4S;
+    if (!nv4 && (w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8))
         return MOE_ERR_INVALID_ARG;
     const int I = w2->K, d = w13->K, E = w13->E;
     if (w13->N != 2 * I || w2->N != d || d % 128 || I % 128)
         return MOE_ERR_UNSUPPORTED;
+    if (nv4) {
+        if (d % 256)
+            return MOE_ERR_UNSUPPORTED;
+        *sfa13_bytes = grouped_nv4_prepare_bytes(E, 2 * I, d);
+        *sfa2_bytes = grouped_nv4_prepare_bytes(w2->E, d, I);
+        return MOE_OK;
+    }
     *sfa13_bytes = static_cast<size_t>(E) * (I / 64) * (d / 128) * 512;
     *sfa2_bytes = static_cast<size_t>(E) * (d / 128) * (I / 128) * 512;
     return MOE_OK;
@@ -709,6 +720,8 @@ MOE_API moe_status_t moe_grouped_prepare(const moe_weights_t *w13, const moe_wei
     moe_status_t st = moe_grouped_prepare_size(w13, w2, &b13, &b2);
     if (st != MOE_OK)
         return st;
+    if (w13->fmt != MOE_W_MXFP8)
+        return MOE_ERR_INVALID_ARG;              // NVFP4S: moe_grouped_prepare_nvfp4s
     if (!w13->scale || !w2->scale || !sfa13 || !sfa2)
         return MOE_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
@@ -719,6 +732,28 @@ MOE_API moe_status_t moe_grouped_prepare(const moe_weights_t *w13, const moe_wei
     prepare_sfa_kernel<<<1024, 256, 0, s>>>(static_cast<const uint8_t *>(w2->scale), w2->E, w2->N, w2->K, 2, w2->K,
                                             static_cast<uint8_t *>(sfa2));
     return launch_status();
+}
+
+MOE_API moe_status_t moe_grouped_prepare_nvfp4s(const moe_weights_t *w13, const moe_weights_t *w2, float alpha_x,
+                                                float alpha_h, void *p13, void *p2, void *stream)
+{
+    size_t b13, b2;
+    if (!w13 || !w2 || w13->fmt != MOE_W_NVFP4S || w2->fmt != MOE_W_NVFP4S)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = moe_grouped_prepare_size(w13, w2, &b13, &b2);
+    if (st != MOE_OK)
+        return st;
+    if (w2->E != w13->E || !w13->zero || !w2->zero || !w13->scale || !w2->scale || !w13->alpha || !w2->alpha ||
+        !p13 || !p2 || !aligned(p13, 256) || !aligned(p2, 256) || !aligned(w13->zero, 16) || !aligned(w2->zero, 16) ||
+        !aligned(w13->scale, 16) || !aligned(w2->scale, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (!(alpha_x > 0.f) || !(alpha_h > 0.f) || !std::isfinite(alpha_x) || !std::isfinite(alpha_h))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    st = grouped_nv4_prepare(w13, alpha_x, p13, s);
+    if (st != MOE_OK)
+        return st;
+    return grouped_nv4_prepare(w2, alpha_h, p2, s);
 }
 
 MOE_API moe_status_t moe_ffn_grouped_workspace_size(int32_t M, int32_t k, int32_t d, int32_t I, int32_t b,
@@ -744,9 +779,10 @@ static moe_status_t grouped_impl(const void *x, int32_t xdt, int32_t M, int32_t 
     if (M < 0 || d < 1 || k < 1 || !w13 || !w2)
         return MOE_ERR_INVALID_ARG;
     const bool awq = w13->fmt == MOE_W_AWQ4 && w2->fmt == MOE_W_AWQ4;
-    if (!awq && (w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8 || xdt != MOE_BF16))
+    const bool nv4 = w13->fmt == MOE_W_NVFP4S && w2->fmt == MOE_W_NVFP4S;
+    if (!awq && !nv4 && (w13->fmt != MOE_W_MXFP8 || w2->fmt != MOE_W_MXFP8 || xdt != MOE_BF16))
         return MOE_ERR_UNSUPPORTED;
-    if (awq && xdt != MOE_FP16 && xdt != MOE_BF16)
+    if ((awq || nv4) && xdt != MOE_FP16 && xdt != MOE_BF16)
         return MOE_ERR_UNSUPPORTED;
     if (ydt != MOE_BF16 && ydt != MOE_FP32)
         return MOE_ERR_UNSUPPORTED;
@@ -760,7 +796,7 @@ static moe_status_t grouped_impl(const void *x, int32_t xdt, int32_t M, int32_t 
         // fixed capacity: any multiple of b holds the layout it was built for
         if (cap_rows < b || cap_rows % b)
             return MOE_ERR_CAPACITY;
-        if (awq)
+        if (awq || nv4)
             return MOE_ERR_UNSUPPORTED;
     } else {
         int32_t need_rows, need_blocks;
@@ -771,6 +807,23 @@ static moe_status_t grouped_impl(const void *x, int32_t xdt, int32_t M, int32_t 
     }
     if (M == 0)
         return MOE_OK;
+    if (nv4) {
+        if (!x || !topk_ids || !topk_w || !y || !sfa13 || !sfa2 || !sorted_route_ids || !expert_ids ||
+            !num_rows_post_pad || !w13->q || !w2->q)
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned(w13->q, 16) || !aligned(w2->q, 16) || !aligned(sfa13, 256) || !aligned(sfa2, 256) ||
+            !aligned(x, 16) || !aligned(y, 16))
+            return MOE_ERR_INVALID_ARG;
+        if (static_cast<int64_t>(M) * (d / 4) > INT32_MAX || d % 256)
+            return MOE_ERR_UNSUPPORTED;
+        size_t need = 0;
+        moe_ffn_grouped_workspace_size(M, k, d, I, b, cap_rows, &need);
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return MOE_ERR_WORKSPACE;
+        return grouped_nv4_launch(x, xdt == MOE_BF16, M, d, I, E, topk_ids, topk_w, k, w13, w2, sfa13, sfa2,
+                                  sorted_route_ids, expert_ids, num_rows_post_pad, b, cap_rows, y, ydt == MOE_FP32, ws,
+                                  dev_status, as_stream(stream));
+    }
     if (awq) {
         if (!x || !topk_ids || !topk_w || !y || !sorted_route_ids || !expert_ids || !num_rows_post_pad ||
             !w13->q || !w2->q || !w13->scale || !w2->scale || !w13->zero || !w2->zero)

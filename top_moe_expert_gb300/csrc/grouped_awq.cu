@@ -36,6 +36,26 @@
 // its terms as long as both operands use the same one: the gather writes Xg
 // and the GEMM1 epilogue writes Hg in that order too (interleave_pos).
 //
+// The same kernel, instantiated for paired 4:8 sparse NVFP4 weights ("Hardware-
+// Native Joint Sparse-Quantization for Trillion-Scale Mixture-of-Experts",
+// Sec. 3.4 and App. D.1: E2M1 values, pair metadata and one UE4M3 scale per
+// 32 weights; activations quantized at run time into 32-element blocks;
+// the tensor-wide scales folded into one factor per expert, applied to the
+// FP32 accumulator in the epilogue), runs the W4A4 grouped layer:
+//   gather_nv4_kernel : Xg[rho] = S * E2M1 of Q_a(x[route(rho) / k]) as fp16,
+//                       natural order (the block's alpha_x left out)
+//   gemm_kernel<Nv4>  : per k-step TMA brings the kept codes (32 bytes a row)
+//                       and a prepared 16-byte side record (8 bytes of pair
+//                       patterns, 4 UE4M3 scales); dequantizing warps expand
+//                       each group of 8 into fp16 UE4M3 * E2M1 at the kept
+//                       pairs and zero elsewhere (exact), into tensor memory;
+//                       GEMM1's epilogue scales by alpha_e, forms h and
+//                       quantizes it by Q_a into Hg (S * E2M1, fp16); GEMM2's
+//                       epilogue scales by w_route * alpha_e.
+// The tensor core then multiplies exact products of the quantized operands,
+// as the block-scaled MMA does; it runs dense fp16 MMAs over the expanded
+// weights (half of them zero) instead of the sparse MMA.
+//
 // Roles (one CTA per SM, persistent over tiles): warp 0 TMA and bulk copies,
 // warps 1 and 2 TMEM and MMA issue (one per 128-row half of a tile), warps
 // 3..6 epilogue, warps 7..18 dequantization.
@@ -64,6 +84,9 @@ constexpr int kMaxASlots = 7;                    // dequantized half-k-steps in 
 constexpr int kHeaderBytes = 1024;
 constexpr int kMaxG = 64;                        // K <= 8192
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kAwq = 0;                          // weight formats of the kernel template
+constexpr int kNv4 = 1;
+constexpr int kNv4SideBytes = 16;                // per weight row and k-step: 8 pattern bytes, 4 scales, 4 unused
 
 // position of value j (0..7) inside its run of 8 in the operand order
 __host__ __device__ constexpr int interleave_pos(int j) { return ((j & 3) << 1) | (j >> 2); }
@@ -80,6 +103,8 @@ struct Args {
     int32_t *dev_status;
     int b, n_mma, n_t, KT, I, d, MK, N, G, stages, aslots, acc_cols, nbuf;
     int E, cap_blocks;        // experts, and the blocks the operands hold (debug bounds checks)
+    const float *ce;          // NVFP4S: per-expert factor alpha_w[e] * alpha_in, fp32 [E]
+    const float *qa;          // NVFP4S, first GEMM: Q_a constants of h (alpha_h, binary32(1 / (6 alpha_h)))
 };
 
 // A tile is 256 weight rows of one expert, in two halves of 128 that two MMA
@@ -96,11 +121,17 @@ struct Args {
 // ([256][64 bytes]).  It is free again once the dequantizing warps have read
 // the packed bytes and both issuers' MMAs that read B have completed.  A
 // dequantized half-k-step ("unit") occupies 64 TMEM columns.
+//
+// NVFP4S: the packed part of a stage is the kept codes ([256][32 bytes],
+// half 1 at +4096) and then the side records ([256][16 bytes], half 1 at
+// +2048).
 struct Geo {
-    int n_mma;
+    int n_mma, nv4;
     __host__ __device__ int b_off() const { return 0; }
     __host__ __device__ int raw_off() const { return n_mma * 256; }
-    __host__ __device__ int bytes() const { return n_mma * 256 + 16384; }   // multiple of 1024 (n_mma % 8 == 0)
+    __host__ __device__ int side_off() const { return raw_off() + 8192; }   // NVFP4S
+    // multiple of 1024 (n_mma % 8 == 0)
+    __host__ __device__ int bytes() const { return n_mma * 256 + (nv4 ? 8192 + 256 * kNv4SideBytes : 16384); }
 };
 
 // Packed word -> four fp16 pairs (n0, n4) (n1, n5) (n2, n6) (n3, n7), each
@@ -148,6 +179,108 @@ __device__ __forceinline__ void dq_words(const uint4 &a, const uint4 &b, uint32_
         dq_word(wd[c], zb2, zb16, sc2, out + 4 * c);
 }
 
+// ---------------------------------------------------------------- NVFP4S
+
+// Two E2M1 codes (low nibble first) -> the fp16 pair of their values (exact).
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte)
+{
+    uint32_t r;
+    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "r"(byte));
+    return r;
+}
+
+// A UE4M3 scale code (sign bit clear) -> the fp16 pair (S, S) (exact).
+__device__ __forceinline__ uint32_t ue4m3_f16x2(uint32_t s)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(s | (s << 8))));
+    return r;
+}
+
+// One group of 8 weights: its four kept codes (pair p0's two values, then
+// pair p1's, low nibble first), its pattern nibble p0 | p1 << 2 and its
+// block's scale pair -> four fp16 pairs in natural order, UE4M3 * E2M1 at
+// the kept pairs (exact: at most 6 significant bits, within fp16's range)
+// and 0 at the others.
+__device__ __forceinline__ void dq_nv4_group(uint32_t codes16, uint32_t nib, uint32_t s2, uint32_t *out)
+{
+    const __half2 S = *reinterpret_cast<const __half2 *>(&s2);
+    const uint32_t a = e2m1x2_f16x2(codes16 & 0xFFu), b = e2m1x2_f16x2(codes16 >> 8);
+    const __half2 ha = __hmul2(*reinterpret_cast<const __half2 *>(&a), S);
+    const __half2 hb = __hmul2(*reinterpret_cast<const __half2 *>(&b), S);
+    const uint32_t P0 = *reinterpret_cast<const uint32_t *>(&ha), P1 = *reinterpret_cast<const uint32_t *>(&hb);
+    const uint32_t p0 = nib & 3u, p1 = nib >> 2;
+    out[0] = p0 == 0 ? P0 : 0u;
+    out[1] = p0 == 1 ? P0 : (p1 == 1 ? P1 : 0u);
+    out[2] = p0 == 2 ? P0 : (p1 == 2 ? P1 : 0u);
+    out[3] = p1 == 3 ? P1 : 0u;
+}
+
+// 64 weights of one row: kept codes (16 bytes, group g in bytes 2g, 2g + 1),
+// the eight groups' pattern nibbles (group g in bits 4g .. 4g + 3) and the
+// two blocks' scale codes (bits 0..7, 8..15) -> 32 fp16 pairs in natural order.
+__device__ __forceinline__ void dq_nv4_words(const uint4 &c, uint32_t meta, uint32_t sc, uint32_t (&out)[32])
+{
+    const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+    const uint32_t s0 = ue4m3_f16x2(sc & 0xFFu), s1 = ue4m3_f16x2((sc >> 8) & 0xFFu);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        dq_nv4_group((wd[g >> 1] >> (16 * (g & 1))) & 0xFFFFu, (meta >> (4 * g)) & 0xFu, g < 4 ? s0 : s1,
+                     out + 4 * g);
+}
+
+// The run-time activation quantizer Q_a of one 32-element block ("Hardware-
+// Native Joint Sparse-Quantization ...", Sec. 3.4 and App. D.1; block scale
+// by Eq. 5 with the tensor-wide factor 1 / alpha), every decision in
+// binary32: t = amax * r6 (r6 = binary32(1 / (6 alpha))) rounded to nearest
+// even onto UE4M3 with saturation at 448 gives the scale S; each value v
+// becomes sign(v) | |v * q| rounded to nearest even onto the E2M1
+// magnitudes with saturation at 6, q = 1 / binary32(alpha * S) (all codes 0
+// when S = 0).  The operand the tensor core takes is S * E2M1 as fp16 (exact);
+// alpha goes to the epilogue.
+struct QaBlock {
+    float q;         // 1 / (alpha S), 0 when S = 0
+    uint32_t s16;    // S as fp16 bits
+};
+
+__device__ __forceinline__ QaBlock qa_block(float amax, float alpha, float r6)
+{
+    const float t = __fmul_rn(amax, r6);
+    uint16_t code;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(code) : "f"(0.0f), "f"(t));
+    const uint32_t s2 = ue4m3_f16x2(code & 0xFFu);
+    const float S = __low2float(*reinterpret_cast<const __half2 *>(&s2));
+    QaBlock b;
+    b.q = S > 0.f ? __frcp_rn(__fmul_rn(alpha, S)) : 0.f;
+    b.s16 = s2 & 0xFFFFu;
+    return b;
+}
+
+// fp16 bits of a (>= 0) rounded to nearest onto {0, .5, 1, 1.5, 2, 3, 4, 6},
+// saturating at 6; a midpoint (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) goes to
+// the neighbour whose E2M1 mantissa bit is 0.
+__device__ __forceinline__ uint32_t e2m1_rne_f16(float a)
+{
+    uint32_t h = 0u;
+    h = a > 0.25f ? 0x3800u : h;
+    h = a >= 0.75f ? 0x3C00u : h;
+    h = a > 1.25f ? 0x3E00u : h;
+    h = a >= 1.75f ? 0x4000u : h;
+    h = a > 2.5f ? 0x4200u : h;
+    h = a >= 3.5f ? 0x4400u : h;
+    h = a > 5.0f ? 0x4600u : h;
+    return h;
+}
+
+// S * E2M1(code of v) as fp16 bits, the sign bit that of v.
+__device__ __forceinline__ uint32_t qa_value_f16(float v, const QaBlock &b)
+{
+    const uint32_t m = e2m1_rne_f16(fabsf(__fmul_rn(v, b.q)));
+    const __half p = __hmul(__ushort_as_half(static_cast<unsigned short>(m)),
+                            __ushort_as_half(static_cast<unsigned short>(b.s16)));
+    return __half_as_ushort(p) | ((__float_as_uint(v) >> 16) & 0x8000u);
+}
+
 // Per-tile group scales and zeros, as copied from global memory: the scale
 // rows of the tile's 256 weight rows, [256][G] fp16, then their zero words,
 // [32][G] int32 (row r's zero in nibble r % 8 of word [r / 8][g]).
@@ -175,16 +308,22 @@ __device__ __forceinline__ int tile_kind(int t, int total1, int n_t1, int n_t2, 
     return 2;
 }
 
+// FMT = kAwq: AWQ codes with per-tile scales and zeros (tmS1 / tmS2
+// unused); FMT = kNv4: NVFP4S kept codes with per-k-step side records
+// (tmS1 / tmS2, no per-tile buffers).
+template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CUtensorMap tmB1,
-            const __grid_constant__ CUtensorMap tmQ2, const __grid_constant__ CUtensorMap tmB2, const Args a1,
+            const __grid_constant__ CUtensorMap tmQ2, const __grid_constant__ CUtensorMap tmB2,
+            const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmS2, const Args a1,
             const Args a2, int32_t *done, int sbuf_g)
 {
+    constexpr bool kN = FMT == kNv4;
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw = tc::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const Geo geo{a1.n_mma};
+    const Geo geo{a1.n_mma, kN ? 1 : 0};
     // kDqGroups <= AS, ceil(AS / 2) < S
     const int S = a1.stages, SB = geo.bytes(), AS = a1.aslots, NB = a1.nbuf;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * SB);
@@ -227,6 +366,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
         tc::prefetch_tmap(&tmB1);
         tc::prefetch_tmap(&tmQ2);
         tc::prefetch_tmap(&tmB2);
+        if (kN) {
+            tc::prefetch_tmap(&tmS1);
+            tc::prefetch_tmap(&tmS2);
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -269,6 +412,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                 const int32_t *zp = kind == 1 ? a1.z : a2.z;
                 const CUtensorMap *tQ = kind == 1 ? &tmQ1 : &tmQ2;
                 const CUtensorMap *tB = kind == 1 ? &tmB1 : &tmB2;
+                const CUtensorMap *tS = kind == 1 ? &tmS1 : &tmS2;
                 const int row0 = e * N;
                 // first weight row of each half
                 const int r0 = kind == 1 ? row0 + 128 * T : row0 + 256 * T;
@@ -292,12 +436,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                     // the tensor-memory-access proxy reads what generic stores wrote
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
-                // the tile's scales and zeros (buffer ti % 2, freed by the
-                // dequantizing warps when they finish tile ti - 2)
+                // AWQ: the tile's scales and zeros (buffer ti % 2, freed by
+                // the dequantizing warps when they finish tile ti - 2)
                 const int sb = ti & 1;
-                if (!tc::mbar_wait(sempty0 + 8 * sb, ((ti >> 1) & 1) ^ 1u, abort_flag, kWaitNs))
+                if (!kN && !tc::mbar_wait(sempty0 + 8 * sb, ((ti >> 1) & 1) ^ 1u, abort_flag, kWaitNs))
                     break;
-                {
+                if (!kN) {
                     const uint32_t fb = sfull0 + 8 * sb;
                     const uint32_t dst = tc::smem_u32(sbuf + sb * SBUF);
                     const int64_t zr0 = static_cast<int64_t>(e) * (N / 8) + (r0 - row0) / 8;
@@ -314,9 +458,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                     uint8_t *st = smem + s * SB;
                     const uint32_t fb = rfull0 + 8 * s;
                     tc::mbar_arrive_expect_tx(fb, tx);
-                    // packed A rows: 64 bytes (128 values) of each, x in bytes
-                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), tQ, kt * 64, r0, fb);
-                    tc::tma_load_2d(tc::smem_u32(st + geo.raw_off() + 8192), tQ, kt * 64, r1, fb);
+                    if (kN) {
+                        // kept codes: 32 bytes (128 weights) of each row; side records: 16 bytes
+                        tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), tQ, kt * 32, r0, fb);
+                        tc::tma_load_2d(tc::smem_u32(st + geo.raw_off() + 4096), tQ, kt * 32, r1, fb);
+                        tc::tma_load_2d(tc::smem_u32(st + geo.side_off()), tS, kt * kNv4SideBytes, r0, fb);
+                        tc::tma_load_2d(tc::smem_u32(st + geo.side_off() + 2048), tS, kt * kNv4SideBytes, r1, fb);
+                    } else {
+                        // packed A rows: 64 bytes (128 values) of each, x in bytes
+                        tc::tma_load_2d(tc::smem_u32(st + geo.raw_off()), tQ, kt * 64, r0, fb);
+                        tc::tma_load_2d(tc::smem_u32(st + geo.raw_off() + 8192), tQ, kt * 64, r1, fb);
+                    }
                     // B: two tiles of n_mma rows x 64 fp16, x in elements
                     tc::tma_load_2d(tc::smem_u32(st + geo.b_off()), tB, kt * 128, jb * b, fb);
                     tc::tma_load_2d(tc::smem_u32(st + geo.b_off() + geo.n_mma * 128), tB, kt * 128 + 64, jb * b, fb);
@@ -338,7 +490,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                 }
                 tc::mbar_wait(rfull0 + 8 * st, pp, &never, kWaitNs);
             }
-            for (int i = 1; i <= 2 && i <= ti; ++i)
+            for (int i = 1; !kN && i <= 2 && i <= ti; ++i)
                 tc::mbar_wait(sfull0 + 8 * ((ti - i) & 1), ((ti - i) >> 1) & 1u, &never, kWaitNs);
         }
     } else if (warp < kEpiWarp0) {
@@ -405,6 +557,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
         const int q = warp & 3;                       // TMEM lane quadrant
         const int etid = threadIdx.x - kEpiWarp0 * 32;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+        // NVFP4S: Q_a constants of h
+        const float qa_alpha = kN ? a1.qa[0] : 0.f, qa_r6 = kN ? a1.qa[1] : 0.f;
         int ti = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
             int jb, T;
@@ -412,13 +566,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
             const int buf = NB == 2 ? (ti & 1) : 0;
             const uint32_t use = static_cast<uint32_t>(NB == 2 ? (ti >> 1) : ti);
             const int rho0 = jb * b;
+            // NVFP4S: the expert's factor alpha_w * alpha_in
+            const float ce = kN ? (kind == 1 ? a1.ce : a2.ce)[a1.expert_ids[jb]] : 1.f;
             if (kind == 2) {
                 for (int c = etid; c < b; c += 128) {
                     int r = a2.sorted[rho0 + c];
                     if (!MOE_IN_BOUNDS(r >= 0 && r <= a2.MK, a2.dev_status))
                         r = a2.MK;                            // read as padding
                     t_route[c] = r;
-                    t_w[c] = r < a2.MK ? a2.wts[r] : 0.f;
+                    if constexpr (kN)
+                        t_w[c] = r < a2.MK ? a2.wts[r] * ce : 0.f;
+                    else
+                        t_w[c] = r < a2.MK ? a2.wts[r] : 0.f;
                 }
             }
             bool ok = tc::mbar_wait(accf0 + 8 * buf, use & 1u, abort_flag, kWaitNs);
@@ -438,12 +597,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                     tc::tmem_ld_32x32b_x32(acc1 + c0, u);
                     tc::tmem_ld_wait();
                     const int n = 128 * T + 32 * q + lane;
-                    __half *hrow = a1.hg + static_cast<int64_t>(rho0 + c0) * a1.I + (n & ~7) + interleave_pos(n & 7);
+                    if constexpr (kN) {
+                        // h -> Q_a: the warp's 32 lanes are the 32 neurons of one block
+                        uint16_t *hrow = reinterpret_cast<uint16_t *>(a1.hg) + static_cast<int64_t>(rho0 + c0) * a1.I + n;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (c < ncol)
-                            hrow[static_cast<int64_t>(c) * a1.I] =
-                                __float2half_rn(silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c])));
+                        for (int c = 0; c < 32; ++c)
+                            if (c < ncol) {
+                                const float hv = silu_mul(__fmul_rn(__uint_as_float(g[c]), ce),
+                                                          __fmul_rn(__uint_as_float(u[c]), ce));
+                                const float amax =
+                                    __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv))));
+                                hrow[static_cast<int64_t>(c) * a1.I] =
+                                    static_cast<uint16_t>(qa_value_f16(hv, qa_block(amax, qa_alpha, qa_r6)));
+                            }
+                    } else {
+                        __half *hrow = a1.hg + static_cast<int64_t>(rho0 + c0) * a1.I + (n & ~7) + interleave_pos(n & 7);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (c < ncol)
+                                hrow[static_cast<int64_t>(c) * a1.I] =
+                                    __float2half_rn(silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c])));
+                    }
                 } else {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -489,7 +663,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
             const int sb = ti & 1;
             const int G = t < total1 ? a1.G : a2.G, KT = t < total1 ? a1.KT : a2.KT;
-            if (!tc::mbar_wait(sfull0 + 8 * sb, (ti >> 1) & 1u, abort_flag, kWaitNs) && a1.dev_status)
+            if (!kN && !tc::mbar_wait(sfull0 + 8 * sb, (ti >> 1) & 1u, abort_flag, kWaitNs) && a1.dev_status)
                 atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
             const uint16_t *sc = reinterpret_cast<const uint16_t *>(sbuf + sb * SBUF);
             const uint32_t *zs = reinterpret_cast<const uint32_t *>(sbuf + sb * SBUF + 512 * G);
@@ -497,14 +671,31 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                 const int i = v >> 1, h = v & 1;
                 const int kt = i - kbase;              // = the quantization group
                 const int r = 128 * h + m;             // row of the tile
-                const uint32_t sv = sc[r * G + kt];
-                const uint32_t zv = (zs[(r >> 3) * G + kt] >> zsh) & 0xFu;
-                const uint32_t sc2 = sv | (sv << 16), zb2 = 0x64006400u | zv | (zv << 16);
-                const uint32_t zb16 = 0xD400D400u | (zv << 4) | (zv << 20);   // -(64 + z): ulp 1/16 in [64, 128)
+                uint32_t sc2 = 0, zb2 = 0, zb16 = 0;
+                if (!kN) {
+                    const uint32_t sv = sc[r * G + kt];
+                    const uint32_t zv = (zs[(r >> 3) * G + kt] >> zsh) & 0xFu;
+                    sc2 = sv | (sv << 16);
+                    zb2 = 0x64006400u | zv | (zv << 16);
+                    zb16 = 0xD400D400u | (zv << 4) | (zv << 20);   // -(64 + z): ulp 1/16 in [64, 128)
+                }
                 if (!tc::mbar_wait(rfull0 + 8 * s, ph, abort_flag, kWaitNs) && a1.dev_status)
                     atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
-                const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * SB + geo.raw_off() + r * 64);
-                const uint4 w0 = src[0], w1 = src[1], w2 = src[2], w3 = src[3];
+                // AWQ: 64 packed bytes of row r; NVFP4S: 32 bytes of kept codes and the 16-byte side record
+                uint4 w0, w1, w2, w3;
+                if (kN) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * SB + geo.raw_off() + r * 32);
+                    w0 = src[0];
+                    w1 = src[1];
+                    w2 = *reinterpret_cast<const uint4 *>(smem + s * SB + geo.side_off() + r * kNv4SideBytes);
+                    w3 = make_uint4(0, 0, 0, 0);
+                } else {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * SB + geo.raw_off() + r * 64);
+                    w0 = src[0];
+                    w1 = src[1];
+                    w2 = src[2];
+                    w3 = src[3];
+                }
                 __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive(rempty0 + 8 * s);  // packed bytes read
@@ -518,15 +709,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                         atomicCAS(a1.dev_status + 1, 0, static_cast<int>(MOE_ERR_TIMEOUT));
                 }
                 tc::tc_fence_after();
-                {
+                if (kN) {
                     uint32_t out[32];
-                    dq_words(w0, w1, zb2, zb16, sc2, out);   // values 0..63 -> columns 0..31
+                    dq_nv4_words(w0, w2.x, w2.z & 0xFFFFu, out);   // weights 0..63 -> columns 0..31
                     tc::tmem_st_32x32b_x32(a_lane + 64 * sa, out);
-                }
-                {
-                    uint32_t out[32];
-                    dq_words(w2, w3, zb2, zb16, sc2, out);   // values 64..127 -> columns 32..63
+                    dq_nv4_words(w1, w2.y, w2.z >> 16, out);       // weights 64..127 -> columns 32..63
                     tc::tmem_st_32x32b_x32(a_lane + 64 * sa + 32, out);
+                } else {
+                    {
+                        uint32_t out[32];
+                        dq_words(w0, w1, zb2, zb16, sc2, out);   // values 0..63 -> columns 0..31
+                        tc::tmem_st_32x32b_x32(a_lane + 64 * sa, out);
+                    }
+                    {
+                        uint32_t out[32];
+                        dq_words(w2, w3, zb2, zb16, sc2, out);   // values 64..127 -> columns 32..63
+                        tc::tmem_st_32x32b_x32(a_lane + 64 * sa + 32, out);
+                    }
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
@@ -544,7 +743,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CU
                     sa -= AS;
             }
             __syncwarp();
-            if (lane == 0)
+            if (!kN && lane == 0)
                 tc::mbar_arrive(sempty0 + 8 * sb);
             kbase += KT;
         }
@@ -596,6 +795,107 @@ __global__ void gather_kernel(const XT *__restrict__ x, int d, int k, int MK, co
         }
         reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(rho) * d)[c] = out;
     }
+}
+
+// Xg[rho] = S * E2M1 of Q_a(x[route / k]) as fp16 bits, natural order (the
+// block's tensor-wide scale alpha_x left out; padding rows zero).  Each
+// thread takes 8 values; 4 neighbouring threads form a block of 32 and share
+// its maximum (d % 256 == 0, so a warp's 32 threads lie in one row).
+template <typename XT>
+__global__ void gather_nv4_kernel(const XT *__restrict__ x, int d, int k, int MK, const int32_t *__restrict__ sorted,
+                                  const int32_t *__restrict__ npp, uint16_t *__restrict__ xg, int b,
+                                  int32_t *__restrict__ done, int cap_rows, int32_t *__restrict__ dev_status,
+                                  const float *__restrict__ qa)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    int rows = *npp;
+    if (!MOE_IN_BOUNDS(rows >= 0 && rows <= cap_rows, dev_status))
+        rows = 0;
+    for (int jb = blockIdx.x * blockDim.x + threadIdx.x; jb < rows / b; jb += gridDim.x * blockDim.x)
+        done[jb] = 0;
+    const float alpha = qa[0], r6 = qa[1];
+    const int d8 = d / 8;
+    const int64_t total = static_cast<int64_t>(rows) * d8;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int rho = static_cast<int>(i / d8), c = static_cast<int>(i - static_cast<int64_t>(rho) * d8);
+        int r = sorted[rho];
+        if (!MOE_IN_BOUNDS(r >= 0 && r <= MK, dev_status))
+            r = MK;                                   // read as padding
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (r < MK) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(r / k) * d) + c);
+            const uint32_t o[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if constexpr (std::is_same<XT, __half>::value) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&o[j]));
+                    v[2 * j] = f.x;
+                    v[2 * j + 1] = f.y;
+                } else {
+                    v[2 * j] = __uint_as_float(o[j] << 16);
+                    v[2 * j + 1] = __uint_as_float(o[j] & 0xFFFF0000u);
+                }
+            }
+        }
+        float am = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            am = fmaxf(am, fabsf(v[j]));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        const QaBlock qb = qa_block(am, alpha, r6);
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            out[j] = qa_value_f16(v[2 * j], qb) | (qa_value_f16(v[2 * j + 1], qb) << 16);
+        reinterpret_cast<uint4 *>(xg + static_cast<int64_t>(rho) * d)[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
+// Prepared NVFP4S projection (moe_grouped_prepare_nvfp4s): a 256-byte head
+// (alpha_in, binary32(1 / (6 alpha_in)) of the activation the projection
+// takes), the per-expert factors alpha_w[e] * alpha_in (fp32 [E], rounded up
+// to 256 bytes), then one 16-byte side record per weight row and k-step of
+// 128: that k-step's 8 pattern bytes, its 4 UE4M3 scale bytes, 4 zero bytes.
+struct Nv4Prep {
+    size_t head, ce, side, total;
+};
+
+static Nv4Prep nv4_prep_layout(int E, int N, int K)
+{
+    Nv4Prep P;
+    P.head = 0;
+    P.ce = 256;
+    P.side = P.ce + ws_round(static_cast<size_t>(E) * sizeof(float));
+    P.total = P.side + static_cast<size_t>(E) * N * (K / 128) * kNv4SideBytes;
+    return P;
+}
+
+__global__ void prepare_nv4_side_kernel(const uint8_t *__restrict__ meta, const uint8_t *__restrict__ sc, int64_t rows,
+                                        int K, uint4 *__restrict__ side)
+{
+    const int KS = K / 128;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * KS;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = i / KS;
+        const int kt = static_cast<int>(i - row * KS);
+        const uint2 m = *reinterpret_cast<const uint2 *>(meta + row * (K / 16) + 8 * kt);
+        const uint32_t s4 = *reinterpret_cast<const uint32_t *>(sc + row * (K / 32) + 4 * kt);
+        side[i] = make_uint4(m.x, m.y, s4, 0u);
+    }
+}
+
+__global__ void prepare_nv4_head_kernel(const float *__restrict__ alpha_w, int E, float alpha_in, float r6,
+                                        float *__restrict__ head, float *__restrict__ ce)
+{
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        head[0] = alpha_in;
+        head[1] = r6;
+    }
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x)
+        ce[e] = __fmul_rn(alpha_w[e], alpha_in);
 }
 
 struct WsLayout {
@@ -658,7 +958,7 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     if (aslots < kDqGroups || smem > 227 * 1024)
         return MOE_ERR_UNSUPPORTED;
     static std::atomic<uint64_t> attr_done{0};
-    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(gemm_kernel), 227 * 1024))
+    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(gemm_kernel<kAwq>), 227 * 1024))
         return MOE_ERR_CUDA;
 
     // tensor maps: packed weights as bytes [E*N][K/2]; activations fp16 [cap_rows][K]
@@ -687,8 +987,106 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
     Args a2{static_cast<const uint16_t *>(w2->scale), static_cast<const int32_t *>(w2->zero), expert_ids, npp, sorted,
             wts, nullptr, yr, dev_status, b, n_mma, d / 256, I / 128, I, d, static_cast<int>(mk), d, G2, stages,
             aslots, acc_cols, nbuf, E, cap_rows / b};
-    if (launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, tQ2, tB2, a1, a2, done, Gmax) !=
-        cudaSuccess)
+    if (launch_pdl(gemm_kernel<kAwq>, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, tQ2, tB2, tQ1, tQ2, a1, a2, done,
+                   Gmax) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return grouped_combine_launch(yr, ids, M, k, d, E, y, y_f32, s);
+}
+
+size_t grouped_nv4_prepare_bytes(int E, int N, int K)
+{
+    return ga::nv4_prep_layout(E, N, K).total;
+}
+
+moe_status_t grouped_nv4_prepare(const moe_weights_t *w, float alpha_in, void *out, cudaStream_t s)
+{
+    using namespace ga;
+    const Nv4Prep P = nv4_prep_layout(w->E, w->N, w->K);
+    uint8_t *o = static_cast<uint8_t *>(out);
+    const float r6 = static_cast<float>(1.0 / (6.0 * static_cast<double>(alpha_in)));
+    prepare_nv4_head_kernel<<<1, 256, 0, s>>>(w->alpha, w->E, alpha_in, r6, reinterpret_cast<float *>(o + P.head),
+                                              reinterpret_cast<float *>(o + P.ce));
+    if (launch_status() != MOE_OK)
+        return MOE_ERR_CUDA;
+    const int64_t rows = static_cast<int64_t>(w->E) * w->N;
+    const int64_t n = rows * (w->K / 128);
+    const int blocks = static_cast<int>(n / 256 + 1 < 4096 ? n / 256 + 1 : 4096);
+    prepare_nv4_side_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t *>(w->zero),
+                                                   static_cast<const uint8_t *>(w->scale), rows, w->K,
+                                                   reinterpret_cast<uint4 *>(o + P.side));
+    return launch_status();
+}
+
+moe_status_t grouped_nv4_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
+                                const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                const void *p13, const void *p2, const int32_t *sorted, const int32_t *expert_ids,
+                                const int32_t *npp, int b, int cap_rows, void *y, bool y_f32, void *ws,
+                                int32_t *dev_status, cudaStream_t s)
+{
+    using namespace ga;
+    const int64_t mk = static_cast<int64_t>(M) * k;
+    const int n_mma = (b + 15) / 16 * 16;
+    const WsLayout L = ws_layout(M, k, d, I, b, cap_rows);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint16_t *xg = reinterpret_cast<uint16_t *>(w + L.xg);
+    __half *hg = reinterpret_cast<__half *>(w + L.hg);
+    float *yr = reinterpret_cast<float *>(w + L.yr);
+    int32_t *done = reinterpret_cast<int32_t *>(w + L.done);
+    const Nv4Prep P13 = nv4_prep_layout(E, 2 * I, d), P2 = nv4_prep_layout(E, d, I);
+    const uint8_t *q13 = static_cast<const uint8_t *>(p13), *q2 = static_cast<const uint8_t *>(p2);
+
+    if (n_mma > 128 || d % 256 || I % 128)
+        return MOE_ERR_UNSUPPORTED;
+    const int stage_bytes = Geo{n_mma, 1}.bytes();
+    const size_t fixed = 1024 + kHeaderBytes + 512 * 4;
+    int stages = static_cast<int>((227 * 1024 - fixed) / stage_bytes);
+    stages = stages > kMaxStages ? kMaxStages : stages;
+    const int acc_cols = (n_mma + 31) / 32 * 32;
+    const int nbuf = 4 * acc_cols + 64 * kDqGroups <= static_cast<int>(kTmemCols) ? 2 : 1;
+    int aslots = (static_cast<int>(kTmemCols) - 2 * nbuf * acc_cols) / 64;
+    aslots = aslots > kMaxASlots ? kMaxASlots : aslots;
+    aslots = aslots > 2 * stages - 2 ? 2 * stages - 2 : aslots;
+    const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
+    if (aslots < kDqGroups || smem > 227 * 1024)
+        return MOE_ERR_UNSUPPORTED;
+    static std::atomic<uint64_t> attr_done{0};
+    if (!smem_attr_once(attr_done, reinterpret_cast<const void *>(gemm_kernel<kNv4>), 227 * 1024))
+        return MOE_ERR_CUDA;
+
+    // tensor maps: kept codes as bytes [E*N][K/4]; side records [E*N][K/128 * 16]; activations fp16 [cap_rows][K]
+    CUtensorMap tQ1, tB1, tQ2, tB2, tS1, tS2;
+    if (!grouped_tmap_2d(&tQ1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w13->q, d / 4, static_cast<uint64_t>(E) * 2 * I, 32,
+                         128, false) ||
+        !grouped_tmap_2d(&tS1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q13 + P13.side, (d / 128) * kNv4SideBytes,
+                         static_cast<uint64_t>(E) * 2 * I, kNv4SideBytes, 128, false) ||
+        !grouped_tmap_2d(&tB1, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xg, d, cap_rows, 64, n_mma, true) ||
+        !grouped_tmap_2d(&tQ2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w2->q, I / 4, static_cast<uint64_t>(E) * d, 32, 128,
+                         false) ||
+        !grouped_tmap_2d(&tS2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q2 + P2.side, (I / 128) * kNv4SideBytes,
+                         static_cast<uint64_t>(E) * d, kNv4SideBytes, 128, false) ||
+        !grouped_tmap_2d(&tB2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hg, I, cap_rows, 64, n_mma, true))
+        return MOE_ERR_CUDA;
+
+    const float *qa_x = reinterpret_cast<const float *>(q13 + P13.head);
+    const float *qa_h = reinterpret_cast<const float *>(q2 + P2.head);
+    const int gblocks = grouped_sm_count() * 4;
+    const cudaError_t ge =
+        x_bf16 ? launch_pdl(gather_nv4_kernel<__nv_bfloat16>, dim3(gblocks), dim3(256), 0, s,
+                            static_cast<const __nv_bfloat16 *>(x), d, k, static_cast<int>(mk), sorted, npp, xg, b, done,
+                            cap_rows, dev_status, qa_x)
+               : launch_pdl(gather_nv4_kernel<__half>, dim3(gblocks), dim3(256), 0, s, static_cast<const __half *>(x),
+                            d, k, static_cast<int>(mk), sorted, npp, xg, b, done, cap_rows, dev_status, qa_x);
+    if (ge != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int grid = grouped_sm_count();
+    Args a1{nullptr, nullptr, expert_ids, npp, sorted, wts, hg, nullptr, dev_status, b, n_mma, I / 128, d / 128, I, d,
+            static_cast<int>(mk), 2 * I, d / 128, stages, aslots, acc_cols, nbuf, E, cap_rows / b,
+            reinterpret_cast<const float *>(q13 + P13.ce), qa_h};
+    Args a2{nullptr, nullptr, expert_ids, npp, sorted, wts, nullptr, yr, dev_status, b, n_mma, d / 256, I / 128, I, d,
+            static_cast<int>(mk), d, I / 128, stages, aslots, acc_cols, nbuf, E, cap_rows / b,
+            reinterpret_cast<const float *>(q2 + P2.ce), nullptr};
+    if (launch_pdl(gemm_kernel<kNv4>, dim3(grid), dim3(kThreads), smem, s, tQ1, tB1, tQ2, tB2, tS1, tS2, a1, a2, done,
+                   0) != cudaSuccess)
         return MOE_ERR_CUDA;
     return grouped_combine_launch(yr, ids, M, k, d, E, y, y_f32, s);
 }

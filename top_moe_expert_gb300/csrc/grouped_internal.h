@@ -26,4 +26,13 @@ moe_status_t grouped_awq_launch(const void *x, bool x_bf16, int M, int d, int I,
                                 const int32_t *sorted, const int32_t *expert_ids, const int32_t *npp, int b,
                                 int cap_rows, void *y, bool y_f32, void *ws, int32_t *dev_status, cudaStream_t s);
 
+// paired 4:8 sparse NVFP4 grouped path (the same kernel, W4A4 with Q_a)
+size_t grouped_nv4_prepare_bytes(int E, int N, int K);
+moe_status_t grouped_nv4_prepare(const moe_weights_t *w, float alpha_in, void *out, cudaStream_t s);
+moe_status_t grouped_nv4_launch(const void *x, bool x_bf16, int M, int d, int I, int E, const int32_t *ids,
+                                const float *wts, int k, const moe_weights_t *w13, const moe_weights_t *w2,
+                                const void *p13, const void *p2, const int32_t *sorted, const int32_t *expert_ids,
+                                const int32_t *npp, int b, int cap_rows, void *y, bool y_f32, void *ws,
+                                int32_t *dev_status, cudaStream_t s);
+
 }  // namespace moe

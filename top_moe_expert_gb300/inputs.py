@@ -164,6 +164,33 @@ def awq_weights(wl: Workload, which: str, experts=None):
     return q, s, z
 
 
+# the six paired 4:8 patterns as nibbles p0 | p1 << 2 (p0 < p1, kept pair indices)
+NV4_PATTERNS = np.array([a | (b << 2) for a in range(4) for b in range(a + 1, 4)], dtype=np.uint8)
+
+
+def nvfp4s_weights(wl: Workload, which: str, experts=None):
+    """Random admissible paired 4:8 sparse NVFP4 weights (no quantizer: the
+    packed fields are drawn directly): v uint8 [E,N,K/4] of uniform random
+    E2M1 codes, m uint8 [E,N,K/16] of patterns drawn uniformly from the six,
+    s uint8 [E,N,K/32] UE4M3 codes uniform in [0x30, 0x40] (0.5 .. 2), and
+    alpha float32 [E] = 0.01 (kept weights of RMS about 0.03, the draws'
+    N(0, 0.02) with half the pairs pruned)."""
+    N, K = (2 * wl.I, wl.d) if which == "w13" else (wl.d, wl.I)
+    experts = range(wl.E) if experts is None else experts
+    mat = 0 if which == "w13" else 1
+    n = len(experts)
+    v = np.empty((n, N, K // 4), dtype=np.uint8)
+    m = np.empty((n, N, K // 16), dtype=np.uint8)
+    sc = np.empty((n, N, K // 32), dtype=np.uint8)
+    for i, e in enumerate(experts):
+        g = rng(wl.seed, 300000 + 2 * int(e) + mat)
+        v[i] = g.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+        pat = NV4_PATTERNS[g.integers(0, 6, size=(N, K // 8))]
+        m[i] = pat[:, 0::2] | (pat[:, 1::2] << 4)
+        sc[i] = g.integers(0x30, 0x41, size=(N, K // 32), dtype=np.uint8)
+    return v, m, sc, np.full(n, 0.01, dtype=np.float32)
+
+
 def bits16(t: torch.Tensor) -> np.ndarray:
     """Raw 16-bit patterns of a bf16/fp16 tensor, as numpy uint16."""
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
