@@ -210,11 +210,12 @@ SRC_FILES = {
     "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh",
                 "attr.h"),
     "awq": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "common.cuh", "tc.cuh", "attr.h"),
-    "awq_decode": ("decode.cu", "decode_pipe_awq.cu", "decode_internal.h", "common.cuh", "tc.cuh", "attr.h"),
+    "awq_decode": ("decode.cu", "decode_pipe_awq.cu", "pipe_common.cuh", "decode_internal.h", "common.cuh", "tc.cuh",
+                   "attr.h"),
     "nv4": ("grouped_awq.cu", "grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh",
             "tc.cuh", "attr.h"),
-    "nv4_decode": ("decode.cu", "decode_nvfp4s.cu", "nvfp4s.cuh", "decode_internal.h", "topk.cu", "topk.cuh",
-                   "common.cuh", "attr.h"),
+    "nv4_decode": ("decode.cu", "decode_pipe_nv4.cu", "pipe_common.cuh", "decode_nvfp4s.cu", "nvfp4s.cuh",
+                   "decode_internal.h", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh", "attr.h"),
 }
 
 
@@ -300,7 +301,7 @@ class Step:
                 moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w13", e, device), q13[e], s13[e])
                 moe.moe_mxfp8_quantize(inputs.weights_fp32_device(wl, "w2", e, device), q2[e], s2[e])
             w0 = ((q13, s13, None), (q2, s2, None))
-        self.routed_in_layer = wl.fmt == "mxfp8" and path == "decode" and M == 1 and E <= 768
+        self.routed_in_layer = wl.fmt in ("mxfp8", "nvfp4s") and path == "decode" and M == 1 and E <= 768
         # one AWQ token: the layer is one kernel (the routing is fixed, so it is not in it)
         self.awq_pipe = self.awq and path == "decode" and M == 1
         lw_bytes = sum(t.numel() * t.element_size() for p in w0 for t in p if t is not None)
@@ -462,6 +463,9 @@ class Step:
         if self.nv4 and self.path == "grouped":
             return ("moe_ffn_grouped (NVFP4S, W4A4): ga::gather_nv4_kernel (Q_a of x) + ga::gemm_kernel<Nv4> "
                     "(both GEMMs, weights expanded on chip, Q_a of h in the epilogue) + combine")
+        if self.nv4 and self.routed_in_layer:
+            return ("moe_ffn_decode_logits (NVFP4S): dpn::pipe_kernel (top-k routing + gate/up + SwiGLU + down + "
+                    "routing-weighted sum), one kernel")
         if self.nv4:
             return "moe_ffn_decode (NVFP4S): dn4::gate_up_kernel + dn4::down_kernel"
         if self.awq_pipe:
@@ -483,6 +487,9 @@ class Step:
         if self.nv4 and self.path == "grouped":
             return ("expert-centric grouped NVFP4S W4A4 (topk + align + Q_a gather + tcgen05 kind::f16 GEMM1/GEMM2 "
                     "on weights expanded in tensor memory + combine, b=%d)" % self.b)
+        if self.nv4 and self.routed_in_layer:
+            return ("single-token NVFP4S decode: routing + gate/up + SwiGLU + down in one kernel, h exchanged "
+                    "through L2, activations kept exact")
         if self.nv4:
             return "output-centric NVFP4S decode (topk + gate/up + down, activations kept exact)"
         if self.awq_pipe:

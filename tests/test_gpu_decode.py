@@ -393,10 +393,78 @@ def test_nvfp4s_decode_matches_oracle(xdt):
         gs.assert_layer_close(y, ref)
     torch.cuda.synchronize()
     assert st.tolist() == [2, 0]
-    y1 = moe.moe_ffn_decode(x[:1].cuda(), torch.from_numpy(ids[:1]).cuda(), torch.from_numpy(w[:1]).cuda(), w13, w2,
+    # a token's result does not depend on the batch's other tokens (two
+    # tokens and four take the same two-kernel form; one token takes the
+    # single-token kernel, checked on its own below)
+    y2 = moe.moe_ffn_decode(x[:2].cuda(), torch.from_numpy(ids[:2]).cuda(), torch.from_numpy(w[:2]).cuda(), w13, w2,
                             out_dtype=torch.float32)
-    assert torch.equal(y1[0], moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
-                                                 w13, w2, out_dtype=torch.float32)[0])
+    assert torch.equal(y2[:2], moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(),
+                                                  w13, w2, out_dtype=torch.float32)[:2])
+
+
+NV4_M1 = inputs.Workload("nvfp4s_m1_d2048_i768_e32_k8", M=1, d=2048, I=768, E=32, k=8, seed=24)
+NV4_M1_SMALL = inputs.Workload("nvfp4s_m1_d1024_i512_e16_k4", M=1, d=1024, I=512, E=16, k=4, seed=25)
+_NV4_CACHE = {}
+
+
+def _nv4_cached(wl):
+    if wl.name not in _NV4_CACHE:
+        _NV4_CACHE[wl.name] = _nvfp4s_layer(wl)
+    return _NV4_CACHE[wl.name]
+
+
+@pytest.mark.parametrize("wl", [NV4_M1_SMALL, NV4_M1], ids=lambda w: w.name)
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float16])
+def test_nvfp4s_single_token(wl, xdt):
+    """One token, paired 4:8 sparse NVFP4: the one-kernel path against the
+    oracle (exact activations), and the counter of the kernel's launches
+    shows that the one-kernel path ran."""
+    w13, w2, p13, p2 = _nv4_cached(wl)
+    x = inputs.activations(wl, dtype=xdt)
+    ids, w = gs.routing(wl)
+    ref = oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, p13, p2)["y"]
+    ws = torch.zeros(moe.moe_ffn_decode_workspace_size(1, wl.k, wl.d, wl.I), dtype=torch.uint8, device="cuda")
+    for out_dtype in (torch.float32, torch.bfloat16):
+        y = moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), w13, w2,
+                               out_dtype=out_dtype, ws=ws)
+        gs.assert_layer_close(y, ref)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ws[:8].view(torch.int64).item() == 2 * sms
+
+
+def test_nvfp4s_single_token_routes_and_repeats():
+    wl = NV4_M1_SMALL
+    w13, w2, p13, p2 = _nv4_cached(wl)
+    x = inputs.activations(wl, dtype=torch.bfloat16)
+    ids = np.array([[5, 5, -1, wl.E]], dtype=np.int32)           # a duplicate and two invalid routes
+    w = np.array([[0.4, 0.3, 0.2, 0.1]], dtype=np.float32)
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ys = [moe.moe_ffn_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), w13, w2,
+                             out_dtype=torch.float32, dev_status=st) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert st.tolist() == [6, 0]
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+    gs.assert_layer_close(ys[0], oracle.moe_layer(gs.x_exact(x), ids, w.astype(np.float64), wl.E, p13, p2)["y"])
+
+
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float16])
+def test_nvfp4s_decode_logits_equals_topk_then_decode(xdt):
+    """One token, NVFP4S: the routing inside the one kernel gives, bit for
+    bit, moe_topk_softmax followed by moe_ffn_decode."""
+    wl = NV4_M1
+    w13, w2, p13, p2 = _nv4_cached(wl)
+    x = inputs.activations(wl, dtype=xdt).cuda()
+    logits = torch.from_numpy(inputs.router_logits(wl)).cuda()
+    y1, ids1, w1 = moe.moe_ffn_decode_logits(logits, x, wl.k, w13, w2, out_dtype=torch.float32)
+    ids2, wt2 = moe.moe_topk_softmax(logits, wl.k)
+    y2 = moe.moe_ffn_decode(x, ids2, wt2, w13, w2, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(ids1, ids2) and torch.equal(w1, wt2)
+    assert torch.equal(y1, y2)
+    gs.assert_layer_close(y1, oracle.moe_layer(gs.x_exact(x.cpu()), ids2.cpu().numpy(),
+                                               wt2.cpu().numpy().astype(np.float64), wl.E, p13, p2)["y"])
 
 
 @pytest.mark.parametrize("xdt", [torch.float16, torch.bfloat16])

@@ -347,6 +347,14 @@ static moe_status_t check_weights(const moe_weights_t *w, int N, int K)
     return MOE_OK;
 }
 
+// the single-token NVFP4S kernel's bulk copies want 16-byte aligned code,
+// pattern and gate/up scale arrays; its down scales are read 8 bytes at a time
+static bool nv4_pipe_aligned(const moe_weights_t *w13, const moe_weights_t *w2)
+{
+    return aligned(w13->q, 16) && aligned(w13->zero, 16) && aligned(w13->scale, 16) && aligned(w2->q, 16) &&
+           aligned(w2->zero, 16) && aligned(w2->scale, 8) && w13->alpha && w2->alpha;
+}
+
 MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32_t d,
                                     const int32_t *topk_ids, const float *topk_w, int32_t k,
                                     const moe_weights_t *w13, const moe_weights_t *w2,
@@ -389,6 +397,11 @@ MOE_API moe_status_t moe_ffn_decode(const void *x, int32_t xdt, int32_t M, int32
     // past the reserved bytes: h of the two-kernel and per-scalar paths
     float *h = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWsReserved);
     cudaStream_t s = as_stream(stream);
+    if (fmt == MOE_W_NVFP4S && decode_pipe_nv4_eligible(M, k, d, I, w13->E) && nv4_pipe_aligned(w13, w2)) {
+        // one token, paired 4:8 sparse NVFP4: one kernel (gate/up, SwiGLU, down)
+        return decode_pipe_nv4_launch(x, xdt == MOE_BF16, d, I, w13->E, topk_ids, topk_w, nullptr, nullptr, nullptr, k,
+                                      w13, w2, y, ydt == MOE_FP32, ws, dev_status, s);
+    }
     if (fmt == MOE_W_NVFP4S)
         return decode_nvfp4s_launch(x, xdt == MOE_BF16, M, d, I, w13->E, topk_ids, topk_w, k, w13, w2, y,
                                     ydt == MOE_FP32, h, dev_status, s);
@@ -468,6 +481,18 @@ MOE_API moe_status_t moe_ffn_decode_logits(const float *logits, const void *x, i
         if (!ws || ws_bytes < need || !aligned(ws, 256))
             return MOE_ERR_WORKSPACE;
         return decode_pipe_awq_launch(x, xdt == MOE_BF16, d, I, E, nullptr, nullptr, logits, topk_ids, topk_w, k,
+                                      w13, w2, y, ydt == MOE_FP32, ws, dev_status, as_stream(stream));
+    }
+    // one token, paired 4:8 sparse NVFP4: one kernel with the routing inside
+    if (M == 1 && w2->fmt == MOE_W_NVFP4S && w13->fmt == MOE_W_NVFP4S && (xdt == MOE_BF16 || xdt == MOE_FP16) &&
+        (ydt == MOE_BF16 || ydt == MOE_FP32) && check_weights(w13, 2 * I, d) == MOE_OK &&
+        check_weights(w2, d, I) == MOE_OK && w2->E == E && decode_pipe_nv4_eligible(1, k, d, I, E) &&
+        decode_pipe_nv4_route_eligible(E, k) && nv4_pipe_aligned(w13, w2) && x && y && aligned(x, 16)) {
+        size_t need;
+        moe_ffn_decode_workspace_size(M, k, d, I, &need);
+        if (!ws || ws_bytes < need || !aligned(ws, 256))
+            return MOE_ERR_WORKSPACE;
+        return decode_pipe_nv4_launch(x, xdt == MOE_BF16, d, I, E, nullptr, nullptr, logits, topk_ids, topk_w, k,
                                       w13, w2, y, ydt == MOE_FP32, ws, dev_status, as_stream(stream));
     }
     // otherwise: routing, then the layer

@@ -51,6 +51,16 @@ moe_status_t decode_pipe_awq_launch(const void *x, bool x_bf16, int d, int I, in
                                     const moe_weights_t *w13, const moe_weights_t *w2, void *y, bool y_f32, void *ws,
                                     int32_t *dev_status, cudaStream_t s);
 
+// single-token paired 4:8 sparse NVFP4 layer in one kernel (decode_pipe_nv4.cu),
+// the same structure and workspace use as decode_pipe.cu; x fp16 or bf16
+bool decode_pipe_nv4_shape_fits(int k, int d, int I, int G);
+bool decode_pipe_nv4_eligible(int M, int k, int d, int I, int E);
+bool decode_pipe_nv4_route_eligible(int E, int k);
+moe_status_t decode_pipe_nv4_launch(const void *x, bool x_bf16, int d, int I, int E, const int32_t *ids,
+                                    const float *wts, const float *logits, int32_t *ids_out, float *wts_out, int k,
+                                    const moe_weights_t *w13, const moe_weights_t *w2, void *y, bool y_f32, void *ws,
+                                    int32_t *dev_status, cudaStream_t s);
+
 // paired 4:8 sparse NVFP4 decode (decode_nvfp4s.cu): a gate/up kernel and a
 // down kernel, h [M*k][I] f32 in `h`
 bool decode_nvfp4s_eligible(int k, int d, int I);

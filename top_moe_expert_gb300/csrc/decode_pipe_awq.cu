@@ -32,6 +32,7 @@
 #include "attr.h"
 #include "common.cuh"
 #include "decode_internal.h"
+#include "pipe_common.cuh"
 #include "tc.cuh"
 #include "topk.cuh"
 
@@ -122,131 +123,7 @@ struct Plan {
     }
 };
 
-__device__ __forceinline__ void set_err(int32_t *st, int code)
-{
-    if (st)
-        atomicCAS(st + 1, 0, code);
-}
-
-__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two)
-{
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(two)));
-    return r;
-}
-
-// acc + w.lo * a.lo + w.hi * a.hi: fp16 products exact in FP32, one rounding each
-__device__ __forceinline__ float fma2(uint32_t w, uint32_t a, float acc)
-{
-    asm("{\n .reg .f16 w0, w1, a0, a1;\n mov.b32 {w0, w1}, %1;\n mov.b32 {a0, a1}, %2;\n"
-        " fma.rn.f32.f16 %0, w0, a0, %0;\n fma.rn.f32.f16 %0, w1, a1, %0;\n}"
-        : "+f"(acc) : "r"(w), "r"(a));
-    return acc;
-}
-
-// four E4M3 codes (one word, byte order) -> two f16x2 words, exactly; the
-// word is split into its 16-bit halves without integer instructions
-__device__ __forceinline__ void cvt_e4m3x4(uint32_t q, uint32_t &w01, uint32_t &w23)
-{
-    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
-        " cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
-        : "=r"(w01), "=r"(w23) : "r"(q));
-}
-
-// sum over 4 E4M3 codes (one word, byte order) times 4 fp16 (two f16x2 words)
-__device__ __forceinline__ float dot4(uint32_t q, uint32_t a01, uint32_t a23, float acc)
-{
-    uint32_t w01, w23;
-    cvt_e4m3x4(q, w01, w23);
-    acc = fma2(w01, a01, acc);
-    return fma2(w23, a23, acc);
-}
-
-// KPL bytes at p (16-byte aligned for KPL >= 16, KPL-aligned otherwise) into words
-template <int KPL>
-__device__ __forceinline__ void lds_codes(const uint8_t *p, uint32_t (&w)[KPL / 4])
-{
-    if constexpr (KPL == 4) {
-        w[0] = *reinterpret_cast<const uint32_t *>(p);
-    } else if constexpr (KPL == 8) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(p);
-        w[0] = v.x; w[1] = v.y;
-    } else {
-#pragma unroll
-        for (int i = 0; i < KPL / 16; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(p + 16 * i);
-            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-        }
-    }
-}
-
-// Sum over 8 values of 32 lanes at once: lane l ends with the total of value
-// v_index(l) = 4 * bit4(l) + 2 * bit3(l) + bit2(l) in every lane of its quad.
-__device__ __forceinline__ float reduce8(const float (&v)[8], int lane)
-{
-    float u[4], t[2];
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = b4 ? v[i] : v[i + 4];
-        u[i] = (b4 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = b3 ? u[i] : u[i + 2];
-        t[i] = (b3 ? u[i + 2] : u[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    float r = (b2 ? t[1] : t[0]) + __shfl_xor_sync(0xffffffffu, b2 ? t[0] : t[1], 4);
-    r += __shfl_xor_sync(0xffffffffu, r, 2);
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
-    return r;
-}
-
-// exponent p with m * 2^p in [2^14, 2^15) for a finite m > 0 (the largest
-// magnitude of a vector); 0 for m == 0
-__device__ __forceinline__ int f16_shift(float m)
-{
-    if (!(m > 0.f))
-        return 0;
-    int ex;
-    frexpf(m, &ex);            // m = f * 2^ex, f in [0.5, 1)
-    const int p = 15 - ex;
-    return p < -100 ? -100 : (p > 100 ? 100 : p);
-}
-
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void red_relaxed_add(unsigned long long *p)
-{
-    asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p) : "memory");
-}
-
-// one (value, tag) word of the h exchange: 8-byte aligned, so single-copy atomic
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// two consecutive exchange words (16-byte aligned); each word is read
-// single-copy atomically on its own
-__device__ __forceinline__ void ld_relaxed_u64x2(const unsigned long long *p, unsigned long long &a,
-                                                 unsigned long long &b)
-{
-    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
+using namespace pipe;
 
 // The (q - z) pairs of one packed word, exact, as fp16x2: o[j] holds
 // (n_j - z, n_{j+4} - z); zz2 is the fp16 pair (1024 + z, 1024 + z).

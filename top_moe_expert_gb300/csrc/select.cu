@@ -17,7 +17,10 @@
 // loses to the grouped path at every M measured (at d = 7168, I = 2048,
 // E = 384, M = 1: 250 us against 80.9 us).  For 4-bit AWQ the single-token
 // kernel is ahead at one token (14.7 against 34.3 us for the grouped path)
-// and the grouped path from two tokens (far ahead at M = 21).
+// and the grouped path from two tokens (far ahead at M = 21).  For paired
+// 4:8 sparse NVFP4 the single-token kernel takes one token and the W4A4
+// grouped path every batch from two tokens (40.9 us at M = 1 against 76 us
+// for the two-kernel decode, and faster at every larger M measured).
 // Host only: nothing here touches a GPU.
 #include "common.cuh"
 #include "decode_internal.h"
@@ -28,6 +31,8 @@ static bool decode_shape_ok(int k, int d, int I, int fmt)
 {
     if (static_cast<size_t>(k) * I * sizeof(float) > 200 * 1024)
         return false;
+    if (fmt == MOE_W_NVFP4S)
+        return d % 64 == 0 && I % 64 == 0;
     return fmt == MOE_W_MXFP8 ? (d % 512 == 0 && I % 32 == 0) : (d % 1024 == 0 && I % 128 == 0);
 }
 
@@ -37,6 +42,8 @@ static bool grouped_shape_ok(int d, int I, int b, int fmt)
         return false;
     if (fmt == MOE_W_AWQ4)
         return d % 256 == 0 && d / 128 <= 64 && I / 128 <= 64 && b <= 128 && (d <= 8064 || b <= 112);
+    if (fmt == MOE_W_NVFP4S)
+        return d % 256 == 0 && b <= 128;
     return true;
 }
 
@@ -53,12 +60,12 @@ MOE_API moe_status_t moe_ffn_select_path(int32_t M, int32_t k, int32_t E, int32_
 {
     if (M < 0 || k < 1 || k > 32 || E < 1 || d < 1 || I < 1 || !path || !block)
         return MOE_ERR_INVALID_ARG;
-    if (fmt != MOE_W_MXFP8 && fmt != MOE_W_AWQ4)
+    if (fmt != MOE_W_MXFP8 && fmt != MOE_W_AWQ4 && fmt != MOE_W_NVFP4S)
         return MOE_ERR_UNSUPPORTED;
     // block size: twice the expected rows per expert, a power of two within
-    // [16, 128] (MXFP8) or [8, 128] (AWQ), so most experts fill one block
+    // [16, 128] (MXFP8) or [8, 128] (AWQ, NVFP4S), so most experts fill one block
     const int64_t rows = 2 * static_cast<int64_t>(M) * k / E;
-    int b = fmt == MOE_W_AWQ4 ? 8 : 16;
+    int b = fmt == MOE_W_MXFP8 ? 16 : 8;
     while (b < rows && b < 128)
         b *= 2;
     if (fmt == MOE_W_AWQ4 && d > 8064 && b > 64)
@@ -66,8 +73,10 @@ MOE_API moe_status_t moe_ffn_select_path(int32_t M, int32_t k, int32_t E, int32_
     const bool dec = decode_shape_ok(k, d, I, fmt), grp = grouped_shape_ok(d, I, b, fmt);
     // the output-centric path for one token where its single-kernel form is
     // built for the format; the grouped path otherwise
-    const bool want_decode = M <= 1 && (fmt == MOE_W_MXFP8 ? decode_pipe_shape_fits(k, d, I, kSelectSMs)
-                                                           : decode_pipe_awq_shape_fits(k, d, I, kSelectSMs));
+    const bool want_decode =
+        M <= 1 && (fmt == MOE_W_MXFP8  ? decode_pipe_shape_fits(k, d, I, kSelectSMs)
+                   : fmt == MOE_W_AWQ4 ? decode_pipe_awq_shape_fits(k, d, I, kSelectSMs)
+                                       : decode_pipe_nv4_shape_fits(k, d, I, kSelectSMs));
     if (want_decode ? dec : !grp) {
         if (!dec)
             return MOE_ERR_UNSUPPORTED;
