@@ -192,7 +192,7 @@ moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_
  * alignment, padding, scatter or combine buffer.
  *   x        [M][d] of xdt (MOE_BF16; MOE_FP16 or MOE_BF16 for AWQ)
  *   topk_ids int32 [M][k], topk_w fp32 [M][k]
- *   w13      N = 2I, K = d (MOE_W_MXFP8 or MOE_W_AWQ4)
+ *   w13      N = 2I, K = d (MOE_W_MXFP8, MOE_W_AWQ4 or MOE_W_NVFP4S)
  *   w2       N = d, K = I, same format as w13
  *   y        [M][d] of ydt (MOE_BF16 or MOE_FP32)
  *   ws       moe_ffn_decode_workspace_size bytes, 256-byte aligned; its
@@ -218,7 +218,15 @@ moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_
  * moe_ffn_decode_logits the routing runs in it too);
  * MXFP8 with M*k <= 512 -> a gate/up kernel and a
  * down kernel chained by programmatic dependent launch;
- * MOE_W_NVFP4S -> a gate/up kernel and a down kernel, one warp per
+ * MOE_W_AWQ4 or MOE_W_NVFP4S with M == 1 and (d, I) in {(1024, 256),
+ * (1024, 512), (2048, 512), (2048, 768)} (k <= 10 at d = 2048, I = 768 for
+ * AWQ, k <= 13 for NVFP4S) -> the same one-kernel structure on the 4-bit
+ * weights (AWQ: (q - z) exact in fp16, the group scale per lane; NVFP4S:
+ * kept pairs times the activation pairs at their pattern positions, the
+ * block scale per lane, alpha per row), code, pattern and scale arrays
+ * 16-byte aligned (NVFP4S down scales 8-byte aligned), with the routing
+ * inside under moe_ffn_decode_logits;
+ * MOE_W_NVFP4S otherwise -> a gate/up kernel and a down kernel, one warp per
  * intermediate / output scalar, 16-byte loads of 64 packed weights, the
  * kept values decoded on the fly, FP32 sums, h in ws past its first 256
  * bytes; d % 64 == 0, I % 64 == 0, x MOE_BF16 or MOE_FP16;
@@ -396,10 +404,17 @@ moe_status_t moe_ffn_grouped_batched(const void *x, int32_t xdt, int32_t M, int3
  *                decode is built for (k, d, I) (d = 1024, I = 256 or 512;
  *                d = 2048, I = 512 or 768), else MOE_PATH_GROUPED (14.7
  *                against 34.3 us at M = 1 on the decode shapes).
+ *   MOE_W_NVFP4S: MOE_PATH_DECODE for M <= 1 where the single-kernel NVFP4S
+ *                decode is built for (k, d, I) (the same (d, I) pairs),
+ *                else MOE_PATH_GROUPED (the W4A4 grouped path, which needs
+ *                moe_grouped_prepare_nvfp4s: 21.4 against 40.9 us at M = 1;
+ *                the grouped path from M = 2, faster than the two-kernel
+ *                decode at every M measured).  Blocks as for AWQ.
  * When the preferred path does not take the shape (the limits of
  * moe_ffn_decode and moe_ffn_grouped on d, I and k), the other one is
  * returned; when neither does, MOE_ERR_UNSUPPORTED.
- *   fmt    MOE_W_MXFP8 or MOE_W_AWQ4 (MOE_ERR_UNSUPPORTED otherwise)
+ *   fmt    MOE_W_MXFP8, MOE_W_AWQ4 or MOE_W_NVFP4S (MOE_ERR_UNSUPPORTED
+ *          otherwise)
  *   path   out: a moe_path_t
  *   block  out: the block size b for moe_align_block_size and
  *          moe_ffn_grouped when the path is grouped (twice the expected

@@ -176,3 +176,10 @@ def test_select_path_at_the_measured_crossover(L):
         sel(21, awq, d=1152, I=256)                          # AWQ: neither (d % 256, d % 1024)
     with pytest.raises(moe.MoeError):
         moe.moe_ffn_select_path(4, 8, 128, 2048, 768, 2)       # the retired K-outer MXFP8 layout
+    # paired 4:8 sparse NVFP4: one token on its single-kernel form, the W4A4
+    # grouped path from two tokens (blocks from 8, as AWQ)
+    nv4 = moe.MOE_W_NVFP4S
+    assert sel(1, nv4) == (D, 0) and sel(2, nv4) == (G, 8) and sel(512, nv4) == (G, 64)
+    assert sel(1, nv4, k=13) == (D, 0) and sel(1, nv4, k=14) == (G, 8)    # the exchange's tag words
+    assert sel(1, nv4, d=3072, I=256) == (G, 8)              # no single-kernel NVFP4S form at this shape
+    assert sel(4, nv4, d=1152, I=256) == (D, 0)              # grouped needs d % 256 == 0
