@@ -8,9 +8,10 @@
 // Trillion-Scale Mixture-of-Experts", App. A: in every group of 8 weights
 // two adjacent pairs are kept (E2M1 codes), one UE4M3 scale per 32 weights,
 // one FP32 constant alpha per expert and matrix.  The structure is the
-// single-token AWQ kernel's (one CTA per SM; warp 0 streams this CTA's
-// gate/up rows -- kept codes, patterns and scales, each a bulk copy -- and
-// then its down rows through one ring; four groups of four warps form
+// single-token AWQ kernel's (one CTA per SM; warp 0 streams the kept codes
+// of this CTA's gate/up rows and then its down rows through one ring, while
+// eight staging warps load the gate/up rows' patterns and scales; four
+// groups of four warps form
 // h = SiLU(g) * u and publish it as (value, launch tag) words; every CTA
 // reads all of h back once the words carry the launch's tag and forms its
 // d / G output rows of every route's down projection).
@@ -56,6 +57,7 @@ constexpr int kBarRoutes = 1;                         // named barriers: routes 
 constexpr int kBarTail = 2;                           //   the compute warps
 constexpr int kBarGroup0 = 3;                         //   gate/up group g: kBarGroup0 + g
 constexpr int kBarRank = kBarGroup0 + kGroups;        //   the compute warps ranking the logits
+constexpr int kBarSide = kBarRank + 1;                //   gate/up patterns, scales and constants staged
 constexpr int kSmemMax = 227 * 1024;
 
 struct Args {
@@ -78,28 +80,26 @@ struct Args {
 };
 
 // Shared-memory plan (bytes), identical on host and device.  A ring slot is
-// kPS gate rows then kPS up rows of kept codes, then the same 2 kPS rows'
-// patterns, then their scales; the down rows of every route reuse the ring
-// after the gate/up stages (codes of the CTA's rows, then their patterns;
-// their scales, 24 bytes a row at I = 768, are not 16-byte aligned and are
-// staged by plain loads).
+// kPS gate rows then kPS up rows of kept codes; the down rows of every route
+// reuse the ring after the gate/up stages (codes of the CTA's rows, then
+// their patterns).  The gate/up rows' patterns and scales (side records,
+// d/16 + d/32 bytes a row) and the down rows' scales (I/32 bytes a row, 24
+// at I = 768, not 16-byte aligned) are staged by plain loads.
 struct Plan {
     int d, I, k, G;
     __host__ __device__ int rows_max() const { return (d + G - 1) / G; }
-    __host__ __device__ int cb() const { return d / 4; }                         // code bytes of a gate/up row
-    __host__ __device__ int mo() const { return 2 * kPS * cb(); }                // patterns in a slot
-    __host__ __device__ int so() const { return mo() + 2 * kPS * (d / 16); }     // scales in a slot
-    __host__ __device__ int s1() const { return so() + 2 * kPS * (d / 32); }
+    __host__ __device__ int s1() const { return 2 * kPS * (d / 4); }
     __host__ __device__ int pmax() const { return (k * I + G - 1) / G; }
+    __host__ __device__ int side() const { return d / 16 + d / 32; }            // side record of a gate/up row
     __host__ __device__ int s2() const { return rows_max() * (I / 4 + I / 16); }  // one route's down rows
     __host__ __device__ int rps() const { return s1() / s2(); }
     __host__ __device__ int w2_stages() const { return (k + rps() - 1) / rps(); }
     __host__ __device__ static int up16(int v) { return (v + 15) & ~15; }
-    // everything but the ring: h, down scales, partials, barriers, the route table
+    // everything but the ring: h, gate/up side records, down scales, partials, barriers, the route table
     __host__ __device__ int fixed() const
     {
-        return up16(k * I * 4) + up16(k * rows_max() * (I / 32)) + kGroups * 2 * kGW * 2 * kPS * 4 +
-               up16(k * rows_max() * 4) + 2 * kMaxSlots * 8 + 5 * kMaxK * 4 + 32;
+        return up16(k * I * 4) + pmax() * 2 * side() + up16(k * rows_max() * (I / 32)) +
+               kGroups * 2 * kGW * 2 * kPS * 4 + up16(k * rows_max() * 4) + 2 * kMaxSlots * 8 + 5 * kMaxK * 4 + 32;
     }
     __host__ __device__ int slots() const
     {
@@ -107,7 +107,8 @@ struct Plan {
         return n > kMaxSlots ? kMaxSlots : n;
     }
     __host__ __device__ int o_h() const { return slots() * s1(); }              // h [k][I] f32
-    __host__ __device__ int o_s2s() const { return o_h() + up16(k * I * 4); }   // down scales [k][RM][I/32]
+    __host__ __device__ int o_gs() const { return o_h() + up16(k * I * 4); }    // side records [P][2][side]
+    __host__ __device__ int o_s2s() const { return o_gs() + pmax() * 2 * side(); }   // down scales [k][RM][I/32]
     __host__ __device__ int o_gpart() const { return o_s2s() + up16(k * rows_max() * (I / 32)); }
     __host__ __device__ int o_dpart() const { return o_gpart() + kGroups * 2 * kGW * 2 * kPS * 4; }
     __host__ __device__ int o_bars() const { return o_dpart() + up16(k * rows_max() * 4); }
@@ -144,9 +145,16 @@ __device__ __forceinline__ float ue4m3(uint32_t s)
 __device__ __forceinline__ float group_dot(uint32_t codes16, uint32_t nib, uint32_t a0, uint32_t a1, uint32_t a2,
                                            uint32_t a3, float acc)
 {
-    const uint32_t p0 = nib & 3u, p1 = nib >> 2;
-    const uint32_t xa = p0 == 0 ? a0 : (p0 == 1 ? a1 : a2);
-    const uint32_t xb = p1 == 3 ? a3 : (p1 == 2 ? a2 : a1);
+    // the pairs at p0 (0..2) and p1 (1..3), chosen without branches (lanes differ in patterns)
+    uint32_t xa, xb;
+    asm("{\n .reg .pred q0, q1, q2, q3;\n"
+        " and.b32 %0, %2, 3;\n shr.b32 %1, %2, 2;\n"
+        " setp.eq.u32 q0, %0, 0;\n setp.eq.u32 q1, %0, 1;\n"
+        " setp.eq.u32 q2, %1, 3;\n setp.eq.u32 q3, %1, 2;\n"
+        " selp.b32 %0, %4, %5, q1;\n selp.b32 %0, %3, %0, q0;\n"
+        " selp.b32 %1, %5, %4, q3;\n selp.b32 %1, %6, %1, q2;\n}"
+        : "=&r"(xa), "=&r"(xb)
+        : "r"(nib), "r"(a0), "r"(a1), "r"(a2), "r"(a3));
     acc = fma2(e2m1x2(codes16 & 0xFFu), xa, acc);
     return fma2(e2m1x2(codes16 >> 8), xb, acc);
 }
@@ -174,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     const int RM = pl.rows_max(), S1 = pl.s1(), S2 = pl.s2(), NS = pl.slots(), RPS = pl.rps();
     uint8_t *ring = smem;
     float *hbuf = reinterpret_cast<float *>(smem + pl.o_h());           // [nv][I] h of every route
+    uint8_t *gs = smem + pl.o_gs();                                      // [P][2][side] gate/up patterns | scales
     uint8_t *s2s = smem + pl.o_s2s();                                    // [k][RM][I/32] down scales
     float *gpart = reinterpret_cast<float *>(smem + pl.o_gpart());       // [grp][2][kGW][2 kPS]
     float *dpart = reinterpret_cast<float *>(smem + pl.o_dpart());       // [k][RM]
@@ -213,8 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             if (ok) {
                 r_e[vi] = e;
                 r_w[vi] = w;
-                r_a13[vi] = __ldg(a.a13 + e);
-                r_a2[vi] = __ldg(a.a2 + e);
             }
             if (lane == 0) {
                 *s_nv = __popc(vm);
@@ -254,8 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             if (rank < k) {
                 r_e[rank] = e;
                 r_l[rank] = l;
-                r_a13[rank] = __ldg(a.a13 + e);
-                r_a2[rank] = __ldg(a.a2 + e);
             }
         }
     }
@@ -274,9 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     if (warp == 0) {
         // ------------------------------------------------ producer
         if (lane == 0) {
-            const int cbw = d / 4, mbw = d / 16, sbw = d / 32;   // bytes of a gate/up row: codes, patterns, scales
+            const int cbw = d / 4;                               // code bytes of a gate/up row
             const int cb2 = I / 4, mb2 = I / 16;                 // of a down row: codes, patterns
-            const int MO = pl.mo(), SO = pl.so();
             tc::fence_proxy_async_smem();                  // the ring held the routing's keys
             int t = 0;
             for (; t < S + SW; ++t) {
@@ -289,16 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 if (t < S) {
                     // gate/up stage t: runs of neurons of one route, gate rows then up rows
                     const int q0 = q_lo + t * kPS, q1 = q_lo + min(t * kPS + kPS, P);
-                    tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(q1 - q0) * 2 * (cbw + mbw + sbw));
+                    tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(q1 - q0) * 2 * cbw);
                     for (int q = q0; q < q1;) {
                         const int r = q / I, n = q - r * I, len = min(q1 - q, I - n), i = q - q0;
                         const int64_t g0 = static_cast<int64_t>(r_e[r]) * 2 * I + n, g1 = g0 + I;
                         tc::bulk_load(tc::smem_u32(st + i * cbw), a.v13 + g0 * cbw, len * cbw, bar);
                         tc::bulk_load(tc::smem_u32(st + (kPS + i) * cbw), a.v13 + g1 * cbw, len * cbw, bar);
-                        tc::bulk_load(tc::smem_u32(st + MO + i * mbw), a.m13 + g0 * mbw, len * mbw, bar);
-                        tc::bulk_load(tc::smem_u32(st + MO + (kPS + i) * mbw), a.m13 + g1 * mbw, len * mbw, bar);
-                        tc::bulk_load(tc::smem_u32(st + SO + i * sbw), a.s13 + g0 * sbw, len * sbw, bar);
-                        tc::bulk_load(tc::smem_u32(st + SO + (kPS + i) * sbw), a.s13 + g1 * sbw, len * sbw, bar);
                         q += len;
                     }
                 } else {
@@ -351,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 xw[i] = *reinterpret_cast<const uint32_t *>(&h2);
             }
         }
-        const int MO = pl.mo(), SO = pl.so();
+        const int SD = pl.side();
+        tc::named_bar(kBarSide, kCW * 32);                 // the side records and constants are staged
         for (int s = grp, m = 0; s < S; s += kGroups, ++m) {
             const int sl = s % NS, buf = m & 1;
             const uint32_t ph = (s / NS) & 1u;
@@ -370,21 +371,23 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                         const int i = 8 * h8 + ii;
                         v8[ii] = 0.f;
                         if (i % kPS < npairs) {
+                            // this row's side record: pair s * kPS + i % kPS, gate (i < kPS) or up
+                            const uint8_t *sr = gs + ((s * kPS + i % kPS) * 2 + i / kPS) * SD;
                             float acc = 0.f;
                             if constexpr (KPL == 16) {
                                 const uint32_t cw4 =
                                     *reinterpret_cast<const uint32_t *>(st + i * (d / 4) + kbase / 4);
-                                const uint32_t mb = st[MO + i * (d / 16) + kbase / 16];
+                                const uint32_t mb = sr[kbase / 16];
                                 acc = group_dot(cw4 & 0xFFFFu, mb & 0xFu, xw[0], xw[1], xw[2], xw[3], acc);
                                 acc = group_dot(cw4 >> 16, mb >> 4, xw[4], xw[5], xw[6], xw[7], acc);
                             } else {
                                 const uint32_t cw2 =
                                     *reinterpret_cast<const uint16_t *>(st + i * (d / 4) + kbase / 4);
-                                const uint32_t mb = st[MO + i * (d / 16) + kbase / 16];
+                                const uint32_t mb = sr[kbase / 16];
                                 acc = group_dot(cw2, (mb >> (4 * ((kbase >> 3) & 1))) & 0xFu, xw[0], xw[1], xw[2],
                                                 xw[3], acc);
                             }
-                            v8[ii] = acc * ue4m3(st[SO + i * (d / 32) + kbase / 32]);
+                            v8[ii] = acc * ue4m3(sr[d / 16 + kbase / 32]);
                         }
                     }
                     const float tot = reduce8(v8, lane) * xinv;
@@ -421,6 +424,25 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     } else {
         // ------------------------------------------------ staging warps
         const int tw = warp - kWarpT0, tt = tid - kWarpT0 * 32;
+        // the side records of this CTA's gate and up rows (patterns d/16
+        // bytes, then scales d/32 bytes), 16-byte loads, and the routes'
+        // experts' constants
+        {
+            const int SD = pl.side(), nm = d / 256, n16 = SD / 16;   // 16-byte pieces: patterns, all
+            for (int i = tt; i < P * 2 * n16; i += kTW * 32) {
+                const int pr = i / (2 * n16), rem = i - pr * 2 * n16, up = rem / n16, j = rem - up * n16;
+                const int q = q_lo + pr, r = q / I, n = q - r * I;
+                const int64_t row = static_cast<int64_t>(r_e[r]) * 2 * I + n + (up ? I : 0);
+                const uint4 v = j < nm ? __ldg(reinterpret_cast<const uint4 *>(a.m13 + row * (d / 16)) + j)
+                                       : __ldg(reinterpret_cast<const uint4 *>(a.s13 + row * (d / 32)) + (j - nm));
+                *reinterpret_cast<uint4 *>(gs + (pr * 2 + up) * SD + 16 * j) = v;
+            }
+            if (tt < nv) {
+                r_a13[tt] = __ldg(a.a13 + r_e[tt]);
+                r_a2[tt] = __ldg(a.a2 + r_e[tt]);
+            }
+        }
+        tc::named_arrive(kBarSide, kCW * 32);
         if constexpr (ROUTE) {
             if (tw == 0) {
                 // the renormalised weights of the chosen routes (needed only at the end)

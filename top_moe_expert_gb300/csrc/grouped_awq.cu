@@ -209,11 +209,17 @@ __device__ __forceinline__ void dq_nv4_group(uint32_t codes16, uint32_t nib, uin
     const __half2 ha = __hmul2(*reinterpret_cast<const __half2 *>(&a), S);
     const __half2 hb = __hmul2(*reinterpret_cast<const __half2 *>(&b), S);
     const uint32_t P0 = *reinterpret_cast<const uint32_t *>(&ha), P1 = *reinterpret_cast<const uint32_t *>(&hb);
-    const uint32_t p0 = nib & 3u, p1 = nib >> 2;
-    out[0] = p0 == 0 ? P0 : 0u;
-    out[1] = p0 == 1 ? P0 : (p1 == 1 ? P1 : 0u);
-    out[2] = p0 == 2 ? P0 : (p1 == 2 ? P1 : 0u);
-    out[3] = p1 == 3 ? P1 : 0u;
+    // place P0 at pair p0 (0..2) and P1 at pair p1 (1..3), without branches
+    asm("{\n .reg .pred a0, a1, a2, b1, b2, b3;\n .reg .b32 p0, p1;\n"
+        " and.b32 p0, %4, 3;\n shr.b32 p1, %4, 2;\n"
+        " setp.eq.u32 a0, p0, 0;\n setp.eq.u32 a1, p0, 1;\n setp.eq.u32 a2, p0, 2;\n"
+        " setp.eq.u32 b1, p1, 1;\n setp.eq.u32 b2, p1, 2;\n setp.eq.u32 b3, p1, 3;\n"
+        " selp.b32 %0, %5, 0, a0;\n"
+        " selp.b32 %1, %6, 0, b1;\n selp.b32 %1, %5, %1, a1;\n"
+        " selp.b32 %2, %6, 0, b2;\n selp.b32 %2, %5, %2, a2;\n"
+        " selp.b32 %3, %6, 0, b3;\n}"
+        : "=&r"(out[0]), "=&r"(out[1]), "=&r"(out[2]), "=&r"(out[3])
+        : "r"(nib), "r"(P0), "r"(P1));
 }
 
 // 64 weights of one row: kept codes (16 bytes, group g in bytes 2g, 2g + 1),
