@@ -207,8 +207,9 @@ moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_
  * y[t] = sum_j topk_w[t][j] * W2_{e_j} (SiLU(g) * u),  [g; u] = W13_{e_j} x[t].
  * Kernels by case: MOE_W_MXFP8 (standard layout) with M == 1,
  * (d, I) in {(512, 256), (1024, 512), (2048, 512), (2048, 768),
- * (2048, 1024)}, k small enough for the shared-memory plan (k <= 10 at
- * d = 2048, I = 768 on 152 SMs) -> one kernel, one CTA per SM (each CTA an
+ * (2048, 1024)}, k small enough for the shared-memory plan and for every
+ * CTA's gate/up stages to fit one lap of its ring (k <= 8 at d = 2048,
+ * I = 768 on 152 SMs) -> one kernel, one CTA per SM (each CTA an
  * even share of the (route, neuron) pairs: gate/up rows streamed by
  * cp.async.bulk, h = SiLU(g)*u published in ws with the call's tag; each
  * CTA reads all of h back once every value carries the tag, then forms its
@@ -219,8 +220,8 @@ moe_status_t moe_mxfp8_quantize(const void *v, int32_t vdt, int64_t rows, int32_
  * MXFP8 with M*k <= 512 -> a gate/up kernel and a
  * down kernel chained by programmatic dependent launch;
  * MOE_W_AWQ4 or MOE_W_NVFP4S with M == 1 and (d, I) in {(1024, 256),
- * (1024, 512), (2048, 512), (2048, 768)} (k <= 10 at d = 2048, I = 768 for
- * AWQ, k <= 13 for NVFP4S) -> the same one-kernel structure on the 4-bit
+ * (1024, 512), (2048, 512), (2048, 768)} (k <= 13 at d = 2048, I = 768)
+ * -> the same one-kernel structure on the 4-bit
  * weights (AWQ: (q - z) exact in fp16, the group scale per lane; NVFP4S:
  * kept pairs times the activation pairs at their pattern positions, the
  * block scale per lane, alpha per row), code, pattern and scale arrays
@@ -395,8 +396,8 @@ moe_status_t moe_ffn_grouped_batched(const void *x, int32_t xdt, int32_t M, int3
  *   MOE_W_MXFP8: MOE_PATH_DECODE for M <= 1 where the single-kernel decode
  *                is built for (k, d, I) on GB300's 152 SMs (d = 512,
  *                I = 256; d = 1024, I = 512; d = 2048, I = 512, 768 or
- *                1024; k small enough for its shared-memory plan, k <= 10
- *                at d = 2048, I = 768), else MOE_PATH_GROUPED (decode 15.4
+ *                1024; k small enough for its plan, k <= 8 at d = 2048,
+ *                I = 768), else MOE_PATH_GROUPED (decode 15.4
  *                against grouped 27.8 us at M = 1; grouped 41.5 against
  *                179 us at M = 4 and faster at every larger M; at d = 7168,
  *                I = 2048, M = 1, grouped 80.9 against 250 us);

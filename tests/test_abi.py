@@ -164,8 +164,9 @@ def test_select_path_at_the_measured_crossover(L):
     # built (the large-expert shape and k beyond its shared-memory plan go
     # to the grouped path, which is faster there than the two-kernel decode)
     assert sel(1, d=7168, I=2048, E=384) == (G, 16)
-    assert sel(1, k=10) == (D, 0) and sel(1, k=11) == (G, 16)
-    assert sel(1, d=2048, I=1024, k=9) == (D, 0) and sel(1, d=2048, I=1024, k=10) == (G, 16)
+    # (every CTA's gate/up stages within one lap of the ring: k <= 8 here)
+    assert sel(1, k=8) == (D, 0) and sel(1, k=9) == (G, 16)
+    assert sel(1, d=2048, I=1024, k=6) == (D, 0) and sel(1, d=2048, I=1024, k=7) == (G, 16)
     assert sel(64, d=1536, I=96) == (D, 0)                   # grouped needs I % 128 == 0
     assert sel(21, awq, d=9216, I=256) == (D, 0)             # AWQ grouped: d / 128 <= 64
     assert sel(21, awq, d=3072, I=256) == (G, 8)

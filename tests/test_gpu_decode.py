@@ -185,6 +185,24 @@ def test_mx_single_token_activation_scales_routes_and_counter():
     assert ws[:8].view(torch.int64).item() == 3 * sms
 
 
+def test_mx_single_token_most_routes():
+    """One token with k = 13, the most routes the one-kernel plan takes at
+    d = 1024, I = 512 on 152 SMs: every CTA's gate/up stages fill the ring's
+    first lap, and the down stages reuse its slots."""
+    wl = inputs.Workload("one_token_d1024_i512_e128_k13", M=1, d=1024, I=512, E=128, k=13, seed=12)
+    layer = mx_layer(dataclasses.replace(wl, name="most_routes_layer"))
+    x = inputs.activations(wl)
+    ids, w = gs.routing(wl)
+    ws = torch.zeros(moe.moe_ffn_decode_workspace_size(1, 13, wl.d, wl.I), dtype=torch.uint8, device="cuda")
+    ys = [run_decode(layer, x, ids, w, torch.float32, ws=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert ws[:8].view(torch.int64).item() == 3 * sms            # the one-kernel path ran
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+    gs.assert_layer_close(ys[0], oracle_decode(layer, x, ids, w))
+
+
 def test_single_token_wait_runs_out_and_reports_timeout():
     """Failure detection without a GPU fault: the one-kernel path's wait for
     h is bounded.  Made to wait for a tag that no CTA writes, it gives up

@@ -126,7 +126,11 @@ struct Plan {
     __host__ __device__ int bytes() const { return o_route() + 3 * kMaxK * 4 + 32; }
     __host__ __device__ bool fits() const
     {
-        return s2() > 0 && s2() <= s1() && slots() >= kMinSlots && w2_stages() <= slots() && bytes() <= kSmemMax &&
+        // every CTA's gate/up stages within the ring's first lap: a group then
+        // never waits (by barrier parity) on a slot that another group's
+        // stage, possibly not landed yet, held one lap earlier
+        return s2() > 0 && s2() <= s1() && slots() >= kMinSlots && w2_stages() <= slots() &&
+               (pmax() + kPS - 1) / kPS <= slots() && bytes() <= kSmemMax &&
                static_cast<size_t>(k) * I * 8 <= kWsTagBytes && k * I <= kCW * 32 * kMaxPerLane;
     }
 };
