@@ -31,7 +31,7 @@ class Workload:
     E: int
     k: int
     b: int = 8
-    fmt: str = "mxfp8"          # "mxfp8" or "awq4"
+    fmt: str = "mxfp8"          # "mxfp8", "awq4" or "nvfp4s"
     routing: str = "uniform"    # "uniform", "zipf", "fixture_a"
     seed: int = 0
 
