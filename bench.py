@@ -1043,7 +1043,7 @@ TABLE8 = {
 }
 
 
-def run_table8(model: str, device, reps: int = 20, out=sys.stdout):
+def run_table8(model: str, device, reps: int = 20, out=sys.stdout, fmt: str = "mxfp8"):
     """The grouped layer over the benchmark's (N, G) grid with per-expert token
     counts {N, 3N/4, N/2, N/4} repeated over the G experts (one route per
     token, weight 1), on the aligned and on the fixed-capacity layout.  One
@@ -1052,17 +1052,30 @@ def run_table8(model: str, device, reps: int = 20, out=sys.stdout):
     weights that together exceed the L2.  One JSON line per (G, N, layout):
     the page's effective TFLOP/s (2 * (2I*d + d*I) * sum N_g / t) and the
     fraction of the measured HBM bandwidth the weight and activation bytes
-    reach."""
+    reach.  fmt "nvfp4s": the paired 4:8 sparse NVFP4 W4A4 grouped path (the
+    page's own format) on random admissible packing, aligned layout only."""
     import top_moe_expert_gb300 as moe
     from top_moe_expert_gb300 import inputs
     d, I, Ns, Gs = TABLE8[model]
     peak_gbs, _ = measured_peak()
+    nv4 = fmt == "nvfp4s"
     for G in Gs:
         wl = inputs.Workload(f"table8_{model}_g{G}", M=1, d=d, I=I, E=G, k=1, seed=30)
-        lw = G * 3 * I * d * 33 // 32
+        # weight bytes: NVFP4S kept codes and side records (3/8 byte a weight) and two factors per expert
+        lw = G * 3 * I * d * 3 // 8 + 8 * G if nv4 else G * 3 * I * d * 33 // 32
         n_copies = max(1, min(8, -(-4 * 130 * 2 ** 20 // lw)))
         layers = []
+        # NVFP4S activation scales, constants of the layer: N(0,1) inputs up to 6.5,
+        # |h| up to 16 (the weights' RMS gives |g|, |u| of order 1)
+        a_x, a_h = 6.5 / (6 * 448), 16.0 / (6 * 448)
         for c in range(n_copies):
+            if nv4:
+                v13, m13, c13, al13 = inputs.nvfp4s_weights_device(wl, "w13", device)
+                v2, m2, c2, al2 = inputs.nvfp4s_weights_device(wl, "w2", device)
+                w13 = moe.Weights(moe.MOE_W_NVFP4S, v13, c13, m13, al13)
+                w2 = moe.Weights(moe.MOE_W_NVFP4S, v2, c2, m2, al2)
+                layers.append((w13, w2, moe.moe_grouped_prepare_nvfp4s(w13, w2, a_x, a_h)))
+                continue
             q13 = torch.empty((G, 2 * I, d), dtype=torch.uint8, device=device)
             s13 = torch.empty((G, 2 * I, d // 32), dtype=torch.uint8, device=device)
             q2 = torch.empty((G, d, I), dtype=torch.uint8, device=device)
@@ -1083,10 +1096,10 @@ def run_table8(model: str, device, reps: int = 20, out=sys.stdout):
             w = torch.ones((M, 1), dtype=torch.float32, device=device)
             x = inputs.activations(inputs.Workload("t8x", M=M, d=d, I=I, E=G, k=1, seed=31)).to(device)
             y = torch.empty((M, d), dtype=torch.bfloat16, device=device)
-            b = moe.moe_ffn_select_path(M, 1, G, d, I)[1] or 16
+            b = moe.moe_ffn_select_path(M, 1, G, d, I, moe.MOE_W_NVFP4S if nv4 else moe.MOE_W_MXFP8)[1] or 16
             C = -(-N // b) * b
             cr, cb = moe.moe_align_capacity(M, 1, G, b)
-            for layout in ("aligned", "fixed"):
+            for layout in (("aligned",) if nv4 else ("aligned", "fixed")):
                 if layout == "aligned":
                     al = (torch.empty(cr, dtype=torch.int32, device=device),
                           torch.empty(cb, dtype=torch.int32, device=device),
@@ -1128,7 +1141,7 @@ def run_table8(model: str, device, reps: int = 20, out=sys.stdout):
                 us = e0.elapsed_time(e1) * 1e3 / (3 * n_steps)
                 flop = 2.0 * (2 * I * d + d * I) * M
                 nbytes = lw + M * d * 2 + M * d * 2
-                print(json.dumps({"table8": model, "G": G, "N": N, "tokens": M, "layout": layout, "b": b,
+                print(json.dumps({"table8": model, "fmt": fmt, "G": G, "N": N, "tokens": M, "layout": layout, "b": b,
                                   "us_per_step": round(us, 2), "eff_tflops": round(flop / (us * 1e-6) / 1e12, 2),
                                   "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peak_gbs, 4),
                                   "weight_copies": n_copies}), file=out, flush=True)
@@ -1151,6 +1164,8 @@ def main():
     ap.add_argument("--block", type=int, default=0, help="MoE block size b of the grouped path (0: automatic)")
     ap.add_argument("--table8", choices=sorted(TABLE8), default=None,
                     help="run the grouped-GEMM benchmark grid (one JSON line per point) instead of the bench line")
+    ap.add_argument("--table8-fmt", choices=["mxfp8", "nvfp4s"], default="mxfp8",
+                    help="weight format of the --table8 grid (nvfp4s: the W4A4 paired 4:8 sparse path)")
     ap.add_argument("--layers", type=int, default=0,
                     help="copies of the layer's weights the steps rotate through (0: enough that the inputs of "
                          "the timed steps exceed the L2; 1 keeps a profiling run small)")
@@ -1180,7 +1195,7 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     if args.table8:
-        run_table8(args.table8, device)
+        run_table8(args.table8, device, fmt=args.table8_fmt)
         return
     line = run_ours(args, rank, world, device)
     if line is not None:

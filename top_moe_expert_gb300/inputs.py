@@ -191,6 +191,26 @@ def nvfp4s_weights(wl: Workload, which: str, experts=None):
     return v, m, sc, np.full(n, 0.01, dtype=np.float32)
 
 
+def nvfp4s_weights_device(wl: Workload, which: str, device):
+    """nvfp4s_weights' distribution drawn on the device (for large grids), one
+    seeded generator per matrix, expert by expert: kept codes, patterns,
+    scale codes, alpha, as torch tensors."""
+    N, K = (2 * wl.I, wl.d) if which == "w13" else (wl.d, wl.I)
+    g = torch.Generator(device=device)
+    g.manual_seed(BASE_SEED + 1000 * wl.seed + (400000 if which == "w13" else 400001))
+    E = wl.E
+    v = torch.empty((E, N, K // 4), dtype=torch.uint8, device=device)
+    m = torch.empty((E, N, K // 16), dtype=torch.uint8, device=device)
+    sc = torch.empty((E, N, K // 32), dtype=torch.uint8, device=device)
+    pats = torch.from_numpy(NV4_PATTERNS).to(device)
+    for e in range(E):
+        v[e] = torch.randint(0, 256, (N, K // 4), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+        pat = pats[torch.randint(0, 6, (N, K // 8), generator=g, device=device)]
+        m[e] = pat[:, 0::2] | (pat[:, 1::2] << 4)
+        sc[e] = torch.randint(0x30, 0x41, (N, K // 32), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+    return v, m, sc, torch.full((E,), 0.01, dtype=torch.float32, device=device)
+
+
 def bits16(t: torch.Tensor) -> np.ndarray:
     """Raw 16-bit patterns of a bf16/fp16 tensor, as numpy uint16."""
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
