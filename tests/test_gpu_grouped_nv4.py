@@ -140,3 +140,50 @@ def test_nv4_grouped_bf16_output():
     y32, _, _ = _run(SMALL, w13, w2, p13d, p2d, x, ids, w, 8)
     y16, _, _ = _run(SMALL, w13, w2, p13d, p2d, x, ids, w, 8, out_dtype=torch.bfloat16)
     assert torch.equal(y16, y32.to(torch.bfloat16))
+
+
+def test_nv4_grouped_full_size_sampled():
+    """The benchmark's shape (d = 2048, I = 768, E = 128, k = 8, M = 64) in the
+    launch configuration the bench times (its random admissible packing,
+    b from the path choice): Q_a(x) of every aligned row bit for bit, and
+    for sampled tokens Q_a(h) per route and the output stage-wise."""
+    wl = inputs.Workload("nv4_full_m64", M=64, d=2048, I=768, E=128, k=8, fmt="nvfp4s", seed=2)
+    v13, m13, c13, a13 = inputs.nvfp4s_weights(wl, "w13")
+    v2, m2, c2, a2 = inputs.nvfp4s_weights(wl, "w2")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    w13 = moe.Weights(moe.MOE_W_NVFP4S, dev(v13), dev(c13), dev(m13), dev(a13))
+    w2 = moe.Weights(moe.MOE_W_NVFP4S, dev(v2), dev(c2), dev(m2), dev(a2))
+    x = inputs.activations(wl)
+    ids, w = gs.routing(wl)
+    a_x = float(np.float32(np.abs(gs.x_exact(x)).max() / (6 * 448)))
+    a_h = 16.0 / (6 * 448)
+    p13d, p2d = moe.moe_grouped_prepare_nvfp4s(w13, w2, a_x, a_h)
+    b = moe.moe_ffn_select_path(wl.M, wl.k, wl.E, wl.d, wl.I, moe.MOE_W_NVFP4S)[1]
+    y, aligned, ws = _run(wl, w13, w2, p13d, p2d, x, ids, w, b)
+    M, k = ids.shape
+    sorted_ids = aligned[0].cpu().numpy()
+    npp = int(aligned[2].item())
+    xg, hg = _xg_hg(ws, sorted_ids.size, wl.d, wl.I)
+    rows = sorted_ids[:npp]
+    valid = rows < M * k
+    c, s = oracle.nvfp4_act_quantize(gs.x_exact(x).astype(np.float32), a_x)
+    np.testing.assert_array_equal(xg[:npp][valid], oracle.nvfp4_act_values(c, s)[rows[valid] // k])
+    # sampled tokens: the oracle on their routes' experts only
+    toks = np.array([0, 17, 63])
+    experts = sorted(set(ids[toks].reshape(-1).tolist()))
+    slot = np.full(wl.E, -1, dtype=np.int32)
+    slot[experts] = np.arange(len(experts), dtype=np.int32)
+    pk = lambda v, m_, c_, al: {"fmt": "nvfp4s", "v": v[experts], "m": m_[experts], "s": c_[experts],
+                                "alpha": al[experts], "slot": slot}
+    o13, o2 = pk(v13, m13, c13, a13), pk(v2, m2, c2, a2)
+    xs, ids_s, w_s = gs.x_exact(x)[toks], ids[toks], w[toks].astype(np.float64)
+    ref = oracle.moe_layer_a4(xs, ids_s, w_s, wl.E, o13, o2, a_x, a_h, want_hv=True)
+    hv_gpu = np.zeros((len(toks) * k, wl.I))
+    pos = {int(r): i for i, r in enumerate(rows) if r < M * k}
+    for ti, t in enumerate(toks):
+        for j in range(k):
+            hv_gpu[ti * k + j] = hg[pos[int(t) * k + j]]
+    diff = hv_gpu != ref["hv"]
+    assert int(diff.sum()) <= 2, f"{int(diff.sum())} Q_a(h) values differ"
+    y_ref = oracle.moe_layer_a4(xs, ids_s, w_s, wl.E, o13, o2, a_x, a_h, hv_in=hv_gpu)["y"]
+    gs.assert_layer_close(y[torch.from_numpy(toks)], y_ref)
