@@ -2,7 +2,8 @@
 // kernels on 4-bit weights (decode_pipe_awq.cu, decode_pipe_nv4.cu): fp16 dot
 // products with FP32 accumulation, the 8-way lane reduction, the exact
 // power-of-two rescale into fp16, and the relaxed loads and stores of the
-// tagged h exchange.
+// tagged h exchange; and the CTA split of every single-token kernel
+// (decode_pipe.cu too).
 #pragma once
 
 #include <cstdint>
@@ -92,6 +93,30 @@ __device__ __forceinline__ void ld_relaxed_u64x2(const unsigned long long *p, un
                                                  unsigned long long &b)
 {
     asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+// This CTA's share of a single-token layer call: the (route, neuron) pairs
+// q = r * I + n in [q_lo, q_lo + P), S gate/up stages of PS neurons, and the
+// output rows [o0, o0 + nrows), SW down stages of RPS routes; both spaces
+// split evenly over the G CTAs (one per SM).  32-bit arithmetic: the plans
+// accept nv * I <= 24576 and d <= 2048, so nv * I * G and d * G stay below
+// 2^31 for any G below 87000.
+struct Split {
+    int q_lo, P, S, o0, nrows, SW;
+};
+
+template <int PS>
+__device__ __forceinline__ Split cta_split(int nv, int I, int d, int c, int G, int RPS)
+{
+    const unsigned g = static_cast<unsigned>(G);
+    Split s;
+    s.q_lo = static_cast<int>(static_cast<unsigned>(nv * I * c) / g);
+    s.P = static_cast<int>(static_cast<unsigned>(nv * I * (c + 1)) / g) - s.q_lo;
+    s.S = (s.P + PS - 1) / PS;
+    s.o0 = static_cast<int>(static_cast<unsigned>(d * c) / g);
+    s.nrows = static_cast<int>(static_cast<unsigned>(d * (c + 1)) / g) - s.o0;
+    s.SW = s.nrows > 0 ? (nv + RPS - 1) / RPS : 0;
+    return s;
 }
 
 }  // namespace pipe
