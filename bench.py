@@ -205,7 +205,7 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 
 SRC_FILES = {
-    "decode": ("decode.cu", "decode_pipe.cu", "decode_stream.cu", "decode_internal.h", "topk.cu", "topk.cuh",
+    "decode": ("decode.cu", "decode_pipe.cu", "pipe_common.cuh", "decode_stream.cu", "decode_internal.h", "topk.cu", "topk.cuh",
                "common.cuh", "tc.cuh", "attr.h"),
     "grouped": ("grouped.cu", "grouped_internal.h", "align.cu", "topk.cu", "topk.cuh", "common.cuh", "tc.cuh",
                 "attr.h"),

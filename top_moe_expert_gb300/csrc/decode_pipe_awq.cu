@@ -53,11 +53,12 @@ constexpr int kThreads = kWarps * 32;                 // 832
 constexpr int kCW = kWarps - kWarpGU0;                // compute warps of the exchange and tail: 24
 constexpr int kMaxPerLane = 32;                       // exchange words per lane, at most
 constexpr uint64_t kWaitNs = 2000000000ull;           // 2 s
-constexpr int kBarRoutes = 1;                         // named barriers: routes published (all warps)
+constexpr int kBarRoutes = 1;                         // named barriers: routes published (all warps but 1)
 constexpr int kBarTail = 2;                           //   the compute warps
 constexpr int kBarGroup0 = 3;                         //   gate/up group g: kBarGroup0 + g
 constexpr int kBarRank = kBarGroup0 + kGroups;        //   the compute warps ranking the logits
-constexpr int kBarScales = kBarRank + 1;              //   gate/up scales and zeros staged (staging warps arrive)
+constexpr int kBarScales = kBarRank + 1;              //   gate/up scales and zeros staged, launch tag formed
+                                                      //   (staging warps and warp 1 arrive)
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kMaxG2 = 8;                             // groups of a down row (I / 128), at most
 
@@ -190,7 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---------------------------------------------------------------- set-up
+    // This CTA's split is formed before the routes barrier wherever the
+    // number of valid routes is known there (routing here: all k are valid;
+    // given routes: warp 0 counts them), so the producer can stream as soon
+    // as the routes are out.
+    pipe::Split sp{};
     if (warp == 0) {
+        if constexpr (ROUTE)
+            sp = pipe::cta_split<kPS>(k, I, d, c, G, RPS);
         if (lane == 0) {
             for (int i = 0; i < NS; ++i) {
                 tc::mbar_init(full + 8 * i, 1);
@@ -213,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 r_e[vi] = e;
                 r_w[vi] = w;
             }
+            sp = pipe::cta_split<kPS>(__popc(vm), I, d, c, G, RPS);
             if (lane == 0) {
                 *s_nv = __popc(vm);
                 if (c == 0 && k > __popc(vm) && a.dev_status)
@@ -220,12 +229,17 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             }
         }
     } else if (warp == 1) {
+        // this launch's tag, from the count read before this CTA adds its
+        // one; the gate/up warps read it after the staging barrier (it is not
+        // needed before, so this warp stays off the routes barrier)
         if (lane == 0) {
-            // this launch's tag, from the count read before this CTA adds its one
             const unsigned long long v = ld_relaxed_u64(a.ctr);
             *s_tag = static_cast<uint32_t>(v / static_cast<unsigned>(G)) + 1u;
             red_relaxed_add(a.ctr);
         }
+        __syncwarp();
+        tc::named_arrive(kBarScales, kCW * 32 + 32);
+        return;
     } else if constexpr (ROUTE) {
         // top-k of the router logits by rank: thread e (of the 24 compute
         // warps) holds expert e's order-preserving key; its slot is the
@@ -237,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
         float l = 0.f;
         if (e < a.E)
             l = __ldcg(a.logits + e);
+        sp = pipe::cta_split<kPS>(k, I, d, c, G, RPS);
         if (e < Ep)
             keys[e] = e < a.E ? topk_key(l) : 0u;
         tc::named_bar(kBarRank, kCW * 32);
@@ -255,17 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             }
         }
     }
-    tc::named_bar(kBarRoutes, kThreads);
+    tc::named_bar(kBarRoutes, kThreads - 32);
 
     const int nv = *s_nv;
+    if constexpr (!ROUTE) {
+        if (warp != 0)
+            sp = pipe::cta_split<kPS>(nv, I, d, c, G, RPS);
+    }
     // this CTA's (route, neuron) pairs: a contiguous range of q = r * I + n,
     // the whole space split evenly over the CTAs (h[q] is formed here)
-    const int q_lo = static_cast<int>(static_cast<int64_t>(nv) * I * c / G);
-    const int P = static_cast<int>(static_cast<int64_t>(nv) * I * (c + 1) / G) - q_lo;
-    const int S = (P + kPS - 1) / kPS;                                              // gate/up stages
-    const int o0 = static_cast<int>(static_cast<int64_t>(d) * c / G);
-    const int nrows = static_cast<int>(static_cast<int64_t>(d) * (c + 1) / G) - o0;
-    const int SW = nrows > 0 ? (nv + RPS - 1) / RPS : 0;                           // down stages
+    const int q_lo = sp.q_lo, P = sp.P, S = sp.S;                     // S gate/up stages
+    const int o0 = sp.o0, nrows = sp.nrows, SW = sp.SW;               // SW down stages
 
     if (warp == 0) {
         // ------------------------------------------------ producer
@@ -309,10 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
         }
         return;
     }
-    if (warp == 1)
-        return;
     const int cw = warp - kWarpGU0;                      // compute warp 0..23
-    const uint32_t tag = *s_tag;
     if (warp < kWarpT0) {
         // ------------------------------------------------ gate/up warps
         const int grp = cw / kGW, om = cw % kGW;
@@ -342,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                     xw[4 * w + j] = *reinterpret_cast<const uint32_t *>(&h2);
                 }
         }
-        tc::named_bar(kBarScales, kCW * 32);               // the scales and zeros are staged
+        tc::named_bar(kBarScales, kCW * 32 + 32);         // the scales and zeros are staged, the tag formed
+        const uint32_t tag = *s_tag;
         for (int s = grp, m = 0; s < S; s += kGroups, ++m) {
             const int sl = s % NS, buf = m & 1;
             const uint32_t ph = (s / NS) & 1u;
@@ -440,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        tc::named_arrive(kBarScales, kCW * 32);
+        tc::named_arrive(kBarScales, kCW * 32 + 32);
         if constexpr (ROUTE) {
             if (tw == 0) {
                 // the renormalised weights of the chosen routes (needed only at the end)
@@ -489,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     if (work) {
         const int NP = nv * I;                                      // words; NP % 64 == 0 (I % 64 == 0)
         const int nj = (NP / 64 + kCW - 1) / kCW;                   // 16-byte loads per lane
+        const uint32_t tag = *s_tag;                                // formed before the staging barrier
         const uint32_t want = a.stall ? tag ^ 0x80000000u : tag;
         uint32_t pend = 0;
         for (int j = 0; j < nj; ++j)
