@@ -106,7 +106,7 @@ struct Split {
 };
 
 template <int PS>
-__device__ __forceinline__ Split cta_split(int nv, int I, int d, int c, int G, int RPS)
+__host__ __device__ __forceinline__ Split cta_split(int nv, int I, int d, int c, int G, int RPS)
 {
     const unsigned g = static_cast<unsigned>(G);
     Split s;
