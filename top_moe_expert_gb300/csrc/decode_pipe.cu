@@ -137,26 +137,16 @@ struct Plan {
     }
 };
 
-__device__ __forceinline__ void set_err(int32_t *st, int code)
-{
-    if (st)
-        atomicCAS(st + 1, 0, code);
-}
+// set_err, fma2, reduce8, f16_shift, warp_max and the relaxed exchange loads
+// and stores come from pipe_common.cuh, shared with the 4-bit single-token
+// kernels.
+using namespace pipe;
 
 __device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two)
 {
     uint32_t r;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(two)));
     return r;
-}
-
-// acc + w.lo * a.lo + w.hi * a.hi: fp16 products exact in FP32, one rounding each
-__device__ __forceinline__ float fma2(uint32_t w, uint32_t a, float acc)
-{
-    asm("{\n .reg .f16 w0, w1, a0, a1;\n mov.b32 {w0, w1}, %1;\n mov.b32 {a0, a1}, %2;\n"
-        " fma.rn.f32.f16 %0, w0, a0, %0;\n fma.rn.f32.f16 %0, w1, a1, %0;\n}"
-        : "+f"(acc) : "r"(w), "r"(a));
-    return acc;
 }
 
 // four E4M3 codes (one word, byte order) -> two f16x2 words, exactly; the
@@ -193,74 +183,6 @@ __device__ __forceinline__ void lds_codes(const uint8_t *p, uint32_t (&w)[KPL / 
             w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
     }
-}
-
-// Sum over 8 values of 32 lanes at once: lane l ends with the total of value
-// v_index(l) = 4 * bit4(l) + 2 * bit3(l) + bit2(l) in every lane of its quad.
-__device__ __forceinline__ float reduce8(const float (&v)[8], int lane)
-{
-    float u[4], t[2];
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = b4 ? v[i] : v[i + 4];
-        u[i] = (b4 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = b3 ? u[i] : u[i + 2];
-        t[i] = (b3 ? u[i + 2] : u[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    float r = (b2 ? t[1] : t[0]) + __shfl_xor_sync(0xffffffffu, b2 ? t[0] : t[1], 4);
-    r += __shfl_xor_sync(0xffffffffu, r, 2);
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
-    return r;
-}
-
-// exponent p with m * 2^p in [2^14, 2^15) for a finite m > 0 (the largest
-// magnitude of a vector); 0 for m == 0
-__device__ __forceinline__ int f16_shift(float m)
-{
-    if (!(m > 0.f))
-        return 0;
-    int ex;
-    frexpf(m, &ex);            // m = f * 2^ex, f in [0.5, 1)
-    const int p = 15 - ex;
-    return p < -100 ? -100 : (p > 100 ? 100 : p);
-}
-
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void red_relaxed_add(unsigned long long *p)
-{
-    asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p) : "memory");
-}
-
-// one (value, tag) word of the h exchange: 8-byte aligned, so single-copy atomic
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// two consecutive exchange words (16-byte aligned); each word is read
-// single-copy atomically on its own
-__device__ __forceinline__ void ld_relaxed_u64x2(const unsigned long long *p, unsigned long long &a,
-                                                 unsigned long long &b)
-{
-    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
 // KPL: gate/up elements per lane of a warp's K slice (d = 32 * kGW * KPL);

@@ -1,9 +1,8 @@
-// pipe_common.cuh -- device helpers shared by the single-token decode
-// kernels on 4-bit weights (decode_pipe_awq.cu, decode_pipe_nv4.cu): fp16 dot
-// products with FP32 accumulation, the 8-way lane reduction, the exact
-// power-of-two rescale into fp16, and the relaxed loads and stores of the
-// tagged h exchange; and the CTA split of every single-token kernel
-// (decode_pipe.cu too).
+// pipe_common.cuh -- helpers shared by the three single-token decode kernels
+// (decode_pipe.cu, decode_pipe_awq.cu, decode_pipe_nv4.cu): fp16 dot products
+// with FP32 accumulation, the 8-way lane reduction, the exact power-of-two
+// rescale into fp16, the relaxed loads and stores of the tagged h exchange,
+// and each CTA's split of the layer.
 #pragma once
 
 #include <cstdint>
