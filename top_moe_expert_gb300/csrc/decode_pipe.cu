@@ -14,13 +14,10 @@
 //   * warp 0, producer: routes the token (or reads the given routing),
 //     publishes the valid routes in slot order, then streams through one
 //     ring of up to 11 slots (176 KB in flight per SM at d = 2048): first
-//     this CTA's gate rows, 4 neurons per stage, then this CTA's rows of
-//     every routed expert's down projection, one or more routes per stage,
-//     each issued as soon as its slot is free.
-//   * warp 1: reads the launch's tag from the call counter and advances it,
-//     then issues the up rows of every gate/up stage into the slot warp 0
-//     fills with the gate rows (two issuing threads: a thread's bulk copies
-//     leave one after another).
+//     this CTA's gate and up rows, 4 neurons per stage, then this CTA's rows
+//     of every routed expert's down projection, one or more routes per
+//     stage, each issued as soon as its slot is free.
+//   * warp 1: reads the launch's epoch from the call counter and advances it.
 //   * warps 2..17, gate/up: 4 groups of 4 warps.  Group g takes stages g,
 //     g+4, g+8, ...; its warps split K, each holding its slice of x in
 //     registers (fp16 after an exact power-of-two rescale), and form the
@@ -74,7 +71,7 @@ constexpr int kThreads = kWarps * 32;                 // 832
 constexpr int kCW = kWarps - kWarpGU0;                // compute warps of the exchange and tail: 24
 constexpr int kMaxPerLane = 32;                       // exchange words per lane, at most
 constexpr uint64_t kWaitNs = 2000000000ull;           // 2 s
-constexpr int kBarRoutes = 1;                         // named barriers: routes published (all warps)
+constexpr int kBarRoutes = 1;                         // named barriers: routes published (all warps but 1)
 constexpr int kBarTail = 2;                           //   the compute warps
 constexpr int kBarGroup0 = 3;                         //   gate/up group g: kBarGroup0 + g
 constexpr int kBarRank = kBarGroup0 + kGroups;        //   the compute warps ranking the logits
@@ -220,10 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
     // ---------------------------------------------------------------- set-up
     // This CTA's split is formed before the routes barrier wherever the
     // number of valid routes is known there (routing here: all k are valid;
-    // given routes: warp 0 counts them), so the producers can stream as soon
+    // given routes: warp 0 counts them), so the producer can stream as soon
     // as the routes are out.
     pipe::Split sp{};
-    unsigned long long ctr_v = 0;
     if (warp == 0) {
         if constexpr (ROUTE)
             sp = pipe::cta_split<kPS>(k, I, d, c, G, RPS);
@@ -257,14 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             }
         }
     } else if (warp == 1) {
-        // the call count, read before this CTA adds its one; the load is in
-        // flight through the routes barrier and its value used after it
-        if constexpr (ROUTE)
-            sp = pipe::cta_split<kPS>(k, I, d, c, G, RPS);
+        // this launch's tag, from the count read before this CTA adds its
+        // one; the gate/up warps read it after the scale barrier (it is not
+        // needed before, so this warp stays off the routes barrier)
         if (lane == 0) {
-            ctr_v = ld_relaxed_u64(a.ctr);
+            const unsigned long long v = ld_relaxed_u64(a.ctr);
+            *s_tag = static_cast<uint32_t>(v / static_cast<unsigned>(G)) + 1u;
             red_relaxed_add(a.ctr);
         }
+        __syncwarp();
+        tc::named_arrive(kBarScales, kCW * 32 + 32);
+        return;
     } else if constexpr (ROUTE) {
         // top-k of the router logits by rank: thread e (of the 24 compute
         // warps) holds expert e's order-preserving key; its slot is the
@@ -295,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             }
         }
     }
-    tc::named_bar(kBarRoutes, kThreads);
+    tc::named_bar(kBarRoutes, kThreads - 32);
 
     const int nv = *s_nv;
     if constexpr (!ROUTE) {
@@ -321,14 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
                 uint8_t *st = ring + sl * S1;
                 const uint32_t bar = full + 8 * sl;
                 if (t < S) {
-                    // gate/up stage t: runs of neurons of one route, the gate rows
-                    // (warp 1 issues the up rows); the stage's bytes are both
+                    // gate/up stage t: runs of neurons of one route, gate rows then up rows
                     const int q0 = q_lo + t * kPS, q1 = q_lo + min(t * kPS + kPS, P);
                     tc::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(q1 - q0) * (2 * d));
                     for (int q = q0; q < q1;) {
                         const int r = q / I, n = q - r * I, len = min(q1 - q, I - n), i = q - q0;
                         const int64_t grow = static_cast<int64_t>(r_e[r]) * 2 * I + n;
                         tc::bulk_load(tc::smem_u32(st + i * rowb), a.q13 + grow * rowb, len * rowb, bar);
+                        tc::bulk_load(tc::smem_u32(st + (kPS + i) * rowb), a.q13 + (grow + I) * rowb, len * rowb,
+                                      bar);
                         q += len;
                     }
                 } else {
@@ -345,38 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const Args a)
             volatile int never = 0;
             for (int u = max(0, t - NS); u < t; ++u)
                 tc::mbar_wait(full + 8 * (u % NS), (u / NS) & 1u, &never, kWaitNs);
-        }
-        return;
-    }
-    if (warp == 1) {
-        // ------------------------------------------------ tag, up rows
-        // this launch's tag (the gate/up warps read it after the scale
-        // barrier), then the up rows of every gate/up stage, each into the
-        // slot that warp 0 fills with the stage's gate rows, after the same
-        // wait for the slot
-        if (lane == 0)
-            *s_tag = static_cast<uint32_t>(ctr_v / static_cast<unsigned>(G)) + 1u;
-        __syncwarp();
-        tc::named_arrive(kBarScales, kCW * 32 + 32);
-        if (lane == 0) {
-            const int64_t rowb = d;
-            tc::fence_proxy_async_smem();          // the ring held the routing's keys
-            for (int t = 0; t < S; ++t) {
-                const int sl = t % NS;
-                const uint32_t ph = (t / NS) & 1u;
-                if (!tc::mbar_wait(empty + 8 * sl, ph ^ 1u, s_abort, kWaitNs))
-                    break;
-                uint8_t *st = ring + sl * S1;
-                const uint32_t bar = full + 8 * sl;
-                const int q0 = q_lo + t * kPS, q1 = q_lo + min(t * kPS + kPS, P);
-                for (int q = q0; q < q1;) {
-                    const int r = q / I, n = q - r * I, len = min(q1 - q, I - n), i = q - q0;
-                    const int64_t grow = static_cast<int64_t>(r_e[r]) * 2 * I + n;
-                    tc::bulk_load(tc::smem_u32(st + (kPS + i) * rowb), a.q13 + (grow + I) * rowb, len * rowb,
-                                  bar);
-                    q += len;
-                }
-            }
         }
         return;
     }
