@@ -89,13 +89,14 @@ def expert_bytes(wl, path: str = "decode") -> int:
     bytes.  AWQ-4bit: 3*I*d/2 packed values + an fp16 scale and a 4-bit zero
     per 128 values.  NVFP4S: 3*I*d/4 bytes of kept codes, plus 3*I*d/16
     pattern and 3*I*d/32 scale bytes (decode path) or the grouped path's
-    16-byte side record per 128 weights (3*I*d/8), plus the expert's fp32
-    constant (decode) or two per-expert factors (grouped)."""
+    16-byte side record per 128 weights (3*I*d/8), plus the expert's two
+    fp32 values: its constants of W13 and W2 (decode) or the two per-expert
+    factors (grouped)."""
     n = 3 * wl.I * wl.d
     if wl.fmt == "awq4":
         return n // 2 + n // 128 * 2 + n // 128 // 2
     if wl.fmt == "nvfp4s":
-        return n // 4 + (n // 8 + 8 if path == "grouped" else n // 16 + n // 32 + 4)
+        return n // 4 + (n // 8 if path == "grouped" else n // 16 + n // 32) + 8
     return n * 33 // 32
 
 
